@@ -1,0 +1,540 @@
+#!/usr/bin/env python3
+"""Benchmark of the sparse-routed gated delta-rule memory scan on GB300.
+
+Default workload: the SDM 1.4B-layer shape (d=1920, H=2 -> N=57600 slots per
+head, d_v=960, per-half top-k=16, W=R=16, B=8, T=4096, bf16 values, fp32
+table).  One step = write addressing + read addressing + the scan over the
+whole batch, continuing the table from the previous step (the scan is a
+recurrence; a step is the next B*T tokens of the same sequences, so every
+step does identical work).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload sdm_14b_layer|sdm_sweep_H2|H4|H8|gdn|kda|sse|sdm_tiny]
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs its own batch
+(independent sequences, no collective in the data path) and the time is the
+max over ranks.  `--impl reference` times the fp64 CPU oracle on this host's
+cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "SDM scan tokens/s (d=1920,H=2,N=57600,W=R=16); achieved HBM GB/s vs peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM traffic of one sparse_scan launch from an ncu capture, valid only while
+# the kernel source hashes to the recorded digest (see profiles/).
+NCU_TRAFFIC = {}
+
+
+def _src_digest(name: str) -> str:
+    p = os.path.join(ROOT, "delta_rule_memory_gb300", "csrc", name)
+    return hashlib.sha1(open(p, "rb").read()).hexdigest()[:12]
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def mark(self, begin: bool):
+        if begin:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if self.t0 is not None and self.t0 - 1 <= r[0] <= (self.t1 or r[0]) + 1]
+        use = inside or rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i, v in enumerate(r[3]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(use)}
+
+
+# ------------------------------------------------------- CPU oracle (spawn)
+def _oracle_sdm_seq(args):
+    """One (b, h) sequence through the oracle: both addressings and the scan."""
+    import numpy as np
+    import oracle
+    s1w, s2w, s1r, s2r, v, alpha, beta, k, W, R, mode = args
+    t0 = time.perf_counter()
+    iw, ww = oracle.address(s1w, s2w, k, W)
+    ir, wr = oracle.address(s1r, s2r, k, R)
+    n = s1w.shape[-1] ** 2
+    M0 = np.zeros((1, 1, n, v.shape[-1]))
+    oracle.sdm_scan(M0, v, alpha, beta, iw, ww, ir, wr, mode)
+    return time.perf_counter() - t0
+
+
+def _oracle_gdn_seq(args):
+    import numpy as np
+    import oracle
+    q, k, v, a, beta, per_channel = args
+    t0 = time.perf_counter()
+    oracle.gdn_scan(np.zeros((1, 1, q.shape[-1], v.shape[-1])), q, k, v, a, beta, per_channel)
+    return time.perf_counter() - t0
+
+
+def _oracle_sse_seq(args):
+    import numpy as np
+    import oracle
+    route, topk, klog, q, v, alpha = args
+    t0 = time.perf_counter()
+    N, c, d = route.shape[-1], klog.shape[-1], v.shape[-1]
+    oracle.sse_scan(np.zeros((1, 1, N + 1, c, d)), route, topk, klog, q, v, alpha)
+    return time.perf_counter() - t0
+
+
+class OracleSampler:
+    """Runs the oracle over whole (b, h) sequences (first t_sample tokens) in a
+    spawn process pool created before any GPU work."""
+
+    def __init__(self, cores: int):
+        self.cores = max(1, cores)
+        self.pool = mp.get_context("spawn").Pool(self.cores)
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+    def run(self, wl: "Workload", inp: dict, t_sample: int, nseq: int):
+        jobs = wl.oracle_jobs(inp, t_sample, nseq)
+        fn = {"sdm": _oracle_sdm_seq, "gdn": _oracle_gdn_seq, "kda": _oracle_gdn_seq, "sse": _oracle_sse_seq}[wl.kind]
+        t0 = time.perf_counter()
+        self.pool.map(fn, jobs, chunksize=1)
+        wall = time.perf_counter() - t0
+        return len(jobs) * t_sample, wall
+
+
+# ---------------------------------------------------------------- workloads
+class Workload:
+    def __init__(self, name: str, mode: str):
+        import synth
+        self.name = name
+        self.mode = {"shared": 0, "perslot": 1}[mode]
+        if name == "sdm_14b_layer":
+            self.kind, self.shape = "sdm", synth.SDM_14B_LAYER
+        elif name.startswith("sdm_sweep_H"):
+            self.kind, self.shape = "sdm", synth.sdm_sweep_shape(int(name[len("sdm_sweep_H"):]))
+        elif name == "sdm_tiny":
+            self.kind, self.shape = "sdm", synth.SDM_TINY
+        elif name in ("gdn", "kda"):
+            self.kind, self.shape = name, synth.GDN_DENSE
+        elif name == "sse":
+            self.kind, self.shape = "sse", synth.SSE_PART
+        else:
+            raise SystemExit(f"unknown workload {name}")
+        sh = self.shape
+        self.tokens = sh.B * sh.T
+
+    def inputs(self, seed: int) -> dict:
+        import synth
+        if self.kind == "sdm":
+            return synth.sdm_inputs(self.shape, seed)
+        if self.kind in ("gdn", "kda"):
+            return synth.gdn_inputs(self.shape, seed)
+        return synth.sse_inputs(self.shape, seed)
+
+    def config(self) -> dict:
+        sh = self.shape
+        if self.kind == "sdm":
+            state_gb = sh.B * sh.H * sh.N * sh.d_v * 4 / 1e9
+            return {"workload": sh.name, "B": sh.B, "T": sh.T, "H": sh.H, "N": sh.N, "sqrtN": sh.sqrtN, "d_v": sh.d_v,
+                    "k": sh.k, "W": sh.W, "R": sh.R, "v_dtype": "bf16" if sh.v_bf16 else "fp32",
+                    "resid": ["shared", "per_slot"][self.mode], "state": f"fp32 {state_gb:.2f} GB, continued across steps",
+                    "l2": f"inputs larger than L2 (table {state_gb:.2f} GB); no flush"}
+        if self.kind in ("gdn", "kda"):
+            return {"workload": "kda_dense" if self.kind == "kda" else "gdn_dense", "B": sh.B, "T": sh.T, "H": sh.H,
+                    "dk": sh.dk, "dv": sh.dv, "qkv_dtype": "bf16", "state": "fp32, continued across steps",
+                    "l2": "inputs (q,k,v,alpha,y ~340-470 MB) larger than L2; no flush"}
+        return {"workload": sh.name, "B": sh.B, "T": sh.T, "H": sh.H, "N": sh.N, "topk": sh.topk, "c": sh.c, "d": sh.d,
+                "qv_dtype": "bf16", "state": "fp32 shared-memory resident per CTA, continued across steps",
+                "l2": "inputs (~1.1 GB) larger than L2; no flush"}
+
+    def oracle_jobs(self, inp: dict, t_sample: int, nseq: int):
+        sh = self.shape
+        pairs = [(b, h) for b in range(sh.B) for h in range(sh.H)][:nseq]
+        jobs = []
+        for b, h in pairs:
+            sl = (slice(b, b + 1), slice(0, t_sample), slice(h, h + 1))
+            if self.kind == "sdm":
+                jobs.append((inp["s1w"][sl].copy(), inp["s2w"][sl].copy(), inp["s1r"][sl].copy(),
+                             inp["s2r"][sl].copy(), inp["v"][sl].copy(), inp["alpha"][sl].copy(),
+                             inp["beta"][sl].copy(), sh.k, sh.W, sh.R, self.mode))
+            elif self.kind in ("gdn", "kda"):
+                a = inp["alpha_kda" if self.kind == "kda" else "alpha_gdn"]
+                jobs.append((inp["q"][sl].copy(), inp["k"][sl].copy(), inp["v"][sl].copy(), a[sl].copy(),
+                             inp["beta"][sl].copy(), self.kind == "kda"))
+            else:
+                jobs.append((inp["route"][sl].copy(), sh.topk, inp["klog"][sl].copy(), inp["q"][sl].copy(),
+                             inp["v"][sl].copy(), inp["alpha"][sl].copy()))
+        return jobs
+
+
+# ------------------------------------------------------------ GPU runners
+def _t(x, bf16=False):
+    import numpy as np
+    import torch
+    x = np.ascontiguousarray(x)
+    if bf16 or x.dtype == np.uint16:
+        return torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16)
+    return torch.from_numpy(x.copy())
+
+
+class GpuRun:
+    """Device buffers plus one step of the workload through the binding."""
+
+    def __init__(self, wl: Workload, inp: dict, device):
+        import torch
+        import delta_rule_memory_gb300 as sdm
+        self.sdm, self.wl, self.dev = sdm, wl, device
+        sh = wl.shape
+        self.host = {}
+        self.d = {}
+        if wl.kind == "sdm":
+            names = ("s1w", "s2w", "s1r", "s2r", "v", "alpha", "beta")
+        elif wl.kind in ("gdn", "kda"):
+            names = ("q", "k", "v", "alpha_kda" if wl.kind == "kda" else "alpha_gdn", "beta")
+        else:
+            names = ("route", "klog", "q", "v", "alpha")
+        for n in names:
+            h = _t(inp[n]).pin_memory()
+            self.host[n] = h
+            self.d[n] = h.to(device)
+        if wl.kind == "sdm":
+            B, T, H = sh.B, sh.T, sh.H
+            self.state = torch.zeros((B, H, sh.N, sh.d_v), dtype=torch.float32, device=device)
+            self.iw = torch.empty((B, T, H, sh.W), dtype=torch.int32, device=device)
+            self.ww = torch.empty((B, T, H, sh.W), dtype=torch.float32, device=device)
+            self.ir = torch.empty((B, T, H, sh.R), dtype=torch.int32, device=device)
+            self.wr = torch.empty((B, T, H, sh.R), dtype=torch.float32, device=device)
+            self.y = torch.empty((B, T, H, sh.d_v), dtype=torch.float32, device=device)
+            self.ws = torch.empty(sdm.sdm_scan_workspace_size(B, T, H, sh.W, sh.R), dtype=torch.uint8, device=device)
+            self.launches_per_step = 4
+        elif wl.kind in ("gdn", "kda"):
+            self.state = torch.zeros((sh.B, sh.H, sh.dk, sh.dv), dtype=torch.float32, device=device)
+            self.y = torch.empty((sh.B, sh.T, sh.H, sh.dv), dtype=torch.float32, device=device)
+            self.launches_per_step = 1
+        else:
+            self.state = torch.zeros((sh.B, sh.H, sh.N + 1, sh.c, sh.d), dtype=torch.float32, device=device)
+            self.y = torch.empty((sh.B, sh.T, sh.H, sh.d), dtype=torch.float32, device=device)
+            self.ws = torch.empty(sdm.sse_scan_workspace_size(sh.B, sh.T, sh.H, sh.N, sh.topk), dtype=torch.uint8,
+                                  device=device)
+            self.launches_per_step = 2
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        self.y_host = torch.empty(self.y.shape, dtype=torch.float32).pin_memory()
+
+    def pre(self):
+        """Work before the dominant kernel (addressing)."""
+        sh, d = self.wl.shape, self.d
+        if self.wl.kind == "sdm":
+            self.sdm.sdm_address(d["s1w"], d["s2w"], sh.k, sh.W, self.iw, self.ww, self.err)
+            self.sdm.sdm_address(d["s1r"], d["s2r"], sh.k, sh.R, self.ir, self.wr, self.err)
+
+    def main(self):
+        """The dominant kernel's call."""
+        sh, d = self.wl.shape, self.d
+        if self.wl.kind == "sdm":
+            self.sdm.sdm_scan(self.state, d["v"], d["alpha"], d["beta"], self.iw, self.ww, self.ir, self.wr,
+                              self.wl.mode, self.y, self.ws, self.err)
+        elif self.wl.kind in ("gdn", "kda"):
+            a = d["alpha_kda" if self.wl.kind == "kda" else "alpha_gdn"]
+            self.sdm.gdn_scan(self.state, d["q"], d["k"], d["v"], a, d["beta"], self.wl.kind == "kda", self.y)
+        else:
+            self.sdm.sse_scan(self.state, d["route"], sh.topk, d["klog"], d["q"], d["v"], d["alpha"], self.y,
+                              None, self.ws, self.err)
+
+    def step(self):
+        self.pre()
+        self.main()
+
+    def h2d(self):
+        for n, h in self.host.items():
+            self.d[n].copy_(h, non_blocking=True)
+
+    def d2h(self):
+        self.y_host.copy_(self.y, non_blocking=True)
+
+    def io_bytes(self):
+        return sum(h.numel() * h.element_size() for h in self.host.values()), self.y.numel() * 4
+
+    def algorithmic(self):
+        """(bytes or flops, unit, bound) of one launch of the dominant call."""
+        import torch
+        sh = self.wl.shape
+        if self.wl.kind == "sdm":
+            W, R = sh.W, sh.R
+            both = torch.cat([self.iw, self.ir], dim=-1).reshape(-1, W + R)
+            srt, _ = torch.sort(both, dim=-1)
+            union = (srt[:, 1:] != srt[:, :-1]).sum(dim=-1) + 1
+            rows = float((union + W).sum().item())       # rows loaded once + written rows stored once
+            tokh = sh.B * sh.T * sh.H
+            vbytes = 2 if sh.v_bf16 else 4
+            per_tok = sh.d_v * vbytes + sh.d_v * 4 + 8 + (W + R) * 8
+            return rows * sh.d_v * 4 + tokh * per_tok, "GB/s", "hbm", {
+                "mean_union_rows": float(union.float().mean().item()),
+                "bytes_per_token_head": (rows * sh.d_v * 4 + tokh * per_tok) / tokh}
+        if self.wl.kind in ("gdn", "kda"):
+            tokh = sh.B * sh.T * sh.H
+            per = 2 * (sh.dk + sh.dk + sh.dv) + 4 * (sh.dk if self.wl.kind == "kda" else 1) + 4 + 4 * sh.dv
+            state = 2 * sh.B * sh.H * sh.dk * sh.dv * 4
+            return tokh * per + state, "GB/s", "hbm", {"bytes_per_token_head": per}
+        tokh = sh.B * sh.T * sh.H
+        flops = tokh * (sh.topk + 1) * sh.c * sh.d * 5.0     # decay mul, write fma, read fma (2+2+1)
+        return flops, "TFLOP/s", "alu", {"flops_per_token_head": flops / tokh}
+
+
+def run_ours(args, rank, world, local_rank, sampler):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    wl = Workload(args.workload, args.mode)
+    inp = wl.inputs(seed=rank)
+    cpu = None
+    if sampler is not None:
+        nseq = min(sampler.cores, wl.shape.B * wl.shape.H)
+        tok, wall = sampler.run(wl, inp, args.cpu_tokens or wl.shape.T, nseq)
+        cpu = {"value": tok / wall, "unit": "tokens/s", "cores": sampler.cores, "kind": "oracle",
+               "sample": f"{nseq} whole (b,h) sequences x first {args.cpu_tokens or wl.shape.T} tokens of the "
+                         f"same workload, fp64 oracle, one process per sequence ({wall:.1f} s wall)"}
+    run = GpuRun(wl, inp, device)
+    del inp
+    stream = torch.cuda.current_stream()
+
+    for _ in range(max(args.warmup, 3)):
+        run.step()
+    torch.cuda.synchronize()
+    if int(run.err.item()) != 0:
+        raise SystemExit(f"device error flag {int(run.err.item())} during warm-up")
+    algo, algo_unit, bound, algo_info = run.algorithmic()
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.mark(True)
+    start.record(stream)
+    for i in range(K):
+        run.pre()
+        ev[i][0].record(stream)
+        run.main()
+        ev[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark(False)
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = start.elapsed_time(end)
+    main_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    if world > 1:
+        t = torch.tensor([total_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / K
+
+    # end to end through the public API: pinned host inputs -> device -> the
+    # same step -> y back to pinned host memory, every step
+    KE = max(3, K // 2)
+    for _ in range(2):
+        run.h2d(); run.step(); run.d2h()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(KE):
+        run.h2d()
+        run.step()
+        run.d2h()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / KE
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d, d2h = run.io_bytes()
+
+    pk, src = peaks()
+    if bound == "hbm":
+        peak = float(pk["hbm_gbs"])
+        achieved = algo / (main_ms * 1e-3) / 1e9
+    else:
+        # FP32 FMA pipe: 152 SMs x 128 lanes x 2 flop x max SM clock
+        peak = 152 * 128 * 2 * float(pk.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
+        achieved = algo / (main_ms * 1e-3) / 1e12
+    kernel_file = {"sdm": "sparse_scan.cu", "gdn": "gdn_scan.cu", "kda": "gdn_scan.cu", "sse": "sse_scan.cu"}[wl.kind]
+    tr = NCU_TRAFFIC.get((wl.name, wl.kind))
+    traffic = tr["bytes"] if tr and tr["digest"] == _src_digest(kernel_file) else None
+    tokens = wl.tokens * world
+    out = {
+        "metric": METRIC if wl.kind == "sdm" else f"{wl.kind} scan tokens/s",
+        "value": tokens / (ms_per_step * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": max(args.warmup, 3),
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded generators; no dataset or weights)",
+        "config": wl.config(),
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": algo_unit,
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": {"sdm": "sdm_scan (hazard prepass + sparse_scan_kernel)", "gdn": "gdn_scan",
+                                "kda": "gdn_scan", "sse": "sse_scan (route prepass + sse_scan_kernel)"}[wl.kind],
+                     "launch_ms": main_ms, "peak_source": f"{src} ({'hbm_gbs' if bound == 'hbm' else 'FP32 lanes x clock'})",
+                     **algo_info},
+        "cpu_baseline": cpu,
+        "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": K * run.launches_per_step,
+        "clocks": clk,
+    }
+    if wl.kind == "sdm":
+        out["step_breakdown_ms"] = {"addressing_x2": ms_per_step - main_ms, "scan": main_ms}
+    return out
+
+
+def run_reference(args, rank, world):
+    """The fp64 CPU oracle on this host's cores, on a bounded sample."""
+    wl = Workload(args.workload, args.mode)
+    inp = wl.inputs(seed=0)
+    cores = args.cpu_cores or min(os.cpu_count() or 1, 16)
+    nseq = min(cores, wl.shape.B * wl.shape.H)
+    t_sample = args.cpu_tokens or min(wl.shape.T, 1024 if wl.kind == "sdm" else 256)
+    sampler = OracleSampler(nseq)
+    for _ in range(max(args.warmup, 0)):
+        sampler.run(wl, inp, t_sample, nseq)
+    walls = []
+    tok = 0
+    for _ in range(args.steps):
+        tok, wall = sampler.run(wl, inp, t_sample, nseq)
+        walls.append(wall)
+    sampler.close()
+    ms = 1e3 * statistics.mean(walls)
+    value = tok / (ms * 1e-3)
+    sample = (f"{nseq} whole (b,h) sequences x first {t_sample} tokens per step, fp64 oracle, one process per "
+              f"sequence")
+    return {"impl": "reference", "metric": METRIC if wl.kind == "sdm" else f"{wl.kind} scan tokens/s",
+            "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded generators; no dataset or weights)", "config": wl.config(),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": nseq, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=60)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="sdm_14b_layer")
+    ap.add_argument("--mode", choices=["shared", "perslot"], default="shared")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-tokens", type=int, default=0, help="tokens per sampled sequence for the oracle")
+    ap.add_argument("--cpu-cores", type=int, default=0)
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+
+    # the oracle's process pool starts before any GPU work
+    sampler = None
+    if rank == 0 and not args.no_cpu_baseline:
+        sampler = OracleSampler(args.cpu_cores or min(os.cpu_count() or 1, 16))
+    import torch
+    import torch.distributed as dist
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo", device_id=torch.device("cuda", local_rank)
+                                if torch.cuda.is_available() else None)
+    try:
+        out = run_ours(args, rank, world, local_rank, sampler)
+    finally:
+        if sampler is not None:
+            sampler.close()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

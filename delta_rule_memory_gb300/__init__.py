@@ -1,0 +1,245 @@
+"""Python binding of libsdm.so, the GB300 (sm_103a) sparse-routed gated
+delta-rule memory scan.
+
+Argument marshalling only: every function here checks shapes and dtypes of
+CUDA tensors, passes their device pointers and the current CUDA stream to the
+C ABI declared in ``include/sdm.h`` (same function names), and raises
+``SdmError`` with the library's message on a non-zero status.  All compute
+runs in the library's kernels.  There is no CPU fallback: importing works
+without a GPU, but every call needs the built library and a CUDA device.
+
+Build the library with ``python -m delta_rule_memory_gb300.build``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "SdmError", "lib", "library_path", "sdm_version", "sdm_address", "sdm_scan", "sdm_scan_workspace_size",
+    "gdn_scan", "gdn_scan_workspace_size", "sse_scan", "sse_scan_workspace_size", "SDM_RESID_SHARED", "SDM_RESID_PERSLOT",
+    "SDM_RESID_ADDITIVE", "SDM_DEVERR_INDEX_RANGE", "SDM_DEVERR_INDEX_REPEAT", "SDM_DEVERR_NONFINITE",
+]
+
+SDM_OK, SDM_ERR_INVALID_ARG, SDM_ERR_SHAPE, SDM_ERR_ALIGN, SDM_ERR_UNSUPPORTED, SDM_ERR_CUDA = range(6)
+SDM_DEVERR_INDEX_RANGE, SDM_DEVERR_INDEX_REPEAT, SDM_DEVERR_NONFINITE = 1, 2, 4
+SDM_DTYPE_F32, SDM_DTYPE_BF16 = 0, 1
+SDM_RESID_SHARED, SDM_RESID_PERSLOT, SDM_RESID_ADDITIVE = 0, 1, 2
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_HERE, "libsdm.so")
+_lock = threading.Lock()
+_lib = None
+
+_P, _I, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+_SIGNATURES = {
+    "sdm_version": (_I, []),
+    "sdm_last_error": (ctypes.c_char_p, []),
+    "sdm_address": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
+    "sdm_scan_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "sdm_scan": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P, _P]),
+    "gdn_scan_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "gdn_scan": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "sse_scan_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "sse_scan": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _SZ, _P, _P]),
+}
+
+
+class SdmError(RuntimeError):
+    """A libsdm call returned a non-zero status."""
+
+    def __init__(self, fn: str, code: int, msg: str):
+        super().__init__(f"{fn} failed with status {code}: {msg}")
+        self.code = code
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libsdm.so.  Raises if it was not built: there is no fallback."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(library_path):
+                raise RuntimeError(f"libsdm.so is not built ({library_path}); run "
+                                   "`python -m delta_rule_memory_gb300.build`")
+            h = ctypes.CDLL(library_path)
+            for name, (res, args) in _SIGNATURES.items():
+                fn = getattr(h, name, None)
+                if fn is None:
+                    continue
+                fn.restype = res
+                fn.argtypes = args
+            _lib = h
+    return _lib
+
+
+def _check(fn: str, rc: int):
+    if rc != SDM_OK:
+        raise SdmError(fn, rc, lib().sdm_last_error().decode(errors="replace"))
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _req(t: torch.Tensor, name: str, dtype, shape=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def sdm_version() -> int:
+    return lib().sdm_version()
+
+
+def sdm_address(s1: torch.Tensor, s2: torch.Tensor, k: int, W: int, idx_out=None, w_out=None, dev_err=None,
+                stream=None):
+    """Product-key addressing of fp32 score halves [B,T,H,sqrtN].
+    Returns (idx int32 [B,T,H,W] in rank order, w fp32 [B,T,H,W])."""
+    _req(s1, "s1", torch.float32)
+    if s1.dim() != 4:
+        raise ValueError("s1 must be [B,T,H,sqrtN]")
+    _req(s2, "s2", torch.float32, s1.shape)
+    B, T, H, sq = s1.shape
+    if idx_out is None:
+        idx_out = torch.empty((B, T, H, W), dtype=torch.int32, device=s1.device)
+    if w_out is None:
+        w_out = torch.empty((B, T, H, W), dtype=torch.float32, device=s1.device)
+    _req(idx_out, "idx_out", torch.int32, (B, T, H, W))
+    _req(w_out, "w_out", torch.float32, (B, T, H, W))
+    if dev_err is not None:
+        _req(dev_err, "dev_err", torch.int32)
+    rc = lib().sdm_address(s1.data_ptr(), s2.data_ptr(), B, T, H, sq, int(k), int(W), idx_out.data_ptr(),
+                           w_out.data_ptr(), _ptr(dev_err), _stream(stream))
+    _check("sdm_address", rc)
+    return idx_out, w_out
+
+
+def sdm_scan_workspace_size(B: int, T: int, H: int, W: int, R: int) -> int:
+    return int(lib().sdm_scan_workspace_size(B, T, H, W, R))
+
+
+def sdm_scan(state, v, alpha, beta, idx_w, w_w, idx_r, w_r, resid_mode=SDM_RESID_SHARED, y=None, workspace=None,
+             dev_err=None, stream=None):
+    """Sparse delta-rule scan; updates `state` [B,H,N,d_v] in place and
+    returns y fp32 [B,T,H,d_v].  v is fp32 or bf16 [B,T,H,d_v]."""
+    _req(state, "state", torch.float32)
+    if state.dim() != 4:
+        raise ValueError("state must be [B,H,N,d_v]")
+    B, H, N, dv = state.shape
+    if v.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("v must be float32 or bfloat16")
+    _req(v, "v", v.dtype)
+    if v.dim() != 4 or v.shape[0] != B or v.shape[2] != H or v.shape[3] != dv:
+        raise ValueError(f"v must be [B,T,H,d_v] = [{B},T,{H},{dv}]")
+    T = v.shape[1]
+    _req(alpha, "alpha", torch.float32, (B, T, H))
+    _req(beta, "beta", torch.float32, (B, T, H))
+    _req(idx_w, "idx_w", torch.int32)
+    W = idx_w.shape[-1]
+    _req(idx_w, "idx_w", torch.int32, (B, T, H, W))
+    _req(w_w, "w_w", torch.float32, (B, T, H, W))
+    _req(idx_r, "idx_r", torch.int32)
+    R = idx_r.shape[-1]
+    _req(idx_r, "idx_r", torch.int32, (B, T, H, R))
+    _req(w_r, "w_r", torch.float32, (B, T, H, R))
+    if y is None:
+        y = torch.empty((B, T, H, dv), dtype=torch.float32, device=state.device)
+    _req(y, "y", torch.float32, (B, T, H, dv))
+    need = sdm_scan_workspace_size(B, T, H, W, R)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=state.device)
+    _req(workspace, "workspace", torch.uint8)
+    if dev_err is not None:
+        _req(dev_err, "dev_err", torch.int32)
+    vdt = SDM_DTYPE_BF16 if v.dtype == torch.bfloat16 else SDM_DTYPE_F32
+    rc = lib().sdm_scan(state.data_ptr(), v.data_ptr(), vdt, alpha.data_ptr(), beta.data_ptr(), idx_w.data_ptr(),
+                        w_w.data_ptr(), W, idx_r.data_ptr(), w_r.data_ptr(), R, B, T, H, N, dv, int(resid_mode),
+                        y.data_ptr(), workspace.data_ptr(), workspace.numel(), _ptr(dev_err), _stream(stream))
+    _check("sdm_scan", rc)
+    return y
+
+
+def gdn_scan_workspace_size(B: int, T: int, H: int, dk: int, dv: int, per_channel: bool) -> int:
+    return int(lib().gdn_scan_workspace_size(B, T, H, dk, dv, int(bool(per_channel))))
+
+
+def gdn_scan(state, q, k, v, alpha, beta, per_channel: bool, y=None, workspace=None, stream=None):
+    """Dense GDN / KDA scan; updates `state` [B,H,dk,dv] in place and returns
+    y fp32 [B,T,H,dv].  q, k bf16 [B,T,H,dk]; v bf16 [B,T,H,dv]; alpha fp32
+    [B,T,H] (GDN) or [B,T,H,dk] (KDA); beta fp32 [B,T,H]."""
+    _req(state, "state", torch.float32)
+    if state.dim() != 4:
+        raise ValueError("state must be [B,H,dk,dv]")
+    B, H, dk, dv = state.shape
+    _req(q, "q", torch.bfloat16)
+    T = q.shape[1]
+    _req(q, "q", torch.bfloat16, (B, T, H, dk))
+    _req(k, "k", torch.bfloat16, (B, T, H, dk))
+    _req(v, "v", torch.bfloat16, (B, T, H, dv))
+    _req(alpha, "alpha", torch.float32, (B, T, H, dk) if per_channel else (B, T, H))
+    _req(beta, "beta", torch.float32, (B, T, H))
+    if y is None:
+        y = torch.empty((B, T, H, dv), dtype=torch.float32, device=state.device)
+    _req(y, "y", torch.float32, (B, T, H, dv))
+    need = gdn_scan_workspace_size(B, T, H, dk, dv, per_channel)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=state.device)
+    if workspace is not None:
+        _req(workspace, "workspace", torch.uint8)
+    rc = lib().gdn_scan(state.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), alpha.data_ptr(),
+                        int(bool(per_channel)), beta.data_ptr(), B, T, H, dk, dv, y.data_ptr(), _ptr(workspace),
+                        0 if workspace is None else workspace.numel(), _stream(stream))
+    _check("gdn_scan", rc)
+    return y
+
+
+def sse_scan_workspace_size(B: int, T: int, H: int, N: int, topk: int) -> int:
+    return int(lib().sse_scan_workspace_size(B, T, H, N, topk))
+
+
+def sse_scan(state, route_logits, topk: int, k_logits, q, v, alpha, y=None, sel_out=None, workspace=None,
+             dev_err=None, stream=None):
+    """Sparse State Expansion scan; updates `state` [B,H,N+1,c,d] in place and
+    returns y fp32 [B,T,H,d] (and fills sel_out int32 [B,T,H,topk] if given)."""
+    _req(state, "state", torch.float32)
+    if state.dim() != 5:
+        raise ValueError("state must be [B,H,N+1,c,d]")
+    B, H, Np1, c, d = state.shape
+    N = Np1 - 1
+    _req(route_logits, "route_logits", torch.float32)
+    T = route_logits.shape[1]
+    _req(route_logits, "route_logits", torch.float32, (B, T, H, N))
+    _req(k_logits, "k_logits", torch.float32, (B, T, H, c))
+    _req(q, "q", torch.bfloat16, (B, T, H, c))
+    _req(v, "v", torch.bfloat16, (B, T, H, d))
+    _req(alpha, "alpha", torch.float32, (B, T, H, c))
+    if y is None:
+        y = torch.empty((B, T, H, d), dtype=torch.float32, device=state.device)
+    _req(y, "y", torch.float32, (B, T, H, d))
+    if sel_out is not None:
+        _req(sel_out, "sel_out", torch.int32, (B, T, H, topk))
+    if dev_err is not None:
+        _req(dev_err, "dev_err", torch.int32)
+    if workspace is None:
+        workspace = torch.empty(max(sse_scan_workspace_size(B, T, H, N, topk), 1), dtype=torch.uint8,
+                                device=state.device)
+    _req(workspace, "workspace", torch.uint8)
+    rc = lib().sse_scan(state.data_ptr(), route_logits.data_ptr(), int(topk), k_logits.data_ptr(), q.data_ptr(),
+                        v.data_ptr(), alpha.data_ptr(), B, T, H, N, c, d, y.data_ptr(), _ptr(sel_out),
+                        workspace.data_ptr(), workspace.numel(), _ptr(dev_err), _stream(stream))
+    _check("sse_scan", rc)
+    return y

@@ -1,0 +1,184 @@
+// gdn_scan.cu - dense Gated DeltaNet / KDA scan (Linear Attention Architectures
+// deck, "GDN and KDA change the granularity of forgetting", Eqs. 15-20), token
+// by token in fp32.
+//
+// One CTA per (batch, head, 32-column tile of the value dimension); the
+// dk x 32 state tile stays in registers for the whole sequence (thread
+// (warp w, lane l) holds rows w, w+8, ... of column l).  Per token: decay the
+// rows, reduce the decayed prediction over rows (one barrier), write, and
+// reduce the read over rows (reduced by the next token's barrier).  Per-token
+// inputs are prefetched P tokens ahead with cp.async.
+#include "common.cuh"
+
+namespace sdm {
+namespace {
+
+constexpr int kGdnCols = 32;
+constexpr int kGdnWarps = 8;
+constexpr int kGdnP = 4;
+
+struct GdnArgs {
+  float *state;
+  const uint16_t *q, *k, *v;
+  const float *alpha, *beta;
+  float *y;
+  int T, H, dk, dv, per_channel, tiles;
+};
+
+// per-token slot (32-bit words): k[dk] bf16, q[dk] bf16, v[32] bf16,
+// alpha[dk or 1], beta, padded to a multiple of 4 words
+__host__ __device__ inline int gdn_slot_words(int dk) { return ((dk / 2) * 2 + 16 + dk + 1 + 3) & ~3; }
+
+template <int RPT>  // rows per thread = dk / 8
+__global__ void __launch_bounds__(kGdnWarps * 32) gdn_recurrent_kernel(const GdnArgs a) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int tile = blockIdx.x % a.tiles;
+  const long bh = blockIdx.x / a.tiles;
+  const int h = static_cast<int>(bh % a.H);
+  const long b = bh / a.H;
+  const int dk = a.dk, dv = a.dv, T = a.T, H = a.H;
+  const int col = tile * kGdnCols + lane;
+
+  float *redP = reinterpret_cast<float *>(smem_raw);          // [8][32]
+  float *redY = redP + kGdnWarps * kGdnCols;                  // [2][8][32]
+  uint32_t *ring = reinterpret_cast<uint32_t *>(redY + 2 * kGdnWarps * kGdnCols);
+  const int sw = gdn_slot_words(dk);
+  const int k_off = 0, q_off = dk / 2, v_off = dk, a_off = dk + 16, b_off = dk + 16 + dk;
+
+  float *gS = a.state + bh * static_cast<long>(dk) * dv;
+  float s[RPT];
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) s[i] = gS[static_cast<long>(warp + kGdnWarps * i) * dv + col];
+
+  const long tok0 = b * T * H + h;
+  const int n_k = dk / 8, n_q = dk / 8, n_v = kGdnCols / 8, n_a = a.per_channel ? dk / 4 : 0;
+  auto issue = [&](int t) {
+    const long tok = tok0 + static_cast<long>(t) * H;
+    uint32_t *sl = ring + (t % (kGdnP + 1)) * sw;
+    const int tid = threadIdx.x;
+    int q = tid;
+    if (q < n_k) { cp_async<16>(sl + k_off + 4 * q, a.k + tok * dk + 8 * q); return; }
+    q -= n_k;
+    if (q < n_q) { cp_async<16>(sl + q_off + 4 * q, a.q + tok * dk + 8 * q); return; }
+    q -= n_q;
+    if (q < n_v) { cp_async<16>(sl + v_off + 4 * q, a.v + tok * dv + tile * kGdnCols + 8 * q); return; }
+    q -= n_v;
+    if (q < n_a) { cp_async<16>(sl + a_off + 4 * q, a.alpha + tok * dk + 4 * q); return; }
+    q -= n_a;
+    if (!a.per_channel) {
+      if (q == 0) cp_async<4>(sl + a_off, a.alpha + tok);
+      else if (q == 1) cp_async<4>(sl + b_off, a.beta + tok);
+    } else if (q == 0) {
+      cp_async<4>(sl + b_off, a.beta + tok);
+    }
+  };
+  for (int t = 0; t < kGdnP; ++t) {
+    if (t < T) issue(t);
+    cp_async_commit();
+  }
+
+  for (int t = 0; t < T; ++t) {
+    cp_async_wait<kGdnP - 1>();
+    __syncthreads();
+    if (t + kGdnP < T) issue(t + kGdnP);
+    cp_async_commit();
+    if (t > 0 && warp == 0) {
+      const float *rd = redY + ((t - 1) & 1) * kGdnWarps * kGdnCols;
+      float acc = 0.f;
+#pragma unroll
+      for (int w = 0; w < kGdnWarps; ++w) acc += rd[w * kGdnCols + lane];
+      a.y[(tok0 + static_cast<long>(t - 1) * H) * dv + col] = acc;
+    }
+    const uint32_t *sl = ring + (t % (kGdnP + 1)) * sw;
+    const uint16_t *kk = reinterpret_cast<const uint16_t *>(sl + k_off);
+    const uint16_t *qq = reinterpret_cast<const uint16_t *>(sl + q_off);
+    const uint16_t *vv = reinterpret_cast<const uint16_t *>(sl + v_off);
+    const float *al = reinterpret_cast<const float *>(sl + a_off);
+    const float be = __uint_as_float(sl[b_off]);
+    // decay every row (D_alpha S), then the decayed prediction S~^T k
+    float pp = 0.f;
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+      const int j = warp + kGdnWarps * i;
+      const float aj = a.per_channel ? al[j] : al[0];
+      s[i] *= aj;
+      pp = fmaf(s[i], bf16_to_f32(kk[j]), pp);
+    }
+    redP[warp * kGdnCols + lane] = pp;
+    __syncthreads();
+    float pred = 0.f;
+#pragma unroll
+    for (int w = 0; w < kGdnWarps; ++w) pred += redP[w * kGdnCols + lane];
+    const float r = be * (bf16_to_f32(vv[lane]) - pred);
+    float yp = 0.f;
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) {
+      const int j = warp + kGdnWarps * i;
+      s[i] = fmaf(bf16_to_f32(kk[j]), r, s[i]);
+      yp = fmaf(s[i], bf16_to_f32(qq[j]), yp);
+    }
+    redY[(t & 1) * kGdnWarps * kGdnCols + warp * kGdnCols + lane] = yp;
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+  if (T > 0 && warp == 0) {
+    const float *rd = redY + ((T - 1) & 1) * kGdnWarps * kGdnCols;
+    float acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < kGdnWarps; ++w) acc += rd[w * kGdnCols + lane];
+    a.y[(tok0 + static_cast<long>(T - 1) * H) * dv + col] = acc;
+  }
+#pragma unroll
+  for (int i = 0; i < RPT; ++i) gS[static_cast<long>(warp + kGdnWarps * i) * dv + col] = s[i];
+}
+
+}  // namespace
+}  // namespace sdm
+
+using namespace sdm;
+
+extern "C" size_t gdn_scan_workspace_size(int B, int T, int H, int dk, int dv, int per_channel) {
+  (void)B; (void)T; (void)H; (void)dk; (void)dv; (void)per_channel;
+  return 0;
+}
+
+extern "C" int gdn_scan(float *state, const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
+                        int per_channel, const float *beta, int B, int T, int H, int dk, int dv, float *y,
+                        void *workspace, size_t workspace_bytes, void *stream) {
+  (void)workspace; (void)workspace_bytes;
+  if (!state || !q || !k || !v || !alpha || !beta || !y) return set_error(SDM_ERR_INVALID_ARG, "gdn_scan: null pointer");
+  if (B < 0 || T < 0 || H < 0) return set_error(SDM_ERR_INVALID_ARG, "gdn_scan: negative size");
+  if ((dk != 16 && dk != 32 && dk != 64 && dk != 128) || dv < 32 || dv % 32 != 0 || dv > 256)
+    return set_error(SDM_ERR_SHAPE, "gdn_scan: need dk in {16,32,64,128}, dv %% 32 == 0, dv <= 256");
+  if (per_channel != 0 && per_channel != 1) return set_error(SDM_ERR_UNSUPPORTED, "gdn_scan: per_channel must be 0/1");
+  if (!aligned(state, 16) || !aligned(y, 16) || !aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) ||
+      !aligned(alpha, per_channel ? 16 : 4) || !aligned(beta, 4))
+    return set_error(SDM_ERR_ALIGN, "gdn_scan: state, y, q, k, v (and KDA alpha) need 16-byte alignment");
+  if (B == 0 || T == 0 || H == 0) return SDM_OK;
+  GdnArgs args;
+  args.state = state;
+  args.q = q;
+  args.k = k;
+  args.v = v;
+  args.alpha = alpha;
+  args.beta = beta;
+  args.y = y;
+  args.T = T;
+  args.H = H;
+  args.dk = dk;
+  args.dv = dv;
+  args.per_channel = per_channel;
+  args.tiles = dv / kGdnCols;
+  const size_t smem = sizeof(float) * 3 * kGdnWarps * kGdnCols + sizeof(uint32_t) * (kGdnP + 1) * gdn_slot_words(dk);
+  const long blocks = static_cast<long>(B) * H * args.tiles;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  switch (dk) {
+    case 16: gdn_recurrent_kernel<2><<<static_cast<unsigned>(blocks), kGdnWarps * 32, smem, st>>>(args); break;
+    case 32: gdn_recurrent_kernel<4><<<static_cast<unsigned>(blocks), kGdnWarps * 32, smem, st>>>(args); break;
+    case 64: gdn_recurrent_kernel<8><<<static_cast<unsigned>(blocks), kGdnWarps * 32, smem, st>>>(args); break;
+    default: gdn_recurrent_kernel<16><<<static_cast<unsigned>(blocks), kGdnWarps * 32, smem, st>>>(args); break;
+  }
+  return check_launch("gdn_scan");
+}

@@ -1,0 +1,316 @@
+// sse_scan.cu - Sparse State Expansion scan (SSE deck, "One gate controls both
+// writes and reads", Eqs. 9-14; "SSE routes tokens into shared-parameter state
+// partitions"; "A memory decays only when its partition is visited").
+//
+// Two kernels:
+//   route  - one warp per token-head: top-k partitions by router logit (ties to
+//            the lower index), their softmax gates over all N partitions (not
+//            renormalised), and the max / inverse normaliser of the key-logit
+//            softmax over the c rows.  One small record per token.
+//   scan   - one CTA per (batch, head, 16-column tile).  All N+1 partitions of
+//            that column tile live in shared memory for the whole sequence; per
+//            token only the k routed partitions and the shared one are touched
+//            (decay, additive write, read).  Per-token inputs are prefetched
+//            P tokens ahead with cp.async; one CTA barrier per token.
+#include <climits>
+
+#include "common.cuh"
+
+namespace sdm {
+namespace {
+
+constexpr int kSseDT = 16;        // columns per CTA
+constexpr int kSseThreads = 256;  // 16 columns x 16 row groups
+constexpr int kSseRG = kSseThreads / kSseDT;
+constexpr int kSseP = 4;          // tokens prefetched ahead
+constexpr int kSseMaxTopk = 8;
+
+__host__ __device__ inline int rec_words(int topk) { return (2 * topk + 2 + 3) & ~3; }
+
+// ---------------------------------------------------------------------------
+// Routing prepass.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) sse_route_kernel(const float *__restrict__ route, const float *__restrict__ klog,
+                                                        long tokens, int N, int topk, int c, uint32_t *__restrict__ rec,
+                                                        int32_t *__restrict__ sel_out, int32_t *__restrict__ dev_err) {
+  const int lane = threadIdx.x & 31;
+  const long tok = static_cast<long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (tok >= tokens) return;  // warp-uniform
+  const float *lg = route + tok * N;
+  // two logits per lane: ids lane and lane + 32
+  uint32_t key[2];
+  int id[2];
+  float lv[2];
+  bool bad = false;
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int j = lane + 32 * e;
+    const bool in = j < N;
+    lv[e] = in ? lg[j] : -INFINITY;
+    bad |= in && !isfinite(lv[e]);
+    key[e] = in ? order_key(lv[e]) : 0u;
+    id[e] = in ? j : INT_MAX;
+  }
+  // softmax over all N logits
+  const float lmax = key_value(__reduce_max_sync(kFull, max(key[0], key[1])));
+  float z = 0.f;
+#pragma unroll
+  for (int e = 0; e < 2; ++e) z += (lane + 32 * e < N) ? expf(lv[e] - lmax) : 0.f;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(kFull, z, off);
+  // top-k: sort each lane's pair, then redux rounds
+  if (key[1] > key[0] || (key[1] == key[0] && id[1] < id[0])) {
+    const uint32_t tk = key[0]; key[0] = key[1]; key[1] = tk;
+    const int ti = id[0]; id[0] = id[1]; id[1] = ti;
+  }
+  uint32_t *r = rec + tok * rec_words(topk);
+  for (int s = 0; s < topk; ++s) {
+    const uint32_t m = __reduce_max_sync(kFull, key[0]);
+    const int wid = __reduce_min_sync(kFull, key[0] == m ? id[0] : INT_MAX);
+    if (key[0] == m && id[0] == wid) {
+      key[0] = key[1]; id[0] = id[1];
+      key[1] = 0u; id[1] = INT_MAX;
+    }
+    if (lane == 0) {
+      r[s] = static_cast<uint32_t>(wid);
+      r[topk + s] = __float_as_uint(expf(key_value(m) - lmax) / z);
+      if (sel_out) sel_out[tok * topk + s] = wid;
+    }
+  }
+  // key-logit softmax statistics over the c rows (c <= 128: four per lane)
+  const float *kl = klog + tok * c;
+  float kv[4];
+  uint32_t km = 0u;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int j = lane + 32 * e;
+    kv[e] = j < c ? kl[j] : -INFINITY;
+    bad |= j < c && !isfinite(kv[e]);
+    km = max(km, j < c ? order_key(kv[e]) : 0u);
+  }
+  const float kmax = key_value(__reduce_max_sync(kFull, km));
+  float kz = 0.f;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) kz += (lane + 32 * e < c) ? expf(kv[e] - kmax) : 0.f;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) kz += __shfl_xor_sync(kFull, kz, off);
+  if (lane == 0) {
+    r[2 * topk] = __float_as_uint(kmax);
+    r[2 * topk + 1] = __float_as_uint(1.0f / kz);
+  }
+  if (__any_sync(kFull, bad) && lane == 0 && dev_err) atomicOr(dev_err, SDM_DEVERR_NONFINITE);
+}
+
+// ---------------------------------------------------------------------------
+// The scan.
+// ---------------------------------------------------------------------------
+struct SseArgs {
+  float *state;
+  const float *klog, *alpha;
+  const uint16_t *q, *v;
+  const uint32_t *rec;
+  float *y;
+  int T, H, N, c, d, topk, tiles, rw;
+};
+
+// per-token input slot, in 16-byte chunks: klog[c], alpha[c], q[c] bf16,
+// v[16] bf16, routing record
+struct SseSlot {
+  static __host__ __device__ int klog_off() { return 0; }
+  static __host__ __device__ int alpha_off(int c) { return c; }        // in words
+  static __host__ __device__ int q_off(int c) { return 2 * c; }        // words
+  static __host__ __device__ int v_off(int c) { return 2 * c + c / 2; }
+  static __host__ __device__ int rec_off(int c) { return 2 * c + c / 2 + kSseDT / 2; }
+  static __host__ __device__ int words(int c, int rw) { return rec_off(c) + rw; }
+};
+
+__global__ void __launch_bounds__(kSseThreads) sse_scan_kernel(const SseArgs a) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int tid = threadIdx.x;
+  const int col = tid % kSseDT;
+  const int rg = tid / kSseDT;
+  const int tile = blockIdx.x % a.tiles;
+  const long bh = blockIdx.x / a.tiles;
+  const int h = static_cast<int>(bh % a.H);
+  const long b = bh / a.H;
+  const int c = a.c, d = a.d, N = a.N, T = a.T, H = a.H, topk = a.topk;
+  const int parts = N + 1;
+
+  float *S = reinterpret_cast<float *>(smem_raw);                  // [parts][c][16]
+  float *red = S + static_cast<size_t>(parts) * c * kSseDT;        // [2][16 row groups][16]
+  uint32_t *ring = reinterpret_cast<uint32_t *>(red + 2 * kSseRG * kSseDT);
+  const int slot_words = SseSlot::words(c, a.rw);                   // multiple of 4
+  const int col0 = tile * kSseDT;
+
+  // load this column tile of every partition
+  float *gS = a.state + bh * static_cast<long>(parts) * c * d;
+  for (int e = tid; e < parts * c * (kSseDT / 4); e += kSseThreads) {
+    const int row = e / (kSseDT / 4), q4 = e % (kSseDT / 4);
+    const float4 x = *reinterpret_cast<const float4 *>(gS + static_cast<long>(row) * d + col0 + 4 * q4);
+    *reinterpret_cast<float4 *>(S + row * kSseDT + 4 * q4) = x;
+  }
+
+  const long tok0 = b * T * H + h;
+  const int n_klog = c / 4, n_alpha = c / 4, n_q = c / 8, n_v = kSseDT / 8, n_rec = a.rw / 4;
+  const int n_chunks = n_klog + n_alpha + n_q + n_v + n_rec;
+  auto issue = [&](int t) {
+    if (tid >= n_chunks) return;
+    const long tok = tok0 + static_cast<long>(t) * H;
+    uint32_t *sl = ring + (t % (kSseP + 1)) * slot_words;
+    int q = tid;
+    if (q < n_klog) { cp_async<16>(sl + SseSlot::klog_off() + 4 * q, a.klog + tok * c + 4 * q); return; }
+    q -= n_klog;
+    if (q < n_alpha) { cp_async<16>(sl + SseSlot::alpha_off(c) + 4 * q, a.alpha + tok * c + 4 * q); return; }
+    q -= n_alpha;
+    if (q < n_q) { cp_async<16>(sl + SseSlot::q_off(c) + 4 * q, a.q + tok * c + 8 * q); return; }
+    q -= n_q;
+    if (q < n_v) { cp_async<16>(sl + SseSlot::v_off(c) + 4 * q, a.v + tok * d + col0 + 8 * q); return; }
+    q -= n_v;
+    cp_async<16>(sl + SseSlot::rec_off(c) + 4 * q, a.rec + tok * a.rw + 4 * q);
+  };
+  for (int t = 0; t < kSseP; ++t) {
+    if (t < T) issue(t);
+    cp_async_commit();
+  }
+
+  const int rpt = c / kSseRG;  // rows per thread: j = rg + 16 i
+  for (int t = 0; t < T; ++t) {
+    cp_async_wait<kSseP - 1>();
+    __syncthreads();
+    if (t + kSseP < T) issue(t + kSseP);
+    cp_async_commit();
+    if (t > 0 && rg == 0) {
+      const float *rd = red + ((t - 1) & 1) * kSseRG * kSseDT;
+      float acc = 0.f;
+#pragma unroll
+      for (int g = 0; g < kSseRG; ++g) acc += rd[g * kSseDT + col];
+      a.y[(tok0 + static_cast<long>(t - 1) * H) * d + col0 + col] = acc;
+    }
+    const uint32_t *sl = ring + (t % (kSseP + 1)) * slot_words;
+    const float *kl = reinterpret_cast<const float *>(sl + SseSlot::klog_off());
+    const float *al = reinterpret_cast<const float *>(sl + SseSlot::alpha_off(c));
+    const uint16_t *qq = reinterpret_cast<const uint16_t *>(sl + SseSlot::q_off(c));
+    const uint16_t *vv = reinterpret_cast<const uint16_t *>(sl + SseSlot::v_off(c));
+    const uint32_t *rc = sl + SseSlot::rec_off(c);
+    const float kmax = __uint_as_float(rc[2 * topk]);
+    const float kinv = __uint_as_float(rc[2 * topk + 1]);
+    const float vcol = bf16_to_f32(vv[col]);
+    float kk[8], aj[8], qj[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (i < rpt) {
+        const int j = rg + kSseRG * i;
+        kk[i] = expf(kl[j] - kmax) * kinv;
+        aj[i] = al[j];
+        qj[i] = bf16_to_f32(qq[j]);
+      }
+    }
+    float part = 0.f;
+    for (int s = 0; s <= topk; ++s) {
+      const int p = s < topk ? static_cast<int>(rc[s]) : N;
+      const float g = s < topk ? __uint_as_float(rc[topk + s]) : 1.0f;
+      float *Sp = S + static_cast<size_t>(p) * c * kSseDT;
+      float inner = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (i < rpt) {
+          const int j = rg + kSseRG * i;
+          const float x = fmaf(aj[i], Sp[j * kSseDT + col], (g * kk[i]) * vcol);
+          Sp[j * kSseDT + col] = x;
+          inner = fmaf(qj[i], x, inner);
+        }
+      }
+      part = fmaf(g, inner, part);
+    }
+    red[(t & 1) * kSseRG * kSseDT + rg * kSseDT + col] = part;
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+  if (T > 0 && rg == 0) {
+    const float *rd = red + ((T - 1) & 1) * kSseRG * kSseDT;
+    float acc = 0.f;
+#pragma unroll
+    for (int g = 0; g < kSseRG; ++g) acc += rd[g * kSseDT + col];
+    a.y[(tok0 + static_cast<long>(T - 1) * H) * d + col0 + col] = acc;
+  }
+  // write the tile of every partition back
+  for (int e = tid; e < parts * c * (kSseDT / 4); e += kSseThreads) {
+    const int row = e / (kSseDT / 4), q4 = e % (kSseDT / 4);
+    *reinterpret_cast<float4 *>(gS + static_cast<long>(row) * d + col0 + 4 * q4) =
+        *reinterpret_cast<const float4 *>(S + row * kSseDT + 4 * q4);
+  }
+}
+
+size_t sse_smem_bytes(int N, int c, int topk) {
+  return sizeof(float) * (static_cast<size_t>(N + 1) * c * kSseDT + 2 * kSseRG * kSseDT) +
+         sizeof(uint32_t) * (kSseP + 1) * SseSlot::words(c, rec_words(topk));
+}
+
+}  // namespace
+}  // namespace sdm
+
+using namespace sdm;
+
+extern "C" size_t sse_scan_workspace_size(int B, int T, int H, int N, int topk) {
+  if (B <= 0 || T <= 0 || H <= 0 || N <= 0 || topk <= 0) return 0;
+  const size_t n = static_cast<size_t>(B) * T * H * rec_words(topk) * sizeof(uint32_t);
+  return (n + 255) & ~static_cast<size_t>(255);
+}
+
+extern "C" int sse_scan(float *state, const float *route_logits, int topk, const float *k_logits, const uint16_t *q,
+                        const uint16_t *v, const float *alpha, int B, int T, int H, int N, int c, int d, float *y,
+                        int32_t *sel_out, void *workspace, size_t workspace_bytes, int32_t *dev_err, void *stream) {
+  if (!state || !route_logits || !k_logits || !q || !v || !alpha || !y)
+    return set_error(SDM_ERR_INVALID_ARG, "sse_scan: null pointer");
+  if (B < 0 || T < 0 || H < 0) return set_error(SDM_ERR_INVALID_ARG, "sse_scan: negative size");
+  if (N < 1 || N > 64 || topk < 1 || topk > N || topk > kSseMaxTopk)
+    return set_error(SDM_ERR_SHAPE, "sse_scan: need 1 <= topk <= min(N, 8), N <= 64");
+  if (c < 16 || c > 128 || c % 16 != 0 || d < kSseDT || d % kSseDT != 0)
+    return set_error(SDM_ERR_SHAPE, "sse_scan: need c %% 16 == 0, 16 <= c <= 128, d %% 16 == 0");
+  int dev = 0, smem_blk = 0;
+  if (!aligned(state, 16) || !aligned(y, 4) || !aligned(k_logits, 16) || !aligned(alpha, 16) ||
+      !aligned(q, 16) || !aligned(v, 16) || !aligned(route_logits, 4) || (sel_out && !aligned(sel_out, 4)) ||
+      (dev_err && !aligned(dev_err, 4)))
+    return set_error(SDM_ERR_ALIGN, "sse_scan: state, k_logits, alpha, q, v need 16-byte alignment");
+  if (B == 0 || T == 0 || H == 0) return SDM_OK;
+  const size_t need = sse_scan_workspace_size(B, T, H, N, topk);
+  if (!workspace || workspace_bytes < need)
+    return set_error(SDM_ERR_INVALID_ARG, "sse_scan: workspace of %zu bytes needed", need);
+  if (!aligned(workspace, 16)) return set_error(SDM_ERR_ALIGN, "sse_scan: workspace must be 16-byte aligned");
+  const size_t smem = sse_smem_bytes(N, c, topk);
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&smem_blk, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (smem > static_cast<size_t>(smem_blk))
+    return set_error(SDM_ERR_SHAPE, "sse_scan: (N+1)*c too large for the shared-memory resident state");
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const long tokens = static_cast<long>(B) * T * H;
+  uint32_t *rec = static_cast<uint32_t *>(workspace);
+  sse_route_kernel<<<static_cast<unsigned>((tokens + 7) / 8), 256, 0, st>>>(route_logits, k_logits, tokens, N, topk,
+                                                                           c, rec, sel_out, dev_err);
+  int rc = check_launch("sse_scan: route kernel");
+  if (rc != SDM_OK) return rc;
+
+  SseArgs args;
+  args.state = state;
+  args.klog = k_logits;
+  args.alpha = alpha;
+  args.q = q;
+  args.v = v;
+  args.rec = rec;
+  args.y = y;
+  args.T = T;
+  args.H = H;
+  args.N = N;
+  args.c = c;
+  args.d = d;
+  args.topk = topk;
+  args.tiles = d / kSseDT;
+  args.rw = rec_words(topk);
+  if (cudaFuncSetAttribute(sse_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+      cudaSuccess)
+    return check_launch("sse_scan: set shared memory");
+  const long blocks = static_cast<long>(B) * H * args.tiles;
+  sse_scan_kernel<<<static_cast<unsigned>(blocks), kSseThreads, smem, st>>>(args);
+  return check_launch("sse_scan: scan kernel");
+}

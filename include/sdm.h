@@ -1,0 +1,198 @@
+/*
+ * sdm.h - C ABI of libsdm.so: the sparse-routed gated delta-rule memory scan
+ * on one GB300 (sm_103a).
+ *
+ * The method: a recurrent memory table per (batch, head) that each token
+ * addresses sparsely, decays only where it writes, updates with a delta rule
+ * and reads after the write.  Sources (reading decks of the three papers):
+ *   [SDM]  "Sparse Delta Memory" deck: "Product keys select addresses without
+ *          scoring every slot" (Secs. 2, 3.1); "Selected slots decay and
+ *          update; other slots persist" (Eqs. 3-5); "A v1 inconsistency
+ *          matters for reproducing the update" (Fig. 2 shared residual).
+ *   [LAA]  "Linear Attention Architectures" deck: "GDN and KDA change the
+ *          granularity of forgetting" (Eqs. 15-20).
+ *   [SSE]  "Sparse State Expansion" deck: "One gate controls both writes and
+ *          reads" (Eqs. 9-14); "SSE routes tokens into shared-parameter state
+ *          partitions" (shared partition); "A memory decays only when its
+ *          partition is visited".
+ *
+ * Conventions for every call below.
+ *   - Tensor pointers are DEVICE pointers (cudaMalloc'd or PyTorch-owned),
+ *     row-major and contiguous in the layout given.  The caller owns every
+ *     buffer; the library keeps no pointer after a call returns and allocates
+ *     no device memory.  Scratch space, where needed, is passed in by the
+ *     caller and sized by the matching *_workspace_size() call.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  All calls
+ *     are asynchronous and stream-ordered; none synchronises the host.
+ *   - Return value: SDM_OK (0) or one of the SDM_ERR_* codes.  On an error
+ *     return nothing has been launched and no output was touched, except for
+ *     SDM_ERR_CUDA (a launch failed; see sdm_last_error()).  Errors found on
+ *     the device (bad indices, non-finite scores) are OR-ed as SDM_DEVERR_*
+ *     bits into the optional `dev_err` word, which the caller reads after
+ *     synchronising; the kernels never trap.
+ *   - bf16 arguments are uint16_t bit patterns.
+ *   - Calls are thread-safe: they hold no global state apart from the
+ *     thread-local error text.
+ */
+#ifndef SDM_H_
+#define SDM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define SDM_OK 0
+#define SDM_ERR_INVALID_ARG 1  /* null pointer, negative size, small workspace */
+#define SDM_ERR_SHAPE 2        /* sizes inconsistent or beyond the limits below */
+#define SDM_ERR_ALIGN 3        /* pointer not aligned as required */
+#define SDM_ERR_UNSUPPORTED 4  /* unknown dtype or mode */
+#define SDM_ERR_CUDA 5         /* a CUDA launch or copy failed */
+
+/* Device-side error bits (OR-ed into *dev_err when dev_err != NULL). */
+#define SDM_DEVERR_INDEX_RANGE 1  /* a slot index outside [0, N) (skipped) */
+#define SDM_DEVERR_INDEX_REPEAT 2 /* a slot repeated within one token's write list */
+#define SDM_DEVERR_NONFINITE 4    /* a NaN or infinite score or logit */
+
+/* Element types of the value input of sdm_scan. */
+#define SDM_DTYPE_F32 0
+#define SDM_DTYPE_BF16 1
+
+/* Residual of the sparse write (sdm_scan). */
+#define SDM_RESID_SHARED 0   /* [SDM] Fig. 2: v_hat = sum_j w_j M~[j]; M[i] = M~[i] + beta w_i (v - v_hat) */
+#define SDM_RESID_PERSLOT 1  /* [SDM] printed Eq. 4: M[i] = M~[i] + beta w_i (v - M~[i]) */
+#define SDM_RESID_ADDITIVE 2 /* additive write, no residual: M[i] = M~[i] + beta w_i v */
+
+/* Library version (major*10000 + minor*100 + patch). */
+int sdm_version(void);
+
+/* Text of the last error raised by a call on this host thread ("" if none). */
+const char *sdm_last_error(void);
+
+/*
+ * sdm_address - product-key addressing, [SDM] "Product keys select addresses
+ * without scoring every slot" (Secs. 2 and 3.1).  Called once for the write
+ * halves (W = |I^w|) and once for the read halves (W = |I^r|).
+ *
+ * For every token-head row r in [0, B*T*H):
+ *   1. keep the top-k entries of s1[r] and of s2[r] (value descending, ties
+ *      to the lower index);
+ *   2. form only the k*k candidate scores s1[a] + s2[b] (one fp32 addition,
+ *      round to nearest) with slot id a*sqrtN + b;
+ *   3. select the top-W candidates by (score descending, slot id ascending);
+ *   4. w = softmax over the W selected scores (no temperature).
+ *
+ * s1, s2  : fp32 [B,T,H,sqrtN] score halves.
+ * idx_out : int32 [B,T,H,W] selected slot ids in rank order (bit-exact).
+ * w_out   : fp32 [B,T,H,W] softmax weights, same order.
+ * dev_err : optional; SDM_DEVERR_NONFINITE if a score is NaN/inf.
+ * Limits: 1 <= sqrtN <= 512, 1 <= k <= min(32, sqrtN), 1 <= W <= min(64, k*k),
+ *         B*T*H < 2^31.  Pointers 4-byte aligned.
+ */
+int sdm_address(const float *s1, const float *s2, int B, int T, int H, int sqrtN, int k, int W,
+                int32_t *idx_out, float *w_out, int32_t *dev_err, void *stream);
+
+/*
+ * Scratch bytes sdm_scan needs for these sizes (a per-token hazard table of
+ * B*T*H*(W+R) uint16 entries, rounded up to 256 bytes).
+ */
+size_t sdm_scan_workspace_size(int B, int T, int H, int W, int R);
+
+/*
+ * sdm_scan - the sparse delta-rule memory scan, [SDM] Eqs. 3-5 with the
+ * Fig. 2 shared residual by default.  For each (b, h), tokens in order:
+ *   M~[i] = alpha_t M[i]                 for i in I^w only (selective decay)
+ *   M[i]  = M~[i] + beta_t w_i * resid   resid per resid_mode (SDM_RESID_*)
+ *   rows not in I^w keep their bits
+ *   y_t   = sum_{i in I^r} r_i M[i]      read after the write
+ *
+ * state     : fp32 [B,H,N,d_v], updated in place (M_0 in, M_T out).  Calling
+ *             again with the same buffer continues the sequence.
+ * v         : [B,T,H,d_v], fp32 or bf16 per v_dtype.
+ * alpha,beta: fp32 [B,T,H] per-head forget and input gates.
+ * idx_w,w_w : int32 / fp32 [B,T,H,W] write slots and weights (from sdm_address).
+ * idx_r,w_r : int32 / fp32 [B,T,H,R] read slots and weights.
+ * y         : fp32 [B,T,H,d_v].
+ * workspace : device scratch of at least sdm_scan_workspace_size(B,T,H,W,R)
+ *             bytes, 16-byte aligned; contents need no initialisation.
+ * dev_err   : optional; SDM_DEVERR_INDEX_RANGE (that slot is read as zero and
+ *             not written) and SDM_DEVERR_INDEX_REPEAT (result for that token
+ *             unspecified, memory-safe).
+ * Limits: 1 <= W, R <= 64; d_v % 4 == 0; N >= 1.  state and y 16-byte
+ *         aligned; v, alpha, beta, idx, w 4-byte aligned.
+ */
+int sdm_scan(float *state, const void *v, int v_dtype, const float *alpha, const float *beta,
+             const int32_t *idx_w, const float *w_w, int W, const int32_t *idx_r, const float *w_r, int R,
+             int B, int T, int H, int N, int d_v, int resid_mode, float *y, void *workspace,
+             size_t workspace_bytes, int32_t *dev_err, void *stream);
+
+/*
+ * Scratch bytes gdn_scan needs (0 for the current kernels; kept so callers
+ * can size a workspace once and keep the call stable).
+ */
+size_t gdn_scan_workspace_size(int B, int T, int H, int dk, int dv, int per_channel);
+
+/*
+ * gdn_scan - dense Gated DeltaNet (per_channel = 0) or Kimi Delta Attention
+ * (per_channel = 1), [LAA] Eqs. 15-20, with the state stored key-major
+ * (S = W^T, rows are key channels):
+ *   S~   = D_alpha S              (GDN: every row scaled by alpha_t)
+ *   pred = S~^T k_t               (decay-adjusted prediction)
+ *   S    = S~ + beta_t k_t (v_t - pred)^T
+ *   y_t  = S^T q_t                (unnormalised read after the write)
+ * This is sdm_scan with every row selected, write weights k_t and read
+ * weights q_t ([SDM] "A v1 inconsistency ...": the dense limit).
+ *
+ * state : fp32 [B,H,dk,dv] in place.
+ * q, k  : bf16 [B,T,H,dk];  v : bf16 [B,T,H,dv].
+ * alpha : fp32 [B,T,H] (GDN) or [B,T,H,dk] (KDA).   beta : fp32 [B,T,H].
+ * y     : fp32 [B,T,H,dv].
+ * Limits: dk in {16, 32, 64, 128}; dv % 32 == 0, dv <= 256.  state and y
+ *         16-byte aligned; q, k, v 16-byte aligned (dk, dv multiples of 8).
+ */
+int gdn_scan(float *state, const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
+             int per_channel, const float *beta, int B, int T, int H, int dk, int dv, float *y, void *workspace,
+             size_t workspace_bytes, void *stream);
+
+/*
+ * Scratch bytes sse_scan needs: one routing record per token (selected
+ * partitions, their gates, and the max and inverse normaliser of the row
+ * softmax), rounded up to 256 bytes.
+ */
+size_t sse_scan_workspace_size(int B, int T, int H, int N, int topk);
+
+/*
+ * sse_scan - Sparse State Expansion, [SSE] Eqs. 9-14, with N routed
+ * partitions plus one always-active shared partition (index N):
+ *   e_t  = softmax(route_t) over all N partitions (not renormalised)
+ *   T_t  = top-k of route_t (value descending, ties to the lower index)
+ *   kk_t = softmax(k_logits_t) over the c rows of a partition
+ *   for p in T_t (gate g = e_t[p]) and p = N (g = 1):
+ *       S^p[j,:] = alpha_t[j] S^p[j,:] + g kk_t[j] v_t     (j < c)
+ *   unvisited partitions keep their bits (their decay clock stops)
+ *   y_t  = sum_p g_p sum_j q_t[j] S^p[j,:]                 (after the write)
+ *
+ * state       : fp32 [B,H,N+1,c,d] in place.
+ * route_logits: fp32 [B,T,H,N].  k_logits : fp32 [B,T,H,c].
+ * q           : bf16 [B,T,H,c].  v : bf16 [B,T,H,d].  alpha : fp32 [B,T,H,c].
+ * y           : fp32 [B,T,H,d].
+ * sel_out     : optional int32 [B,T,H,topk], the selected partitions in rank order.
+ * workspace   : device scratch of at least sse_scan_workspace_size() bytes,
+ *               16-byte aligned.
+ * dev_err     : optional; SDM_DEVERR_NONFINITE if a logit is NaN/inf.
+ * Limits: 1 <= topk <= N <= 64, topk <= 8; c % 16 == 0, 16 <= c <= 128;
+ *         d % 16 == 0.  state, y, k_logits, alpha 16-byte aligned; q, v
+ *         16-byte aligned.
+ */
+int sse_scan(float *state, const float *route_logits, int topk, const float *k_logits, const uint16_t *q,
+             const uint16_t *v, const float *alpha, int B, int T, int H, int N, int c, int d, float *y,
+             int32_t *sel_out, void *workspace, size_t workspace_bytes, int32_t *dev_err, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SDM_H_ */

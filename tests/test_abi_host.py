@@ -1,0 +1,96 @@
+"""Host-side checks of the C ABI (no GPU): the library builds, loads, exports
+every function that include/sdm.h declares, and rejects bad arguments with
+the documented status codes before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "sdm.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^(?:const\s+)?(?:int|size_t|char|void)\s*\*?\s*(\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def sdm():
+    from delta_rule_memory_gb300 import build as b
+    b.build()
+    import delta_rule_memory_gb300 as m
+    return m
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for fn in ("sdm_address", "sdm_scan", "gdn_scan", "sse_scan", "sdm_version", "sdm_last_error",
+               "sdm_scan_workspace_size", "gdn_scan_workspace_size"):
+        assert fn in names
+
+
+def test_library_exports_every_declared_symbol(sdm):
+    lib = ctypes.CDLL(sdm.library_path)
+    missing = [n for n in _declared_functions() if not hasattr(lib, n)]
+    assert not missing, f"declared in sdm.h but not exported: {missing}"
+
+
+def test_version_and_workspace(sdm):
+    assert sdm.sdm_version() >= 10000
+    # one uint16 hazard code per (token, slot), rows padded to an even count
+    assert sdm.sdm_scan_workspace_size(8, 4096, 2, 16, 16) == 8 * 4096 * 2 * 32 * 2
+    assert sdm.sdm_scan_workspace_size(1, 3, 1, 3, 4) == 256
+    assert sdm.sdm_scan_workspace_size(0, 3, 1, 3, 4) == 0
+
+
+# Fake, 256-byte aligned "device" addresses: every call below must return an
+# error during host validation, before any CUDA call.
+A = 1 << 20
+B_ = 2 << 20
+
+
+def test_address_rejects_bad_arguments(sdm):
+    L = sdm.lib()
+    assert L.sdm_address(None, A, 1, 1, 1, 8, 4, 4, A, A, None, None) == sdm.SDM_ERR_INVALID_ARG
+    assert L.sdm_address(A, A, -1, 1, 1, 8, 4, 4, A, A, None, None) == sdm.SDM_ERR_INVALID_ARG
+    assert L.sdm_address(A, A, 1, 1, 1, 8, 9, 4, A, A, None, None) == sdm.SDM_ERR_SHAPE      # k > sqrtN
+    assert L.sdm_address(A, A, 1, 1, 1, 8, 4, 17, A, A, None, None) == sdm.SDM_ERR_SHAPE     # W > k^2
+    assert L.sdm_address(A, A, 1, 1, 1, 600, 4, 4, A, A, None, None) == sdm.SDM_ERR_SHAPE    # sqrtN > 512
+    assert L.sdm_address(A, A, 1, 1, 1, 64, 33, 4, A, A, None, None) == sdm.SDM_ERR_SHAPE    # k > 32
+    assert L.sdm_address(A + 2, A, 1, 1, 1, 8, 4, 4, A, A, None, None) == sdm.SDM_ERR_ALIGN
+    assert b"sdm_address" in L.sdm_last_error()
+
+
+def test_scan_rejects_bad_arguments(sdm):
+    L = sdm.lib()
+
+    def call(**kw):
+        a = dict(state=A, v=A, vdt=1, alpha=A, beta=A, iw=A, ww=A, W=16, ir=A, wr=A, R=16, B=1, T=4, H=1,
+                 N=64, dv=16, mode=0, y=A, ws=B_, wsb=1 << 20, err=None)
+        a.update(kw)
+        return L.sdm_scan(a["state"], a["v"], a["vdt"], a["alpha"], a["beta"], a["iw"], a["ww"], a["W"], a["ir"],
+                          a["wr"], a["R"], a["B"], a["T"], a["H"], a["N"], a["dv"], a["mode"], a["y"], a["ws"],
+                          a["wsb"], a["err"], None)
+
+    assert call(state=None) == sdm.SDM_ERR_INVALID_ARG
+    assert call(W=0) == sdm.SDM_ERR_SHAPE
+    assert call(R=65) == sdm.SDM_ERR_SHAPE
+    assert call(dv=18) == sdm.SDM_ERR_SHAPE
+    assert call(vdt=7) == sdm.SDM_ERR_UNSUPPORTED
+    assert call(mode=3) == sdm.SDM_ERR_UNSUPPORTED
+    assert call(state=A + 4) == sdm.SDM_ERR_ALIGN
+    assert call(wsb=16) == sdm.SDM_ERR_INVALID_ARG            # workspace too small
+    assert call(ws=None) == sdm.SDM_ERR_INVALID_ARG
+    assert call(ws=B_ + 8) == sdm.SDM_ERR_ALIGN
+    assert b"workspace" in L.sdm_last_error()
+
+
+def test_binding_fails_loudly_without_cuda_tensors(sdm):
+    import torch
+    with pytest.raises(TypeError):
+        sdm.sdm_address(torch.zeros(1, 1, 1, 8), torch.zeros(1, 1, 1, 8), 4, 4)

@@ -1,0 +1,165 @@
+"""GPU parity of the dense (gdn_scan: GDN / KDA) and Sparse State Expansion
+(sse_scan) paths against the fp64 CPU oracle, through the C ABI."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import assert_state_close, assert_y_close, dev, host, need_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+# ---------------------------------------------------------------- dense GDN/KDA
+def _gdn_gpu(sdm, S0, inp, per_channel):
+    state = dev(S0)
+    a = inp["alpha_kda"] if per_channel else inp["alpha_gdn"]
+    y = sdm.gdn_scan(state, dev(inp["q"]), dev(inp["k"]), dev(inp["v"]), dev(a), dev(inp["beta"]), per_channel)
+    return host(state), host(y)
+
+
+@pytest.mark.parametrize("per_channel", [False, True])
+@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 96), (16, 32)])
+def test_gdn_reduced_parity(per_channel, dk, dv):
+    sdm = need_gpu()
+    sh = synth.GDN_DENSE.with_(B=2, T=200, H=3, dk=dk, dv=dv)
+    inp = synth.gdn_inputs(sh, seed=dk + dv)
+    S0 = synth.random_state((2, 3, dk, dv), seed=1, scale=0.3)
+    a = inp["alpha_kda"] if per_channel else inp["alpha_gdn"]
+    Sr, yr = oracle.gdn_scan(S0, inp["q"], inp["k"], inp["v"], a, inp["beta"], per_channel)
+    S, y = _gdn_gpu(sdm, S0, inp, per_channel)
+    assert_y_close(y, yr)
+    assert_state_close(S, Sr)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("per_channel", [False, True])
+def test_gdn_full_size_sampled(per_channel):
+    """The full dense workload (B=4, T=4096, H=16, dk=dv=128, zero state) on the
+    GPU; the oracle recomputes three whole (b, h) sequences."""
+    sdm = need_gpu()
+    sh = synth.GDN_DENSE
+    inp = synth.gdn_inputs(sh, seed=0)
+    S0 = np.zeros((sh.B, sh.H, sh.dk, sh.dv), np.float32)
+    S, y = _gdn_gpu(sdm, S0, inp, per_channel)
+    a = inp["alpha_kda"] if per_channel else inp["alpha_gdn"]
+    for b, h in ((0, 0), (2, 7), (3, 15)):
+        sl = (slice(b, b + 1), slice(None), slice(h, h + 1))
+        Sr, yr = oracle.gdn_scan(np.zeros((1, 1, sh.dk, sh.dv)), inp["q"][sl], inp["k"][sl], inp["v"][sl], a[sl],
+                                 inp["beta"][sl], per_channel)
+        assert_y_close(y[sl], yr, what=f"y[{b},{h}]")
+        assert_state_close(S[b:b + 1, h:h + 1], Sr, what=f"state[{b},{h}]")
+
+
+def test_kda_with_constant_channel_decay_is_gdn_bitexact():
+    sdm = need_gpu()
+    sh = synth.GDN_DENSE.with_(B=1, T=64, H=2)
+    inp = synth.gdn_inputs(sh, seed=3)
+    inp2 = dict(inp)
+    inp2["alpha_kda"] = np.repeat(inp["alpha_gdn"][..., None], sh.dk, axis=-1).copy()
+    S0 = synth.random_state((1, 2, sh.dk, sh.dv), seed=4, scale=0.2)
+    Sg, yg = _gdn_gpu(sdm, S0, inp, False)
+    Sk, yk = _gdn_gpu(sdm, S0, inp2, True)
+    assert np.array_equal(yg, yk) and np.array_equal(Sg, Sk)
+
+
+def test_sparse_scan_with_every_row_selected_matches_dense():
+    """sdm_scan with N = dk, all rows selected, weights k_t / q_t and the shared
+    residual is gdn_scan (the dense limit of the sparse write)."""
+    sdm = need_gpu()
+    import torch
+    sh = synth.GDN_DENSE.with_(B=1, T=96, H=2, dk=32, dv=64)
+    inp = synth.gdn_inputs(sh, seed=8)
+    S0 = synth.random_state((1, 2, 32, 64), seed=2, scale=0.5)
+    Sg, yg = _gdn_gpu(sdm, S0, inp, False)
+    kk = oracle.widen(inp["k"]).astype(np.float32)
+    qq = oracle.widen(inp["q"]).astype(np.float32)
+    idx = np.broadcast_to(np.arange(32, dtype=np.int32), (1, 96, 2, 32)).copy()
+    state = dev(S0)
+    y = sdm.sdm_scan(state, dev(inp["v"]), dev(inp["alpha_gdn"]), dev(inp["beta"]), dev(idx), dev(kk), dev(idx),
+                     dev(qq))
+    torch.cuda.synchronize()
+    assert_y_close(host(y), yg)
+    assert_state_close(host(state), Sg)
+
+
+def test_gdn_teaching_example_on_gpu(golden):
+    sdm = need_gpu()
+    g = golden("deltanet_teaching.txt")
+    dk, dv = 16, 32
+    S0 = np.zeros((1, 1, dk, dv), np.float32)
+    S0[0, 0, 3] = g["prediction"][0]
+    e = np.zeros((1, 1, 1, dk), np.float32)
+    e[..., 3] = 1.0
+    inp = {"q": synth.to_bf16_bits(__import__("torch").from_numpy(e)), "k": None,
+           "v": synth.to_bf16_bits(__import__("torch").full((1, 1, 1, dv), g["target"][0])),
+           "alpha_gdn": np.ones((1, 1, 1), np.float32), "beta": np.full((1, 1, 1), g["beta"][0], np.float32)}
+    inp["k"] = inp["q"]
+    _, y = _gdn_gpu(sdm, S0, inp, False)
+    np.testing.assert_allclose(y.ravel(), g["new_prediction"][0], atol=1e-6)
+
+
+# ------------------------------------------------------------------------- SSE
+def _sse_gpu(sdm, S0, inp, topk):
+    import torch
+    B, T, H, N = inp["route"].shape
+    state = dev(S0)
+    sel = torch.zeros((B, T, H, topk), dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y = sdm.sse_scan(state, dev(inp["route"]), topk, dev(inp["klog"]), dev(inp["q"]), dev(inp["v"]),
+                     dev(inp["alpha"]), sel_out=sel, dev_err=err)
+    return host(state), host(y), host(sel), int(host(err)[0])
+
+
+@pytest.mark.parametrize("N,topk,c,d", [(8, 2, 128, 128), (4, 1, 64, 32), (16, 3, 32, 48), (1, 1, 16, 16)])
+def test_sse_reduced_parity(N, topk, c, d):
+    sdm = need_gpu()
+    sh = synth.SSE_PART.with_(B=2, T=150, H=3, N=N, topk=topk, c=c, d=d)
+    inp = synth.sse_inputs(sh, seed=N + c)
+    S0 = synth.random_state((2, 3, N + 1, c, d), seed=5)
+    Sr, yr, selr = oracle.sse_scan(S0, inp["route"], topk, inp["klog"], inp["q"], inp["v"], inp["alpha"])
+    S, y, sel, err = _sse_gpu(sdm, S0, inp, topk)
+    assert err == 0
+    np.testing.assert_array_equal(sel, selr)
+    assert_y_close(y, yr)
+    assert_state_close(S, Sr)
+
+
+@pytest.mark.slow
+def test_sse_full_size_sampled():
+    """The full SSE workload (B=4, T=4096, H=8, 8+1 partitions of 128x128,
+    top-2) on the GPU; the oracle recomputes two whole (b, h) sequences."""
+    sdm = need_gpu()
+    sh = synth.SSE_PART
+    inp = synth.sse_inputs(sh, seed=0)
+    S0 = np.zeros((sh.B, sh.H, sh.N + 1, sh.c, sh.d), np.float32)
+    S, y, sel, err = _sse_gpu(sdm, S0, inp, sh.topk)
+    assert err == 0
+    for b, h in ((0, 0), (3, 7)):
+        sl = (slice(b, b + 1), slice(None), slice(h, h + 1))
+        Sr, yr, selr = oracle.sse_scan(np.zeros((1, 1, sh.N + 1, sh.c, sh.d)), inp["route"][sl], sh.topk,
+                                       inp["klog"][sl], inp["q"][sl], inp["v"][sl], inp["alpha"][sl])
+        np.testing.assert_array_equal(sel[sl], selr)
+        assert_y_close(y[sl], yr, what=f"y[{b},{h}]")
+        assert_state_close(S[b:b + 1, h:h + 1], Sr, what=f"state[{b},{h}]")
+
+
+def test_sse_local_clock_on_gpu(golden):
+    sdm = need_gpu()
+    g = golden("sse_local_clock.txt")
+    a, T, visits = g["decay"][0], int(g["tokens"][0]), int(g["visits"][0])
+    N, c, d = 4, 16, 16
+    route = np.full((1, T, 1, N), -5.0, np.float32)
+    route[0, :, 0, 1] = 3.0
+    route[0, np.linspace(0, T - 1, visits).astype(int), 0, 0] = 4.0
+    S0 = synth.random_state((1, 1, N + 1, c, d), seed=21) + 2.0
+    zeros_bf = np.zeros((1, T, 1, c), np.uint16)
+    inp = {"route": route, "klog": np.zeros((1, T, 1, c), np.float32), "q": zeros_bf,
+           "v": np.zeros((1, T, 1, d), np.uint16), "alpha": np.full((1, T, 1, c), a, np.float32)}
+    S, _, sel, _ = _sse_gpu(sdm, S0, inp, 1)
+    assert np.sum(sel == 0) == visits
+    np.testing.assert_allclose(S[0, 0, 0] / S0[0, 0, 0], a ** visits, rtol=2e-6)
+    np.testing.assert_allclose(S[0, 0, 0] / S0[0, 0, 0], g["sparse_retained"][0], atol=5e-4)
+    np.testing.assert_allclose(S[0, 0, N] / S0[0, 0, N], g["dense_retained"][0], atol=5e-4)
+    for p in (2, 3):
+        assert np.array_equal(S[0, 0, p].view(np.uint32), S0[0, 0, p].view(np.uint32))
