@@ -71,7 +71,21 @@ __global__ void hazard_kernel(const int32_t *__restrict__ idx_w, const int32_t *
 }
 
 // ---------------------------------------------------------------------------
-// The scan.
+// The scan.  One CTA of NG warps per (batch, head, column tile of tw <= 128
+// columns).  Lane l owns columns [4l, 4l+4) of the tile (a float4 quad); warp
+// g owns the write slots and read slots j == g (mod NG) of every token, so a
+// token's rows are processed by all warps at once.  Per token:
+//   B1  barrier: this token's rows (prefetched P tokens ago) have landed;
+//       issue the prefetch of token t+P (rows) and t+2P (metadata);
+//   2.  decay own write rows, partial shared prediction -> red1
+//   B2  barrier (shared residual only): v_hat = sum over warps
+//   3.  delta write of own write rows (history ring + table in HBM); read own
+//       read rows -> partial y -> red2 (summed by warp 0 after the next B1).
+// Rings in shared memory: incoming write rows (P+1 slots), post-write history
+// (P+1 slots, the forwarding source), incoming read rows (P+1), metadata
+// (2P+1).  A read slot that names a row written by the same token (distance
+// 0) recomputes that row's new value from the same inputs, so no warp reads a
+// history slot while another warp is writing it.
 // ---------------------------------------------------------------------------
 struct ScanArgs {
   float *state;
@@ -81,96 +95,93 @@ struct ScanArgs {
   const float *w_w, *w_r;
   const uint16_t *hz;
   float *y;
-  int W, R, T, H, N, d_v, mode, v_bf16, tiles, hzs;
-  long total_warps;
+  int W, R, T, H, N, d_v, mode, v_bf16, tiles, tw, hzs;
 };
 
-template <int CPL, int SLOTS, int P>
-struct ScanLayout {
-  static constexpr int TC = 32 * CPL;  // tile columns
-  static constexpr int NW = 2 * P + 1; // write-row ring: P in flight, current, P history
-  static constexpr int NR = P + 1;     // read-row ring: P in flight, current
-  static constexpr int NM = 2 * P + 1; // per-token metadata ring
-  struct alignas(16) Meta {
-    int32_t iw[SLOTS];
-    float ww[SLOTS];
-    int32_t ir[SLOTS];
-    float wr[SLOTS];
-    uint16_t hz[2 * SLOTS];
-    uint32_t vraw[TC];  // TC fp32 or TC/2 words of bf16 pairs
-    float ab[2];        // alpha, beta
-  };
-  static constexpr size_t kRowsBytes = static_cast<size_t>(NW + NR) * SLOTS * TC * sizeof(float);
-  static constexpr size_t kZeroOffset = kRowsBytes + NM * sizeof(Meta);  // one all-zero row
-  static constexpr size_t kWarpBytes = (kZeroOffset + TC * sizeof(float) + 127) & ~static_cast<size_t>(127);
-  static_assert(sizeof(Meta) % 16 == 0 && kRowsBytes % 16 == 0, "16-byte alignment of the warp's regions");
+constexpr int kNG = 8;  // warps (row groups) per CTA
+
+template <int SLOTS>
+struct alignas(16) ScanMeta {
+  int32_t iw[SLOTS];
+  float ww[SLOTS];
+  int32_t ir[SLOTS];
+  float wr[SLOTS];
+  uint16_t hz[2 * SLOTS];
+  uint32_t vraw[128];  // tw fp32 values or tw/2 words of bf16 pairs
+  float ab[4];         // alpha, beta
 };
 
-template <int CPL>
-__device__ __forceinline__ void load_cols(const float *p, float (&x)[CPL]) {
-  if constexpr (CPL == 4) {
-    const float4 q = *reinterpret_cast<const float4 *>(p);
-    x[0] = q.x; x[1] = q.y; x[2] = q.z; x[3] = q.w;
-  } else if constexpr (CPL == 2) {
-    const float2 q = *reinterpret_cast<const float2 *>(p);
-    x[0] = q.x; x[1] = q.y;
-  } else {
-    x[0] = *p;
-  }
-}
-template <int CPL>
-__device__ __forceinline__ void store_cols(float *p, const float (&x)[CPL]) {
-  if constexpr (CPL == 4) {
-    *reinterpret_cast<float4 *>(p) = make_float4(x[0], x[1], x[2], x[3]);
-  } else if constexpr (CPL == 2) {
-    *reinterpret_cast<float2 *>(p) = make_float2(x[0], x[1]);
-  } else {
-    *p = x[0];
-  }
+template <int SLOTS>
+__host__ __device__ inline size_t scan_smem_bytes(int P, int tw) {
+  const size_t rows = static_cast<size_t>(3) * (P + 1) * SLOTS * tw * sizeof(float);
+  return rows + static_cast<size_t>(2 * P + 1) * sizeof(ScanMeta<SLOTS>) + 3 * kNG * 32 * sizeof(float4);
 }
 
-template <int CPL, int SLOTS, int P>
-__global__ void __launch_bounds__(256) sparse_scan_kernel(const ScanArgs a) {
-  using L = ScanLayout<CPL, SLOTS, P>;
-  using Meta = typename L::Meta;
-  constexpr int TC = L::TC;
+__device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ void st4(float *p, float4 x) { *reinterpret_cast<float4 *>(p) = x; }
+__device__ __forceinline__ float4 f4_fma(float s, float4 x, float4 acc) {
+  return make_float4(fmaf(s, x.x, acc.x), fmaf(s, x.y, acc.y), fmaf(s, x.z, acc.z), fmaf(s, x.w, acc.w));
+}
+__device__ __forceinline__ float4 f4_scale(float s, float4 x) { return make_float4(s * x.x, s * x.y, s * x.z, s * x.w); }
+__device__ __forceinline__ float4 f4_add(float4 a, float4 b) {
+  return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
+__device__ __forceinline__ float4 f4_sub(float4 a, float4 b) {
+  return make_float4(a.x - b.x, a.y - b.y, a.z - b.z, a.w - b.w);
+}
+
+template <int P, int SLOTS>
+__global__ void __launch_bounds__(kNG * 32, 1) sparse_scan_kernel(const ScanArgs a) {
+  using Meta = ScanMeta<SLOTS>;
+  constexpr int NI = P + 1, NH = P + 1, NR = P + 1, NM = 2 * P + 1;
+  constexpr int NT = kNG * 32;
+  constexpr int WPG = (SLOTS + kNG - 1) / kNG;           // write (or read) slots per warp
+  constexpr int KMAX = (2 * SLOTS * 32 + NT - 1) / NT;  // row chunks per thread per token
   extern __shared__ __align__(16) unsigned char smem_raw[];
 
-  const int lane = threadIdx.x & 31;
-  const int wib = threadIdx.x >> 5;
-  const long gw = static_cast<long>(blockIdx.x) * (blockDim.x >> 5) + wib;
-  if (gw >= a.total_warps) return;  // warp-uniform; the kernel has no CTA barrier
-  const int tile = static_cast<int>(gw % a.tiles);
-  const long bh = gw / a.tiles;
+  const int tid = threadIdx.x, lane = tid & 31, g = tid >> 5;
+  const int tile = blockIdx.x % a.tiles;
+  const long bh = blockIdx.x / a.tiles;
   const int h = static_cast<int>(bh % a.H);
   const long b = bh / a.H;
+  const int W = a.W, R = a.R, T = a.T, H = a.H, d_v = a.d_v, N = a.N;
+  const int col0 = tile * a.tw;
+  const int tw = min(a.tw, d_v - col0);  // this tile's width, a multiple of 4
+  const int nq = tw >> 2;                // active quads (lanes)
+  const int RS = a.tw;                   // smem row stride (floats)
+  const bool qa = lane < nq;
 
-  unsigned char *base = smem_raw + static_cast<size_t>(wib) * L::kWarpBytes;
-  float(*wring)[SLOTS][TC] = reinterpret_cast<float(*)[SLOTS][TC]>(base);
-  float(*rring)[SLOTS][TC] = reinterpret_cast<float(*)[SLOTS][TC]>(base + sizeof(float) * L::NW * SLOTS * TC);
-  Meta *meta = reinterpret_cast<Meta *>(base + L::kRowsBytes);
-  float *zero_row = reinterpret_cast<float *>(base + L::kZeroOffset);
+  float *inW = reinterpret_cast<float *>(smem_raw);
+  float *hist = inW + NI * SLOTS * RS;
+  float *inR = hist + NH * SLOTS * RS;
+  Meta *meta = reinterpret_cast<Meta *>(inR + NR * SLOTS * RS);
+  float4 *red1 = reinterpret_cast<float4 *>(meta + NM);  // [NG][32]
+  float4 *red2 = red1 + kNG * 32;                         // [2][NG][32]
 
-  const int lc = lane * CPL;               // first column of this lane inside the tile
-  const int col = tile * TC + lc;          // absolute column
-  const bool active = col < a.d_v;
-  const int W = a.W, R = a.R, T = a.T, H = a.H, d_v = a.d_v;
-  float *table = a.state + bh * static_cast<long>(a.N) * d_v;  // [N, d_v] of this (b, h)
-  const long tok0 = b * T * H + h;                               // token t -> tok0 + t*H
+  float *table = a.state + bh * static_cast<long>(N) * d_v + col0;
+  const long tok0 = b * T * H + h;
 
-  // words of metadata per token, in copy order
-  const int v_words = a.v_bf16 ? TC / 2 : TC;
+  // this thread's row chunks: chunk c = tid + k*NT of the (W+R) x nq grid
+  int ck_row[KMAX], ck_q[KMAX];
+#pragma unroll
+  for (int k = 0; k < KMAX; ++k) {
+    const int c = tid + k * NT;
+    const int row = nq > 0 ? c / nq : 0;
+    ck_row[k] = (c < (W + R) * nq) ? row : -1;
+    ck_q[k] = c - row * nq;
+  }
+
+  const int v_words = a.v_bf16 ? tw / 2 : tw;
   const int hz_words = a.hzs / 2;
   const int m_total = 2 * W + 2 * R + hz_words + v_words + 2;
 
   auto issue_meta = [&](int t) {
-    Meta &m = meta[t % L::NM];
+    Meta &m = meta[t % NM];
     const long tok = tok0 + static_cast<long>(t) * H;
-    for (int q = lane; q < m_total; q += 32) {
+    for (int q = tid; q < m_total; q += NT) {
       int r = q;
       void *dst;
       const void *src;
-      bool ok = true;
       if (r < W) { dst = &m.iw[r]; src = a.idx_w + tok * W + r; }
       else if ((r -= W) < W) { dst = &m.ww[r]; src = a.w_w + tok * W + r; }
       else if ((r -= W) < R) { dst = &m.ir[r]; src = a.idx_r + tok * R + r; }
@@ -179,168 +190,180 @@ __global__ void __launch_bounds__(256) sparse_scan_kernel(const ScanArgs a) {
         dst = reinterpret_cast<uint32_t *>(m.hz) + r;
         src = reinterpret_cast<const uint32_t *>(a.hz + tok * a.hzs) + r;
       } else if ((r -= hz_words) < v_words) {
-        const int c0 = tile * TC + (a.v_bf16 ? 2 * r : r);
-        ok = c0 < d_v;
         dst = &m.vraw[r];
-        src = a.v_bf16 ? static_cast<const void *>(static_cast<const uint16_t *>(a.v) + tok * d_v + c0)
-                       : static_cast<const void *>(static_cast<const float *>(a.v) + tok * d_v + c0);
+        src = a.v_bf16 ? static_cast<const void *>(static_cast<const uint16_t *>(a.v) + tok * d_v + col0 + 2 * r)
+                       : static_cast<const void *>(static_cast<const float *>(a.v) + tok * d_v + col0 + r);
       } else {
         r -= v_words;
         dst = &m.ab[r];
         src = (r == 0 ? a.alpha : a.beta) + tok;
       }
-      if (ok) cp_async<4>(dst, src);
+      cp_async<4>(dst, src);
     }
   };
   auto issue_rows = [&](int t) {
-    const Meta &m = meta[t % L::NM];
-    if (!active) return;
-    float(*wr)[TC] = wring[t % L::NW];
-    float(*rr)[TC] = rring[t % L::NR];
-    for (int j = 0; j < W; ++j) {
-      const int i = m.iw[j];
-      if (static_cast<unsigned>(i) < static_cast<unsigned>(a.N))
-        cp_async<4 * CPL>(&wr[j][lc], table + static_cast<long>(i) * d_v + col);
-    }
-    for (int j = 0; j < R; ++j) {
-      const int i = m.ir[j];
-      if (static_cast<unsigned>(i) < static_cast<unsigned>(a.N))
-        cp_async<4 * CPL>(&rr[j][lc], table + static_cast<long>(i) * d_v + col);
+    const Meta &m = meta[t % NM];
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+      const int row = ck_row[k];
+      if (row < 0) continue;
+      const bool isw = row < W;
+      const int j = isw ? row : row - W;
+      const int i = isw ? m.iw[j] : m.ir[j];
+      float *dst = (isw ? inW + (t % NI) * SLOTS * RS : inR + (t % NR) * SLOTS * RS) + j * RS + 4 * ck_q[k];
+      if (static_cast<unsigned>(i) < static_cast<unsigned>(N))
+        cp_async<16>(dst, table + static_cast<long>(i) * d_v + 4 * ck_q[k]);
     }
   };
 
-  // prologue: metadata of tokens [0, P) first, then P groups that each carry
-  // the metadata of token j+P and the rows of token j.
+  // prologue: metadata of tokens [0, P), then P groups (rows of j, meta of j+P)
   for (int t = 0; t < P && t < T; ++t) issue_meta(t);
   cp_async_commit();
   cp_async_wait<0>();
-  __syncwarp();
+  __syncthreads();
   for (int j = 0; j < P; ++j) {
     if (j + P < T) issue_meta(j + P);
     if (j < T) issue_rows(j);
     cp_async_commit();
   }
 
-#pragma unroll
-  for (int c = 0; c < CPL; ++c) zero_row[lc + c] = 0.f;
+  const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int t = 0; t < T; ++t) {
-    // group t-P (rows of t, metadata of t+P) has landed
     cp_async_wait<P - 1>();
-    __syncwarp();
+    __syncthreads();  // B1
+    if (t > 0 && g == 0 && qa) {
+      const float4 *rd = red2 + ((t - 1) & 1) * kNG * 32;
+      float4 acc = rd[lane];
+#pragma unroll
+      for (int w = 1; w < kNG; ++w) acc = f4_add(acc, rd[w * 32 + lane]);
+      st4(a.y + (tok0 + static_cast<long>(t - 1) * H) * d_v + col0 + 4 * lane, acc);
+    }
     if (t + 2 * P < T) issue_meta(t + 2 * P);
     if (t + P < T) issue_rows(t + P);
     cp_async_commit();
 
-    const Meta &m = meta[t % L::NM];
-    float(*cur)[TC] = wring[t % L::NW];
+    const Meta &m = meta[t % NM];
     const float al = m.ab[0], be = m.ab[1];
-    float vv[CPL];
-#pragma unroll
-    for (int c = 0; c < CPL; ++c) {
+    float4 vv = zero4;
+    if (qa) {
       if (a.v_bf16) {
-        const uint32_t wd = m.vraw[(lc + c) >> 1];
-        vv[c] = bf16_to_f32(static_cast<uint16_t>(((lc + c) & 1) ? (wd >> 16) : (wd & 0xffff)));
+        const uint32_t w0 = m.vraw[2 * lane], w1 = m.vraw[2 * lane + 1];
+        vv = make_float4(bf16_to_f32(w0 & 0xffff), bf16_to_f32(w0 >> 16), bf16_to_f32(w1 & 0xffff),
+                         bf16_to_f32(w1 >> 16));
       } else {
-        vv[c] = __uint_as_float(m.vraw[lc + c]);
+        vv = make_float4(__uint_as_float(m.vraw[4 * lane]), __uint_as_float(m.vraw[4 * lane + 1]),
+                         __uint_as_float(m.vraw[4 * lane + 2]), __uint_as_float(m.vraw[4 * lane + 3]));
       }
     }
-    auto src_row = [&](uint16_t code, const float *prefetched) -> const float * {
-      if (code == kHzNone) return prefetched;
-      if (code == kHzInvalid) return zero_row + lc;
-      const int d = code >> 8, s = code & 0xff;
-      return &wring[(t - d) % L::NW][s][lc];
+    const float *cur_in = inW + (t % NI) * SLOTS * RS + 4 * lane;
+    auto hist_row = [&](int d, int s) { return hist + ((t - d) % NH) * SLOTS * RS + s * RS + 4 * lane; };
+    // the row a write slot starts from (before decay)
+    auto write_src = [&](int j) -> float4 {
+      const uint16_t code = m.hz[j];
+      if (code == kHzNone) return ld4(cur_in + j * RS);
+      if (code == kHzInvalid) return zero4;
+      return ld4(hist_row(code >> 8, code & 0xff));
     };
 
-    if (active) {
-      // shared prediction from the decayed rows (Fig. 2)
-      float vh[CPL] = {};
-      if (a.mode == SDM_RESID_SHARED) {
-        for (int j = 0; j < W; ++j) {
-          float x[CPL];
-          load_cols<CPL>(src_row(m.hz[j], &cur[j][lc]), x);
-          const float wj = m.ww[j];
+    // phase 2: selective decay of the written rows, partial shared prediction
+    float4 md[WPG];
+    float4 vh = zero4;
 #pragma unroll
-          for (int c = 0; c < CPL; ++c) vh[c] = fmaf(wj, al * x[c], vh[c]);
-        }
+    for (int i = 0; i < WPG; ++i) {
+      const int j = g + kNG * i;
+      md[i] = zero4;
+      if (j < W && qa) {
+        md[i] = f4_scale(al, write_src(j));
+        vh = f4_fma(m.ww[j], md[i], vh);
       }
-      // selective decay and delta write
-      for (int j = 0; j < W; ++j) {
-        const uint16_t code = m.hz[j];
-        float x[CPL];
-        load_cols<CPL>(src_row(code, &cur[j][lc]), x);
-        const float g = be * m.ww[j];
-        float nw[CPL];
-#pragma unroll
-        for (int c = 0; c < CPL; ++c) {
-          const float md = al * x[c];
-          const float resid = a.mode == SDM_RESID_SHARED ? vv[c] - vh[c]
-                              : a.mode == SDM_RESID_PERSLOT ? vv[c] - md
-                                                            : vv[c];
-          nw[c] = fmaf(g, resid, md);
-        }
-        store_cols<CPL>(&cur[j][lc], nw);
-        if (code != kHzInvalid && static_cast<unsigned>(m.iw[j]) < static_cast<unsigned>(a.N))
-          store_cols<CPL>(table + static_cast<long>(m.iw[j]) * d_v + col, nw);
-      }
-      // read after the write
-      float acc[CPL] = {};
-      const float(*rr)[TC] = rring[t % L::NR];
-      for (int j = 0; j < R; ++j) {
-        float x[CPL];
-        load_cols<CPL>(src_row(m.hz[W + j], &rr[j][lc]), x);
-        const float rj = m.wr[j];
-#pragma unroll
-        for (int c = 0; c < CPL; ++c) acc[c] = fmaf(rj, x[c], acc[c]);
-      }
-      store_cols<CPL>(a.y + (tok0 + static_cast<long>(t) * H) * d_v + col, acc);
     }
+    if (a.mode == SDM_RESID_SHARED) {
+      red1[g * 32 + lane] = vh;
+      __syncthreads();  // B2
+      vh = red1[lane];
+#pragma unroll
+      for (int w = 1; w < kNG; ++w) vh = f4_add(vh, red1[w * 32 + lane]);
+    }
+    const float4 base = a.mode == SDM_RESID_SHARED ? f4_sub(vv, vh) : vv;
+    auto new_row = [&](float4 mdj, float gj) -> float4 {
+      const float4 resid = a.mode == SDM_RESID_PERSLOT ? f4_sub(vv, mdj) : base;
+      return f4_fma(gj, resid, mdj);
+    };
+
+    // phase 3: delta write into the history ring and the table
+    float *cur_hist = hist + (t % NH) * SLOTS * RS + 4 * lane;
+#pragma unroll
+    for (int i = 0; i < WPG; ++i) {
+      const int j = g + kNG * i;
+      if (j < W && qa) {
+        const float4 nw = new_row(md[i], be * m.ww[j]);
+        st4(cur_hist + j * RS, nw);
+        const int row = m.iw[j];
+        if (m.hz[j] != kHzInvalid && static_cast<unsigned>(row) < static_cast<unsigned>(N))
+          st4(table + static_cast<long>(row) * d_v + 4 * lane, nw);
+      }
+    }
+    // read after the write
+    float4 yp = zero4;
+    const float *cur_r = inR + (t % NR) * SLOTS * RS + 4 * lane;
+#pragma unroll
+    for (int i = 0; i < WPG; ++i) {
+      const int j = g + kNG * i;
+      if (j < R && qa) {
+        const uint16_t code = m.hz[W + j];
+        float4 x;
+        if (code == kHzNone) {
+          x = ld4(cur_r + j * RS);
+        } else if (code == kHzInvalid) {
+          x = zero4;
+        } else if ((code >> 8) == 0) {
+          const int s = code & 0xff;  // written by this token: recompute its new value
+          x = new_row(f4_scale(al, write_src(s)), be * m.ww[s]);
+        } else {
+          x = ld4(hist_row(code >> 8, code & 0xff));
+        }
+        yp = f4_fma(m.wr[j], x, yp);
+      }
+    }
+    red2[(t & 1) * kNG * 32 + g * 32 + lane] = yp;
   }
   cp_async_wait<0>();
+  __syncthreads();
+  if (T > 0 && g == 0 && qa) {
+    const float4 *rd = red2 + ((T - 1) & 1) * kNG * 32;
+    float4 acc = rd[lane];
+#pragma unroll
+    for (int w = 1; w < kNG; ++w) acc = f4_add(acc, rd[w * 32 + lane]);
+    st4(a.y + (tok0 + static_cast<long>(T - 1) * H) * d_v + col0 + 4 * lane, acc);
+  }
 }
-
-struct Tuning {
-  int cpl, window, warps_per_cta;
-};
 
 int env_int(const char *name, int dflt) {
   const char *s = getenv(name);
   return (s && *s) ? atoi(s) : dflt;
 }
 
-template <int CPL, int SLOTS, int P>
-size_t warp_bytes() {
-  return ScanLayout<CPL, SLOTS, P>::kWarpBytes;
+size_t smem_dispatch(int slots, int P, int tw) {
+  return slots == 16 ? scan_smem_bytes<16>(P, tw) : scan_smem_bytes<64>(P, tw);
 }
 
-size_t warp_bytes_dispatch(int cpl, int slots, int p) {
-#define SDM_WB(C, S, PP) \
-  if (cpl == C && slots == S && p == PP) return warp_bytes<C, S, PP>();
-  SDM_WB(1, 16, 4) SDM_WB(2, 16, 4) SDM_WB(4, 16, 4) SDM_WB(1, 16, 8) SDM_WB(2, 16, 8) SDM_WB(4, 16, 8)
-  SDM_WB(1, 64, 4) SDM_WB(2, 64, 4) SDM_WB(4, 64, 4) SDM_WB(1, 64, 8) SDM_WB(2, 64, 8) SDM_WB(4, 64, 8)
-#undef SDM_WB
-  return 0;
-}
-
-template <int CPL, int SLOTS, int P>
-int launch_scan(const ScanArgs &args, int wpc, cudaStream_t st) {
-  using L = ScanLayout<CPL, SLOTS, P>;
-  const size_t smem = L::kWarpBytes * wpc;
-  auto kern = sparse_scan_kernel<CPL, SLOTS, P>;
+template <int P, int SLOTS>
+int launch_scan(const ScanArgs &args, long blocks, cudaStream_t st) {
+  const size_t smem = scan_smem_bytes<SLOTS>(P, args.tw);
+  auto kern = sparse_scan_kernel<P, SLOTS>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)
     return check_launch("sdm_scan: set shared memory");
-  const long blocks = (args.total_warps + wpc - 1) / wpc;
-  kern<<<static_cast<unsigned>(blocks), wpc * 32, smem, st>>>(args);
+  kern<<<static_cast<unsigned>(blocks), kNG * 32, smem, st>>>(args);
   return check_launch("sdm_scan: scan kernel");
 }
 
-int launch_dispatch(int cpl, int slots, int p, const ScanArgs &args, int wpc, cudaStream_t st) {
-#define SDM_LS(C, S, PP) \
-  if (cpl == C && slots == S && p == PP) return launch_scan<C, S, PP>(args, wpc, st);
-  SDM_LS(1, 16, 4) SDM_LS(2, 16, 4) SDM_LS(4, 16, 4) SDM_LS(1, 16, 8) SDM_LS(2, 16, 8) SDM_LS(4, 16, 8)
-  SDM_LS(1, 64, 4) SDM_LS(2, 64, 4) SDM_LS(4, 64, 4) SDM_LS(1, 64, 8) SDM_LS(2, 64, 8) SDM_LS(4, 64, 8)
+int launch_dispatch(int slots, int P, const ScanArgs &args, long blocks, cudaStream_t st) {
+#define SDM_LS(S, PP) \
+  if (slots == S && P == PP) return launch_scan<PP, S>(args, blocks, st);
+  SDM_LS(16, 4) SDM_LS(16, 6) SDM_LS(16, 8) SDM_LS(64, 4) SDM_LS(64, 6) SDM_LS(64, 8)
 #undef SDM_LS
-  return set_error(SDM_ERR_UNSUPPORTED, "sdm_scan: no kernel for cpl=%d slots=%d window=%d", cpl, slots, p);
+  return set_error(SDM_ERR_UNSUPPORTED, "sdm_scan: no kernel for slots=%d window=%d", slots, P);
 }
 
 }  // namespace
@@ -379,43 +402,38 @@ extern "C" int sdm_scan(float *state, const void *v, int v_dtype, const float *a
     return set_error(SDM_ERR_INVALID_ARG, "sdm_scan: workspace of %zu bytes needed", need);
   if (!aligned(workspace, 16)) return set_error(SDM_ERR_ALIGN, "sdm_scan: workspace must be 16-byte aligned");
 
-  // Tuning: columns per lane (cpl), prefetch window (tokens in flight) and
-  // warps per CTA.  Every warp runs the whole sequence, so the launch must be
-  // a single wave: pick the first (window, cpl) whose warps all fit at once.
+  // Launch shape: one CTA of 8 warps per (b, h, column tile).  Every CTA
+  // runs the whole sequence, so the grid should be one wave: split d_v into
+  // as many tiles (<= 128 columns each) as the SMs allow, then take the
+  // deepest prefetch window whose shared-memory rings fit.
   const int slots = (W <= 16 && R <= 16) ? 16 : 64;
-  int dev = 0, smem_blk = 0, smem_sm = 0, sms = 0;
+  int dev = 0, smem_blk = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&smem_blk, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  static const int kOrder[][2] = {{1, 8}, {2, 8}, {1, 4}, {2, 4}, {4, 4}, {4, 8}};
-  int cpl = 0, window = 0;
-  for (const auto &o : kOrder) {
-    const size_t wb = warp_bytes_dispatch(o[0], slots, o[1]);
-    if (wb == 0 || wb > static_cast<size_t>(smem_blk)) continue;
-    const long tiles_o = (d_v + 32 * o[0] - 1) / (32 * o[0]);
-    const long warps_o = static_cast<long>(B) * H * tiles_o;
-    const long per_sm = static_cast<long>(smem_sm - 1024) / static_cast<long>(wb);
-    if (cpl == 0) { cpl = o[0]; window = o[1]; }  // fallback: first that fits a CTA
-    if (per_sm >= 1 && warps_o <= per_sm * sms) { cpl = o[0]; window = o[1]; break; }
+  const long bh_count = static_cast<long>(B) * H;
+  const int quads = d_v / 4;
+  const int tiles_min = (quads + 31) / 32;
+  long tiles_want = sms / bh_count;
+  if (tiles_want > quads) tiles_want = quads;
+  int tiles = static_cast<int>(tiles_want > tiles_min ? tiles_want : tiles_min);
+  tiles = env_int("SDM_SCAN_TILES", tiles);
+  if (tiles < tiles_min) tiles = tiles_min;
+  if (tiles > quads) tiles = quads;
+  int tw = 4 * ((quads + tiles - 1) / tiles);
+  int window = 0;
+  const int want_window = env_int("SDM_SCAN_WINDOW", 0);
+  for (int p : {8, 6, 4}) {
+    if (want_window && p != want_window) continue;
+    if (smem_dispatch(slots, p, tw) <= static_cast<size_t>(smem_blk)) { window = p; break; }
   }
-  cpl = env_int("SDM_SCAN_CPL", cpl);
-  window = env_int("SDM_SCAN_WINDOW", window);
-  if ((cpl != 1 && cpl != 2 && cpl != 4) || (window != 4 && window != 8))
-    return set_error(SDM_ERR_INVALID_ARG, "sdm_scan: SDM_SCAN_CPL must be 1/2/4 and SDM_SCAN_WINDOW 4/8");
-  const size_t wb = warp_bytes_dispatch(cpl, slots, window);
-  if (wb == 0 || wb > static_cast<size_t>(smem_blk))
-    return set_error(SDM_ERR_SHAPE, "sdm_scan: W/R too large for shared memory");
-  const int tc = 32 * cpl;
-  const int tiles = (d_v + tc - 1) / tc;
-  const long total_warps = static_cast<long>(B) * H * tiles;
-  const int fit = static_cast<int>(static_cast<size_t>(smem_blk) / wb);
-  int wpc = env_int("SDM_SCAN_WARPS", 0);
-  if (wpc <= 0) {
-    const long per_sm = (total_warps + sms - 1) / sms;
-    wpc = static_cast<int>(per_sm < 1 ? 1 : per_sm);
+  if (window == 0) {  // narrower tiles until the smallest window fits
+    window = want_window ? want_window : 4;
+    while (tw > 4 && smem_dispatch(slots, window, tw) > static_cast<size_t>(smem_blk)) tw -= 4;
+    if (smem_dispatch(slots, window, tw) > static_cast<size_t>(smem_blk))
+      return set_error(SDM_ERR_SHAPE, "sdm_scan: W/R too large for shared memory");
   }
-  wpc = min(min(wpc, fit), 8);
+  tiles = (d_v + tw - 1) / tw;
 
   ScanArgs args;
   args.state = state;
@@ -437,8 +455,8 @@ extern "C" int sdm_scan(float *state, const void *v, int v_dtype, const float *a
   args.mode = resid_mode;
   args.v_bf16 = v_dtype == SDM_DTYPE_BF16;
   args.tiles = tiles;
+  args.tw = tw;
   args.hzs = hz_stride(W, R);
-  args.total_warps = total_warps;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const long total = static_cast<long>(B) * T * H * (W + R);
@@ -446,5 +464,5 @@ extern "C" int sdm_scan(float *state, const void *v, int v_dtype, const float *a
       idx_w, idx_r, W, R, T, H, N, window, total, static_cast<uint16_t *>(workspace), dev_err);
   int rc = check_launch("sdm_scan: hazard kernel");
   if (rc != SDM_OK) return rc;
-  return launch_dispatch(cpl, slots, window, args, wpc, st);
+  return launch_dispatch(slots, window, args, bh_count * tiles, st);
 }
