@@ -466,3 +466,4 @@ extern "C" int sdm_scan(float *state, const void *v, int v_dtype, const float *a
   if (rc != SDM_OK) return rc;
   return launch_dispatch(slots, window, args, bh_count * tiles, st);
 }
+

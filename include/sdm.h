@@ -40,6 +40,12 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#if defined(__GNUC__)
+#define SDM_API __attribute__((visibility("default")))
+#else
+#define SDM_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -67,10 +73,10 @@ extern "C" {
 #define SDM_RESID_ADDITIVE 2 /* additive write, no residual: M[i] = M~[i] + beta w_i v */
 
 /* Library version (major*10000 + minor*100 + patch). */
-int sdm_version(void);
+SDM_API int sdm_version(void);
 
 /* Text of the last error raised by a call on this host thread ("" if none). */
-const char *sdm_last_error(void);
+SDM_API const char *sdm_last_error(void);
 
 /*
  * sdm_address - product-key addressing, [SDM] "Product keys select addresses
@@ -92,14 +98,14 @@ const char *sdm_last_error(void);
  * Limits: 1 <= sqrtN <= 512, 1 <= k <= min(32, sqrtN), 1 <= W <= min(64, k*k),
  *         B*T*H < 2^31.  Pointers 4-byte aligned.
  */
-int sdm_address(const float *s1, const float *s2, int B, int T, int H, int sqrtN, int k, int W,
+SDM_API int sdm_address(const float *s1, const float *s2, int B, int T, int H, int sqrtN, int k, int W,
                 int32_t *idx_out, float *w_out, int32_t *dev_err, void *stream);
 
 /*
  * Scratch bytes sdm_scan needs for these sizes (a per-token hazard table of
  * B*T*H*(W+R) uint16 entries, rounded up to 256 bytes).
  */
-size_t sdm_scan_workspace_size(int B, int T, int H, int W, int R);
+SDM_API size_t sdm_scan_workspace_size(int B, int T, int H, int W, int R);
 
 /*
  * sdm_scan - the sparse delta-rule memory scan, [SDM] Eqs. 3-5 with the
@@ -124,7 +130,7 @@ size_t sdm_scan_workspace_size(int B, int T, int H, int W, int R);
  * Limits: 1 <= W, R <= 64; d_v % 4 == 0; N >= 1.  state and y 16-byte
  *         aligned; v, alpha, beta, idx, w 4-byte aligned.
  */
-int sdm_scan(float *state, const void *v, int v_dtype, const float *alpha, const float *beta,
+SDM_API int sdm_scan(float *state, const void *v, int v_dtype, const float *alpha, const float *beta,
              const int32_t *idx_w, const float *w_w, int W, const int32_t *idx_r, const float *w_r, int R,
              int B, int T, int H, int N, int d_v, int resid_mode, float *y, void *workspace,
              size_t workspace_bytes, int32_t *dev_err, void *stream);
@@ -133,7 +139,7 @@ int sdm_scan(float *state, const void *v, int v_dtype, const float *alpha, const
  * Scratch bytes gdn_scan needs (0 for the current kernels; kept so callers
  * can size a workspace once and keep the call stable).
  */
-size_t gdn_scan_workspace_size(int B, int T, int H, int dk, int dv, int per_channel);
+SDM_API size_t gdn_scan_workspace_size(int B, int T, int H, int dk, int dv, int per_channel);
 
 /*
  * gdn_scan - dense Gated DeltaNet (per_channel = 0) or Kimi Delta Attention
@@ -153,7 +159,7 @@ size_t gdn_scan_workspace_size(int B, int T, int H, int dk, int dv, int per_chan
  * Limits: dk in {16, 32, 64, 128}; dv % 32 == 0, dv <= 256.  state and y
  *         16-byte aligned; q, k, v 16-byte aligned (dk, dv multiples of 8).
  */
-int gdn_scan(float *state, const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
+SDM_API int gdn_scan(float *state, const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
              int per_channel, const float *beta, int B, int T, int H, int dk, int dv, float *y, void *workspace,
              size_t workspace_bytes, void *stream);
 
@@ -162,7 +168,7 @@ int gdn_scan(float *state, const uint16_t *q, const uint16_t *k, const uint16_t 
  * partitions, their gates, and the max and inverse normaliser of the row
  * softmax), rounded up to 256 bytes.
  */
-size_t sse_scan_workspace_size(int B, int T, int H, int N, int topk);
+SDM_API size_t sse_scan_workspace_size(int B, int T, int H, int N, int topk);
 
 /*
  * sse_scan - Sparse State Expansion, [SSE] Eqs. 9-14, with N routed
@@ -187,7 +193,7 @@ size_t sse_scan_workspace_size(int B, int T, int H, int N, int topk);
  *         d % 16 == 0.  state, y, k_logits, alpha 16-byte aligned; q, v
  *         16-byte aligned.
  */
-int sse_scan(float *state, const float *route_logits, int topk, const float *k_logits, const uint16_t *q,
+SDM_API int sse_scan(float *state, const float *route_logits, int topk, const float *k_logits, const uint16_t *q,
              const uint16_t *v, const float *alpha, int B, int T, int H, int N, int c, int d, float *y,
              int32_t *sel_out, void *workspace, size_t workspace_bytes, int32_t *dev_err, void *stream);
 

@@ -15,7 +15,7 @@ HEADER = os.path.join(ROOT, "include", "sdm.h")
 def _declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    names = re.findall(r"^(?:const\s+)?(?:int|size_t|char|void)\s*\*?\s*(\w+)\s*\(", text, flags=re.M)
+    names = re.findall(r"^(?:SDM_API\s+)?(?:const\s+)?(?:int|size_t|char|void)\s*\*?\s*(\w+)\s*\(", text, flags=re.M)
     return sorted(set(names))
 
 
@@ -30,7 +30,7 @@ def sdm():
 def test_header_declares_the_boundary():
     names = _declared_functions()
     for fn in ("sdm_address", "sdm_scan", "gdn_scan", "sse_scan", "sdm_version", "sdm_last_error",
-               "sdm_scan_workspace_size", "gdn_scan_workspace_size"):
+               "sdm_scan_workspace_size", "gdn_scan_workspace_size", "sse_scan_workspace_size"):
         assert fn in names
 
 
