@@ -20,6 +20,7 @@ import torch
 
 __all__ = [
     "SdmError", "lib", "library_path", "sdm_version", "sdm_address", "sdm_scan", "sdm_scan_workspace_size",
+    "sdm_scan_noalloc",
     "gdn_scan", "gdn_scan_workspace_size", "sse_scan", "sse_scan_workspace_size", "SDM_RESID_SHARED", "SDM_RESID_PERSLOT",
     "SDM_RESID_ADDITIVE", "SDM_DEVERR_INDEX_RANGE", "SDM_DEVERR_INDEX_REPEAT", "SDM_DEVERR_NONFINITE",
 ]
@@ -41,6 +42,7 @@ _SIGNATURES = {
     "sdm_address": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
     "sdm_scan_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "sdm_scan": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P, _P]),
+    "sdm_scan_noalloc": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
     "gdn_scan_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "gdn_scan": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "sse_scan_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
@@ -170,6 +172,40 @@ def sdm_scan(state, v, alpha, beta, idx_w, w_w, idx_r, w_r, resid_mode=SDM_RESID
                         w_w.data_ptr(), W, idx_r.data_ptr(), w_r.data_ptr(), R, B, T, H, N, dv, int(resid_mode),
                         y.data_ptr(), workspace.data_ptr(), workspace.numel(), _ptr(dev_err), _stream(stream))
     _check("sdm_scan", rc)
+    return y
+
+
+def sdm_scan_noalloc(state, v, alpha, beta, idx_w, w_w, idx_r, w_r, resid_mode=SDM_RESID_SHARED, y=None,
+                     dev_err=None, stream=None):
+    """sdm_scan without a workspace argument: the library keeps the scratch
+    in a fixed 8 MiB device array shared by all calls (see sdm.h).  For
+    callers that cannot allocate device memory; concurrent calls race."""
+    _req(state, "state", torch.float32)
+    if state.dim() != 4:
+        raise ValueError("state must be [B,H,N,d_v]")
+    B, H, N, dv = state.shape
+    if v.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("v must be float32 or bfloat16")
+    _req(v, "v", v.dtype)
+    T = v.shape[1]
+    _req(v, "v", v.dtype, (B, T, H, dv))
+    _req(alpha, "alpha", torch.float32, (B, T, H))
+    _req(beta, "beta", torch.float32, (B, T, H))
+    W, R = idx_w.shape[-1], idx_r.shape[-1]
+    _req(idx_w, "idx_w", torch.int32, (B, T, H, W))
+    _req(w_w, "w_w", torch.float32, (B, T, H, W))
+    _req(idx_r, "idx_r", torch.int32, (B, T, H, R))
+    _req(w_r, "w_r", torch.float32, (B, T, H, R))
+    if y is None:
+        y = torch.empty((B, T, H, dv), dtype=torch.float32, device=state.device)
+    _req(y, "y", torch.float32, (B, T, H, dv))
+    if dev_err is not None:
+        _req(dev_err, "dev_err", torch.int32)
+    vdt = SDM_DTYPE_BF16 if v.dtype == torch.bfloat16 else SDM_DTYPE_F32
+    rc = lib().sdm_scan_noalloc(state.data_ptr(), v.data_ptr(), vdt, alpha.data_ptr(), beta.data_ptr(),
+                                idx_w.data_ptr(), w_w.data_ptr(), W, idx_r.data_ptr(), w_r.data_ptr(), R, B, T, H, N,
+                                dv, int(resid_mode), y.data_ptr(), _ptr(dev_err), _stream(stream))
+    _check("sdm_scan_noalloc", rc)
     return y
 
 

@@ -16,6 +16,7 @@
 //     from that writer's slot in the shared-memory history instead.
 #include <climits>
 #include <cstdlib>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -467,3 +468,62 @@ extern "C" int sdm_scan(float *state, const void *v, int v_dtype, const float *a
   return launch_dispatch(slots, window, args, bh_count * tiles, st);
 }
 
+// ---------------------------------------------------------------------------
+// sdm_scan_noalloc: sdm_scan for callers that cannot hand over device scratch
+// memory.  The hazard table lives in a fixed, file-scope device array instead
+// of a caller workspace.  Host code cannot use the array's name as a device
+// address, so the address is looked up once per device with
+// cudaGetSymbolAddress (with that device current) and cached; the first call
+// on a device does this lookup, so make that first call before capturing any
+// stream.  Every call shares the one array: calls that can overlap on the GPU
+// (different streams, or several host threads) race on it and must be
+// serialised by the caller.  The hazard table is fully rewritten by every
+// call, so nothing has to be cleared between calls.
+// ---------------------------------------------------------------------------
+namespace sdm {
+namespace {
+constexpr size_t kStaticScratchBytes = static_cast<size_t>(8) << 20;  // 8 MiB per device
+__device__ __align__(256) unsigned char g_scan_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void *g_scratch_addr[kMaxDevices] = {};
+
+int static_scratch(void **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return set_error(SDM_ERR_CUDA, "sdm_scan_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return set_error(SDM_ERR_UNSUPPORTED, "sdm_scan_noalloc: device %d", dev);
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_scan_scratch);
+    if (e != cudaSuccess || !p)
+      return set_error(SDM_ERR_CUDA, "sdm_scan_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return SDM_OK;
+}
+}  // namespace
+}  // namespace sdm
+
+extern "C" int sdm_scan_noalloc(float *state, const void *v, int v_dtype, const float *alpha, const float *beta,
+                                const int32_t *idx_w, const float *w_w, int W, const int32_t *idx_r,
+                                const float *w_r, int R, int B, int T, int H, int N, int d_v, int resid_mode,
+                                float *y, int32_t *dev_err, void *stream) {
+  if (B < 0 || T < 0 || H < 0 || W < 1 || W > 64 || R < 1 || R > 64)
+    return set_error(SDM_ERR_SHAPE, "sdm_scan_noalloc: bad sizes");
+  const size_t need = sdm_scan_workspace_size(B, T, H, W, R);
+  if (need > sdm::kStaticScratchBytes)
+    return set_error(SDM_ERR_SHAPE,
+                     "sdm_scan_noalloc: B*T*H*(W+R) too large: needs %zu bytes of scratch, the static array holds "
+                     "%zu; use sdm_scan with a workspace",
+                     need, sdm::kStaticScratchBytes);
+  if (B == 0 || T == 0 || H == 0) return SDM_OK;
+  void *scratch = nullptr;
+  const int rc = sdm::static_scratch(&scratch);
+  if (rc != SDM_OK) return rc;
+  return sdm_scan(state, v, v_dtype, alpha, beta, idx_w, w_w, W, idx_r, w_r, R, B, T, H, N, d_v, resid_mode, y,
+                  scratch, sdm::kStaticScratchBytes, dev_err, stream);
+}

@@ -136,6 +136,35 @@ SDM_API int sdm_scan(float *state, const void *v, int v_dtype, const float *alph
              size_t workspace_bytes, int32_t *dev_err, void *stream);
 
 /*
+ * sdm_scan_noalloc - sdm_scan for callers that cannot give the library device
+ * scratch memory.  The papers have no counterpart: this is an interface
+ * convenience of this library, not a step of the method.
+ *
+ * Some callers cannot call cudaMalloc at the point where they run the scan:
+ * hosts that hand out all device memory from their own pool and forbid raw
+ * allocations once running (an allocation can synchronise the device and
+ * fragments the pool), or plug-in code that receives only its input and
+ * output buffers.  This entry point takes the same arguments as sdm_scan
+ * minus the workspace, and keeps its scratch (the per-token hazard table) in
+ * one fixed 8 MiB array in device memory that every GPU loading this library
+ * holds until the process exits.  It allocates nothing and frees nothing.
+ *
+ * Limit: sdm_scan_workspace_size(B,T,H,W,R) <= 8 MiB, i.e.
+ * B*T*H*(W+R rounded up to even) <= 4 Mi entries (B*T*H <= 131072 at
+ * W = R = 16); larger calls return SDM_ERR_SHAPE and launch nothing.
+ * Set-up: the first call on a device looks up the array's device address
+ * (with that device current); make that first call before any stream capture.
+ * Sharing: all calls in the process share the one array, which keeps the last
+ * call's contents (nothing in it needs clearing: every call rewrites what it
+ * reads).  Calls that can overlap on the GPU - on different streams, or from
+ * several host threads - race on it; serialise them.
+ */
+SDM_API int sdm_scan_noalloc(float *state, const void *v, int v_dtype, const float *alpha, const float *beta,
+                     const int32_t *idx_w, const float *w_w, int W, const int32_t *idx_r, const float *w_r, int R,
+                     int B, int T, int H, int N, int d_v, int resid_mode, float *y, int32_t *dev_err,
+                     void *stream);
+
+/*
  * Scratch bytes gdn_scan needs (0 for the current kernels; kept so callers
  * can size a workspace once and keep the call stable).
  */
