@@ -102,8 +102,10 @@ SDM_API int sdm_address(const float *s1, const float *s2, int B, int T, int H, i
                 int32_t *idx_out, float *w_out, int32_t *dev_err, void *stream);
 
 /*
- * Scratch bytes sdm_scan needs for these sizes (a per-token hazard table of
- * B*T*H*(W+R) uint16 entries, rounded up to 256 bytes).
+ * Scratch bytes sdm_scan needs for these sizes: one packed record per
+ * token-head (its slot ids, weights, gates and where each slot's row is read
+ * from), 336 bytes when W, R <= 16 and 1296 bytes otherwise, rounded up to
+ * 256.  0 for invalid sizes.
  */
 SDM_API size_t sdm_scan_workspace_size(int B, int T, int H, int W, int R);
 
@@ -124,11 +126,13 @@ SDM_API size_t sdm_scan_workspace_size(int B, int T, int H, int W, int R);
  * y         : fp32 [B,T,H,d_v].
  * workspace : device scratch of at least sdm_scan_workspace_size(B,T,H,W,R)
  *             bytes, 16-byte aligned; contents need no initialisation.
+ *             Calls sharing one workspace must not overlap on the GPU.
  * dev_err   : optional; SDM_DEVERR_INDEX_RANGE (that slot is read as zero and
  *             not written) and SDM_DEVERR_INDEX_REPEAT (result for that token
  *             unspecified, memory-safe).
- * Limits: 1 <= W, R <= 64; d_v % 4 == 0; N >= 1.  state and y 16-byte
- *         aligned; v, alpha, beta, idx, w 4-byte aligned.
+ * Limits: 1 <= W, R <= 64; d_v % 4 == 0; N >= 1; B*T*H < 2e9.  state, y
+ *         and fp32 v 16-byte aligned; bf16 v 8-byte; alpha, beta, idx, w
+ *         4-byte.
  */
 SDM_API int sdm_scan(float *state, const void *v, int v_dtype, const float *alpha, const float *beta,
              const int32_t *idx_w, const float *w_w, int W, const int32_t *idx_r, const float *w_r, int R,
@@ -145,13 +149,13 @@ SDM_API int sdm_scan(float *state, const void *v, int v_dtype, const float *alph
  * allocations once running (an allocation can synchronise the device and
  * fragments the pool), or plug-in code that receives only its input and
  * output buffers.  This entry point takes the same arguments as sdm_scan
- * minus the workspace, and keeps its scratch (the per-token hazard table) in
- * one fixed 8 MiB array in device memory that every GPU loading this library
+ * minus the workspace, and keeps its scratch (the per-token records) in one
+ * fixed 32 MiB array in device memory that every GPU loading this library
  * holds until the process exits.  It allocates nothing and frees nothing.
  *
- * Limit: sdm_scan_workspace_size(B,T,H,W,R) <= 8 MiB, i.e.
- * B*T*H*(W+R rounded up to even) <= 4 Mi entries (B*T*H <= 131072 at
- * W = R = 16); larger calls return SDM_ERR_SHAPE and launch nothing.
+ * Limit: sdm_scan_workspace_size(B,T,H,W,R) <= 32 MiB, i.e. B*T*H <= 99864
+ * when W, R <= 16 (336 bytes per token-head) and B*T*H <= 25890 when either
+ * is larger (1296 bytes); larger calls return SDM_ERR_SHAPE and launch nothing.
  * Set-up: the first call on a device looks up the array's device address
  * (with that device current); make that first call before any stream capture.
  * Sharing: all calls in the process share the one array, which keeps the last

@@ -42,9 +42,10 @@ def test_library_exports_every_declared_symbol(sdm):
 
 def test_version_and_workspace(sdm):
     assert sdm.sdm_version() >= 10000
-    # one uint16 hazard code per (token, slot), rows padded to an even count
-    assert sdm.sdm_scan_workspace_size(8, 4096, 2, 16, 16) == 8 * 4096 * 2 * 32 * 2
-    assert sdm.sdm_scan_workspace_size(1, 3, 1, 3, 4) == 256
+    # one packed record per token-head: 336 bytes for W, R <= 16, else 1296
+    assert sdm.sdm_scan_workspace_size(8, 4096, 2, 16, 16) == 8 * 4096 * 2 * 336
+    assert sdm.sdm_scan_workspace_size(1, 3, 1, 3, 4) == 1024
+    assert sdm.sdm_scan_workspace_size(1, 1, 1, 17, 4) == 1536
     assert sdm.sdm_scan_workspace_size(0, 3, 1, 3, 4) == 0
 
 
@@ -84,6 +85,7 @@ def test_scan_rejects_bad_arguments(sdm):
     assert call(vdt=7) == sdm.SDM_ERR_UNSUPPORTED
     assert call(mode=3) == sdm.SDM_ERR_UNSUPPORTED
     assert call(state=A + 4) == sdm.SDM_ERR_ALIGN
+    assert call(v=A + 4) == sdm.SDM_ERR_ALIGN                 # bf16 v needs 8-byte alignment
     assert call(wsb=16) == sdm.SDM_ERR_INVALID_ARG            # workspace too small
     assert call(ws=None) == sdm.SDM_ERR_INVALID_ARG
     assert call(ws=B_ + 8) == sdm.SDM_ERR_ALIGN

@@ -65,7 +65,7 @@ def test_noalloc_matches_workspace_scan_on_two_calls_in_a_row():
 def test_noalloc_rejects_sizes_beyond_its_array():
     sdm = need_gpu()
     L = sdm.lib()
-    # B*T*H*(W+R) uint16 entries beyond 8 MiB: refused before any launch
+    # 64*8192*2 token-head records of 336 bytes exceed the 32 MiB array: refused before any launch
     rc = L.sdm_scan_noalloc(1 << 20, 1 << 20, 1, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 16, 1 << 20, 1 << 20, 16,
                             64, 8192, 2, 57600, 960, 0, 1 << 20, None, None)
     assert rc == sdm.SDM_ERR_SHAPE
