@@ -30,11 +30,11 @@
 namespace sdm {
 namespace {
 
-// source codes of a slot (see above)
-constexpr uint16_t kSrcIncoming = 0x8000;   // the prefetched copy of this slot's row
-constexpr uint16_t kSrcZero = 0xffff;       // padding or out-of-range index: zero row, no store
-constexpr uint16_t kSrcRecompute = 0x4000;  // | s: read of write slot s of the same token
-// otherwise: row ((t - d) % (P + 1)) * SLOTS + s of the history ring
+// A slot's source is stored as the number of a 128-byte row (32 floats) of
+// the warp's shared memory, numbered across the rings of ScanLayout: the
+// prefetched copy, a post-write history row or the zero row.  A read of a
+// row the same token writes is kRecompute | write slot.
+constexpr uint16_t kRecompute = 0x8000;
 
 // Packed per-token record, 16-byte aligned.  Slot positions are permuted so
 // lane subgroup r finds its 2*RPL slots (RPL write then RPL read) contiguous:
@@ -54,15 +54,38 @@ __host__ __device__ constexpr size_t rec_bytes() { return sizeof(TokenRec<SLOTS>
 
 __host__ __device__ inline int pick_slots(int W, int R) { return (W <= 16 && R <= 16) ? 16 : 64; }
 
+template <int P, int SLOTS>
+struct ScanLayout {
+  static constexpr int NI = P + 1;      // incoming rows: P in flight + current
+  static constexpr int NH = P + 1;      // post-write history: current + P back
+  static constexpr int NM = 2 * P + 1;  // records: needed from t-P (row issue) to t
+  // 128-byte row numbers of the rings
+  static constexpr int kRowW = 0;                    // incoming write rows [NI][SLOTS]
+  static constexpr int kRowH = NI * SLOTS;           // history [NH][SLOTS]
+  static constexpr int kRowR = (NI + NH) * SLOTS;    // incoming read rows [NI][SLOTS]
+  static constexpr int kRowZero = (2 * NI + NH) * SLOTS;
+  static constexpr size_t kRecOff = static_cast<size_t>(kRowZero + 1) * 128;
+  static constexpr size_t kVOff = kRecOff + NM * rec_bytes<SLOTS>();
+  static constexpr size_t kWarpBytes = kVOff + NM * 128;  // 32 columns of v per record, fp32 or bf16
+  static_assert(kRowZero < kRecompute, "row numbers must stay below the recompute flag");
+};
+
+
 // ---------------------------------------------------------------------------
-// Prepass: one thread per (token, record position).
+// Prepass: one thread per (token, record position).  Resolves, for every
+// slot, which shared-memory row the scan warp reads it from at token t:
+// write slot j -> its prefetched copy, or the history row of the most recent
+// earlier token (within the prefetch window P) that wrote the same table row;
+// read slot j -> likewise, or kRecompute | s when write slot s of the same
+// token holds the row; out-of-range ids and padding -> the zero row.
 // ---------------------------------------------------------------------------
-template <int SLOTS>
+template <int P, int SLOTS>
 __global__ void record_kernel(const int32_t *__restrict__ idx_w, const float *__restrict__ w_w,
                               const int32_t *__restrict__ idx_r, const float *__restrict__ w_r,
                               const float *__restrict__ alpha, const float *__restrict__ beta, int W, int R, int T,
-                              int H, int N, int window, long total, TokenRec<SLOTS> *__restrict__ rec,
+                              int H, int N, long total, TokenRec<SLOTS> *__restrict__ rec,
                               int32_t *__restrict__ dev_err) {
+  using L = ScanLayout<P, SLOTS>;
   constexpr int RPL = SLOTS / 4;
   const long tid = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (tid >= total) return;
@@ -82,35 +105,36 @@ __global__ void record_kernel(const int32_t *__restrict__ idx_w, const float *__
   if (j >= n) {  // padding slot
     o.idx[pos] = -1;
     o.w[pos] = 0.f;
-    o.src[pos] = kSrcZero;
+    o.src[pos] = static_cast<uint16_t>(L::kRowZero);
     return;
   }
   const int my = is_w ? idx_w[tok * W + j] : idx_r[tok * R + j];
   o.idx[pos] = my;
   o.w[pos] = is_w ? w_w[tok * W + j] : w_r[tok * R + j];
   int err = 0;
-  uint16_t code = kSrcIncoming;
+  int code = is_w ? L::kRowW + (t % L::NI) * SLOTS + j : L::kRowR + (t % L::NI) * SLOTS + j;
   if (my < 0 || my >= N) {
-    code = kSrcZero;
+    code = L::kRowZero;
     err |= SDM_DEVERR_INDEX_RANGE;
   } else {
     if (is_w) {
       for (int jj = 0; jj < j; ++jj)
         if (idx_w[tok * W + jj] == my) err |= SDM_DEVERR_INDEX_REPEAT;
     }
-    const int dmax = min(window, t);
-    for (int d = is_w ? 1 : 0; d <= dmax && code == kSrcIncoming; ++d) {
+    const int dmax = min(P, t);
+    bool found = false;
+    for (int d = is_w ? 1 : 0; d <= dmax && !found; ++d) {
       const int32_t *lst = idx_w + (tok - static_cast<long>(d) * H) * W;
       for (int s = W - 1; s >= 0; --s) {
         if (lst[s] == my) {
-          code = d == 0 ? static_cast<uint16_t>(kSrcRecompute | s)
-                        : static_cast<uint16_t>(((t - d) % (window + 1)) * SLOTS + s);
+          code = d == 0 ? (kRecompute | s) : L::kRowH + ((t - d) % L::NH) * SLOTS + s;
+          found = true;
           break;
         }
       }
     }
   }
-  o.src[pos] = code;
+  o.src[pos] = static_cast<uint16_t>(code);
   if (err && dev_err) atomicOr(dev_err, err);
 }
 
@@ -124,18 +148,6 @@ struct ScanArgs {
   float *y;
   int T, H, N, d_v, v_bf16, tiles;
   long total_warps;
-};
-
-template <int P, int SLOTS>
-struct ScanLayout {
-  static constexpr int NI = P + 1;      // incoming rows: P in flight + current
-  static constexpr int NH = P + 1;      // post-write history: current + P back
-  static constexpr int NM = 2 * P + 1;  // records: needed from t-P (row issue) to t
-  static constexpr size_t kSlotBytes = static_cast<size_t>(SLOTS) * 32 * sizeof(float);
-  static constexpr size_t kRecOff = 3 * NI * kSlotBytes;  // inW, hist, inR rings
-  static constexpr size_t kVOff = kRecOff + NM * rec_bytes<SLOTS>();
-  static constexpr size_t kZeroOff = kVOff + NM * 128;      // 32 columns of v per record, fp32 or bf16
-  static constexpr size_t kWarpBytes = kZeroOff + 128;      // one all-zero 32-float row
 };
 
 __device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
@@ -163,9 +175,8 @@ __global__ void __launch_bounds__(128) sparse_scan_kernel(const ScanArgs a) {
   using L = ScanLayout<P, SLOTS>;
   using Rec = TokenRec<SLOTS>;
   constexpr int RPL = SLOTS / 4;
-  constexpr int SLOT_F = SLOTS * 32;  // floats per ring slot
+  constexpr int SLOT_B = SLOTS * 128;  // bytes per ring slot
   constexpr int REC_CHUNKS = static_cast<int>(sizeof(Rec) / 16);
-  static_assert(REC_CHUNKS + 8 <= 32 || SLOTS == 64, "one copy per lane for the 16-slot record");
   extern __shared__ __align__(16) unsigned char smem_raw[];
 
   const int lane = threadIdx.x & 31;
@@ -176,104 +187,114 @@ __global__ void __launch_bounds__(128) sparse_scan_kernel(const ScanArgs a) {
   const long bh = gw / a.tiles;
   const int h = static_cast<int>(bh % a.H);
   const long b = bh / a.H;
-  const int T = a.T, H = a.H, d_v = a.d_v;
+  const int T = a.T, d_v = a.d_v;
   const int q = lane & 7, r = lane >> 3;
   const int col = tile * 32 + 4 * q;
   const bool active = col < d_v;
 
   unsigned char *base = smem_raw + static_cast<size_t>(wib) * L::kWarpBytes;
-  float *inW = reinterpret_cast<float *>(base);
-  float *hist = inW + L::NI * SLOT_F;
-  float *inR = hist + L::NH * SLOT_F;
+  unsigned char *lbase = base + 16 * q;  // this lane's quad inside any 128-byte row
   Rec *recs = reinterpret_cast<Rec *>(base + L::kRecOff);
   uint32_t *vbuf = reinterpret_cast<uint32_t *>(base + L::kVOff);  // [NM][32 words]
-  float *zrow = reinterpret_cast<float *>(base + L::kZeroOff);
-  zrow[lane] = 0.f;
+  reinterpret_cast<float *>(base + L::kRowZero * 128)[lane] = 0.f;
+  auto row_ptr = [&](int row) -> const float * {
+    return reinterpret_cast<const float *>(lbase + min(row, L::kRowZero) * 128);
+  };
 
-  float *table = a.state + bh * static_cast<long>(a.N) * d_v + col;  // this lane's quad of row 0
-  const long tok0 = b * T * H + h;
-  const Rec *grec = static_cast<const Rec *>(a.rec);
-  const int lq = 4 * q;  // this lane's column offset inside a 32-float ring row
+  const size_t rowbytes = static_cast<size_t>(d_v) * sizeof(float);
+  const unsigned char *table = reinterpret_cast<const unsigned char *>(a.state + bh * static_cast<long>(a.N) * d_v + col);
+  unsigned char *table_w = reinterpret_cast<unsigned char *>(a.state + bh * static_cast<long>(a.N) * d_v + col);
+  const long tok0 = b * T * a.H + h;
+  const long tok_stride = a.H;
 
-  // per token: the record (REC_CHUNKS x 16 B) and 32 columns of v
-  // (8 x 8 B of bf16 or 8 x 16 B of fp32); one copy per lane
-  auto issue_meta = [&](int t) {
-    const long tok = tok0 + static_cast<long>(t) * H;
-    const int slot = t % L::NM;
+  // per-token global sources (this token's record and v), advanced one token
+  // at a time; chunk c < REC_CHUNKS is 16 bytes of the record, the next 8 are
+  // the v columns 4vc .. 4vc+3 of this tile
+  const int esz = a.v_bf16 ? 2 : 4;
+  const unsigned char *rec_tok = reinterpret_cast<const unsigned char *>(static_cast<const Rec *>(a.rec) + tok0);
+  const unsigned char *v_tok = static_cast<const unsigned char *>(a.v) + (tok0 * d_v + tile * 32) * esz;
+  const long rec_step = tok_stride * static_cast<long>(sizeof(Rec));
+  const long v_step = tok_stride * d_v * esz;
+  int meta_slot = 0;  // ring slot of the next record to fetch
+  auto issue_meta = [&]() {
     for (int c = lane; c < REC_CHUNKS + 8; c += 32) {
       if (c < REC_CHUNKS) {
-        cp_async<16>(reinterpret_cast<unsigned char *>(recs + slot) + 16 * c,
-                     reinterpret_cast<const unsigned char *>(grec + tok) + 16 * c);
+        cp_async<16>(reinterpret_cast<unsigned char *>(recs + meta_slot) + 16 * c, rec_tok + 16 * c);
       } else {
-        const int vc = c - REC_CHUNKS;  // columns 4vc .. 4vc+3
+        const int vc = c - REC_CHUNKS;
         if (tile * 32 + 4 * vc < d_v) {
-          if (a.v_bf16)
-            cp_async<8>(vbuf + slot * 32 + 2 * vc, static_cast<const uint16_t *>(a.v) + tok * d_v + tile * 32 + 4 * vc);
-          else
-            cp_async<16>(vbuf + slot * 32 + 4 * vc, static_cast<const float *>(a.v) + tok * d_v + tile * 32 + 4 * vc);
+          unsigned char *dst = reinterpret_cast<unsigned char *>(vbuf + meta_slot * 32) + vc * 4 * esz;
+          if (a.v_bf16) cp_async<8>(dst, v_tok + vc * 8);
+          else cp_async<16>(dst, v_tok + vc * 16);
         }
       }
     }
+    rec_tok += rec_step;
+    v_tok += v_step;
+    meta_slot = meta_slot + 1 == L::NM ? 0 : meta_slot + 1;
   };
-  // the row quads this lane consumes: write slots r+4k into inW, read slots into inR
-  auto issue_rows = [&](int t) {
-    if (!active) return;
-    const Rec &m = recs[t % L::NM];
-    int id[2 * RPL];
+  // the row quads this lane consumes: write slots r+4k and read slots r+4k
+  int fetch_rec = 0, fetch_ring = 0;  // record slot and row-ring slot of the next token to fetch
+  auto issue_rows = [&]() {
+    if (active) {
+      const Rec &m = recs[fetch_rec];
+      const int4 *ip = reinterpret_cast<const int4 *>(m.idx + r * 2 * RPL);
+      unsigned char *dw = lbase + (L::kRowW * 128 + fetch_ring * SLOT_B);
+      unsigned char *dr = lbase + (L::kRowR * 128 + fetch_ring * SLOT_B);
 #pragma unroll
-    for (int k = 0; k < 2 * RPL; k += 4) {
-      const int4 x = *reinterpret_cast<const int4 *>(m.idx + r * 2 * RPL + k);
-      id[k] = x.x; id[k + 1] = x.y; id[k + 2] = x.z; id[k + 3] = x.w;
-    }
-    float *dw = inW + (t % L::NI) * SLOT_F + lq;
-    float *dr = inR + (t % L::NI) * SLOT_F + lq;
+      for (int k4 = 0; k4 < 2 * RPL / 4; ++k4) {
+        const int4 x = ip[k4];
+        const int ids[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-    for (int k = 0; k < 2 * RPL; ++k) {
-      const int i = id[k];
-      const int j = r + 4 * (k < RPL ? k : k - RPL);
-      if (static_cast<unsigned>(i) < static_cast<unsigned>(a.N))
-        cp_async<16>((k < RPL ? dw : dr) + j * 32, table + static_cast<long>(i) * d_v);
+        for (int e = 0; e < 4; ++e) {
+          const int k = 4 * k4 + e;
+          const int j = r + 4 * (k < RPL ? k : k - RPL);
+          if (static_cast<unsigned>(ids[e]) < static_cast<unsigned>(a.N))
+            cp_async<16>((k < RPL ? dw : dr) + j * 128, table + static_cast<size_t>(ids[e]) * rowbytes);
+        }
+      }
     }
+    fetch_rec = fetch_rec + 1 == L::NM ? 0 : fetch_rec + 1;
+    fetch_ring = fetch_ring + 1 == L::NI ? 0 : fetch_ring + 1;
   };
 
   // prologue: records of tokens [0, P), then P groups (rows of j, record of j+P)
-  for (int t = 0; t < P && t < T; ++t) issue_meta(t);
+  for (int t = 0; t < P && t < T; ++t) issue_meta();
   cp_async_commit();
   cp_async_wait<0>();
   __syncwarp();
   for (int j = 0; j < P; ++j) {
-    if (j + P < T) issue_meta(j + P);
-    if (j < T) issue_rows(j);
+    if (j + P < T) issue_meta();
+    if (j < T) issue_rows();
     cp_async_commit();
   }
 
+  float *yp_out = a.y + tok0 * d_v + col;
+  const long y_step = tok_stride * d_v;
   const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  int cur_rec = 0, cur_ring = 0;
   for (int t = 0; t < T; ++t) {
     cp_async_wait<P - 1>();
     __syncwarp();
-    if (t + 2 * P < T) issue_meta(t + 2 * P);
-    if (t + P < T) issue_rows(t + P);
+    if (t + 2 * P < T) issue_meta();
+    if (t + P < T) issue_rows();
     cp_async_commit();
 
-    const Rec &m = recs[t % L::NM];
+    const Rec &m = recs[cur_rec];
     const float al = m.alpha, be = m.beta;
-    const uint32_t *vw = vbuf + (t % L::NM) * 32;
+    const uint32_t *vw = vbuf + cur_rec * 32;
     float4 vv;
     if (a.v_bf16) {
-      const uint32_t w0 = vw[2 * q], w1 = vw[2 * q + 1];
-      vv = make_float4(bf16_to_f32(w0 & 0xffff), bf16_to_f32(w0 >> 16), bf16_to_f32(w1 & 0xffff),
-                       bf16_to_f32(w1 >> 16));
+      const uint2 w2 = *reinterpret_cast<const uint2 *>(vw + 2 * q);
+      vv = make_float4(bf16_to_f32(w2.x & 0xffff), bf16_to_f32(w2.x >> 16), bf16_to_f32(w2.y & 0xffff),
+                       bf16_to_f32(w2.y >> 16));
     } else {
-      vv = make_float4(__uint_as_float(vw[4 * q]), __uint_as_float(vw[4 * q + 1]), __uint_as_float(vw[4 * q + 2]),
-                       __uint_as_float(vw[4 * q + 3]));
+      vv = *reinterpret_cast<const float4 *>(vw + 4 * q);
     }
-    const float *cur_w = inW + (t % L::NI) * SLOT_F + lq;
-    const float *cur_r = inR + (t % L::NI) * SLOT_F + lq;
-    float *cur_h = hist + (t % L::NH) * SLOT_F + lq;
-    // this lane's 2*RPL slots: ids, weights and source codes, vector loads
+    // this lane's slots: ids (write), weights and source rows, vector loads
     int my_idx[RPL];
     float my_w[2 * RPL];
-    uint16_t my_src[2 * RPL];
+    int my_src[2 * RPL];
 #pragma unroll
     for (int k = 0; k < RPL; k += 4) {
       const int4 x = *reinterpret_cast<const int4 *>(m.idx + r * 2 * RPL + k);
@@ -290,37 +311,30 @@ __global__ void __launch_bounds__(128) sparse_scan_kernel(const ScanArgs a) {
       const uint32_t u[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        my_src[k + 2 * e] = static_cast<uint16_t>(u[e] & 0xffff);
-        my_src[k + 2 * e + 1] = static_cast<uint16_t>(u[e] >> 16);
+        my_src[k + 2 * e] = static_cast<int>(u[e] & 0xffff);
+        my_src[k + 2 * e + 1] = static_cast<int>(u[e] >> 16);
       }
     }
-    // shared-memory address of the row a slot starts from (branch-free):
-    // the prefetched copy, a history row, or the zero row
-    auto row_addr = [&](uint16_t code, const float *incoming) -> const float * {
-      const float *hrow = hist + (code < L::NH * SLOTS ? code : 0) * 32 + lq;
-      return code == kSrcIncoming ? incoming : (code == kSrcZero ? zrow + lq : hrow);
-    };
 
     // selective decay of the written rows and the shared prediction (Fig. 2)
     float4 md[RPL];
     float4 vh = zero4;
 #pragma unroll
-    for (int k = 0; k < RPL; ++k) md[k] = ld4(row_addr(my_src[k], cur_w + (r + 4 * k) * 32));
-#pragma unroll
-    for (int k = 0; k < RPL; ++k) {
-      md[k] = mul4(al, md[k]);
-      if (MODE == SDM_RESID_SHARED) vh = fma4(my_w[k], md[k], vh);
-    }
-    // read rows (prefetched, history, or zero); reads of a row this token
-    // writes are patched below
+    for (int k = 0; k < RPL; ++k) md[k] = ld4(row_ptr(my_src[k]));
+    // read rows; a read of a row this token writes is patched below
     float4 xr[RPL];
     bool recomp = false;
 #pragma unroll
     for (int k = 0; k < RPL; ++k) {
-      const uint16_t code = my_src[RPL + k];
-      const bool rc = code != kSrcIncoming && code != kSrcZero && (code & kSrcRecompute);
+      const int code = my_src[RPL + k];
+      const bool rc = (code & kRecompute) != 0;
       recomp |= rc;
-      xr[k] = ld4(rc ? zrow + lq : row_addr(code, cur_r + (r + 4 * k) * 32));
+      xr[k] = ld4(row_ptr(rc ? L::kRowZero : code));
+    }
+#pragma unroll
+    for (int k = 0; k < RPL; ++k) {
+      md[k] = mul4(al, md[k]);
+      if (MODE == SDM_RESID_SHARED) vh = fma4(my_w[k], md[k], vh);
     }
     float4 base4 = vv;
     if (MODE == SDM_RESID_SHARED) base4 = sub4(vv, xsum4(vh));
@@ -329,24 +343,24 @@ __global__ void __launch_bounds__(128) sparse_scan_kernel(const ScanArgs a) {
     };
 
     // delta write: history ring (forwarding source) and the table in HBM
+    unsigned char *hslot = lbase + (L::kRowH * 128 + cur_ring * SLOT_B);
 #pragma unroll
     for (int k = 0; k < RPL; ++k) {
       const float4 nw = new_row(md[k], be * my_w[k]);
-      st4(cur_h + (r + 4 * k) * 32, nw);
+      st4(reinterpret_cast<float *>(hslot + (r + 4 * k) * 128), nw);
       const int i = my_idx[k];
       if (active && static_cast<unsigned>(i) < static_cast<unsigned>(a.N))
-        st4(table + static_cast<long>(i) * d_v, nw);
+        st4(reinterpret_cast<float *>(table_w + static_cast<size_t>(i) * rowbytes), nw);
     }
     // rare: a read of a row written by this same token -> recompute its new value
     if (__any_sync(kFull, recomp)) {
 #pragma unroll
       for (int k = 0; k < RPL; ++k) {
-        const uint16_t code = my_src[RPL + k];
-        if (code != kSrcIncoming && code != kSrcZero && (code & kSrcRecompute)) {
-          const int s = code & 0xff;                     // write slot s of this token
-          const int ps = (s & 3) * 2 * RPL + (s >> 2);   // its record position
-          const float4 x0 = ld4(row_addr(m.src[ps], cur_w + s * 32));
-          xr[k] = new_row(mul4(al, x0), be * m.w[ps]);
+        const int code = my_src[RPL + k];
+        if (code & kRecompute) {
+          const int sw = code & 0xff;                     // write slot of this token
+          const int ps = (sw & 3) * 2 * RPL + (sw >> 2);  // its record position
+          xr[k] = new_row(mul4(al, ld4(row_ptr(m.src[ps]))), be * m.w[ps]);
         }
       }
     }
@@ -355,7 +369,10 @@ __global__ void __launch_bounds__(128) sparse_scan_kernel(const ScanArgs a) {
 #pragma unroll
     for (int k = 0; k < RPL; ++k) yp = fma4(my_w[RPL + k], xr[k], yp);
     yp = xsum4(yp);
-    if (r == 0 && active) st4(a.y + (tok0 + static_cast<long>(t) * H) * d_v + col, yp);
+    if (r == 0 && active) st4(yp_out, yp);
+    yp_out += y_step;
+    cur_rec = cur_rec + 1 == L::NM ? 0 : cur_rec + 1;
+    cur_ring = cur_ring + 1 == L::NI ? 0 : cur_ring + 1;
   }
   cp_async_wait<0>();
 }
@@ -472,12 +489,14 @@ chosen:
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const long total = static_cast<long>(B) * T * H * 2 * slots;
   const unsigned rblocks = static_cast<unsigned>((total + 255) / 256);
-  if (slots == 16)
-    record_kernel<16><<<rblocks, 256, 0, st>>>(idx_w, w_w, idx_r, w_r, alpha, beta, W, R, T, H, N, window, total,
-                                               static_cast<TokenRec<16> *>(workspace), dev_err);
-  else
-    record_kernel<64><<<rblocks, 256, 0, st>>>(idx_w, w_w, idx_r, w_r, alpha, beta, W, R, T, H, N, window, total,
-                                               static_cast<TokenRec<64> *>(workspace), dev_err);
+#define SDM_REC(PP, S)                                                                                          \
+  record_kernel<PP, S><<<rblocks, 256, 0, st>>>(idx_w, w_w, idx_r, w_r, alpha, beta, W, R, T, H, N, total, \
+                                                static_cast<TokenRec<S> *>(workspace), dev_err)
+  if (slots == 16 && window == 4) SDM_REC(4, 16);
+  else if (slots == 16 && window == 6) SDM_REC(6, 16);
+  else if (slots == 16 && window == 8) SDM_REC(8, 16);
+  else SDM_REC(4, 64);
+#undef SDM_REC
   int rc = check_launch("sdm_scan: record kernel");
   if (rc != SDM_OK) return rc;
 
