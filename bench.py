@@ -167,7 +167,7 @@ class OracleSampler:
 
 # ---------------------------------------------------------------- workloads
 class Workload:
-    def __init__(self, name: str, mode: str):
+    def __init__(self, name: str, mode: str, batch: int = 0):
         import synth
         self.name = name
         self.mode = {"shared": 0, "perslot": 1}[mode]
@@ -183,6 +183,8 @@ class Workload:
             self.kind, self.shape = "sse", synth.SSE_PART
         else:
             raise SystemExit(f"unknown workload {name}")
+        if batch:
+            self.shape = self.shape.with_(B=batch)
         sh = self.shape
         self.tokens = sh.B * sh.T
 
@@ -350,7 +352,7 @@ def run_ours(args, rank, world, local_rank, sampler):
 
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
-    wl = Workload(args.workload, args.mode)
+    wl = Workload(args.workload, args.mode, args.batch)
     inp = wl.inputs(seed=rank)
     cpu = None
     if sampler is not None:
@@ -467,7 +469,7 @@ def run_ours(args, rank, world, local_rank, sampler):
 
 def run_reference(args, rank, world):
     """The fp64 CPU oracle on this host's cores, on a bounded sample."""
-    wl = Workload(args.workload, args.mode)
+    wl = Workload(args.workload, args.mode, args.batch)
     inp = wl.inputs(seed=0)
     cores = args.cpu_cores or min(os.cpu_count() or 1, 16)
     nseq = min(cores, wl.shape.B * wl.shape.H)
@@ -504,6 +506,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=0, help="tokens per sampled sequence for the oracle")
     ap.add_argument("--cpu-cores", type=int, default=0)
+    ap.add_argument("--batch", type=int, default=0, help="override B (small cases for profiling only)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
