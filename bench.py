@@ -38,7 +38,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM traffic of one sparse_scan launch from an ncu capture, valid only while
 # the kernel source hashes to the recorded digest (see profiles/).
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # dram__bytes_read.sum + dram__bytes_write.sum of one full-size launch
+    # (8.01 GB + 4.19 GB), profiles/sparse_scan_1.4b_layer.md
+    ("sdm_14b_layer", "sdm"): {"bytes": 12.20e9, "digest": "ed6ed4049bda"},
+}
 
 
 def _src_digest(name: str) -> str:

@@ -1,16 +1,17 @@
 // address.cu - product-key addressing (Sparse Delta Memory deck, "Product keys
 // select addresses without scoring every slot", Secs. 2 and 3.1).
 //
-// One warp per token-head row.  Each stage is an exact warp-level top-k over
-// (key descending, id ascending), where key is the order-preserving uint32
-// image of an fp32 score:
-//   * every lane holds E candidates in registers, sorted locally;
-//   * per output rank, one redux.sync max finds the best head key, one
-//     redux.sync min picks the lowest id among lanes holding that key, and the
-//     winning lane pops its head.
-// Stage 1 and 2 select the top-k of each score half (ids = positions); stage 3
-// forms the k*k fp32 sums s1[a] + s2[b] (ids = a*sqrtN + b) and selects the
-// top-W; the weights are the softmax of the selected sums.
+// One warp per token-head row (persistent warps).  Each stage is an exact
+// warp-level top-k over (key descending, id ascending), where key is the
+// order-preserving uint32 image of an fp32 score: candidates sit in lane
+// registers, and per output rank one redux.sync max finds the best key, one
+// redux.sync min the lowest id holding it, and the owning lane pops it.
+// Stage 1 and 2 select the top-k of each score half (ids = positions), first
+// filtering by a provable lower bound of the k-th score; stage 3 forms the
+// fp32 sums s1[a] + s2[b] (ids = a*sqrtN + b) of only the candidates that can
+// reach the top-W (a staircase of the two sorted halves), checks that no sum
+// outside it ties the W-th, and selects the top-W; the weights are the
+// softmax of the selected sums.
 #include <climits>
 
 #include "common.cuh"
@@ -75,81 +76,217 @@ __device__ __forceinline__ void warp_topk(uint32_t (&key)[E], int (&id)[E], int 
   }
 }
 
+// Exact top-`count` of up to 64 (key, id) pairs held two per lane: sorted
+// pair, then one redux round per output rank (as warp_topk, cheaper pops).
+__device__ __forceinline__ void warp_topk2(uint32_t k0, int i0, uint32_t k1, int i1, int count, uint32_t (&okey)[2],
+                                           int (&oid)[2]) {
+  const int lane = threadIdx.x & 31;
+  if (k1 > k0 || (k1 == k0 && i1 < i0)) {
+    const uint32_t tk = k0; k0 = k1; k1 = tk;
+    const int ti = i0; i0 = i1; i1 = ti;
+  }
+  okey[0] = okey[1] = 0;
+  oid[0] = oid[1] = INT_MAX;
+  for (int r = 0; r < count; ++r) {
+    const uint32_t m = __reduce_max_sync(kFull, k0);
+    const int wid = __reduce_min_sync(kFull, k0 == m ? i0 : INT_MAX);
+    const bool pop = k0 == m && i0 == wid;
+    k0 = pop ? k1 : k0;
+    i0 = pop ? i1 : i0;
+    k1 = pop ? 0u : k1;
+    i1 = pop ? INT_MAX : i1;
+    if (r == lane) { okey[0] = m; oid[0] = wid; }
+    if (r == lane + 32) { okey[1] = m; oid[1] = wid; }
+  }
+}
+
+// Top-k of one score half (positions 0..n-1, E values per lane at lane+32e).
+// Fast path: tau = the k-th largest of the 32 lane maxima is a lower bound of
+// the k-th largest score, so every top-k element has key >= tau; when at most
+// 64 elements qualify they are compacted (ballot order) and selected exactly.
+// Otherwise the full per-lane sorted selection runs.  Returns rank `lane`.
 template <int E>
+__device__ __forceinline__ void half_topk(const uint32_t (&key)[E], int n, int k, uint2 *cbuf, uint32_t &okey,
+                                          int &oid) {
+  const int lane = threadIdx.x & 31;
+  uint32_t lm = 0;
+#pragma unroll
+  for (int e = 0; e < E; ++e) lm = max(lm, key[e]);
+  int cnt = 0;
+  uint32_t tau = 0;
+  if (E > 2) {
+    // k-th largest lane maximum: remove the largest k-1 lane maxima
+    uint32_t v = lm;
+    for (int r = 0; r < k - 1; ++r) {
+      const uint32_t m = __reduce_max_sync(kFull, v);
+      const unsigned who = __ballot_sync(kFull, v == m);
+      if (lane == __ffs(who) - 1) v = 0;
+    }
+    tau = __reduce_max_sync(kFull, v);
+#pragma unroll
+    for (int e = 0; e < E; ++e) cnt += __popc(__ballot_sync(kFull, key[e] >= tau && lane + 32 * e < n));
+  }
+  if (E > 2 && cnt <= 64) {
+    int basepos = 0;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const bool in = key[e] >= tau && lane + 32 * e < n;
+      const unsigned bal = __ballot_sync(kFull, in);
+      if (in) cbuf[basepos + __popc(bal & ((1u << lane) - 1))] = make_uint2(key[e], lane + 32 * e);
+      basepos += __popc(bal);
+    }
+    __syncwarp();
+    const uint2 c0 = lane < cnt ? cbuf[lane] : make_uint2(0u, static_cast<unsigned>(INT_MAX));
+    const uint2 c1 = lane + 32 < cnt ? cbuf[lane + 32] : make_uint2(0u, static_cast<unsigned>(INT_MAX));
+    __syncwarp();
+    uint32_t ok[2];
+    int oi[2];
+    warp_topk2(c0.x, static_cast<int>(c0.y), c1.x, static_cast<int>(c1.y), k, ok, oi);
+    okey = ok[0];
+    oid = oi[0];
+  } else if (E <= 2) {
+    uint32_t k0 = key[0], k1 = E > 1 ? key[E - 1] : 0u;
+    int i0 = lane < n ? lane : INT_MAX, i1 = (E > 1 && lane + 32 < n) ? lane + 32 : INT_MAX;
+    if (!(lane < n)) k0 = 0u;
+    if (!(E > 1 && lane + 32 < n)) k1 = 0u;
+    uint32_t ok[2];
+    int oi[2];
+    warp_topk2(k0, i0, k1, i1, k, ok, oi);
+    okey = ok[0];
+    oid = oi[0];
+  } else {
+    uint32_t kk[E];
+    int id[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      kk[e] = lane + 32 * e < n ? key[e] : 0u;
+      id[e] = lane + 32 * e < n ? lane + 32 * e : INT_MAX;
+    }
+    uint32_t ok[1];
+    int oi[1];
+    warp_topk<E, 1>(kk, id, k, ok, oi);
+    okey = ok[0];
+    oid = oi[0];
+  }
+}
+
+// One warp per row, persistent over rows.  E1 = score values per lane of a
+// half; E3 = per-lane candidates of the full k*k fallback (8 or 32).
+template <int E1, int E3>
 __global__ void __launch_bounds__(kAddrWarps * 32) address_kernel(const float *__restrict__ s1,
                                                                   const float *__restrict__ s2, long rows,
                                                                   int sqrtN, int k, int W,
                                                                   int32_t *__restrict__ idx_out,
                                                                   float *__restrict__ w_out,
                                                                   int32_t *__restrict__ dev_err) {
+  __shared__ uint2 cbuf_all[kAddrWarps][64];
   const int lane = threadIdx.x & 31;
-  const long row = static_cast<long>(blockIdx.x) * kAddrWarps + (threadIdx.x >> 5);
-  if (row >= rows) return;  // warp-uniform
-
-  // --- stage 1 and 2: top-k of each half (one lane holds rank `lane`) ---
-  float hv[2];
-  int hid[2];
-  bool bad = false;
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    const float *src = (half == 0 ? s1 : s2) + row * sqrtN;
-    uint32_t key[E];
-    int id[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      const int j = lane + 32 * e;
-      const bool in = j < sqrtN;
-      const float x = in ? src[j] : 0.f;
-      bad |= in && !isfinite(x);
-      key[e] = in ? order_key(x) : 0u;
-      id[e] = in ? j : INT_MAX;
+  uint2 *cbuf = cbuf_all[threadIdx.x >> 5];
+  // pruned candidate set P = {(x, y) : (x+1)(y+1) <= W}: every slot outside P
+  // is dominated by at least W slots of P (the sorted halves make the sum
+  // monotone in x and y), so the top-W lies in P unless the W-th sum ties with
+  // a sum outside P.  Lane owns P entries lane and lane+32.
+  int px[2], py[2], npr = 0;
+  px[0] = px[1] = py[0] = py[1] = -1;
+  for (int x = 0; x < k; ++x) {
+    const int cnt = min(k, W / (x + 1));
+    for (int o = 0; o < 2; ++o) {
+      const int c = lane + 32 * o - npr;
+      if (c >= 0 && c < cnt) { px[o] = x; py[o] = c; }
     }
-    uint32_t ok[1];
-    int oi[1];
-    warp_topk<E, 1>(key, id, k, ok, oi);
-    hv[half] = key_value(ok[0]);
-    hid[half] = oi[0];
+    npr += cnt;
   }
-  if (__any_sync(kFull, bad) && lane == 0 && dev_err) atomicOr(dev_err, SDM_DEVERR_NONFINITE);
+  const bool pruned_ok = npr <= 64;
+  // corner of the complement of P in column x: (x, floor(W/(x+1))) if inside the k x k grid
+  const int corner_y = lane < k ? W / (lane + 1) : k;
 
-  // --- stage 3: the k*k candidate sums, top-W ---
-  uint32_t key[E];
-  int id[E];
-  const int kk = k * k;
+  const long stride = static_cast<long>(gridDim.x) * kAddrWarps;
+  for (long row = static_cast<long>(blockIdx.x) * kAddrWarps + (threadIdx.x >> 5); row < rows; row += stride) {
+    // --- stage 1 and 2: top-k of each half (lane holds rank `lane`) ---
+    float hv[2];
+    int hid[2];
+    bool bad = false;
 #pragma unroll
-  for (int e = 0; e < E; ++e) {
-    const int c = lane + 32 * e;
-    const int x = c / k, y = c - (c / k) * k;
-    const float av = __shfl_sync(kFull, hv[0], x & 31);
-    const float bv = __shfl_sync(kFull, hv[1], y & 31);
-    const int ai = __shfl_sync(kFull, hid[0], x & 31);
-    const int bi = __shfl_sync(kFull, hid[1], y & 31);
-    const bool in = c < kk;
-    key[e] = in ? order_key(__fadd_rn(av, bv)) : 0u;
-    id[e] = in ? ai * sqrtN + bi : INT_MAX;
-  }
-  uint32_t ok[2];
-  int oi[2];
-  warp_topk<E, 2>(key, id, W, ok, oi);
+    for (int half = 0; half < 2; ++half) {
+      const float *src = (half == 0 ? s1 : s2) + row * sqrtN;
+      uint32_t key[E1];
+#pragma unroll
+      for (int e = 0; e < E1; ++e) {
+        const int j = lane + 32 * e;
+        const float x = j < sqrtN ? src[j] : 0.f;
+        bad |= j < sqrtN && !isfinite(x);
+        key[e] = j < sqrtN ? order_key(x) : 0u;
+      }
+      uint32_t ok;
+      int oi;
+      half_topk<E1>(key, sqrtN, k, cbuf, ok, oi);
+      hv[half] = key_value(ok);
+      hid[half] = oi;
+    }
+    if (__any_sync(kFull, bad) && lane == 0 && dev_err) atomicOr(dev_err, SDM_DEVERR_NONFINITE);
 
-  // --- weights: softmax over the W selected sums (max = rank 0) ---
-  const float smax = key_value(__shfl_sync(kFull, ok[0], 0));
-  float ex[2];
-  float part = 0.f;
+    // --- stage 3: top-W of the k*k sums s1[a_x] + s2[b_y] ---
+    uint32_t ok[2];
+    int oi[2];
+    bool done = false;
+    if (pruned_ok) {
+      uint32_t ck[2];
+      int ci[2];
 #pragma unroll
-  for (int o = 0; o < 2; ++o) {
-    const int r = lane + 32 * o;
-    ex[o] = (r < W) ? expf(key_value(ok[o]) - smax) : 0.f;
-    part += ex[o];
-  }
+      for (int o = 0; o < 2; ++o) {
+        const int x = px[o] < 0 ? 0 : px[o], y = py[o] < 0 ? 0 : py[o];
+        const float av = __shfl_sync(kFull, hv[0], x);
+        const float bv = __shfl_sync(kFull, hv[1], y);
+        const int ai = __shfl_sync(kFull, hid[0], x);
+        const int bi = __shfl_sync(kFull, hid[1], y);
+        ck[o] = px[o] >= 0 ? order_key(__fadd_rn(av, bv)) : 0u;
+        ci[o] = px[o] >= 0 ? ai * sqrtN + bi : INT_MAX;
+      }
+      warp_topk2(ck[0], ci[0], ck[1], ci[1], W, ok, oi);
+      // exactness: the best sum outside P sits on one of its corners
+      const uint32_t kw = __shfl_sync(kFull, (W - 1) < 32 ? ok[0] : ok[1], (W - 1) & 31);
+      const float bcorner = __shfl_sync(kFull, hv[1], corner_y < k ? corner_y : 0);
+      const bool tie = lane < k && corner_y < k && order_key(__fadd_rn(hv[0], bcorner)) >= kw;
+      done = !__any_sync(kFull, tie);
+    }
+    if (!done) {  // full k*k candidate set
+      uint32_t key[E3];
+      int id[E3];
+      const int kk = k * k;
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(kFull, part, off);
+      for (int e = 0; e < E3; ++e) {
+        const int c = lane + 32 * e;
+        const int x = c / k, y = c - (c / k) * k;
+        const float av = __shfl_sync(kFull, hv[0], x & 31);
+        const float bv = __shfl_sync(kFull, hv[1], y & 31);
+        const int ai = __shfl_sync(kFull, hid[0], x & 31);
+        const int bi = __shfl_sync(kFull, hid[1], y & 31);
+        const bool in = c < kk;
+        key[e] = in ? order_key(__fadd_rn(av, bv)) : 0u;
+        id[e] = in ? ai * sqrtN + bi : INT_MAX;
+      }
+      warp_topk<E3, 2>(key, id, W, ok, oi);
+    }
+
+    // --- weights: softmax over the W selected sums (max = rank 0) ---
+    const float smax = key_value(__shfl_sync(kFull, ok[0], 0));
+    float ex[2];
+    float part = 0.f;
 #pragma unroll
-  for (int o = 0; o < 2; ++o) {
-    const int r = lane + 32 * o;
-    if (r < W) {
-      idx_out[row * W + r] = oi[o];
-      w_out[row * W + r] = ex[o] / part;
+    for (int o = 0; o < 2; ++o) {
+      const int r = lane + 32 * o;
+      ex[o] = (r < W) ? expf(key_value(ok[o]) - smax) : 0.f;
+      part += ex[o];
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(kFull, part, off);
+#pragma unroll
+    for (int o = 0; o < 2; ++o) {
+      const int r = lane + 32 * o;
+      if (r < W) {
+        idx_out[row * W + r] = oi[o];
+        w_out[row * W + r] = ex[o] / part;
+      }
     }
   }
 }
@@ -177,18 +314,29 @@ extern "C" int sdm_address(const float *s1, const float *s2, int B, int T, int H
   const long rows = static_cast<long>(B) * T * H;
   if (rows >= (1L << 31)) return set_error(SDM_ERR_SHAPE, "sdm_address: B*T*H must be < 2^31");
   if (rows == 0) return SDM_OK;
-  const int E = pow2_at_least(max((sqrtN + 31) / 32, (k * k + 31) / 32));
-  const dim3 grid(static_cast<unsigned>((rows + kAddrWarps - 1) / kAddrWarps));
+  const int E1 = pow2_at_least((sqrtN + 31) / 32);
+  const int E3 = pow2_at_least((k * k + 31) / 32);
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  long blocks = (rows + kAddrWarps - 1) / kAddrWarps;
+  if (blocks > static_cast<long>(sms) * 8) blocks = static_cast<long>(sms) * 8;
+  const dim3 grid(static_cast<unsigned>(blocks));
   const dim3 block(kAddrWarps * 32);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  switch (E) {
-    case 1: address_kernel<1><<<grid, block, 0, st>>>(s1, s2, rows, sqrtN, k, W, idx_out, w_out, dev_err); break;
-    case 2: address_kernel<2><<<grid, block, 0, st>>>(s1, s2, rows, sqrtN, k, W, idx_out, w_out, dev_err); break;
-    case 4: address_kernel<4><<<grid, block, 0, st>>>(s1, s2, rows, sqrtN, k, W, idx_out, w_out, dev_err); break;
-    case 8: address_kernel<8><<<grid, block, 0, st>>>(s1, s2, rows, sqrtN, k, W, idx_out, w_out, dev_err); break;
-    case 16: address_kernel<16><<<grid, block, 0, st>>>(s1, s2, rows, sqrtN, k, W, idx_out, w_out, dev_err); break;
-    case 32: address_kernel<32><<<grid, block, 0, st>>>(s1, s2, rows, sqrtN, k, W, idx_out, w_out, dev_err); break;
-    default: return set_error(SDM_ERR_SHAPE, "sdm_address: unsupported size");
+#define SDM_AK(A, C) \
+  address_kernel<A, C><<<grid, block, 0, st>>>(s1, s2, rows, sqrtN, k, W, idx_out, w_out, dev_err)
+#define SDM_AK_E3(A)            \
+  if (E3 <= 8) SDM_AK(A, 8);    \
+  else SDM_AK(A, 32);
+  switch (E1) {
+    case 1: SDM_AK_E3(1); break;
+    case 2: SDM_AK_E3(2); break;
+    case 4: SDM_AK_E3(4); break;
+    case 8: SDM_AK_E3(8); break;
+    default: SDM_AK_E3(16); break;
   }
+#undef SDM_AK_E3
+#undef SDM_AK
   return check_launch("sdm_address");
 }
