@@ -20,7 +20,7 @@ import torch
 
 __all__ = [
     "SdmError", "lib", "library_path", "sdm_version", "sdm_address", "sdm_scan", "sdm_scan_workspace_size",
-    "sdm_scan_noalloc",
+    "sdm_scan_noalloc", "sdm_forward_host", "sdm_forward_host_workspace_size",
     "gdn_scan", "gdn_scan_workspace_size", "sse_scan", "sse_scan_workspace_size", "SDM_RESID_SHARED", "SDM_RESID_PERSLOT",
     "SDM_RESID_ADDITIVE", "SDM_DEVERR_INDEX_RANGE", "SDM_DEVERR_INDEX_REPEAT", "SDM_DEVERR_NONFINITE",
 ]
@@ -43,6 +43,9 @@ _SIGNATURES = {
     "sdm_scan_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "sdm_scan": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P, _P]),
     "sdm_scan_noalloc": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "sdm_forward_host_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I, _I, _I]),
+    "sdm_forward_host": (_I, [_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _I, _P,
+                              _SZ, _P, _P]),
     "gdn_scan_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "gdn_scan": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "sse_scan_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
@@ -172,6 +175,59 @@ def sdm_scan(state, v, alpha, beta, idx_w, w_w, idx_r, w_r, resid_mode=SDM_RESID
                         w_w.data_ptr(), W, idx_r.data_ptr(), w_r.data_ptr(), R, B, T, H, N, dv, int(resid_mode),
                         y.data_ptr(), workspace.data_ptr(), workspace.numel(), _ptr(dev_err), _stream(stream))
     _check("sdm_scan", rc)
+    return y
+
+
+def sdm_forward_host_workspace_size(B, T, H, sqrtN, d_v, W, R, v_bf16: bool, chunk_T: int) -> int:
+    return int(lib().sdm_forward_host_workspace_size(B, T, H, sqrtN, d_v, W, R,
+                                                     SDM_DTYPE_BF16 if v_bf16 else SDM_DTYPE_F32, chunk_T))
+
+
+def _req_host(t: torch.Tensor, name: str, dtype, shape=None):
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise TypeError(f"{name} must be a CPU (preferably pinned) tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def sdm_forward_host(s1w, s2w, s1r, s2r, v, alpha, beta, k: int, W: int, R: int, state, y=None,
+                     resid_mode=SDM_RESID_SHARED, chunk_T: int = 512, workspace=None, dev_err=None, stream=None):
+    """Whole sparse step from host tensors (pinned for overlap): addressing of
+    both score-half pairs and the scan, pipelined over chunks of chunk_T
+    tokens.  `state` is the CUDA table [B,H,N,d_v]; returns the host y
+    [B,T,H,d_v], valid once `stream` is synchronised."""
+    _req_host(s1w, "s1w", torch.float32)
+    if s1w.dim() != 4:
+        raise ValueError("s1w must be [B,T,H,sqrtN]")
+    B, T, H, sq = s1w.shape
+    for n_, t_ in (("s2w", s2w), ("s1r", s1r), ("s2r", s2r)):
+        _req_host(t_, n_, torch.float32, (B, T, H, sq))
+    _req(state, "state", torch.float32, (B, H, sq * sq, state.shape[-1]))
+    dv = state.shape[-1]
+    if v.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("v must be float32 or bfloat16")
+    _req_host(v, "v", v.dtype, (B, T, H, dv))
+    _req_host(alpha, "alpha", torch.float32, (B, T, H))
+    _req_host(beta, "beta", torch.float32, (B, T, H))
+    if y is None:
+        y = torch.empty((B, T, H, dv), dtype=torch.float32).pin_memory()
+    _req_host(y, "y", torch.float32, (B, T, H, dv))
+    bf = v.dtype == torch.bfloat16
+    need = sdm_forward_host_workspace_size(B, T, H, sq, dv, W, R, bf, chunk_T)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=state.device)
+    _req(workspace, "workspace", torch.uint8)
+    if dev_err is not None:
+        _req(dev_err, "dev_err", torch.int32)
+    rc = lib().sdm_forward_host(s1w.data_ptr(), s2w.data_ptr(), s1r.data_ptr(), s2r.data_ptr(), v.data_ptr(),
+                                SDM_DTYPE_BF16 if bf else SDM_DTYPE_F32, alpha.data_ptr(), beta.data_ptr(), B, T, H,
+                                sq, int(k), int(W), int(R), dv, int(resid_mode), state.data_ptr(), y.data_ptr(),
+                                int(chunk_T), workspace.data_ptr(), workspace.numel(), _ptr(dev_err), _stream(stream))
+    _check("sdm_forward_host", rc)
     return y
 
 

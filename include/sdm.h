@@ -140,6 +140,44 @@ SDM_API int sdm_scan(float *state, const void *v, int v_dtype, const float *alph
              size_t workspace_bytes, int32_t *dev_err, void *stream);
 
 /*
+ * Device bytes sdm_forward_host needs as staging for these sizes (two chunk
+ * buffers of every input and output plus the scan's records); 0 for invalid
+ * sizes.
+ */
+SDM_API size_t sdm_forward_host_workspace_size(int B, int T, int H, int sqrtN, int d_v, int W, int R, int v_dtype,
+                                               int chunk_T);
+
+/*
+ * sdm_forward_host - one whole sparse step from HOST buffers: write and read
+ * addressing ([SDM] "Product keys select addresses ...") and the scan ([SDM]
+ * Eqs. 3-5), i.e. sdm_address twice and sdm_scan, with the per-step inputs
+ * and y in host memory and the table resident on the device.
+ *
+ * The sequence is processed in chunks of chunk_T tokens; chunk c+1's inputs
+ * are copied in and chunk c-1's y copied out while chunk c is computed (two
+ * internal copy streams, ordered by events after the work already queued on
+ * `stream`, and before anything queued on `stream` afterwards).  Results are
+ * bit-identical to one sdm_address/sdm_address/sdm_scan sequence on the whole
+ * input (the scan continues its table across chunks).
+ *
+ * s1w, s2w, s1r, s2r : host fp32 [B,T,H,sqrtN] write and read score halves.
+ * v          : host [B,T,H,d_v], fp32 or bf16 per v_dtype.
+ * alpha, beta: host fp32 [B,T,H].
+ * state      : DEVICE fp32 [B,H,N,d_v], N = sqrtN^2, updated in place.
+ * y          : host fp32 [B,T,H,d_v], written when `stream` reaches the end
+ *              of this call's work (synchronise `stream` before reading it).
+ * workspace  : DEVICE scratch, 256-byte aligned, at least
+ *              sdm_forward_host_workspace_size(...) bytes.
+ * Host buffers should be page-locked (cudaHostAlloc / cudaHostRegister) for
+ * the copies to overlap compute; pageable memory works but serialises.
+ * Limits and errors: those of sdm_address and sdm_scan.
+ */
+SDM_API int sdm_forward_host(const float *s1w, const float *s2w, const float *s1r, const float *s2r, const void *v,
+                             int v_dtype, const float *alpha, const float *beta, int B, int T, int H, int sqrtN, int k,
+                             int W, int R, int d_v, int resid_mode, float *state, float *y, int chunk_T,
+                             void *workspace, size_t workspace_bytes, int32_t *dev_err, void *stream);
+
+/*
  * sdm_scan_noalloc - sdm_scan for callers that cannot give the library device
  * scratch memory.  The papers have no counterpart: this is an interface
  * convenience of this library, not a step of the method.

@@ -116,19 +116,18 @@ def test_scan_tiny_full_pipeline(gmode, omode):
     assert_state_close(M, ref["state"])
 
 
-@pytest.mark.parametrize("cpl", [1, 2, 4])
-@pytest.mark.parametrize("window", [4, 8])
+@pytest.mark.parametrize("d_v", [36, 68, 132])
+@pytest.mark.parametrize("window", [4, 6, 8])
 @pytest.mark.parametrize("gmode,omode", MODES)
-def test_scan_hazard_stress(monkeypatch, cpl, window, gmode, omode):
+def test_scan_hazard_stress(monkeypatch, d_v, window, gmode, omode):
     """Tiny tables with W = R = 16: rows are rewritten by almost every token,
-    so nearly every slot is forwarded from the history ring.  Ragged d_v,
-    random nonzero initial state, every compiled (cpl, window) variant."""
+    so nearly every slot is forwarded from the history ring.  Ragged d_v (a
+    partial last column tile), random nonzero initial state, every compiled
+    prefetch window."""
     sdm = need_gpu()
-    monkeypatch.setenv("SDM_SCAN_CPL", str(cpl))
     monkeypatch.setenv("SDM_SCAN_WINDOW", str(window))
     for sq, k, seed in ((4, 4, 1), (8, 8, 2)):
-        sh = synth.SdmShape("stress", B=2, T=97, H=3, sqrtN=sq, d_v=36 + 32 * (cpl - 1), k=k, W=16, R=16,
-                            v_bf16=False)
+        sh = synth.SdmShape("stress", B=2, T=97, H=3, sqrtN=sq, d_v=d_v, k=k, W=16, R=16, v_bf16=False)
         inp = synth.sdm_inputs(sh, seed=seed)
         iw, ww = oracle.address(inp["s1w"], inp["s2w"], k, 16)
         ir, wr = oracle.address(inp["s1r"], inp["s2r"], k, 16)
@@ -315,3 +314,30 @@ def test_two_slot_worked_example_on_gpu(golden):
     for mode, key in ((1, "per_slot"), (0, "shared")):
         M, _, _ = _run_gpu_scan(sdm, M0, inp, idx, w, idx, w, mode)
         np.testing.assert_allclose(M[0, 0, :, 0], g[key], atol=1e-6)
+
+
+# ------------------------------------------------------------- host path
+@pytest.mark.parametrize("chunk", [100, 4096])
+def test_forward_host_matches_device_path_bitexact(chunk):
+    """sdm_forward_host (host inputs and y, chunked copy/compute pipeline) gives
+    the same bits as sdm_address x2 + sdm_scan on device inputs."""
+    sdm = need_gpu()
+    import torch
+    sh = synth.SDM_14B_LAYER.with_(B=2, T=333, H=2, sqrtN=64, d_v=96)
+    inp = synth.sdm_inputs(sh, seed=17)
+    M0 = synth.random_state((sh.B, sh.H, sh.N, sh.d_v), seed=18, scale=0.1)
+    iw, ww = sdm.sdm_address(dev(inp["s1w"]), dev(inp["s2w"]), sh.k, sh.W)
+    ir, wr = sdm.sdm_address(dev(inp["s1r"]), dev(inp["s2r"]), sh.k, sh.R)
+    st_dev = dev(M0)
+    y_dev = sdm.sdm_scan(st_dev, dev(inp["v"]), dev(inp["alpha"]), dev(inp["beta"]), iw, ww, ir, wr)
+    hostt = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    v_h = torch.from_numpy(inp["v"].view(np.int16).copy()).view(torch.bfloat16).pin_memory()
+    st_host = dev(M0)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y_h = sdm.sdm_forward_host(hostt(inp["s1w"]), hostt(inp["s2w"]), hostt(inp["s1r"]), hostt(inp["s2r"]), v_h,
+                               hostt(inp["alpha"]), hostt(inp["beta"]), sh.k, sh.W, sh.R, st_host, chunk_T=chunk,
+                               dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.array_equal(y_h.numpy(), host(y_dev))
+    assert np.array_equal(host(st_host), host(st_dev))
