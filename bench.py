@@ -50,6 +50,23 @@ def _src_digest(name: str) -> str:
     return hashlib.sha1(open(p, "rb").read()).hexdigest()[:12]
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Largest x over all ranks (the slowest rank's time); x itself at N=1.
+    Works on the nccl (CUDA tensor) and gloo (CPU tensor) backends."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def shard_seed(rank: int) -> int:
+    """Each rank draws its own batch: independent sequences, no exchange."""
+    return rank
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -377,7 +394,7 @@ def run_ours(args, rank, world, local_rank, sampler):
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
     wl = Workload(args.workload, args.mode, args.batch)
-    inp = wl.inputs(seed=rank)
+    inp = wl.inputs(seed=shard_seed(rank))
     cpu = None
     if sampler is not None:
         nseq = min(sampler.cores, wl.shape.B * wl.shape.H)
@@ -419,10 +436,7 @@ def run_ours(args, rank, world, local_rank, sampler):
     clk = clocks.stop()
     total_ms = start.elapsed_time(end)
     main_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    if world > 1:
-        t = torch.tensor([total_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, device)
     ms_per_step = total_ms / K
 
     # end to end through the public API: pinned host inputs -> device -> the
@@ -440,10 +454,7 @@ def run_ours(args, rank, world, local_rank, sampler):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / KE
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, world, device)
     h2d, d2h = run.io_bytes()
 
     pk, src = peaks()
