@@ -26,7 +26,7 @@ __all__ = [
 ]
 
 SDM_OK, SDM_ERR_INVALID_ARG, SDM_ERR_SHAPE, SDM_ERR_ALIGN, SDM_ERR_UNSUPPORTED, SDM_ERR_CUDA = range(6)
-SDM_DEVERR_INDEX_RANGE, SDM_DEVERR_INDEX_REPEAT, SDM_DEVERR_NONFINITE = 1, 2, 4
+SDM_DEVERR_INDEX_RANGE, SDM_DEVERR_INDEX_REPEAT, SDM_DEVERR_NONFINITE, SDM_DEVERR_TIMEOUT = 1, 2, 4, 8
 SDM_DTYPE_F32, SDM_DTYPE_BF16 = 0, 1
 SDM_RESID_SHARED, SDM_RESID_PERSLOT, SDM_RESID_ADDITIVE = 0, 1, 2
 
@@ -47,7 +47,7 @@ _SIGNATURES = {
     "sdm_forward_host": (_I, [_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _I, _P,
                               _SZ, _P, _P]),
     "gdn_scan_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
-    "gdn_scan": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "gdn_scan": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _SZ, _P, _P]),
     "sse_scan_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "sse_scan": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _SZ, _P, _P]),
 }
@@ -269,7 +269,7 @@ def gdn_scan_workspace_size(B: int, T: int, H: int, dk: int, dv: int, per_channe
     return int(lib().gdn_scan_workspace_size(B, T, H, dk, dv, int(bool(per_channel))))
 
 
-def gdn_scan(state, q, k, v, alpha, beta, per_channel: bool, y=None, workspace=None, stream=None):
+def gdn_scan(state, q, k, v, alpha, beta, per_channel: bool, y=None, workspace=None, dev_err=None, stream=None):
     """Dense GDN / KDA scan; updates `state` [B,H,dk,dv] in place and returns
     y fp32 [B,T,H,dv].  q, k bf16 [B,T,H,dk]; v bf16 [B,T,H,dv]; alpha fp32
     [B,T,H] (GDN) or [B,T,H,dk] (KDA); beta fp32 [B,T,H]."""
@@ -292,9 +292,11 @@ def gdn_scan(state, q, k, v, alpha, beta, per_channel: bool, y=None, workspace=N
         workspace = torch.empty(need, dtype=torch.uint8, device=state.device)
     if workspace is not None:
         _req(workspace, "workspace", torch.uint8)
+    if dev_err is not None:
+        _req(dev_err, "dev_err", torch.int32)
     rc = lib().gdn_scan(state.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), alpha.data_ptr(),
                         int(bool(per_channel)), beta.data_ptr(), B, T, H, dk, dv, y.data_ptr(), _ptr(workspace),
-                        0 if workspace is None else workspace.numel(), _stream(stream))
+                        0 if workspace is None else workspace.numel(), _ptr(dev_err), _stream(stream))
     _check("gdn_scan", rc)
     return y
 

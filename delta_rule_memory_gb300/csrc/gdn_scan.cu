@@ -1,6 +1,8 @@
 // gdn_scan.cu - dense Gated DeltaNet / KDA scan (Linear Attention Architectures
-// deck, "GDN and KDA change the granularity of forgetting", Eqs. 15-20), token
-// by token in fp32.
+// deck, "GDN and KDA change the granularity of forgetting", Eqs. 15-20): the
+// C ABI entry point, and the token-by-token fp32 kernel used for KDA and for
+// widths other than d_k = d_v = 128 (dense GDN at 128 x 128 runs chunkwise on
+// the tensor cores, gdn_chunk.cu).
 //
 // One CTA per (batch, head, 32-column tile of the value dimension); the
 // dk x 32 state tile stays in registers for the whole sequence (thread
@@ -8,6 +10,8 @@
 // rows, reduce the decayed prediction over rows (one barrier), write, and
 // reduce the read over rows (reduced by the next token's barrier).  Per-token
 // inputs are prefetched P tokens ahead with cp.async.
+#include <cstdlib>
+
 #include "common.cuh"
 
 namespace sdm {
@@ -135,6 +139,10 @@ __global__ void __launch_bounds__(kGdnWarps * 32) gdn_recurrent_kernel(const Gdn
 }
 
 }  // namespace
+
+int launch_gdn_chunk(float *state, const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
+                     const float *beta, int B, int T, int H, float *y, int32_t *err, cudaStream_t st);
+
 }  // namespace sdm
 
 using namespace sdm;
@@ -146,7 +154,7 @@ extern "C" size_t gdn_scan_workspace_size(int B, int T, int H, int dk, int dv, i
 
 extern "C" int gdn_scan(float *state, const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
                         int per_channel, const float *beta, int B, int T, int H, int dk, int dv, float *y,
-                        void *workspace, size_t workspace_bytes, void *stream) {
+                        void *workspace, size_t workspace_bytes, int32_t *dev_err, void *stream) {
   (void)workspace; (void)workspace_bytes;
   if (!state || !q || !k || !v || !alpha || !beta || !y) return set_error(SDM_ERR_INVALID_ARG, "gdn_scan: null pointer");
   if (B < 0 || T < 0 || H < 0) return set_error(SDM_ERR_INVALID_ARG, "gdn_scan: negative size");
@@ -157,6 +165,15 @@ extern "C" int gdn_scan(float *state, const uint16_t *q, const uint16_t *k, cons
       !aligned(alpha, per_channel ? 16 : 4) || !aligned(beta, 4))
     return set_error(SDM_ERR_ALIGN, "gdn_scan: state, y, q, k, v (and KDA alpha) need 16-byte alignment");
   if (B == 0 || T == 0 || H == 0) return SDM_OK;
+  if (dev_err && !aligned(dev_err, 4)) return set_error(SDM_ERR_ALIGN, "gdn_scan: dev_err must be 4-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // dense GDN at d_k = d_v = 128: chunkwise form on the tensor cores; every
+  // other shape (and KDA) runs token by token.  SDM_GDN_PATH=recurrent forces
+  // the token-by-token kernel (for cross-checks).
+  const char *path = getenv("SDM_GDN_PATH");
+  const bool want_recurrent = !(path && path[0] == 'c');
+  if (!per_channel && dk == 128 && dv == 128 && !want_recurrent)
+    return launch_gdn_chunk(state, q, k, v, alpha, beta, B, T, H, y, dev_err, st);
   GdnArgs args;
   args.state = state;
   args.q = q;
@@ -173,7 +190,6 @@ extern "C" int gdn_scan(float *state, const uint16_t *q, const uint16_t *k, cons
   args.tiles = dv / kGdnCols;
   const size_t smem = sizeof(float) * 3 * kGdnWarps * kGdnCols + sizeof(uint32_t) * (kGdnP + 1) * gdn_slot_words(dk);
   const long blocks = static_cast<long>(B) * H * args.tiles;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   switch (dk) {
     case 16: gdn_recurrent_kernel<2><<<static_cast<unsigned>(blocks), kGdnWarps * 32, smem, st>>>(args); break;
     case 32: gdn_recurrent_kernel<4><<<static_cast<unsigned>(blocks), kGdnWarps * 32, smem, st>>>(args); break;

@@ -62,6 +62,7 @@ extern "C" {
 #define SDM_DEVERR_INDEX_RANGE 1  /* a slot index outside [0, N) (skipped) */
 #define SDM_DEVERR_INDEX_REPEAT 2 /* a slot repeated within one token's write list */
 #define SDM_DEVERR_NONFINITE 4    /* a NaN or infinite score or logit */
+#define SDM_DEVERR_TIMEOUT 8      /* a bounded on-device wait gave up; outputs invalid */
 
 /* Element types of the value input of sdm_scan. */
 #define SDM_DTYPE_F32 0
@@ -227,12 +228,17 @@ SDM_API size_t gdn_scan_workspace_size(int B, int T, int H, int dk, int dv, int 
  * q, k  : bf16 [B,T,H,dk];  v : bf16 [B,T,H,dv].
  * alpha : fp32 [B,T,H] (GDN) or [B,T,H,dk] (KDA).   beta : fp32 [B,T,H].
  * y     : fp32 [B,T,H,dv].
+ * dev_err : optional; SDM_DEVERR_TIMEOUT if a bounded wait of the tensor-core
+ *           kernel gave up (outputs then invalid).
+ * Kernels: dense GDN with dk = dv = 128 runs chunkwise (64 tokens) on the
+ *          tensor cores ([SDM] App. A.1-A.2, Eq. 7, dense case; the state stays
+ *          in tensor memory); KDA and other widths run token by token in fp32.
  * Limits: dk in {16, 32, 64, 128}; dv % 32 == 0, dv <= 256.  state and y
  *         16-byte aligned; q, k, v 16-byte aligned (dk, dv multiples of 8).
  */
 SDM_API int gdn_scan(float *state, const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
-             int per_channel, const float *beta, int B, int T, int H, int dk, int dv, float *y, void *workspace,
-             size_t workspace_bytes, void *stream);
+                     int per_channel, const float *beta, int B, int T, int H, int dk, int dv, float *y,
+                     void *workspace, size_t workspace_bytes, int32_t *dev_err, void *stream);
 
 /*
  * Scratch bytes sse_scan needs: one routing record per token (selected

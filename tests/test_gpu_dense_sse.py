@@ -51,6 +51,40 @@ def test_gdn_full_size_sampled(per_channel):
         assert_state_close(S[b:b + 1, h:h + 1], Sr, what=f"state[{b},{h}]")
 
 
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 200])
+def test_gdn_chunked_path_lengths(T, monkeypatch):
+    """Dense GDN at d_k = d_v = 128 runs chunkwise (64 tokens) on the tensor
+    cores: lengths below, at and across a chunk boundary, nonzero state."""
+    sdm = need_gpu()
+    monkeypatch.setenv("SDM_GDN_PATH", "chunk")
+    import torch
+    sh = synth.GDN_DENSE.with_(B=2, T=T, H=2)
+    inp = synth.gdn_inputs(sh, seed=40 + T)
+    S0 = synth.random_state((2, 2, 128, 128), seed=41, scale=0.3)
+    Sr, yr = oracle.gdn_scan(S0, inp["q"], inp["k"], inp["v"], inp["alpha_gdn"], inp["beta"], False)
+    state = dev(S0)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y = sdm.gdn_scan(state, dev(inp["q"]), dev(inp["k"]), dev(inp["v"]), dev(inp["alpha_gdn"]), dev(inp["beta"]),
+                     False, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_y_close(host(y), yr)
+    assert_state_close(host(state), Sr)
+
+
+def test_gdn_chunked_matches_token_recurrent(monkeypatch):
+    sdm = need_gpu()
+    sh = synth.GDN_DENSE.with_(B=1, T=300, H=3)
+    inp = synth.gdn_inputs(sh, seed=44)
+    S0 = synth.random_state((1, 3, 128, 128), seed=45, scale=0.3)
+    monkeypatch.setenv("SDM_GDN_PATH", "chunk")
+    Sc, yc = _gdn_gpu(sdm, S0, inp, False)
+    monkeypatch.setenv("SDM_GDN_PATH", "recurrent")
+    Sr, yr = _gdn_gpu(sdm, S0, inp, False)
+    assert_y_close(yc, yr)
+    assert_state_close(Sc, Sr)
+
+
 def test_kda_with_constant_channel_decay_is_gdn_bitexact():
     sdm = need_gpu()
     sh = synth.GDN_DENSE.with_(B=1, T=64, H=2)
