@@ -171,7 +171,7 @@ extern "C" int gdn_scan(float *state, const uint16_t *q, const uint16_t *k, cons
   // other shape (and KDA) runs token by token.  SDM_GDN_PATH=recurrent forces
   // the token-by-token kernel (for cross-checks).
   const char *path = getenv("SDM_GDN_PATH");
-  const bool want_recurrent = !(path && path[0] == 'c');
+  const bool want_recurrent = path && path[0] == 'r';
   if (!per_channel && dk == 128 && dv == 128 && !want_recurrent)
     return launch_gdn_chunk(state, q, k, v, alpha, beta, B, T, H, y, dev_err, st);
   GdnArgs args;
