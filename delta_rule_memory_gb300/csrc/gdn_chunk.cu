@@ -51,8 +51,8 @@ constexpr uint32_t kOffRU = kOffSl + 128 * kDK * 2;       // R^T / U^T hi+lo: 2 
 constexpr uint32_t kOffT = kOffRU + 2 * 128 * kC * 2;     // T hi+lo: 2 x 64 x 64 bf16            16 KB
 constexpr uint32_t kOffM = kOffT + 2 * kC * kC * 2;       // Mq hi+lo                             16 KB
 constexpr uint32_t kOffKh = kOffM + 2 * kC * kC * 2;      // Khat^T hi+lo: 2 x 128 x 64 bf16      32 KB
-constexpr uint32_t kOffGate = kOffKh + 2 * 128 * kC * 2;  // per buffer: log alpha, beta, lambda, gamma
-constexpr uint32_t kOffBar = kOffGate + 8 * kC * 4;
+constexpr uint32_t kOffGate = kOffKh + 2 * 128 * kC * 2;  // per buffer: log alpha, beta, lambda, gamma, e^(l_C-l_j)
+constexpr uint32_t kOffBar = kOffGate + 10 * kC * 4;
 constexpr uint32_t kSmemBytes = kOffBar + 64;
 // scratch views during the triangular solve (regions free at that time)
 constexpr int kLd = kC + 1;                        // padded fp32 row stride
@@ -76,15 +76,16 @@ __device__ __forceinline__ uint32_t tmem_addr(uint32_t base, int lane_base, uint
 }
 
 // 8 consecutive fp32 -> one 16-byte chunk of bf16 hi and one of bf16 lo
+// (hi = bf16(x), lo = bf16(x - hi), converted two at a time)
 __device__ __forceinline__ void store_split8(unsigned char *hi, unsigned char *lo, uint32_t off, const float *x) {
   uint32_t h[4], l[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    uint16_t h0, l0, h1, l1;
-    split_bf16(x[2 * e], h0, l0);
-    split_bf16(x[2 * e + 1], h1, l1);
-    h[e] = static_cast<uint32_t>(h0) | (static_cast<uint32_t>(h1) << 16);
-    l[e] = static_cast<uint32_t>(l0) | (static_cast<uint32_t>(l1) << 16);
+    const __nv_bfloat162 hb = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+    const float2 hf = __bfloat1622float2(hb);
+    const __nv_bfloat162 lb = __floats2bfloat162_rn(x[2 * e] - hf.x, x[2 * e + 1] - hf.y);
+    h[e] = *reinterpret_cast<const uint32_t *>(&hb);
+    l[e] = *reinterpret_cast<const uint32_t *>(&lb);
   }
   *reinterpret_cast<uint4 *>(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
   *reinterpret_cast<uint4 *>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
@@ -120,7 +121,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const ChunkArgs 
   unsigned char *sTh = sm + kOffT, *sTl = sm + kOffT + kC * kC * 2;
   unsigned char *sMh = sm + kOffM, *sMl = sm + kOffM + kC * kC * 2;
   unsigned char *sKhh = sm + kOffKh, *sKhl = sm + kOffKh + 128 * kC * 2;
-  float *gate = reinterpret_cast<float *>(sm + kOffGate);  // [2 buffers][log alpha, beta, lambda, gamma][64]
+  float *gate = reinterpret_cast<float *>(sm + kOffGate);  // [2 buffers][log alpha, beta, lambda, gamma, tail][64]
   float *sA = reinterpret_cast<float *>(sm + kOffA);
   float *sTf = reinterpret_cast<float *>(sm + kOffTf);
   float *sZ = reinterpret_cast<float *>(sm + kOffZ);
@@ -177,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const ChunkArgs 
     }
     if (tid < kC) {
       const int t = t0 + tid;
-      float *g = gate + buf * 4 * kC;
+      float *g = gate + buf * 5 * kC;
       g[tid] = t < T ? __logf(a.alpha[tok0 + static_cast<long>(t) * H]) : 0.f;  // padding: alpha = 1
       g[kC + tid] = t < T ? a.beta[tok0 + static_cast<long>(t) * H] : 0.f;       // padding: beta = 0
     }
@@ -202,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const ChunkArgs 
   for (int c = 0; c < nchunks; ++c) {
     const int buf = c & 1;
     const uint32_t par = static_cast<uint32_t>(c & 1);
-    float *g = gate + buf * 4 * kC;  // [0]: log alpha, [1]: beta, [2]: lambda, [3]: gamma
+    float *g = gate + buf * 5 * kC;  // [0]: log alpha, [1]: beta, [2]: lambda, [3]: gamma, [4]: e^(l_C - l_j)
     cp_async_wait<0>();
     // lambda = inclusive prefix sum of log alpha (two warps of 32 tokens)
     if (warp < 2) {
@@ -219,7 +220,10 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const ChunkArgs 
     __syncthreads();
     if (warp == 1) g[2 * kC + tid] += g[2 * kC + 31];
     __syncthreads();
-    if (tid < kC) g[3 * kC + tid] = __expf(g[2 * kC + tid]);
+    if (tid < kC) {
+      g[3 * kC + tid] = __expf(g[2 * kC + tid]);
+      g[4 * kC + tid] = __expf(g[2 * kC + kC - 1] - g[2 * kC + tid]);
+    }
     tc_fence_after();
 
     // ---- MMAs that need only the chunk's K, Q and the incoming state
@@ -238,11 +242,11 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const ChunkArgs 
     // ---- A (decayed, gated K K^T) and Mq (decayed Q K^T) from the GP tile
     if (!wait_ok(mbGP, par)) { failed = true; break; }
     const float *lam = g + 2 * kC;
-    if (half == 0) {
+    {
       const int i = row & 63;
       const float li = lam[i];
       const float bi = g[kC + i];
-      for (int j0 = 0; j0 < kC; j0 += 16) {
+      for (int j0 = half * 32; j0 < half * 32 + 32; j0 += 16) {
         float x[16];
         tmem_ld16(tmem_addr(tmem, lane_base, kColGP + j0), x);
         tmem_ld_wait();
@@ -320,14 +324,14 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const ChunkArgs 
     __syncthreads();  // sA (in the Khat region) is no longer read
     // Khat^T[c][j] = exp(lambda_C - lambda_j) k_j[c] (B operand of the state update)
     {
-      const float lC = lam[kC - 1];
+      const float *tail = g + 4 * kC;  // e^(lambda_C - lambda_j)
       for (int j0 = half * 32; j0 < half * 32 + 32; j0 += 8) {
         float x[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int j = j0 + e;
           const uint16_t kb = *reinterpret_cast<const uint16_t *>(sKQ + kmajor_off(j, row, kDK));
-          x[e] = __expf(lC - lam[j]) * bf16_to_f32(kb);
+          x[e] = tail[j] * bf16_to_f32(kb);
         }
         store_split8(sKhh, sKhl, kmajor_off(row, j0, kC), x);
       }

@@ -85,15 +85,22 @@ def test_gdn_chunked_matches_token_recurrent(monkeypatch):
     assert_state_close(Sc, Sr)
 
 
-def test_kda_with_constant_channel_decay_is_gdn_bitexact():
+def test_kda_with_constant_channel_decay_is_gdn(monkeypatch):
+    """KDA with alpha = alpha_t * 1 is GDN (Linear Attention Architectures
+    deck, Eqs. 18-20): bit-exact on the same token-by-token kernel, and within
+    tolerance of the tensor-core GDN path."""
     sdm = need_gpu()
     sh = synth.GDN_DENSE.with_(B=1, T=64, H=2)
     inp = synth.gdn_inputs(sh, seed=3)
     inp2 = dict(inp)
     inp2["alpha_kda"] = np.repeat(inp["alpha_gdn"][..., None], sh.dk, axis=-1).copy()
     S0 = synth.random_state((1, 2, sh.dk, sh.dv), seed=4, scale=0.2)
-    Sg, yg = _gdn_gpu(sdm, S0, inp, False)
     Sk, yk = _gdn_gpu(sdm, S0, inp2, True)
+    Sc, yc = _gdn_gpu(sdm, S0, inp, False)          # chunked tensor-core path
+    assert_y_close(yc, yk)
+    assert_state_close(Sc, Sk)
+    monkeypatch.setenv("SDM_GDN_PATH", "recurrent")
+    Sg, yg = _gdn_gpu(sdm, S0, inp, False)
     assert np.array_equal(yg, yk) and np.array_equal(Sg, Sk)
 
 
