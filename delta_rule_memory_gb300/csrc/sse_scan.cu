@@ -10,8 +10,9 @@
 //   scan   - one CTA per (batch, head, 16-column tile).  All N+1 partitions of
 //            that column tile live in shared memory for the whole sequence; per
 //            token only the k routed partitions and the shared one are touched
-//            (decay, additive write, read).  Per-token inputs are prefetched
-//            P tokens ahead with cp.async; one CTA barrier per token.
+//            (decay, additive write, read), two columns per thread with packed
+//            fp32x2 arithmetic.  Per-token inputs are prefetched P tokens ahead
+//            with cp.async; one CTA barrier per token.
 #include <climits>
 
 #include "common.cuh"
@@ -21,7 +22,6 @@ namespace {
 
 constexpr int kSseDT = 16;        // columns per CTA
 constexpr int kSseThreads = 256;  // 16 columns x 16 row groups
-constexpr int kSseRG = kSseThreads / kSseDT;
 constexpr int kSseP = 4;          // tokens prefetched ahead
 constexpr int kSseMaxTopk = 8;
 
@@ -124,11 +124,37 @@ struct SseSlot {
   static __host__ __device__ int words(int c, int rw) { return rec_off(c) + rw; }
 };
 
+// packed fp32x2 helpers (one instruction for two lanes of math)
+__device__ __forceinline__ unsigned long long pk(float x, float y) {
+  return (static_cast<unsigned long long>(__float_as_uint(y)) << 32) | __float_as_uint(x);
+}
+__device__ __forceinline__ float2 upk(unsigned long long v) {
+  return make_float2(__uint_as_float(static_cast<uint32_t>(v)), __uint_as_float(static_cast<uint32_t>(v >> 32)));
+}
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b, unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// Thread (pair cp = tid % 8, row group rg = tid / 8) owns columns 2cp, 2cp+1
+// of the tile and rows rg, rg+32, rg+64, rg+96 of every partition; the read
+// is summed over the four row groups of a warp with shuffles, then over the
+// eight warps through shared memory (summed after the next token's barrier).
+constexpr int kSseRows = 32;  // row groups
+constexpr int kSseRPT = 4;    // rows per thread (c <= 128)
+
 __global__ void __launch_bounds__(kSseThreads) sse_scan_kernel(const SseArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int tid = threadIdx.x;
-  const int col = tid % kSseDT;
-  const int rg = tid / kSseDT;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int cp = tid & 7;
+  const int rg = tid >> 3;
   const int tile = blockIdx.x % a.tiles;
   const long bh = blockIdx.x / a.tiles;
   const int h = static_cast<int>(bh % a.H);
@@ -136,18 +162,17 @@ __global__ void __launch_bounds__(kSseThreads) sse_scan_kernel(const SseArgs a) 
   const int c = a.c, d = a.d, N = a.N, T = a.T, H = a.H, topk = a.topk;
   const int parts = N + 1;
 
-  float *S = reinterpret_cast<float *>(smem_raw);                  // [parts][c][16]
-  float *red = S + static_cast<size_t>(parts) * c * kSseDT;        // [2][16 row groups][16]
-  uint32_t *ring = reinterpret_cast<uint32_t *>(red + 2 * kSseRG * kSseDT);
-  const int slot_words = SseSlot::words(c, a.rw);                   // multiple of 4
+  float *S = reinterpret_cast<float *>(smem_raw);            // [parts][c][16]
+  float *red = S + static_cast<size_t>(parts) * c * kSseDT;   // [2][8 warps][16]
+  uint32_t *ring = reinterpret_cast<uint32_t *>(red + 2 * 8 * kSseDT);
+  const int slot_words = SseSlot::words(c, a.rw);
   const int col0 = tile * kSseDT;
 
-  // load this column tile of every partition
   float *gS = a.state + bh * static_cast<long>(parts) * c * d;
   for (int e = tid; e < parts * c * (kSseDT / 4); e += kSseThreads) {
     const int row = e / (kSseDT / 4), q4 = e % (kSseDT / 4);
-    const float4 x = *reinterpret_cast<const float4 *>(gS + static_cast<long>(row) * d + col0 + 4 * q4);
-    *reinterpret_cast<float4 *>(S + row * kSseDT + 4 * q4) = x;
+    *reinterpret_cast<float4 *>(S + row * kSseDT + 4 * q4) =
+        *reinterpret_cast<const float4 *>(gS + static_cast<long>(row) * d + col0 + 4 * q4);
   }
 
   const long tok0 = b * T * H + h;
@@ -173,67 +198,73 @@ __global__ void __launch_bounds__(kSseThreads) sse_scan_kernel(const SseArgs a) 
     cp_async_commit();
   }
 
-  const int rpt = c / kSseRG;  // rows per thread: j = rg + 16 i
+  auto emit_y = [&](int t) {  // threads 0..15: column tid, sum of the 8 warp partials of token t
+    const float *rd = red + (t & 1) * 8 * kSseDT;
+    float acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) acc += rd[w * kSseDT + tid];
+    a.y[(tok0 + static_cast<long>(t) * H) * d + col0 + tid] = acc;
+  };
+
   for (int t = 0; t < T; ++t) {
     cp_async_wait<kSseP - 1>();
     __syncthreads();
     if (t + kSseP < T) issue(t + kSseP);
     cp_async_commit();
-    if (t > 0 && rg == 0) {
-      const float *rd = red + ((t - 1) & 1) * kSseRG * kSseDT;
-      float acc = 0.f;
-#pragma unroll
-      for (int g = 0; g < kSseRG; ++g) acc += rd[g * kSseDT + col];
-      a.y[(tok0 + static_cast<long>(t - 1) * H) * d + col0 + col] = acc;
-    }
+    if (t > 0 && tid < kSseDT) emit_y(t - 1);
     const uint32_t *sl = ring + (t % (kSseP + 1)) * slot_words;
     const float *kl = reinterpret_cast<const float *>(sl + SseSlot::klog_off());
     const float *al = reinterpret_cast<const float *>(sl + SseSlot::alpha_off(c));
     const uint16_t *qq = reinterpret_cast<const uint16_t *>(sl + SseSlot::q_off(c));
-    const uint16_t *vv = reinterpret_cast<const uint16_t *>(sl + SseSlot::v_off(c));
+    const uint32_t vw = sl[SseSlot::v_off(c) + cp];  // bf16 pair: columns 2cp, 2cp+1
     const uint32_t *rc = sl + SseSlot::rec_off(c);
     const float kmax = __uint_as_float(rc[2 * topk]);
     const float kinv = __uint_as_float(rc[2 * topk + 1]);
-    const float vcol = bf16_to_f32(vv[col]);
-    float kk[8], aj[8], qj[8];
+    const unsigned long long v2 = pk(bf16_to_f32(vw & 0xffff), bf16_to_f32(vw >> 16));
+    // per own row: decay pair, key weight kk_j, query q_j
+    unsigned long long a2[kSseRPT], q2[kSseRPT];
+    float kk[kSseRPT];
+    bool in[kSseRPT];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      if (i < rpt) {
-        const int j = rg + kSseRG * i;
-        kk[i] = expf(kl[j] - kmax) * kinv;
-        aj[i] = al[j];
-        qj[i] = bf16_to_f32(qq[j]);
-      }
+    for (int i = 0; i < kSseRPT; ++i) {
+      const int j = rg + kSseRows * i;
+      in[i] = j < c;
+      const int jj = in[i] ? j : 0;
+      kk[i] = __expf(kl[jj] - kmax) * kinv;
+      a2[i] = pk(al[jj], al[jj]);
+      const float qv = bf16_to_f32(qq[jj]);
+      q2[i] = pk(qv, qv);
     }
-    float part = 0.f;
+    unsigned long long part = 0ull;
     for (int s = 0; s <= topk; ++s) {
       const int p = s < topk ? static_cast<int>(rc[s]) : N;
       const float g = s < topk ? __uint_as_float(rc[topk + s]) : 1.0f;
-      float *Sp = S + static_cast<size_t>(p) * c * kSseDT;
-      float inner = 0.f;
+      float *Sp = S + static_cast<size_t>(p) * c * kSseDT + 2 * cp;
+      unsigned long long inner = 0ull;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        if (i < rpt) {
-          const int j = rg + kSseRG * i;
-          const float x = fmaf(aj[i], Sp[j * kSseDT + col], (g * kk[i]) * vcol);
-          Sp[j * kSseDT + col] = x;
-          inner = fmaf(qj[i], x, inner);
+      for (int i = 0; i < kSseRPT; ++i) {
+        if (in[i]) {
+          const int j = rg + kSseRows * i;
+          unsigned long long *cell = reinterpret_cast<unsigned long long *>(Sp + j * kSseDT);
+          const float gk = g * kk[i];
+          const unsigned long long x = fma2(a2[i], *cell, mul2(pk(gk, gk), v2));  // alpha_j S + g kk_j v
+          *cell = x;
+          inner = fma2(q2[i], x, inner);
         }
       }
-      part = fmaf(g, inner, part);
+      part = fma2(pk(g, g), inner, part);
     }
-    red[(t & 1) * kSseRG * kSseDT + rg * kSseDT + col] = part;
+    float2 pv = upk(part);
+#pragma unroll
+    for (int m = 8; m <= 16; m <<= 1) {  // the warp's four row groups
+      pv.x += __shfl_xor_sync(kFull, pv.x, m);
+      pv.y += __shfl_xor_sync(kFull, pv.y, m);
+    }
+    if (lane < 8) *reinterpret_cast<float2 *>(red + (t & 1) * 8 * kSseDT + warp * kSseDT + 2 * cp) = pv;
   }
   cp_async_wait<0>();
   __syncthreads();
-  if (T > 0 && rg == 0) {
-    const float *rd = red + ((T - 1) & 1) * kSseRG * kSseDT;
-    float acc = 0.f;
-#pragma unroll
-    for (int g = 0; g < kSseRG; ++g) acc += rd[g * kSseDT + col];
-    a.y[(tok0 + static_cast<long>(T - 1) * H) * d + col0 + col] = acc;
-  }
-  // write the tile of every partition back
+  if (T > 0 && tid < kSseDT) emit_y(T - 1);
   for (int e = tid; e < parts * c * (kSseDT / 4); e += kSseThreads) {
     const int row = e / (kSseDT / 4), q4 = e % (kSseDT / 4);
     *reinterpret_cast<float4 *>(gS + static_cast<long>(row) * d + col0 + 4 * q4) =
@@ -242,7 +273,7 @@ __global__ void __launch_bounds__(kSseThreads) sse_scan_kernel(const SseArgs a) 
 }
 
 size_t sse_smem_bytes(int N, int c, int topk) {
-  return sizeof(float) * (static_cast<size_t>(N + 1) * c * kSseDT + 2 * kSseRG * kSseDT) +
+  return sizeof(float) * (static_cast<size_t>(N + 1) * c * kSseDT + 2 * 8 * kSseDT) +
          sizeof(uint32_t) * (kSseP + 1) * SseSlot::words(c, rec_words(topk));
 }
 
