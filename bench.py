@@ -296,7 +296,10 @@ class GpuRun:
         elif wl.kind in ("gdn", "kda"):
             self.state = torch.zeros((sh.B, sh.H, sh.dk, sh.dv), dtype=torch.float32, device=device)
             self.y = torch.empty((sh.B, sh.T, sh.H, sh.dv), dtype=torch.float32, device=device)
-            self.launches_per_step = 1
+            nws = sdm.gdn_scan_workspace_size(sh.B, sh.T, sh.H, sh.dk, sh.dv, wl.kind == "kda")
+            self.ws = torch.empty(max(nws, 1), dtype=torch.uint8, device=device)
+            # chunked GDN: preparation kernel + chain kernel; KDA: one recurrent kernel
+            self.launches_per_step = 2 if nws > 0 else 1
         else:
             self.state = torch.zeros((sh.B, sh.H, sh.N + 1, sh.c, sh.d), dtype=torch.float32, device=device)
             self.y = torch.empty((sh.B, sh.T, sh.H, sh.d), dtype=torch.float32, device=device)
@@ -321,7 +324,8 @@ class GpuRun:
                               self.wl.mode, self.y, self.ws, self.err)
         elif self.wl.kind in ("gdn", "kda"):
             a = d["alpha_kda" if self.wl.kind == "kda" else "alpha_gdn"]
-            self.sdm.gdn_scan(self.state, d["q"], d["k"], d["v"], a, d["beta"], self.wl.kind == "kda", self.y)
+            self.sdm.gdn_scan(self.state, d["q"], d["k"], d["v"], a, d["beta"], self.wl.kind == "kda", self.y,
+                              workspace=self.ws, dev_err=self.err)
         else:
             self.sdm.sse_scan(self.state, d["route"], sh.topk, d["klog"], d["q"], d["v"], d["alpha"], self.y,
                               None, self.ws, self.err)
@@ -465,7 +469,7 @@ def run_ours(args, rank, world, local_rank, sampler):
         # FP32 FMA pipe: 152 SMs x 128 lanes x 2 flop x max SM clock
         peak = 152 * 128 * 2 * float(pk.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
         achieved = algo / (main_ms * 1e-3) / 1e12
-    kernel_file = {"sdm": "sparse_scan.cu", "gdn": "gdn_scan.cu", "kda": "gdn_scan.cu", "sse": "sse_scan.cu"}[wl.kind]
+    kernel_file = {"sdm": "sparse_scan.cu", "gdn": "gdn_chunk.cu", "kda": "gdn_scan.cu", "sse": "sse_scan.cu"}[wl.kind]
     tr = NCU_TRAFFIC.get((wl.name, wl.kind))
     traffic = tr["bytes"] if tr and tr["digest"] == _src_digest(kernel_file) else None
     tokens = wl.tokens * world
@@ -485,7 +489,7 @@ def run_ours(args, rank, world, local_rank, sampler):
         "config": wl.config(),
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": algo_unit,
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": {"sdm": "sdm_scan (hazard prepass + sparse_scan_kernel)", "gdn": "gdn_scan",
+                     "kernel": {"sdm": "sdm_scan (hazard prepass + sparse_scan_kernel)", "gdn": "gdn_scan (chunk preparation + chain kernels)",
                                 "kda": "gdn_scan", "sse": "sse_scan (route prepass + sse_scan_kernel)"}[wl.kind],
                      "launch_ms": main_ms, "peak_source": f"{src} ({'hbm_gbs' if bound == 'hbm' else 'FP32 lanes x clock'})",
                      **algo_info},

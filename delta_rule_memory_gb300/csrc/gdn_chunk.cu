@@ -4,20 +4,27 @@
 // the granularity of forgetting", Eqs. 15-17).
 //
 // Within a chunk of C = 64 tokens, with lambda_i = sum_{j<=i} log alpha_j,
-// gamma_i = exp(lambda_i), the token recurrence is equivalent to
-//   (I + A) U = diag(beta) (V - diag(gamma) K S0),  A_ij = beta_i e^{l_i-l_j} k_i.k_j (j < i)
-//   Y   = diag(gamma) Q S0 + Mq U,                  Mq_ij = e^{l_i-l_j} q_i.k_j   (j <= i)
-//   S_C = gamma_C S0 + Khat^T U,                    Khat_j = e^{l_C-l_j} k_j
-// Every state contraction is written transposed so that its M dimension is
-// d_v = 128 and the state S^T (d_v x d_k, fp32) stays in tensor memory as an
-// accumulator for the whole sequence.  Operands that are not exact in bf16
-// (the state, R, U, T, Mq, Khat) are split into bf16 hi + lo and multiplied
-// as hi*hi + hi*lo + lo*hi, which keeps fp32-level accuracy.  Decay ratios
-// are always formed as exp(l_i - l_j) with j <= i.
-//
-// One CTA (256 threads, one tensor-memory allocation of 512 columns) runs one
-// (batch, head) sequence chunk by chunk.  Thread (row d = tid % 128,
-// half = tid / 128) owns tensor-memory lane d and half of each tile's columns.
+// gamma_i = exp(lambda_i), L = I + A, A_ij = beta_i e^{l_i-l_j} k_i.k_j (j < i)
+// and T = L^-1 diag(beta), the token recurrence is equivalent to
+//   U   = T V - T diag(gamma) K S0 = Ut - W S0
+//   Y   = diag(gamma) Q S0 + Mq U,     Mq_ij = e^{l_i-l_j} q_i.k_j   (j <= i)
+//   S_C = gamma_C S0 + Khat^T U,       Khat_j = e^{l_C-l_j} k_j
+// Only the products with S0 and with U depend on the state, so the work is
+// split in two kernels:
+//   gdn_prep_kernel  - every chunk in parallel (persistent CTAs): A, the
+//                      triangular inverse, T, then W and Ut by MMA, Mq and
+//                      Khat, written to the workspace as ready-made operand
+//                      tiles of the second kernel.
+//   gdn_chain_kernel - one CTA per (batch, head), chunk after chunk: two
+//                      rounds of MMAs on the state (S^T, d_v x d_k, fp32,
+//                      held in the registers of the worker warps), fed by a
+//                      producer warp; the next chunk's tiles stream in with
+//                      bulk asynchronous copies meanwhile.
+// Every state contraction is written transposed so that its M is d_v = 128.
+// Operands that are not exact in bf16 (state, U, T, W, Mq, Khat) are split
+// into bf16 hi + lo and multiplied as hi*hi + hi*lo + lo*hi, which keeps
+// fp32-level accuracy.  Decay ratios are always formed as exp(l_i - l_j) with
+// j <= i.
 #include <climits>
 
 #include "common.cuh"
@@ -34,42 +41,18 @@ constexpr int kDV = 128;    // value width (the MMA M)
 constexpr int kThreads = 256;
 constexpr uint32_t kWaitLimit = 1u << 20;  // polls (about 0.1 s) before an mbarrier wait gives up
 
-// tensor-memory columns (fp32)
-constexpr uint32_t kColS = 0;     // S^T          [128 x 128]
-constexpr uint32_t kColGP = 128;  // [K;Q] K^T    [128 x 64]: rows 0..63 = K K^T, 64..127 = Q K^T
-constexpr uint32_t kColX = 192;   // S0^T K^T     [128 x 64]
-constexpr uint32_t kColY1 = 256;  // S0^T Q^T     [128 x 64]
-constexpr uint32_t kColU = 320;   // U^T          [128 x 64]
-constexpr uint32_t kColY2 = 384;  // U^T Mq^T     [128 x 64]
-constexpr uint32_t kTmemCols = 512;
-
-// shared memory (bytes); operand tiles are K-major, no swizzle (umma.cuh)
-constexpr uint32_t kOffKQ = 0;                            // [K;Q]: 128 rows x 128, bf16          32 KB
-constexpr uint32_t kOffSh = kOffKQ + 128 * kDK * 2;       // S^T hi: 128 x 128 bf16               32 KB
-constexpr uint32_t kOffSl = kOffSh + 128 * kDK * 2;       // S^T lo                               32 KB
-constexpr uint32_t kOffRU = kOffSl + 128 * kDK * 2;       // R^T / U^T hi+lo: 2 x 128 x 64 bf16   32 KB
-constexpr uint32_t kOffT = kOffRU + 2 * 128 * kC * 2;     // T hi+lo: 2 x 64 x 64 bf16            16 KB
-constexpr uint32_t kOffM = kOffT + 2 * kC * kC * 2;       // Mq hi+lo                             16 KB
-constexpr uint32_t kOffKh = kOffM + 2 * kC * kC * 2;      // Khat^T hi+lo: 2 x 128 x 64 bf16      32 KB
-constexpr uint32_t kOffGate = kOffKh + 2 * 128 * kC * 2;  // per buffer: log alpha, beta, lambda, gamma, e^(l_C-l_j)
-constexpr uint32_t kOffBar = kOffGate + 10 * kC * 4;
-constexpr uint32_t kSmemBytes = kOffBar + 64;
-// scratch views during the triangular solve (regions free at that time)
-constexpr int kLd = kC + 1;                        // padded fp32 row stride
-constexpr uint32_t kOffA = kOffKh;                 // L = I + A, fp32 [64][65]
-constexpr uint32_t kOffTf = kOffRU;                // L^-1, fp32 [64][65]
-constexpr uint32_t kOffZ = kOffRU + kC * kLd * 4;  // block products, fp32 [3][16][16]
-static_assert(kC * kLd * 4 <= 2 * 128 * kC * 2, "A fits in the Khat region");
-static_assert(kC * kLd * 4 + 3 * 256 * 4 <= 2 * 128 * kC * 2, "L^-1 and Z fit in the R/U region");
-
-struct ChunkArgs {
-  float *state;
-  const uint16_t *q, *k, *v;
-  const float *alpha, *beta;
-  float *y;
-  int T, H;
-  int32_t *err;
-};
+// ---- one chunk's tiles in the workspace (bytes; K-major no-swizzle bf16 tiles, umma.cuh)
+constexpr uint32_t kUW = 0;       // W hi, lo        [64 i][128 c]   16 KB each
+constexpr uint32_t kUQ = 32768;   // Q               [64 i][128 c]   16 KB
+constexpr uint32_t kUMq = 49152;  // Mq hi, lo       [64 i][64 j]     8 KB each
+constexpr uint32_t kUKh = 65536;  // Khat^T hi, lo   [128 c][64 j]   16 KB each
+constexpr uint32_t kUG = 98304;   // gamma_i         fp32 [64]
+constexpr uint32_t kUU = 98560;   // Ut = T V        fp32 [64 i][128 d]
+constexpr uint32_t kUnit = kUU + kC * kDV * 4;
+constexpr uint32_t kWBytes = kUMq - kUW;  // W and Q: one bulk copy (round 1 operands)
+constexpr uint32_t kMBytes = kUG - kUMq;  // Mq and Khat: one bulk copy (round 2 operands)
+constexpr uint32_t kGBytes = kUU - kUG;   // gamma
+static_assert(kUnit % 16 == 0 && kWBytes % 16 == 0 && kMBytes % 16 == 0, "bulk copies need 16-byte multiples");
 
 __device__ __forceinline__ uint32_t tmem_addr(uint32_t base, int lane_base, uint32_t col) {
   return base + (static_cast<uint32_t>(lane_base) << 16) + col;
@@ -103,152 +86,186 @@ __device__ __forceinline__ void mma_tile(uint32_t d, uint32_t a, int ka, uint32_
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const ChunkArgs a) {
+// ===========================================================================
+// Kernel 1: the state-independent part of every chunk.
+// ===========================================================================
+struct PrepArgs {
+  const uint16_t *q, *k, *v;
+  const float *alpha, *beta;
+  unsigned char *ws;
+  float *gC;  // gamma_C of every chunk
+  int T, H, nchunks;
+  long units;  // B * H * nchunks
+  int32_t *err;
+};
+
+// shared memory (bytes)
+constexpr uint32_t kPKQ = 0;                    // [K;Q] 128 rows x 128, two buffers     2 x 32 KB
+constexpr uint32_t kPV = kPKQ + 2 * 32768;      // V rows [64][128] bf16 row-major, two   2 x 16 KB
+constexpr uint32_t kPKt = kPV + 2 * 16384;      // K^T [128 c][64 j]                       16 KB
+constexpr uint32_t kPVt = kPKt + 16384;         // V^T [128 d][64 j]                       16 KB
+constexpr uint32_t kPT = kPVt + 16384;          // T hi, lo [64 i][64 j]                   16 KB
+constexpr uint32_t kPTG = kPT + 16384;          // T diag(gamma) hi, lo                    16 KB
+constexpr int kLd = kC + 1;                     // padded fp32 row stride of the solve
+constexpr uint32_t kPA = kPTG + 16384;          // L = I + A, fp32 [64][65]
+constexpr uint32_t kPTf = kPA + kC * kLd * 4;   // L^-1, fp32 [64][65]
+constexpr uint32_t kPZ = kPTf + kC * kLd * 4;   // block products, fp32 [3][16][16]
+constexpr uint32_t kPWst = kPA;                 // W hi, lo staging (32 KB) once the solve is done
+constexpr uint32_t kPGate = kPZ + 3 * 256 * 4;  // per buffer: alpha, beta [64]; then lambda, gamma, tail [64]
+constexpr uint32_t kPBar = kPGate + (2 * 2 + 3) * kC * 4;
+constexpr uint32_t kPrepSmem = kPBar + 64;
+static_assert(kPGate - kPA >= 32768, "W staging fits over the solve's scratch");
+constexpr uint32_t kPColGP = 0, kPColW = 64, kPColU = 128, kPrepTmemCols = 256;
+
+__global__ void __launch_bounds__(kThreads, 1) gdn_prep_kernel(const PrepArgs a) {
   extern __shared__ __align__(1024) unsigned char sm[];
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
-  const int row = tid & 127;  // tensor-memory lane / value row d
-  const int half = tid >> 7;  // which half of each tile's columns
+  const int row = tid & 127;
+  const int half = tid >> 7;
   const int lane_base = 32 * (warp & 3);
-  const long bh = blockIdx.x;
-  const int h = static_cast<int>(bh % a.H);
-  const long b = bh / a.H;
   const int T = a.T, H = a.H;
-  const long tok0 = b * T * H + h;  // token t -> tok0 + t*H
 
-  unsigned char *sKQ = sm + kOffKQ, *sSh = sm + kOffSh, *sSl = sm + kOffSl;
-  unsigned char *sRh = sm + kOffRU, *sRl = sm + kOffRU + 128 * kC * 2;
-  unsigned char *sTh = sm + kOffT, *sTl = sm + kOffT + kC * kC * 2;
-  unsigned char *sMh = sm + kOffM, *sMl = sm + kOffM + kC * kC * 2;
-  unsigned char *sKhh = sm + kOffKh, *sKhl = sm + kOffKh + 128 * kC * 2;
-  float *gate = reinterpret_cast<float *>(sm + kOffGate);  // [2 buffers][log alpha, beta, lambda, gamma, tail][64]
-  float *sA = reinterpret_cast<float *>(sm + kOffA);
-  float *sTf = reinterpret_cast<float *>(sm + kOffTf);
-  float *sZ = reinterpret_cast<float *>(sm + kOffZ);
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kOffBar);
-  uint32_t *holder = reinterpret_cast<uint32_t *>(sm + kOffBar + 40);
-  const uint32_t mbGP = smem_addr(bars + 0), mbXY = smem_addr(bars + 1), mbU = smem_addr(bars + 2),
-                 mbYS = smem_addr(bars + 3), mbEnd = smem_addr(bars + 4);
+  unsigned char *sKt = sm + kPKt, *sVt = sm + kPVt;
+  unsigned char *sTh = sm + kPT, *sTl = sm + kPT + 8192, *sTGh = sm + kPTG, *sTGl = sm + kPTG + 8192;
+  unsigned char *sWh = sm + kPWst, *sWl = sm + kPWst + 16384;
+  float *sA = reinterpret_cast<float *>(sm + kPA);
+  float *sTf = reinterpret_cast<float *>(sm + kPTf);
+  float *sZ = reinterpret_cast<float *>(sm + kPZ);
+  float *gin = reinterpret_cast<float *>(sm + kPGate);  // [buf][alpha 64, beta 64]
+  float *lam = gin + 4 * kC, *gam = gin + 5 * kC, *tail = gin + 6 * kC;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kPBar);
+  uint32_t *holder = reinterpret_cast<uint32_t *>(sm + kPBar + 32);
+  const uint32_t mbGP = smem_addr(bars + 0), mbW = smem_addr(bars + 1), mbEnd = smem_addr(bars + 2);
 
   if (tid == 0) {
     mbar_init(mbGP, 1);
-    mbar_init(mbXY, 1);
-    mbar_init(mbU, 1);
-    mbar_init(mbYS, 1);
+    mbar_init(mbW, 1);
     mbar_init(mbEnd, 1);
+    fence_mbar_init();
   }
-  if (warp == 0) tmem_alloc(smem_addr(holder), kTmemCols);
+  if (warp == 0) tmem_alloc(smem_addr(holder), kPrepTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *holder;
+
+  // K and Q rows into the [K;Q] tile, V rows, alpha and beta of unit u
+  // (padding tokens: k = q = v = 0, alpha = 1, beta = 0)
+  auto load_inputs = [&](long u, int buf) {
+    const long bh = u / a.nchunks;
+    const int t0 = static_cast<int>(u - bh * a.nchunks) * kC;
+    const long tok0 = (bh / H) * T * H + bh % H;
+    unsigned char *kq = sm + kPKQ + buf * 32768, *vr = sm + kPV + buf * 16384;
+    for (int id = tid; id < 128 * 16; id += kThreads) {
+      const int r = id >> 4, k8 = id & 15;
+      const int t = t0 + (r & 63);
+      unsigned char *dst = kq + kmajor_off(r, k8 * 8, kDK);
+      if (t < T)
+        cp_async<16>(dst, (r < 64 ? a.k : a.q) + (tok0 + static_cast<long>(t) * H) * kDK + k8 * 8);
+      else
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+    }
+    for (int id = tid; id < kC * 16; id += kThreads) {
+      const int r = id >> 4, k8 = id & 15;
+      const int t = t0 + r;
+      unsigned char *dst = vr + r * (kDV * 2) + k8 * 16;
+      if (t < T)
+        cp_async<16>(dst, a.v + (tok0 + static_cast<long>(t) * H) * kDV + k8 * 8);
+      else
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+    }
+    if (tid < 2 * kC) {  // the thread that loads alpha_i / beta_i is the one that first reads it
+      const int t = t0 + (tid & 63);
+      float *dst = gin + buf * 2 * kC + tid;
+      if (t < T)
+        cp_async<4>(dst, (tid < kC ? a.alpha : a.beta) + tok0 + static_cast<long>(t) * H);
+      else
+        *dst = tid < kC ? 1.f : 0.f;
+    }
+  };
+
   bool failed = false;
   // every thread waits, then the CTA agrees: either all continue or all stop
   auto wait_ok = [&](uint32_t mb, uint32_t parity) -> bool {
     const bool ok = mbar_wait(mb, parity, kWaitLimit);
+    tc_fence_before();
+    const bool all = __syncthreads_and(ok) != 0;
     tc_fence_after();
-    return __syncthreads_and(ok) != 0;
+    return all;
   };
 
-  // ---- the initial state: S^T into tensor memory and its bf16 split into smem
-  float *gS = a.state + bh * kDK * kDV;
-  for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 16) {
-    float x[16];
-#pragma unroll
-    for (int e = 0; e < 16; ++e) x[e] = gS[static_cast<long>(c0 + e) * kDV + row];  // S[c][d]
-    tmem_st16(tmem_addr(tmem, lane_base, kColS + c0), x);
-    store_split8(sSh, sSl, kmajor_off(row, c0, kDK), x);
-    store_split8(sSh, sSl, kmajor_off(row, c0 + 8, kDK), x + 8);
-  }
-  tmem_st_wait();
-
-  // ---- per-chunk inputs: K and Q rows into the [K;Q] tile, gates into smem
-  auto load_chunk = [&](int c, int buf) {
-    const int t0 = c * kC;
-    for (int id = tid; id < 128 * (kDK / 8); id += kThreads) {
-      const int r = id >> 4, k8 = id & 15;
-      const int t = t0 + (r & 63);
-      unsigned char *dst = sKQ + kmajor_off(r, k8 * 8, kDK);
-      if (t < T) {
-        const uint16_t *src = (r < 64 ? a.k : a.q) + (tok0 + static_cast<long>(t) * H) * kDK + k8 * 8;
-        cp_async<16>(dst, src);
-      } else {
-        *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
-      }
-    }
-    if (tid < kC) {
-      const int t = t0 + tid;
-      float *g = gate + buf * 5 * kC;
-      g[tid] = t < T ? __logf(a.alpha[tok0 + static_cast<long>(t) * H]) : 0.f;  // padding: alpha = 1
-      g[kC + tid] = t < T ? a.beta[tok0 + static_cast<long>(t) * H] : 0.f;       // padding: beta = 0
-    }
-  };
-  // this thread's 32 values of V for a chunk (column d, tokens half*32 ..)
-  uint16_t vreg[32];
-  auto load_v = [&](int c) {
-    const int t0 = c * kC + half * 32;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int t = t0 + i;
-      vreg[i] = t < T ? a.v[(tok0 + static_cast<long>(t) * H) * kDV + row] : static_cast<uint16_t>(0);
-    }
-  };
-
-  const int nchunks = (T + kC - 1) / kC;
-  if (nchunks > 0) {
-    load_chunk(0, 0);
-    load_v(0);
-  }
+  if (static_cast<long>(blockIdx.x) < a.units) load_inputs(blockIdx.x, 0);
   cp_async_commit();
-  for (int c = 0; c < nchunks; ++c) {
-    const int buf = c & 1;
-    const uint32_t par = static_cast<uint32_t>(c & 1);
-    float *g = gate + buf * 5 * kC;  // [0]: log alpha, [1]: beta, [2]: lambda, [3]: gamma, [4]: e^(l_C - l_j)
+  int it = 0;
+  for (long u = blockIdx.x; u < a.units; u += gridDim.x, ++it) {
+    const int buf = it & 1;
+    const uint32_t par = static_cast<uint32_t>(it & 1);
+    unsigned char *ws = a.ws + u * kUnit;
+    const unsigned char *kq = sm + kPKQ + buf * 32768, *vr = sm + kPV + buf * 16384;
+    const float *al = gin + buf * 2 * kC, *be = al + kC;
+
     cp_async_wait<0>();
     // lambda = inclusive prefix sum of log alpha (two warps of 32 tokens)
     if (warp < 2) {
-      float x = g[tid];
+      float x = __logf(al[tid]);
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const float y = __shfl_up_sync(kFull, x, o);
         if ((tid & 31) >= o) x += y;
       }
-      g[2 * kC + tid] = x;
+      lam[tid] = x;
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) g[2 * kC + tid] += g[2 * kC + 31];
+    tc_fence_after();
+    // the next unit's inputs into the other buffer (its readers are done)
+    if (u + gridDim.x < a.units) load_inputs(u + gridDim.x, buf ^ 1);
+    cp_async_commit();
+    if (tid == 0) {  // G = [K;Q] K^T: rows 0..63 K K^T, 64..127 Q K^T
+      const uint32_t kqa = smem_addr(kq);
+      mma_tile(tmem + kPColGP, kqa, kDK, kqa, kDK, kDK / 16, kC, false);
+      mma_commit(mbGP);
+    }
+    if (warp == 1) lam[tid] += lam[31];
     __syncthreads();
     if (tid < kC) {
-      g[3 * kC + tid] = __expf(g[2 * kC + tid]);
-      g[4 * kC + tid] = __expf(g[2 * kC + kC - 1] - g[2 * kC + tid]);
+      gam[tid] = __expf(lam[tid]);
+      tail[tid] = __expf(lam[kC - 1] - lam[tid]);
     }
-    tc_fence_after();
+    __syncthreads();
 
-    // ---- MMAs that need only the chunk's K, Q and the incoming state
-    if (tid == 0) {
-      const uint32_t kq = smem_addr(sKQ);
-      const uint32_t kblk = kq, qblk = kq + 8 * (kDK * 16);  // rows 0..63 = K, 64..127 = Q
-      mma_tile(tmem + kColGP, kq, kDK, kblk, kDK, kDK / 16, kC, false);  // [K;Q] K^T
-      mma_commit(mbGP);
-      mma_tile(tmem + kColX, smem_addr(sSh), kDK, kblk, kDK, kDK / 16, kC, false);  // S^T K^T
-      mma_tile(tmem + kColX, smem_addr(sSl), kDK, kblk, kDK, kDK / 16, kC, true);
-      mma_tile(tmem + kColY1, smem_addr(sSh), kDK, qblk, kDK, kDK / 16, kC, false);  // S^T Q^T
-      mma_tile(tmem + kColY1, smem_addr(sSl), kDK, qblk, kDK, kDK / 16, kC, true);
-      mma_commit(mbXY);
+    // K^T and V^T operand tiles; Khat^T hi/lo straight to the workspace
+    for (int j0 = half * 32; j0 < half * 32 + 32; j0 += 8) {
+      uint16_t kv[8], vv[8];
+      float x[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        kv[e] = *reinterpret_cast<const uint16_t *>(kq + kmajor_off(j0 + e, row, kDK));
+        vv[e] = *reinterpret_cast<const uint16_t *>(vr + (j0 + e) * (kDV * 2) + row * 2);
+        x[e] = tail[j0 + e] * bf16_to_f32(kv[e]);
+      }
+      uint32_t pk[4], pv[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        pk[e] = static_cast<uint32_t>(kv[2 * e]) | (static_cast<uint32_t>(kv[2 * e + 1]) << 16);
+        pv[e] = static_cast<uint32_t>(vv[2 * e]) | (static_cast<uint32_t>(vv[2 * e + 1]) << 16);
+      }
+      *reinterpret_cast<uint4 *>(sKt + kmajor_off(row, j0, kC)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      *reinterpret_cast<uint4 *>(sVt + kmajor_off(row, j0, kC)) = make_uint4(pv[0], pv[1], pv[2], pv[3]);
+      store_split8(ws + kUKh, ws + kUKh + 16384, kmajor_off(row, j0, kC), x);
     }
 
-    // ---- A (decayed, gated K K^T) and Mq (decayed Q K^T) from the GP tile
+    // ---- A (decayed, gated K K^T) and Mq (decayed Q K^T) from G
     if (!wait_ok(mbGP, par)) { failed = true; break; }
-    const float *lam = g + 2 * kC;
     {
       const int i = row & 63;
       const float li = lam[i];
-      const float bi = g[kC + i];
+      const float bi = be[i];
       for (int j0 = half * 32; j0 < half * 32 + 32; j0 += 16) {
         float x[16];
-        tmem_ld16(tmem_addr(tmem, lane_base, kColGP + j0), x);
+        tmem_ld16(tmem_addr(tmem, lane_base, kPColGP + j0), x);
         tmem_ld_wait();
         if (row < 64) {  // strictly lower part of L = I + A (the unit diagonal is implicit)
 #pragma unroll
@@ -256,20 +273,20 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const ChunkArgs 
             const int j = j0 + e;
             sA[i * kLd + j] = j < i ? bi * __expf(li - lam[j]) * x[e] : 0.f;
           }
-        } else {  // Mq, lower part including the diagonal
+        } else {  // Mq, lower part including the diagonal, to the workspace
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int j = j0 + e;
             x[e] = j <= i ? __expf(li - lam[j]) * x[e] : 0.f;
           }
-          store_split8(sMh, sMl, kmajor_off(i, j0, kC), x);
-          store_split8(sMh, sMl, kmajor_off(i, j0 + 8, kC), x + 8);
+          store_split8(ws + kUMq, ws + kUMq + 8192, kmajor_off(i, j0, kC), x);
+          store_split8(ws + kUMq, ws + kUMq + 8192, kmajor_off(i, j0 + 8, kC), x + 8);
         }
       }
     }
     __syncthreads();
 
-    // ---- T = (I + A)^-1 diag(beta): 16x16 diagonal blocks by substitution ...
+    // ---- L^-1: 16x16 diagonal blocks by substitution ...
     if (tid < 64) {
       const int I = tid >> 4, cc = tid & 15, o = I * 16;
       float xv[16];
@@ -309,178 +326,432 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const ChunkArgs 
       }
       __syncthreads();
     }
-    // T = L^-1 diag(beta) (lower triangle), split into the B-operand tile
+    // T = L^-1 diag(beta) and T diag(gamma), lower triangles, as B-operand tiles
     {
       const int i = tid >> 2, j0 = (tid & 3) * 16;
-      float x[16];
+      float x[16], xg[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         const int j = j0 + e;
-        x[e] = j <= i ? sTf[i * kLd + j] * g[kC + j] : 0.f;
+        x[e] = j <= i ? sTf[i * kLd + j] * be[j] : 0.f;
+        xg[e] = x[e] * gam[j];
       }
       store_split8(sTh, sTl, kmajor_off(i, j0, kC), x);
       store_split8(sTh, sTl, kmajor_off(i, j0 + 8, kC), x + 8);
-    }
-    __syncthreads();  // sA (in the Khat region) is no longer read
-    // Khat^T[c][j] = exp(lambda_C - lambda_j) k_j[c] (B operand of the state update)
-    {
-      const float *tail = g + 4 * kC;  // e^(lambda_C - lambda_j)
-      for (int j0 = half * 32; j0 < half * 32 + 32; j0 += 8) {
-        float x[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int j = j0 + e;
-          const uint16_t kb = *reinterpret_cast<const uint16_t *>(sKQ + kmajor_off(j, row, kDK));
-          x[e] = tail[j] * bf16_to_f32(kb);
-        }
-        store_split8(sKhh, sKhl, kmajor_off(row, j0, kC), x);
-      }
-    }
-
-    // ---- R^T = V^T - (S0^T K^T) diag(gamma), split into the A-operand tile
-    if (!wait_ok(mbXY, par)) { failed = true; break; }
-    {
-      const float *gam = g + 3 * kC;
-      for (int i0 = half * 32; i0 < half * 32 + 32; i0 += 16) {
-        float x[16];
-        tmem_ld16(tmem_addr(tmem, lane_base, kColX + i0), x);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 16; ++e) x[e] = bf16_to_f32(vreg[i0 - half * 32 + e]) - gam[i0 + e] * x[e];
-        store_split8(sRh, sRl, kmajor_off(row, i0, kC), x);
-        store_split8(sRh, sRl, kmajor_off(row, i0 + 8, kC), x + 8);
-      }
+      store_split8(sTGh, sTGl, kmajor_off(i, j0, kC), xg);
+      store_split8(sTGh, sTGl, kmajor_off(i, j0 + 8, kC), xg + 8);
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // the chunk's K, Q and V are consumed: prefetch the next chunk
-    if (c + 1 < nchunks) {
-      load_chunk(c + 1, buf ^ 1);
-      load_v(c + 1);
-    }
-    cp_async_commit();
-
-    // ---- U^T = R^T T^T
+    // ---- W^T = K^T (T diag(gamma))^T and Ut^T = V^T T^T
     if (tid == 0) {
-      const uint32_t rh = smem_addr(sRh), rl = smem_addr(sRl), th = smem_addr(sTh), tl = smem_addr(sTl);
-      mma_tile(tmem + kColU, rh, kC, th, kC, kC / 16, kC, false);
-      mma_tile(tmem + kColU, rh, kC, tl, kC, kC / 16, kC, true);
-      mma_tile(tmem + kColU, rl, kC, th, kC, kC / 16, kC, true);
-      mma_commit(mbU);
+      const uint32_t kt = smem_addr(sKt), vt = smem_addr(sVt);
+      mma_tile(tmem + kPColW, kt, kC, smem_addr(sTGh), kC, kC / 16, kC, false);
+      mma_tile(tmem + kPColW, kt, kC, smem_addr(sTGl), kC, kC / 16, kC, true);
+      mma_tile(tmem + kPColU, vt, kC, smem_addr(sTh), kC, kC / 16, kC, false);
+      mma_tile(tmem + kPColU, vt, kC, smem_addr(sTl), kC, kC / 16, kC, true);
+      mma_commit(mbW);
     }
-    if (!wait_ok(mbU, par)) { failed = true; break; }
-    // U^T split into the A-operand tile (over R, whose reads are complete);
-    // S^T scaled by gamma_C in tensor memory before the state update
+    if (tid < kC) reinterpret_cast<float *>(ws + kUG)[tid] = gam[tid];
+    if (tid == 0) a.gC[u] = gam[kC - 1];
+    if (!wait_ok(mbW, par)) { failed = true; break; }
+    // Ut[i][d] to the workspace (thread d: coalesced over d); W^T[c][i] split
+    // into the K-major [64 i][128 c] staging tiles
     {
+      float *gU = reinterpret_cast<float *>(ws + kUU);
       for (int i0 = half * 32; i0 < half * 32 + 32; i0 += 16) {
         float x[16];
-        tmem_ld16(tmem_addr(tmem, lane_base, kColU + i0), x);
-        tmem_ld_wait();
-        store_split8(sRh, sRl, kmajor_off(row, i0, kC), x);
-        store_split8(sRh, sRl, kmajor_off(row, i0 + 8, kC), x + 8);
-      }
-      const float gC = g[3 * kC + kC - 1];
-      for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 16) {
-        float x[16];
-        tmem_ld16(tmem_addr(tmem, lane_base, kColS + c0), x);
+        tmem_ld16(tmem_addr(tmem, lane_base, kPColU + i0), x);
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) x[e] *= gC;
-        tmem_st16(tmem_addr(tmem, lane_base, kColS + c0), x);
-      }
-      tmem_st_wait();
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-
-    // ---- Y2^T = U^T Mq^T and S^T += U^T Khat
-    if (tid == 0) {
-      const uint32_t uh = smem_addr(sRh), ul = smem_addr(sRl);
-      const uint32_t mh = smem_addr(sMh), ml = smem_addr(sMl), kh = smem_addr(sKhh), kl = smem_addr(sKhl);
-      mma_tile(tmem + kColY2, uh, kC, mh, kC, kC / 16, kC, false);
-      mma_tile(tmem + kColY2, uh, kC, ml, kC, kC / 16, kC, true);
-      mma_tile(tmem + kColY2, ul, kC, mh, kC, kC / 16, kC, true);
-      mma_tile(tmem + kColS, uh, kC, kh, kC, kC / 16, kDK, true);
-      mma_tile(tmem + kColS, uh, kC, kl, kC, kC / 16, kDK, true);
-      mma_tile(tmem + kColS, ul, kC, kh, kC, kC / 16, kDK, true);
-      mma_commit(mbYS);
-    }
-    if (!wait_ok(mbYS, par)) { failed = true; break; }
-
-    // ---- y = gamma_i (S0^T Q^T)[:, i] + (U^T Mq^T)[:, i], and the new state's split
-    {
-      const float *gam = g + 3 * kC;
-      const int t0 = c * kC;
-      for (int i0 = half * 32; i0 < half * 32 + 32; i0 += 16) {
-        float y1[16], y2[16];
-        tmem_ld16(tmem_addr(tmem, lane_base, kColY1 + i0), y1);
-        tmem_ld16(tmem_addr(tmem, lane_base, kColY2 + i0), y2);
+        for (int e = 0; e < 16; ++e) gU[(i0 + e) * kDV + row] = x[e];
+        tmem_ld16(tmem_addr(tmem, lane_base, kPColW + i0), x);
         tmem_ld_wait();
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const int t = t0 + i0 + e;
-          if (t < T) a.y[(tok0 + static_cast<long>(t) * H) * kDV + row] = fmaf(gam[i0 + e], y1[e], y2[e]);
+          const __nv_bfloat16 hb = __float2bfloat16_rn(x[e]);
+          const __nv_bfloat16 lb = __float2bfloat16_rn(x[e] - __bfloat162float(hb));
+          const uint32_t off = kmajor_off(i0 + e, row, kDK);
+          *reinterpret_cast<__nv_bfloat16 *>(sWh + off) = hb;
+          *reinterpret_cast<__nv_bfloat16 *>(sWl + off) = lb;
         }
       }
-      for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 16) {
-        float x[16];
-        tmem_ld16(tmem_addr(tmem, lane_base, kColS + c0), x);
-        tmem_ld_wait();
-        store_split8(sSh, sSl, kmajor_off(row, c0, kDK), x);
-        store_split8(sSh, sSl, kmajor_off(row, c0 + 8, kDK), x + 8);
-      }
     }
-    fence_async_smem();
+    __syncthreads();
+    for (int o = tid * 16; o < 2 * 16384; o += kThreads * 16)
+      *reinterpret_cast<uint4 *>(ws + kUW + o) = *reinterpret_cast<const uint4 *>(sWh + o);
+    for (int o = tid * 16; o < 16384; o += kThreads * 16)  // Q rows of [K;Q] (rows 64..127: the upper 16 KB)
+      *reinterpret_cast<uint4 *>(ws + kUQ + o) = *reinterpret_cast<const uint4 *>(kq + 16384 + o);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
   }
   cp_async_wait<0>();
   if (failed) {
-    // stop cleanly: wait (bounded) for this CTA's tensor-core work, report
+    // a tensor-core wait ran out: drain this CTA's MMAs (bounded) and report;
+    // the chain kernel then reads invalid tiles but ends normally
     if (tid == 0) mma_commit(mbEnd);
     mbar_wait(mbEnd, 0, kWaitLimit);
     if (tid == 0 && a.err) atomicOr(a.err, SDM_DEVERR_TIMEOUT);
-  } else {
-    // ---- the final state back to HBM (S[c][d] = S^T[d][c])
-    for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 16) {
-      float x[16];
-      tmem_ld16(tmem_addr(tmem, lane_base, kColS + c0), x);
-      tmem_ld_wait();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, kPrepTmemCols);
+}
+
+// ===========================================================================
+// Kernel 2: the chain of chunks of one (batch, head).
+//
+// Warps 0-15 (workers): warp w owns tensor-memory lanes 32*(w%4) .. +31
+// (value rows d) and quarter w/4 of each tile's columns; it keeps its 32
+// columns of S^T in registers.  Warp 16 (producer, one lane) issues the bulk
+// copies and the MMAs.  Per chunk:
+//   round 1  X = S0^T W^T (then Y1 = S0^T Q^T), issued in two column groups as
+//            the workers publish the bf16 split of S0 (S_ready[g]);
+//   workers  U^T = Ut^T - X, split, published (U_ready);
+//   round 2  Y2 = U^T Mq^T, then D = U^T Khat;
+//   workers  y = gamma_i Y1 + Y2; S^T <- gamma_C S^T + D, split for the next
+//            round 1.
+// ===========================================================================
+struct ChainArgs {
+  float *state;
+  const unsigned char *ws;
+  const float *gC;
+  float *y;
+  int T, H, nchunks;
+  int32_t *err;
+};
+
+constexpr int kWorkers = 512;
+constexpr int kChainThreads = kWorkers + 32;
+
+// tensor-memory columns (fp32)
+constexpr uint32_t kColD = 0;     // U^T Khat     [128 d x 128 c]
+constexpr uint32_t kColX = 128;   // S0^T W^T     [128 x 64]
+constexpr uint32_t kColY1 = 192;  // S0^T Q^T     [128 x 64]
+constexpr uint32_t kColY2 = 256;  // U^T Mq^T     [128 x 64]
+constexpr uint32_t kChainTmemCols = 512;
+
+// shared memory (bytes)
+constexpr uint32_t kCS = 0;               // S^T hi, lo [128 d][128 c]        2 x 32 KB
+constexpr uint32_t kCU = kCS + 65536;     // U^T hi, lo [128 d][64 j]         2 x 16 KB
+constexpr uint32_t kCW = kCU + 32768;     // W hi, lo, Q (bulk copy)          48 KB
+constexpr uint32_t kCM = kCW + kWBytes;   // Mq hi, lo, Khat^T hi, lo (bulk)  48 KB
+constexpr uint32_t kCG = kCM + kMBytes;   // gamma_i, two buffers             2 x 256 B
+constexpr uint32_t kCBar = kCG + 2 * kGBytes;
+constexpr int kNBar = 12;
+constexpr uint32_t kChainSmem = kCBar + kNBar * 8 + 16;
+
+// bounded wait that also gives up as soon as another thread has
+__device__ __forceinline__ bool chain_wait(uint32_t mbar, uint32_t parity, volatile int *abort_flag) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(done)
+        : "r"(mbar), "r"(parity)
+        : "memory");
+    if (done) {
+      tc_fence_after();
+      return true;
+    }
+    if (i > 64) {
+      if (*abort_flag) return false;
+      __nanosleep(64);
+    }
+  }
+  *abort_flag = 1;
+  return false;
+}
+
+__global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
+  extern __shared__ __align__(1024) unsigned char sm[];
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const long bh = blockIdx.x;
+  const int T = a.T, H = a.H, n = a.nchunks;
+  const long tok0 = (bh / H) * T * H + bh % H;  // token t -> tok0 + t*H
+  const long u0 = bh * n;
+
+  unsigned char *sSh = sm + kCS, *sSl = sm + kCS + 32768;
+  unsigned char *sUh = sm + kCU, *sUl = sm + kCU + 16384;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kCBar);
+  // barriers: 0 W, 1 M, 2-3 gamma buffers, 4 X done, 5 round 1 done, 6 Y2 done,
+  // 7 round 2 done, 8-9 S_ready[g], 10 U_ready, 11 drain
+  auto bar = [&](int i) { return smem_addr(bars + i); };
+  uint32_t *holder = reinterpret_cast<uint32_t *>(sm + kCBar + kNBar * 8);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + kCBar + kNBar * 8 + 4);
+
+  if (tid == 0) {
+    for (int i = 0; i < 8; ++i) mbar_init(bar(i), 1);
+    for (int i = 8; i < 11; ++i) mbar_init(bar(i), kWorkers);
+    mbar_init(bar(11), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(smem_addr(holder), kChainTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *holder;
+
+  if (warp < kWorkers / 32) {
+    // ------------------------------------------------------------ workers
+    const int row = 32 * (warp & 3) + (tid & 31), qtr = warp >> 2;
+    const uint32_t lanes = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    // waits agree across the warp (its tensor-memory loads are warp-wide)
+    auto wwait = [&](uint32_t mb, uint32_t parity) -> bool {
+      return __all_sync(kFull, chain_wait(mb, parity, abort_flag)) != 0;
+    };
+    float *gS = a.state + bh * kDK * kDV;
+    float S[32];  // S^T[row][32*qtr + j]
 #pragma unroll
-      for (int e = 0; e < 16; ++e) gS[static_cast<long>(c0 + e) * kDV + row] = x[e];
+    for (int j = 0; j < 32; ++j) S[j] = gS[static_cast<long>(32 * qtr + j) * kDV + row];
+    // publish the bf16 split of columns [32*qtr + 16g, +16) of S^T
+    auto publish_s = [&](int g) {
+      store_split8(sSh, sSl, kmajor_off(row, 32 * qtr + 16 * g, kDK), S + 16 * g);
+      store_split8(sSh, sSl, kmajor_off(row, 32 * qtr + 16 * g + 8, kDK), S + 16 * g + 8);
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(8 + g));
+    };
+    publish_s(0);
+    publish_s(1);
+    float ut[16];  // Ut[16*qtr + e][row] of the next chunk
+    auto load_ut = [&](int c) {
+      const float *src = reinterpret_cast<const float *>(a.ws + (u0 + c) * kUnit + kUU) + row;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) ut[e] = __ldg(src + (16 * qtr + e) * kDV);
+    };
+    load_ut(0);
+    for (int c = 0; c < n; ++c) {
+      const uint32_t par = static_cast<uint32_t>(c & 1);
+      const bool last = c + 1 == n;
+      const float gc = __ldg(a.gC + u0 + c);
+      // U^T = Ut^T - X for this warp's 16 tokens
+      if (!wwait(bar(4), par)) break;
+      {
+        float x[16];
+        tmem_ld16(lanes + kColX + 16 * qtr, x);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) x[e] = ut[e] - x[e];
+        store_split8(sUh, sUl, kmajor_off(row, 16 * qtr, kC), x);
+        store_split8(sUh, sUl, kmajor_off(row, 16 * qtr + 8, kC), x + 8);
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar(10));
+      }
+      if (!last) load_ut(c + 1);
+      // y = gamma_i Y1 + Y2
+      if (!wwait(bar(6), par)) break;
+      if (!wwait(bar(2 + (c & 1)), static_cast<uint32_t>((c >> 1) & 1))) break;
+      {
+        const float *gam = reinterpret_cast<const float *>(sm + kCG + (c & 1) * kGBytes) + 16 * qtr;
+        const int t0 = c * kC + 16 * qtr;
+        float *yp = a.y + (tok0 + static_cast<long>(t0) * H) * kDV + row;
+#pragma unroll
+        for (int h8 = 0; h8 < 16; h8 += 8) {
+          float y1[8], y2[8];
+          tmem_ld8(lanes + kColY1 + 16 * qtr + h8, y1);
+          tmem_ld8(lanes + kColY2 + 16 * qtr + h8, y2);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            if (t0 + h8 + e < T) yp[static_cast<long>(h8 + e) * H * kDV] = fmaf(gam[h8 + e], y1[e], y2[e]);
+        }
+      }
+      // S^T <- gamma_C S^T + D, published group by group for the next round 1
+      if (!wwait(bar(7), par)) break;
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        float x[16];
+        tmem_ld16(lanes + kColD + 32 * qtr + 16 * g, x);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) S[16 * g + e] = fmaf(gc, S[16 * g + e], x[e]);
+        if (!last) publish_s(g);
+      }
+      if (last) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) gS[static_cast<long>(32 * qtr + j) * kDV + row] = S[j];
+      }
+    }
+  } else if (tid == kWorkers) {
+    // ------------------------------------------------------------ producer
+    const uint32_t sh = smem_addr(sSh), sl = smem_addr(sSl), uh = smem_addr(sUh), ul = smem_addr(sUl);
+    const uint32_t wh = smem_addr(sm + kCW), wl = wh + 16384, qa = wh + 32768;
+    const uint32_t mh = smem_addr(sm + kCM), ml = mh + 8192, kh = mh + 16384, kl = mh + 32768;
+    const uint32_t id64 = idesc_bf16_f32(128, kC), id128 = idesc_bf16_f32(128, kDK);
+    // operand descriptors at k-step 0; k-step ks starts 256 bytes further on,
+    // i.e. 16 in the descriptor's address field
+    const uint64_t dSh = smem_desc(sh, 128, kDK * 16), dSl = smem_desc(sl, 128, kDK * 16);
+    const uint64_t dWh = smem_desc(wh, 128, kDK * 16), dWl = smem_desc(wl, 128, kDK * 16);
+    const uint64_t dQ = smem_desc(qa, 128, kDK * 16);
+    const uint64_t dUh = smem_desc(uh, 128, kC * 16), dUl = smem_desc(ul, 128, kC * 16);
+    const uint64_t dMh = smem_desc(mh, 128, kC * 16), dMl = smem_desc(ml, 128, kC * 16);
+    const uint64_t dKh = smem_desc(kh, 128, kC * 16), dKl = smem_desc(kl, 128, kC * 16);
+    auto mma = [&](uint32_t d, uint64_t A, uint64_t Bm, int ks, uint32_t idesc, bool acc) {
+      mma_bf16(d, A + 16u * ks, Bm + 16u * ks, idesc, acc);
+    };
+    int w_issued = 0, w_done = 0, m_issued = 0, m_done = 0, g_issued = 0, g_done = 0;
+    auto load = [&](int which, int c) {
+      const unsigned char *src = a.ws + (u0 + c) * kUnit;
+      fence_async_smem();
+      if (which == 0) {
+        mbar_expect_tx(bar(0), kWBytes);
+        bulk_g2s(wh, src + kUW, kWBytes, bar(0));
+        ++w_issued;
+      } else {
+        mbar_expect_tx(bar(1), kMBytes);
+        bulk_g2s(mh, src + kUMq, kMBytes, bar(1));
+        mbar_expect_tx(bar(2 + (c & 1)), kGBytes);
+        bulk_g2s(smem_addr(sm + kCG + (c & 1) * kGBytes), src + kUG, kGBytes, bar(2 + (c & 1)));
+        ++m_issued;
+        ++g_issued;
+      }
+    };
+    // the operands of chunk c into L2 ahead of their copies (three pieces of at most 48 KB)
+    auto prefetch = [&](int c) {
+      const unsigned char *pf = a.ws + (u0 + c) * kUnit;
+      prefetch_l2(pf + kUW, kWBytes);
+      prefetch_l2(pf + kUMq, kMBytes + kGBytes);
+      prefetch_l2(pf + kUU, kUnit - kUU);
+    };
+    if (n > 1) prefetch(1);
+    load(0, 0);
+    load(1, 0);
+    bool ok = true;
+    for (int c = 0; c < n && ok; ++c) {
+      const uint32_t par = static_cast<uint32_t>(c & 1);
+      if (c + 2 < n) prefetch(c + 2);  // chunk c + 2 into L2 while this one runs
+      // round 1, column group g = k-steps g, g + 2, g + 4, g + 6 of S^T
+      ok = chain_wait(bar(0), par, abort_flag);
+      if (ok) ++w_done;
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        if (ok) ok = chain_wait(bar(8 + g), par, abort_flag);
+        if (!ok) break;
+#pragma unroll
+        for (int ks = g; ks < 8; ks += 2) {
+          mma(tmem + kColX, dSh, dWh, ks, id64, ks != 0);
+          mma(tmem + kColX, dSh, dWl, ks, id64, true);
+          mma(tmem + kColX, dSl, dWh, ks, id64, true);
+        }
+        if (g == 1) mma_commit(bar(4));
+#pragma unroll
+        for (int ks = g; ks < 8; ks += 2) {
+          mma(tmem + kColY1, dSh, dQ, ks, id64, ks != 0);
+          mma(tmem + kColY1, dSl, dQ, ks, id64, true);
+        }
+      }
+      if (!ok) break;
+      mma_commit(bar(5));
+      // round 2
+      ok = chain_wait(bar(1), par, abort_flag);
+      if (ok) ++m_done;
+      if (ok) ok = chain_wait(bar(10), par, abort_flag);
+      if (!ok) break;
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        mma(tmem + kColY2, dUh, dMh, ks, id64, ks != 0);
+        mma(tmem + kColY2, dUh, dMl, ks, id64, true);
+        mma(tmem + kColY2, dUl, dMh, ks, id64, true);
+      }
+      mma_commit(bar(6));
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        mma(tmem + kColD, dUh, dKh, ks, id128, ks != 0);
+        mma(tmem + kColD, dUh, dKl, ks, id128, true);
+        mma(tmem + kColD, dUl, dKh, ks, id128, true);
+      }
+      mma_commit(bar(7));
+      if (c + 1 < n) {
+        // the next chunk's operands, each as soon as its buffer is free
+        ok = chain_wait(bar(5), par, abort_flag);
+        if (ok) load(0, c + 1);
+        if (ok) ok = chain_wait(bar(7), par, abort_flag);
+        if (ok) load(1, c + 1);
+      }
+    }
+    if (!ok || *abort_flag) {
+      // stop cleanly: wait (bounded) for the MMAs and the bulk copies in flight
+      mma_commit(bar(11));
+      mbar_wait(bar(11), 0, kWaitLimit);
+      while (w_done < w_issued) mbar_wait(bar(0), static_cast<uint32_t>(w_done++ & 1), kWaitLimit);
+      while (m_done < m_issued) mbar_wait(bar(1), static_cast<uint32_t>(m_done++ & 1), kWaitLimit);
+      for (; g_done < g_issued; ++g_done)
+        mbar_wait(bar(2 + (g_done & 1)), static_cast<uint32_t>((g_done >> 1) & 1), kWaitLimit);
+      *abort_flag = 1;
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+  if (tid == 0 && *abort_flag && a.err) atomicOr(a.err, SDM_DEVERR_TIMEOUT);
+  if (warp == 0) tmem_dealloc(tmem, kChainTmemCols);
 }
 
 }  // namespace
 
+// workspace of the chunked GDN path: one unit of tiles per chunk, then gamma_C
+// of every chunk
+size_t gdn_chunk_workspace_size(int B, int T, int H) {
+  const long units = static_cast<long>(B) * H * ((T + kC - 1) / kC);
+  const size_t n = static_cast<size_t>(units) * (kUnit + sizeof(float));
+  return (n + 255) & ~static_cast<size_t>(255);
+}
+
 // launched by gdn_scan for dense GDN with d_k = d_v = 128
 int launch_gdn_chunk(float *state, const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
-                     const float *beta, int B, int T, int H, float *y, int32_t *err, cudaStream_t st) {
-  ChunkArgs args;
-  args.state = state;
-  args.q = q;
-  args.k = k;
-  args.v = v;
-  args.alpha = alpha;
-  args.beta = beta;
-  args.y = y;
-  args.T = T;
-  args.H = H;
-  args.err = err;
-  if (cudaFuncSetAttribute(gdn_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(kSmemBytes)) != cudaSuccess)
+                     const float *beta, int B, int T, int H, float *y, void *workspace, int32_t *err,
+                     cudaStream_t st) {
+  const int nchunks = (T + kC - 1) / kC;
+  const long units = static_cast<long>(B) * H * nchunks;
+  unsigned char *ws = static_cast<unsigned char *>(workspace);
+  float *gC = reinterpret_cast<float *>(ws + static_cast<size_t>(units) * kUnit);
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+
+  PrepArgs pa;
+  pa.q = q;
+  pa.k = k;
+  pa.v = v;
+  pa.alpha = alpha;
+  pa.beta = beta;
+  pa.ws = ws;
+  pa.gC = gC;
+  pa.T = T;
+  pa.H = H;
+  pa.nchunks = nchunks;
+  pa.units = units;
+  pa.err = err;
+  if (cudaFuncSetAttribute(gdn_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kPrepSmem)) != cudaSuccess)
     return check_launch("gdn_scan: set shared memory");
-  gdn_chunk_kernel<<<static_cast<unsigned>(static_cast<long>(B) * H), kThreads, kSmemBytes, st>>>(args);
-  return check_launch("gdn_scan: chunk kernel");
+  const long pgrid = units < sms ? units : sms;
+  gdn_prep_kernel<<<static_cast<unsigned>(pgrid), kThreads, kPrepSmem, st>>>(pa);
+  const int rc = check_launch("gdn_scan: chunk preparation kernel");
+  if (rc != SDM_OK) return rc;
+
+  ChainArgs ca;
+  ca.state = state;
+  ca.ws = ws;
+  ca.gC = gC;
+  ca.y = y;
+  ca.T = T;
+  ca.H = H;
+  ca.nchunks = nchunks;
+  ca.err = err;
+  if (cudaFuncSetAttribute(gdn_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kChainSmem)) != cudaSuccess)
+    return check_launch("gdn_scan: set shared memory");
+  gdn_chain_kernel<<<static_cast<unsigned>(static_cast<long>(B) * H), kChainThreads, kChainSmem, st>>>(ca);
+  return check_launch("gdn_scan: chunk chain kernel");
 }
 
 }  // namespace sdm

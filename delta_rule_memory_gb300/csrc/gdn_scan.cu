@@ -140,22 +140,32 @@ __global__ void __launch_bounds__(kGdnWarps * 32) gdn_recurrent_kernel(const Gdn
 
 }  // namespace
 
+size_t gdn_chunk_workspace_size(int B, int T, int H);
 int launch_gdn_chunk(float *state, const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
-                     const float *beta, int B, int T, int H, float *y, int32_t *err, cudaStream_t st);
+                     const float *beta, int B, int T, int H, float *y, void *workspace, int32_t *err,
+                     cudaStream_t st);
+
+// dense GDN at d_k = d_v = 128 runs chunkwise on the tensor cores; every other
+// shape (and KDA) runs token by token.  SDM_GDN_PATH=recurrent forces the
+// token-by-token kernel (for cross-checks).
+static bool use_chunked(int dk, int dv, int per_channel) {
+  const char *path = getenv("SDM_GDN_PATH");
+  const bool want_recurrent = path && path[0] == 'r';
+  return !per_channel && dk == 128 && dv == 128 && !want_recurrent;
+}
 
 }  // namespace sdm
 
 using namespace sdm;
 
 extern "C" size_t gdn_scan_workspace_size(int B, int T, int H, int dk, int dv, int per_channel) {
-  (void)B; (void)T; (void)H; (void)dk; (void)dv; (void)per_channel;
-  return 0;
+  if (B <= 0 || T <= 0 || H <= 0 || !use_chunked(dk, dv, per_channel)) return 0;
+  return gdn_chunk_workspace_size(B, T, H);
 }
 
 extern "C" int gdn_scan(float *state, const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
                         int per_channel, const float *beta, int B, int T, int H, int dk, int dv, float *y,
                         void *workspace, size_t workspace_bytes, int32_t *dev_err, void *stream) {
-  (void)workspace; (void)workspace_bytes;
   if (!state || !q || !k || !v || !alpha || !beta || !y) return set_error(SDM_ERR_INVALID_ARG, "gdn_scan: null pointer");
   if (B < 0 || T < 0 || H < 0) return set_error(SDM_ERR_INVALID_ARG, "gdn_scan: negative size");
   if ((dk != 16 && dk != 32 && dk != 64 && dk != 128) || dv < 32 || dv % 32 != 0 || dv > 256)
@@ -167,13 +177,13 @@ extern "C" int gdn_scan(float *state, const uint16_t *q, const uint16_t *k, cons
   if (B == 0 || T == 0 || H == 0) return SDM_OK;
   if (dev_err && !aligned(dev_err, 4)) return set_error(SDM_ERR_ALIGN, "gdn_scan: dev_err must be 4-byte aligned");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // dense GDN at d_k = d_v = 128: chunkwise form on the tensor cores; every
-  // other shape (and KDA) runs token by token.  SDM_GDN_PATH=recurrent forces
-  // the token-by-token kernel (for cross-checks).
-  const char *path = getenv("SDM_GDN_PATH");
-  const bool want_recurrent = path && path[0] == 'r';
-  if (!per_channel && dk == 128 && dv == 128 && !want_recurrent)
-    return launch_gdn_chunk(state, q, k, v, alpha, beta, B, T, H, y, dev_err, st);
+  if (use_chunked(dk, dv, per_channel)) {
+    const size_t need = gdn_chunk_workspace_size(B, T, H);
+    if (!workspace || workspace_bytes < need)
+      return set_error(SDM_ERR_INVALID_ARG, "gdn_scan: workspace of %zu bytes needed", need);
+    if (!aligned(workspace, 16)) return set_error(SDM_ERR_ALIGN, "gdn_scan: workspace must be 16-byte aligned");
+    return launch_gdn_chunk(state, q, k, v, alpha, beta, B, T, H, y, workspace, dev_err, st);
+  }
   GdnArgs args;
   args.state = state;
   args.q = q;

@@ -208,8 +208,11 @@ SDM_API int sdm_scan_noalloc(float *state, const void *v, int v_dtype, const flo
                      void *stream);
 
 /*
- * Scratch bytes gdn_scan needs (0 for the current kernels; kept so callers
- * can size a workspace once and keep the call stable).
+ * Scratch bytes gdn_scan needs.  Dense GDN at dk = dv = 128 (the chunked
+ * tensor-core path) needs one tile set per chunk of 64 tokens (operands of
+ * the state-dependent products: 114,944 bytes) plus 4 bytes per chunk,
+ * rounded up to 256: about 1.8 KB per token-head.  Every other shape, KDA, and
+ * SDM_GDN_PATH=recurrent need none (0).
  */
 SDM_API size_t gdn_scan_workspace_size(int B, int T, int H, int dk, int dv, int per_channel);
 
@@ -228,11 +231,17 @@ SDM_API size_t gdn_scan_workspace_size(int B, int T, int H, int dk, int dv, int 
  * q, k  : bf16 [B,T,H,dk];  v : bf16 [B,T,H,dv].
  * alpha : fp32 [B,T,H] (GDN) or [B,T,H,dk] (KDA).   beta : fp32 [B,T,H].
  * y     : fp32 [B,T,H,dv].
+ * workspace : device scratch of gdn_scan_workspace_size() bytes, 16-byte
+ *           aligned, owned by the caller (NULL allowed when that size is 0);
+ *           its contents on return are undefined.  Too small: SDM_ERR_INVALID_ARG.
  * dev_err : optional; SDM_DEVERR_TIMEOUT if a bounded wait of the tensor-core
- *           kernel gave up (outputs then invalid).
+ *           kernels gave up (outputs then invalid).
  * Kernels: dense GDN with dk = dv = 128 runs chunkwise (64 tokens) on the
- *          tensor cores ([SDM] App. A.1-A.2, Eq. 7, dense case; the state stays
- *          in tensor memory); KDA and other widths run token by token in fp32.
+ *          tensor cores ([SDM] App. A.1-A.2, Eq. 7, dense case): a kernel
+ *          parallel over all chunks prepares each chunk's state-independent
+ *          operands in the workspace, then one CTA per (batch, head) runs the
+ *          chunks in order with the state in tensor memory.  KDA and other
+ *          widths run token by token in fp32.
  * Limits: dk in {16, 32, 64, 128}; dv % 32 == 0, dv <= 256.  state and y
  *         16-byte aligned; q, k, v 16-byte aligned (dk, dv multiples of 8).
  */
