@@ -42,10 +42,10 @@ constexpr int kThreads = 256;
 constexpr uint32_t kWaitLimit = 1u << 20;  // polls (about 0.1 s) before an mbarrier wait gives up
 
 // ---- one chunk's tiles in the workspace (bytes; K-major no-swizzle bf16 tiles, umma.cuh)
-constexpr uint32_t kUW = 0;       // W hi, lo        [64 i][128 c]   16 KB each
+constexpr uint32_t kUW = 0;       // W hi, lo        [64 i][128 c]   16 KB each, MN-major (8 tokens per 16 B)
 constexpr uint32_t kUQ = 32768;   // Q               [64 i][128 c]   16 KB
 constexpr uint32_t kUMq = 49152;  // Mq hi, lo       [64 i][64 j]     8 KB each
-constexpr uint32_t kUKh = 65536;  // Khat^T hi, lo   [128 c][64 j]   16 KB each
+constexpr uint32_t kUKh = 65536;  // Khat hi, lo     [64 j][128 c]   16 KB each, MN-major B of S^T += U^T Khat
 constexpr uint32_t kUG = 98304;   // gamma_i         fp32 [64]
 constexpr uint32_t kUU = 98560;   // Ut = T V        fp32 [64 i][128 d]
 constexpr uint32_t kUnit = kUU + kC * kDV * 4;
@@ -74,20 +74,15 @@ __device__ __forceinline__ void store_split8(unsigned char *hi, unsigned char *l
   *reinterpret_cast<uint4 *>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
-// issue `ksteps` MMAs of K = 16 into d (M = 128, N); A and B K-major tiles
-// whose rows hold ka and kb elements
-__device__ __forceinline__ void mma_tile(uint32_t d, uint32_t a, int ka, uint32_t b, int kb, int ksteps, int N,
-                                         bool accumulate) {
-  const uint32_t idesc = idesc_bf16_f32(128, N);
-  for (int s = 0; s < ksteps; ++s) {
-    const uint64_t ad = smem_desc(a + s * 256, 128, ka * 16);
-    const uint64_t bd = smem_desc(b + s * 256, 128, kb * 16);
-    mma_bf16(d, ad, bd, idesc, accumulate || s > 0);
-  }
-}
-
 // ===========================================================================
 // Kernel 1: the state-independent part of every chunk.
+//
+// Operand tiles (umma.cuh) are read either K-major or MN-major: the K and V
+// tiles as loaded, [64 j][128 c] with 8 consecutive c per 16-byte row, are
+// the K-major B operand of K K^T and also the MN-major A operands of
+// W^T = K^T (T diag(gamma))^T and Ut^T = V^T T^T (descriptor: LBO = 2048, the
+// stride between 8-token groups; SBO = 128, the stride between 8-column
+// groups).  Two CTAs share an SM.
 // ===========================================================================
 struct PrepArgs {
   const uint16_t *q, *k, *v;
@@ -99,25 +94,26 @@ struct PrepArgs {
   int32_t *err;
 };
 
+constexpr int kPrepCtasPerSm = 2;
+constexpr int kLd = kC;  // fp32 row stride of the solve (columns swizzled, sw())
 // shared memory (bytes)
-constexpr uint32_t kPKQ = 0;                    // [K;Q] 128 rows x 128, two buffers     2 x 32 KB
-constexpr uint32_t kPV = kPKQ + 2 * 32768;      // V rows [64][128] bf16 row-major, two   2 x 16 KB
-constexpr uint32_t kPKt = kPV + 2 * 16384;      // K^T [128 c][64 j]                       16 KB
-constexpr uint32_t kPVt = kPKt + 16384;         // V^T [128 d][64 j]                       16 KB
-constexpr uint32_t kPT = kPVt + 16384;          // T hi, lo [64 i][64 j]                   16 KB
+constexpr uint32_t kPK = 0;                     // K rows [64 j][128 c]                    16 KB
+constexpr uint32_t kPQ = kPK + 16384;           // Q rows [64 i][128 c] (rows 64..127 of [K;Q]); then L = I + A
+constexpr uint32_t kPV = kPQ + 16384;           // V rows [64 j][128 d]                    16 KB
+constexpr uint32_t kPT = kPV + 16384;           // T hi, lo [64 i][64 j]; block products during the solve
 constexpr uint32_t kPTG = kPT + 16384;          // T diag(gamma) hi, lo                    16 KB
-constexpr int kLd = kC + 1;                     // padded fp32 row stride of the solve
-constexpr uint32_t kPA = kPTG + 16384;          // L = I + A, fp32 [64][65]
-constexpr uint32_t kPTf = kPA + kC * kLd * 4;   // L^-1, fp32 [64][65]
-constexpr uint32_t kPZ = kPTf + kC * kLd * 4;   // block products, fp32 [3][16][16]
-constexpr uint32_t kPWst = kPA;                 // W hi, lo staging (32 KB) once the solve is done
-constexpr uint32_t kPGate = kPZ + 3 * 256 * 4;  // per buffer: alpha, beta [64]; then lambda, gamma, tail [64]
-constexpr uint32_t kPBar = kPGate + (2 * 2 + 3) * kC * 4;
+constexpr uint32_t kPTf = kPTG + 16384;         // L^-1, fp32 [64][64]                     16 KB
+constexpr uint32_t kPGate = kPTf + 16384;       // alpha, beta, lambda, gamma, tail [64] each
+constexpr uint32_t kPBar = kPGate + 5 * kC * 4;
 constexpr uint32_t kPrepSmem = kPBar + 64;
-static_assert(kPGate - kPA >= 32768, "W staging fits over the solve's scratch");
 constexpr uint32_t kPColGP = 0, kPColW = 64, kPColU = 128, kPrepTmemCols = 256;
+static_assert(2 * (kPrepSmem + 1024) <= 228 * 1024, "two preparation CTAs per SM");
 
-__global__ void __launch_bounds__(kThreads, 1) gdn_prep_kernel(const PrepArgs a) {
+// swizzled index of element (i, j) of a 64 x 64 fp32 matrix: rows are 64
+// floats, columns XOR-ed with the row so that a column read hits 32 banks
+__device__ __forceinline__ int sw(int i, int j) { return i * kLd + (j ^ (i & 31)); }
+
+__global__ void __launch_bounds__(kThreads, kPrepCtasPerSm) gdn_prep_kernel(const PrepArgs a) {
   extern __shared__ __align__(1024) unsigned char sm[];
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -126,14 +122,13 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prep_kernel(const PrepArgs a)
   const int lane_base = 32 * (warp & 3);
   const int T = a.T, H = a.H;
 
-  unsigned char *sKt = sm + kPKt, *sVt = sm + kPVt;
+  unsigned char *sK = sm + kPK, *sQ = sm + kPQ, *sV = sm + kPV;
   unsigned char *sTh = sm + kPT, *sTl = sm + kPT + 8192, *sTGh = sm + kPTG, *sTGl = sm + kPTG + 8192;
-  unsigned char *sWh = sm + kPWst, *sWl = sm + kPWst + 16384;
-  float *sA = reinterpret_cast<float *>(sm + kPA);
+  float *sA = reinterpret_cast<float *>(sm + kPQ);
   float *sTf = reinterpret_cast<float *>(sm + kPTf);
-  float *sZ = reinterpret_cast<float *>(sm + kPZ);
-  float *gin = reinterpret_cast<float *>(sm + kPGate);  // [buf][alpha 64, beta 64]
-  float *lam = gin + 4 * kC, *gam = gin + 5 * kC, *tail = gin + 6 * kC;
+  float *sZ = reinterpret_cast<float *>(sm + kPT);
+  float *al = reinterpret_cast<float *>(sm + kPGate);
+  float *be = al + kC, *lam = al + 2 * kC, *gam = al + 3 * kC, *tail = al + 4 * kC;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kPBar);
   uint32_t *holder = reinterpret_cast<uint32_t *>(sm + kPBar + 32);
   const uint32_t mbGP = smem_addr(bars + 0), mbW = smem_addr(bars + 1), mbEnd = smem_addr(bars + 2);
@@ -149,41 +144,11 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prep_kernel(const PrepArgs a)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *holder;
-
-  // K and Q rows into the [K;Q] tile, V rows, alpha and beta of unit u
-  // (padding tokens: k = q = v = 0, alpha = 1, beta = 0)
-  auto load_inputs = [&](long u, int buf) {
-    const long bh = u / a.nchunks;
-    const int t0 = static_cast<int>(u - bh * a.nchunks) * kC;
-    const long tok0 = (bh / H) * T * H + bh % H;
-    unsigned char *kq = sm + kPKQ + buf * 32768, *vr = sm + kPV + buf * 16384;
-    for (int id = tid; id < 128 * 16; id += kThreads) {
-      const int r = id >> 4, k8 = id & 15;
-      const int t = t0 + (r & 63);
-      unsigned char *dst = kq + kmajor_off(r, k8 * 8, kDK);
-      if (t < T)
-        cp_async<16>(dst, (r < 64 ? a.k : a.q) + (tok0 + static_cast<long>(t) * H) * kDK + k8 * 8);
-      else
-        *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
-    }
-    for (int id = tid; id < kC * 16; id += kThreads) {
-      const int r = id >> 4, k8 = id & 15;
-      const int t = t0 + r;
-      unsigned char *dst = vr + r * (kDV * 2) + k8 * 16;
-      if (t < T)
-        cp_async<16>(dst, a.v + (tok0 + static_cast<long>(t) * H) * kDV + k8 * 8);
-      else
-        *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
-    }
-    if (tid < 2 * kC) {  // the thread that loads alpha_i / beta_i is the one that first reads it
-      const int t = t0 + (tid & 63);
-      float *dst = gin + buf * 2 * kC + tid;
-      if (t < T)
-        cp_async<4>(dst, (tid < kC ? a.alpha : a.beta) + tok0 + static_cast<long>(t) * H);
-      else
-        *dst = tid < kC ? 1.f : 0.f;
-    }
-  };
+  // descriptors at k-step 0 (MN-major A: k-step advances 4096 bytes = 256 units)
+  const uint64_t dKmn = smem_desc(smem_addr(sK), 2048, 128), dVmn = smem_desc(smem_addr(sV), 2048, 128);
+  const uint64_t dTh = smem_desc(smem_addr(sTh), 128, kC * 16), dTl = smem_desc(smem_addr(sTl), 128, kC * 16);
+  const uint64_t dTGh = smem_desc(smem_addr(sTGh), 128, kC * 16), dTGl = smem_desc(smem_addr(sTGl), 128, kC * 16);
+  const uint32_t idMN = idesc_bf16_f32(128, kC) | (1u << 15);  // A MN-major
 
   bool failed = false;
   // every thread waits, then the CTA agrees: either all continue or all stop
@@ -195,16 +160,33 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prep_kernel(const PrepArgs a)
     return all;
   };
 
-  if (static_cast<long>(blockIdx.x) < a.units) load_inputs(blockIdx.x, 0);
-  cp_async_commit();
   int it = 0;
   for (long u = blockIdx.x; u < a.units; u += gridDim.x, ++it) {
-    const int buf = it & 1;
     const uint32_t par = static_cast<uint32_t>(it & 1);
     unsigned char *ws = a.ws + u * kUnit;
-    const unsigned char *kq = sm + kPKQ + buf * 32768, *vr = sm + kPV + buf * 16384;
-    const float *al = gin + buf * 2 * kC, *be = al + kC;
+    const long bh = u / a.nchunks;
+    const int t0 = static_cast<int>(u - bh * a.nchunks) * kC;
+    const long tok0 = (bh / H) * T * H + bh % H;
 
+    // ---- inputs: K, Q, V rows (8 columns per 16-byte piece), alpha, beta
+    // (padding tokens: k = q = v = 0, alpha = 1, beta = 0)
+    for (int id = tid; id < 3 * kC * 16; id += kThreads) {
+      const int m = id >> 10, r = (id >> 4) & 63, k8 = id & 15;
+      const int t = t0 + r;
+      unsigned char *dst = sm + m * 16384 + kmajor_off(r, k8 * 8, kDK);
+      if (t < T)
+        cp_async<16>(dst, (m == 0 ? a.k : m == 1 ? a.q : a.v) + (tok0 + static_cast<long>(t) * H) * kDK + k8 * 8);
+      else
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+    }
+    if (tid < 2 * kC) {  // the thread that loads alpha_i / beta_i is the one that first reads it
+      const int t = t0 + (tid & 63);
+      if (t < T)
+        cp_async<4>(al + tid, (tid < kC ? a.alpha : a.beta) + tok0 + static_cast<long>(t) * H);
+      else
+        al[tid] = tid < kC ? 1.f : 0.f;
+    }
+    cp_async_commit();
     cp_async_wait<0>();
     // lambda = inclusive prefix sum of log alpha (two warps of 32 tokens)
     if (warp < 2) {
@@ -220,12 +202,11 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prep_kernel(const PrepArgs a)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // the next unit's inputs into the other buffer (its readers are done)
-    if (u + gridDim.x < a.units) load_inputs(u + gridDim.x, buf ^ 1);
-    cp_async_commit();
     if (tid == 0) {  // G = [K;Q] K^T: rows 0..63 K K^T, 64..127 Q K^T
-      const uint32_t kqa = smem_addr(kq);
-      mma_tile(tmem + kPColGP, kqa, kDK, kqa, kDK, kDK / 16, kC, false);
+      const uint64_t dKQ = smem_desc(smem_addr(sK), 128, kDK * 16);
+      const uint32_t idG = idesc_bf16_f32(128, kC);
+#pragma unroll
+      for (int ks = 0; ks < kDK / 16; ++ks) mma_bf16(tmem + kPColGP, dKQ + 16u * ks, dKQ + 16u * ks, idG, ks > 0);
       mma_commit(mbGP);
     }
     if (warp == 1) lam[tid] += lam[31];
@@ -235,26 +216,23 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prep_kernel(const PrepArgs a)
       tail[tid] = __expf(lam[kC - 1] - lam[tid]);
     }
     __syncthreads();
-
-    // K^T and V^T operand tiles; Khat^T hi/lo straight to the workspace
-    for (int j0 = half * 32; j0 < half * 32 + 32; j0 += 8) {
-      uint16_t kv[8], vv[8];
+    // Q tile to the workspace (read by the chain as is); Khat hi/lo: the K
+    // tile with row j scaled by e^(lambda_C - lambda_j), the MN-major B
+    // operand of the chain's state update
+    for (int o = tid; o < 1024; o += kThreads) {
+      const uint4 qv = reinterpret_cast<const uint4 *>(sQ)[o];
+      reinterpret_cast<uint4 *>(ws + kUQ)[o] = qv;
+      const uint4 kv = reinterpret_cast<const uint4 *>(sK)[o];
+      const int j = ((o >> 7) << 3) | (o & 7);  // row of the 16-byte piece o (kmajor_off with K = 128)
+      const float tj = tail[j];
+      const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w};
       float x[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        kv[e] = *reinterpret_cast<const uint16_t *>(kq + kmajor_off(j0 + e, row, kDK));
-        vv[e] = *reinterpret_cast<const uint16_t *>(vr + (j0 + e) * (kDV * 2) + row * 2);
-        x[e] = tail[j0 + e] * bf16_to_f32(kv[e]);
-      }
-      uint32_t pk[4], pv[4];
-#pragma unroll
       for (int e = 0; e < 4; ++e) {
-        pk[e] = static_cast<uint32_t>(kv[2 * e]) | (static_cast<uint32_t>(kv[2 * e + 1]) << 16);
-        pv[e] = static_cast<uint32_t>(vv[2 * e]) | (static_cast<uint32_t>(vv[2 * e + 1]) << 16);
+        x[2 * e] = tj * bf16_to_f32(static_cast<uint16_t>(kw[e] & 0xffff));
+        x[2 * e + 1] = tj * bf16_to_f32(static_cast<uint16_t>(kw[e] >> 16));
       }
-      *reinterpret_cast<uint4 *>(sKt + kmajor_off(row, j0, kC)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-      *reinterpret_cast<uint4 *>(sVt + kmajor_off(row, j0, kC)) = make_uint4(pv[0], pv[1], pv[2], pv[3]);
-      store_split8(ws + kUKh, ws + kUKh + 16384, kmajor_off(row, j0, kC), x);
+      store_split8(ws + kUKh, ws + kUKh + 16384, o * 16, x);
     }
 
     // ---- A (decayed, gated K K^T) and Mq (decayed Q K^T) from G
@@ -271,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prep_kernel(const PrepArgs a)
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int j = j0 + e;
-            sA[i * kLd + j] = j < i ? bi * __expf(li - lam[j]) * x[e] : 0.f;
+            sA[sw(i, j)] = j < i ? bi * __expf(li - lam[j]) * x[e] : 0.f;
           }
         } else {  // Mq, lower part including the diagonal, to the workspace
 #pragma unroll
@@ -294,11 +272,11 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prep_kernel(const PrepArgs a)
       for (int r = 0; r < 16; ++r) {
         float acc = (r == cc) ? 1.f : 0.f;
 #pragma unroll
-        for (int j = 0; j < r; ++j) acc -= sA[(o + r) * kLd + o + j] * xv[j];
+        for (int j = 0; j < r; ++j) acc -= sA[sw(o + r, o + j)] * xv[j];
         xv[r] = acc;
       }
 #pragma unroll
-      for (int r = 0; r < 16; ++r) sTf[(o + r) * kLd + o + cc] = xv[r];
+      for (int r = 0; r < 16; ++r) sTf[sw(o + r, o + cc)] = xv[r];
     }
     __syncthreads();
     // ... then the blocks below the diagonal, one block distance at a time:
@@ -311,8 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prep_kernel(const PrepArgs a)
         float acc = 0.f;
         for (int K = J; K < I; ++K)
 #pragma unroll
-          for (int kk = 0; kk < 16; ++kk)
-            acc += sA[(I * 16 + r) * kLd + K * 16 + kk] * sTf[(K * 16 + kk) * kLd + J * 16 + cc];
+          for (int kk = 0; kk < 16; ++kk) acc += sA[sw(I * 16 + r, K * 16 + kk)] * sTf[sw(K * 16 + kk, J * 16 + cc)];
         sZ[p * 256 + r * 16 + cc] = acc;
       }
       __syncthreads();
@@ -321,8 +298,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prep_kernel(const PrepArgs a)
         const int J = p, I = p + dist;
         float acc = 0.f;
 #pragma unroll
-        for (int kk = 0; kk < 16; ++kk) acc += sTf[(I * 16 + r) * kLd + I * 16 + kk] * sZ[p * 256 + kk * 16 + cc];
-        sTf[(I * 16 + r) * kLd + J * 16 + cc] = -acc;
+        for (int kk = 0; kk < 16; ++kk) acc += sTf[sw(I * 16 + r, I * 16 + kk)] * sZ[p * 256 + kk * 16 + cc];
+        sTf[sw(I * 16 + r, J * 16 + cc)] = -acc;
       }
       __syncthreads();
     }
@@ -333,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prep_kernel(const PrepArgs a)
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         const int j = j0 + e;
-        x[e] = j <= i ? sTf[i * kLd + j] * be[j] : 0.f;
+        x[e] = j <= i ? sTf[sw(i, j)] * be[j] : 0.f;
         xg[e] = x[e] * gam[j];
       }
       store_split8(sTh, sTl, kmajor_off(i, j0, kC), x);
@@ -345,20 +322,23 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prep_kernel(const PrepArgs a)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // ---- W^T = K^T (T diag(gamma))^T and Ut^T = V^T T^T
+    // ---- W^T = K^T (T diag(gamma))^T and Ut^T = V^T T^T (A MN-major)
     if (tid == 0) {
-      const uint32_t kt = smem_addr(sKt), vt = smem_addr(sVt);
-      mma_tile(tmem + kPColW, kt, kC, smem_addr(sTGh), kC, kC / 16, kC, false);
-      mma_tile(tmem + kPColW, kt, kC, smem_addr(sTGl), kC, kC / 16, kC, true);
-      mma_tile(tmem + kPColU, vt, kC, smem_addr(sTh), kC, kC / 16, kC, false);
-      mma_tile(tmem + kPColU, vt, kC, smem_addr(sTl), kC, kC / 16, kC, true);
+#pragma unroll
+      for (int ks = 0; ks < kC / 16; ++ks) {
+        mma_bf16(tmem + kPColW, dKmn + 256u * ks, dTGh + 16u * ks, idMN, ks > 0);
+        mma_bf16(tmem + kPColW, dKmn + 256u * ks, dTGl + 16u * ks, idMN, true);
+        mma_bf16(tmem + kPColU, dVmn + 256u * ks, dTh + 16u * ks, idMN, ks > 0);
+        mma_bf16(tmem + kPColU, dVmn + 256u * ks, dTl + 16u * ks, idMN, true);
+      }
       mma_commit(mbW);
     }
     if (tid < kC) reinterpret_cast<float *>(ws + kUG)[tid] = gam[tid];
     if (tid == 0) a.gC[u] = gam[kC - 1];
     if (!wait_ok(mbW, par)) { failed = true; break; }
-    // Ut[i][d] to the workspace (thread d: coalesced over d); W^T[c][i] split
-    // into the K-major [64 i][128 c] staging tiles
+    // Ut[i][d] to the workspace (thread d: coalesced over d); W (lane c,
+    // tokens i) as the MN-major B operand of the chain: 8 consecutive i of
+    // column c per 16 bytes, at (i/8)*2048 + (c/8)*128 + (c%8)*16
     {
       float *gU = reinterpret_cast<float *>(ws + kUU);
       for (int i0 = half * 32; i0 < half * 32 + 32; i0 += 16) {
@@ -369,26 +349,15 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prep_kernel(const PrepArgs a)
         for (int e = 0; e < 16; ++e) gU[(i0 + e) * kDV + row] = x[e];
         tmem_ld16(tmem_addr(tmem, lane_base, kPColW + i0), x);
         tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const __nv_bfloat16 hb = __float2bfloat16_rn(x[e]);
-          const __nv_bfloat16 lb = __float2bfloat16_rn(x[e] - __bfloat162float(hb));
-          const uint32_t off = kmajor_off(i0 + e, row, kDK);
-          *reinterpret_cast<__nv_bfloat16 *>(sWh + off) = hb;
-          *reinterpret_cast<__nv_bfloat16 *>(sWl + off) = lb;
-        }
+        const uint32_t off = (i0 >> 3) * 2048 + (row >> 3) * 128 + (row & 7) * 16;
+        store_split8(ws + kUW, ws + kUW + 16384, off, x);
+        store_split8(ws + kUW, ws + kUW + 16384, off + 2048, x + 8);
       }
     }
-    __syncthreads();
-    for (int o = tid * 16; o < 2 * 16384; o += kThreads * 16)
-      *reinterpret_cast<uint4 *>(ws + kUW + o) = *reinterpret_cast<const uint4 *>(sWh + o);
-    for (int o = tid * 16; o < 16384; o += kThreads * 16)  // Q rows of [K;Q] (rows 64..127: the upper 16 KB)
-      *reinterpret_cast<uint4 *>(ws + kUQ + o) = *reinterpret_cast<const uint4 *>(kq + 16384 + o);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
   }
-  cp_async_wait<0>();
   if (failed) {
     // a tensor-core wait ran out: drain this CTA's MMAs (bounded) and report;
     // the chain kernel then reads invalid tiles but ends normally
@@ -438,7 +407,7 @@ constexpr uint32_t kChainTmemCols = 512;
 constexpr uint32_t kCS = 0;               // S^T hi, lo [128 d][128 c]        2 x 32 KB
 constexpr uint32_t kCU = kCS + 65536;     // U^T hi, lo [128 d][64 j]         2 x 16 KB
 constexpr uint32_t kCW = kCU + 32768;     // W hi, lo, Q (bulk copy)          48 KB
-constexpr uint32_t kCM = kCW + kWBytes;   // Mq hi, lo, Khat^T hi, lo (bulk)  48 KB
+constexpr uint32_t kCM = kCW + kWBytes;   // Mq hi, lo, Khat hi, lo (bulk)    48 KB
 constexpr uint32_t kCG = kCM + kMBytes;   // gamma_i, two buffers             2 x 256 B
 constexpr uint32_t kCBar = kCG + 2 * kGBytes;
 constexpr int kNBar = 12;
@@ -590,13 +559,16 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
     // operand descriptors at k-step 0; k-step ks starts 256 bytes further on,
     // i.e. 16 in the descriptor's address field
     const uint64_t dSh = smem_desc(sh, 128, kDK * 16), dSl = smem_desc(sl, 128, kDK * 16);
-    const uint64_t dWh = smem_desc(wh, 128, kDK * 16), dWl = smem_desc(wl, 128, kDK * 16);
+    // W and Khat^T arrive MN-major (token-contiguous W, column-contiguous Khat)
+    const uint64_t dWh = smem_desc(wh, 128, 2048), dWl = smem_desc(wl, 128, 2048);
     const uint64_t dQ = smem_desc(qa, 128, kDK * 16);
     const uint64_t dUh = smem_desc(uh, 128, kC * 16), dUl = smem_desc(ul, 128, kC * 16);
     const uint64_t dMh = smem_desc(mh, 128, kC * 16), dMl = smem_desc(ml, 128, kC * 16);
-    const uint64_t dKh = smem_desc(kh, 128, kC * 16), dKl = smem_desc(kl, 128, kC * 16);
-    auto mma = [&](uint32_t d, uint64_t A, uint64_t Bm, int ks, uint32_t idesc, bool acc) {
-      mma_bf16(d, A + 16u * ks, Bm + 16u * ks, idesc, acc);
+    const uint64_t dKh = smem_desc(kh, 2048, 128), dKl = smem_desc(kl, 2048, 128);
+    const uint32_t id64w = id64 | (1u << 16), id128k = id128 | (1u << 16);  // B MN-major
+    // k-step ks: A advances 256 bytes (16 in the descriptor); B by bstep
+    auto mma = [&](uint32_t d, uint64_t A, uint64_t Bm, int ks, uint32_t idesc, bool acc, uint32_t bstep = 16u) {
+      mma_bf16(d, A + 16u * ks, Bm + bstep * ks, idesc, acc);
     };
     int w_issued = 0, w_done = 0, m_issued = 0, m_done = 0, g_issued = 0, g_done = 0;
     auto load = [&](int which, int c) {
@@ -638,9 +610,9 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
         if (!ok) break;
 #pragma unroll
         for (int ks = g; ks < 8; ks += 2) {
-          mma(tmem + kColX, dSh, dWh, ks, id64, ks != 0);
-          mma(tmem + kColX, dSh, dWl, ks, id64, true);
-          mma(tmem + kColX, dSl, dWh, ks, id64, true);
+          mma(tmem + kColX, dSh, dWh, ks, id64w, ks != 0);
+          mma(tmem + kColX, dSh, dWl, ks, id64w, true);
+          mma(tmem + kColX, dSl, dWh, ks, id64w, true);
         }
         if (g == 1) mma_commit(bar(4));
 #pragma unroll
@@ -665,9 +637,9 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
       mma_commit(bar(6));
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
-        mma(tmem + kColD, dUh, dKh, ks, id128, ks != 0);
-        mma(tmem + kColD, dUh, dKl, ks, id128, true);
-        mma(tmem + kColD, dUl, dKh, ks, id128, true);
+        mma(tmem + kColD, dUh, dKh, ks, id128k, ks != 0, 256u);
+        mma(tmem + kColD, dUh, dKl, ks, id128k, true, 256u);
+        mma(tmem + kColD, dUl, dKh, ks, id128k, true, 256u);
       }
       mma_commit(bar(7));
       if (c + 1 < n) {
@@ -733,7 +705,8 @@ int launch_gdn_chunk(float *state, const uint16_t *q, const uint16_t *k, const u
   if (cudaFuncSetAttribute(gdn_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kPrepSmem)) != cudaSuccess)
     return check_launch("gdn_scan: set shared memory");
-  const long pgrid = units < sms ? units : sms;
+  const long pmax = static_cast<long>(sms) * kPrepCtasPerSm;
+  const long pgrid = units < pmax ? units : pmax;
   gdn_prep_kernel<<<static_cast<unsigned>(pgrid), kThreads, kPrepSmem, st>>>(pa);
   const int rc = check_launch("gdn_scan: chunk preparation kernel");
   if (rc != SDM_OK) return rc;
