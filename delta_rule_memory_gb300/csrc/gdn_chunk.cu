@@ -95,23 +95,20 @@ struct PrepArgs {
 };
 
 constexpr int kPrepCtasPerSm = 2;
-constexpr int kLd = kC;  // fp32 row stride of the solve (columns swizzled, sw())
+constexpr int kLd = kC + 4;  // fp32 row stride of the solve (rows 16-byte aligned, 4 banks apart)
+constexpr uint32_t kSolve = kC * kLd * 4;
 // shared memory (bytes)
 constexpr uint32_t kPK = 0;                     // K rows [64 j][128 c]                    16 KB
 constexpr uint32_t kPQ = kPK + 16384;           // Q rows [64 i][128 c] (rows 64..127 of [K;Q]); then L = I + A
-constexpr uint32_t kPV = kPQ + 16384;           // V rows [64 j][128 d]                    16 KB
+constexpr uint32_t kPV = kPQ + kSolve;          // V rows [64 j][128 d]                    16 KB
 constexpr uint32_t kPT = kPV + 16384;           // T hi, lo [64 i][64 j]; block products during the solve
 constexpr uint32_t kPTG = kPT + 16384;          // T diag(gamma) hi, lo                    16 KB
-constexpr uint32_t kPTf = kPTG + 16384;         // L^-1, fp32 [64][64]                     16 KB
-constexpr uint32_t kPGate = kPTf + 16384;       // alpha, beta, lambda, gamma, tail [64] each
+constexpr uint32_t kPTf = kPTG + 16384;         // L^-1, fp32 [64][kLd]
+constexpr uint32_t kPGate = kPTf + kSolve;      // alpha, beta, lambda, gamma, tail [64] each
 constexpr uint32_t kPBar = kPGate + 5 * kC * 4;
 constexpr uint32_t kPrepSmem = kPBar + 64;
 constexpr uint32_t kPColGP = 0, kPColW = 64, kPColU = 128, kPrepTmemCols = 256;
 static_assert(2 * (kPrepSmem + 1024) <= 228 * 1024, "two preparation CTAs per SM");
-
-// swizzled index of element (i, j) of a 64 x 64 fp32 matrix: rows are 64
-// floats, columns XOR-ed with the row so that a column read hits 32 banks
-__device__ __forceinline__ int sw(int i, int j) { return i * kLd + (j ^ (i & 31)); }
 
 __global__ void __launch_bounds__(kThreads, kPrepCtasPerSm) gdn_prep_kernel(const PrepArgs a) {
   extern __shared__ __align__(1024) unsigned char sm[];
@@ -173,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, kPrepCtasPerSm) gdn_prep_kernel(cons
     for (int id = tid; id < 3 * kC * 16; id += kThreads) {
       const int m = id >> 10, r = (id >> 4) & 63, k8 = id & 15;
       const int t = t0 + r;
-      unsigned char *dst = sm + m * 16384 + kmajor_off(r, k8 * 8, kDK);
+      unsigned char *dst = sm + (m == 0 ? kPK : m == 1 ? kPQ : kPV) + kmajor_off(r, k8 * 8, kDK);
       if (t < T)
         cp_async<16>(dst, (m == 0 ? a.k : m == 1 ? a.q : a.v) + (tok0 + static_cast<long>(t) * H) * kDK + k8 * 8);
       else
@@ -249,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, kPrepCtasPerSm) gdn_prep_kernel(cons
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int j = j0 + e;
-            sA[sw(i, j)] = j < i ? bi * __expf(li - lam[j]) * x[e] : 0.f;
+            sA[i * kLd + j] = j < i ? bi * __expf(li - lam[j]) * x[e] : 0.f;
           }
         } else {  // Mq, lower part including the diagonal, to the workspace
 #pragma unroll
@@ -272,34 +269,63 @@ __global__ void __launch_bounds__(kThreads, kPrepCtasPerSm) gdn_prep_kernel(cons
       for (int r = 0; r < 16; ++r) {
         float acc = (r == cc) ? 1.f : 0.f;
 #pragma unroll
-        for (int j = 0; j < r; ++j) acc -= sA[sw(o + r, o + j)] * xv[j];
+        for (int j = 0; j < r; ++j) acc -= sA[(o + r) * kLd + o + j] * xv[j];
         xv[r] = acc;
       }
 #pragma unroll
-      for (int r = 0; r < 16; ++r) sTf[sw(o + r, o + cc)] = xv[r];
+      for (int r = 0; r < 16; ++r) sTf[(o + r) * kLd + o + cc] = xv[r];
     }
     __syncthreads();
     // ... then the blocks below the diagonal, one block distance at a time:
-    // X_IJ = -L_II^-1 sum_{K=J}^{I-1} L_IK X_KJ
-    for (int dist = 1; dist < 4; ++dist) {
-      const int npairs = 4 - dist;
-      for (int oi = tid; oi < npairs * 256; oi += kThreads) {
-        const int p = oi >> 8, r = (oi >> 4) & 15, cc = oi & 15;
-        const int J = p, I = p + dist;
-        float acc = 0.f;
-        for (int K = J; K < I; ++K)
+    // X_IJ = -L_II^-1 sum_{K=J}^{I-1} L_IK X_KJ.  A thread computes a 1 x 4
+    // strip (pair p, row r, columns c4..c4+3) with 16-byte loads.
 #pragma unroll
-          for (int kk = 0; kk < 16; ++kk) acc += sA[sw(I * 16 + r, K * 16 + kk)] * sTf[sw(K * 16 + kk, J * 16 + cc)];
-        sZ[p * 256 + r * 16 + cc] = acc;
+    for (int dist = 1; dist < 4; ++dist) {
+      const bool mine = tid < (4 - dist) * 64;
+      const int p = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
+      const int J = p, I = p + dist;
+      if (mine) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int K = 0; K < dist; ++K) {
+          const float *arow = sA + (I * 16 + r) * kLd + (J + K) * 16;
+          const float *xcol = sTf + (J + K) * 16 * kLd + J * 16 + c4;
+#pragma unroll
+          for (int k4 = 0; k4 < 16; k4 += 4) {
+            const float4 av = *reinterpret_cast<const float4 *>(arow + k4);
+            const float aa[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float4 xv = *reinterpret_cast<const float4 *>(xcol + (k4 + e) * kLd);
+              acc[0] = fmaf(aa[e], xv.x, acc[0]);
+              acc[1] = fmaf(aa[e], xv.y, acc[1]);
+              acc[2] = fmaf(aa[e], xv.z, acc[2]);
+              acc[3] = fmaf(aa[e], xv.w, acc[3]);
+            }
+          }
+        }
+        *reinterpret_cast<float4 *>(sZ + p * 256 + r * 16 + c4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
       }
       __syncthreads();
-      for (int oi = tid; oi < npairs * 256; oi += kThreads) {
-        const int p = oi >> 8, r = (oi >> 4) & 15, cc = oi & 15;
-        const int J = p, I = p + dist;
-        float acc = 0.f;
+      if (mine) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const float *xrow = sTf + (I * 16 + r) * kLd + I * 16;
+        const float *zcol = sZ + p * 256 + c4;
 #pragma unroll
-        for (int kk = 0; kk < 16; ++kk) acc += sTf[sw(I * 16 + r, I * 16 + kk)] * sZ[p * 256 + kk * 16 + cc];
-        sTf[sw(I * 16 + r, J * 16 + cc)] = -acc;
+        for (int k4 = 0; k4 < 16; k4 += 4) {
+          const float4 xv = *reinterpret_cast<const float4 *>(xrow + k4);
+          const float xx[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float4 zv = *reinterpret_cast<const float4 *>(zcol + (k4 + e) * 16);
+            acc[0] = fmaf(xx[e], zv.x, acc[0]);
+            acc[1] = fmaf(xx[e], zv.y, acc[1]);
+            acc[2] = fmaf(xx[e], zv.z, acc[2]);
+            acc[3] = fmaf(xx[e], zv.w, acc[3]);
+          }
+        }
+        *reinterpret_cast<float4 *>(sTf + (I * 16 + r) * kLd + J * 16 + c4) =
+            make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
       }
       __syncthreads();
     }
@@ -310,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, kPrepCtasPerSm) gdn_prep_kernel(cons
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         const int j = j0 + e;
-        x[e] = j <= i ? sTf[sw(i, j)] * be[j] : 0.f;
+        x[e] = j <= i ? sTf[i * kLd + j] * be[j] : 0.f;
         xg[e] = x[e] * gam[j];
       }
       store_split8(sTh, sTl, kmajor_off(i, j0, kC), x);
