@@ -54,6 +54,7 @@ def _load():
             lib.oracle_address.argtypes = [P, P, I, I, I, I, I, I, P, P]
             lib.oracle_sdm_scan.argtypes = [P, P, P, P, P, P, I, P, P, I, I, I, I, I, I, I, P]
             lib.oracle_gdn_scan.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, P]
+            lib.oracle_gdn2_scan.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, P]
             lib.oracle_sse_scan.argtypes = [P, P, I, P, P, P, P, I, I, I, I, I, I, P, P]
             lib.oracle_widen_bf16.argtypes = [P, P, ctypes.c_long]
             for f in (lib.oracle_address, lib.oracle_sdm_scan, lib.oracle_gdn_scan, lib.oracle_sse_scan):
@@ -137,6 +138,24 @@ def gdn_scan(state, q, k, v, alpha, beta, per_channel: bool):
                                  B, T, H, dk, dv, _p(y))
     if rc != 0:
         raise ValueError(f"oracle_gdn_scan failed (rc={rc})")
+    return S, y
+
+
+def gdn2_scan(state, q, k, v, alpha, b_erase, w_write):
+    """GDN2: per-key-channel decay alpha [B,T,H,dk], erase gate b_erase
+    [B,T,H,dk] and write gate w_write [B,T,H,dv].  state [B,H,dk,dv];
+    q, k [B,T,H,dk]; v [B,T,H,dv].  Returns (final state, y) in fp64."""
+    S = np.array(state, dtype=np.float64, copy=True, order="C")
+    B, H, dk, dv = S.shape
+    qq, kk, vv = (_c(widen(x), np.float64) for x in (q, k, v))
+    T = qq.shape[1]
+    a, be, wr = (_c(x, np.float64) for x in (alpha, b_erase, w_write))
+    assert qq.shape == (B, T, H, dk) and kk.shape == (B, T, H, dk) and vv.shape == (B, T, H, dv)
+    assert a.shape == (B, T, H, dk) and be.shape == (B, T, H, dk) and wr.shape == (B, T, H, dv)
+    y = np.zeros((B, T, H, dv), np.float64)
+    rc = _load().oracle_gdn2_scan(_p(S), _p(qq), _p(kk), _p(vv), _p(a), _p(be), _p(wr), B, T, H, dk, dv, _p(y))
+    if rc != 0:
+        raise ValueError(f"oracle_gdn2_scan failed (rc={rc})")
     return S, y
 
 

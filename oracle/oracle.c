@@ -18,6 +18,8 @@
  *   oracle_gdn_scan  - dense Gated DeltaNet / KDA (Linear Attention
  *                      Architectures deck, "GDN and KDA change the granularity
  *                      of forgetting", Eqs. 15-20).
+ *   oracle_gdn2_scan - GDN2 (same deck, "GDN2 separates key-side erase and
+ *                      value-side write", Eqs. 21-24).
  *   oracle_sse_scan  - Sparse State Expansion (SSE deck, "One gate controls
  *                      both writes and reads", Eqs. 9-14, with the always-active
  *                      shared partition of "SSE routes tokens into
@@ -277,6 +279,61 @@ int oracle_gdn_scan(double *state, const double *q, const double *k, const doubl
         }
     }
     free(pred);
+    return 0;
+}
+
+/*
+ * GDN2 (Linear Attention Architectures deck, "GDN2 separates key-side erase
+ * and value-side write", Eqs. 21-24), with the state stored key-major
+ * (S = W^T, so W D_alpha is D_alpha S):
+ *
+ * state  : fp64 [B,H,dk,dv] in place.   q, k : fp64 [B,T,H,dk].  v : [B,T,H,dv].
+ * alpha  : fp64 [B,T,H,dk] per-key-channel decay.
+ * berase : fp64 [B,T,H,dk] erase gate b.   wwrite : fp64 [B,T,H,dv] write gate w.
+ * y      : fp64 [B,T,H,dv].
+ *
+ * Per token:  S~ = D_alpha S
+ *             e = b (.) k,   z = w (.) v
+ *             r = z - S~^T e             (the residual at the erase key)
+ *             S = S~ + k r^T             (the outer product takes k, not e)
+ *             y = S^T q
+ */
+int oracle_gdn2_scan(double *state, const double *q, const double *k, const double *v, const double *alpha,
+                     const double *berase, const double *wwrite, int B, int T, int H, int dk, int dv, double *y)
+{
+    if (B < 0 || T < 0 || H < 0 || dk < 1 || dv < 1) return -1;
+    double *r = (double *)malloc(sizeof(double) * (size_t)dv);
+    double *e = (double *)malloc(sizeof(double) * (size_t)dk);
+    if (!r || !e) { free(r); free(e); return -1; }
+    for (int b = 0; b < B; ++b) {
+        for (int h = 0; h < H; ++h) {
+            double *S = state + ((size_t)b * H + h) * (size_t)dk * dv;
+            for (int t = 0; t < T; ++t) {
+                size_t tok = ((size_t)b * T + t) * H + h;
+                const double *qt = q + tok * dk, *kt = k + tok * dk, *vt = v + tok * dv;
+                for (int i = 0; i < dk; ++i) {
+                    double a = alpha[tok * dk + i];
+                    for (int c = 0; c < dv; ++c) S[(size_t)i * dv + c] *= a;
+                    e[i] = berase[tok * dk + i] * kt[i];
+                }
+                for (int c = 0; c < dv; ++c) {
+                    double s = 0.0;
+                    for (int i = 0; i < dk; ++i) s += S[(size_t)i * dv + c] * e[i];
+                    r[c] = wwrite[tok * dv + c] * vt[c] - s;
+                }
+                for (int i = 0; i < dk; ++i)
+                    for (int c = 0; c < dv; ++c) S[(size_t)i * dv + c] += kt[i] * r[c];
+                double *yt = y + tok * dv;
+                for (int c = 0; c < dv; ++c) {
+                    double s = 0.0;
+                    for (int i = 0; i < dk; ++i) s += S[(size_t)i * dv + c] * qt[i];
+                    yt[c] = s;
+                }
+            }
+        }
+    }
+    free(r);
+    free(e);
     return 0;
 }
 

@@ -146,7 +146,10 @@ def gdn_inputs(shape: GdnShape, seed: int = 0) -> dict:
     """Draw q, k, v (N(0,1), [B,T,H,d]); q and k L2-normalised per head in
     fp32, then all three cast to bf16 bits.  alpha_gdn = exp(-softplus(N(0,1)))
     [B,T,H]; alpha_kda the same recipe per key channel [B,T,H,dk];
-    beta = sigmoid(N(0,1)) [B,T,H]."""
+    beta = sigmoid(N(0,1)) [B,T,H]; then the GDN2 gates b_erase =
+    sigmoid(N(0,1)) [B,T,H,dk] and w_write = sigmoid(N(0,1)) [B,T,H,dv] (both
+    in (0,1), drawn after everything else so the earlier tensors keep their
+    values)."""
     g = _gen(seed)
     B, T, H, dk, dv = shape.B, shape.T, shape.H, shape.dk, shape.dv
     q = torch.randn((B, T, H, dk), generator=g)
@@ -157,8 +160,11 @@ def gdn_inputs(shape: GdnShape, seed: int = 0) -> dict:
     a_gdn = torch.exp(-torch.nn.functional.softplus(torch.randn((B, T, H), generator=g)))
     a_kda = torch.exp(-torch.nn.functional.softplus(torch.randn((B, T, H, dk), generator=g)))
     beta = torch.sigmoid(torch.randn((B, T, H), generator=g))
+    b_erase = torch.sigmoid(torch.randn((B, T, H, dk), generator=g))
+    w_write = torch.sigmoid(torch.randn((B, T, H, dv), generator=g))
     return {"q": to_bf16_bits(q), "k": to_bf16_bits(k), "v": to_bf16_bits(v),
-            "alpha_gdn": a_gdn.numpy(), "alpha_kda": a_kda.numpy(), "beta": beta.numpy()}
+            "alpha_gdn": a_gdn.numpy(), "alpha_kda": a_kda.numpy(), "beta": beta.numpy(),
+            "b_erase": b_erase.numpy(), "w_write": w_write.numpy()}
 
 
 def sse_inputs(shape: SseShape, seed: int = 0) -> dict:

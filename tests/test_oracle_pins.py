@@ -179,6 +179,87 @@ def test_kda_constant_vector_is_gdn():
 
 
 # ---------------------------------------------------------------------------
+# GDN2 (Linear Attention Architectures deck, "GDN2 separates key-side erase and
+# value-side write", Eqs. 21-24): erase gate b on the key side, write gate w on
+# the value side, outer product with the key itself.
+# ---------------------------------------------------------------------------
+def _gdn2_one(S0, k, q, v, alpha, b, w):
+    return oracle.gdn2_scan(S0, _one_token(q), _one_token(k), _one_token(v), _one_token(alpha), _one_token(b),
+                            _one_token(w))
+
+
+def test_gdn2_gates_equal_to_beta_are_kda():
+    """b = w = beta 1 recovers KDA (the deck's stated special case)."""
+    shape = synth.GDN_DENSE.with_(B=2, T=30, H=2, dk=16, dv=8)
+    inp = synth.gdn_inputs(shape, seed=21)
+    S0 = synth.random_state((2, 2, 16, 8), seed=22)
+    bb = np.repeat(inp["beta"][..., None], 16, axis=-1)
+    ww = np.repeat(inp["beta"][..., None], 8, axis=-1)
+    S2, y2 = oracle.gdn2_scan(S0, inp["q"], inp["k"], inp["v"], inp["alpha_kda"], bb, ww)
+    Sk, yk = oracle.gdn_scan(S0, inp["q"], inp["k"], inp["v"], inp["alpha_kda"], inp["beta"], per_channel=True)
+    np.testing.assert_allclose(S2, Sk, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(y2, yk, rtol=1e-12, atol=1e-13)
+
+
+def test_gdn2_teaching_example(golden):
+    """Prediction 2 at a unit key, target 5, b = w = 0.5: the DeltaNet teaching
+    value 3.5; with the write gate opened to w = 1 (erase still 0.5) the
+    prediction becomes 2 + (5 - 0.5 * 2) = 6: erase and write act separately."""
+    g = golden("deltanet_teaching.txt")
+    dk, dv = 5, 3
+    S0 = synth.random_state((1, 1, dk, dv), seed=23).astype(np.float64)
+    S0[0, 0, 1, :] = g["prediction"][0]
+    k = np.zeros(dk); k[1] = 1.0
+    v = np.full(dv, g["target"][0])
+    half = g["beta"][0]
+    S, y = _gdn2_one(S0, k, k, v, np.ones(dk), np.full(dk, half), np.full(dv, half))
+    np.testing.assert_allclose(y.ravel(), g["new_prediction"][0], atol=1e-12)
+    S, y = _gdn2_one(S0, k, k, v, np.ones(dk), np.full(dk, half), np.ones(dv))
+    np.testing.assert_allclose(y.ravel(), 6.0, atol=1e-12)
+    keep = [r for r in range(dk) if r != 1]
+    np.testing.assert_array_equal(S[0, 0, keep], S0[0, 0, keep])
+
+
+def test_gdn2_update_is_along_the_key_not_the_erase_vector():
+    """W_new - W~ = r k^T: directions orthogonal to k see no change even when
+    they are not orthogonal to e = b (.) k."""
+    dk, dv = 12, 6
+    S0 = RNG.standard_normal((1, 1, dk, dv))
+    k = RNG.standard_normal(dk)
+    b = RNG.uniform(0.05, 0.95, dk)
+    S, _ = _gdn2_one(S0, k, RNG.standard_normal(dk), RNG.standard_normal(dv), np.ones(dk), b,
+                     RNG.uniform(0.05, 0.95, dv))
+    dS = S[0, 0] - S0[0, 0]                     # alpha = 1: S~ = S0
+    u = RNG.standard_normal(dk); u -= (u @ k) / (k @ k) * k          # u orthogonal to k
+    np.testing.assert_allclose(u @ dS, 0.0, atol=1e-12)
+    e = b * k
+    assert abs(u @ e) > 1e-3                    # ... yet not orthogonal to e
+    assert np.linalg.norm(dS) > 1e-3
+
+
+def test_gdn2_zero_erase_is_an_additive_write():
+    """b = 0 and alpha = 1: S_T = S_0 + sum_t k_t (w_t (.) v_t)^T = S_0 + K^T (W (.) V)."""
+    T, dk, dv = 7, 9, 4
+    S0 = RNG.standard_normal((1, 1, dk, dv))
+    k = RNG.standard_normal((1, T, 1, dk))
+    v = RNG.standard_normal((1, T, 1, dv))
+    w = RNG.uniform(0.1, 0.9, (1, T, 1, dv))
+    S, _ = oracle.gdn2_scan(S0, RNG.standard_normal((1, T, 1, dk)), k, v, np.ones((1, T, 1, dk)),
+                            np.zeros((1, T, 1, dk)), w)
+    np.testing.assert_allclose(S[0, 0], S0[0, 0] + k[0, :, 0].T @ (w * v)[0, :, 0], rtol=1e-12, atol=1e-12)
+
+
+def test_gdn2_full_gates_at_a_unit_key_reach_the_target():
+    """b = w = 1, alpha = 1, unit-norm key: the new prediction at k is v."""
+    dk, dv = 10, 5
+    S0 = RNG.standard_normal((1, 1, dk, dv))
+    k = RNG.standard_normal(dk); k /= np.linalg.norm(k)
+    v = RNG.standard_normal(dv)
+    S, y = _gdn2_one(S0, k, k, v, np.ones(dk), np.ones(dk), np.ones(dv))
+    np.testing.assert_allclose(y.ravel(), v, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
 # Sparse <-> dense: with every row selected, weights k_t (write) and q_t (read)
 # and the shared residual, the sparse table update is Gated DeltaNet (SDM deck,
 # "A v1 inconsistency ...": only the shared residual gives the GDN limit).
