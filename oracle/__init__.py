@@ -30,6 +30,7 @@ _lock = threading.Lock()
 _lib = None
 
 RESID_SHARED, RESID_PERSLOT, RESID_ADDITIVE = 0, 1, 2
+SSE_WRITE_ADDITIVE, SSE_WRITE_DELTA = 0, 1
 
 
 def build(force: bool = False) -> str:
@@ -55,7 +56,7 @@ def _load():
             lib.oracle_sdm_scan.argtypes = [P, P, P, P, P, P, I, P, P, I, I, I, I, I, I, I, P]
             lib.oracle_gdn_scan.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, P]
             lib.oracle_gdn2_scan.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, P]
-            lib.oracle_sse_scan.argtypes = [P, P, I, P, P, P, P, I, I, I, I, I, I, P, P]
+            lib.oracle_sse_scan.argtypes = [P, P, I, P, P, P, P, I, I, I, I, I, I, P, P, I]
             lib.oracle_widen_bf16.argtypes = [P, P, ctypes.c_long]
             for f in (lib.oracle_address, lib.oracle_sdm_scan, lib.oracle_gdn_scan, lib.oracle_sse_scan):
                 f.restype = I
@@ -159,9 +160,10 @@ def gdn2_scan(state, q, k, v, alpha, b_erase, w_write):
     return S, y
 
 
-def sse_scan(state, route, topk, klog, q, v, alpha):
+def sse_scan(state, route, topk, klog, q, v, alpha, mode=0):
     """SSE scan.  state [B,H,N+1,c,d]; route fp32 [B,T,H,N]; klog fp32
-    [B,T,H,c]; q [B,T,H,c]; v [B,T,H,d]; alpha [B,T,H,c].
+    [B,T,H,c]; q [B,T,H,c]; v [B,T,H,d]; alpha [B,T,H,c]; mode
+    SSE_WRITE_ADDITIVE (0) or SSE_WRITE_DELTA (1).
     Returns (final state, y [B,T,H,d], sel int32 [B,T,H,topk])."""
     S = np.array(state, dtype=np.float64, copy=True, order="C")
     B, H, Np1, c, d = S.shape
@@ -176,7 +178,7 @@ def sse_scan(state, route, topk, klog, q, v, alpha):
     y = np.zeros((B, T, H, d), np.float64)
     sel = np.zeros((B, T, H, topk), np.int32)
     rc = _load().oracle_sse_scan(_p(S), _p(rt), int(topk), _p(kl), _p(qq), _p(vv), _p(a), B, T, H, N, c, d,
-                                 _p(y), _p(sel))
+                                 _p(y), _p(sel), int(mode))
     if rc != 0:
         raise ValueError(f"oracle_sse_scan failed (rc={rc})")
     return S, y, sel

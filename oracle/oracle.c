@@ -347,6 +347,11 @@ int oracle_gdn2_scan(double *state, const double *q, const double *k, const doub
  * q      : fp64 [B,T,H,c].  v : fp64 [B,T,H,d].
  * alpha  : fp64 [B,T,H,c]  per-row (GLA-style) decay Lambda_t = diag(alpha_t).
  * y      : fp64 [B,T,H,d].  sel : int32 [B,T,H,topk] selected partitions (rank order).
+ * mode   : 0 additive write (the deck's SSE), 1 delta write: the write
+ *          residual of every visited partition is shared by its rows,
+ *          v - vhat_p with vhat_p = sum_j kk_j alpha_j S^p[j,:] (the decayed
+ *          prediction of the partition, as the Sparse Delta Memory deck's
+ *          shared residual of Fig. 2 with weights kk and strength g).
  *
  * Per token:  e = softmax(route) over all N (not renormalised after top-k);
  *             T_t = top-k of the fp32 logits (ties to the lower index);
@@ -358,16 +363,18 @@ int oracle_gdn2_scan(double *state, const double *q, const double *k, const doub
  */
 int oracle_sse_scan(double *state, const float *route, int topk, const float *klog, const double *q,
                     const double *v, const double *alpha, int B, int T, int H, int N, int c, int d, double *y,
-                    int32_t *sel)
+                    int32_t *sel, int mode)
 {
     if (B < 0 || T < 0 || H < 0 || N < 1 || topk < 1 || topk > N || c < 1 || d < 1) return -1;
+    if (mode != 0 && mode != 1) return -1;
     cand_t *work = (cand_t *)malloc(sizeof(cand_t) * (size_t)N);
     int *tsel = (int *)malloc(sizeof(int) * (size_t)(topk + 1));
     double *e = (double *)malloc(sizeof(double) * (size_t)N);
     double *kk = (double *)malloc(sizeof(double) * (size_t)c);
     double *g = (double *)malloc(sizeof(double) * (size_t)(topk + 1));
-    if (!work || !tsel || !e || !kk || !g) {
-        free(work); free(tsel); free(e); free(kk); free(g);
+    double *res = (double *)malloc(sizeof(double) * (size_t)d);
+    if (!work || !tsel || !e || !kk || !g || !res) {
+        free(work); free(tsel); free(e); free(kk); free(g); free(res);
         return -1;
     }
     size_t part = (size_t)c * d;
@@ -402,9 +409,15 @@ int oracle_sse_scan(double *state, const float *route, int topk, const float *kl
                 /* update the visited partitions */
                 for (int s = 0; s <= topk; ++s) {
                     double *Sp = S + (size_t)tsel[s] * part;
+                    for (int col = 0; col < d; ++col) {
+                        double vhat = 0.0;
+                        if (mode == 1)
+                            for (int j = 0; j < c; ++j) vhat += kk[j] * at[j] * Sp[(size_t)j * d + col];
+                        res[col] = vt[col] - vhat;
+                    }
                     for (int j = 0; j < c; ++j)
                         for (int col = 0; col < d; ++col)
-                            Sp[(size_t)j * d + col] = at[j] * Sp[(size_t)j * d + col] + g[s] * kk[j] * vt[col];
+                            Sp[(size_t)j * d + col] = at[j] * Sp[(size_t)j * d + col] + g[s] * kk[j] * res[col];
                 }
                 /* read the updated visited partitions */
                 double *yt = y + tok * d;
@@ -421,7 +434,7 @@ int oracle_sse_scan(double *state, const float *route, int topk, const float *kl
             }
         }
     }
-    free(work); free(tsel); free(e); free(kk); free(g);
+    free(work); free(tsel); free(e); free(kk); free(g); free(res);
     return 0;
 }
 

@@ -473,6 +473,83 @@ def test_sse_unvisited_partitions_bit_unchanged():
 # ---------------------------------------------------------------------------
 # Table sizes (SDM deck, Eq. 6 and the learned-state column of its table).
 # ---------------------------------------------------------------------------
+# ---------------------------------------------------------------------------
+# SSE with a delta write: the partition's rows share one residual, the
+# Sparse Delta Memory deck's shared residual (Fig. 2) with row weights kk and
+# strength g.
+# ---------------------------------------------------------------------------
+def _one_hot_logits(c, row):
+    kl = np.full(c, -1e30, np.float32)
+    kl[row] = 0.0
+    return kl
+
+
+def test_sse_delta_teaching_example(golden):
+    """Two routed partitions with equal logits (gates 1/2), top-1 picks the
+    lower one; a one-hot key on row 0 holding prediction 2, target 5: the
+    routed row becomes 2 + 0.5 (5 - 2) = 3.5 (the DeltaNet teaching value)
+    and the shared partition (gate 1) reaches the target 5."""
+    g = golden("deltanet_teaching.txt")
+    N, c, d = 2, 4, 3
+    S0 = synth.random_state((1, 1, N + 1, c, d), seed=41).astype(np.float64)
+    S0[0, 0, 0, 0] = g["prediction"][0]
+    S0[0, 0, N, 0] = g["prediction"][0]
+    route = np.zeros((1, 1, 1, N), np.float32)
+    klog = _one_hot_logits(c, 0).reshape(1, 1, 1, c)
+    v = np.full((1, 1, 1, d), g["target"][0])
+    S, _, sel = oracle.sse_scan(S0, route, 1, klog, np.zeros((1, 1, 1, c)), v, np.ones((1, 1, 1, c)),
+                                oracle.SSE_WRITE_DELTA)
+    assert sel.ravel().tolist() == [0]
+    np.testing.assert_allclose(S[0, 0, 0, 0], g["new_prediction"][0], atol=1e-12)
+    np.testing.assert_allclose(S[0, 0, N, 0], g["target"][0], atol=1e-12)
+    np.testing.assert_array_equal(S[0, 0, 0, 1:], S0[0, 0, 0, 1:])     # rows with weight 0 keep their bits
+    np.testing.assert_array_equal(S[0, 0, 1], S0[0, 0, 1])             # unvisited partition untouched
+
+
+def test_sse_delta_is_the_sdm_shared_residual():
+    """One routed partition (gate 1) and the shared one, decay equal across
+    rows: each partition evolves exactly as the sparse scan with every row
+    written (weights kk, beta = 1, shared residual) and read with weights q, so
+    y is twice the sparse scan's read."""
+    T, N, c, d = 12, 1, 6, 5
+    rng = np.random.default_rng(42)
+    S0p = rng.standard_normal((c, d))
+    S0 = np.broadcast_to(S0p, (1, 1, N + 1, c, d)).copy()
+    klog = rng.standard_normal((1, T, 1, c)).astype(np.float32)
+    q = rng.standard_normal((1, T, 1, c))
+    v = rng.standard_normal((1, T, 1, d))
+    a_tok = rng.uniform(0.6, 1.0, (1, T, 1))
+    alpha = np.repeat(a_tok[..., None], c, axis=-1)
+    S, y, _ = oracle.sse_scan(S0, np.zeros((1, T, 1, N), np.float32), 1, klog, q, v, alpha, oracle.SSE_WRITE_DELTA)
+    kl64 = klog.astype(np.float64)
+    kk = np.exp(kl64 - kl64.max(axis=-1, keepdims=True))
+    kk /= kk.sum(axis=-1, keepdims=True)
+    idx = np.broadcast_to(np.arange(c, dtype=np.int32), (1, T, 1, c)).copy()
+    M, ys = oracle.sdm_scan(S0p.reshape(1, 1, c, d), v, a_tok, np.ones((1, T, 1)), idx, kk, idx, q,
+                            oracle.RESID_SHARED)
+    np.testing.assert_allclose(S[0, 0, 0], M[0, 0], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(S[0, 0, N], M[0, 0], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(y, 2 * ys, rtol=1e-12, atol=1e-12)
+
+
+def test_sse_delta_from_zero_state_first_token_is_additive():
+    shape = synth.SSE_PART.with_(B=1, T=3, H=2, N=4, topk=2, c=16, d=8)
+    inp = synth.sse_inputs(shape, seed=43)
+    S0 = np.zeros((1, 2, 5, 16, 8))
+    first = {k: v[:, :1] for k, v in inp.items()}
+    Sa, ya, _ = oracle.sse_scan(S0, first["route"], 2, first["klog"], first["q"], first["v"], first["alpha"],
+                                oracle.SSE_WRITE_ADDITIVE)
+    Sd, yd, _ = oracle.sse_scan(S0, first["route"], 2, first["klog"], first["q"], first["v"], first["alpha"],
+                                oracle.SSE_WRITE_DELTA)
+    np.testing.assert_array_equal(Sa, Sd)
+    np.testing.assert_array_equal(ya, yd)
+    Sa, _, _ = oracle.sse_scan(S0, inp["route"], 2, inp["klog"], inp["q"], inp["v"], inp["alpha"],
+                               oracle.SSE_WRITE_ADDITIVE)
+    Sd, _, _ = oracle.sse_scan(S0, inp["route"], 2, inp["klog"], inp["q"], inp["v"], inp["alpha"],
+                               oracle.SSE_WRITE_DELTA)
+    assert np.max(np.abs(Sa - Sd)) > 1e-6           # later tokens see a nonzero prediction
+
+
 def test_state_sizes(golden):
     g = golden("sdm_state_sizes.txt")
     for d, H, n_slots, layers, total, unit in g["rows"]:
