@@ -9,7 +9,7 @@ recurrence; a step is the next B*T tokens of the same sequences, so every
 step does identical work).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload sdm_14b_layer|sdm_sweep_H2|H4|H8|gdn|kda|sse|sdm_tiny]
+                    [--workload sdm_14b_layer|sdm_sweep_H2|H4|H8|gdn|kda|gdn2|sse|sse_delta|sdm_tiny|sdm_decode|sse_decode]
 
 Prints one JSON line (rank 0).  Under torchrun each rank runs its own batch
 (independent sequences, no collective in the data path) and the time is the
@@ -155,13 +155,22 @@ def _oracle_gdn_seq(args):
     return time.perf_counter() - t0
 
 
+def _oracle_gdn2_seq(args):
+    import numpy as np
+    import oracle
+    q, k, v, a, b_erase, w_write = args
+    t0 = time.perf_counter()
+    oracle.gdn2_scan(np.zeros((1, 1, q.shape[-1], v.shape[-1])), q, k, v, a, b_erase, w_write)
+    return time.perf_counter() - t0
+
+
 def _oracle_sse_seq(args):
     import numpy as np
     import oracle
-    route, topk, klog, q, v, alpha = args
+    route, topk, klog, q, v, alpha, mode = args
     t0 = time.perf_counter()
     N, c, d = route.shape[-1], klog.shape[-1], v.shape[-1]
-    oracle.sse_scan(np.zeros((1, 1, N + 1, c, d)), route, topk, klog, q, v, alpha)
+    oracle.sse_scan(np.zeros((1, 1, N + 1, c, d)), route, topk, klog, q, v, alpha, mode)
     return time.perf_counter() - t0
 
 
@@ -179,11 +188,18 @@ class OracleSampler:
 
     def run(self, wl: "Workload", inp: dict, t_sample: int, nseq: int):
         jobs = wl.oracle_jobs(inp, t_sample, nseq)
-        fn = {"sdm": _oracle_sdm_seq, "gdn": _oracle_gdn_seq, "kda": _oracle_gdn_seq, "sse": _oracle_sse_seq}[wl.kind]
+        fn = {"sdm": _oracle_sdm_seq, "gdn": _oracle_gdn_seq, "kda": _oracle_gdn_seq, "gdn2": _oracle_gdn2_seq,
+              "sse": _oracle_sse_seq}[wl.kind]
         t0 = time.perf_counter()
         self.pool.map(fn, jobs, chunksize=1)
         wall = time.perf_counter() - t0
         return len(jobs) * t_sample, wall
+
+
+def metric_name(wl) -> str:
+    if wl.decode:
+        return f"{wl.kind} decode tokens/s (one token per sequence per step; ms_per_step is the step latency)"
+    return METRIC if wl.kind == "sdm" else f"{wl.kind} scan tokens/s"
 
 
 # ---------------------------------------------------------------- workloads
@@ -192,20 +208,27 @@ class Workload:
         import synth
         self.name = name
         self.mode = {"shared": 0, "perslot": 1}[mode]
+        # decode: one token per sequence per step (T = 1), the state carried across steps
+        self.decode = name.endswith("_decode")
+        if self.decode:
+            name = {"sdm_decode": "sdm_14b_layer", "sse_decode": "sse"}[name]
         if name == "sdm_14b_layer":
             self.kind, self.shape = "sdm", synth.SDM_14B_LAYER
         elif name.startswith("sdm_sweep_H"):
             self.kind, self.shape = "sdm", synth.sdm_sweep_shape(int(name[len("sdm_sweep_H"):]))
         elif name == "sdm_tiny":
             self.kind, self.shape = "sdm", synth.SDM_TINY
-        elif name in ("gdn", "kda"):
+        elif name in ("gdn", "kda", "gdn2"):
             self.kind, self.shape = name, synth.GDN_DENSE
-        elif name == "sse":
+        elif name in ("sse", "sse_delta"):
             self.kind, self.shape = "sse", synth.SSE_PART
         else:
             raise SystemExit(f"unknown workload {name}")
+        self.sse_mode = 1 if name == "sse_delta" else 0  # sse_scan write mode: additive / delta
         if batch:
             self.shape = self.shape.with_(B=batch)
+        if self.decode:
+            self.shape = self.shape.with_(T=1, name=self.shape.name + "_decode")
         sh = self.shape
         self.tokens = sh.B * sh.T
 
@@ -213,7 +236,7 @@ class Workload:
         import synth
         if self.kind == "sdm":
             return synth.sdm_inputs(self.shape, seed)
-        if self.kind in ("gdn", "kda"):
+        if self.kind in ("gdn", "kda", "gdn2"):
             return synth.gdn_inputs(self.shape, seed)
         return synth.sse_inputs(self.shape, seed)
 
@@ -225,12 +248,12 @@ class Workload:
                     "k": sh.k, "W": sh.W, "R": sh.R, "v_dtype": "bf16" if sh.v_bf16 else "fp32",
                     "resid": ["shared", "per_slot"][self.mode], "state": f"fp32 {state_gb:.2f} GB, continued across steps",
                     "l2": f"inputs larger than L2 (table {state_gb:.2f} GB); no flush"}
-        if self.kind in ("gdn", "kda"):
-            return {"workload": "kda_dense" if self.kind == "kda" else "gdn_dense", "B": sh.B, "T": sh.T, "H": sh.H,
+        if self.kind in ("gdn", "kda", "gdn2"):
+            return {"workload": f"{self.kind}_dense", "B": sh.B, "T": sh.T, "H": sh.H,
                     "dk": sh.dk, "dv": sh.dv, "qkv_dtype": "bf16", "state": "fp32, continued across steps",
                     "l2": "inputs (q,k,v,alpha,y ~340-470 MB) larger than L2; no flush"}
         return {"workload": sh.name, "B": sh.B, "T": sh.T, "H": sh.H, "N": sh.N, "topk": sh.topk, "c": sh.c, "d": sh.d,
-                "qv_dtype": "bf16", "state": "fp32 shared-memory resident per CTA, continued across steps",
+                "write": ["additive", "delta"][self.sse_mode], "qv_dtype": "bf16", "state": "fp32 shared-memory resident per CTA, continued across steps",
                 "l2": "inputs (~1.1 GB) larger than L2; no flush"}
 
     def oracle_jobs(self, inp: dict, t_sample: int, nseq: int):
@@ -243,13 +266,16 @@ class Workload:
                 jobs.append((inp["s1w"][sl].copy(), inp["s2w"][sl].copy(), inp["s1r"][sl].copy(),
                              inp["s2r"][sl].copy(), inp["v"][sl].copy(), inp["alpha"][sl].copy(),
                              inp["beta"][sl].copy(), sh.k, sh.W, sh.R, self.mode))
+            elif self.kind == "gdn2":
+                jobs.append((inp["q"][sl].copy(), inp["k"][sl].copy(), inp["v"][sl].copy(), inp["alpha_kda"][sl].copy(),
+                             inp["b_erase"][sl].copy(), inp["w_write"][sl].copy()))
             elif self.kind in ("gdn", "kda"):
                 a = inp["alpha_kda" if self.kind == "kda" else "alpha_gdn"]
                 jobs.append((inp["q"][sl].copy(), inp["k"][sl].copy(), inp["v"][sl].copy(), a[sl].copy(),
                              inp["beta"][sl].copy(), self.kind == "kda"))
             else:
                 jobs.append((inp["route"][sl].copy(), sh.topk, inp["klog"][sl].copy(), inp["q"][sl].copy(),
-                             inp["v"][sl].copy(), inp["alpha"][sl].copy()))
+                             inp["v"][sl].copy(), inp["alpha"][sl].copy(), self.sse_mode))
         return jobs
 
 
@@ -275,6 +301,8 @@ class GpuRun:
         self.d = {}
         if wl.kind == "sdm":
             names = ("s1w", "s2w", "s1r", "s2r", "v", "alpha", "beta")
+        elif wl.kind == "gdn2":
+            names = ("q", "k", "v", "alpha_kda", "b_erase", "w_write")
         elif wl.kind in ("gdn", "kda"):
             names = ("q", "k", "v", "alpha_kda" if wl.kind == "kda" else "alpha_gdn", "beta")
         else:
@@ -293,6 +321,10 @@ class GpuRun:
             self.y = torch.empty((B, T, H, sh.d_v), dtype=torch.float32, device=device)
             self.ws = torch.empty(sdm.sdm_scan_workspace_size(B, T, H, sh.W, sh.R), dtype=torch.uint8, device=device)
             self.launches_per_step = 4
+        elif wl.kind == "gdn2":
+            self.state = torch.zeros((sh.B, sh.H, sh.dk, sh.dv), dtype=torch.float32, device=device)
+            self.y = torch.empty((sh.B, sh.T, sh.H, sh.dv), dtype=torch.float32, device=device)
+            self.launches_per_step = 1
         elif wl.kind in ("gdn", "kda"):
             self.state = torch.zeros((sh.B, sh.H, sh.dk, sh.dv), dtype=torch.float32, device=device)
             self.y = torch.empty((sh.B, sh.T, sh.H, sh.dv), dtype=torch.float32, device=device)
@@ -322,13 +354,15 @@ class GpuRun:
         if self.wl.kind == "sdm":
             self.sdm.sdm_scan(self.state, d["v"], d["alpha"], d["beta"], self.iw, self.ww, self.ir, self.wr,
                               self.wl.mode, self.y, self.ws, self.err)
+        elif self.wl.kind == "gdn2":
+            self.sdm.gdn2_scan(self.state, d["q"], d["k"], d["v"], d["alpha_kda"], d["b_erase"], d["w_write"], self.y)
         elif self.wl.kind in ("gdn", "kda"):
             a = d["alpha_kda" if self.wl.kind == "kda" else "alpha_gdn"]
             self.sdm.gdn_scan(self.state, d["q"], d["k"], d["v"], a, d["beta"], self.wl.kind == "kda", self.y,
                               workspace=self.ws, dev_err=self.err)
         else:
             self.sdm.sse_scan(self.state, d["route"], sh.topk, d["klog"], d["q"], d["v"], d["alpha"], self.y,
-                              None, self.ws, self.err)
+                              None, self.ws, self.err, write_mode=self.wl.sse_mode)
 
     def step(self):
         self.pre()
@@ -380,13 +414,19 @@ class GpuRun:
             return rows * sh.d_v * 4 + tokh * per_tok, "GB/s", "hbm", {
                 "mean_union_rows": float(union.float().mean().item()),
                 "bytes_per_token_head": (rows * sh.d_v * 4 + tokh * per_tok) / tokh}
+        if self.wl.kind == "gdn2":
+            tokh = sh.B * sh.T * sh.H
+            per = 2 * (sh.dk + sh.dk + sh.dv) + 4 * sh.dk * 2 + 4 * sh.dv + 4 * sh.dv  # q k v, alpha b, w, y
+            state = 2 * sh.B * sh.H * sh.dk * sh.dv * 4
+            return tokh * per + state, "GB/s", "hbm", {"bytes_per_token_head": per}
         if self.wl.kind in ("gdn", "kda"):
             tokh = sh.B * sh.T * sh.H
             per = 2 * (sh.dk + sh.dk + sh.dv) + 4 * (sh.dk if self.wl.kind == "kda" else 1) + 4 + 4 * sh.dv
             state = 2 * sh.B * sh.H * sh.dk * sh.dv * 4
             return tokh * per + state, "GB/s", "hbm", {"bytes_per_token_head": per}
         tokh = sh.B * sh.T * sh.H
-        flops = tokh * (sh.topk + 1) * sh.c * sh.d * 5.0     # decay mul, write fma, read fma (2+2+1)
+        # decay mul, write fma, read fma (1 + 2 + 2); the delta write adds the prediction fma (2)
+        flops = tokh * (sh.topk + 1) * sh.c * sh.d * (7.0 if self.wl.sse_mode else 5.0)
         return flops, "TFLOP/s", "alu", {"flops_per_token_head": flops / tokh}
 
 
@@ -469,12 +509,13 @@ def run_ours(args, rank, world, local_rank, sampler):
         # FP32 FMA pipe: 152 SMs x 128 lanes x 2 flop x max SM clock
         peak = 152 * 128 * 2 * float(pk.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
         achieved = algo / (main_ms * 1e-3) / 1e12
-    kernel_file = {"sdm": "sparse_scan.cu", "gdn": "gdn_chunk.cu", "kda": "gdn_scan.cu", "sse": "sse_scan.cu"}[wl.kind]
+    kernel_file = {"sdm": "sparse_scan.cu", "gdn": "gdn_chunk.cu", "kda": "gdn_scan.cu", "gdn2": "gdn_scan.cu",
+                   "sse": "sse_scan.cu"}[wl.kind]
     tr = NCU_TRAFFIC.get((wl.name, wl.kind))
     traffic = tr["bytes"] if tr and tr["digest"] == _src_digest(kernel_file) else None
     tokens = wl.tokens * world
     out = {
-        "metric": METRIC if wl.kind == "sdm" else f"{wl.kind} scan tokens/s",
+        "metric": metric_name(wl),
         "value": tokens / (ms_per_step * 1e-3),
         "unit": "tokens/s",
         "n_gpus": world,
@@ -490,7 +531,8 @@ def run_ours(args, rank, world, local_rank, sampler):
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": algo_unit,
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": {"sdm": "sdm_scan (hazard prepass + sparse_scan_kernel)", "gdn": "gdn_scan (chunk preparation + chain kernels)",
-                                "kda": "gdn_scan", "sse": "sse_scan (route prepass + sse_scan_kernel)"}[wl.kind],
+                                "kda": "gdn_scan", "gdn2": "gdn2_scan",
+                                "sse": "sse_scan (route prepass + sse_scan_kernel)"}[wl.kind],
                      "launch_ms": main_ms, "peak_source": f"{src} ({'hbm_gbs' if bound == 'hbm' else 'FP32 lanes x clock'})",
                      **algo_info},
         "cpu_baseline": cpu,
@@ -526,7 +568,7 @@ def run_reference(args, rank, world):
     value = tok / (ms * 1e-3)
     sample = (f"{nseq} whole (b,h) sequences x first {t_sample} tokens per step, fp64 oracle, one process per "
               f"sequence")
-    return {"impl": "reference", "metric": METRIC if wl.kind == "sdm" else f"{wl.kind} scan tokens/s",
+    return {"impl": "reference", "metric": metric_name(wl),
             "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded generators; no dataset or weights)", "config": wl.config(),

@@ -21,7 +21,7 @@ import torch
 __all__ = [
     "SdmError", "lib", "library_path", "sdm_version", "sdm_address", "sdm_scan", "sdm_scan_workspace_size",
     "sdm_scan_noalloc", "sdm_forward_host", "sdm_forward_host_workspace_size",
-    "gdn_scan", "gdn_scan_workspace_size", "sse_scan", "sse_scan_workspace_size", "SDM_RESID_SHARED", "SDM_RESID_PERSLOT",
+    "gdn_scan", "gdn_scan_workspace_size", "gdn2_scan", "sse_scan", "sse_scan_workspace_size", "SDM_RESID_SHARED", "SDM_RESID_PERSLOT", "SSE_WRITE_ADDITIVE", "SSE_WRITE_DELTA",
     "SDM_RESID_ADDITIVE", "SDM_DEVERR_INDEX_RANGE", "SDM_DEVERR_INDEX_REPEAT", "SDM_DEVERR_NONFINITE",
 ]
 
@@ -29,6 +29,7 @@ SDM_OK, SDM_ERR_INVALID_ARG, SDM_ERR_SHAPE, SDM_ERR_ALIGN, SDM_ERR_UNSUPPORTED, 
 SDM_DEVERR_INDEX_RANGE, SDM_DEVERR_INDEX_REPEAT, SDM_DEVERR_NONFINITE, SDM_DEVERR_TIMEOUT = 1, 2, 4, 8
 SDM_DTYPE_F32, SDM_DTYPE_BF16 = 0, 1
 SDM_RESID_SHARED, SDM_RESID_PERSLOT, SDM_RESID_ADDITIVE = 0, 1, 2
+SSE_WRITE_ADDITIVE, SSE_WRITE_DELTA = 0, 1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_HERE, "libsdm.so")
@@ -48,8 +49,9 @@ _SIGNATURES = {
                               _SZ, _P, _P]),
     "gdn_scan_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "gdn_scan": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _SZ, _P, _P]),
+    "gdn2_scan": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "sse_scan_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
-    "sse_scan": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _SZ, _P, _P]),
+    "sse_scan": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _SZ, _P, _P]),
 }
 
 
@@ -301,14 +303,43 @@ def gdn_scan(state, q, k, v, alpha, beta, per_channel: bool, y=None, workspace=N
     return y
 
 
+def gdn2_scan(state, q, k, v, alpha, b_erase, w_write, y=None, dev_err=None, stream=None):
+    """GDN2 scan; updates `state` [B,H,dk,dv] in place and returns y fp32
+    [B,T,H,dv].  q, k bf16 [B,T,H,dk]; v bf16 [B,T,H,dv]; alpha and b_erase
+    fp32 [B,T,H,dk]; w_write fp32 [B,T,H,dv]."""
+    _req(state, "state", torch.float32)
+    if state.dim() != 4:
+        raise ValueError("state must be [B,H,dk,dv]")
+    B, H, dk, dv = state.shape
+    _req(q, "q", torch.bfloat16)
+    T = q.shape[1]
+    _req(q, "q", torch.bfloat16, (B, T, H, dk))
+    _req(k, "k", torch.bfloat16, (B, T, H, dk))
+    _req(v, "v", torch.bfloat16, (B, T, H, dv))
+    _req(alpha, "alpha", torch.float32, (B, T, H, dk))
+    _req(b_erase, "b_erase", torch.float32, (B, T, H, dk))
+    _req(w_write, "w_write", torch.float32, (B, T, H, dv))
+    if y is None:
+        y = torch.empty((B, T, H, dv), dtype=torch.float32, device=state.device)
+    _req(y, "y", torch.float32, (B, T, H, dv))
+    if dev_err is not None:
+        _req(dev_err, "dev_err", torch.int32)
+    rc = lib().gdn2_scan(state.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), alpha.data_ptr(),
+                         b_erase.data_ptr(), w_write.data_ptr(), B, T, H, dk, dv, y.data_ptr(), _ptr(dev_err),
+                         _stream(stream))
+    _check("gdn2_scan", rc)
+    return y
+
+
 def sse_scan_workspace_size(B: int, T: int, H: int, N: int, topk: int) -> int:
     return int(lib().sse_scan_workspace_size(B, T, H, N, topk))
 
 
 def sse_scan(state, route_logits, topk: int, k_logits, q, v, alpha, y=None, sel_out=None, workspace=None,
-             dev_err=None, stream=None):
+             dev_err=None, stream=None, write_mode: int = 0):
     """Sparse State Expansion scan; updates `state` [B,H,N+1,c,d] in place and
-    returns y fp32 [B,T,H,d] (and fills sel_out int32 [B,T,H,topk] if given)."""
+    returns y fp32 [B,T,H,d] (and fills sel_out int32 [B,T,H,topk] if given).
+    write_mode: SSE_WRITE_ADDITIVE (0) or SSE_WRITE_DELTA (1)."""
     _req(state, "state", torch.float32)
     if state.dim() != 5:
         raise ValueError("state must be [B,H,N+1,c,d]")
@@ -333,7 +364,7 @@ def sse_scan(state, route_logits, topk: int, k_logits, q, v, alpha, y=None, sel_
                                 device=state.device)
     _req(workspace, "workspace", torch.uint8)
     rc = lib().sse_scan(state.data_ptr(), route_logits.data_ptr(), int(topk), k_logits.data_ptr(), q.data_ptr(),
-                        v.data_ptr(), alpha.data_ptr(), B, T, H, N, c, d, y.data_ptr(), _ptr(sel_out),
+                        v.data_ptr(), alpha.data_ptr(), int(write_mode), B, T, H, N, c, d, y.data_ptr(), _ptr(sel_out),
                         workspace.data_ptr(), workspace.numel(), _ptr(dev_err), _stream(stream))
     _check("sse_scan", rc)
     return y

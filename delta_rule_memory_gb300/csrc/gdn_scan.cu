@@ -1,8 +1,9 @@
 // gdn_scan.cu - dense Gated DeltaNet / KDA scan (Linear Attention Architectures
-// deck, "GDN and KDA change the granularity of forgetting", Eqs. 15-20): the
-// C ABI entry point, and the token-by-token fp32 kernel used for KDA and for
-// widths other than d_k = d_v = 128 (dense GDN at 128 x 128 runs chunkwise on
-// the tensor cores, gdn_chunk.cu).
+// deck, "GDN and KDA change the granularity of forgetting", Eqs. 15-20) and
+// GDN2 (same deck, "GDN2 separates key-side erase and value-side write",
+// Eqs. 21-24): the C ABI entry points, and the token-by-token fp32 kernel used
+// for KDA, GDN2 and widths other than d_k = d_v = 128 (dense GDN at 128 x 128
+// runs chunkwise on the tensor cores, gdn_chunk.cu).
 //
 // One CTA per (batch, head, 32-column tile of the value dimension); the
 // dk x 32 state tile stays in registers for the whole sequence (thread
@@ -25,13 +26,17 @@ struct GdnArgs {
   float *state;
   const uint16_t *q, *k, *v;
   const float *alpha, *beta;
+  const float *berase, *wwrite;  // GDN2 gates (gdn2 = 1), else unused
   float *y;
-  int T, H, dk, dv, per_channel, tiles;
+  int T, H, dk, dv, per_channel, gdn2, tiles;
 };
 
 // per-token slot (32-bit words): k[dk] bf16, q[dk] bf16, v[32] bf16,
-// alpha[dk or 1], beta, padded to a multiple of 4 words
-__host__ __device__ inline int gdn_slot_words(int dk) { return ((dk / 2) * 2 + 16 + dk + 1 + 3) & ~3; }
+// alpha[dk or 1], then beta (GDN, KDA) or b_erase[dk], w_write[32] (GDN2),
+// padded to a multiple of 4 words
+__host__ __device__ inline int gdn_slot_words(int dk, int gdn2) {
+  return (dk + 16 + dk + (gdn2 ? dk + 32 : 1) + 3) & ~3;
+}
 
 template <int RPT>  // rows per thread = dk / 8
 __global__ void __launch_bounds__(kGdnWarps * 32) gdn_recurrent_kernel(const GdnArgs a) {
@@ -48,8 +53,9 @@ __global__ void __launch_bounds__(kGdnWarps * 32) gdn_recurrent_kernel(const Gdn
   float *redP = reinterpret_cast<float *>(smem_raw);          // [8][32]
   float *redY = redP + kGdnWarps * kGdnCols;                  // [2][8][32]
   uint32_t *ring = reinterpret_cast<uint32_t *>(redY + 2 * kGdnWarps * kGdnCols);
-  const int sw = gdn_slot_words(dk);
+  const int sw = gdn_slot_words(dk, a.gdn2);
   const int k_off = 0, q_off = dk / 2, v_off = dk, a_off = dk + 16, b_off = dk + 16 + dk;
+  const int e_off = b_off, w_off = b_off + dk;  // GDN2: erase gate b[dk], write gate w[32 columns]
 
   float *gS = a.state + bh * static_cast<long>(dk) * dv;
   float s[RPT];
@@ -58,6 +64,7 @@ __global__ void __launch_bounds__(kGdnWarps * 32) gdn_recurrent_kernel(const Gdn
 
   const long tok0 = b * T * H + h;
   const int n_k = dk / 8, n_q = dk / 8, n_v = kGdnCols / 8, n_a = a.per_channel ? dk / 4 : 0;
+  const int n_e = a.gdn2 ? dk / 4 : 0, n_w = a.gdn2 ? kGdnCols / 4 : 0;
   auto issue = [&](int t) {
     const long tok = tok0 + static_cast<long>(t) * H;
     uint32_t *sl = ring + (t % (kGdnP + 1)) * sw;
@@ -71,6 +78,11 @@ __global__ void __launch_bounds__(kGdnWarps * 32) gdn_recurrent_kernel(const Gdn
     q -= n_v;
     if (q < n_a) { cp_async<16>(sl + a_off + 4 * q, a.alpha + tok * dk + 4 * q); return; }
     q -= n_a;
+    if (q < n_e) { cp_async<16>(sl + e_off + 4 * q, a.berase + tok * dk + 4 * q); return; }
+    q -= n_e;
+    if (q < n_w) { cp_async<16>(sl + w_off + 4 * q, a.wwrite + tok * dv + tile * kGdnCols + 4 * q); return; }
+    q -= n_w;
+    if (a.gdn2) return;
     if (!a.per_channel) {
       if (q == 0) cp_async<4>(sl + a_off, a.alpha + tok);
       else if (q == 1) cp_async<4>(sl + b_off, a.beta + tok);
@@ -100,22 +112,27 @@ __global__ void __launch_bounds__(kGdnWarps * 32) gdn_recurrent_kernel(const Gdn
     const uint16_t *qq = reinterpret_cast<const uint16_t *>(sl + q_off);
     const uint16_t *vv = reinterpret_cast<const uint16_t *>(sl + v_off);
     const float *al = reinterpret_cast<const float *>(sl + a_off);
-    const float be = __uint_as_float(sl[b_off]);
+    const float *eb = reinterpret_cast<const float *>(sl + e_off);  // GDN2 erase gate b
+    const float *wg = reinterpret_cast<const float *>(sl + w_off);  // GDN2 write gate w
+    const float be = a.gdn2 ? 0.f : __uint_as_float(sl[b_off]);
     // decay every row (D_alpha S), then the decayed prediction S~^T k
+    // (GDN2: at the erase key e = b (.) k)
     float pp = 0.f;
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
       const int j = warp + kGdnWarps * i;
       const float aj = a.per_channel ? al[j] : al[0];
+      const float kj = bf16_to_f32(kk[j]);
       s[i] *= aj;
-      pp = fmaf(s[i], bf16_to_f32(kk[j]), pp);
+      pp = fmaf(s[i], a.gdn2 ? eb[j] * kj : kj, pp);
     }
     redP[warp * kGdnCols + lane] = pp;
     __syncthreads();
     float pred = 0.f;
 #pragma unroll
     for (int w = 0; w < kGdnWarps; ++w) pred += redP[w * kGdnCols + lane];
-    const float r = be * (bf16_to_f32(vv[lane]) - pred);
+    const float vl = bf16_to_f32(vv[lane]);
+    const float r = a.gdn2 ? fmaf(wg[lane], vl, -pred) : be * (vl - pred);  // GDN2: w (.) v - pred
     float yp = 0.f;
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
@@ -136,6 +153,21 @@ __global__ void __launch_bounds__(kGdnWarps * 32) gdn_recurrent_kernel(const Gdn
   }
 #pragma unroll
   for (int i = 0; i < RPT; ++i) gS[static_cast<long>(warp + kGdnWarps * i) * dv + col] = s[i];
+}
+
+// one CTA per (batch, head, 32-column tile)
+int launch_recurrent(GdnArgs &args, int B, cudaStream_t st, const char *what) {
+  args.tiles = args.dv / kGdnCols;
+  const size_t smem = sizeof(float) * 3 * kGdnWarps * kGdnCols +
+                      sizeof(uint32_t) * (kGdnP + 1) * gdn_slot_words(args.dk, args.gdn2);
+  const long blocks = static_cast<long>(B) * args.H * args.tiles;
+  switch (args.dk) {
+    case 16: gdn_recurrent_kernel<2><<<static_cast<unsigned>(blocks), kGdnWarps * 32, smem, st>>>(args); break;
+    case 32: gdn_recurrent_kernel<4><<<static_cast<unsigned>(blocks), kGdnWarps * 32, smem, st>>>(args); break;
+    case 64: gdn_recurrent_kernel<8><<<static_cast<unsigned>(blocks), kGdnWarps * 32, smem, st>>>(args); break;
+    default: gdn_recurrent_kernel<16><<<static_cast<unsigned>(blocks), kGdnWarps * 32, smem, st>>>(args); break;
+  }
+  return check_launch(what);
 }
 
 }  // namespace
@@ -184,7 +216,7 @@ extern "C" int gdn_scan(float *state, const uint16_t *q, const uint16_t *k, cons
     if (!aligned(workspace, 16)) return set_error(SDM_ERR_ALIGN, "gdn_scan: workspace must be 16-byte aligned");
     return launch_gdn_chunk(state, q, k, v, alpha, beta, B, T, H, y, workspace, dev_err, st);
   }
-  GdnArgs args;
+  GdnArgs args{};
   args.state = state;
   args.q = q;
   args.k = k;
@@ -197,14 +229,36 @@ extern "C" int gdn_scan(float *state, const uint16_t *q, const uint16_t *k, cons
   args.dk = dk;
   args.dv = dv;
   args.per_channel = per_channel;
-  args.tiles = dv / kGdnCols;
-  const size_t smem = sizeof(float) * 3 * kGdnWarps * kGdnCols + sizeof(uint32_t) * (kGdnP + 1) * gdn_slot_words(dk);
-  const long blocks = static_cast<long>(B) * H * args.tiles;
-  switch (dk) {
-    case 16: gdn_recurrent_kernel<2><<<static_cast<unsigned>(blocks), kGdnWarps * 32, smem, st>>>(args); break;
-    case 32: gdn_recurrent_kernel<4><<<static_cast<unsigned>(blocks), kGdnWarps * 32, smem, st>>>(args); break;
-    case 64: gdn_recurrent_kernel<8><<<static_cast<unsigned>(blocks), kGdnWarps * 32, smem, st>>>(args); break;
-    default: gdn_recurrent_kernel<16><<<static_cast<unsigned>(blocks), kGdnWarps * 32, smem, st>>>(args); break;
-  }
-  return check_launch("gdn_scan");
+  return launch_recurrent(args, B, st, "gdn_scan");
+}
+
+extern "C" int gdn2_scan(float *state, const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
+                         const float *b_erase, const float *w_write, int B, int T, int H, int dk, int dv, float *y,
+                         int32_t *dev_err, void *stream) {
+  (void)dev_err;
+  if (!state || !q || !k || !v || !alpha || !b_erase || !w_write || !y)
+    return set_error(SDM_ERR_INVALID_ARG, "gdn2_scan: null pointer");
+  if (B < 0 || T < 0 || H < 0) return set_error(SDM_ERR_INVALID_ARG, "gdn2_scan: negative size");
+  if ((dk != 16 && dk != 32 && dk != 64 && dk != 128) || dv < 32 || dv % 32 != 0 || dv > 256)
+    return set_error(SDM_ERR_SHAPE, "gdn2_scan: need dk in {16,32,64,128}, dv %% 32 == 0, dv <= 256");
+  if (!aligned(state, 16) || !aligned(y, 16) || !aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) ||
+      !aligned(alpha, 16) || !aligned(b_erase, 16) || !aligned(w_write, 16))
+    return set_error(SDM_ERR_ALIGN, "gdn2_scan: every tensor needs 16-byte alignment");
+  if (B == 0 || T == 0 || H == 0) return SDM_OK;
+  GdnArgs args{};
+  args.state = state;
+  args.q = q;
+  args.k = k;
+  args.v = v;
+  args.alpha = alpha;
+  args.berase = b_erase;
+  args.wwrite = w_write;
+  args.y = y;
+  args.T = T;
+  args.H = H;
+  args.dk = dk;
+  args.dv = dv;
+  args.per_channel = 1;
+  args.gdn2 = 1;
+  return launch_recurrent(args, B, static_cast<cudaStream_t>(stream), "gdn2_scan");
 }

@@ -10,9 +10,14 @@
 //   scan   - one CTA per (batch, head, 16-column tile).  All N+1 partitions of
 //            that column tile live in shared memory for the whole sequence; per
 //            token only the k routed partitions and the shared one are touched
-//            (decay, additive write, read), two columns per thread with packed
-//            fp32x2 arithmetic.  Per-token inputs are prefetched P tokens ahead
-//            with cp.async; one CTA barrier per token.
+//            (decay, write, read), two columns per thread with packed fp32x2
+//            arithmetic.  Per-token inputs are prefetched P tokens ahead with
+//            cp.async; one CTA barrier per token (two with the delta write).
+//
+// Write modes: additive (the deck's SSE: S^p[j,:] += g kk_j v after the
+// decay) and delta, where the rows of a visited partition share one residual
+// v - vhat_p, vhat_p = sum_j kk_j alpha_j S^p[j,:] (the Sparse Delta Memory
+// deck's shared residual, Fig. 2, with row weights kk and strength g).
 #include <climits>
 
 #include "common.cuh"
@@ -110,7 +115,7 @@ struct SseArgs {
   const uint16_t *q, *v;
   const uint32_t *rec;
   float *y;
-  int T, H, N, c, d, topk, tiles, rw;
+  int T, H, N, c, d, topk, tiles, rw, mode;
 };
 
 // per-token input slot, in 16-byte chunks: klog[c], alpha[c], q[c] bf16,
@@ -149,6 +154,7 @@ __device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigne
 constexpr int kSseRows = 32;  // row groups
 constexpr int kSseRPT = 4;    // rows per thread (c <= 128)
 
+template <int MODE>  // SSE_WRITE_ADDITIVE or SSE_WRITE_DELTA
 __global__ void __launch_bounds__(kSseThreads) sse_scan_kernel(const SseArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int tid = threadIdx.x;
@@ -164,7 +170,8 @@ __global__ void __launch_bounds__(kSseThreads) sse_scan_kernel(const SseArgs a) 
 
   float *S = reinterpret_cast<float *>(smem_raw);            // [parts][c][16]
   float *red = S + static_cast<size_t>(parts) * c * kSseDT;   // [2][8 warps][16]
-  uint32_t *ring = reinterpret_cast<uint32_t *>(red + 2 * 8 * kSseDT);
+  float *redv = red + 2 * 8 * kSseDT;  // delta write: [topk+1][8 warps][16] predictions
+  uint32_t *ring = reinterpret_cast<uint32_t *>(redv + (MODE == SSE_WRITE_DELTA ? (kSseMaxTopk + 1) * 8 * kSseDT : 0));
   const int slot_words = SseSlot::words(c, a.rw);
   const int col0 = tile * kSseDT;
 
@@ -235,11 +242,47 @@ __global__ void __launch_bounds__(kSseThreads) sse_scan_kernel(const SseArgs a) 
       const float qv = bf16_to_f32(qq[jj]);
       q2[i] = pk(qv, qv);
     }
+    if (MODE == SSE_WRITE_DELTA) {
+      // the decayed prediction of every visited partition, summed over rows
+      for (int s = 0; s <= topk; ++s) {
+        const int p = s < topk ? static_cast<int>(rc[s]) : N;
+        const float *Sp = S + static_cast<size_t>(p) * c * kSseDT + 2 * cp;
+        unsigned long long acc = 0ull;
+#pragma unroll
+        for (int i = 0; i < kSseRPT; ++i) {
+          if (in[i]) {
+            const int j = rg + kSseRows * i;
+            const float ka = kk[i] * al[j];
+            acc = fma2(pk(ka, ka), *reinterpret_cast<const unsigned long long *>(Sp + j * kSseDT), acc);
+          }
+        }
+        float2 pv = upk(acc);
+#pragma unroll
+        for (int m = 8; m <= 16; m <<= 1) {
+          pv.x += __shfl_xor_sync(kFull, pv.x, m);
+          pv.y += __shfl_xor_sync(kFull, pv.y, m);
+        }
+        if (lane < 8) *reinterpret_cast<float2 *>(redv + (s * 8 + warp) * kSseDT + 2 * cp) = pv;
+      }
+      __syncthreads();
+    }
     unsigned long long part = 0ull;
     for (int s = 0; s <= topk; ++s) {
       const int p = s < topk ? static_cast<int>(rc[s]) : N;
       const float g = s < topk ? __uint_as_float(rc[topk + s]) : 1.0f;
       float *Sp = S + static_cast<size_t>(p) * c * kSseDT + 2 * cp;
+      unsigned long long src = v2;  // what is written: v (additive) or v - vhat_p (delta)
+      if (MODE == SSE_WRITE_DELTA) {
+        float2 vh = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+          const float2 t2 = *reinterpret_cast<const float2 *>(redv + (s * 8 + w) * kSseDT + 2 * cp);
+          vh.x += t2.x;
+          vh.y += t2.y;
+        }
+        const float2 vf = upk(v2);
+        src = pk(vf.x - vh.x, vf.y - vh.y);
+      }
       unsigned long long inner = 0ull;
 #pragma unroll
       for (int i = 0; i < kSseRPT; ++i) {
@@ -247,7 +290,7 @@ __global__ void __launch_bounds__(kSseThreads) sse_scan_kernel(const SseArgs a) 
           const int j = rg + kSseRows * i;
           unsigned long long *cell = reinterpret_cast<unsigned long long *>(Sp + j * kSseDT);
           const float gk = g * kk[i];
-          const unsigned long long x = fma2(a2[i], *cell, mul2(pk(gk, gk), v2));  // alpha_j S + g kk_j v
+          const unsigned long long x = fma2(a2[i], *cell, mul2(pk(gk, gk), src));  // alpha_j S + g kk_j src
           *cell = x;
           inner = fma2(q2[i], x, inner);
         }
@@ -272,8 +315,9 @@ __global__ void __launch_bounds__(kSseThreads) sse_scan_kernel(const SseArgs a) 
   }
 }
 
-size_t sse_smem_bytes(int N, int c, int topk) {
-  return sizeof(float) * (static_cast<size_t>(N + 1) * c * kSseDT + 2 * 8 * kSseDT) +
+size_t sse_smem_bytes(int N, int c, int topk, int mode) {
+  const size_t pred = mode == SSE_WRITE_DELTA ? (kSseMaxTopk + 1) * 8 * kSseDT : 0;
+  return sizeof(float) * (static_cast<size_t>(N + 1) * c * kSseDT + 2 * 8 * kSseDT + pred) +
          sizeof(uint32_t) * (kSseP + 1) * SseSlot::words(c, rec_words(topk));
 }
 
@@ -289,11 +333,14 @@ extern "C" size_t sse_scan_workspace_size(int B, int T, int H, int N, int topk) 
 }
 
 extern "C" int sse_scan(float *state, const float *route_logits, int topk, const float *k_logits, const uint16_t *q,
-                        const uint16_t *v, const float *alpha, int B, int T, int H, int N, int c, int d, float *y,
+                        const uint16_t *v, const float *alpha, int write_mode, int B, int T, int H, int N, int c, int d,
+                        float *y,
                         int32_t *sel_out, void *workspace, size_t workspace_bytes, int32_t *dev_err, void *stream) {
   if (!state || !route_logits || !k_logits || !q || !v || !alpha || !y)
     return set_error(SDM_ERR_INVALID_ARG, "sse_scan: null pointer");
   if (B < 0 || T < 0 || H < 0) return set_error(SDM_ERR_INVALID_ARG, "sse_scan: negative size");
+  if (write_mode != SSE_WRITE_ADDITIVE && write_mode != SSE_WRITE_DELTA)
+    return set_error(SDM_ERR_UNSUPPORTED, "sse_scan: write_mode must be SSE_WRITE_ADDITIVE or SSE_WRITE_DELTA");
   if (N < 1 || N > 64 || topk < 1 || topk > N || topk > kSseMaxTopk)
     return set_error(SDM_ERR_SHAPE, "sse_scan: need 1 <= topk <= min(N, 8), N <= 64");
   if (c < 16 || c > 128 || c % 16 != 0 || d < kSseDT || d % kSseDT != 0)
@@ -308,7 +355,7 @@ extern "C" int sse_scan(float *state, const float *route_logits, int topk, const
   if (!workspace || workspace_bytes < need)
     return set_error(SDM_ERR_INVALID_ARG, "sse_scan: workspace of %zu bytes needed", need);
   if (!aligned(workspace, 16)) return set_error(SDM_ERR_ALIGN, "sse_scan: workspace must be 16-byte aligned");
-  const size_t smem = sse_smem_bytes(N, c, topk);
+  const size_t smem = sse_smem_bytes(N, c, topk, write_mode);
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&smem_blk, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (smem > static_cast<size_t>(smem_blk))
@@ -338,10 +385,11 @@ extern "C" int sse_scan(float *state, const float *route_logits, int topk, const
   args.topk = topk;
   args.tiles = d / kSseDT;
   args.rw = rec_words(topk);
-  if (cudaFuncSetAttribute(sse_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-      cudaSuccess)
+  args.mode = write_mode;
+  auto kern = write_mode == SSE_WRITE_DELTA ? sse_scan_kernel<SSE_WRITE_DELTA> : sse_scan_kernel<SSE_WRITE_ADDITIVE>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
     return check_launch("sse_scan: set shared memory");
   const long blocks = static_cast<long>(B) * H * args.tiles;
-  sse_scan_kernel<<<static_cast<unsigned>(blocks), kSseThreads, smem, st>>>(args);
+  kern<<<static_cast<unsigned>(blocks), kSseThreads, smem, st>>>(args);
   return check_launch("sse_scan: scan kernel");
 }

@@ -73,6 +73,10 @@ extern "C" {
 #define SDM_RESID_PERSLOT 1  /* [SDM] printed Eq. 4: M[i] = M~[i] + beta w_i (v - M~[i]) */
 #define SDM_RESID_ADDITIVE 2 /* additive write, no residual: M[i] = M~[i] + beta w_i v */
 
+/* sse_scan write modes */
+#define SSE_WRITE_ADDITIVE 0 /* [SSE] Eqs. 9-14: S^p[j,:] = alpha_j S^p[j,:] + g kk_j v */
+#define SSE_WRITE_DELTA 1    /* shared residual per partition: v replaced by v - sum_j kk_j alpha_j S^p[j,:] */
+
 /* Library version (major*10000 + minor*100 + patch). */
 SDM_API int sdm_version(void);
 
@@ -250,6 +254,28 @@ SDM_API int gdn_scan(float *state, const uint16_t *q, const uint16_t *k, const u
                      void *workspace, size_t workspace_bytes, int32_t *dev_err, void *stream);
 
 /*
+ * gdn2_scan - GDN2, [LAA] "GDN2 separates key-side erase and value-side
+ * write", Eqs. 21-24, state stored key-major (S = W^T):
+ *   S~   = D_alpha S                  (per-key-channel decay, as KDA)
+ *   e    = b (.) k,   z = w (.) v     (erase gate on keys, write gate on values)
+ *   S    = S~ + k (z - S~^T e)^T      (the outer product takes k, not e)
+ *   y_t  = S^T q_t
+ * b = w = beta 1 is KDA.
+ *
+ * state   : fp32 [B,H,dk,dv] in place.
+ * q, k    : bf16 [B,T,H,dk];  v : bf16 [B,T,H,dv].
+ * alpha   : fp32 [B,T,H,dk].  b_erase : fp32 [B,T,H,dk].  w_write : fp32 [B,T,H,dv].
+ * y       : fp32 [B,T,H,dv].
+ * dev_err : unused (kept for a uniform call shape); may be NULL.
+ * Kernel: token by token in fp32, one CTA per (batch, head, 32 value columns).
+ * Limits: dk in {16, 32, 64, 128}; dv % 32 == 0, dv <= 256; every tensor
+ *         16-byte aligned.  No workspace.
+ */
+SDM_API int gdn2_scan(float *state, const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
+                      const float *b_erase, const float *w_write, int B, int T, int H, int dk, int dv, float *y,
+                      int32_t *dev_err, void *stream);
+
+/*
  * Scratch bytes sse_scan needs: one routing record per token (selected
  * partitions, their gates, and the max and inverse normaliser of the row
  * softmax), rounded up to 256 bytes.
@@ -263,13 +289,19 @@ SDM_API size_t sse_scan_workspace_size(int B, int T, int H, int N, int topk);
  *   T_t  = top-k of route_t (value descending, ties to the lower index)
  *   kk_t = softmax(k_logits_t) over the c rows of a partition
  *   for p in T_t (gate g = e_t[p]) and p = N (g = 1):
- *       S^p[j,:] = alpha_t[j] S^p[j,:] + g kk_t[j] v_t     (j < c)
+ *       S^p[j,:] = alpha_t[j] S^p[j,:] + g kk_t[j] r_p      (j < c)
+ *       r_p = v_t                                  (write_mode SSE_WRITE_ADDITIVE)
+ *       r_p = v_t - sum_j kk_t[j] alpha_t[j] S^p[j,:]   (SSE_WRITE_DELTA: the
+ *             partition's rows share one residual, the [SDM] Fig. 2 shared
+ *             residual with row weights kk and strength g; the SSE deck names
+ *             delta-rule transitions as follow-up work without a formula)
  *   unvisited partitions keep their bits (their decay clock stops)
  *   y_t  = sum_p g_p sum_j q_t[j] S^p[j,:]                 (after the write)
  *
  * state       : fp32 [B,H,N+1,c,d] in place.
  * route_logits: fp32 [B,T,H,N].  k_logits : fp32 [B,T,H,c].
  * q           : bf16 [B,T,H,c].  v : bf16 [B,T,H,d].  alpha : fp32 [B,T,H,c].
+ * write_mode  : SSE_WRITE_ADDITIVE or SSE_WRITE_DELTA (else SDM_ERR_UNSUPPORTED).
  * y           : fp32 [B,T,H,d].
  * sel_out     : optional int32 [B,T,H,topk], the selected partitions in rank order.
  * workspace   : device scratch of at least sse_scan_workspace_size() bytes,
@@ -280,8 +312,8 @@ SDM_API size_t sse_scan_workspace_size(int B, int T, int H, int N, int topk);
  *         16-byte aligned.
  */
 SDM_API int sse_scan(float *state, const float *route_logits, int topk, const float *k_logits, const uint16_t *q,
-             const uint16_t *v, const float *alpha, int B, int T, int H, int N, int c, int d, float *y,
-             int32_t *sel_out, void *workspace, size_t workspace_bytes, int32_t *dev_err, void *stream);
+             const uint16_t *v, const float *alpha, int write_mode, int B, int T, int H, int N, int c, int d,
+             float *y, int32_t *sel_out, void *workspace, size_t workspace_bytes, int32_t *dev_err, void *stream);
 
 #ifdef __cplusplus
 }

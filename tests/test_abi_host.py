@@ -29,7 +29,7 @@ def sdm():
 
 def test_header_declares_the_boundary():
     names = _declared_functions()
-    for fn in ("sdm_address", "sdm_scan", "gdn_scan", "sse_scan", "sdm_version", "sdm_last_error",
+    for fn in ("sdm_address", "sdm_scan", "gdn_scan", "gdn2_scan", "sse_scan", "sdm_version", "sdm_last_error",
                "sdm_scan_workspace_size", "gdn_scan_workspace_size", "sse_scan_workspace_size"):
         assert fn in names
 

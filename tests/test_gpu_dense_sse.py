@@ -140,15 +140,67 @@ def test_gdn_teaching_example_on_gpu(golden):
     np.testing.assert_allclose(y.ravel(), g["new_prediction"][0], atol=1e-6)
 
 
+# ------------------------------------------------------------------------ GDN2
+def _gdn2_gpu(sdm, S0, inp):
+    state = dev(S0)
+    y = sdm.gdn2_scan(state, dev(inp["q"]), dev(inp["k"]), dev(inp["v"]), dev(inp["alpha_kda"]),
+                      dev(inp["b_erase"]), dev(inp["w_write"]))
+    return host(state), host(y)
+
+
+@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 96), (16, 32)])
+def test_gdn2_reduced_parity(dk, dv):
+    sdm = need_gpu()
+    sh = synth.GDN_DENSE.with_(B=2, T=200, H=3, dk=dk, dv=dv)
+    inp = synth.gdn_inputs(sh, seed=3 * dk + dv)
+    S0 = synth.random_state((2, 3, dk, dv), seed=4, scale=0.3)
+    Sr, yr = oracle.gdn2_scan(S0, inp["q"], inp["k"], inp["v"], inp["alpha_kda"], inp["b_erase"], inp["w_write"])
+    S, y = _gdn2_gpu(sdm, S0, inp)
+    assert_y_close(y, yr)
+    assert_state_close(S, Sr)
+
+
+@pytest.mark.slow
+def test_gdn2_full_size_sampled():
+    """The dense workload's shape (B=4, T=4096, H=16, dk=dv=128) through GDN2;
+    the oracle recomputes three whole (b, h) sequences."""
+    sdm = need_gpu()
+    sh = synth.GDN_DENSE
+    inp = synth.gdn_inputs(sh, seed=0)
+    S, y = _gdn2_gpu(sdm, np.zeros((sh.B, sh.H, sh.dk, sh.dv), np.float32), inp)
+    for b, h in ((0, 0), (1, 9), (3, 15)):
+        sl = (slice(b, b + 1), slice(None), slice(h, h + 1))
+        Sr, yr = oracle.gdn2_scan(np.zeros((1, 1, sh.dk, sh.dv)), inp["q"][sl], inp["k"][sl], inp["v"][sl],
+                                  inp["alpha_kda"][sl], inp["b_erase"][sl], inp["w_write"][sl])
+        assert_y_close(y[sl], yr, what=f"y[{b},{h}]")
+        assert_state_close(S[b:b + 1, h:h + 1], Sr, what=f"state[{b},{h}]")
+
+
+def test_gdn2_gates_equal_to_beta_match_the_kda_kernel():
+    """b = w = beta 1 on the GPU gives the KDA kernel's result (within fp32
+    rounding of the differently ordered products)."""
+    sdm = need_gpu()
+    sh = synth.GDN_DENSE.with_(B=1, T=150, H=2, dk=64, dv=64)
+    inp = synth.gdn_inputs(sh, seed=31)
+    S0 = synth.random_state((1, 2, 64, 64), seed=32, scale=0.3)
+    inp = dict(inp)
+    inp["b_erase"] = np.repeat(inp["beta"][..., None], 64, axis=-1).astype(np.float32)
+    inp["w_write"] = np.repeat(inp["beta"][..., None], 64, axis=-1).astype(np.float32)
+    S2, y2 = _gdn2_gpu(sdm, S0, inp)
+    Sk, yk = _gdn_gpu(sdm, S0, inp, True)
+    assert_y_close(y2, yk.astype(np.float64))
+    assert_state_close(S2, Sk.astype(np.float64))
+
+
 # ------------------------------------------------------------------------- SSE
-def _sse_gpu(sdm, S0, inp, topk):
+def _sse_gpu(sdm, S0, inp, topk, mode=0):
     import torch
     B, T, H, N = inp["route"].shape
     state = dev(S0)
     sel = torch.zeros((B, T, H, topk), dtype=torch.int32, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     y = sdm.sse_scan(state, dev(inp["route"]), topk, dev(inp["klog"]), dev(inp["q"]), dev(inp["v"]),
-                     dev(inp["alpha"]), sel_out=sel, dev_err=err)
+                     dev(inp["alpha"]), sel_out=sel, dev_err=err, write_mode=mode)
     return host(state), host(y), host(sel), int(host(err)[0])
 
 
@@ -180,6 +232,45 @@ def test_sse_full_size_sampled():
         sl = (slice(b, b + 1), slice(None), slice(h, h + 1))
         Sr, yr, selr = oracle.sse_scan(np.zeros((1, 1, sh.N + 1, sh.c, sh.d)), inp["route"][sl], sh.topk,
                                        inp["klog"][sl], inp["q"][sl], inp["v"][sl], inp["alpha"][sl])
+        np.testing.assert_array_equal(sel[sl], selr)
+        assert_y_close(y[sl], yr, what=f"y[{b},{h}]")
+        assert_state_close(S[b:b + 1, h:h + 1], Sr, what=f"state[{b},{h}]")
+
+
+@pytest.mark.parametrize("N,topk,c,d", [(8, 2, 128, 128), (4, 1, 64, 32), (16, 3, 32, 48), (1, 1, 16, 16)])
+def test_sse_delta_reduced_parity(N, topk, c, d):
+    """The delta write (shared residual per visited partition); partitions no
+    token visits keep their bits."""
+    sdm = need_gpu()
+    sh = synth.SSE_PART.with_(B=2, T=150, H=3, N=N, topk=topk, c=c, d=d)
+    inp = synth.sse_inputs(sh, seed=2 * N + c + 1)
+    S0 = synth.random_state((2, 3, N + 1, c, d), seed=6, scale=0.5)
+    Sr, yr, selr = oracle.sse_scan(S0, inp["route"], topk, inp["klog"], inp["q"], inp["v"], inp["alpha"],
+                                   oracle.SSE_WRITE_DELTA)
+    S, y, sel, err = _sse_gpu(sdm, S0, inp, topk, oracle.SSE_WRITE_DELTA)
+    assert err == 0
+    np.testing.assert_array_equal(sel, selr)
+    assert_y_close(y, yr)
+    assert_state_close(S, Sr)
+    for b in range(2):
+        for h in range(3):
+            for p in set(range(N)) - set(sel[b, :, h].ravel().tolist()):
+                np.testing.assert_array_equal(S[b, h, p], S0[b, h, p])
+
+
+@pytest.mark.slow
+def test_sse_delta_full_size_sampled():
+    sdm = need_gpu()
+    sh = synth.SSE_PART
+    inp = synth.sse_inputs(sh, seed=1)
+    S0 = np.zeros((sh.B, sh.H, sh.N + 1, sh.c, sh.d), np.float32)
+    S, y, sel, err = _sse_gpu(sdm, S0, inp, sh.topk, oracle.SSE_WRITE_DELTA)
+    assert err == 0
+    for b, h in ((1, 2), (2, 6)):
+        sl = (slice(b, b + 1), slice(None), slice(h, h + 1))
+        Sr, yr, selr = oracle.sse_scan(np.zeros((1, 1, sh.N + 1, sh.c, sh.d)), inp["route"][sl], sh.topk,
+                                       inp["klog"][sl], inp["q"][sl], inp["v"][sl], inp["alpha"][sl],
+                                       oracle.SSE_WRITE_DELTA)
         np.testing.assert_array_equal(sel[sl], selr)
         assert_y_close(y[sl], yr, what=f"y[{b},{h}]")
         assert_state_close(S[b:b + 1, h:h + 1], Sr, what=f"state[{b},{h}]")
