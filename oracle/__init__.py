@@ -53,12 +53,15 @@ def _load():
             P = ctypes.c_void_p
             I = ctypes.c_int
             lib.oracle_address.argtypes = [P, P, I, I, I, I, I, I, P, P]
-            lib.oracle_sdm_scan.argtypes = [P, P, P, P, P, P, I, P, P, I, I, I, I, I, I, I, P]
+            lib.oracle_sdm_scan.argtypes = [P, P, P, P, P, P, I, P, P, I, I, I, I, I, I, I, P, P]
+            lib.oracle_sdm_scan_backward.argtypes = [P, P, P, P, P, P, P, I, P, P, I, I, I, I, I, I, I, P, P, P, P, P,
+                                                     P, P]
             lib.oracle_gdn_scan.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, P]
             lib.oracle_gdn2_scan.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, P]
             lib.oracle_sse_scan.argtypes = [P, P, I, P, P, P, P, I, I, I, I, I, I, P, P, I]
             lib.oracle_widen_bf16.argtypes = [P, P, ctypes.c_long]
-            for f in (lib.oracle_address, lib.oracle_sdm_scan, lib.oracle_gdn_scan, lib.oracle_sse_scan):
+            for f in (lib.oracle_address, lib.oracle_sdm_scan, lib.oracle_sdm_scan_backward, lib.oracle_gdn_scan,
+                      lib.oracle_gdn2_scan, lib.oracle_sse_scan):
                 f.restype = I
             _lib = lib
     return _lib
@@ -97,10 +100,11 @@ def address(s1: np.ndarray, s2: np.ndarray, k: int, W: int):
     return idx, w
 
 
-def sdm_scan(state, v, alpha, beta, idx_w, w_w, idx_r, w_r, mode=RESID_SHARED):
+def sdm_scan(state, v, alpha, beta, idx_w, w_w, idx_r, w_r, mode=RESID_SHARED, keep_undo=False):
     """Sparse delta-rule scan.  state [B,H,N,dv] (copied, fp64); v [B,T,H,dv]
     (fp32, fp64 or bf16 bits); alpha, beta [B,T,H]; idx_*/w_* [B,T,H,W|R].
-    Returns (final state fp64, y fp64 [B,T,H,dv])."""
+    Returns (final state fp64, y fp64 [B,T,H,dv]), plus the undo log
+    [B,T,H,W,dv] (rows of I^w before each token's decay) if keep_undo."""
     M = np.array(state, dtype=np.float64, copy=True, order="C")
     B, H, N, dv = M.shape
     vv = _c(widen(v), np.float64)
@@ -115,11 +119,37 @@ def sdm_scan(state, v, alpha, beta, idx_w, w_w, idx_r, w_r, mode=RESID_SHARED):
     assert vv.shape == (B, T, H, dv) and iw.shape == (B, T, H, W) and ir.shape == (B, T, H, R)
     assert a.shape == (B, T, H) and b.shape == (B, T, H)
     y = np.zeros((B, T, H, dv), np.float64)
+    undo = np.zeros((B, T, H, W, dv), np.float64) if keep_undo else None
     rc = _load().oracle_sdm_scan(_p(M), _p(vv), _p(a), _p(b), _p(iw), _p(ww), W, _p(ir), _p(wr), R,
-                                 B, T, H, N, dv, int(mode), _p(y))
+                                 B, T, H, N, dv, int(mode), _p(y), _p(undo) if keep_undo else None)
     if rc != 0:
         raise ValueError(f"oracle_sdm_scan failed (rc={rc})")
-    return M, y
+    return (M, y, undo) if keep_undo else (M, y)
+
+
+def sdm_scan_backward(state_T, dstate_T, v, alpha, beta, idx_w, w_w, idx_r, w_r, mode, undo, dy):
+    """Gradients of sdm_scan by undoing its writes.  state_T: the forward's
+    final table; dstate_T: dL/dM_T; undo: the forward's log; dy: dL/dy.
+    Returns (M_0, dL/dM_0, dv, dalpha, dbeta, dw_w, dw_r), all fp64."""
+    M = np.array(state_T, dtype=np.float64, copy=True, order="C")
+    dM = np.array(dstate_T, dtype=np.float64, copy=True, order="C")
+    B, H, N, dv = M.shape
+    vv = _c(widen(v), np.float64)
+    T = vv.shape[1]
+    iw, ir = _c(idx_w, np.int32), _c(idx_r, np.int32)
+    W, R = iw.shape[-1], ir.shape[-1]
+    ww, wr, a, b = (_c(x, np.float64) for x in (w_w, w_r, alpha, beta))
+    un, g = _c(undo, np.float64), _c(dy, np.float64)
+    assert dM.shape == M.shape and un.shape == (B, T, H, W, dv) and g.shape == (B, T, H, dv)
+    dvo = np.zeros((B, T, H, dv))
+    da, db = np.zeros((B, T, H)), np.zeros((B, T, H))
+    dww, dwr = np.zeros((B, T, H, W)), np.zeros((B, T, H, R))
+    rc = _load().oracle_sdm_scan_backward(_p(M), _p(dM), _p(vv), _p(a), _p(b), _p(iw), _p(ww), W, _p(ir), _p(wr), R,
+                                          B, T, H, N, dv, int(mode), _p(un), _p(g), _p(dvo), _p(da), _p(db),
+                                          _p(dww), _p(dwr))
+    if rc != 0:
+        raise ValueError(f"oracle_sdm_scan_backward failed (rc={rc})")
+    return M, dM, dvo, da, db, dww, dwr
 
 
 def gdn_scan(state, q, k, v, alpha, beta, per_channel: bool):

@@ -15,6 +15,12 @@
  *                      deck, "Selected slots decay and update; other slots
  *                      persist", Eqs. 3-5, and "A v1 inconsistency matters for
  *                      reproducing the update", Fig. 2 shared residual).
+ *   oracle_sdm_scan_backward - the gradients of oracle_sdm_scan, walking the
+ *                      tokens backwards and undoing each token's writes from
+ *                      the rows the forward logged (same deck, "Training
+ *                      parallelizes within chunks and recurs across chunks"
+ *                      and "Backup: undoing writes avoids repeated full-table
+ *                      snapshots", App. A.3).
  *   oracle_gdn_scan  - dense Gated DeltaNet / KDA (Linear Attention
  *                      Architectures deck, "GDN and KDA change the granularity
  *                      of forgetting", Eqs. 15-20).
@@ -154,6 +160,8 @@ int oracle_address(const float *s1, const float *s2, int B, int T, int H, int sq
  * idx_w, w_w  : int32 / fp64 [B,T,H,W]  write slots I^w and weights k^(i).
  * idx_r, w_r  : int32 / fp64 [B,T,H,R]  read slots I^r and weights q^(i).
  * y     : fp64 [B,T,H,dv].
+ * undo  : optional fp64 [B,T,H,W,dv] (NULL: not kept): the rows of I^w as
+ *         they were before token t's decay, the log the backward undoes.
  *
  * For each (b,h), tokens in order:
  *   M~[i]  = alpha * M[i]                          for i in I^w only
@@ -166,7 +174,7 @@ int oracle_address(const float *s1, const float *s2, int B, int T, int H, int sq
  */
 int oracle_sdm_scan(double *state, const double *v, const double *alpha, const double *beta,
                     const int32_t *idx_w, const double *w_w, int W, const int32_t *idx_r, const double *w_r,
-                    int R, int B, int T, int H, int N, int dv, int mode, double *y)
+                    int R, int B, int T, int H, int N, int dv, int mode, double *y, double *undo)
 {
     if (B < 0 || T < 0 || H < 0 || N < 1 || dv < 1 || W < 1 || R < 1) return -1;
     if (mode != ORACLE_RESID_SHARED && mode != ORACLE_RESID_PERSLOT && mode != ORACLE_RESID_ADDITIVE)
@@ -196,6 +204,9 @@ int oracle_sdm_scan(double *state, const double *v, const double *alpha, const d
                 }
                 for (int j = 0; j < R; ++j)
                     if (ir[j] < 0 || ir[j] >= N) { rc = -2; goto done; }
+                if (undo)
+                    for (int j = 0; j < W; ++j)
+                        memcpy(undo + (tok * W + j) * (size_t)dv, M + (size_t)iw[j] * dv, sizeof(double) * dv);
                 /* selective decay of the written rows only */
                 for (int j = 0; j < W; ++j)
                     for (int c = 0; c < dv; ++c) mt[(size_t)j * dv + c] = a * M[(size_t)iw[j] * dv + c];
@@ -230,6 +241,118 @@ int oracle_sdm_scan(double *state, const double *v, const double *alpha, const d
 done:
     free(mt); free(vhat);
     return rc;
+}
+
+/*
+ * Backward of oracle_sdm_scan, undoing the writes (SDM deck, App. A.3: the
+ * forward keeps only the sparse update log, the backward walks the tokens in
+ * reverse and restores each token's written rows from it).
+ *
+ * state  : fp64 [B,H,N,dv]  M_T in; M_0 out (every written row restored).
+ * dstate : fp64 [B,H,N,dv]  dL/dM_T in; dL/dM_0 out.
+ * v, alpha, beta, idx_w, w_w, idx_r, w_r, mode : as in oracle_sdm_scan.
+ * undo   : fp64 [B,T,H,W,dv]  the forward's log (rows of I^w before decay).
+ * dy     : fp64 [B,T,H,dv]    dL/dy.
+ * dv     : fp64 [B,T,H,dv] out.   dalpha, dbeta : fp64 [B,T,H] out.
+ * dw_w   : fp64 [B,T,H,W] out.    dw_r : fp64 [B,T,H,R] out.
+ *
+ * For token t (last to first), with M = M_t and G = dL/dM_t:
+ *   read   y = sum_i r_i M[i]:       dr_i = <dy, M[i]>,  G[i] += r_i dy
+ *   write  M[i_j] = m_j + beta w_j rho_j,  m_j = alpha undo_j, with
+ *            shared   rho_j = v - sum_k w_k m_k
+ *            per-slot rho_j = v - m_j
+ *            additive rho_j = v
+ *          and G_j = G[i_j]:
+ *            dbeta   = sum_j w_j <G_j, rho_j>
+ *            dw_j    = beta <G_j, rho_j>  (- <g, m_j> for shared)
+ *            dv      = g = beta sum_j w_j G_j
+ *            dm_j    = G_j - w_j g (shared), G_j (1 - beta w_j) (per-slot), G_j (additive)
+ *            dalpha  = sum_j <dm_j, undo_j>
+ *          then G[i_j] = alpha dm_j and M[i_j] = undo_j.
+ * Rows outside I^w pass their gradient through unchanged.
+ */
+int oracle_sdm_scan_backward(double *state, double *dstate, const double *v, const double *alpha,
+                             const double *beta, const int32_t *idx_w, const double *w_w, int W,
+                             const int32_t *idx_r, const double *w_r, int R, int B, int T, int H, int N, int dv,
+                             int mode, const double *undo, const double *dy, double *dvo, double *dalpha,
+                             double *dbeta, double *dw_w, double *dw_r)
+{
+    if (B < 0 || T < 0 || H < 0 || N < 1 || dv < 1 || W < 1 || R < 1) return -1;
+    if (mode != ORACLE_RESID_SHARED && mode != ORACLE_RESID_PERSLOT && mode != ORACLE_RESID_ADDITIVE)
+        return -1;
+    double *m = (double *)malloc(sizeof(double) * (size_t)W * dv);
+    double *G = (double *)malloc(sizeof(double) * (size_t)W * dv);
+    double *res = (double *)malloc(sizeof(double) * (size_t)W * dv);
+    double *g = (double *)malloc(sizeof(double) * (size_t)dv);
+    if (!m || !G || !res || !g) {
+        free(m); free(G); free(res); free(g);
+        return -1;
+    }
+    for (int b = 0; b < B; ++b) {
+        for (int h = 0; h < H; ++h) {
+            double *M = state + ((size_t)b * H + h) * (size_t)N * dv;
+            double *dM = dstate + ((size_t)b * H + h) * (size_t)N * dv;
+            for (int t = T - 1; t >= 0; --t) {
+                size_t tok = ((size_t)b * T + t) * H + h;
+                const int32_t *iw = idx_w + tok * W, *ir = idx_r + tok * R;
+                const double *ww = w_w + tok * W, *wr = w_r + tok * R;
+                const double *vt = v + tok * dv, *dyt = dy + tok * dv;
+                const double *un = undo + tok * (size_t)W * dv;
+                double a = alpha[tok], be = beta[tok];
+                /* read after the write */
+                for (int i = 0; i < R; ++i) {
+                    double *row = M + (size_t)ir[i] * dv, *drow = dM + (size_t)ir[i] * dv;
+                    double s = 0.0;
+                    for (int c = 0; c < dv; ++c) s += dyt[c] * row[c];
+                    dw_r[tok * R + i] = s;
+                    for (int c = 0; c < dv; ++c) drow[c] += wr[i] * dyt[c];
+                }
+                /* the write: decayed rows, residuals, incoming gradients */
+                for (int j = 0; j < W; ++j)
+                    for (int c = 0; c < dv; ++c) {
+                        m[(size_t)j * dv + c] = a * un[(size_t)j * dv + c];
+                        G[(size_t)j * dv + c] = dM[(size_t)iw[j] * dv + c];
+                    }
+                for (int c = 0; c < dv; ++c) {
+                    double vh = 0.0;
+                    if (mode == ORACLE_RESID_SHARED)
+                        for (int j = 0; j < W; ++j) vh += ww[j] * m[(size_t)j * dv + c];
+                    for (int j = 0; j < W; ++j)
+                        res[(size_t)j * dv + c] = mode == ORACLE_RESID_SHARED    ? vt[c] - vh
+                                                  : mode == ORACLE_RESID_PERSLOT ? vt[c] - m[(size_t)j * dv + c]
+                                                                                 : vt[c];
+                    double s = 0.0;
+                    for (int j = 0; j < W; ++j) s += ww[j] * G[(size_t)j * dv + c];
+                    g[c] = be * s;
+                    dvo[tok * dv + c] = g[c];
+                }
+                double db = 0.0, da = 0.0;
+                for (int j = 0; j < W; ++j) {
+                    double gr = 0.0, gm = 0.0;
+                    for (int c = 0; c < dv; ++c) {
+                        gr += G[(size_t)j * dv + c] * res[(size_t)j * dv + c];
+                        gm += g[c] * m[(size_t)j * dv + c];
+                    }
+                    db += ww[j] * gr;
+                    dw_w[tok * W + j] = be * gr - (mode == ORACLE_RESID_SHARED ? gm : 0.0);
+                    double *drow = dM + (size_t)iw[j] * dv, *row = M + (size_t)iw[j] * dv;
+                    for (int c = 0; c < dv; ++c) {
+                        double Gc = G[(size_t)j * dv + c];
+                        double dm = mode == ORACLE_RESID_SHARED    ? Gc - ww[j] * g[c]
+                                    : mode == ORACLE_RESID_PERSLOT ? Gc * (1.0 - be * ww[j])
+                                                                   : Gc;
+                        da += dm * un[(size_t)j * dv + c];
+                        drow[c] = a * dm;
+                        row[c] = un[(size_t)j * dv + c];
+                    }
+                }
+                dbeta[tok] = db;
+                dalpha[tok] = da;
+            }
+        }
+    }
+    free(m); free(G); free(res); free(g);
+    return 0;
 }
 
 /*
