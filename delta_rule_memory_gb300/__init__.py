@@ -20,7 +20,8 @@ import torch
 
 __all__ = [
     "SdmError", "lib", "library_path", "sdm_version", "sdm_address", "sdm_scan", "sdm_scan_workspace_size",
-    "sdm_scan_noalloc", "sdm_forward_host", "sdm_forward_host_workspace_size",
+    "sdm_scan_noalloc", "sdm_forward_host", "sdm_forward_host_workspace_size", "sdm_scan_train",
+    "sdm_scan_backward", "sdm_scan_backward_workspace_size",
     "gdn_scan", "gdn_scan_workspace_size", "gdn2_scan", "sse_scan", "sse_scan_workspace_size", "SDM_RESID_SHARED", "SDM_RESID_PERSLOT", "SSE_WRITE_ADDITIVE", "SSE_WRITE_DELTA",
     "SDM_RESID_ADDITIVE", "SDM_DEVERR_INDEX_RANGE", "SDM_DEVERR_INDEX_REPEAT", "SDM_DEVERR_NONFINITE",
 ]
@@ -44,6 +45,11 @@ _SIGNATURES = {
     "sdm_scan_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "sdm_scan": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P, _P]),
     "sdm_scan_noalloc": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "sdm_scan_train": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _SZ, _P,
+                            _P]),
+    "sdm_scan_backward_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "sdm_scan_backward": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P,
+                               _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "sdm_forward_host_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I, _I, _I]),
     "sdm_forward_host": (_I, [_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _I, _P,
                               _SZ, _P, _P]),
@@ -137,6 +143,92 @@ def sdm_address(s1: torch.Tensor, s2: torch.Tensor, k: int, W: int, idx_out=None
 
 def sdm_scan_workspace_size(B: int, T: int, H: int, W: int, R: int) -> int:
     return int(lib().sdm_scan_workspace_size(B, T, H, W, R))
+
+
+def _scan_shapes(state, v, alpha, beta, idx_w, w_w, idx_r, w_r):
+    _req(state, "state", torch.float32)
+    if state.dim() != 4:
+        raise ValueError("state must be [B,H,N,d_v]")
+    B, H, N, dv = state.shape
+    if v.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("v must be float32 or bfloat16")
+    _req(v, "v", v.dtype)
+    if v.dim() != 4 or v.shape[0] != B or v.shape[2] != H or v.shape[3] != dv:
+        raise ValueError(f"v must be [B,T,H,d_v] = [{B},T,{H},{dv}]")
+    T = v.shape[1]
+    _req(alpha, "alpha", torch.float32, (B, T, H))
+    _req(beta, "beta", torch.float32, (B, T, H))
+    _req(idx_w, "idx_w", torch.int32)
+    W = idx_w.shape[-1]
+    _req(idx_w, "idx_w", torch.int32, (B, T, H, W))
+    _req(w_w, "w_w", torch.float32, (B, T, H, W))
+    _req(idx_r, "idx_r", torch.int32)
+    R = idx_r.shape[-1]
+    _req(idx_r, "idx_r", torch.int32, (B, T, H, R))
+    _req(w_r, "w_r", torch.float32, (B, T, H, R))
+    return B, T, H, N, dv, W, R
+
+
+def sdm_scan_train(state, v, alpha, beta, idx_w, w_w, idx_r, w_r, resid_mode=SDM_RESID_SHARED, y=None, undo=None,
+                   workspace=None, dev_err=None, stream=None):
+    """sdm_scan that also returns the undo log fp32 [B,T,H,W,d_v] (the
+    written rows before each token's decay) for sdm_scan_backward.
+    Returns (y, undo)."""
+    B, T, H, N, dv, W, R = _scan_shapes(state, v, alpha, beta, idx_w, w_w, idx_r, w_r)
+    if y is None:
+        y = torch.empty((B, T, H, dv), dtype=torch.float32, device=state.device)
+    _req(y, "y", torch.float32, (B, T, H, dv))
+    if undo is None:
+        undo = torch.empty((B, T, H, W, dv), dtype=torch.float32, device=state.device)
+    _req(undo, "undo", torch.float32, (B, T, H, W, dv))
+    need = sdm_scan_workspace_size(B, T, H, W, R)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=state.device)
+    _req(workspace, "workspace", torch.uint8)
+    if dev_err is not None:
+        _req(dev_err, "dev_err", torch.int32)
+    vdt = SDM_DTYPE_BF16 if v.dtype == torch.bfloat16 else SDM_DTYPE_F32
+    rc = lib().sdm_scan_train(state.data_ptr(), v.data_ptr(), vdt, alpha.data_ptr(), beta.data_ptr(),
+                              idx_w.data_ptr(), w_w.data_ptr(), W, idx_r.data_ptr(), w_r.data_ptr(), R, B, T, H, N, dv,
+                              int(resid_mode), y.data_ptr(), undo.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                              _ptr(dev_err), _stream(stream))
+    _check("sdm_scan_train", rc)
+    return y, undo
+
+
+def sdm_scan_backward_workspace_size(B: int, T: int, H: int, W: int, R: int, d_v: int) -> int:
+    return int(lib().sdm_scan_backward_workspace_size(B, T, H, W, R, d_v))
+
+
+def sdm_scan_backward(state, dstate, v, alpha, beta, idx_w, w_w, idx_r, w_r, undo, dy, resid_mode=SDM_RESID_SHARED,
+                      workspace=None, dev_err=None, stream=None):
+    """Gradients of sdm_scan_train.  `state` holds M_T and becomes M_0;
+    `dstate` holds dL/dM_T and becomes dL/dM_0 (both in place).  Returns
+    (dv, dalpha, dbeta, dw_w, dw_r), fp32."""
+    B, T, H, N, dv_, W, R = _scan_shapes(state, v, alpha, beta, idx_w, w_w, idx_r, w_r)
+    _req(dstate, "dstate", torch.float32, (B, H, N, dv_))
+    _req(undo, "undo", torch.float32, (B, T, H, W, dv_))
+    _req(dy, "dy", torch.float32, (B, T, H, dv_))
+    dev = state.device
+    dv = torch.empty((B, T, H, dv_), dtype=torch.float32, device=dev)
+    dalpha = torch.empty((B, T, H), dtype=torch.float32, device=dev)
+    dbeta = torch.empty((B, T, H), dtype=torch.float32, device=dev)
+    dw_w = torch.empty((B, T, H, W), dtype=torch.float32, device=dev)
+    dw_r = torch.empty((B, T, H, R), dtype=torch.float32, device=dev)
+    need = sdm_scan_backward_workspace_size(B, T, H, W, R, dv_)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    _req(workspace, "workspace", torch.uint8)
+    if dev_err is not None:
+        _req(dev_err, "dev_err", torch.int32)
+    vdt = SDM_DTYPE_BF16 if v.dtype == torch.bfloat16 else SDM_DTYPE_F32
+    rc = lib().sdm_scan_backward(state.data_ptr(), dstate.data_ptr(), v.data_ptr(), vdt, alpha.data_ptr(),
+                                 beta.data_ptr(), idx_w.data_ptr(), w_w.data_ptr(), W, idx_r.data_ptr(), w_r.data_ptr(),
+                                 R, B, T, H, N, dv_, int(resid_mode), undo.data_ptr(), dy.data_ptr(), dv.data_ptr(),
+                                 dalpha.data_ptr(), dbeta.data_ptr(), dw_w.data_ptr(), dw_r.data_ptr(),
+                                 workspace.data_ptr(), workspace.numel(), _ptr(dev_err), _stream(stream))
+    _check("sdm_scan_backward", rc)
+    return dv, dalpha, dbeta, dw_w, dw_r
 
 
 def sdm_scan(state, v, alpha, beta, idx_w, w_w, idx_r, w_r, resid_mode=SDM_RESID_SHARED, y=None, workspace=None,

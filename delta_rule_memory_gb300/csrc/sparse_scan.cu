@@ -146,7 +146,8 @@ struct ScanArgs {
   const void *v;
   const void *rec;
   float *y;
-  int T, H, N, d_v, v_bf16, tiles;
+  float *undo;  // optional [B,T,H,W,d_v]: the written rows before each token's decay
+  int T, H, N, d_v, v_bf16, tiles, W;
   long total_warps;
 };
 
@@ -170,7 +171,7 @@ __device__ __forceinline__ float4 xsum4(float4 a) {  // sum over the four row su
   return a;
 }
 
-template <int P, int SLOTS, int MODE>
+template <int P, int SLOTS, int MODE, bool LOG>  // LOG: also write the undo log
 __global__ void __launch_bounds__(128) sparse_scan_kernel(const ScanArgs a) {
   using L = ScanLayout<P, SLOTS>;
   using Rec = TokenRec<SLOTS>;
@@ -271,6 +272,8 @@ __global__ void __launch_bounds__(128) sparse_scan_kernel(const ScanArgs a) {
 
   float *yp_out = a.y + tok0 * d_v + col;
   const long y_step = tok_stride * d_v;
+  float *undo_out = LOG ? a.undo + tok0 * a.W * d_v + col : nullptr;
+  const long undo_step = tok_stride * a.W * d_v;
   const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
   int cur_rec = 0, cur_ring = 0;
   for (int t = 0; t < T; ++t) {
@@ -321,6 +324,12 @@ __global__ void __launch_bounds__(128) sparse_scan_kernel(const ScanArgs a) {
     float4 vh = zero4;
 #pragma unroll
     for (int k = 0; k < RPL; ++k) md[k] = ld4(row_ptr(my_src[k]));
+    if (LOG) {  // the undo log: write slot j = r + 4k before the decay
+#pragma unroll
+      for (int k = 0; k < RPL; ++k)
+        if (active && r + 4 * k < a.W) st4(undo_out + static_cast<long>(r + 4 * k) * d_v, md[k]);
+      undo_out += undo_step;
+    }
     // read rows; a read of a row this token writes is patched below
     float4 xr[RPL];
     bool recomp = false;
@@ -393,7 +402,7 @@ size_t warp_bytes_dispatch(int slots, int P) {
 template <int P, int SLOTS, int MODE>
 int launch_scan(const ScanArgs &args, int wpc, cudaStream_t st) {
   const size_t smem = ScanLayout<P, SLOTS>::kWarpBytes * wpc;
-  auto kern = sparse_scan_kernel<P, SLOTS, MODE>;
+  auto kern = args.undo ? sparse_scan_kernel<P, SLOTS, MODE, true> : sparse_scan_kernel<P, SLOTS, MODE, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)
     return check_launch("sdm_scan: set shared memory");
@@ -430,10 +439,10 @@ extern "C" size_t sdm_scan_workspace_size(int B, int T, int H, int W, int R) {
   return (n + 255) & ~static_cast<size_t>(255);
 }
 
-extern "C" int sdm_scan(float *state, const void *v, int v_dtype, const float *alpha, const float *beta,
-                        const int32_t *idx_w, const float *w_w, int W, const int32_t *idx_r, const float *w_r, int R,
-                        int B, int T, int H, int N, int d_v, int resid_mode, float *y, void *workspace,
-                        size_t workspace_bytes, int32_t *dev_err, void *stream) {
+static int scan_core(float *state, const void *v, int v_dtype, const float *alpha, const float *beta,
+                     const int32_t *idx_w, const float *w_w, int W, const int32_t *idx_r, const float *w_r, int R,
+                     int B, int T, int H, int N, int d_v, int resid_mode, float *y, float *undo, void *workspace,
+                     size_t workspace_bytes, int32_t *dev_err, void *stream) {
   if (!state || !v || !alpha || !beta || !idx_w || !w_w || !idx_r || !w_r || !y)
     return set_error(SDM_ERR_INVALID_ARG, "sdm_scan: null pointer");
   if (B < 0 || T < 0 || H < 0 || N < 1 || d_v < 1)
@@ -512,7 +521,27 @@ chosen:
   args.v_bf16 = v_dtype == SDM_DTYPE_BF16;
   args.tiles = tiles;
   args.total_warps = total_warps;
+  args.undo = undo;
+  args.W = W;
   return launch_dispatch(slots, window, resid_mode, args, wpc, st);
+}
+
+extern "C" int sdm_scan(float *state, const void *v, int v_dtype, const float *alpha, const float *beta,
+                        const int32_t *idx_w, const float *w_w, int W, const int32_t *idx_r, const float *w_r, int R,
+                        int B, int T, int H, int N, int d_v, int resid_mode, float *y, void *workspace,
+                        size_t workspace_bytes, int32_t *dev_err, void *stream) {
+  return scan_core(state, v, v_dtype, alpha, beta, idx_w, w_w, W, idx_r, w_r, R, B, T, H, N, d_v, resid_mode, y,
+                   nullptr, workspace, workspace_bytes, dev_err, stream);
+}
+
+extern "C" int sdm_scan_train(float *state, const void *v, int v_dtype, const float *alpha, const float *beta,
+                              const int32_t *idx_w, const float *w_w, int W, const int32_t *idx_r, const float *w_r,
+                              int R, int B, int T, int H, int N, int d_v, int resid_mode, float *y, float *undo,
+                              void *workspace, size_t workspace_bytes, int32_t *dev_err, void *stream) {
+  if (!undo) return set_error(SDM_ERR_INVALID_ARG, "sdm_scan_train: null undo log");
+  if (!aligned(undo, 16)) return set_error(SDM_ERR_ALIGN, "sdm_scan_train: the undo log needs 16-byte alignment");
+  return scan_core(state, v, v_dtype, alpha, beta, idx_w, w_w, W, idx_r, w_r, R, B, T, H, N, d_v, resid_mode, y,
+                   undo, workspace, workspace_bytes, dev_err, stream);
 }
 
 // ---------------------------------------------------------------------------

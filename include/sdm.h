@@ -212,6 +212,63 @@ SDM_API int sdm_scan_noalloc(float *state, const void *v, int v_dtype, const flo
                      void *stream);
 
 /*
+ * sdm_scan_train - sdm_scan that also keeps the undo log the backward needs
+ * ([SDM] "Backup: undoing writes avoids repeated full-table snapshots",
+ * App. A.3: the forward keeps only the sparse update information, T W d_v
+ * values, instead of table snapshots).
+ *
+ * Arguments as sdm_scan, plus
+ * undo : fp32 [B,T,H,W,d_v], 16-byte aligned, written: undo[b,t,h,j,:] is
+ *        row idx_w[b,t,h,j] of the table as it was just before token t
+ *        (before the decay).  For the 1.4B-layer shape: 61 KB per token-head.
+ * y, the final table and the error codes are identical to sdm_scan's.
+ */
+SDM_API int sdm_scan_train(float *state, const void *v, int v_dtype, const float *alpha, const float *beta,
+                           const int32_t *idx_w, const float *w_w, int W, const int32_t *idx_r, const float *w_r,
+                           int R, int B, int T, int H, int N, int d_v, int resid_mode, float *y, float *undo,
+                           void *workspace, size_t workspace_bytes, int32_t *dev_err, void *stream);
+
+/*
+ * Scratch bytes sdm_scan_backward needs: per 32-column tile of d_v and per
+ * token-head, R + W + 2 fp32 partial column sums, rounded up to 256.
+ */
+SDM_API size_t sdm_scan_backward_workspace_size(int B, int T, int H, int W, int R, int d_v);
+
+/*
+ * sdm_scan_backward - gradients of sdm_scan through its undo log, walking the
+ * tokens backwards (same deck, App. A.3).  For token t (last to first), with
+ * M = M_t and G = dL/dM_t:
+ *   read   dL/dw_r[i] = <dy_t, M[idx_r[i]]>,   G[idx_r[i]] += w_r[i] dy_t
+ *   write  M[i_j] = m_j + beta w_j rho_j with m_j = alpha undo_j and rho_j the
+ *          residual of resid_mode; G_j = G[i_j]; g = beta sum_j w_j G_j:
+ *          dL/dv_t = g;  dL/dbeta = sum_j w_j <G_j, rho_j>;
+ *          dL/dw_w[j] = beta <G_j, rho_j> (- <g, m_j> for SDM_RESID_SHARED);
+ *          dm_j = G_j - w_j g (shared) | G_j (1 - beta w_j) (per-slot) | G_j;
+ *          dL/dalpha = sum_j <dm_j, undo_j>;  then G[i_j] = alpha dm_j and
+ *          M[i_j] = undo_j.
+ *
+ * state  : fp32 [B,H,N,d_v]: M_T (as sdm_scan_train left it) in, M_0 out
+ *          (bit-identical to the table before the forward).
+ * dstate : fp32 [B,H,N,d_v]: dL/dM_T in (zeros if the loss ignores the final
+ *          table), dL/dM_0 out.
+ * v, v_dtype, alpha, beta, idx_w, w_w, W, idx_r, w_r, R, sizes, resid_mode :
+ *          exactly as given to sdm_scan_train.
+ * undo   : its log.   dy : fp32 [B,T,H,d_v], dL/dy.
+ * dv     : fp32 [B,T,H,d_v] out.   dalpha, dbeta : fp32 [B,T,H] out.
+ * dw_w   : fp32 [B,T,H,W] out.     dw_r : fp32 [B,T,H,R] out.
+ * workspace : sdm_scan_backward_workspace_size() bytes.
+ * dev_err : optional; SDM_DEVERR_INDEX_RANGE for an id outside [0, N) (skipped).
+ * Work: one warp per (batch, head, 32 columns), one column per lane, then a
+ *       deterministic reduction of the column sums over the tiles.
+ */
+SDM_API int sdm_scan_backward(float *state, float *dstate, const void *v, int v_dtype, const float *alpha,
+                              const float *beta, const int32_t *idx_w, const float *w_w, int W,
+                              const int32_t *idx_r, const float *w_r, int R, int B, int T, int H, int N, int d_v,
+                              int resid_mode, const float *undo, const float *dy, float *dv, float *dalpha,
+                              float *dbeta, float *dw_w, float *dw_r, void *workspace, size_t workspace_bytes,
+                              int32_t *dev_err, void *stream);
+
+/*
  * Scratch bytes gdn_scan needs.  Dense GDN at dk = dv = 128 (the chunked
  * tensor-core path) needs one tile set per chunk of 64 tokens (operands of
  * the state-dependent products: 114,944 bytes) plus 4 bytes per chunk,
