@@ -9,7 +9,8 @@ recurrence; a step is the next B*T tokens of the same sequences, so every
 step does identical work).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload sdm_14b_layer|sdm_sweep_H2|H4|H8|gdn|kda|gdn2|sse|sse_delta|sdm_tiny|sdm_decode|sse_decode]
+                    [--workload sdm_14b_layer|sdm_sweep_H2|H4|H8|gdn|kda|gdn2|sse|sse_delta|sdm_tiny|sdm_decode|sse_decode|
+                               sdm_train]
 
 Prints one JSON line (rank 0).  Under torchrun each rank runs its own batch
 (independent sequences, no collective in the data path) and the time is the
@@ -199,6 +200,8 @@ class OracleSampler:
 def metric_name(wl) -> str:
     if wl.decode:
         return f"{wl.kind} decode tokens/s (one token per sequence per step; ms_per_step is the step latency)"
+    if wl.train:
+        return "SDM training step tokens/s (addressing, forward with undo log, scan and address backward)"
     return METRIC if wl.kind == "sdm" else f"{wl.kind} scan tokens/s"
 
 
@@ -212,6 +215,10 @@ class Workload:
         self.decode = name.endswith("_decode")
         if self.decode:
             name = {"sdm_decode": "sdm_14b_layer", "sse_decode": "sse"}[name]
+        # train: forward with the undo log, the scan backward and the address backward
+        self.train = name == "sdm_train"
+        if self.train:
+            name = "sdm_14b_layer"
         if name == "sdm_14b_layer":
             self.kind, self.shape = "sdm", synth.SDM_14B_LAYER
         elif name.startswith("sdm_sweep_H"):
@@ -229,6 +236,8 @@ class Workload:
             self.shape = self.shape.with_(B=batch)
         if self.decode:
             self.shape = self.shape.with_(T=1, name=self.shape.name + "_decode")
+        if self.train:
+            self.shape = self.shape.with_(name=self.shape.name + "_train")
         sh = self.shape
         self.tokens = sh.B * sh.T
 
@@ -321,6 +330,16 @@ class GpuRun:
             self.y = torch.empty((B, T, H, sh.d_v), dtype=torch.float32, device=device)
             self.ws = torch.empty(sdm.sdm_scan_workspace_size(B, T, H, sh.W, sh.R), dtype=torch.uint8, device=device)
             self.launches_per_step = 4
+            if wl.train:
+                g = torch.Generator(device=device)
+                g.manual_seed(12345)
+                self.undo = torch.empty((B, T, H, sh.W, sh.d_v), dtype=torch.float32, device=device)
+                # dL/dM_T carries over from step to step (accumulated), so no table-sized memset per step
+                self.dstate = torch.zeros_like(self.state)
+                self.dy = torch.randn((B, T, H, sh.d_v), generator=g, device=device)
+                self.ws_b = torch.empty(sdm.sdm_scan_backward_workspace_size(B, T, H, sh.W, sh.R, sh.d_v),
+                                        dtype=torch.uint8, device=device)
+                self.launches_per_step = 8  # 2 address, record + scan, backward + reduce, 2 address backward
         elif wl.kind == "gdn2":
             self.state = torch.zeros((sh.B, sh.H, sh.dk, sh.dv), dtype=torch.float32, device=device)
             self.y = torch.empty((sh.B, sh.T, sh.H, sh.dv), dtype=torch.float32, device=device)
@@ -351,7 +370,15 @@ class GpuRun:
     def main(self):
         """The dominant kernel's call."""
         sh, d = self.wl.shape, self.d
-        if self.wl.kind == "sdm":
+        if self.wl.kind == "sdm" and self.wl.train:
+            self.sdm.sdm_scan_train(self.state, d["v"], d["alpha"], d["beta"], self.iw, self.ww, self.ir, self.wr,
+                                    self.wl.mode, self.y, self.undo, self.ws, self.err)
+            _, _, _, dww, dwr = self.sdm.sdm_scan_backward(self.state, self.dstate, d["v"], d["alpha"], d["beta"],
+                                                           self.iw, self.ww, self.ir, self.wr, self.undo, self.dy,
+                                                           self.wl.mode, self.ws_b, self.err)
+            self.sdm.sdm_address_backward(self.iw, self.ww, dww, sh.sqrtN, self.err)
+            self.sdm.sdm_address_backward(self.ir, self.wr, dwr, sh.sqrtN, self.err)
+        elif self.wl.kind == "sdm":
             self.sdm.sdm_scan(self.state, d["v"], d["alpha"], d["beta"], self.iw, self.ww, self.ir, self.wr,
                               self.wl.mode, self.y, self.ws, self.err)
         elif self.wl.kind == "gdn2":
@@ -372,8 +399,9 @@ class GpuRun:
         """One step through the public API from host buffers: for the sparse
         workloads the native pipelined entry point sdm_forward_host (inputs
         copied in and y copied out per chunk, overlapped with compute); for the
-        dense and SSE scans, copies of the step's inputs and y around the call."""
-        if self.wl.kind == "sdm":
+        dense and SSE scans and the training step, copies of the step's inputs
+        and y around the call."""
+        if self.wl.kind == "sdm" and not self.wl.train:
             import torch
             sh, hst = self.wl.shape, self.host
             if not hasattr(self, "fh_ws"):
@@ -411,9 +439,17 @@ class GpuRun:
             tokh = sh.B * sh.T * sh.H
             vbytes = 2 if sh.v_bf16 else 4
             per_tok = sh.d_v * vbytes + sh.d_v * 4 + 8 + (W + R) * 8
-            return rows * sh.d_v * 4 + tokh * per_tok, "GB/s", "hbm", {
+            total = rows * sh.d_v * 4 + tokh * per_tok
+            if self.wl.train:
+                # + the undo log written; backward: M rows read for the read slots, gradient rows read and
+                # written for read and write slots, the log read and the table rows restored; v, dy read,
+                # dv written; per-tile column sums written and read; both address backwards' score rows
+                tiles = (sh.d_v + 31) // 32
+                total += tokh * (W * sh.d_v * 4 + (3 * R + 4 * W) * sh.d_v * 4 + sh.d_v * (vbytes + 8) + 8
+                                 + 2 * tiles * (W + R + 2) * 4 + 2 * 2 * sh.sqrtN * 4 + (W + R) * 16)
+            return total, "GB/s", "hbm", {
                 "mean_union_rows": float(union.float().mean().item()),
-                "bytes_per_token_head": (rows * sh.d_v * 4 + tokh * per_tok) / tokh}
+                "bytes_per_token_head": total / tokh}
         if self.wl.kind == "gdn2":
             tokh = sh.B * sh.T * sh.H
             per = 2 * (sh.dk + sh.dk + sh.dv) + 4 * sh.dk * 2 + 4 * sh.dv + 4 * sh.dv  # q k v, alpha b, w, y
@@ -530,15 +566,16 @@ def run_ours(args, rank, world, local_rank, sampler):
         "config": wl.config(),
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": algo_unit,
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": {"sdm": "sdm_scan (hazard prepass + sparse_scan_kernel)", "gdn": "gdn_scan (chunk preparation + chain kernels)",
-                                "kda": "gdn_scan", "gdn2": "gdn2_scan",
-                                "sse": "sse_scan (route prepass + sse_scan_kernel)"}[wl.kind],
+                     "kernel": "sdm_scan_train + sdm_scan_backward + 2 sdm_address_backward" if wl.train else
+                     {"sdm": "sdm_scan (hazard prepass + sparse_scan_kernel)",
+                      "gdn": "gdn_scan (chunk preparation + chain kernels)", "kda": "gdn_scan", "gdn2": "gdn2_scan",
+                      "sse": "sse_scan (route prepass + sse_scan_kernel)"}[wl.kind],
                      "launch_ms": main_ms, "peak_source": f"{src} ({'hbm_gbs' if bound == 'hbm' else 'FP32 lanes x clock'})",
                      **algo_info},
         "cpu_baseline": cpu,
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "path": "sdm_forward_host (chunked copy/compute pipeline)" if wl.kind == "sdm"
+                "path": "sdm_forward_host (chunked copy/compute pipeline)" if wl.kind == "sdm" and not wl.train
                 else "pinned H2D copies + scan call + D2H of y"},
         "gpu_launches": K * run.launches_per_step,
         "clocks": clk,

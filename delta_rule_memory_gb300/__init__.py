@@ -21,7 +21,7 @@ import torch
 __all__ = [
     "SdmError", "lib", "library_path", "sdm_version", "sdm_address", "sdm_scan", "sdm_scan_workspace_size",
     "sdm_scan_noalloc", "sdm_forward_host", "sdm_forward_host_workspace_size", "sdm_scan_train",
-    "sdm_scan_backward", "sdm_scan_backward_workspace_size",
+    "sdm_scan_backward", "sdm_scan_backward_workspace_size", "sdm_address_backward",
     "gdn_scan", "gdn_scan_workspace_size", "gdn2_scan", "sse_scan", "sse_scan_workspace_size", "SDM_RESID_SHARED", "SDM_RESID_PERSLOT", "SSE_WRITE_ADDITIVE", "SSE_WRITE_DELTA",
     "SDM_RESID_ADDITIVE", "SDM_DEVERR_INDEX_RANGE", "SDM_DEVERR_INDEX_REPEAT", "SDM_DEVERR_NONFINITE",
 ]
@@ -48,6 +48,7 @@ _SIGNATURES = {
     "sdm_scan_train": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _SZ, _P,
                             _P]),
     "sdm_scan_backward_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "sdm_address_backward": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
     "sdm_scan_backward": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P,
                                _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "sdm_forward_host_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I, _I, _I]),
@@ -194,6 +195,23 @@ def sdm_scan_train(state, v, alpha, beta, idx_w, w_w, idx_r, w_r, resid_mode=SDM
                               _ptr(dev_err), _stream(stream))
     _check("sdm_scan_train", rc)
     return y, undo
+
+
+def sdm_address_backward(idx, w, dw, sqrtN: int, dev_err=None, stream=None):
+    """Gradient of sdm_address's weights w.r.t. the score halves: idx int32,
+    w and dw fp32 [B,T,H,W] -> (ds1, ds2) fp32 [B,T,H,sqrtN]."""
+    _req(idx, "idx", torch.int32)
+    B, T, H, W = idx.shape
+    _req(w, "w", torch.float32, (B, T, H, W))
+    _req(dw, "dw", torch.float32, (B, T, H, W))
+    ds1 = torch.empty((B, T, H, sqrtN), dtype=torch.float32, device=idx.device)
+    ds2 = torch.empty((B, T, H, sqrtN), dtype=torch.float32, device=idx.device)
+    if dev_err is not None:
+        _req(dev_err, "dev_err", torch.int32)
+    rc = lib().sdm_address_backward(idx.data_ptr(), w.data_ptr(), dw.data_ptr(), B, T, H, int(sqrtN), W,
+                                    ds1.data_ptr(), ds2.data_ptr(), _ptr(dev_err), _stream(stream))
+    _check("sdm_address_backward", rc)
+    return ds1, ds2
 
 
 def sdm_scan_backward_workspace_size(B: int, T: int, H: int, W: int, R: int, d_v: int) -> int:

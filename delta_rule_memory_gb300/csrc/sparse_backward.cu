@@ -20,6 +20,8 @@
 // column of M and G and needs no synchronisation.  The column sums (dr, dw,
 // dalpha, dbeta) are reduced over the warp and written per tile; a second
 // kernel adds the tiles in a fixed order.
+#include <climits>
+
 #include "common.cuh"
 
 namespace sdm {
@@ -134,6 +136,177 @@ __global__ void __launch_bounds__(128) sparse_backward_kernel(const BackArgs a) 
   if (bad && lane == 0 && a.err) atomicOr(a.err, SDM_DEVERR_INDEX_RANGE);
 }
 
+// The same step for W, R <= 16 with every row of a token loaded at once into
+// registers (one memory round trip per token instead of one per slot).  A
+// write slot whose row is also read by the token takes the read's gradient
+// from registers; the gradient rows are stored read slots first, then write
+// slots, so a row in both ends with the write slot's value, which includes it.
+template <int MODE>
+__global__ void __launch_bounds__(128) sparse_backward_kernel16(const BackArgs a) {
+  constexpr int S = 16;
+  const int lane = threadIdx.x & 31;
+  const long gw = static_cast<long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (gw >= a.total_warps) return;  // warp-uniform
+  const int tile = static_cast<int>(gw % a.tiles);
+  const long bh = gw / a.tiles;
+  const int h = static_cast<int>(bh % a.H);
+  const long b = bh / a.H;
+  const int T = a.T, H = a.H, N = a.N, d_v = a.d_v, W = a.W, R = a.R;
+  const int col = tile * 32 + lane;
+  const bool active = col < d_v;
+  const int ccol = active ? col : 0;
+  float *M = a.state + bh * static_cast<long>(N) * d_v + ccol;
+  float *G = a.dstate + bh * static_cast<long>(N) * d_v + ccol;
+  const int np = R + W + 2;
+  bool bad = false;
+
+  for (int t = T - 1; t >= 0; --t) {
+    const long tok = (b * T + t) * H + h;
+    const float al = a.alpha[tok], be = a.beta[tok];
+    const float vc = a.v_bf16 ? bf16_to_f32(static_cast<const uint16_t *>(a.v)[tok * d_v + ccol])
+                              : static_cast<const float *>(a.v)[tok * d_v + ccol];
+    const float dyc = a.dy[tok * d_v + ccol];
+    float *pt = a.part + (static_cast<long>(tile) * (a.total_warps / a.tiles) * T + tok) * np;
+    // slot data: lane k < 16 holds read slot k, lane 16 + k write slot k
+    const int ks = lane & 15;
+    const bool is_w = lane >= 16;
+    const bool has = ks < (is_w ? W : R);
+    const int my_id = has ? (is_w ? a.idx_w[tok * W + ks] : a.idx_r[tok * R + ks]) : -1;
+    const float my_wt = has ? (is_w ? a.w_w[tok * W + ks] : a.w_r[tok * R + ks]) : 0.f;
+    bad |= has && static_cast<unsigned>(my_id) >= static_cast<unsigned>(N);
+    // a write lane finds the read slot (if any) with its row
+    int my_match = -1;
+#pragma unroll
+    for (int i = 0; i < S; ++i) {
+      const int ri = __shfl_sync(kFull, my_id, i);
+      if (is_w && has && ri == my_id) my_match = i;
+    }
+    float Mr[S], Gr[S], Gw[S], U[S];
+#pragma unroll
+    for (int k = 0; k < S; ++k) {  // every row of the token at once
+      const int ri = __shfl_sync(kFull, my_id, k), wi = __shfl_sync(kFull, my_id, 16 + k);
+      const bool okr = static_cast<unsigned>(ri) < static_cast<unsigned>(N);
+      const bool okw = static_cast<unsigned>(wi) < static_cast<unsigned>(N);
+      Mr[k] = okr ? M[static_cast<long>(ri) * d_v] : 0.f;
+      Gr[k] = okr ? G[static_cast<long>(ri) * d_v] : 0.f;
+      Gw[k] = okw ? G[static_cast<long>(wi) * d_v] : 0.f;
+      U[k] = k < W ? a.undo[(tok * W + k) * static_cast<long>(d_v) + ccol] : 0.f;
+    }
+    // the read after the write
+#pragma unroll
+    for (int i = 0; i < S; ++i) {
+      if (i < R) {
+        const float dr = warp_sum(active ? dyc * Mr[i] : 0.f);
+        if (lane == 0) pt[i] = dr;
+        Gr[i] = fmaf(__shfl_sync(kFull, my_wt, i), dyc, Gr[i]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < S; ++j) {  // a written row that is also read takes the read gradient
+      const int mi = __shfl_sync(kFull, my_match, 16 + j);
+#pragma unroll
+      for (int i = 0; i < S; ++i)
+        if (mi == i) Gw[j] = Gr[i];
+    }
+    // the write
+    float vh = 0.f, gs = 0.f;
+#pragma unroll
+    for (int j = 0; j < S; ++j) {
+      const float wj = __shfl_sync(kFull, my_wt, 16 + j);
+      if (MODE == SDM_RESID_SHARED) vh = fmaf(wj, al * U[j], vh);
+      gs = fmaf(wj, Gw[j], gs);
+    }
+    gs *= be;
+    const float res_sh = vc - vh;
+    if (active) a.dv[tok * d_v + col] = gs;
+    float dbeta = 0.f, dalpha = 0.f;
+#pragma unroll
+    for (int j = 0; j < S; ++j) {
+      const float wj = __shfl_sync(kFull, my_wt, 16 + j);
+      if (j < W) {
+        const float m = al * U[j];
+        const float rho = MODE == SDM_RESID_SHARED ? res_sh : MODE == SDM_RESID_PERSLOT ? vc - m : vc;
+        dbeta = fmaf(wj * Gw[j], rho, dbeta);
+        float dw = be * Gw[j] * rho;
+        if (MODE == SDM_RESID_SHARED) dw = fmaf(-gs, m, dw);
+        const float dm = MODE == SDM_RESID_SHARED ? fmaf(-wj, gs, Gw[j])
+                         : MODE == SDM_RESID_PERSLOT ? Gw[j] * (1.f - be * wj) : Gw[j];
+        dalpha = fmaf(dm, U[j], dalpha);
+        Gw[j] = al * dm;
+        dw = warp_sum(active ? dw : 0.f);
+        if (lane == 0) pt[R + j] = dw;
+      }
+    }
+    dalpha = warp_sum(active ? dalpha : 0.f);
+    dbeta = warp_sum(active ? dbeta : 0.f);
+    if (lane == 0) {
+      pt[R + W] = dalpha;
+      pt[R + W + 1] = dbeta;
+    }
+    // stores: read rows, then written rows (gradient and the undone table row)
+#pragma unroll
+    for (int i = 0; i < S; ++i) {
+      const int ri = __shfl_sync(kFull, my_id, i);
+      if (active && static_cast<unsigned>(ri) < static_cast<unsigned>(N)) G[static_cast<long>(ri) * d_v] = Gr[i];
+    }
+#pragma unroll
+    for (int j = 0; j < S; ++j) {
+      const int wi = __shfl_sync(kFull, my_id, 16 + j);
+      if (active && static_cast<unsigned>(wi) < static_cast<unsigned>(N)) {
+        G[static_cast<long>(wi) * d_v] = Gw[j];
+        M[static_cast<long>(wi) * d_v] = U[j];
+      }
+    }
+  }
+  if (__any_sync(kFull, bad) && lane == 0 && a.err) atomicOr(a.err, SDM_DEVERR_INDEX_RANGE);
+}
+
+// Addressing backward (SDM deck, Secs. 2 / 3.1): w = softmax of the W selected
+// sums s_i = s1[a_i] + s2[b_i]; ds_i = w_i (dw_i - sum_j w_j dw_j) lands on
+// s1[a_i] and s2[b_i], every other score gets 0.  One warp per row; the warp
+// zeroes the row, then adds the slots in order (deterministic).
+__global__ void __launch_bounds__(256) address_backward_kernel(const int32_t *idx, const float *w, const float *dw,
+                                                               long rows, int sqrtN, int W, float *ds1, float *ds2,
+                                                               int32_t *err) {
+  const int lane = threadIdx.x & 31;
+  const long r = static_cast<long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (r >= rows) return;  // warp-uniform
+  float *d1 = ds1 + r * sqrtN, *d2 = ds2 + r * sqrtN;
+  for (int a = lane; a < sqrtN; a += 32) d1[a] = d2[a] = 0.f;
+  float wv[2], dv2[2], ds[2];
+  int id[2];
+  float dot = 0.f;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int j = lane + 32 * k;
+    const bool in = j < W;
+    id[k] = in ? idx[r * W + j] : -1;
+    wv[k] = in ? w[r * W + j] : 0.f;
+    dv2[k] = in ? dw[r * W + j] : 0.f;
+    dot = fmaf(wv[k], dv2[k], dot);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(kFull, dot, o);
+#pragma unroll
+  for (int k = 0; k < 2; ++k) ds[k] = wv[k] * (dv2[k] - dot);
+  __syncwarp();
+  bool bad = false;
+  for (int j = 0; j < W; ++j) {
+    const int k = j >> 5;
+    const float g = __shfl_sync(kFull, k ? ds[1] : ds[0], j & 31);
+    const int i = __shfl_sync(kFull, k ? id[1] : id[0], j & 31);
+    if (lane == 0) {
+      if (static_cast<unsigned>(i) < static_cast<unsigned>(sqrtN * sqrtN)) {
+        d1[i / sqrtN] += g;
+        d2[i % sqrtN] += g;
+      } else {
+        bad = true;
+      }
+    }
+  }
+  if (bad && err) atomicOr(err, SDM_DEVERR_INDEX_RANGE);
+}
+
 // sum of the per-tile column sums, tile by tile in order
 __global__ void sparse_backward_reduce(const float *part, long rows, int np, int tiles, int W, int R, float *dw_r,
                                        float *dw_w, float *dalpha, float *dbeta) {
@@ -212,9 +385,15 @@ extern "C" int sdm_scan_backward(float *state, float *dstate, const void *v, int
   args.total_warps = static_cast<long>(B) * H * args.tiles;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const unsigned blocks = static_cast<unsigned>((args.total_warps + 3) / 4);
-  if (resid_mode == SDM_RESID_SHARED) sparse_backward_kernel<SDM_RESID_SHARED><<<blocks, 128, 0, st>>>(args);
-  else if (resid_mode == SDM_RESID_PERSLOT) sparse_backward_kernel<SDM_RESID_PERSLOT><<<blocks, 128, 0, st>>>(args);
-  else sparse_backward_kernel<SDM_RESID_ADDITIVE><<<blocks, 128, 0, st>>>(args);
+  if (W <= 16 && R <= 16) {
+    if (resid_mode == SDM_RESID_SHARED) sparse_backward_kernel16<SDM_RESID_SHARED><<<blocks, 128, 0, st>>>(args);
+    else if (resid_mode == SDM_RESID_PERSLOT) sparse_backward_kernel16<SDM_RESID_PERSLOT><<<blocks, 128, 0, st>>>(args);
+    else sparse_backward_kernel16<SDM_RESID_ADDITIVE><<<blocks, 128, 0, st>>>(args);
+  } else {
+    if (resid_mode == SDM_RESID_SHARED) sparse_backward_kernel<SDM_RESID_SHARED><<<blocks, 128, 0, st>>>(args);
+    else if (resid_mode == SDM_RESID_PERSLOT) sparse_backward_kernel<SDM_RESID_PERSLOT><<<blocks, 128, 0, st>>>(args);
+    else sparse_backward_kernel<SDM_RESID_ADDITIVE><<<blocks, 128, 0, st>>>(args);
+  }
   int rc = check_launch("sdm_scan_backward: kernel");
   if (rc != SDM_OK) return rc;
   const long rows = static_cast<long>(B) * T * H;
@@ -222,4 +401,20 @@ extern "C" int sdm_scan_backward(float *state, float *dstate, const void *v, int
   const unsigned rb = static_cast<unsigned>((rows * np + 255) / 256);
   sparse_backward_reduce<<<rb, 256, 0, st>>>(args.part, rows, np, args.tiles, W, R, dw_r, dw_w, dalpha, dbeta);
   return check_launch("sdm_scan_backward: reduce kernel");
+}
+
+extern "C" int sdm_address_backward(const int32_t *idx, const float *w, const float *dw, int B, int T, int H,
+                                    int sqrtN, int W, float *ds1, float *ds2, int32_t *dev_err, void *stream) {
+  if (!idx || !w || !dw || !ds1 || !ds2) return set_error(SDM_ERR_INVALID_ARG, "sdm_address_backward: null pointer");
+  if (B < 0 || T < 0 || H < 0 || sqrtN < 1) return set_error(SDM_ERR_INVALID_ARG, "sdm_address_backward: bad sizes");
+  if (W < 1 || W > 64) return set_error(SDM_ERR_SHAPE, "sdm_address_backward: need 1 <= W <= 64");
+  if (static_cast<long>(sqrtN) * sqrtN > INT_MAX) return set_error(SDM_ERR_SHAPE, "sdm_address_backward: sqrtN too large");
+  if (!aligned(idx, 4) || !aligned(w, 4) || !aligned(dw, 4) || !aligned(ds1, 4) || !aligned(ds2, 4) ||
+      (dev_err && !aligned(dev_err, 4)))
+    return set_error(SDM_ERR_ALIGN, "sdm_address_backward: 4-byte alignment needed");
+  const long rows = static_cast<long>(B) * T * H;
+  if (rows == 0) return SDM_OK;
+  address_backward_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      idx, w, dw, rows, sqrtN, W, ds1, ds2, dev_err);
+  return check_launch("sdm_address_backward");
 }

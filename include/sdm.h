@@ -212,6 +212,23 @@ SDM_API int sdm_scan_noalloc(float *state, const void *v, int v_dtype, const flo
                      void *stream);
 
 /*
+ * sdm_address_backward - gradient of the addressing weights with respect to
+ * the two score halves ([SDM] Secs. 2 / 3.1).  The selection is piecewise
+ * constant; the weights are w = softmax of the W selected sums
+ * s_i = s1[a_i] + s2[b_i] (i = a_i sqrtN + b_i), so
+ *   ds_i = w_i (dw_i - sum_j w_j dw_j),  ds1[a_i] += ds_i,  ds2[b_i] += ds_i
+ * and every other score gets 0.
+ *
+ * idx, w : int32 / fp32 [B,T,H,W], as sdm_address returned them.
+ * dw     : fp32 [B,T,H,W], dL/dw (e.g. from sdm_scan_backward).
+ * ds1, ds2 : fp32 [B,T,H,sqrtN] out (overwritten).
+ * dev_err : optional; SDM_DEVERR_INDEX_RANGE for an id outside [0, sqrtN^2).
+ * Deterministic: one warp per row, slots added in order.
+ */
+SDM_API int sdm_address_backward(const int32_t *idx, const float *w, const float *dw, int B, int T, int H, int sqrtN,
+                                 int W, float *ds1, float *ds2, int32_t *dev_err, void *stream);
+
+/*
  * sdm_scan_train - sdm_scan that also keeps the undo log the backward needs
  * ([SDM] "Backup: undoing writes avoids repeated full-table snapshots",
  * App. A.3: the forward keeps only the sparse update information, T W d_v

@@ -53,6 +53,7 @@ def _load():
             P = ctypes.c_void_p
             I = ctypes.c_int
             lib.oracle_address.argtypes = [P, P, I, I, I, I, I, I, P, P]
+            lib.oracle_address_backward.argtypes = [P, P, P, ctypes.c_long, I, I, P, P]
             lib.oracle_sdm_scan.argtypes = [P, P, P, P, P, P, I, P, P, I, I, I, I, I, I, I, P, P]
             lib.oracle_sdm_scan_backward.argtypes = [P, P, P, P, P, P, P, I, P, P, I, I, I, I, I, I, I, P, P, P, P, P,
                                                      P, P]
@@ -60,7 +61,7 @@ def _load():
             lib.oracle_gdn2_scan.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, P]
             lib.oracle_sse_scan.argtypes = [P, P, I, P, P, P, P, I, I, I, I, I, I, P, P, I]
             lib.oracle_widen_bf16.argtypes = [P, P, ctypes.c_long]
-            for f in (lib.oracle_address, lib.oracle_sdm_scan, lib.oracle_sdm_scan_backward, lib.oracle_gdn_scan,
+            for f in (lib.oracle_address, lib.oracle_address_backward, lib.oracle_sdm_scan, lib.oracle_sdm_scan_backward, lib.oracle_gdn_scan,
                       lib.oracle_gdn2_scan, lib.oracle_sse_scan):
                 f.restype = I
             _lib = lib
@@ -98,6 +99,22 @@ def address(s1: np.ndarray, s2: np.ndarray, k: int, W: int):
     if rc != 0:
         raise ValueError(f"oracle_address: bad sizes (rc={rc})")
     return idx, w
+
+
+def address_backward(idx, w, dw, sqrtN: int):
+    """Gradient of the addressing weights w.r.t. the score halves: idx int32,
+    w and dw [..., W] -> (ds1, ds2) fp64 [..., sqrtN]."""
+    ix = _c(idx, np.int32)
+    ww, dd = _c(w, np.float64), _c(dw, np.float64)
+    W = ix.shape[-1]
+    rows = ix.size // W
+    lead = ix.shape[:-1]
+    ds1 = np.zeros(lead + (sqrtN,))
+    ds2 = np.zeros(lead + (sqrtN,))
+    rc = _load().oracle_address_backward(_p(ix), _p(ww), _p(dd), rows, sqrtN, W, _p(ds1), _p(ds2))
+    if rc != 0:
+        raise ValueError(f"oracle_address_backward failed (rc={rc})")
+    return ds1, ds2
 
 
 def sdm_scan(state, v, alpha, beta, idx_w, w_w, idx_r, w_r, mode=RESID_SHARED, keep_undo=False):

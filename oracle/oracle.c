@@ -11,6 +11,10 @@
  *   oracle_address   - product-key addressing (Sparse Delta Memory deck,
  *                      "Product keys select addresses without scoring every
  *                      slot", Secs. 2 / 3.1).
+ *   oracle_address_backward - the gradient of the selected weights with
+ *                      respect to the two score halves (softmax over the
+ *                      selected sums; the selection itself is piecewise
+ *                      constant).
  *   oracle_sdm_scan  - selective decay, delta write, read after write (same
  *                      deck, "Selected slots decay and update; other slots
  *                      persist", Eqs. 3-5, and "A v1 inconsistency matters for
@@ -143,6 +147,36 @@ int oracle_address(const float *s1, const float *s2, int B, int T, int H, int sq
         address_one(s1 + r * sqrtN, s2 + r * sqrtN, sqrtN, k, W, idx_out + r * W, w_out + r * W, work, ta,
                     tb);
     free(work); free(ta); free(tb);
+    return 0;
+}
+
+/*
+ * Backward of the addressing weights (SDM deck, Secs. 2 / 3.1): with
+ * w = softmax(s) over the W selected sums s_i = s1[a_i] + s2[b_i],
+ * i = a_i sqrtN + b_i, the loss gradient dw gives
+ *   ds_i = w_i (dw_i - sum_j w_j dw_j),   ds1[a_i] += ds_i,   ds2[b_i] += ds_i,
+ * and zero for every score outside the selection.
+ *
+ * idx, w, dw : [rows][W] (int32, fp64, fp64).  ds1, ds2 : fp64 [rows][sqrtN] out.
+ */
+int oracle_address_backward(const int32_t *idx, const double *w, const double *dw, long rows, int sqrtN, int W,
+                            double *ds1, double *ds2)
+{
+    if (rows < 0 || sqrtN < 1 || W < 1) return -1;
+    for (long r = 0; r < rows; ++r) {
+        const int32_t *ix = idx + r * W;
+        const double *wr = w + r * W, *dwr = dw + r * W;
+        double *d1 = ds1 + r * sqrtN, *d2 = ds2 + r * sqrtN;
+        for (int a = 0; a < sqrtN; ++a) d1[a] = d2[a] = 0.0;
+        double dot = 0.0;
+        for (int j = 0; j < W; ++j) dot += wr[j] * dwr[j];
+        for (int j = 0; j < W; ++j) {
+            if (ix[j] < 0 || ix[j] >= sqrtN * sqrtN) return -2;
+            double ds = wr[j] * (dwr[j] - dot);
+            d1[ix[j] / sqrtN] += ds;
+            d2[ix[j] % sqrtN] += ds;
+        }
+    }
     return 0;
 }
 

@@ -72,3 +72,18 @@ def test_backward_matches_the_oracle_and_restores_the_table(shape, mode):
     assert_y_close(host(db), dbr, what="dL/dbeta")
     assert_y_close(host(dww), dwwr, what="dL/dw_w")
     assert_y_close(host(dwr), dwrr, what="dL/dw_r")
+
+
+def test_address_backward_matches_the_oracle():
+    """The 1.4B layer's halves (sqrtN = 240, k = 16, W = 16) on a reduced
+    batch: the score gradients equal the oracle's (fp32 vs fp64)."""
+    sdm = need_gpu()
+    sh = synth.SDM_14B_LAYER.with_(B=2, T=64)
+    inp = synth.sdm_inputs(sh, seed=70)
+    idx, w = oracle.address(inp["s1w"], inp["s2w"], sh.k, sh.W)
+    dw = synth.random_state(idx.shape, seed=71)
+    ds1, ds2 = sdm.sdm_address_backward(dev(idx), dev(w.astype(np.float32)), dev(dw), sh.sqrtN)
+    r1, r2 = oracle.address_backward(idx, w.astype(np.float32), dw, sh.sqrtN)
+    assert_y_close(host(ds1), r1, what="ds1")
+    assert_y_close(host(ds2), r2, what="ds2")
+    assert np.all(host(ds1)[r1 == 0] == 0) and np.all(host(ds2)[r2 == 0] == 0)

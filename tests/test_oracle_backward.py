@@ -82,3 +82,49 @@ def test_unwritten_rows_pass_their_gradient_through():
                                           c["w_r"], oracle.RESID_SHARED, undo, c["dy"])
     np.testing.assert_array_equal(dM0[:, :, 9], c["dMT"][:, :, 9])
     assert np.max(np.abs(dM0[:, :, :9] - c["dMT"][:, :, :9])) > 1e-3   # the touched rows do change
+
+
+def test_address_backward_matches_finite_differences():
+    """Scores drawn so that no k-th or W-th value is within 1e-3 of the next:
+    small perturbations keep the selection, and d(sum dw * w) / d(scores)
+    is the softmax backward scattered to the two halves."""
+    rng = np.random.default_rng(77)
+    sq, k, W = 8, 4, 6
+    s1 = (rng.permutation(sq) * 0.37 + rng.uniform(0, 0.01, sq)).astype(np.float32).reshape(1, 1, 1, sq)
+    s2 = (rng.permutation(sq) * 0.53 + rng.uniform(0, 0.01, sq)).astype(np.float32).reshape(1, 1, 1, sq)
+    dw = rng.standard_normal((1, 1, 1, W))
+    idx, w = oracle.address(s1, s2, k, W)
+    ds1, ds2 = oracle.address_backward(idx, w, dw, sq)
+    eps = 1e-3                                   # fp32 scores: a coarse but exact-enough step
+    for which, base in (("s1", s1), ("s2", s2)):
+        for a in range(sq):
+            up, dn = base.copy(), base.copy()
+            up[..., a] += eps
+            dn[..., a] -= eps
+            args_up = (up, s2) if which == "s1" else (s1, up)
+            args_dn = (dn, s2) if which == "s1" else (s1, dn)
+            iu, wu = oracle.address(*args_up, k, W)
+            idn, wd = oracle.address(*args_dn, k, W)
+            assert (iu == idx).all() and (idn == idx).all()
+            fd = ((wu - wd) * dw).sum() / (float(up[..., a].item()) - float(dn[..., a].item()))
+            got = (ds1 if which == "s1" else ds2)[0, 0, 0, a]
+            np.testing.assert_allclose(got, fd, rtol=1e-4, atol=1e-6)
+
+
+def test_address_backward_is_zero_outside_the_selection():
+    rng = np.random.default_rng(78)
+    shape = (2, 3, 2, 16)
+    s1 = rng.standard_normal(shape).astype(np.float32)
+    s2 = rng.standard_normal(shape).astype(np.float32)
+    idx, w = oracle.address(s1, s2, 4, 5)
+    ds1, ds2 = oracle.address_backward(idx, w, rng.standard_normal(idx.shape), 16)
+    sel_a = np.zeros(shape, bool)
+    sel_b = np.zeros(shape, bool)
+    for ix in np.ndindex(idx.shape[:-1]):
+        sel_a[ix][idx[ix] // 16] = True
+        sel_b[ix][idx[ix] % 16] = True
+    assert np.all(ds1[~sel_a] == 0) and np.all(ds2[~sel_b] == 0)
+    # softmax weights sum to one: a constant shift of all dw changes nothing
+    d1b, d2b = oracle.address_backward(idx, w, rng.standard_normal(idx.shape) * 0 + 3.0, 16)
+    np.testing.assert_allclose(d1b, 0.0, atol=1e-12)
+    np.testing.assert_allclose(d2b, 0.0, atol=1e-12)
