@@ -10,7 +10,7 @@ step does identical work).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload sdm_14b_layer|sdm_sweep_H2|H4|H8|gdn|kda|gdn2|sse|sse_delta|sdm_tiny|sdm_decode|sse_decode|
-                               sdm_train]
+                               sdm_train|sdm_chunked]
 
 Prints one JSON line (rank 0).  Under torchrun each rank runs its own batch
 (independent sequences, no collective in the data path) and the time is the
@@ -217,7 +217,9 @@ class Workload:
             name = {"sdm_decode": "sdm_14b_layer", "sse_decode": "sse"}[name]
         # train: forward with the undo log, the scan backward and the address backward
         self.train = name == "sdm_train"
-        if self.train:
+        # chunked: the same scan in chunked form (sdm_scan_chunked)
+        self.chunked = name == "sdm_chunked"
+        if self.train or self.chunked:
             name = "sdm_14b_layer"
         if name == "sdm_14b_layer":
             self.kind, self.shape = "sdm", synth.SDM_14B_LAYER
@@ -238,6 +240,8 @@ class Workload:
             self.shape = self.shape.with_(T=1, name=self.shape.name + "_decode")
         if self.train:
             self.shape = self.shape.with_(name=self.shape.name + "_train")
+        if self.chunked:
+            self.shape = self.shape.with_(name=self.shape.name + "_chunked")
         sh = self.shape
         self.tokens = sh.B * sh.T
 
@@ -330,6 +334,9 @@ class GpuRun:
             self.y = torch.empty((B, T, H, sh.d_v), dtype=torch.float32, device=device)
             self.ws = torch.empty(sdm.sdm_scan_workspace_size(B, T, H, sh.W, sh.R), dtype=torch.uint8, device=device)
             self.launches_per_step = 4
+            if wl.chunked:
+                self.ws_c = torch.empty(sdm.sdm_scan_chunked_workspace_size(B, T, H, sh.W, sh.R), dtype=torch.uint8,
+                                        device=device)
             if wl.train:
                 g = torch.Generator(device=device)
                 g.manual_seed(12345)
@@ -378,6 +385,9 @@ class GpuRun:
                                                            self.wl.mode, self.ws_b, self.err)
             self.sdm.sdm_address_backward(self.iw, self.ww, dww, sh.sqrtN, self.err)
             self.sdm.sdm_address_backward(self.ir, self.wr, dwr, sh.sqrtN, self.err)
+        elif self.wl.kind == "sdm" and self.wl.chunked:
+            self.sdm.sdm_scan_chunked(self.state, d["v"], d["alpha"], d["beta"], self.iw, self.ww, self.ir, self.wr,
+                                      self.wl.mode, self.y, self.ws_c, self.err)
         elif self.wl.kind == "sdm":
             self.sdm.sdm_scan(self.state, d["v"], d["alpha"], d["beta"], self.iw, self.ww, self.ir, self.wr,
                               self.wl.mode, self.y, self.ws, self.err)
@@ -401,7 +411,7 @@ class GpuRun:
         copied in and y copied out per chunk, overlapped with compute); for the
         dense and SSE scans and the training step, copies of the step's inputs
         and y around the call."""
-        if self.wl.kind == "sdm" and not self.wl.train:
+        if self.wl.kind == "sdm" and not self.wl.train and not self.wl.chunked:
             import torch
             sh, hst = self.wl.shape, self.host
             if not hasattr(self, "fh_ws"):
@@ -567,6 +577,7 @@ def run_ours(args, rank, world, local_rank, sampler):
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": algo_unit,
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": "sdm_scan_train + sdm_scan_backward + 2 sdm_address_backward" if wl.train else
+                     "sdm_scan_chunked (chunk preparation + chain kernels)" if wl.chunked else
                      {"sdm": "sdm_scan (hazard prepass + sparse_scan_kernel)",
                       "gdn": "gdn_scan (chunk preparation + chain kernels)", "kda": "gdn_scan", "gdn2": "gdn2_scan",
                       "sse": "sse_scan (route prepass + sse_scan_kernel)"}[wl.kind],
@@ -575,7 +586,8 @@ def run_ours(args, rank, world, local_rank, sampler):
         "cpu_baseline": cpu,
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "path": "sdm_forward_host (chunked copy/compute pipeline)" if wl.kind == "sdm" and not wl.train
+                "path": "sdm_forward_host (chunked copy/compute pipeline)"
+                if wl.kind == "sdm" and not wl.train and not wl.chunked
                 else "pinned H2D copies + scan call + D2H of y"},
         "gpu_launches": K * run.launches_per_step,
         "clocks": clk,

@@ -21,7 +21,8 @@ import torch
 __all__ = [
     "SdmError", "lib", "library_path", "sdm_version", "sdm_address", "sdm_scan", "sdm_scan_workspace_size",
     "sdm_scan_noalloc", "sdm_forward_host", "sdm_forward_host_workspace_size", "sdm_scan_train",
-    "sdm_scan_backward", "sdm_scan_backward_workspace_size", "sdm_address_backward",
+    "sdm_scan_backward", "sdm_scan_backward_workspace_size", "sdm_address_backward", "sdm_scan_chunked",
+    "sdm_scan_chunked_workspace_size",
     "gdn_scan", "gdn_scan_workspace_size", "gdn2_scan", "sse_scan", "sse_scan_workspace_size", "SDM_RESID_SHARED", "SDM_RESID_PERSLOT", "SSE_WRITE_ADDITIVE", "SSE_WRITE_DELTA",
     "SDM_RESID_ADDITIVE", "SDM_DEVERR_INDEX_RANGE", "SDM_DEVERR_INDEX_REPEAT", "SDM_DEVERR_NONFINITE",
 ]
@@ -49,6 +50,9 @@ _SIGNATURES = {
                             _P]),
     "sdm_scan_backward_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "sdm_address_backward": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
+    "sdm_scan_chunked_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "sdm_scan_chunked": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P,
+                              _P]),
     "sdm_scan_backward": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P,
                                _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "sdm_forward_host_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I, _I, _I]),
@@ -168,6 +172,34 @@ def _scan_shapes(state, v, alpha, beta, idx_w, w_w, idx_r, w_r):
     _req(idx_r, "idx_r", torch.int32, (B, T, H, R))
     _req(w_r, "w_r", torch.float32, (B, T, H, R))
     return B, T, H, N, dv, W, R
+
+
+def sdm_scan_chunked(state, v, alpha, beta, idx_w, w_w, idx_r, w_r, resid_mode=SDM_RESID_SHARED, y=None,
+                     workspace=None, dev_err=None, stream=None):
+    """The sparse scan in chunked form (64-token chunks, the work inside a
+    chunk in parallel); same arguments and result as sdm_scan, shared or
+    additive write, W, R <= 16."""
+    B, T, H, N, dv, W, R = _scan_shapes(state, v, alpha, beta, idx_w, w_w, idx_r, w_r)
+    if y is None:
+        y = torch.empty((B, T, H, dv), dtype=torch.float32, device=state.device)
+    _req(y, "y", torch.float32, (B, T, H, dv))
+    need = int(lib().sdm_scan_chunked_workspace_size(B, T, H, W, R))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=state.device)
+    _req(workspace, "workspace", torch.uint8)
+    if dev_err is not None:
+        _req(dev_err, "dev_err", torch.int32)
+    vdt = SDM_DTYPE_BF16 if v.dtype == torch.bfloat16 else SDM_DTYPE_F32
+    rc = lib().sdm_scan_chunked(state.data_ptr(), v.data_ptr(), vdt, alpha.data_ptr(), beta.data_ptr(),
+                                idx_w.data_ptr(), w_w.data_ptr(), W, idx_r.data_ptr(), w_r.data_ptr(), R, B, T, H, N,
+                                dv, int(resid_mode), y.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                                _ptr(dev_err), _stream(stream))
+    _check("sdm_scan_chunked", rc)
+    return y
+
+
+def sdm_scan_chunked_workspace_size(B: int, T: int, H: int, W: int, R: int) -> int:
+    return int(lib().sdm_scan_chunked_workspace_size(B, T, H, W, R))
 
 
 def sdm_scan_train(state, v, alpha, beta, idx_w, w_w, idx_r, w_r, resid_mode=SDM_RESID_SHARED, y=None, undo=None,

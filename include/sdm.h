@@ -212,6 +212,35 @@ SDM_API int sdm_scan_noalloc(float *state, const void *v, int v_dtype, const flo
                      void *stream);
 
 /*
+ * Scratch bytes sdm_scan_chunked needs: one 60 KB record per chunk of 64
+ * tokens and (batch, head).
+ */
+SDM_API size_t sdm_scan_chunked_workspace_size(int B, int T, int H, int W, int R);
+
+/*
+ * sdm_scan_chunked - the same scan as sdm_scan (shared residual or additive
+ * write) in chunked form ([SDM] "Training parallelizes within chunks and
+ * recurs across chunks", "Backup: sparse interactions drive the triangular
+ * solve", App. A.1-A.2, Eq. 7).  Within a chunk of C = 64 tokens, with
+ * lambda_i(s) the sum of log alpha over the tokens j <= i that write slot s:
+ *   (I + A diag(beta)) u = v - p,   p_i = sum_n k_in e^{lambda_i(s_in)} M0[s_in],
+ *   A[i,j] = sum_{s_in = s_jm} k_in k_jm e^{lambda_i(s) - lambda_j(s)} (j < i);
+ *   y_i and the end-of-chunk rows follow from u (see chunked_scan.cu).
+ * All the gathers of a chunk are independent, so the work inside a chunk is
+ * parallel; chunks run in order.  Results equal sdm_scan's up to fp32
+ * rounding.
+ *
+ * Arguments as sdm_scan; resid_mode SDM_RESID_SHARED or SDM_RESID_ADDITIVE
+ * (SDM_RESID_PERSLOT: SDM_ERR_UNSUPPORTED); W, R <= 16; N <= 2^25.
+ * workspace : sdm_scan_chunked_workspace_size() bytes, 16-byte aligned.
+ * dev_err   : optional; SDM_DEVERR_INDEX_RANGE / SDM_DEVERR_INDEX_REPEAT.
+ */
+SDM_API int sdm_scan_chunked(float *state, const void *v, int v_dtype, const float *alpha, const float *beta,
+                             const int32_t *idx_w, const float *w_w, int W, const int32_t *idx_r, const float *w_r,
+                             int R, int B, int T, int H, int N, int d_v, int resid_mode, float *y, void *workspace,
+                             size_t workspace_bytes, int32_t *dev_err, void *stream);
+
+/*
  * sdm_address_backward - gradient of the addressing weights with respect to
  * the two score halves ([SDM] Secs. 2 / 3.1).  The selection is piecewise
  * constant; the weights are w = softmax of the W selected sums
