@@ -355,17 +355,20 @@ __global__ void __launch_bounds__(kChainThreadsC) chunk_chain_kernel(const Chunk
         const long tok = tok0 + static_cast<long>(t0 + i) * H;
         const float vv = a.v_bf16 ? bf16_to_f32(static_cast<const uint16_t *>(a.v)[tok * d_v + ccol])
                                   : static_cast<const float *>(a.v)[tok * d_v + ccol];
+        // the token's 16 write rows and 16 read rows, all loads in flight at once
+        float gw[kCS], gr[kCS];
+#pragma unroll
+        for (int n = 0; n < kCS; ++n) {
+          const int sw = (!a.additive && n < W) ? sWs[i * kCS + n] : -1;
+          const int sr_ = n < R ? sRs[i * kCS + n] : -1;
+          gw[n] = sw >= 0 ? M[static_cast<long>(sw) * d_v] : 0.f;
+          gr[n] = sr_ >= 0 ? M[static_cast<long>(sr_) * d_v] : 0.f;
+        }
         float p = 0.f;
-        if (!a.additive)
-#pragma unroll 4
-          for (int n = 0; n < W; ++n) {
-            const int s = sWs[i * kCS + n];
-            if (s >= 0) p = fmaf(sWcp[i * kCS + n], M[static_cast<long>(s) * d_v], p);
-          }
-#pragma unroll 4
-        for (int m = 0; m < R; ++m) {
-          const int s = sRs[i * kCS + m];
-          if (s >= 0) yy = fmaf(sRc[i * kCS + m], M[static_cast<long>(s) * d_v], yy);
+#pragma unroll
+        for (int n = 0; n < kCS; ++n) {
+          p = fmaf(sWcp[i * kCS + n], gw[n], p);   // unused pairs have coefficient 0
+          yy = fmaf(sRc[i * kCS + n], gr[n], yy);
         }
         r = vv - p;
       }
@@ -392,17 +395,26 @@ __global__ void __launch_bounds__(kChainThreadsC) chunk_chain_kernel(const Chunk
         if (active) a.y[(tok0 + static_cast<long>(t0 + i) * H) * d_v + col] = yy;
       }
     }
-    // one scatter per distinct written slot, by the thread holding its run's last pair
-    for (int p = warp * (kCP / 8); p < (warp + 1) * (kCP / 8); ++p) {
-      const int32_t ln = sWln[p];
-      if (!(ln & kLast)) continue;
-      const long o = static_cast<long>(sWs[p]) * d_v;
-      float val = sWdc[p] * M[o];
-      for (int q = p; q >= 0;) {
-        val = fmaf(sWsc[q], su[(q >> 4) * kRS + lane], val);
-        q = (sWln[q] & 0xffff) - 1;
+    // one scatter per distinct written slot, by the warp holding its run's last
+    // pair; 32 pairs at a time: their old rows are loaded together, then updated
+    for (int base = warp * (kCP / 8); base < (warp + 1) * (kCP / 8); base += 32) {
+      float old[32];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const int p = base + k;
+        old[k] = (sWln[p] & kLast) ? M[static_cast<long>(sWs[p]) * d_v] : 0.f;
       }
-      if (active) M[o] = val;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const int p = base + k;
+        if (!(sWln[p] & kLast)) continue;
+        float val = sWdc[p] * old[k];
+        for (int q = p; q >= 0;) {
+          val = fmaf(sWsc[q], su[(q >> 4) * kRS + lane], val);
+          q = (sWln[q] & 0xffff) - 1;
+        }
+        if (active) M[static_cast<long>(sWs[p]) * d_v] = val;
+      }
     }
     __syncthreads();
   }
