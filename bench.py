@@ -236,6 +236,7 @@ class Workload:
         else:
             raise SystemExit(f"unknown workload {name}")
         self.sse_mode = 1 if name == "sse_delta" else 0  # sse_scan write mode: additive / delta
+        self.sse_chunked = False  # set once the workspace query tells which path sse_scan takes
         if batch:
             self.shape = self.shape.with_(B=batch)
         if self.decode:
@@ -268,7 +269,8 @@ class Workload:
                     "dk": sh.dk, "dv": sh.dv, "qkv_dtype": "bf16", "state": "fp32, continued across steps",
                     "l2": "inputs (q,k,v,alpha,y ~340-470 MB) larger than L2; no flush"}
         return {"workload": sh.name, "B": sh.B, "T": sh.T, "H": sh.H, "N": sh.N, "topk": sh.topk, "c": sh.c, "d": sh.d,
-                "write": ["additive", "delta"][self.sse_mode], "qv_dtype": "bf16", "state": "fp32 shared-memory resident per CTA, continued across steps",
+                "write": ["additive", "delta"][self.sse_mode], "qv_dtype": "bf16",
+                "state": "fp32, continued across steps",
                 "l2": "inputs (~1.1 GB) larger than L2; no flush"}
 
     def oracle_jobs(self, inp: dict, t_sample: int, nseq: int):
@@ -363,9 +365,12 @@ class GpuRun:
         else:
             self.state = torch.zeros((sh.B, sh.H, sh.N + 1, sh.c, sh.d), dtype=torch.float32, device=device)
             self.y = torch.empty((sh.B, sh.T, sh.H, sh.d), dtype=torch.float32, device=device)
-            self.ws = torch.empty(sdm.sse_scan_workspace_size(sh.B, sh.T, sh.H, sh.N, sh.topk), dtype=torch.uint8,
-                                  device=device)
-            self.launches_per_step = 2
+            nws = sdm.sse_scan_workspace_size(sh.B, sh.T, sh.H, sh.N, sh.topk, sh.c, sh.d, wl.sse_mode)
+            self.ws = torch.empty(nws, dtype=torch.uint8, device=device)
+            # chunked prefill: route, group, chunk preparation, chain, combine; else route + scan kernel
+            rec = (sh.B * sh.T * sh.H * ((2 * sh.topk + 5) & ~3) * 4 + 255) // 256 * 256
+            wl.sse_chunked = nws > rec
+            self.launches_per_step = 5 if wl.sse_chunked else 2
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
         self.y_host = torch.empty(self.y.shape, dtype=torch.float32).pin_memory()
 
@@ -473,6 +478,12 @@ class GpuRun:
             state = 2 * sh.B * sh.H * sh.dk * sh.dv * 4
             return tokh * per + state, "GB/s", "hbm", {"bytes_per_token_head": per}
         tokh = sh.B * sh.T * sh.H
+        if self.wl.sse_chunked:
+            # chunked prefill: bound by its I/O (router and key logits, q, v, alpha in; y out; every
+            # partition's state read and written once); its MMAs (~3e5 flop per token-head) take less
+            per = 4 * sh.N + 4 * sh.c + 2 * sh.c + 2 * sh.d + 4 * sh.c + 4 * sh.d
+            state = 2 * sh.B * sh.H * (sh.N + 1) * sh.c * sh.d * 4
+            return tokh * per + state, "GB/s", "hbm", {"bytes_per_token_head": per}
         # decay mul, write fma, read fma (1 + 2 + 2); the delta write adds the prediction fma (2)
         flops = tokh * (sh.topk + 1) * sh.c * sh.d * (7.0 if self.wl.sse_mode else 5.0)
         return flops, "TFLOP/s", "alu", {"flops_per_token_head": flops / tokh}
@@ -558,7 +569,7 @@ def run_ours(args, rank, world, local_rank, sampler):
         peak = 152 * 128 * 2 * float(pk.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
         achieved = algo / (main_ms * 1e-3) / 1e12
     kernel_file = {"sdm": "sparse_scan.cu", "gdn": "gdn_chunk.cu", "kda": "gdn_scan.cu", "gdn2": "gdn_scan.cu",
-                   "sse": "sse_scan.cu"}[wl.kind]
+                   "sse": "sse_chunk.cu" if wl.sse_chunked else "sse_scan.cu"}[wl.kind]
     tr = NCU_TRAFFIC.get((wl.name, wl.kind))
     traffic = tr["bytes"] if tr and tr["digest"] == _src_digest(kernel_file) else None
     tokens = wl.tokens * world
@@ -582,7 +593,8 @@ def run_ours(args, rank, world, local_rank, sampler):
                      "sdm_scan_chunked (chunk preparation + chain kernels)" if wl.chunked else
                      {"sdm": "sdm_scan (hazard prepass + sparse_scan_kernel)",
                       "gdn": "gdn_scan (chunk preparation + chain kernels)", "kda": "gdn_scan", "gdn2": "gdn2_scan",
-                      "sse": "sse_scan (route prepass + sse_scan_kernel)"}[wl.kind],
+                      "sse": "sse_scan (route, group, chunk preparation, chain, combine kernels)"
+                      if wl.sse_chunked else "sse_scan (route prepass + sse_scan_kernel)"}[wl.kind],
                      "launch_ms": main_ms, "peak_source": f"{src} ({'hbm_gbs' if bound == 'hbm' else 'FP32 lanes x clock'})",
                      **algo_info},
         "cpu_baseline": cpu,

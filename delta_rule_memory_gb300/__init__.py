@@ -61,7 +61,7 @@ _SIGNATURES = {
     "gdn_scan_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "gdn_scan": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _SZ, _P, _P]),
     "gdn2_scan": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
-    "sse_scan_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "sse_scan_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I, _I]),
     "sse_scan": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _SZ, _P, _P]),
 }
 
@@ -473,8 +473,9 @@ def gdn2_scan(state, q, k, v, alpha, b_erase, w_write, y=None, dev_err=None, str
     return y
 
 
-def sse_scan_workspace_size(B: int, T: int, H: int, N: int, topk: int) -> int:
-    return int(lib().sse_scan_workspace_size(B, T, H, N, topk))
+def sse_scan_workspace_size(B: int, T: int, H: int, N: int, topk: int, c: int = 128, d: int = 128,
+                            write_mode: int = 0) -> int:
+    return int(lib().sse_scan_workspace_size(B, T, H, N, topk, c, d, write_mode))
 
 
 def sse_scan(state, route_logits, topk: int, k_logits, q, v, alpha, y=None, sel_out=None, workspace=None,
@@ -502,7 +503,7 @@ def sse_scan(state, route_logits, topk: int, k_logits, q, v, alpha, y=None, sel_
     if dev_err is not None:
         _req(dev_err, "dev_err", torch.int32)
     if workspace is None:
-        workspace = torch.empty(max(sse_scan_workspace_size(B, T, H, N, topk), 1), dtype=torch.uint8,
+        workspace = torch.empty(max(sse_scan_workspace_size(B, T, H, N, topk, c, d, write_mode), 1), dtype=torch.uint8,
                                 device=state.device)
     _req(workspace, "workspace", torch.uint8)
     rc = lib().sse_scan(state.data_ptr(), route_logits.data_ptr(), int(topk), k_logits.data_ptr(), q.data_ptr(),

@@ -58,22 +58,6 @@ __device__ __forceinline__ uint32_t tmem_addr(uint32_t base, int lane_base, uint
   return base + (static_cast<uint32_t>(lane_base) << 16) + col;
 }
 
-// 8 consecutive fp32 -> one 16-byte chunk of bf16 hi and one of bf16 lo
-// (hi = bf16(x), lo = bf16(x - hi), converted two at a time)
-__device__ __forceinline__ void store_split8(unsigned char *hi, unsigned char *lo, uint32_t off, const float *x) {
-  uint32_t h[4], l[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const __nv_bfloat162 hb = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
-    const float2 hf = __bfloat1622float2(hb);
-    const __nv_bfloat162 lb = __floats2bfloat162_rn(x[2 * e] - hf.x, x[2 * e + 1] - hf.y);
-    h[e] = *reinterpret_cast<const uint32_t *>(&hb);
-    l[e] = *reinterpret_cast<const uint32_t *>(&lb);
-  }
-  *reinterpret_cast<uint4 *>(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
-  *reinterpret_cast<uint4 *>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
-}
-
 // ===========================================================================
 // Kernel 1: the state-independent part of every chunk.
 //
@@ -441,26 +425,7 @@ constexpr uint32_t kChainSmem = kCBar + kNBar * 8 + 16;
 
 // bounded wait that also gives up as soon as another thread has
 __device__ __forceinline__ bool chain_wait(uint32_t mbar, uint32_t parity, volatile int *abort_flag) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}\n"
-        : "=r"(done)
-        : "r"(mbar), "r"(parity)
-        : "memory");
-    if (done) {
-      tc_fence_after();
-      return true;
-    }
-    if (i > 64) {
-      if (*abort_flag) return false;
-      __nanosleep(64);
-    }
-  }
-  *abort_flag = 1;
-  return false;
+  return mbar_wait_abortable(mbar, parity, kWaitLimit, abort_flag);
 }
 
 __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {

@@ -19,6 +19,8 @@
 // v - vhat_p, vhat_p = sum_j kk_j alpha_j S^p[j,:] (the Sparse Delta Memory
 // deck's shared residual, Fig. 2, with row weights kk and strength g).
 #include <climits>
+#include <cstdlib>
+#include <cstring>
 
 #include "common.cuh"
 
@@ -326,10 +328,36 @@ size_t sse_smem_bytes(int N, int c, int topk, int mode) {
 
 using namespace sdm;
 
-extern "C" size_t sse_scan_workspace_size(int B, int T, int H, int N, int topk) {
-  if (B <= 0 || T <= 0 || H <= 0 || N <= 0 || topk <= 0) return 0;
+namespace sdm {
+size_t sse_chunk_workspace_size(int B, int T, int H, int N, int topk);
+bool sse_chunk_supported(int write_mode, int N, int topk, int c, int d);
+int launch_sse_chunk(float *state, const uint32_t *rec, int rw, const float *klog, const uint16_t *q,
+                     const uint16_t *v, const float *alpha, int B, int T, int H, int N, int topk, float *y,
+                     unsigned char *chunk_ws, int32_t *err, cudaStream_t st);
+}  // namespace sdm
+
+// The additive write with c = d = 128 runs as a chunked prefill by partition
+// (sse_chunk.cu) once T reaches one chunk; other shapes, the delta write and
+// short sequences run token by token.  SDM_SSE_PATH=recurrent forces the
+// token-by-token kernel, SDM_SSE_PATH=chunk the chunked path for any T.
+static bool use_sse_chunk(int write_mode, int T, int N, int topk, int c, int d) {
+  if (!sse_chunk_supported(write_mode, N, topk, c, d)) return false;
+  const char *path = getenv("SDM_SSE_PATH");
+  if (path && strcmp(path, "recurrent") == 0) return false;
+  if (path && strcmp(path, "chunk") == 0) return true;
+  return T >= 64;
+}
+
+static size_t rec_bytes(int B, int T, int H, int topk) {
   const size_t n = static_cast<size_t>(B) * T * H * rec_words(topk) * sizeof(uint32_t);
   return (n + 255) & ~static_cast<size_t>(255);
+}
+
+extern "C" size_t sse_scan_workspace_size(int B, int T, int H, int N, int topk, int c, int d, int write_mode) {
+  if (B <= 0 || T <= 0 || H <= 0 || N <= 0 || topk <= 0) return 0;
+  size_t n = rec_bytes(B, T, H, topk);
+  if (use_sse_chunk(write_mode, T, N, topk, c, d)) n += sse_chunk_workspace_size(B, T, H, N, topk);
+  return n;
 }
 
 extern "C" int sse_scan(float *state, const float *route_logits, int topk, const float *k_logits, const uint16_t *q,
@@ -351,15 +379,22 @@ extern "C" int sse_scan(float *state, const float *route_logits, int topk, const
       (dev_err && !aligned(dev_err, 4)))
     return set_error(SDM_ERR_ALIGN, "sse_scan: state, k_logits, alpha, q, v need 16-byte alignment");
   if (B == 0 || T == 0 || H == 0) return SDM_OK;
-  const size_t need = sse_scan_workspace_size(B, T, H, N, topk);
+  if (static_cast<long>(B) * T * H * (topk + 1) >= INT_MAX || T >= (1 << 27))
+    return set_error(SDM_ERR_SHAPE, "sse_scan: B*T*H*(topk+1) must stay below 2^31 and T below 2^27");
+  const size_t need = sse_scan_workspace_size(B, T, H, N, topk, c, d, write_mode);
   if (!workspace || workspace_bytes < need)
     return set_error(SDM_ERR_INVALID_ARG, "sse_scan: workspace of %zu bytes needed", need);
   if (!aligned(workspace, 16)) return set_error(SDM_ERR_ALIGN, "sse_scan: workspace must be 16-byte aligned");
+  const bool chunk = use_sse_chunk(write_mode, T, N, topk, c, d);
   const size_t smem = sse_smem_bytes(N, c, topk, write_mode);
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&smem_blk, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  if (smem > static_cast<size_t>(smem_blk))
-    return set_error(SDM_ERR_SHAPE, "sse_scan: (N+1)*c too large for the shared-memory resident state");
+  if (chunk) {
+    if (!aligned(y, 16)) return set_error(SDM_ERR_ALIGN, "sse_scan: y must be 16-byte aligned");
+  } else {
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&smem_blk, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (smem > static_cast<size_t>(smem_blk))
+      return set_error(SDM_ERR_SHAPE, "sse_scan: (N+1)*c too large for the shared-memory resident state");
+  }
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const long tokens = static_cast<long>(B) * T * H;
@@ -368,6 +403,10 @@ extern "C" int sse_scan(float *state, const float *route_logits, int topk, const
                                                                            c, rec, sel_out, dev_err);
   int rc = check_launch("sse_scan: route kernel");
   if (rc != SDM_OK) return rc;
+
+  if (chunk)
+    return launch_sse_chunk(state, rec, rec_words(topk), k_logits, q, v, alpha, B, T, H, N, topk, y,
+                            static_cast<unsigned char *>(workspace) + rec_bytes(B, T, H, topk), dev_err, st);
 
   SseArgs args;
   args.state = state;

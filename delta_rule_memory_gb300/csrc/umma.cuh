@@ -173,6 +173,48 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 // proxy (the tensor core reads operands through it)
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
 
+// Wait as mbar_wait does, but also give up as soon as another thread of the
+// CTA has (abort_flag set); a wait that runs out sets the flag itself.
+__device__ __forceinline__ bool mbar_wait_abortable(uint32_t mbar, uint32_t parity, uint32_t limit,
+                                                    volatile int *abort_flag) {
+  for (uint32_t i = 0; i < limit; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(done)
+        : "r"(mbar), "r"(parity)
+        : "memory");
+    if (done) {
+      asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+      return true;
+    }
+    if (i > 64) {
+      if (*abort_flag) return false;
+      __nanosleep(64);
+    }
+  }
+  *abort_flag = 1;
+  return false;
+}
+
+// 8 consecutive fp32 -> one 16-byte chunk of bf16 hi and one of bf16 lo
+// (hi = bf16(x), lo = bf16(x - hi), converted two at a time)
+__device__ __forceinline__ void store_split8(unsigned char *hi, unsigned char *lo, uint32_t off, const float *x) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const __nv_bfloat162 hb = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+    const float2 hf = __bfloat1622float2(hb);
+    const __nv_bfloat162 lb = __floats2bfloat162_rn(x[2 * e] - hf.x, x[2 * e + 1] - hf.y);
+    h[e] = *reinterpret_cast<const uint32_t *>(&hb);
+    l[e] = *reinterpret_cast<const uint32_t *>(&lb);
+  }
+  *reinterpret_cast<uint4 *>(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
+  *reinterpret_cast<uint4 *>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
 // split x into bf16 hi + bf16 lo with hi + lo = x to ~2^-16 relative
 __device__ __forceinline__ void split_bf16(float x, uint16_t &hi, uint16_t &lo) {
   const __nv_bfloat16 h = __float2bfloat16_rn(x);

@@ -379,11 +379,16 @@ SDM_API int gdn2_scan(float *state, const uint16_t *q, const uint16_t *k, const 
                       int32_t *dev_err, void *stream);
 
 /*
- * Scratch bytes sse_scan needs: one routing record per token (selected
- * partitions, their gates, and the max and inverse normaliser of the row
- * softmax), rounded up to 256 bytes.
+ * Scratch bytes sse_scan needs for these sizes and write mode: one routing
+ * record per token (selected partitions, their gates, and the max and
+ * inverse normaliser of the row softmax), rounded up to 256 bytes; when the
+ * call takes the chunked prefill path (below) also, per (batch, head), the
+ * visit lists grouped by partition, one operand unit of 99,072 bytes per
+ * chunk of 64 visits (at most ceil(T/64) + floor((topk*T + 63*N)/64) units),
+ * and one staging row of d fp32 per visit.  Read SDM_SSE_PATH at the call,
+ * so query it under the same environment as sse_scan.
  */
-SDM_API size_t sse_scan_workspace_size(int B, int T, int H, int N, int topk);
+SDM_API size_t sse_scan_workspace_size(int B, int T, int H, int N, int topk, int c, int d, int write_mode);
 
 /*
  * sse_scan - Sparse State Expansion, [SSE] Eqs. 9-14, with N routed
@@ -401,6 +406,16 @@ SDM_API size_t sse_scan_workspace_size(int B, int T, int H, int N, int topk);
  *   unvisited partitions keep their bits (their decay clock stops)
  *   y_t  = sum_p g_p sum_j q_t[j] S^p[j,:]                 (after the write)
  *
+ * Paths.  The additive write with c = d = 128 and T >= 64 runs as a prefill
+ * by varlen grouping ([SSE] "Varlen groups tokens while preserving causal
+ * order"): the visits of each partition gathered in time order, each group
+ * run in chunks of 64 visits on the tensor cores (chunkwise GLA form), and
+ * every token's visit outputs summed in a fixed order (routed ranks, then the
+ * shared partition), so results are deterministic.  Everything else runs
+ * token by token with the partitions resident in shared memory.  The
+ * environment variable SDM_SSE_PATH=recurrent forces the token-by-token
+ * kernel; SDM_SSE_PATH=chunk the chunked path for any T (same shape rules).
+ *
  * state       : fp32 [B,H,N+1,c,d] in place.
  * route_logits: fp32 [B,T,H,N].  k_logits : fp32 [B,T,H,c].
  * q           : bf16 [B,T,H,c].  v : bf16 [B,T,H,d].  alpha : fp32 [B,T,H,c].
@@ -409,10 +424,13 @@ SDM_API size_t sse_scan_workspace_size(int B, int T, int H, int N, int topk);
  * sel_out     : optional int32 [B,T,H,topk], the selected partitions in rank order.
  * workspace   : device scratch of at least sse_scan_workspace_size() bytes,
  *               16-byte aligned.
- * dev_err     : optional; SDM_DEVERR_NONFINITE if a logit is NaN/inf.
+ * dev_err     : optional; SDM_DEVERR_NONFINITE if a logit is NaN/inf;
+ *               SDM_DEVERR_TIMEOUT if a tensor-core wait of the chunked path
+ *               gave up (its outputs are then invalid).
  * Limits: 1 <= topk <= N <= 64, topk <= 8; c % 16 == 0, 16 <= c <= 128;
- *         d % 16 == 0.  state, y, k_logits, alpha 16-byte aligned; q, v
- *         16-byte aligned.
+ *         d % 16 == 0; B*T*H*(topk+1) < 2^31, T < 2^27.  state, k_logits,
+ *         alpha, q, v 16-byte aligned; y 4-byte aligned (16 on the chunked
+ *         path).  Token by token, (N+1)*c*16 fp32 must fit in shared memory.
  */
 SDM_API int sse_scan(float *state, const float *route_logits, int topk, const float *k_logits, const uint16_t *q,
              const uint16_t *v, const float *alpha, int write_mode, int B, int T, int H, int N, int c, int d,
