@@ -172,6 +172,7 @@ struct PrepArgs {
   unsigned char *units;
   int T, H, N, topk, rw, umax;
   long gwords, total;  // total = B * H * umax
+  int32_t *err;
 };
 
 constexpr int kPThreads = 256;
@@ -183,8 +184,8 @@ constexpr uint32_t kPal = kPq + kC * kCh * 2;        // alpha, then q * (product
 constexpr uint32_t kPkk = kPal + kC * kLdA * 4;      // key logits, then kk, then kk * (product in the block after j)
 constexpr uint32_t kPAf = kPkk + kC * kLdA * 4;      // A fp32 [64][kLdF]
 constexpr uint32_t kPPb = kPAf + kC * kLdF * 4;      // block products, prefix, suffix [3][4][128]
-constexpr uint32_t kPRow = kPPb + 3 * 4 * kCh * 4;   // per visit: token-head, slot, gate, kmax, kinv
-constexpr uint32_t kPInfo = kPRow + 5 * kC * 4;      // the unit: partition, first position, visits, list offset
+constexpr uint32_t kPRow = kPPb + 3 * 4 * kCh * 4;   // per visit: token-head, slot, gate
+constexpr uint32_t kPInfo = kPRow + 3 * kC * 4;      // the unit: partition, first position, visits, list offset
 constexpr uint32_t kPrepSmem = kPInfo + 16;
 static_assert(2 * (kPrepSmem + 1024) <= 228 * 1024, "two preparation CTAs per SM");
 
@@ -197,7 +198,7 @@ __global__ void __launch_bounds__(kPThreads, 2) sse_prep_kernel(const PrepArgs a
   float *sA = reinterpret_cast<float *>(sm + kPAf);
   float *sP = reinterpret_cast<float *>(sm + kPPb), *sPre = sP + 4 * kCh, *sSuf = sP + 8 * kCh;
   int *rtok = reinterpret_cast<int *>(sm + kPRow), *rslot = rtok + kC;
-  float *rg = reinterpret_cast<float *>(rslot + kC), *rkm = rg + kC, *rki = rkm + kC;
+  float *rg = reinterpret_cast<float *>(rslot + kC);
   int *info = reinterpret_cast<int *>(sm + kPInfo);
   const int T = a.T, H = a.H, N = a.N, topk = a.topk;
   const int nS = (T + kC - 1) / kC;
@@ -230,7 +231,7 @@ __global__ void __launch_bounds__(kPThreads, 2) sse_prep_kernel(const PrepArgs a
     if (tid < kC) {
       const int p = info[0], pos = info[1] + tid;
       int tk = -1, slot = topk;
-      float gate = 0.f, km = 0.f, ki = 0.f;
+      float gate = 0.f;
       if (pos < info[2]) {
         int t = pos, r = topk;
         if (p < N) {
@@ -241,16 +242,12 @@ __global__ void __launch_bounds__(kPThreads, 2) sse_prep_kernel(const PrepArgs a
         const long tl = (b * T + t) * H + h;
         const uint32_t *rc = a.rec + tl * a.rw;
         gate = r < topk ? __uint_as_float(rc[topk + r]) : 1.f;
-        km = __uint_as_float(rc[2 * topk]);
-        ki = __uint_as_float(rc[2 * topk + 1]);
         tk = static_cast<int>(tl);
         slot = r;
       }
       rtok[tid] = tk;
       rslot[tid] = slot;
       rg[tid] = gate;
-      rkm[tid] = km;
-      rki[tid] = ki;
     }
     __syncthreads();
     unsigned char *unit = a.units + ug * kXUnit;
@@ -290,11 +287,34 @@ __global__ void __launch_bounds__(kPThreads, 2) sse_prep_kernel(const PrepArgs a
     if (tid < kC) reinterpret_cast<int *>(unit + kXR)[tid] = rtok[tid] >= 0 ? rtok[tid] * (topk + 1) + rslot[tid] : -1;
     cp_async_wait<0>();
     __syncthreads();
-    // kk = softmax of the key logits (max and normaliser from the routing record)
-    for (int e = tid; e < kC * kCh; e += kPThreads) {
-      const int i = e >> 7, r = e & 127;
-      float &x = skk[i * kLdA + r];
-      x = rtok[i] >= 0 ? __expf(x - rkm[i]) * rki[i] : 0.f;
+    // kk = softmax of each visit's key logits (warp: 8 rows, lane: 4 channels)
+#pragma unroll 2
+    for (int e = 0; e < kC / 8; ++e) {
+      const int i = (kC / 8) * warp + e;
+      float4 *x = reinterpret_cast<float4 *>(skk + i * kLdA) + lane;
+      float4 v = *x;
+      if (rtok[i] >= 0) {  // warp-uniform
+        const bool bad = !(isfinite(v.x) && isfinite(v.y) && isfinite(v.z) && isfinite(v.w));
+        if (__any_sync(kFull, bad) && lane == 0 && a.err) atomicOr(a.err, SDM_DEVERR_NONFINITE);
+        float m = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+        v.x = __expf(v.x - m);
+        v.y = __expf(v.y - m);
+        v.z = __expf(v.z - m);
+        v.w = __expf(v.w - m);
+        float z = (v.x + v.y) + (v.z + v.w);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(kFull, z, o);
+        const float zi = 1.0f / z;
+        v.x *= zi;
+        v.y *= zi;
+        v.z *= zi;
+        v.w *= zi;
+      } else {
+        v = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      *x = v;
     }
     __syncthreads();
 
@@ -488,13 +508,16 @@ __global__ void __launch_bounds__(kPThreads, 2) sse_prep_kernel(const PrepArgs a
 // chain: the units of one partition in order.
 //
 // Warps 0-15 (workers): warp w owns tensor-memory lanes 32*(w%4) .. +31
-// (value columns d) and quarter w/4 of the rows r (S) and of the chunk's
+// (value columns d) and quarter w/4 of the rows r (S) and of the unit's
 // visits (O).  Warp 16 (producer, one lane) issues the bulk copies and the
-// MMAs.  Per unit:
-//   producer  D = V^T Kh and O^T = V^T A^T (state-independent), then, once
-//             the workers have published S0: O^T += S0^T Qt^T
-//   workers   S^T <- gamma S^T + D, published as bf16 hi/lo for the next
-//             unit; O^T staged per visit
+// MMAs.  Per unit c (buffers b = c % 2 for A/V/Kh, gamma/rows, D and O):
+//   producer  D[b] = V^T Kh and O[b]^T = V^T A^T (state-independent; issued
+//             as soon as unit c's tiles are in and unit c-2's D/O were read),
+//             then, once the workers have published S0: O[b]^T += S0^T Qt^T;
+//             then the copies of unit c+1
+//   workers   S^T <- gamma S^T + D[b], published as bf16 hi/lo for unit c+1;
+//             O[b]^T staged per visit
+// so unit c+1's state-independent MMAs run while the workers fold unit c.
 // ===========================================================================
 struct ChainArgs {
   float *state;
@@ -508,15 +531,17 @@ struct ChainArgs {
 
 constexpr int kWorkers = 512;
 constexpr int kChainThreads = kWorkers + 32;
-constexpr uint32_t kColD = 0, kColO = 128, kChainTmemCols = 256;
+// tensor-memory columns (fp32): D[2] 128 each, O[2] 64 each
+constexpr uint32_t kColD = 0, kColO = 256, kChainTmemCols = 512;
 // shared memory (bytes)
 constexpr uint32_t kSS = 0;                      // S^T hi, lo [128 d][128 r]   2 x 32 KB
 constexpr uint32_t kSX = 65536;                  // Qt hi, lo                   32 KB
-constexpr uint32_t kSY = kSX + kXQBytes;         // A hi, lo, V, Kh hi, lo      64 KB
-constexpr uint32_t kSZ = kSY + kXYBytes;         // gamma + rows, two buffers   2 x 768 B
+constexpr uint32_t kSY = kSX + kXQBytes;         // A hi, lo, V, Kh hi, lo      2 x 64 KB
+constexpr uint32_t kSZ = kSY + 2 * kXYBytes;     // gamma + rows                2 x 768 B
 constexpr uint32_t kSBar = kSZ + 2 * kXZBytes;
-constexpr int kNBar = 8;
+constexpr int kNBar = 10;
 constexpr uint32_t kChainSmem = kSBar + kNBar * 8 + 16;
+static_assert(kChainSmem <= 227 * 1024, "chain shared memory");
 
 __global__ void __maxnreg__(96) sse_chain_kernel(const ChainArgs a) {
   extern __shared__ __align__(1024) unsigned char sm[];
@@ -541,17 +566,16 @@ __global__ void __maxnreg__(96) sse_chain_kernel(const ChainArgs a) {
 
   unsigned char *sSh = sm + kSS, *sSl = sm + kSS + 32768;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kSBar);
-  // barriers: 0 Qt loaded, 1 A/V/Kh loaded, 2-3 gamma/rows loaded [2], 4 MMAs of the unit done,
-  // 5 S published (workers), 6 D and O read (workers), 7 drain
+  // barriers: 0 Qt loaded, 1-2 A/V/Kh loaded [b], 3-4 gamma/rows loaded [b], 5 MMAs of the unit done,
+  // 6 S published (workers), 7-8 D[b] and O[b] read (workers), 9 drain
+  enum { kBarX = 0, kBarY = 1, kBarZ = 3, kBarMma = 5, kBarS = 6, kBarFree = 7, kBarDrain = 9 };
   auto bar = [&](int i) { return smem_addr(bars + i); };
   uint32_t *holder = reinterpret_cast<uint32_t *>(sm + kSBar + kNBar * 8);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + kSBar + kNBar * 8 + 4);
 
   if (tid == 0) {
-    for (int i = 0; i < 5; ++i) mbar_init(bar(i), 1);
-    mbar_init(bar(5), kWorkers);
-    mbar_init(bar(6), kWorkers);
-    mbar_init(bar(7), 1);
+    for (int i = 0; i < kNBar; ++i)
+      mbar_init(bar(i), (i == kBarS || i == kBarFree || i == kBarFree + 1) ? kWorkers : 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -576,19 +600,20 @@ __global__ void __maxnreg__(96) sse_chain_kernel(const ChainArgs a) {
       for (int g8 = 0; g8 < 4; ++g8) store_split8(sSh, sSl, kmajor_off(row, 32 * qtr + 8 * g8, kCh), S + 8 * g8);
       fence_async_smem();
       tc_fence_before();
-      mbar_arrive(bar(5));
+      mbar_arrive(bar(kBarS));
     };
     publish();
     for (int c = 0; c < n; ++c) {
+      const int b = c & 1;
       const bool last = c + 1 == n;
-      if (!wwait(bar(4), static_cast<uint32_t>(c & 1))) break;
-      if (!wwait(bar(2 + (c & 1)), static_cast<uint32_t>((c >> 1) & 1))) break;
-      const unsigned char *z = sm + kSZ + (c & 1) * kXZBytes;
+      if (!wwait(bar(kBarMma), static_cast<uint32_t>(c & 1))) break;
+      if (!wwait(bar(kBarZ + b), static_cast<uint32_t>((c >> 1) & 1))) break;
+      const unsigned char *z = sm + kSZ + b * kXZBytes;
       const float *gam = reinterpret_cast<const float *>(z) + 32 * qtr;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         float x[16];
-        tmem_ld16(lanes + kColD + 32 * qtr + 16 * hh, x);
+        tmem_ld16(lanes + kColD + 128 * b + 32 * qtr + 16 * hh, x);
         tmem_ld_wait();
 #pragma unroll
         for (int e = 0; e < 16; ++e) S[16 * hh + e] = fmaf(gam[16 * hh + e], S[16 * hh + e], x[e]);
@@ -597,7 +622,7 @@ __global__ void __maxnreg__(96) sse_chain_kernel(const ChainArgs a) {
       {
         const int *rows = reinterpret_cast<const int *>(z + (kXR - kXG)) + 16 * qtr;
         float o[16];
-        tmem_ld16(lanes + kColO + 16 * qtr, o);
+        tmem_ld16(lanes + kColO + 64 * b + 16 * qtr, o);
         tmem_ld_wait();
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
@@ -606,7 +631,7 @@ __global__ void __maxnreg__(96) sse_chain_kernel(const ChainArgs a) {
         }
       }
       tc_fence_before();
-      mbar_arrive(bar(6));
+      mbar_arrive(bar(kBarFree + b));
       if (last) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) gS[static_cast<long>(32 * qtr + j) * kD + row] = S[j];
@@ -615,31 +640,28 @@ __global__ void __maxnreg__(96) sse_chain_kernel(const ChainArgs a) {
   } else if (tid == kWorkers) {
     // ------------------------------------------------------------ producer
     const uint32_t sh = smem_addr(sSh), sl = smem_addr(sSl);
-    const uint32_t xq = smem_addr(sm + kSX), ya = smem_addr(sm + kSY);
-    const uint32_t yv = ya + (kXV - kXA), yk = ya + (kXK - kXA);
+    const uint32_t xq = smem_addr(sm + kSX);
     const uint64_t dSh = smem_desc(sh, 128, kCh * 16), dSl = smem_desc(sl, 128, kCh * 16);
     const uint64_t dQh = smem_desc(xq, 128, kCh * 16), dQl = smem_desc(xq + 16384, 128, kCh * 16);
-    const uint64_t dAh = smem_desc(ya, 128, kC * 16), dAl = smem_desc(ya + 8192, 128, kC * 16);
-    // V^T (A operand) and Kh (B operand) are MN-major: 8 consecutive d (or r)
-    // per 16 bytes, 8-visit groups 2048 bytes apart; a k-step of 16 visits is
-    // 4096 bytes (256 in the descriptor)
-    const uint64_t dV = smem_desc(yv, 2048, 128);
-    const uint64_t dKh = smem_desc(yk, 2048, 128), dKl = smem_desc(yk + 16384, 2048, 128);
     const uint32_t idO = idesc_bf16_f32(128, kC), idOv = idO | (1u << 15);
     const uint32_t idD = idesc_bf16_f32(128, kCh) | (1u << 15) | (1u << 16);
-    int x_issued = 0, x_done = 0, y_issued = 0, y_done = 0, z_issued = 0;
-    auto load = [&](int c) {
-      const unsigned char *src = ub + static_cast<long>(c) * kXUnit;
+    int x_issued = 0, x_done = 0, y_issued[2] = {0, 0}, y_done[2] = {0, 0}, z_issued[2] = {0, 0};
+    auto load_x = [&](int c) {
       fence_async_smem();
-      mbar_expect_tx(bar(0), kXQBytes);
-      bulk_g2s(xq, src + kXQ, kXQBytes, bar(0));
+      mbar_expect_tx(bar(kBarX), kXQBytes);
+      bulk_g2s(xq, ub + static_cast<long>(c) * kXUnit + kXQ, kXQBytes, bar(kBarX));
       ++x_issued;
-      mbar_expect_tx(bar(1), kXYBytes);
-      bulk_g2s(ya, src + kXA, kXYBytes, bar(1));
-      ++y_issued;
-      mbar_expect_tx(bar(2 + (c & 1)), kXZBytes);
-      bulk_g2s(smem_addr(sm + kSZ + (c & 1) * kXZBytes), src + kXG, kXZBytes, bar(2 + (c & 1)));
-      ++z_issued;
+    };
+    auto load_yz = [&](int c) {
+      const unsigned char *src = ub + static_cast<long>(c) * kXUnit;
+      const int b = c & 1;
+      fence_async_smem();
+      mbar_expect_tx(bar(kBarY + b), kXYBytes);
+      bulk_g2s(smem_addr(sm + kSY + b * kXYBytes), src + kXA, kXYBytes, bar(kBarY + b));
+      ++y_issued[b];
+      mbar_expect_tx(bar(kBarZ + b), kXZBytes);
+      bulk_g2s(smem_addr(sm + kSZ + b * kXZBytes), src + kXG, kXZBytes, bar(kBarZ + b));
+      ++z_issued[b];
     };
     auto prefetch = [&](int c) {
       const unsigned char *pf = ub + static_cast<long>(c) * kXUnit;
@@ -648,50 +670,66 @@ __global__ void __maxnreg__(96) sse_chain_kernel(const ChainArgs a) {
     };
     auto wait = [&](int i, uint32_t parity) { return mbar_wait_abortable(bar(i), parity, kWaitLimit, abort_flag); };
     if (n > 1) prefetch(1);
-    load(0);
+    load_x(0);
+    load_yz(0);
     bool ok = true;
     for (int c = 0; c < n && ok; ++c) {
-      const uint32_t par = static_cast<uint32_t>(c & 1);
+      const int b = c & 1;
       if (c + 2 < n) prefetch(c + 2);
-      ok = wait(1, par);
-      if (ok) ++y_done;
-      if (ok && c > 0) ok = wait(6, static_cast<uint32_t>((c - 1) & 1));  // D and O of the last unit read
+      // state-independent MMAs of unit c
+      ok = wait(kBarY + b, static_cast<uint32_t>((c >> 1) & 1));
+      if (ok) ++y_done[b];
+      if (ok && c >= 2) ok = wait(kBarFree + b, static_cast<uint32_t>(((c - 2) >> 1) & 1));  // D[b], O[b] read
       if (!ok) break;
+      const uint32_t ya = smem_addr(sm + kSY + b * kXYBytes);
+      const uint32_t yv = ya + (kXV - kXA), yk = ya + (kXK - kXA);
+      const uint64_t dAh = smem_desc(ya, 128, kC * 16), dAl = smem_desc(ya + 8192, 128, kC * 16);
+      // V^T (A operand) and Kh (B operand) are MN-major: 8 consecutive d (or
+      // r) per 16 bytes, 8-visit groups 2048 bytes apart; a k-step of 16
+      // visits is 4096 bytes (256 in the descriptor)
+      const uint64_t dV = smem_desc(yv, 2048, 128);
+      const uint64_t dKh = smem_desc(yk, 2048, 128), dKl = smem_desc(yk + 16384, 2048, 128);
+      const uint32_t tD = tmem + kColD + 128 * b, tO = tmem + kColO + 64 * b;
 #pragma unroll
       for (int ks = 0; ks < kC / 16; ++ks) {
-        mma_bf16(tmem + kColD, dV + 256u * ks, dKh + 256u * ks, idD, ks > 0);
-        mma_bf16(tmem + kColD, dV + 256u * ks, dKl + 256u * ks, idD, true);
+        mma_bf16(tD, dV + 256u * ks, dKh + 256u * ks, idD, ks > 0);
+        mma_bf16(tD, dV + 256u * ks, dKl + 256u * ks, idD, true);
       }
 #pragma unroll
       for (int ks = 0; ks < kC / 16; ++ks) {
-        mma_bf16(tmem + kColO, dV + 256u * ks, dAh + 16u * ks, idOv, ks > 0);
-        mma_bf16(tmem + kColO, dV + 256u * ks, dAl + 16u * ks, idOv, true);
+        mma_bf16(tO, dV + 256u * ks, dAh + 16u * ks, idOv, ks > 0);
+        mma_bf16(tO, dV + 256u * ks, dAl + 16u * ks, idOv, true);
       }
-      ok = wait(0, par);
+      // the state-dependent part
+      ok = wait(kBarX, static_cast<uint32_t>(c & 1));
       if (ok) ++x_done;
-      if (ok) ok = wait(5, par);  // S0 of this unit published
+      if (ok) ok = wait(kBarS, static_cast<uint32_t>(c & 1));  // S0 of unit c published
       if (!ok) break;
 #pragma unroll
       for (int ks = 0; ks < kCh / 16; ++ks) {
-        mma_bf16(tmem + kColO, dSh + 16u * ks, dQh + 16u * ks, idO, true);
-        mma_bf16(tmem + kColO, dSh + 16u * ks, dQl + 16u * ks, idO, true);
-        mma_bf16(tmem + kColO, dSl + 16u * ks, dQh + 16u * ks, idO, true);
+        mma_bf16(tO, dSh + 16u * ks, dQh + 16u * ks, idO, true);
+        mma_bf16(tO, dSh + 16u * ks, dQl + 16u * ks, idO, true);
+        mma_bf16(tO, dSl + 16u * ks, dQh + 16u * ks, idO, true);
       }
-      mma_commit(bar(4));
+      mma_commit(bar(kBarMma));
       if (c + 1 < n) {
-        ok = wait(4, par);  // this unit's operands consumed
-        if (ok) load(c + 1);
+        // unit c+1's tiles into the other buffers once the workers are done with unit c-1
+        if (c >= 1) ok = wait(kBarFree + (b ^ 1), static_cast<uint32_t>(((c - 1) >> 1) & 1));
+        if (ok) load_yz(c + 1);
+        // its Qt once this unit's MMAs have read theirs
+        if (ok) ok = wait(kBarMma, static_cast<uint32_t>(c & 1));
+        if (ok) load_x(c + 1);
       }
     }
     if (!ok || *abort_flag) {
       // stop cleanly: wait (bounded) for the MMAs and the bulk copies in flight
-      mma_commit(bar(7));
-      mbar_wait(bar(7), 0, kWaitLimit);
-      if (x_done < x_issued) mbar_wait(bar(0), static_cast<uint32_t>((x_issued - 1) & 1), kWaitLimit);
-      if (y_done < y_issued) mbar_wait(bar(1), static_cast<uint32_t>((y_issued - 1) & 1), kWaitLimit);
-      for (int zb = 0; zb < 2; ++zb) {
-        const int m = (z_issued + 1 - zb) / 2;  // loads issued into buffer zb
-        if (m > 0) mbar_wait(bar(2 + zb), static_cast<uint32_t>((m - 1) & 1), kWaitLimit);
+      mma_commit(bar(kBarDrain));
+      mbar_wait(bar(kBarDrain), 0, kWaitLimit);
+      if (x_done < x_issued) mbar_wait(bar(kBarX), static_cast<uint32_t>((x_issued - 1) & 1), kWaitLimit);
+      for (int bb = 0; bb < 2; ++bb) {
+        if (y_done[bb] < y_issued[bb])
+          mbar_wait(bar(kBarY + bb), static_cast<uint32_t>((y_issued[bb] - 1) & 1), kWaitLimit);
+        if (z_issued[bb] > 0) mbar_wait(bar(kBarZ + bb), static_cast<uint32_t>((z_issued[bb] - 1) & 1), kWaitLimit);
       }
       *abort_flag = 1;
     }
@@ -777,6 +815,7 @@ int launch_sse_chunk(float *state, const uint32_t *rec, int rw, const float *klo
   pa.umax = umax;
   pa.gwords = gwords;
   pa.total = bhn * umax;
+  pa.err = err;
   if (cudaFuncSetAttribute(sse_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kPrepSmem)) != cudaSuccess)
     return check_launch("sse_scan: set shared memory");

@@ -38,8 +38,9 @@ __host__ __device__ inline int rec_words(int topk) { return (2 * topk + 2 + 3) &
 // Routing prepass.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) sse_route_kernel(const float *__restrict__ route, const float *__restrict__ klog,
-                                                        long tokens, int N, int topk, int c, uint32_t *__restrict__ rec,
-                                                        int32_t *__restrict__ sel_out, int32_t *__restrict__ dev_err) {
+                                                        long tokens, int N, int topk, int c, bool kstats,
+                                                        uint32_t *__restrict__ rec, int32_t *__restrict__ sel_out,
+                                                        int32_t *__restrict__ dev_err) {
   const int lane = threadIdx.x & 31;
   const long tok = static_cast<long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   if (tok >= tokens) return;  // warp-uniform
@@ -84,7 +85,12 @@ __global__ void __launch_bounds__(256) sse_route_kernel(const float *__restrict_
       if (sel_out) sel_out[tok * topk + s] = wid;
     }
   }
-  // key-logit softmax statistics over the c rows (c <= 128: four per lane)
+  // key-logit softmax statistics over the c rows (c <= 128: four per lane);
+  // the chunked path computes them where it reads the logits
+  if (!kstats) {
+    if (__any_sync(kFull, bad) && lane == 0 && dev_err) atomicOr(dev_err, SDM_DEVERR_NONFINITE);
+    return;
+  }
   const float *kl = klog + tok * c;
   float kv[4];
   uint32_t km = 0u;
@@ -400,7 +406,7 @@ extern "C" int sse_scan(float *state, const float *route_logits, int topk, const
   const long tokens = static_cast<long>(B) * T * H;
   uint32_t *rec = static_cast<uint32_t *>(workspace);
   sse_route_kernel<<<static_cast<unsigned>((tokens + 7) / 8), 256, 0, st>>>(route_logits, k_logits, tokens, N, topk,
-                                                                           c, rec, sel_out, dev_err);
+                                                                           c, !chunk, rec, sel_out, dev_err);
   int rc = check_launch("sse_scan: route kernel");
   if (rc != SDM_OK) return rc;
 
