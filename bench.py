@@ -44,7 +44,10 @@ NCU_TRAFFIC = {
     # (8.01 GB + 4.19 GB), profiles/sparse_scan_1.4b_layer.md
     ("sdm_14b_layer", "sdm"): {"bytes": 12.20e9, "digest": "651ec4880368"},
     # both kernels of one full-size gdn_scan call (746.4 MB + 590.5 MB), profiles/gdn_chunk_dense.md
-    ("gdn", "gdn"): {"bytes": 1.337e9, "digest": "4f85348a1ab7"},
+    ("gdn", "gdn"): {"bytes": 1.337e9, "digest": "4469700d7705"},
+    # the five kernels of one full-size sse_scan call on the chunked path (1.072 GB read + 0.799 GB
+    # written), profiles/sse_chunk_prefill.md
+    ("sse", "sse"): {"bytes": 1.871e9, "digest": "c7400c3e5885"},
 }
 
 
