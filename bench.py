@@ -377,14 +377,49 @@ class GpuRun:
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
         self.y_host = torch.empty(self.y.shape, dtype=torch.float32).pin_memory()
 
+    def enable_graphs(self):
+        """Replay the step's launches as CUDA graphs (decode: a handful of short
+        kernels per token, so host launch latency would otherwise dominate).
+        Every buffer, the state included, stays where it is, so a replay is the
+        same step; the library's calls allocate nothing and never synchronise,
+        which makes them capturable."""
+        import torch
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            self._run_pre()
+            self._run_main()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        if self.wl.kind == "sdm":
+            self.g_pre = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.g_pre):
+                self._run_pre()
+        self.g_main = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.g_main):
+            self._run_main()
+        torch.cuda.synchronize()
+
     def pre(self):
+        if getattr(self, "g_pre", None) is not None:
+            self.g_pre.replay()
+        elif getattr(self, "g_main", None) is None:
+            self._run_pre()
+
+    def main(self):
+        if getattr(self, "g_main", None) is not None:
+            self.g_main.replay()
+        else:
+            self._run_main()
+
+    def _run_pre(self):
         """Work before the dominant kernel (addressing)."""
         sh, d = self.wl.shape, self.d
         if self.wl.kind == "sdm":
             self.sdm.sdm_address(d["s1w"], d["s2w"], sh.k, sh.W, self.iw, self.ww, self.err)
             self.sdm.sdm_address(d["s1r"], d["s2r"], sh.k, sh.R, self.ir, self.wr, self.err)
 
-    def main(self):
+    def _run_main(self):
         """The dominant kernel's call."""
         sh, d = self.wl.shape, self.d
         if self.wl.kind == "sdm" and self.wl.train:
@@ -517,6 +552,8 @@ def run_ours(args, rank, world, local_rank, sampler):
     torch.cuda.synchronize()
     if int(run.err.item()) != 0:
         raise SystemExit(f"device error flag {int(run.err.item())} during warm-up")
+    if wl.decode:
+        run.enable_graphs()
     algo, algo_unit, bound, algo_info = run.algorithmic()
 
     clocks = ClockSampler(local_rank)
@@ -607,6 +644,7 @@ def run_ours(args, rank, world, local_rank, sampler):
                 if wl.kind == "sdm" and not wl.train and not wl.chunked
                 else "pinned H2D copies + scan call + D2H of y"},
         "gpu_launches": K * run.launches_per_step,
+        "step_launch": "CUDA graph replay of the step's kernels" if wl.decode else "stream launches",
         "clocks": clk,
     }
     if wl.kind == "sdm":

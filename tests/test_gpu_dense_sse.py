@@ -51,10 +51,11 @@ def test_gdn_full_size_sampled(per_channel):
         assert_state_close(S[b:b + 1, h:h + 1], Sr, what=f"state[{b},{h}]")
 
 
-@pytest.mark.parametrize("T", [1, 63, 64, 65, 200])
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 200, 512, 700])
 def test_gdn_chunked_path_lengths(T, monkeypatch):
     """Dense GDN at d_k = d_v = 128 runs chunkwise (64 tokens) on the tensor
-    cores: lengths below, at and across a chunk boundary, nonzero state."""
+    cores: lengths below, at and across a chunk boundary, nonzero state, and
+    longer sequences of 8 and 11 chunks."""
     sdm = need_gpu()
     monkeypatch.setenv("SDM_GDN_PATH", "chunk")
     import torch
@@ -70,6 +71,28 @@ def test_gdn_chunked_path_lengths(T, monkeypatch):
     assert int(err.item()) == 0
     assert_y_close(host(y), yr)
     assert_state_close(host(state), Sr)
+
+
+def test_gdn_chunked_is_deterministic_and_continues_the_state(monkeypatch):
+    """The chunked path (T = 900: 15 chunks) gives the same bits on every
+    call, and a sequence cut at a chunk boundary into two calls equals one
+    call (the second call continues from the state the first left)."""
+    sdm = need_gpu()
+    monkeypatch.setenv("SDM_GDN_PATH", "chunk")
+    sh = synth.GDN_DENSE.with_(B=2, T=900, H=2)
+    inp = synth.gdn_inputs(sh, seed=46)
+    S0 = synth.random_state((2, 2, 128, 128), seed=47, scale=0.3)
+    S1, y1 = _gdn_gpu(sdm, S0, inp, False)
+    S2, y2 = _gdn_gpu(sdm, S0, inp, False)
+    np.testing.assert_array_equal(y1, y2)
+    np.testing.assert_array_equal(S1, S2)
+    cut = 576
+    first = {k: v[:, :cut] for k, v in inp.items() if isinstance(v, np.ndarray) and v.ndim >= 3}
+    second = {k: v[:, cut:] for k, v in inp.items() if isinstance(v, np.ndarray) and v.ndim >= 3}
+    Sa, ya = _gdn_gpu(sdm, S0, first, False)
+    Sb, yb = _gdn_gpu(sdm, Sa, second, False)
+    assert_y_close(np.concatenate([ya, yb], axis=1), y1.astype(np.float64))
+    assert_state_close(Sb, S1.astype(np.float64))
 
 
 def test_gdn_chunked_matches_token_recurrent(monkeypatch):
