@@ -192,21 +192,20 @@ __global__ void __launch_bounds__(128) sparse_backward_kernel16(const BackArgs a
       Gw[k] = okw ? G[static_cast<long>(wi) * d_v] : 0.f;
       U[k] = k < W ? a.undo[(tok * W + k) * static_cast<long>(d_v) + ccol] : 0.f;
     }
+    // per-lane column partials of the token's sums: [0, 16) dr_i, [16, 32) dw_j
+    float part[2 * S];
     // the read after the write
 #pragma unroll
     for (int i = 0; i < S; ++i) {
-      if (i < R) {
-        const float dr = warp_sum(active ? dyc * Mr[i] : 0.f);
-        if (lane == 0) pt[i] = dr;
-        Gr[i] = fmaf(__shfl_sync(kFull, my_wt, i), dyc, Gr[i]);
-      }
+      part[i] = (i < R && active) ? dyc * Mr[i] : 0.f;
+      if (i < R) Gr[i] = fmaf(__shfl_sync(kFull, my_wt, i), dyc, Gr[i]);
     }
+    // a written row that is also read takes the read gradient (same fma as its read slot)
 #pragma unroll
-    for (int j = 0; j < S; ++j) {  // a written row that is also read takes the read gradient
+    for (int j = 0; j < S; ++j) {
       const int mi = __shfl_sync(kFull, my_match, 16 + j);
-#pragma unroll
-      for (int i = 0; i < S; ++i)
-        if (mi == i) Gw[j] = Gr[i];
+      const float wr = __shfl_sync(kFull, my_wt, mi & 15);
+      if (mi >= 0) Gw[j] = fmaf(wr, dyc, Gw[j]);
     }
     // the write
     float vh = 0.f, gs = 0.f;
@@ -223,6 +222,7 @@ __global__ void __launch_bounds__(128) sparse_backward_kernel16(const BackArgs a
 #pragma unroll
     for (int j = 0; j < S; ++j) {
       const float wj = __shfl_sync(kFull, my_wt, 16 + j);
+      part[S + j] = 0.f;
       if (j < W) {
         const float m = al * U[j];
         const float rho = MODE == SDM_RESID_SHARED ? res_sh : MODE == SDM_RESID_PERSLOT ? vc - m : vc;
@@ -233,12 +233,24 @@ __global__ void __launch_bounds__(128) sparse_backward_kernel16(const BackArgs a
                          : MODE == SDM_RESID_PERSLOT ? Gw[j] * (1.f - be * wj) : Gw[j];
         dalpha = fmaf(dm, U[j], dalpha);
         Gw[j] = al * dm;
-        dw = warp_sum(active ? dw : 0.f);
-        if (lane == 0) pt[R + j] = dw;
+        part[S + j] = active ? dw : 0.f;
       }
     }
     dalpha = warp_sum(active ? dalpha : 0.f);
     dbeta = warp_sum(active ? dbeta : 0.f);
+    // reduce-scatter of the 32 partials over the warp (31 shuffles): lane l
+    // ends with the column sum of partial l
+#pragma unroll
+    for (int o = 16, n = 2 * S; o >= 1; o >>= 1, n >>= 1) {
+      const bool upper = (lane & o) != 0;
+#pragma unroll
+      for (int i = 0; i < n / 2; ++i) {
+        const float send = upper ? part[i] : part[i + n / 2];
+        const float recv = __shfl_xor_sync(kFull, send, o);
+        part[i] = (upper ? part[i + n / 2] : part[i]) + recv;
+      }
+    }
+    if (lane < S ? lane < R : lane - S < W) pt[lane < S ? lane : R + lane - S] = part[0];
     if (lane == 0) {
       pt[R + W] = dalpha;
       pt[R + W + 1] = dbeta;
