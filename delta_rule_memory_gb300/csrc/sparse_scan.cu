@@ -5,14 +5,15 @@
 // The table is HBM-resident fp32 [B,H,N,d_v]; every token gathers its write
 // and read rows, decays and updates the written ones, scatters them back and
 // reads.  Every value column evolves independently (the addresses do not
-// depend on the table), so the work splits into (batch, head, 32-column tile)
-// slices, one warp each, with no synchronisation between warps.
+// depend on the table), so the work splits into (batch, head, column tile)
+// slices of TW = 32 or 16 columns, one warp each, with no synchronisation
+// between warps (16-column tiles double the warps for small batches).
 //
-// Inside a warp, lane = q + 8 r: q picks a float4 column quad of the tile, r a
-// row subgroup; lane (q, r) owns write slots and read slots r, r+4, r+8, ...
-// of every token.  It copies exactly those row quads (cp.async, 16 bytes),
-// decays and updates them; the shared prediction v_hat and the read y are
-// summed over the four subgroups with two xor-shuffles.
+// Inside a warp, lane = q + Q r with Q = TW/4: q picks a float4 column quad of
+// the tile, r one of RG = 32/Q row subgroups; lane (q, r) owns write slots and
+// read slots r, r+RG, r+2RG, ... of every token.  It copies exactly those row
+// quads (cp.async, 16 bytes), decays and updates them; the shared prediction
+// v_hat and the read y are summed over the subgroups with xor-shuffles.
 //
 // The rows of token t+P are prefetched while token t is computed.  A row that
 // one of the last P tokens wrote is stale in that prefetch, so a prepass
@@ -30,16 +31,16 @@
 namespace sdm {
 namespace {
 
-// A slot's source is stored as the number of a 128-byte row (32 floats) of
-// the warp's shared memory, numbered across the rings of ScanLayout: the
+// A slot's source is stored as the number of a tile row (TW floats) of the
+// warp's shared memory, numbered across the rings of ScanLayout: the
 // prefetched copy, a post-write history row or the zero row.  A read of a
 // row the same token writes is kRecompute | write slot.
 constexpr uint16_t kRecompute = 0x8000;
 
 // Packed per-token record, 16-byte aligned.  Slot positions are permuted so
 // lane subgroup r finds its 2*RPL slots (RPL write then RPL read) contiguous:
-// position r*2*RPL + k is write slot r + 4k (k < RPL) or read slot
-// r + 4(k - RPL) (k >= RPL).
+// position r*2*RPL + k is write slot r + RG k (k < RPL) or read slot
+// r + RG (k - RPL) (k >= RPL), RG the number of row subgroups of the tile.
 template <int SLOTS>
 struct alignas(16) TokenRec {
   int32_t idx[2 * SLOTS];
@@ -54,20 +55,31 @@ __host__ __device__ constexpr size_t rec_bytes() { return sizeof(TokenRec<SLOTS>
 
 __host__ __device__ inline int pick_slots(int W, int R) { return (W <= 16 && R <= 16) ? 16 : 64; }
 
-template <int P, int SLOTS>
+// Column tile of a warp: TW columns as Q float4 quads, RG row subgroups.
+template <int TW>
+struct Tile {
+  static_assert(TW == 16 || TW == 32, "16- or 32-column tiles");
+  static constexpr int Q = TW / 4;
+  static constexpr int RG = 32 / Q;
+  static constexpr int RB = TW * 4;  // bytes of one tile row
+};
+
+template <int P, int SLOTS, int TW>
 struct ScanLayout {
+  static constexpr int RB = Tile<TW>::RB;
   static constexpr int NI = P + 1;      // incoming rows: P in flight + current
   static constexpr int NH = P + 1;      // post-write history: current + P back
   static constexpr int NM = 2 * P + 1;  // records: needed from t-P (row issue) to t
-  // 128-byte row numbers of the rings
+  // tile-row numbers of the rings
   static constexpr int kRowW = 0;                    // incoming write rows [NI][SLOTS]
   static constexpr int kRowH = NI * SLOTS;           // history [NH][SLOTS]
   static constexpr int kRowR = (NI + NH) * SLOTS;    // incoming read rows [NI][SLOTS]
   static constexpr int kRowZero = (2 * NI + NH) * SLOTS;
-  static constexpr size_t kRecOff = static_cast<size_t>(kRowZero + 1) * 128;
+  static constexpr size_t kRecOff = static_cast<size_t>(kRowZero + 1) * RB;
   static constexpr size_t kVOff = kRecOff + NM * rec_bytes<SLOTS>();
-  static constexpr size_t kWarpBytes = kVOff + NM * 128;  // 32 columns of v per record, fp32 or bf16
+  static constexpr size_t kWarpBytes = kVOff + NM * RB;  // TW columns of v per record, fp32 or bf16
   static_assert(kRowZero < kRecompute, "row numbers must stay below the recompute flag");
+  static_assert(kRecOff % 16 == 0 && kVOff % 16 == 0 && kWarpBytes % 16 == 0, "16-byte aligned regions");
 };
 
 
@@ -79,21 +91,22 @@ struct ScanLayout {
 // read slot j -> likewise, or kRecompute | s when write slot s of the same
 // token holds the row; out-of-range ids and padding -> the zero row.
 // ---------------------------------------------------------------------------
-template <int P, int SLOTS>
+template <int P, int SLOTS, int TW>
 __global__ void record_kernel(const int32_t *__restrict__ idx_w, const float *__restrict__ w_w,
                               const int32_t *__restrict__ idx_r, const float *__restrict__ w_r,
                               const float *__restrict__ alpha, const float *__restrict__ beta, int W, int R, int T,
                               int H, int N, long total, TokenRec<SLOTS> *__restrict__ rec,
                               int32_t *__restrict__ dev_err) {
-  using L = ScanLayout<P, SLOTS>;
-  constexpr int RPL = SLOTS / 4;
+  using L = ScanLayout<P, SLOTS, TW>;
+  constexpr int RG = Tile<TW>::RG;
+  constexpr int RPL = SLOTS / RG;
   const long tid = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (tid >= total) return;
   const long tok = tid / (2 * SLOTS);
   const int pos = static_cast<int>(tid - tok * 2 * SLOTS);
   const int r = pos / (2 * RPL), k = pos % (2 * RPL);
   const bool is_w = k < RPL;
-  const int j = r + 4 * (is_w ? k : k - RPL);
+  const int j = r + RG * (is_w ? k : k - RPL);
   const int t = static_cast<int>((tok / H) % T);
   TokenRec<SLOTS> &o = rec[tok];
   if (pos == 0) {
@@ -160,9 +173,10 @@ __device__ __forceinline__ float4 mul4(float s, float4 x) { return make_float4(s
 __device__ __forceinline__ float4 sub4(float4 a, float4 b) {
   return make_float4(a.x - b.x, a.y - b.y, a.z - b.z, a.w - b.w);
 }
-__device__ __forceinline__ float4 xsum4(float4 a) {  // sum over the four row subgroups (lane bits 3, 4)
+template <int Q>
+__device__ __forceinline__ float4 xsum4(float4 a) {  // sum over the row subgroups (lane bits from log2 Q up)
 #pragma unroll
-  for (int m = 8; m <= 16; m <<= 1) {
+  for (int m = Q; m <= 16; m <<= 1) {
     a.x += __shfl_xor_sync(kFull, a.x, m);
     a.y += __shfl_xor_sync(kFull, a.y, m);
     a.z += __shfl_xor_sync(kFull, a.z, m);
@@ -171,12 +185,13 @@ __device__ __forceinline__ float4 xsum4(float4 a) {  // sum over the four row su
   return a;
 }
 
-template <int P, int SLOTS, int MODE, bool LOG>  // LOG: also write the undo log
+template <int P, int SLOTS, int TW, int MODE, bool LOG>  // LOG: also write the undo log
 __global__ void __launch_bounds__(128) sparse_scan_kernel(const ScanArgs a) {
-  using L = ScanLayout<P, SLOTS>;
+  using L = ScanLayout<P, SLOTS, TW>;
   using Rec = TokenRec<SLOTS>;
-  constexpr int RPL = SLOTS / 4;
-  constexpr int SLOT_B = SLOTS * 128;  // bytes per ring slot
+  constexpr int Q = Tile<TW>::Q, RG = Tile<TW>::RG, RB = Tile<TW>::RB;
+  constexpr int RPL = SLOTS / RG;
+  constexpr int SLOT_B = SLOTS * RB;  // bytes per ring slot
   constexpr int REC_CHUNKS = static_cast<int>(sizeof(Rec) / 16);
   extern __shared__ __align__(16) unsigned char smem_raw[];
 
@@ -189,17 +204,17 @@ __global__ void __launch_bounds__(128) sparse_scan_kernel(const ScanArgs a) {
   const int h = static_cast<int>(bh % a.H);
   const long b = bh / a.H;
   const int T = a.T, d_v = a.d_v;
-  const int q = lane & 7, r = lane >> 3;
-  const int col = tile * 32 + 4 * q;
+  const int q = lane % Q, r = lane / Q;
+  const int col = tile * TW + 4 * q;
   const bool active = col < d_v;
 
   unsigned char *base = smem_raw + static_cast<size_t>(wib) * L::kWarpBytes;
   unsigned char *lbase = base + 16 * q;  // this lane's quad inside any 128-byte row
   Rec *recs = reinterpret_cast<Rec *>(base + L::kRecOff);
-  uint32_t *vbuf = reinterpret_cast<uint32_t *>(base + L::kVOff);  // [NM][32 words]
-  reinterpret_cast<float *>(base + L::kRowZero * 128)[lane] = 0.f;
+  uint32_t *vbuf = reinterpret_cast<uint32_t *>(base + L::kVOff);  // [NM][TW words]
+  if (lane < TW) reinterpret_cast<float *>(base + L::kRowZero * RB)[lane] = 0.f;
   auto row_ptr = [&](int row) -> const float * {
-    return reinterpret_cast<const float *>(lbase + min(row, L::kRowZero) * 128);
+    return reinterpret_cast<const float *>(lbase + min(row, L::kRowZero) * RB);
   };
 
   const size_t rowbytes = static_cast<size_t>(d_v) * sizeof(float);
@@ -209,22 +224,22 @@ __global__ void __launch_bounds__(128) sparse_scan_kernel(const ScanArgs a) {
   const long tok_stride = a.H;
 
   // per-token global sources (this token's record and v), advanced one token
-  // at a time; chunk c < REC_CHUNKS is 16 bytes of the record, the next 8 are
+  // at a time; chunk c < REC_CHUNKS is 16 bytes of the record, the next Q are
   // the v columns 4vc .. 4vc+3 of this tile
   const int esz = a.v_bf16 ? 2 : 4;
   const unsigned char *rec_tok = reinterpret_cast<const unsigned char *>(static_cast<const Rec *>(a.rec) + tok0);
-  const unsigned char *v_tok = static_cast<const unsigned char *>(a.v) + (tok0 * d_v + tile * 32) * esz;
+  const unsigned char *v_tok = static_cast<const unsigned char *>(a.v) + (tok0 * d_v + tile * TW) * esz;
   const long rec_step = tok_stride * static_cast<long>(sizeof(Rec));
   const long v_step = tok_stride * d_v * esz;
   int meta_slot = 0;  // ring slot of the next record to fetch
   auto issue_meta = [&]() {
-    for (int c = lane; c < REC_CHUNKS + 8; c += 32) {
+    for (int c = lane; c < REC_CHUNKS + Q; c += 32) {
       if (c < REC_CHUNKS) {
         cp_async<16>(reinterpret_cast<unsigned char *>(recs + meta_slot) + 16 * c, rec_tok + 16 * c);
       } else {
         const int vc = c - REC_CHUNKS;
-        if (tile * 32 + 4 * vc < d_v) {
-          unsigned char *dst = reinterpret_cast<unsigned char *>(vbuf + meta_slot * 32) + vc * 4 * esz;
+        if (tile * TW + 4 * vc < d_v) {
+          unsigned char *dst = reinterpret_cast<unsigned char *>(vbuf + meta_slot * TW) + vc * 4 * esz;
           if (a.v_bf16) cp_async<8>(dst, v_tok + vc * 8);
           else cp_async<16>(dst, v_tok + vc * 16);
         }
@@ -234,14 +249,14 @@ __global__ void __launch_bounds__(128) sparse_scan_kernel(const ScanArgs a) {
     v_tok += v_step;
     meta_slot = meta_slot + 1 == L::NM ? 0 : meta_slot + 1;
   };
-  // the row quads this lane consumes: write slots r+4k and read slots r+4k
+  // the row quads this lane consumes: write slots r+RG k and read slots r+RG k
   int fetch_rec = 0, fetch_ring = 0;  // record slot and row-ring slot of the next token to fetch
   auto issue_rows = [&]() {
     if (active) {
       const Rec &m = recs[fetch_rec];
       const int4 *ip = reinterpret_cast<const int4 *>(m.idx + r * 2 * RPL);
-      unsigned char *dw = lbase + (L::kRowW * 128 + fetch_ring * SLOT_B);
-      unsigned char *dr = lbase + (L::kRowR * 128 + fetch_ring * SLOT_B);
+      unsigned char *dw = lbase + (L::kRowW * RB + fetch_ring * SLOT_B);
+      unsigned char *dr = lbase + (L::kRowR * RB + fetch_ring * SLOT_B);
 #pragma unroll
       for (int k4 = 0; k4 < 2 * RPL / 4; ++k4) {
         const int4 x = ip[k4];
@@ -249,9 +264,9 @@ __global__ void __launch_bounds__(128) sparse_scan_kernel(const ScanArgs a) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int k = 4 * k4 + e;
-          const int j = r + 4 * (k < RPL ? k : k - RPL);
+          const int j = r + RG * (k < RPL ? k : k - RPL);
           if (static_cast<unsigned>(ids[e]) < static_cast<unsigned>(a.N))
-            cp_async<16>((k < RPL ? dw : dr) + j * 128, table + static_cast<size_t>(ids[e]) * rowbytes);
+            cp_async<16>((k < RPL ? dw : dr) + j * RB, table + static_cast<size_t>(ids[e]) * rowbytes);
         }
       }
     }
@@ -285,7 +300,7 @@ __global__ void __launch_bounds__(128) sparse_scan_kernel(const ScanArgs a) {
 
     const Rec &m = recs[cur_rec];
     const float al = m.alpha, be = m.beta;
-    const uint32_t *vw = vbuf + cur_rec * 32;
+    const uint32_t *vw = vbuf + cur_rec * TW;
     float4 vv;
     if (a.v_bf16) {
       const uint2 w2 = *reinterpret_cast<const uint2 *>(vw + 2 * q);
@@ -299,24 +314,35 @@ __global__ void __launch_bounds__(128) sparse_scan_kernel(const ScanArgs a) {
     float my_w[2 * RPL];
     int my_src[2 * RPL];
 #pragma unroll
-    for (int k = 0; k < RPL; k += 4) {
+    for (int k = 0; k < RPL; k += 4) {  // the first RPL of the lane's positions are its write slots
       const int4 x = *reinterpret_cast<const int4 *>(m.idx + r * 2 * RPL + k);
-      my_idx[k] = x.x; my_idx[k + 1] = x.y; my_idx[k + 2] = x.z; my_idx[k + 3] = x.w;
+      const int xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (k + e < RPL) my_idx[k + e] = xs[e];
     }
 #pragma unroll
     for (int k = 0; k < 2 * RPL; k += 4) {
       const float4 x = *reinterpret_cast<const float4 *>(m.w + r * 2 * RPL + k);
       my_w[k] = x.x; my_w[k + 1] = x.y; my_w[k + 2] = x.z; my_w[k + 3] = x.w;
     }
+    if constexpr (2 * RPL % 8 == 0) {
 #pragma unroll
-    for (int k = 0; k < 2 * RPL; k += 8) {
-      const uint4 x = *reinterpret_cast<const uint4 *>(m.src + r * 2 * RPL + k);
-      const uint32_t u[4] = {x.x, x.y, x.z, x.w};
+      for (int k = 0; k < 2 * RPL; k += 8) {
+        const uint4 x = *reinterpret_cast<const uint4 *>(m.src + r * 2 * RPL + k);
+        const uint32_t u[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        my_src[k + 2 * e] = static_cast<int>(u[e] & 0xffff);
-        my_src[k + 2 * e + 1] = static_cast<int>(u[e] >> 16);
+        for (int e = 0; e < 4; ++e) {
+          my_src[k + 2 * e] = static_cast<int>(u[e] & 0xffff);
+          my_src[k + 2 * e + 1] = static_cast<int>(u[e] >> 16);
+        }
       }
+    } else {
+      const uint2 x = *reinterpret_cast<const uint2 *>(m.src + r * 2 * RPL);
+      my_src[0] = static_cast<int>(x.x & 0xffff);
+      my_src[1] = static_cast<int>(x.x >> 16);
+      my_src[2] = static_cast<int>(x.y & 0xffff);
+      my_src[3] = static_cast<int>(x.y >> 16);
     }
 
     // selective decay of the written rows and the shared prediction (Fig. 2)
@@ -324,10 +350,10 @@ __global__ void __launch_bounds__(128) sparse_scan_kernel(const ScanArgs a) {
     float4 vh = zero4;
 #pragma unroll
     for (int k = 0; k < RPL; ++k) md[k] = ld4(row_ptr(my_src[k]));
-    if (LOG) {  // the undo log: write slot j = r + 4k before the decay
+    if (LOG) {  // the undo log: write slot j = r + RG k before the decay
 #pragma unroll
       for (int k = 0; k < RPL; ++k)
-        if (active && r + 4 * k < a.W) st4(undo_out + static_cast<long>(r + 4 * k) * d_v, md[k]);
+        if (active && r + RG * k < a.W) st4(undo_out + static_cast<long>(r + RG * k) * d_v, md[k]);
       undo_out += undo_step;
     }
     // read rows; a read of a row this token writes is patched below
@@ -346,17 +372,17 @@ __global__ void __launch_bounds__(128) sparse_scan_kernel(const ScanArgs a) {
       if (MODE == SDM_RESID_SHARED) vh = fma4(my_w[k], md[k], vh);
     }
     float4 base4 = vv;
-    if (MODE == SDM_RESID_SHARED) base4 = sub4(vv, xsum4(vh));
+    if (MODE == SDM_RESID_SHARED) base4 = sub4(vv, xsum4<Q>(vh));
     auto new_row = [&](float4 mdk, float gk) -> float4 {
       return fma4(gk, MODE == SDM_RESID_PERSLOT ? sub4(vv, mdk) : base4, mdk);
     };
 
     // delta write: history ring (forwarding source) and the table in HBM
-    unsigned char *hslot = lbase + (L::kRowH * 128 + cur_ring * SLOT_B);
+    unsigned char *hslot = lbase + (L::kRowH * RB + cur_ring * SLOT_B);
 #pragma unroll
     for (int k = 0; k < RPL; ++k) {
       const float4 nw = new_row(md[k], be * my_w[k]);
-      st4(reinterpret_cast<float *>(hslot + (r + 4 * k) * 128), nw);
+      st4(reinterpret_cast<float *>(hslot + (r + RG * k) * RB), nw);
       const int i = my_idx[k];
       if (active && static_cast<unsigned>(i) < static_cast<unsigned>(a.N))
         st4(reinterpret_cast<float *>(table_w + static_cast<size_t>(i) * rowbytes), nw);
@@ -367,8 +393,8 @@ __global__ void __launch_bounds__(128) sparse_scan_kernel(const ScanArgs a) {
       for (int k = 0; k < RPL; ++k) {
         const int code = my_src[RPL + k];
         if (code & kRecompute) {
-          const int sw = code & 0xff;                     // write slot of this token
-          const int ps = (sw & 3) * 2 * RPL + (sw >> 2);  // its record position
+          const int sw = code & 0xff;                       // write slot of this token
+          const int ps = (sw % RG) * 2 * RPL + (sw / RG);  // its record position
           xr[k] = new_row(mul4(al, ld4(row_ptr(m.src[ps]))), be * m.w[ps]);
         }
       }
@@ -377,7 +403,7 @@ __global__ void __launch_bounds__(128) sparse_scan_kernel(const ScanArgs a) {
     float4 yp = zero4;
 #pragma unroll
     for (int k = 0; k < RPL; ++k) yp = fma4(my_w[RPL + k], xr[k], yp);
-    yp = xsum4(yp);
+    yp = xsum4<Q>(yp);
     if (r == 0 && active) st4(yp_out, yp);
     yp_out += y_step;
     cur_rec = cur_rec + 1 == L::NM ? 0 : cur_rec + 1;
@@ -391,18 +417,22 @@ int env_int(const char *name, int dflt) {
   return (s && *s) ? atoi(s) : dflt;
 }
 
-template <int P, int SLOTS>
-size_t warp_bytes() { return ScanLayout<P, SLOTS>::kWarpBytes; }
+template <int P, int SLOTS, int TW>
+size_t warp_bytes() { return ScanLayout<P, SLOTS, TW>::kWarpBytes; }
 
-size_t warp_bytes_dispatch(int slots, int P) {
-  if (slots == 16) return P == 4 ? warp_bytes<4, 16>() : P == 6 ? warp_bytes<6, 16>() : warp_bytes<8, 16>();
-  return P == 4 ? warp_bytes<4, 64>() : 0;
+size_t warp_bytes_dispatch(int slots, int P, int tw) {
+  if (slots == 16 && tw == 32)
+    return P == 4 ? warp_bytes<4, 16, 32>() : P == 6 ? warp_bytes<6, 16, 32>() : warp_bytes<8, 16, 32>();
+  if (slots == 16 && tw == 16)
+    return P == 4 ? warp_bytes<4, 16, 16>() : P == 6 ? warp_bytes<6, 16, 16>() : warp_bytes<8, 16, 16>();
+  return (P == 4 && tw == 32) ? warp_bytes<4, 64, 32>() : 0;
 }
 
-template <int P, int SLOTS, int MODE>
+template <int P, int SLOTS, int TW, int MODE>
 int launch_scan(const ScanArgs &args, int wpc, cudaStream_t st) {
-  const size_t smem = ScanLayout<P, SLOTS>::kWarpBytes * wpc;
-  auto kern = args.undo ? sparse_scan_kernel<P, SLOTS, MODE, true> : sparse_scan_kernel<P, SLOTS, MODE, false>;
+  const size_t smem = ScanLayout<P, SLOTS, TW>::kWarpBytes * wpc;
+  auto kern =
+      args.undo ? sparse_scan_kernel<P, SLOTS, TW, MODE, true> : sparse_scan_kernel<P, SLOTS, TW, MODE, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)
     return check_launch("sdm_scan: set shared memory");
@@ -411,19 +441,22 @@ int launch_scan(const ScanArgs &args, int wpc, cudaStream_t st) {
   return check_launch("sdm_scan: scan kernel");
 }
 
-template <int P, int SLOTS>
+template <int P, int SLOTS, int TW>
 int launch_mode(int mode, const ScanArgs &args, int wpc, cudaStream_t st) {
-  if (mode == SDM_RESID_SHARED) return launch_scan<P, SLOTS, SDM_RESID_SHARED>(args, wpc, st);
-  if (mode == SDM_RESID_PERSLOT) return launch_scan<P, SLOTS, SDM_RESID_PERSLOT>(args, wpc, st);
-  return launch_scan<P, SLOTS, SDM_RESID_ADDITIVE>(args, wpc, st);
+  if (mode == SDM_RESID_SHARED) return launch_scan<P, SLOTS, TW, SDM_RESID_SHARED>(args, wpc, st);
+  if (mode == SDM_RESID_PERSLOT) return launch_scan<P, SLOTS, TW, SDM_RESID_PERSLOT>(args, wpc, st);
+  return launch_scan<P, SLOTS, TW, SDM_RESID_ADDITIVE>(args, wpc, st);
 }
 
-int launch_dispatch(int slots, int P, int mode, const ScanArgs &args, int wpc, cudaStream_t st) {
-  if (slots == 16 && P == 4) return launch_mode<4, 16>(mode, args, wpc, st);
-  if (slots == 16 && P == 6) return launch_mode<6, 16>(mode, args, wpc, st);
-  if (slots == 16 && P == 8) return launch_mode<8, 16>(mode, args, wpc, st);
-  if (slots == 64 && P == 4) return launch_mode<4, 64>(mode, args, wpc, st);
-  return set_error(SDM_ERR_UNSUPPORTED, "sdm_scan: no kernel for slots=%d window=%d", slots, P);
+int launch_dispatch(int slots, int P, int tw, int mode, const ScanArgs &args, int wpc, cudaStream_t st) {
+  if (slots == 16 && tw == 32 && P == 4) return launch_mode<4, 16, 32>(mode, args, wpc, st);
+  if (slots == 16 && tw == 32 && P == 6) return launch_mode<6, 16, 32>(mode, args, wpc, st);
+  if (slots == 16 && tw == 32 && P == 8) return launch_mode<8, 16, 32>(mode, args, wpc, st);
+  if (slots == 16 && tw == 16 && P == 4) return launch_mode<4, 16, 16>(mode, args, wpc, st);
+  if (slots == 16 && tw == 16 && P == 6) return launch_mode<6, 16, 16>(mode, args, wpc, st);
+  if (slots == 16 && tw == 16 && P == 8) return launch_mode<8, 16, 16>(mode, args, wpc, st);
+  if (slots == 64 && tw == 32 && P == 4) return launch_mode<4, 64, 32>(mode, args, wpc, st);
+  return set_error(SDM_ERR_UNSUPPORTED, "sdm_scan: no kernel for slots=%d window=%d tile=%d", slots, P, tw);
 }
 
 size_t record_bytes(int W, int R) { return pick_slots(W, R) == 16 ? rec_bytes<16>() : rec_bytes<64>(); }
@@ -465,46 +498,56 @@ static int scan_core(float *state, const void *v, int v_dtype, const float *alph
     return set_error(SDM_ERR_INVALID_ARG, "sdm_scan: workspace of %zu bytes needed", need);
   if (!aligned(workspace, 16)) return set_error(SDM_ERR_ALIGN, "sdm_scan: workspace must be 16-byte aligned");
 
-  // Launch shape: B*H*ceil(d_v/32) independent warps.  Each runs the whole
-  // sequence, so all must be resident at once; take the deepest prefetch
-  // window whose shared-memory rings still let every warp fit in one wave.
+  // Launch shape: B*H*ceil(d_v/TW) independent warps.  Each runs the whole
+  // sequence, so all must be resident at once.  Per-warp speed is bound by
+  // its own per-token chain, so more warps (16-column tiles) go first; for
+  // each tile width take the deepest prefetch window whose shared-memory rings
+  // still let every warp fit in one wave.  SDM_SCAN_TILE / SDM_SCAN_WINDOW /
+  // SDM_SCAN_WARPS force a choice.
   const int slots = pick_slots(W, R);
   int dev = 0, smem_blk = 0, smem_sm = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&smem_blk, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int tiles = (d_v + 31) / 32;
-  const long total_warps = static_cast<long>(B) * H * tiles;
-  const int want_window = env_int("SDM_SCAN_WINDOW", 0);
-  int window = 0, wpc = 1;
-  for (int p : {8, 6, 4}) {
-    if (want_window && p != want_window) continue;
-    const size_t wb = warp_bytes_dispatch(slots, p);
-    if (wb == 0 || wb > static_cast<size_t>(smem_blk)) continue;
-    for (int c : {4, 2, 1}) {  // warps per CTA
-      if (c * wb > static_cast<size_t>(smem_blk)) continue;
-      const long ctas_sm = static_cast<long>(smem_sm) / static_cast<long>(c * wb + 1024);
-      if (window == 0) { window = p; wpc = c; }  // fallback: the first that fits at all
-      if (ctas_sm >= 1 && total_warps <= ctas_sm * c * sms) { window = p; wpc = c; goto chosen; }
+  const int want_window = env_int("SDM_SCAN_WINDOW", 0), want_tile = env_int("SDM_SCAN_TILE", 0);
+  int window = 0, wpc = 1, tw = 0;
+  for (int w_t : {16, 32}) {
+    if (want_tile && w_t != want_tile) continue;
+    const long warps_t = static_cast<long>(B) * H * ((d_v + w_t - 1) / w_t);
+    for (int p : {8, 6, 4}) {
+      if (want_window && p != want_window) continue;
+      const size_t wb = warp_bytes_dispatch(slots, p, w_t);
+      if (wb == 0 || wb > static_cast<size_t>(smem_blk)) continue;
+      for (int c : {4, 2, 1}) {  // warps per CTA
+        if (c * wb > static_cast<size_t>(smem_blk)) continue;
+        const long ctas_sm = static_cast<long>(smem_sm) / static_cast<long>(c * wb + 1024);
+        if (window == 0) { window = p; wpc = c; tw = w_t; }  // fallback: the first that fits at all
+        if (ctas_sm >= 1 && warps_t <= ctas_sm * c * sms) { window = p; wpc = c; tw = w_t; goto chosen; }
+      }
     }
   }
 chosen:
   if (window == 0) return set_error(SDM_ERR_SHAPE, "sdm_scan: W/R too large for shared memory");
   wpc = env_int("SDM_SCAN_WARPS", wpc);
-  if (wpc < 1 || static_cast<size_t>(wpc) * warp_bytes_dispatch(slots, window) > static_cast<size_t>(smem_blk))
+  if (wpc < 1 || static_cast<size_t>(wpc) * warp_bytes_dispatch(slots, window, tw) > static_cast<size_t>(smem_blk))
     return set_error(SDM_ERR_INVALID_ARG, "sdm_scan: SDM_SCAN_WARPS does not fit");
+  const int tiles = (d_v + tw - 1) / tw;
+  const long total_warps = static_cast<long>(B) * H * tiles;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const long total = static_cast<long>(B) * T * H * 2 * slots;
   const unsigned rblocks = static_cast<unsigned>((total + 255) / 256);
-#define SDM_REC(PP, S)                                                                                          \
-  record_kernel<PP, S><<<rblocks, 256, 0, st>>>(idx_w, w_w, idx_r, w_r, alpha, beta, W, R, T, H, N, total, \
-                                                static_cast<TokenRec<S> *>(workspace), dev_err)
-  if (slots == 16 && window == 4) SDM_REC(4, 16);
-  else if (slots == 16 && window == 6) SDM_REC(6, 16);
-  else if (slots == 16 && window == 8) SDM_REC(8, 16);
-  else SDM_REC(4, 64);
+#define SDM_REC(PP, S, TT)                                                                                       \
+  record_kernel<PP, S, TT><<<rblocks, 256, 0, st>>>(idx_w, w_w, idx_r, w_r, alpha, beta, W, R, T, H, N, total, \
+                                                    static_cast<TokenRec<S> *>(workspace), dev_err)
+  if (slots == 16 && tw == 32 && window == 4) SDM_REC(4, 16, 32);
+  else if (slots == 16 && tw == 32 && window == 6) SDM_REC(6, 16, 32);
+  else if (slots == 16 && tw == 32 && window == 8) SDM_REC(8, 16, 32);
+  else if (slots == 16 && tw == 16 && window == 4) SDM_REC(4, 16, 16);
+  else if (slots == 16 && tw == 16 && window == 6) SDM_REC(6, 16, 16);
+  else if (slots == 16 && tw == 16 && window == 8) SDM_REC(8, 16, 16);
+  else SDM_REC(4, 64, 32);
 #undef SDM_REC
   int rc = check_launch("sdm_scan: record kernel");
   if (rc != SDM_OK) return rc;
@@ -523,7 +566,7 @@ chosen:
   args.total_warps = total_warps;
   args.undo = undo;
   args.W = W;
-  return launch_dispatch(slots, window, resid_mode, args, wpc, st);
+  return launch_dispatch(slots, window, tw, resid_mode, args, wpc, st);
 }
 
 extern "C" int sdm_scan(float *state, const void *v, int v_dtype, const float *alpha, const float *beta,

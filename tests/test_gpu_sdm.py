@@ -118,14 +118,16 @@ def test_scan_tiny_full_pipeline(gmode, omode):
 
 @pytest.mark.parametrize("d_v", [36, 68, 132])
 @pytest.mark.parametrize("window", [4, 6, 8])
+@pytest.mark.parametrize("tile", [16, 32])
 @pytest.mark.parametrize("gmode,omode", MODES)
-def test_scan_hazard_stress(monkeypatch, d_v, window, gmode, omode):
+def test_scan_hazard_stress(monkeypatch, d_v, window, tile, gmode, omode):
     """Tiny tables with W = R = 16: rows are rewritten by almost every token,
     so nearly every slot is forwarded from the history ring.  Ragged d_v (a
     partial last column tile), random nonzero initial state, every compiled
-    prefetch window."""
+    prefetch window and both column-tile widths."""
     sdm = need_gpu()
     monkeypatch.setenv("SDM_SCAN_WINDOW", str(window))
+    monkeypatch.setenv("SDM_SCAN_TILE", str(tile))
     for sq, k, seed in ((4, 4, 1), (8, 8, 2)):
         sh = synth.SdmShape("stress", B=2, T=97, H=3, sqrtN=sq, d_v=d_v, k=k, W=16, R=16, v_bf16=False)
         inp = synth.sdm_inputs(sh, seed=seed)
