@@ -42,7 +42,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 NCU_TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of one full-size launch
     # (8.01 GB + 4.19 GB), profiles/sparse_scan_1.4b_layer.md
-    ("sdm_14b_layer", "sdm"): {"bytes": 12.20e9, "digest": "651ec4880368"},
+    ("sdm_14b_layer", "sdm"): {"bytes": 12.20e9, "digest": "bcc6a3a96443"},
     # both kernels of one full-size gdn_scan call (746.4 MB + 590.5 MB), profiles/gdn_chunk_dense.md
     ("gdn", "gdn"): {"bytes": 1.337e9, "digest": "4469700d7705"},
     # the five kernels of one full-size sse_scan call on the chunked path (1.072 GB read + 0.799 GB
