@@ -26,6 +26,7 @@
 // fp32-level accuracy.  Decay ratios are always formed as exp(l_i - l_j) with
 // j <= i.
 #include <climits>
+#include <cstdlib>
 
 #include "common.cuh"
 #include "umma.cuh"
@@ -400,6 +401,7 @@ struct ChainArgs {
   const float *gC;
   float *y;
   int T, H, nchunks;
+  int drop_signal;  // test hook: the first X-done signal is never sent, so the workers' bounded wait runs out
   int32_t *err;
 };
 
@@ -561,7 +563,7 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
     auto mma = [&](uint32_t d, uint64_t A, uint64_t Bm, int ks, uint32_t idesc, bool acc, uint32_t bstep = 16u) {
       mma_bf16(d, A + 16u * ks, Bm + bstep * ks, idesc, acc);
     };
-    int w_issued = 0, w_done = 0, m_issued = 0, m_done = 0, g_issued = 0, g_done = 0;
+    int w_issued = 0, w_done = 0, m_issued = 0, m_done = 0, g_issued = 0;
     auto load = [&](int which, int c) {
       const unsigned char *src = a.ws + (u0 + c) * kUnit;
       fence_async_smem();
@@ -605,7 +607,7 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
           mma(tmem + kColX, dSh, dWl, ks, id64w, true);
           mma(tmem + kColX, dSl, dWh, ks, id64w, true);
         }
-        if (g == 1) mma_commit(bar(4));
+        if (g == 1 && !(a.drop_signal && c == 0)) mma_commit(bar(4));
 #pragma unroll
         for (int ks = g; ks < 8; ks += 2) {
           mma(tmem + kColY1, dSh, dQ, ks, id64, ks != 0);
@@ -641,16 +643,20 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
         if (ok) load(1, c + 1);
       }
     }
-    if (!ok || *abort_flag) {
-      // stop cleanly: wait (bounded) for the MMAs and the bulk copies in flight
-      mma_commit(bar(11));
-      mbar_wait(bar(11), 0, kWaitLimit);
-      while (w_done < w_issued) mbar_wait(bar(0), static_cast<uint32_t>(w_done++ & 1), kWaitLimit);
-      while (m_done < m_issued) mbar_wait(bar(1), static_cast<uint32_t>(m_done++ & 1), kWaitLimit);
-      for (; g_done < g_issued; ++g_done)
-        mbar_wait(bar(2 + (g_done & 1)), static_cast<uint32_t>((g_done >> 1) & 1), kWaitLimit);
-      *abort_flag = 1;
+    // every MMA issued has completed before tensor memory is freed (also when
+    // a worker's wait ran out after this loop ended) ...
+    mma_commit(bar(11));
+    mbar_wait(bar(11), 0, kWaitLimit);
+    // ... and every bulk copy has landed before the CTA exits: at most the last
+    // copy into each buffer can be unobserved (bounded waits; in the normal
+    // path all have been seen complete already)
+    if (w_done < w_issued) mbar_wait(bar(0), static_cast<uint32_t>((w_issued - 1) & 1), kWaitLimit);
+    if (m_done < m_issued) mbar_wait(bar(1), static_cast<uint32_t>((m_issued - 1) & 1), kWaitLimit);
+    for (int gb = 0; gb < 2; ++gb) {
+      const int loads = (g_issued + 1 - gb) / 2;  // gamma copies issued into buffer gb
+      if (loads > 0) mbar_wait(bar(2 + gb), static_cast<uint32_t>((loads - 1) & 1), kWaitLimit);
     }
+    if (!ok) *abort_flag = 1;
   }
   tc_fence_before();
   __syncthreads();
@@ -666,6 +672,15 @@ size_t gdn_chunk_workspace_size(int B, int T, int H) {
   const long units = static_cast<long>(B) * H * ((T + kC - 1) / kC);
   const size_t n = static_cast<size_t>(units) * (kUnit + sizeof(float));
   return (n + 255) & ~static_cast<size_t>(255);
+}
+
+// Test hook for the failure path: SDM_TEST_DROP_SIGNAL=1 makes the chain
+// kernels skip one mbarrier signal, so a bounded on-device wait runs out and
+// the call reports SDM_DEVERR_TIMEOUT (outputs invalid) with the context
+// still usable.  Read per call; off unless set.
+int test_drop_signal() {
+  const char *s = getenv("SDM_TEST_DROP_SIGNAL");
+  return (s && s[0] == '1') ? 1 : 0;
 }
 
 // launched by gdn_scan for dense GDN with d_k = d_v = 128
@@ -711,6 +726,7 @@ int launch_gdn_chunk(float *state, const uint16_t *q, const uint16_t *k, const u
   ca.H = H;
   ca.nchunks = nchunks;
   ca.err = err;
+  ca.drop_signal = test_drop_signal();
   if (cudaFuncSetAttribute(gdn_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kChainSmem)) != cudaSuccess)
     return check_launch("gdn_scan: set shared memory");

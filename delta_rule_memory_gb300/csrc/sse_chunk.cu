@@ -526,6 +526,7 @@ struct ChainArgs {
   float *stage;
   int T, N, umax;
   long bh_count, gwords;
+  int drop_signal;  // test hook: the first unit's MMA-done signal is never sent (bounded waits run out)
   int32_t *err;
 };
 
@@ -711,7 +712,7 @@ __global__ void __maxnreg__(96) sse_chain_kernel(const ChainArgs a) {
         mma_bf16(tO, dSh + 16u * ks, dQl + 16u * ks, idO, true);
         mma_bf16(tO, dSl + 16u * ks, dQh + 16u * ks, idO, true);
       }
-      mma_commit(bar(kBarMma));
+      if (!(a.drop_signal && c == 0)) mma_commit(bar(kBarMma));
       if (c + 1 < n) {
         // unit c+1's tiles into the other buffers once the workers are done with unit c-1
         if (c >= 1) ok = wait(kBarFree + (b ^ 1), static_cast<uint32_t>(((c - 1) >> 1) & 1));
@@ -721,18 +722,19 @@ __global__ void __maxnreg__(96) sse_chain_kernel(const ChainArgs a) {
         if (ok) load_x(c + 1);
       }
     }
-    if (!ok || *abort_flag) {
-      // stop cleanly: wait (bounded) for the MMAs and the bulk copies in flight
-      mma_commit(bar(kBarDrain));
-      mbar_wait(bar(kBarDrain), 0, kWaitLimit);
-      if (x_done < x_issued) mbar_wait(bar(kBarX), static_cast<uint32_t>((x_issued - 1) & 1), kWaitLimit);
-      for (int bb = 0; bb < 2; ++bb) {
-        if (y_done[bb] < y_issued[bb])
-          mbar_wait(bar(kBarY + bb), static_cast<uint32_t>((y_issued[bb] - 1) & 1), kWaitLimit);
-        if (z_issued[bb] > 0) mbar_wait(bar(kBarZ + bb), static_cast<uint32_t>((z_issued[bb] - 1) & 1), kWaitLimit);
-      }
-      *abort_flag = 1;
+    // every MMA issued has completed before tensor memory is freed (also when
+    // a worker's wait ran out after this loop ended)
+    mma_commit(bar(kBarDrain));
+    mbar_wait(bar(kBarDrain), 0, kWaitLimit);
+    // and every bulk copy has landed before the CTA exits (bounded waits; in
+    // the normal path they have all been seen complete already)
+    if (x_done < x_issued) mbar_wait(bar(kBarX), static_cast<uint32_t>((x_issued - 1) & 1), kWaitLimit);
+    for (int bb = 0; bb < 2; ++bb) {
+      if (y_done[bb] < y_issued[bb])
+        mbar_wait(bar(kBarY + bb), static_cast<uint32_t>((y_issued[bb] - 1) & 1), kWaitLimit);
+      if (z_issued[bb] > 0) mbar_wait(bar(kBarZ + bb), static_cast<uint32_t>((z_issued[bb] - 1) & 1), kWaitLimit);
     }
+    if (!ok) *abort_flag = 1;
   }
   tc_fence_before();
   __syncthreads();
@@ -779,6 +781,8 @@ size_t sse_chunk_workspace_size(int B, int T, int H, int N, int topk) {
 bool sse_chunk_supported(int write_mode, int N, int topk, int c, int d) {
   return write_mode == SSE_WRITE_ADDITIVE && c == kCh && d == kD && N <= kMaxN && topk <= kMaxTopk;
 }
+
+int test_drop_signal();  // gdn_chunk.cu: the SDM_TEST_DROP_SIGNAL test hook
 
 // launched by sse_scan after the routing prepass (rec: the routing records;
 // chunk_ws: sse_chunk_workspace_size bytes, 256-byte aligned)
@@ -835,6 +839,7 @@ int launch_sse_chunk(float *state, const uint32_t *rec, int rw, const float *klo
   ca.bh_count = bhn;
   ca.gwords = gwords;
   ca.err = err;
+  ca.drop_signal = test_drop_signal();
   if (cudaFuncSetAttribute(sse_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kChainSmem)) != cudaSuccess)
     return check_launch("sse_scan: set shared memory");

@@ -1,0 +1,71 @@
+"""Failure detection on the GPU without a fault: the tensor-core chain kernels
+bound every mbarrier wait, and when one runs out they drain their MMAs and
+copies, free tensor memory, return normally and report SDM_DEVERR_TIMEOUT in
+the caller's error word.  SDM_TEST_DROP_SIGNAL=1 makes the chain skip one
+signal (a flag that nothing then sets), so a wait runs out on purpose; the
+next call on the same context must still be exact."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import assert_state_close, assert_y_close, dev, host, need_gpu
+
+pytestmark = pytest.mark.gpu
+
+SDM_DEVERR_TIMEOUT = 8
+
+
+def _gdn(sdm, S0, inp):
+    import torch
+    state = dev(S0)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y = sdm.gdn_scan(state, dev(inp["q"]), dev(inp["k"]), dev(inp["v"]), dev(inp["alpha_gdn"]), dev(inp["beta"]),
+                     False, dev_err=err)
+    torch.cuda.synchronize()
+    return host(state), host(y), int(host(err)[0])
+
+
+def _sse(sdm, S0, inp, topk):
+    import torch
+    state = dev(S0)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y = sdm.sse_scan(state, dev(inp["route"]), topk, dev(inp["klog"]), dev(inp["q"]), dev(inp["v"]),
+                     dev(inp["alpha"]), dev_err=err)
+    torch.cuda.synchronize()
+    return host(state), host(y), int(host(err)[0])
+
+
+def test_gdn_chain_wait_runs_out_and_the_context_stays_usable(monkeypatch):
+    sdm = need_gpu()
+    monkeypatch.setenv("SDM_GDN_PATH", "chunk")
+    sh = synth.GDN_DENSE.with_(B=1, T=200, H=2)
+    inp = synth.gdn_inputs(sh, seed=90)
+    S0 = synth.random_state((1, 2, 128, 128), seed=91, scale=0.3)
+    monkeypatch.setenv("SDM_TEST_DROP_SIGNAL", "1")
+    _, _, err = _gdn(sdm, S0, inp)
+    assert err & SDM_DEVERR_TIMEOUT
+    monkeypatch.delenv("SDM_TEST_DROP_SIGNAL")
+    S, y, err = _gdn(sdm, S0, inp)
+    assert err == 0
+    Sr, yr = oracle.gdn_scan(S0, inp["q"], inp["k"], inp["v"], inp["alpha_gdn"], inp["beta"], False)
+    assert_y_close(y, yr)
+    assert_state_close(S, Sr)
+
+
+def test_sse_chain_wait_runs_out_and_the_context_stays_usable(monkeypatch):
+    sdm = need_gpu()
+    monkeypatch.setenv("SDM_SSE_PATH", "chunk")
+    sh = synth.SSE_PART.with_(B=1, T=200, H=2)
+    inp = synth.sse_inputs(sh, seed=92)
+    S0 = synth.random_state((1, 2, sh.N + 1, 128, 128), seed=93, scale=0.5)
+    monkeypatch.setenv("SDM_TEST_DROP_SIGNAL", "1")
+    _, _, err = _sse(sdm, S0, inp, sh.topk)
+    assert err & SDM_DEVERR_TIMEOUT
+    monkeypatch.delenv("SDM_TEST_DROP_SIGNAL")
+    S, y, err = _sse(sdm, S0, inp, sh.topk)
+    assert err == 0
+    Sr, yr, _ = oracle.sse_scan(S0, inp["route"], sh.topk, inp["klog"], inp["q"], inp["v"], inp["alpha"])
+    assert_y_close(y, yr)
+    assert_state_close(S, Sr)
+    assert np.all(np.isfinite(S))
