@@ -44,10 +44,10 @@ NCU_TRAFFIC = {
     # (8.01 GB + 4.19 GB), profiles/sparse_scan_1.4b_layer.md
     ("sdm_14b_layer", "sdm"): {"bytes": 12.20e9, "digest": "bcc6a3a96443"},
     # both kernels of one full-size gdn_scan call (746.4 MB + 590.5 MB), profiles/gdn_chunk_dense.md
-    ("gdn", "gdn"): {"bytes": 1.337e9, "digest": "4469700d7705"},
+    ("gdn", "gdn"): {"bytes": 1.337e9, "digest": "e2c62e1f689e"},
     # the five kernels of one full-size sse_scan call on the chunked path (1.072 GB read + 0.799 GB
     # written), profiles/sse_chunk_prefill.md
-    ("sse", "sse"): {"bytes": 1.871e9, "digest": "c7400c3e5885"},
+    ("sse", "sse"): {"bytes": 1.870e9, "digest": "2c3458fbad0b"},
 }
 
 
