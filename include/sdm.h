@@ -64,6 +64,23 @@ extern "C" {
 #define SDM_DEVERR_NONFINITE 4    /* a NaN or infinite score or logit */
 #define SDM_DEVERR_TIMEOUT 8      /* a bounded on-device wait gave up; outputs invalid */
 
+/*
+ * Environment variables read at each call (all optional; unset = the library's
+ * own choice):
+ *   SDM_SCAN_TILE=16|32, SDM_SCAN_WINDOW=4|6|8, SDM_SCAN_WARPS=1..4
+ *       sdm_scan / sdm_scan_train: column-tile width, prefetch window and warps
+ *       per CTA of the scan kernel (default: the 16-column tile if every warp
+ *       fits in one wave, then the deepest window that does, 4 warps per CTA).
+ *   SDM_GDN_PATH=recurrent|chunk    gdn_scan: force the token-recurrent or the
+ *       chunked tensor-core path (shape rules permitting).
+ *   SDM_SSE_PATH=recurrent|chunk    sse_scan: force the token-by-token or the
+ *       chunked prefill path (shape rules permitting).
+ *   SDM_TEST_DROP_SIGNAL=1          test hook: the chunked GDN and SSE chain
+ *       kernels skip one internal signal, so a bounded on-device wait runs out
+ *       and the call reports SDM_DEVERR_TIMEOUT (its outputs are invalid; the
+ *       CUDA context stays usable).  Never set in normal use.
+ */
+
 /* Element types of the value input of sdm_scan. */
 #define SDM_DTYPE_F32 0
 #define SDM_DTYPE_BF16 1
