@@ -253,26 +253,24 @@ __global__ void __launch_bounds__(kPThreads, 2) sse_prep_kernel(const PrepArgs a
     unsigned char *unit = a.units + ug * kXUnit;
 
     // ---- q, key logits, alpha rows (padding: q = 0, logits 0, alpha = 1)
-    for (int id = tid; id < kC * 80; id += kPThreads) {
-      const int i = id / 80, k = id - i * 80;
+    for (int id = tid; id < kC * 16; id += kPThreads) {  // q: 16 pieces per row
+      const int i = id >> 4, k = id & 15;
       const long tk = rtok[i];
-      void *dst;
-      const void *src;
-      if (k < 16) {
-        dst = sq + i * kCh + 8 * k;
-        src = a.q + tk * kCh + 8 * k;
-      } else if (k < 48) {
-        dst = skk + i * kLdA + 4 * (k - 16);
-        src = a.klog + tk * kCh + 4 * (k - 16);
+      uint16_t *dst = sq + i * kCh + 8 * k;
+      if (tk >= 0) cp_async<16>(dst, a.q + tk * kCh + 8 * k);
+      else *reinterpret_cast<uint4 *>(dst) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    for (int id = tid; id < kC * 32; id += kPThreads) {  // key logits and alpha: 32 pieces per row each
+      const int i = id >> 5, k = id & 31;
+      const long tk = rtok[i];
+      float *dk = skk + i * kLdA + 4 * k, *da = sal + i * kLdA + 4 * k;
+      if (tk >= 0) {
+        cp_async<16>(dk, a.klog + tk * kCh + 4 * k);
+        cp_async<16>(da, a.alpha + tk * kCh + 4 * k);
       } else {
-        dst = sal + i * kLdA + 4 * (k - 48);
-        src = a.alpha + tk * kCh + 4 * (k - 48);
+        *reinterpret_cast<uint4 *>(dk) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<float4 *>(da) = make_float4(1.f, 1.f, 1.f, 1.f);
       }
-      if (tk >= 0)
-        cp_async<16>(dst, src);
-      else
-        *reinterpret_cast<uint4 *>(dst) = k < 48 ? make_uint4(0u, 0u, 0u, 0u)
-                                                 : make_uint4(0x3f800000u, 0x3f800000u, 0x3f800000u, 0x3f800000u);
     }
     cp_async_commit();
     // V tile (8 values of d per 16 bytes, the K-tile layout) and the staging
@@ -493,9 +491,19 @@ __global__ void __launch_bounds__(kPThreads, 2) sse_prep_kernel(const PrepArgs a
       const float gi = rg[i];
       float x[8], y[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        x[e] = gi * sal[i * kLdA + r0 + e] * sPre[J * kCh + r0 + e];
-        y[e] = gi * skk[i * kLdA + r0 + e] * sSuf[J * kCh + r0 + e];
+      for (int h4 = 0; h4 < 8; h4 += 4) {  // 16-byte rows: kLdA and r0 are multiples of 4
+        const float4 qf = *reinterpret_cast<const float4 *>(sal + i * kLdA + r0 + h4);
+        const float4 pr = *reinterpret_cast<const float4 *>(sPre + J * kCh + r0 + h4);
+        const float4 kr = *reinterpret_cast<const float4 *>(skk + i * kLdA + r0 + h4);
+        const float4 sf = *reinterpret_cast<const float4 *>(sSuf + J * kCh + r0 + h4);
+        x[h4] = gi * qf.x * pr.x;
+        x[h4 + 1] = gi * qf.y * pr.y;
+        x[h4 + 2] = gi * qf.z * pr.z;
+        x[h4 + 3] = gi * qf.w * pr.w;
+        y[h4] = gi * kr.x * sf.x;
+        y[h4 + 1] = gi * kr.y * sf.y;
+        y[h4 + 2] = gi * kr.z * sf.z;
+        y[h4 + 3] = gi * kr.w * sf.w;
       }
       store_split8(unit + kXQ, unit + kXQ + 16384, kmajor_off(i, r0, kCh), x);
       store_split8(unit + kXK, unit + kXK + 16384, kmajor_off(i, r0, kCh), y);
