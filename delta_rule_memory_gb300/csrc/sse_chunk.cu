@@ -417,11 +417,14 @@ __global__ void __launch_bounds__(kPThreads, 2) sse_prep_kernel(const PrepArgs a
     __syncthreads();
 
     // ---- A, blocks below the diagonal: A_ij = sum_r qF_ir mid_r kkR_jr with
-    // mid = the whole blocks between J and I.  Thread: rows i0 = 16I + rp and
-    // i0 + 8, columns j0..j0+3 (the 8 lanes of a quarter-warp share the
-    // columns and read 8 rows 4 banks apart)
+    // mid = the whole blocks between J and I.  Thread pair (tid, tid^1): a
+    // 4 x 4 tile, rows 16I + rq + 4e, columns j0..j0+3, the two threads taking
+    // the float4 channel groups 8m + 4ch + u (ch = 0, 1), which puts the 8
+    // lanes of a quarter-warp (4 row offsets x 2 channel halves) on distinct
+    // banks
     if (tid < 192) {
-      const int rp = tid & 7, gq = tid >> 3;
+      const int ch = tid & 1, tt = tid >> 1;
+      const int rq = tt & 3, gq = tt >> 2;  // gq: (I, J, jq) as below, 24 of them
       int I, J, jq;
       if (gq < 4) {
         I = 1; J = 0; jq = gq;
@@ -430,46 +433,61 @@ __global__ void __launch_bounds__(kPThreads, 2) sse_prep_kernel(const PrepArgs a
       } else {
         I = 3; J = (gq - 12) >> 2; jq = (gq - 12) & 3;
       }
-      const int i0 = 16 * I + rp, j0 = 16 * J + 4 * jq;
+      const int i0 = 16 * I + rq, j0 = 16 * J + 4 * jq;
       const int gap = I - J;  // warp-uniform
       const float *m0 = sP + (J + 1) * kCh, *m1 = sP + (J + 2) * kCh;
-      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll 4
-      for (int k4 = 0; k4 < 32; ++k4) {
-        const float4 qa = *reinterpret_cast<const float4 *>(sal + i0 * kLdA + 4 * k4);
-        const float4 qb = *reinterpret_cast<const float4 *>(sal + (i0 + 8) * kLdA + 4 * k4);
-        float4 mid = make_float4(1.f, 1.f, 1.f, 1.f);
-        if (gap >= 2) mid = *reinterpret_cast<const float4 *>(m0 + 4 * k4);
-        if (gap == 3) {
-          const float4 m2 = *reinterpret_cast<const float4 *>(m1 + 4 * k4);
-          mid.x *= m2.x;
-          mid.y *= m2.y;
-          mid.z *= m2.z;
-          mid.w *= m2.w;
-        }
+      float acc[4][4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float4 kv = *reinterpret_cast<const float4 *>(skk + (j0 + e) * kLdA + 4 * k4);
-          if (gap >= 2) {
-            kv.x *= mid.x;
-            kv.y *= mid.y;
-            kv.z *= mid.z;
-            kv.w *= mid.w;
+      for (int e = 0; e < 4; ++e)
+#pragma unroll
+        for (int f = 0; f < 4; ++f) acc[e][f] = 0.f;
+#pragma unroll 2
+      for (int m = 0; m < 4; ++m) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int k4 = 8 * m + 4 * ch + u;
+          float4 mid = make_float4(1.f, 1.f, 1.f, 1.f);
+          if (gap >= 2) mid = *reinterpret_cast<const float4 *>(m0 + 4 * k4);
+          if (gap == 3) {
+            const float4 m2 = *reinterpret_cast<const float4 *>(m1 + 4 * k4);
+            mid.x *= m2.x;
+            mid.y *= m2.y;
+            mid.z *= m2.z;
+            mid.w *= m2.w;
           }
-          acc[0][e] = fmaf(qa.x, kv.x, acc[0][e]);
-          acc[0][e] = fmaf(qa.y, kv.y, acc[0][e]);
-          acc[0][e] = fmaf(qa.z, kv.z, acc[0][e]);
-          acc[0][e] = fmaf(qa.w, kv.w, acc[0][e]);
-          acc[1][e] = fmaf(qb.x, kv.x, acc[1][e]);
-          acc[1][e] = fmaf(qb.y, kv.y, acc[1][e]);
-          acc[1][e] = fmaf(qb.z, kv.z, acc[1][e]);
-          acc[1][e] = fmaf(qb.w, kv.w, acc[1][e]);
+          float4 kv[4];
+#pragma unroll
+          for (int f = 0; f < 4; ++f) {
+            kv[f] = *reinterpret_cast<const float4 *>(skk + (j0 + f) * kLdA + 4 * k4);
+            if (gap >= 2) {
+              kv[f].x *= mid.x;
+              kv[f].y *= mid.y;
+              kv[f].z *= mid.z;
+              kv[f].w *= mid.w;
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float4 qv = *reinterpret_cast<const float4 *>(sal + (i0 + 4 * e) * kLdA + 4 * k4);
+#pragma unroll
+            for (int f = 0; f < 4; ++f) {
+              acc[e][f] = fmaf(qv.x, kv[f].x, acc[e][f]);
+              acc[e][f] = fmaf(qv.y, kv[f].y, acc[e][f]);
+              acc[e][f] = fmaf(qv.z, kv[f].z, acc[e][f]);
+              acc[e][f] = fmaf(qv.w, kv[f].w, acc[e][f]);
+            }
+          }
         }
       }
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        sA[i0 * kLdF + j0 + e] = acc[0][e];
-        sA[(i0 + 8) * kLdF + j0 + e] = acc[1][e];
+      for (int e = 0; e < 4; ++e)
+#pragma unroll
+        for (int f = 0; f < 4; ++f) acc[e][f] += __shfl_xor_sync(0xffffffffu, acc[e][f], 1);
+      if (ch == 0) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          *reinterpret_cast<float4 *>(sA + (i0 + 4 * e) * kLdF + j0) =
+              make_float4(acc[e][0], acc[e][1], acc[e][2], acc[e][3]);
       }
     }
     __syncthreads();
