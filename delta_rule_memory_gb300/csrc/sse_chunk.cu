@@ -316,47 +316,69 @@ __global__ void __launch_bounds__(kPThreads, 2) sse_prep_kernel(const PrepArgs a
     }
     __syncthreads();
 
-    // ---- A, diagonal blocks: thread (block J, row i, channel quarter cq)
-    // walks j = i down to the block start with qf_r = q_ir prod_{t=j+1..i}
-    // alpha_tr; its channels are the float4 groups cq, cq+4, ..., cq+28 (so
-    // the four quarters read distinct banks)
+    // ---- A, diagonal blocks: thread (block J, rows i and i + 8, channel
+    // slice cs) walks j from row i + 8 down to the block start with qf_r =
+    // q_ir prod_{t=j+1..i} alpha_tr for both rows, so every key and decay row
+    // it loads serves two rows; its channels are the float4 groups cs, cs+8,
+    // cs+16, cs+24 (the 8 slices of a row read distinct banks)
     {
-      const int J = tid >> 6, il = (tid >> 2) & 15, cq = tid & 3;
-      const int i = 16 * J + il;
-      float qf[32];
+      const int J = tid >> 6, il = (tid >> 3) & 7, cs = tid & 7;
+      const int ia = 16 * J + il, ib = ia + 8;
+      float qa[16], qb[16];
 #pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        const uint2 w = *reinterpret_cast<const uint2 *>(sq + i * kCh + 4 * (4 * m + cq));
-        qf[4 * m] = bf16_to_f32(static_cast<uint16_t>(w.x & 0xffffu));
-        qf[4 * m + 1] = bf16_to_f32(static_cast<uint16_t>(w.x >> 16));
-        qf[4 * m + 2] = bf16_to_f32(static_cast<uint16_t>(w.y & 0xffffu));
-        qf[4 * m + 3] = bf16_to_f32(static_cast<uint16_t>(w.y >> 16));
+      for (int m = 0; m < 4; ++m) {
+        const uint2 wa = *reinterpret_cast<const uint2 *>(sq + ia * kCh + 4 * (cs + 8 * m));
+        const uint2 wb = *reinterpret_cast<const uint2 *>(sq + ib * kCh + 4 * (cs + 8 * m));
+        qa[4 * m] = bf16_to_f32(static_cast<uint16_t>(wa.x & 0xffffu));
+        qa[4 * m + 1] = bf16_to_f32(static_cast<uint16_t>(wa.x >> 16));
+        qa[4 * m + 2] = bf16_to_f32(static_cast<uint16_t>(wa.y & 0xffffu));
+        qa[4 * m + 3] = bf16_to_f32(static_cast<uint16_t>(wa.y >> 16));
+        qb[4 * m] = bf16_to_f32(static_cast<uint16_t>(wb.x & 0xffffu));
+        qb[4 * m + 1] = bf16_to_f32(static_cast<uint16_t>(wb.x >> 16));
+        qb[4 * m + 2] = bf16_to_f32(static_cast<uint16_t>(wb.y & 0xffffu));
+        qb[4 * m + 3] = bf16_to_f32(static_cast<uint16_t>(wb.y >> 16));
       }
-      for (int jl = il | 7; jl >= 0; --jl) {  // warp-uniform trip count (a warp holds rows 0-7 or 8-15)
-        const bool act = jl <= il;
+      for (int jl = (il | 3) + 8; jl >= 0; --jl) {  // warp-uniform trip count (a warp holds 4 consecutive il)
+        const bool acta = jl <= il, actb = jl <= il + 8;
         const int j = 16 * J + jl;
         const float *kr = skk + j * kLdA;
-        float acc = 0.f;
+        float acc_a = 0.f, acc_b = 0.f;
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          const float4 kv = *reinterpret_cast<const float4 *>(kr + 4 * (4 * m + cq));
-          acc = fmaf(qf[4 * m], kv.x, acc);
-          acc = fmaf(qf[4 * m + 1], kv.y, acc);
-          acc = fmaf(qf[4 * m + 2], kv.z, acc);
-          acc = fmaf(qf[4 * m + 3], kv.w, acc);
+        for (int m = 0; m < 4; ++m) {
+          const float4 kv = *reinterpret_cast<const float4 *>(kr + 4 * (cs + 8 * m));
+          acc_a = fmaf(qa[4 * m], kv.x, acc_a);
+          acc_a = fmaf(qa[4 * m + 1], kv.y, acc_a);
+          acc_a = fmaf(qa[4 * m + 2], kv.z, acc_a);
+          acc_a = fmaf(qa[4 * m + 3], kv.w, acc_a);
+          acc_b = fmaf(qb[4 * m], kv.x, acc_b);
+          acc_b = fmaf(qb[4 * m + 1], kv.y, acc_b);
+          acc_b = fmaf(qb[4 * m + 2], kv.z, acc_b);
+          acc_b = fmaf(qb[4 * m + 3], kv.w, acc_b);
         }
-        acc += __shfl_xor_sync(kFull, acc, 1);
-        acc += __shfl_xor_sync(kFull, acc, 2);
-        if (act && cq == 0) sA[i * kLdF + j] = acc;
-        if (act) {  // toward j - 1: include alpha_j
-          const float *ar = sal + j * kLdA;
 #pragma unroll
-          for (int m = 0; m < 8; ++m) {
-            const float4 av = *reinterpret_cast<const float4 *>(ar + 4 * (4 * m + cq));
-            qf[4 * m] *= av.x;
-            qf[4 * m + 1] *= av.y;
-            qf[4 * m + 2] *= av.z;
-            qf[4 * m + 3] *= av.w;
+        for (int o = 1; o < 8; o <<= 1) {
+          acc_a += __shfl_xor_sync(kFull, acc_a, o);
+          acc_b += __shfl_xor_sync(kFull, acc_b, o);
+        }
+        if (cs == 0) {
+          if (acta) sA[ia * kLdF + j] = acc_a;
+          if (actb) sA[ib * kLdF + j] = acc_b;
+        }
+        const float *ar = sal + j * kLdA;  // toward j - 1: include alpha_j
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const float4 av = *reinterpret_cast<const float4 *>(ar + 4 * (cs + 8 * m));
+          if (acta) {
+            qa[4 * m] *= av.x;
+            qa[4 * m + 1] *= av.y;
+            qa[4 * m + 2] *= av.z;
+            qa[4 * m + 3] *= av.w;
+          }
+          if (actb) {
+            qb[4 * m] *= av.x;
+            qb[4 * m + 1] *= av.y;
+            qb[4 * m + 2] *= av.z;
+            qb[4 * m + 3] *= av.w;
           }
         }
       }
