@@ -84,30 +84,48 @@ struct ScanLayout {
 
 
 // ---------------------------------------------------------------------------
-// Prepass: one thread per (token, record position).  Resolves, for every
-// slot, which shared-memory row the scan warp reads it from at token t:
-// write slot j -> its prefetched copy, or the history row of the most recent
-// earlier token (within the prefetch window P) that wrote the same table row;
-// read slot j -> likewise, or kRecompute | s when write slot s of the same
-// token holds the row; out-of-range ids and padding -> the zero row.
+// Prepass: resolves, for every slot, which shared-memory row the scan warp
+// reads it from at token t: write slot j -> its prefetched copy, or the
+// history row of the most recent earlier token (within the prefetch window P)
+// that wrote the same table row; read slot j -> likewise, or kRecompute | s
+// when write slot s of the same token holds the row; out-of-range ids and
+// padding -> the zero row.  A CTA takes TB consecutive tokens of one (batch,
+// head), one thread per (token, record position), and first stages the write
+// lists of tokens t0 - P .. t0 + TB - 1 in shared memory, so every hazard
+// search reads shared memory only.
 // ---------------------------------------------------------------------------
+constexpr int kRecThreads = 256;
+
 template <int P, int SLOTS, int TW>
-__global__ void record_kernel(const int32_t *__restrict__ idx_w, const float *__restrict__ w_w,
-                              const int32_t *__restrict__ idx_r, const float *__restrict__ w_r,
-                              const float *__restrict__ alpha, const float *__restrict__ beta, int W, int R, int T,
-                              int H, int N, long total, TokenRec<SLOTS> *__restrict__ rec,
-                              int32_t *__restrict__ dev_err) {
+__global__ void __launch_bounds__(kRecThreads) record_kernel(
+    const int32_t *__restrict__ idx_w, const float *__restrict__ w_w, const int32_t *__restrict__ idx_r,
+    const float *__restrict__ w_r, const float *__restrict__ alpha, const float *__restrict__ beta, int W, int R,
+    int T, int H, int N, int t_blocks, TokenRec<SLOTS> *__restrict__ rec, int32_t *__restrict__ dev_err) {
   using L = ScanLayout<P, SLOTS, TW>;
   constexpr int RG = Tile<TW>::RG;
   constexpr int RPL = SLOTS / RG;
-  const long tid = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (tid >= total) return;
-  const long tok = tid / (2 * SLOTS);
-  const int pos = static_cast<int>(tid - tok * 2 * SLOTS);
+  constexpr int PPOS = 2 * SLOTS;            // record positions per token
+  constexpr int TB = kRecThreads / PPOS;     // tokens per CTA
+  constexpr int NROW = TB + P;               // staged write lists
+  __shared__ __align__(16) int32_t sw[NROW * SLOTS];
+  const long bh = blockIdx.x / t_blocks;
+  const int t0 = static_cast<int>(blockIdx.x - bh * t_blocks) * TB;
+  const long b = bh / H;
+  const int h = static_cast<int>(bh - b * H);
+  for (int id = threadIdx.x; id < NROW * SLOTS; id += kRecThreads) {
+    const int tt = t0 - P + id / SLOTS, s = id % SLOTS;
+    int32_t x = -1;  // matches no valid id
+    if (tt >= 0 && tt < T && s < W) x = idx_w[((b * T + tt) * H + h) * W + s];
+    sw[id] = x;
+  }
+  __syncthreads();
+  const int tl = threadIdx.x / PPOS, pos = threadIdx.x % PPOS;
+  const int t = t0 + tl;
+  if (t >= T) return;
+  const long tok = (b * T + t) * H + h;
   const int r = pos / (2 * RPL), k = pos % (2 * RPL);
   const bool is_w = k < RPL;
   const int j = r + RG * (is_w ? k : k - RPL);
-  const int t = static_cast<int>((tok / H) % T);
   TokenRec<SLOTS> &o = rec[tok];
   if (pos == 0) {
     o.alpha = alpha[tok];
@@ -121,7 +139,8 @@ __global__ void record_kernel(const int32_t *__restrict__ idx_w, const float *__
     o.src[pos] = static_cast<uint16_t>(L::kRowZero);
     return;
   }
-  const int my = is_w ? idx_w[tok * W + j] : idx_r[tok * R + j];
+  const int32_t *own = sw + (tl + P) * SLOTS;
+  const int my = is_w ? own[j] : idx_r[tok * R + j];
   o.idx[pos] = my;
   o.w[pos] = is_w ? w_w[tok * W + j] : w_r[tok * R + j];
   int err = 0;
@@ -130,21 +149,33 @@ __global__ void record_kernel(const int32_t *__restrict__ idx_w, const float *__
     code = L::kRowZero;
     err |= SDM_DEVERR_INDEX_RANGE;
   } else {
-    if (is_w) {
-      for (int jj = 0; jj < j; ++jj)
-        if (idx_w[tok * W + jj] == my) err |= SDM_DEVERR_INDEX_REPEAT;
-    }
-    const int dmax = min(P, t);
-    bool found = false;
-    for (int d = is_w ? 1 : 0; d <= dmax && !found; ++d) {
-      const int32_t *lst = idx_w + (tok - static_cast<long>(d) * H) * W;
-      for (int s = W - 1; s >= 0; --s) {
-        if (lst[s] == my) {
-          code = d == 0 ? (kRecompute | s) : L::kRowH + ((t - d) % L::NH) * SLOTS + s;
-          found = true;
-          break;
+    // the nearest earlier writer: smallest distance d, then the largest slot
+    // s; walking d downwards and s upwards, the last match is that one
+    int hit = -1;
+#pragma unroll
+    for (int d = P; d >= 0; --d) {
+      const int4 *row = reinterpret_cast<const int4 *>(sw + (tl + P - d) * SLOTS);
+#pragma unroll
+      for (int s4 = 0; s4 < SLOTS / 4; ++s4) {
+        const int4 x = row[s4];
+        const int xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int s = 4 * s4 + e;
+          if (d == 0) {
+            if (xs[e] == my) {
+              if (is_w && s < j) err |= SDM_DEVERR_INDEX_REPEAT;
+              if (!is_w) hit = s;
+            }
+          } else if (xs[e] == my) {
+            hit = (d << 8) | s;
+          }
         }
       }
+    }
+    if (hit >= 0) {
+      const int d = hit >> 8, s = hit & 0xff;
+      code = d == 0 ? (kRecompute | s) : L::kRowH + ((t - d) % L::NH) * SLOTS + s;
     }
   }
   o.src[pos] = static_cast<uint16_t>(code);
@@ -536,11 +567,12 @@ chosen:
   const long total_warps = static_cast<long>(B) * H * tiles;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const long total = static_cast<long>(B) * T * H * 2 * slots;
-  const unsigned rblocks = static_cast<unsigned>((total + 255) / 256);
-#define SDM_REC(PP, S, TT)                                                                                       \
-  record_kernel<PP, S, TT><<<rblocks, 256, 0, st>>>(idx_w, w_w, idx_r, w_r, alpha, beta, W, R, T, H, N, total, \
-                                                    static_cast<TokenRec<S> *>(workspace), dev_err)
+  const int rec_tb = kRecThreads / (2 * slots);  // tokens per prepass CTA
+  const int t_blocks = (T + rec_tb - 1) / rec_tb;
+  const unsigned rblocks = static_cast<unsigned>(static_cast<long>(B) * H * t_blocks);
+#define SDM_REC(PP, S, TT)                                                                                  \
+  record_kernel<PP, S, TT><<<rblocks, kRecThreads, 0, st>>>(idx_w, w_w, idx_r, w_r, alpha, beta, W, R, T, H, N, \
+                                                            t_blocks, static_cast<TokenRec<S> *>(workspace), dev_err)
   if (slots == 16 && tw == 32 && window == 4) SDM_REC(4, 16, 32);
   else if (slots == 16 && tw == 32 && window == 6) SDM_REC(6, 16, 32);
   else if (slots == 16 && tw == 32 && window == 8) SDM_REC(8, 16, 32);
