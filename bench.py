@@ -42,7 +42,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 NCU_TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of one full-size launch
     # (8.01 GB + 4.19 GB), profiles/sparse_scan_1.4b_layer.md
-    ("sdm_14b_layer", "sdm"): {"bytes": 12.20e9, "digest": "bcc6a3a96443"},
+    ("sdm_14b_layer", "sdm"): {"bytes": 12.20e9, "digest": "ce4a87fa8968"},
     # both kernels of one full-size gdn_scan call (746.4 MB + 590.5 MB), profiles/gdn_chunk_dense.md
     ("gdn", "gdn"): {"bytes": 1.337e9, "digest": "e2c62e1f689e"},
     # the five kernels of one full-size sse_scan call on the chunked path (1.072 GB read + 0.799 GB
@@ -731,6 +731,23 @@ def run_reference(args, rank, world):
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_gather_probe():
+    """Compile and run the row-piece gather probe: the DRAM throughput that
+    the sparse scan's access pattern (random 64-byte pieces of 3840-byte rows,
+    two reads per write) allows, next to larger pieces."""
+    import shutil
+    import tempfile
+    src = os.path.join(ROOT, "delta_rule_memory_gb300", "csrc", "probe", "gather_ceiling.cu")
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    with tempfile.TemporaryDirectory() as tmp:
+        exe = os.path.join(tmp, "gather_ceiling")
+        subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-o", exe, src], check=True)
+        r = subprocess.run([exe], capture_output=True, text=True)
+        sys.stdout.write(r.stdout)
+        if r.returncode != 0:
+            raise SystemExit(f"gather probe failed: {r.stderr.strip()}")
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -743,6 +760,9 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=0, help="tokens per sampled sequence for the oracle")
     ap.add_argument("--cpu-cores", type=int, default=0)
     ap.add_argument("--batch", type=int, default=0, help="override B (small cases for profiling only)")
+    ap.add_argument("--probe", choices=["gather"], default=None,
+                    help="instead of a step, run a measurement probe: 'gather' times random row-piece gathers and "
+                         "scatters on a 3.54 GB table by piece size (csrc/probe/gather_ceiling.cu)")
     ap.add_argument("--overlap-addressing", action="store_true",
                     help="sparse inference step: run step s+1's addressing on a second stream during step s's "
                          "scan (higher step throughput; the scan's own time then includes the interference)")
@@ -752,6 +772,9 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
 
+    if args.probe == "gather":
+        run_gather_probe()
+        return
     if args.impl == "reference":
         if rank != 0:
             return
