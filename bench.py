@@ -633,14 +633,14 @@ def run_ours(args, rank, world, local_rank, sampler):
     # same step -> y back to pinned host memory, every step
     KE = max(3, K // 2)
     for _ in range(2):
-        run.e2e_step()
+        run.e2e_step(args.e2e_chunk)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(KE):
-        run.e2e_step()
+        run.e2e_step(args.e2e_chunk)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / KE
@@ -687,7 +687,7 @@ def run_ours(args, rank, world, local_rank, sampler):
         "cpu_baseline": cpu,
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "path": "sdm_forward_host (chunked copy/compute pipeline)"
+                "path": f"sdm_forward_host (copy/compute pipeline, {args.e2e_chunk}-token chunks)"
                 if wl.kind == "sdm" and not wl.train and not wl.chunked
                 else "pinned H2D copies + scan call + D2H of y"},
         "gpu_launches": K * run.launches_per_step,
@@ -760,6 +760,8 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=0, help="tokens per sampled sequence for the oracle")
     ap.add_argument("--cpu-cores", type=int, default=0)
     ap.add_argument("--batch", type=int, default=0, help="override B (small cases for profiling only)")
+    ap.add_argument("--e2e-chunk", type=int, default=512,
+                    help="tokens per pipelined chunk of the end-to-end sparse step (sdm_forward_host chunk_T)")
     ap.add_argument("--probe", choices=["gather"], default=None,
                     help="instead of a step, run a measurement probe: 'gather' times random row-piece gathers and "
                          "scatters on a 3.54 GB table by piece size (csrc/probe/gather_ceiling.cu)")

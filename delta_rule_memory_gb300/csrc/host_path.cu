@@ -1,8 +1,12 @@
 // host_path.cu - the whole sparse step from host buffers, with transfers
 // overlapped with compute.
 //
-// The sequence is cut into chunks of chunk_T tokens.  For chunk c (staging
-// slot c % 2) three streams run a software pipeline:
+// The sequence is cut into chunks of at most chunk_T tokens: the first and
+// the last are a quarter of chunk_T, so the pipeline fills (the first chunk's
+// inputs cross before any compute) and drains (the last chunk's y crosses
+// after it) quickly, and the tokens between are split evenly into chunks of
+// at most chunk_T.  For chunk c (staging slot c % 2) three streams run a
+// software pipeline:
 //   copy-in  : the chunk's score halves, v, alpha and beta, host -> device
 //   compute  : write addressing, read addressing, scan (the caller's stream;
 //              the table continues from chunk to chunk)
@@ -35,6 +39,32 @@ struct Slot {
     y = align_up(th * d_v * 4);
     ws = align_up(sdm_scan_workspace_size(B, Tc, H, W, R));
     total = 4 * s + v + 2 * g + 2 * iw + 2 * ir + y + ws;
+  }
+};
+
+// Chunk start of chunk c under the schedule above (c = nchunks gives T).
+struct Schedule {
+  int T, edge, mid_n, mid_base, mid_extra, n;
+  Schedule(int T_, int chunk_T) : T(T_) {
+    edge = chunk_T / 4 > 0 ? chunk_T / 4 : 1;
+    if (T <= chunk_T) {  // one chunk
+      edge = T;
+      mid_n = mid_base = mid_extra = 0;
+      n = 1;
+      return;
+    }
+    const int mid = T - 2 * edge;  // >= 0: edge <= chunk_T / 2 < T / 2, or edge = 1 < T
+    mid_n = (mid + chunk_T - 1) / chunk_T;
+    mid_base = mid_n ? mid / mid_n : 0;
+    mid_extra = mid_n ? mid % mid_n : 0;  // the first mid_extra middle chunks take one token more
+    n = mid_n + 2;
+  }
+  int start(int c) const {
+    if (c <= 0) return 0;
+    if (n == 1 || c >= n) return T;
+    const int m = c - 1;  // middle chunks before chunk c
+    if (m >= mid_n) return T - edge;
+    return edge + m * mid_base + (m < mid_extra ? m : mid_extra);
   }
 };
 
@@ -106,11 +136,12 @@ extern "C" int sdm_forward_host(const float *s1w, const float *s2w, const float 
     ok(cudaStreamWaitEvent(cout, start, 0), "wait");
   }
 
-  const int nchunks = (T + Tc - 1) / Tc;
+  const Schedule sched(T, Tc);
+  const int nchunks = sched.n;
   for (int c = 0; c < nchunks && rc == SDM_OK; ++c) {
     const int s = c & 1;
-    const int t0 = c * Tc;
-    const int tc = (T - t0) < Tc ? (T - t0) : Tc;
+    const int t0 = sched.start(c);
+    const int tc = sched.start(c + 1) - t0;
     char *base = static_cast<char *>(workspace) + s * sl.total;
     float *d_s[4];
     for (int i = 0; i < 4; ++i) d_s[i] = reinterpret_cast<float *>(base + i * sl.s);

@@ -319,10 +319,12 @@ def test_two_slot_worked_example_on_gpu(golden):
 
 
 # ------------------------------------------------------------- host path
-@pytest.mark.parametrize("chunk", [100, 4096])
+@pytest.mark.parametrize("chunk", [3, 100, 4096])
 def test_forward_host_matches_device_path_bitexact(chunk):
     """sdm_forward_host (host inputs and y, chunked copy/compute pipeline) gives
-    the same bits as sdm_address x2 + sdm_scan on device inputs."""
+    the same bits as sdm_address x2 + sdm_scan on device inputs: one chunk
+    (4096), quarter-size first and last chunks around even middle chunks
+    (100: 25, 95, 94, 94, 25 tokens), one-token edges (3)."""
     sdm = need_gpu()
     import torch
     sh = synth.SDM_14B_LAYER.with_(B=2, T=333, H=2, sqrtN=64, d_v=96)
