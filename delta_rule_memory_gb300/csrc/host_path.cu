@@ -5,11 +5,13 @@
 // the last are a quarter of chunk_T, so the pipeline fills (the first chunk's
 // inputs cross before any compute) and drains (the last chunk's y crosses
 // after it) quickly, and the tokens between are split evenly into chunks of
-// at most chunk_T.  For chunk c (staging slot c % 2) three streams run a
+// at most chunk_T.  For chunk c (staging slot c % 2) four streams run a
 // software pipeline:
 //   copy-in  : the chunk's score halves, v, alpha and beta, host -> device
-//   compute  : write addressing, read addressing, scan (the caller's stream;
-//              the table continues from chunk to chunk)
+//   address  : write and read addressing (independent of the table, so chunk
+//              c+1's runs while chunk c is scanned)
+//   compute  : the scan (the caller's stream; the table continues from chunk
+//              to chunk)
 //   copy-out : the chunk's y, device -> host
 // Events order each stage after the one it depends on and keep a staging
 // slot from being refilled before its previous chunk has left it.  Rows of a
@@ -115,8 +117,8 @@ extern "C" int sdm_forward_host(const float *s1w, const float *s2w, const float 
   const int Tc = chunk_T < T ? chunk_T : T;
   const Slot sl(B, Tc, H, sqrtN, d_v, W, R, esz);
   cudaStream_t compute = static_cast<cudaStream_t>(stream);
-  cudaStream_t cin = nullptr, cout = nullptr;
-  cudaEvent_t start = nullptr, in_done[2] = {}, comp_done[2] = {}, out_done[2] = {};
+  cudaStream_t cin = nullptr, cout = nullptr, caddr = nullptr;
+  cudaEvent_t start = nullptr, in_done[2] = {}, addr_done[2] = {}, comp_done[2] = {}, out_done[2] = {};
   int rc = SDM_OK;
   auto ok = [&](cudaError_t e, const char *what) {
     if (e != cudaSuccess && rc == SDM_OK) rc = set_error(SDM_ERR_CUDA, "sdm_forward_host: %s: %s", what, cudaGetErrorString(e));
@@ -124,9 +126,11 @@ extern "C" int sdm_forward_host(const float *s1w, const float *s2w, const float 
   };
   ok(cudaStreamCreateWithFlags(&cin, cudaStreamNonBlocking), "stream");
   ok(cudaStreamCreateWithFlags(&cout, cudaStreamNonBlocking), "stream");
+  ok(cudaStreamCreateWithFlags(&caddr, cudaStreamNonBlocking), "stream");
   ok(cudaEventCreateWithFlags(&start, cudaEventDisableTiming), "event");
   for (int i = 0; i < 2; ++i) {
     ok(cudaEventCreateWithFlags(&in_done[i], cudaEventDisableTiming), "event");
+    ok(cudaEventCreateWithFlags(&addr_done[i], cudaEventDisableTiming), "event");
     ok(cudaEventCreateWithFlags(&comp_done[i], cudaEventDisableTiming), "event");
     ok(cudaEventCreateWithFlags(&out_done[i], cudaEventDisableTiming), "event");
   }
@@ -134,6 +138,7 @@ extern "C" int sdm_forward_host(const float *s1w, const float *s2w, const float 
   if (rc == SDM_OK && ok(cudaEventRecord(start, compute), "record")) {
     ok(cudaStreamWaitEvent(cin, start, 0), "wait");
     ok(cudaStreamWaitEvent(cout, start, 0), "wait");
+    ok(cudaStreamWaitEvent(caddr, start, 0), "wait");
   }
 
   const Schedule sched(T, Tc);
@@ -166,14 +171,18 @@ extern "C" int sdm_forward_host(const float *s1w, const float *s2w, const float 
     if (rc == SDM_OK) rc = copy_chunk_2d(d_b, beta, 4, B, T, H, t0, tc, false, cin);
     if (rc != SDM_OK || !ok(cudaEventRecord(in_done[s], cin), "record")) break;
 
-    // compute (after its inputs landed and chunk c-2's y left this slot)
-    if (!ok(cudaStreamWaitEvent(compute, in_done[s], 0), "wait")) break;
+    // addressing (after its inputs landed; this slot's previous ids were read
+    // by chunk c-2's scan, which the copy-in already waited for)
+    if (!ok(cudaStreamWaitEvent(caddr, in_done[s], 0), "wait")) break;
+    rc = sdm_address(d_s[0], d_s[1], B, tc, H, sqrtN, k, W, d_iw, d_ww, dev_err, caddr);
+    if (rc == SDM_OK) rc = sdm_address(d_s[2], d_s[3], B, tc, H, sqrtN, k, R, d_ir, d_wr, dev_err, caddr);
+    if (rc != SDM_OK || !ok(cudaEventRecord(addr_done[s], caddr), "record")) break;
+
+    // scan (after the addressing and after chunk c-2's y left this slot)
+    if (!ok(cudaStreamWaitEvent(compute, addr_done[s], 0), "wait")) break;
     if (c >= 2 && !ok(cudaStreamWaitEvent(compute, out_done[s], 0), "wait")) break;
-    rc = sdm_address(d_s[0], d_s[1], B, tc, H, sqrtN, k, W, d_iw, d_ww, dev_err, compute);
-    if (rc == SDM_OK) rc = sdm_address(d_s[2], d_s[3], B, tc, H, sqrtN, k, R, d_ir, d_wr, dev_err, compute);
-    if (rc == SDM_OK)
-      rc = sdm_scan(state, d_vb, v_dtype, d_a, d_b, d_iw, d_ww, W, d_ir, d_wr, R, B, tc, H, sqrtN * sqrtN, d_v,
-                    resid_mode, d_y, d_ws, sl.ws, dev_err, compute);
+    rc = sdm_scan(state, d_vb, v_dtype, d_a, d_b, d_iw, d_ww, W, d_ir, d_wr, R, B, tc, H, sqrtN * sqrtN, d_v,
+                  resid_mode, d_y, d_ws, sl.ws, dev_err, compute);
     if (rc != SDM_OK || !ok(cudaEventRecord(comp_done[s], compute), "record")) break;
 
     // copy-out
@@ -189,17 +198,21 @@ extern "C" int sdm_forward_host(const float *s1w, const float *s2w, const float 
       cudaStreamWaitEvent(compute, fin, 0);
       cudaEventRecord(fin, cin);
       cudaStreamWaitEvent(compute, fin, 0);
+      cudaEventRecord(fin, caddr);
+      cudaStreamWaitEvent(compute, fin, 0);
       cudaEventDestroy(fin);
     }
   }
   // streams and events are released once their queued work completes
   for (int i = 0; i < 2; ++i) {
     if (in_done[i]) cudaEventDestroy(in_done[i]);
+    if (addr_done[i]) cudaEventDestroy(addr_done[i]);
     if (comp_done[i]) cudaEventDestroy(comp_done[i]);
     if (out_done[i]) cudaEventDestroy(out_done[i]);
   }
   if (start) cudaEventDestroy(start);
   if (cin) cudaStreamDestroy(cin);
   if (cout) cudaStreamDestroy(cout);
+  if (caddr) cudaStreamDestroy(caddr);
   return rc;
 }

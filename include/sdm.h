@@ -178,10 +178,11 @@ SDM_API size_t sdm_forward_host_workspace_size(int B, int T, int H, int sqrtN, i
  * The sequence is processed in chunks of at most chunk_T tokens: the first
  * and the last hold chunk_T/4 tokens (at least 1), so that the pipeline fills
  * and drains quickly, and the tokens between are split evenly (a sequence of
- * at most chunk_T tokens is one chunk).  Chunk c+1's inputs are copied in and
- * chunk c-1's y copied out while chunk c is computed (two
- * internal copy streams, ordered by events after the work already queued on
- * `stream`, and before anything queued on `stream` afterwards).  Results are
+ * at most chunk_T tokens is one chunk).  Chunk c+1's inputs are copied in,
+ * and its addressing runs, while chunk c is scanned and chunk c-1's y is
+ * copied out (three internal streams for the copies and the addressing,
+ * ordered by events after the work already queued on `stream`, and before
+ * anything queued on `stream` afterwards; the scans run on `stream`).  Results are
  * bit-identical to one sdm_address/sdm_address/sdm_scan sequence on the whole
  * input (the scan continues its table across chunks).
  *
