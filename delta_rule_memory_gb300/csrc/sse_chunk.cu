@@ -520,33 +520,47 @@ __global__ void __launch_bounds__(kPThreads, 2) sse_prep_kernel(const PrepArgs a
       const float gi = rg[i];
       float x[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int j = j0 + e;
-        x[e] = j <= i ? sA[i * kLdF + j] * gi * rg[j] : 0.f;
+      for (int h4 = 0; h4 < 8; h4 += 4) {  // kLdF and j0 are multiples of 4; rg is 16-byte aligned
+        const float4 a4 = *reinterpret_cast<const float4 *>(sA + i * kLdF + j0 + h4);
+        const float4 g4 = *reinterpret_cast<const float4 *>(rg + j0 + h4);
+        const float av[4] = {a4.x, a4.y, a4.z, a4.w}, gv[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[h4 + e] = j0 + h4 + e <= i ? av[e] * gi * gv[e] : 0.f;
       }
       store_split8(unit + kXA, unit + kXA + 8192, kmajor_off(i, j0, kC), x);
     }
-    for (int id = tid; id < kC * 16; id += kPThreads) {
-      const int i = id >> 4, r0 = (id & 15) * 8, J = i >> 4;
-      const float gi = rg[i];
-      float x[8], y[8];
+    {  // thread: block J, channels r0..r0+7, rows 16J + il + 4m (m < 4), so the
+       // block's prefix and suffix products are loaded once
+      const int r0 = (tid & 15) * 8, il = (tid >> 4) & 3, J = tid >> 6;
+      float pr[8], sf[8];
 #pragma unroll
       for (int h4 = 0; h4 < 8; h4 += 4) {  // 16-byte rows: kLdA and r0 are multiples of 4
-        const float4 qf = *reinterpret_cast<const float4 *>(sal + i * kLdA + r0 + h4);
-        const float4 pr = *reinterpret_cast<const float4 *>(sPre + J * kCh + r0 + h4);
-        const float4 kr = *reinterpret_cast<const float4 *>(skk + i * kLdA + r0 + h4);
-        const float4 sf = *reinterpret_cast<const float4 *>(sSuf + J * kCh + r0 + h4);
-        x[h4] = gi * qf.x * pr.x;
-        x[h4 + 1] = gi * qf.y * pr.y;
-        x[h4 + 2] = gi * qf.z * pr.z;
-        x[h4 + 3] = gi * qf.w * pr.w;
-        y[h4] = gi * kr.x * sf.x;
-        y[h4 + 1] = gi * kr.y * sf.y;
-        y[h4 + 2] = gi * kr.z * sf.z;
-        y[h4 + 3] = gi * kr.w * sf.w;
+        const float4 p4 = *reinterpret_cast<const float4 *>(sPre + J * kCh + r0 + h4);
+        const float4 s4 = *reinterpret_cast<const float4 *>(sSuf + J * kCh + r0 + h4);
+        pr[h4] = p4.x; pr[h4 + 1] = p4.y; pr[h4 + 2] = p4.z; pr[h4 + 3] = p4.w;
+        sf[h4] = s4.x; sf[h4 + 1] = s4.y; sf[h4 + 2] = s4.z; sf[h4 + 3] = s4.w;
       }
-      store_split8(unit + kXQ, unit + kXQ + 16384, kmajor_off(i, r0, kCh), x);
-      store_split8(unit + kXK, unit + kXK + 16384, kmajor_off(i, r0, kCh), y);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int i = 16 * J + il + 4 * m;
+        const float gi = rg[i];
+        float x[8], y[8];
+#pragma unroll
+        for (int h4 = 0; h4 < 8; h4 += 4) {
+          const float4 qf = *reinterpret_cast<const float4 *>(sal + i * kLdA + r0 + h4);
+          const float4 kr = *reinterpret_cast<const float4 *>(skk + i * kLdA + r0 + h4);
+          x[h4] = gi * qf.x * pr[h4];
+          x[h4 + 1] = gi * qf.y * pr[h4 + 1];
+          x[h4 + 2] = gi * qf.z * pr[h4 + 2];
+          x[h4 + 3] = gi * qf.w * pr[h4 + 3];
+          y[h4] = gi * kr.x * sf[h4];
+          y[h4 + 1] = gi * kr.y * sf[h4 + 1];
+          y[h4 + 2] = gi * kr.z * sf[h4 + 2];
+          y[h4 + 3] = gi * kr.w * sf[h4 + 3];
+        }
+        store_split8(unit + kXQ, unit + kXQ + 16384, kmajor_off(i, r0, kCh), x);
+        store_split8(unit + kXK, unit + kXK + 16384, kmajor_off(i, r0, kCh), y);
+      }
     }
     __syncthreads();  // shared memory is reused by the next unit
   }
