@@ -159,20 +159,60 @@ __global__ void __launch_bounds__(128) sparse_backward_kernel16(const BackArgs a
   float *G = a.dstate + bh * static_cast<long>(N) * d_v + ccol;
   const int np = R + W + 2;
   bool bad = false;
+  // slot data: lane k < 16 holds read slot k, lane 16 + k write slot k
+  const int ks = lane & 15;
+  const bool is_w = lane >= 16;
+  const bool has = ks < (is_w ? W : R);
+  auto tok_of = [&](int t) { return (b * T + t) * H + h; };
+
+  // Software pipeline over the reversed tokens: the slot ids of token t-2 and
+  // the rows, gates, v and dy of token t-1 are loaded while token t is
+  // computed.  A lane is the only reader and writer of its column, so a row
+  // of token t-1 that token t then stores was prefetched stale (the load came
+  // first in program order); those few slots are loaded again after the
+  // stores.
+  struct Scal { float al, be, vc, dyc; };
+  auto load_ids = [&](int t, int &id, float &wt) {
+    const long tok = tok_of(t);
+    id = has ? (is_w ? a.idx_w[tok * W + ks] : a.idx_r[tok * R + ks]) : -1;
+    wt = has ? (is_w ? a.w_w[tok * W + ks] : a.w_r[tok * R + ks]) : 0.f;
+  };
+  auto load_tok = [&](int t, int id, float (&Mr)[S], float (&Gr)[S], float (&Gw)[S], float (&U)[S], Scal &sc) {
+    const long tok = tok_of(t);
+    sc.al = a.alpha[tok];
+    sc.be = a.beta[tok];
+    sc.vc = a.v_bf16 ? bf16_to_f32(static_cast<const uint16_t *>(a.v)[tok * d_v + ccol])
+                     : static_cast<const float *>(a.v)[tok * d_v + ccol];
+    sc.dyc = a.dy[tok * d_v + ccol];
+#pragma unroll
+    for (int k = 0; k < S; ++k) {  // every row of the token at once
+      const int ri = __shfl_sync(kFull, id, k), wi = __shfl_sync(kFull, id, 16 + k);
+      const bool okr = static_cast<unsigned>(ri) < static_cast<unsigned>(N);
+      const bool okw = static_cast<unsigned>(wi) < static_cast<unsigned>(N);
+      Mr[k] = okr ? M[static_cast<long>(ri) * d_v] : 0.f;
+      Gr[k] = okr ? G[static_cast<long>(ri) * d_v] : 0.f;
+      Gw[k] = okw ? G[static_cast<long>(wi) * d_v] : 0.f;
+      U[k] = k < W ? a.undo[(tok * W + k) * static_cast<long>(d_v) + ccol] : 0.f;
+    }
+  };
+  float Mr[S], Gr[S], Gw[S], U[S], nMr[S], nGr[S], nGw[S], nU[S];
+  Scal sc, nsc;
+  int my_id = -1, n_id = -1;
+  float my_wt = 0.f, n_wt = 0.f;
+  if (T > 0) {
+    load_ids(T - 1, my_id, my_wt);
+    load_tok(T - 1, my_id, Mr, Gr, Gw, U, sc);
+  }
+  if (T > 1) load_ids(T - 2, n_id, n_wt);
 
   for (int t = T - 1; t >= 0; --t) {
-    const long tok = (b * T + t) * H + h;
-    const float al = a.alpha[tok], be = a.beta[tok];
-    const float vc = a.v_bf16 ? bf16_to_f32(static_cast<const uint16_t *>(a.v)[tok * d_v + ccol])
-                              : static_cast<const float *>(a.v)[tok * d_v + ccol];
-    const float dyc = a.dy[tok * d_v + ccol];
+    const long tok = tok_of(t);
+    if (t >= 1) load_tok(t - 1, n_id, nMr, nGr, nGw, nU, nsc);  // next token's rows (prefetch)
+    int nn_id = -1;
+    float nn_wt = 0.f;
+    if (t >= 2) load_ids(t - 2, nn_id, nn_wt);                   // and the ids after it
+    const float al = sc.al, be = sc.be, vc = sc.vc, dyc = sc.dyc;
     float *pt = a.part + (static_cast<long>(tile) * (a.total_warps / a.tiles) * T + tok) * np;
-    // slot data: lane k < 16 holds read slot k, lane 16 + k write slot k
-    const int ks = lane & 15;
-    const bool is_w = lane >= 16;
-    const bool has = ks < (is_w ? W : R);
-    const int my_id = has ? (is_w ? a.idx_w[tok * W + ks] : a.idx_r[tok * R + ks]) : -1;
-    const float my_wt = has ? (is_w ? a.w_w[tok * W + ks] : a.w_r[tok * R + ks]) : 0.f;
     bad |= has && static_cast<unsigned>(my_id) >= static_cast<unsigned>(N);
     // a write lane finds the read slot (if any) with its row
     int my_match = -1;
@@ -180,17 +220,6 @@ __global__ void __launch_bounds__(128) sparse_backward_kernel16(const BackArgs a
     for (int i = 0; i < S; ++i) {
       const int ri = __shfl_sync(kFull, my_id, i);
       if (is_w && has && ri == my_id) my_match = i;
-    }
-    float Mr[S], Gr[S], Gw[S], U[S];
-#pragma unroll
-    for (int k = 0; k < S; ++k) {  // every row of the token at once
-      const int ri = __shfl_sync(kFull, my_id, k), wi = __shfl_sync(kFull, my_id, 16 + k);
-      const bool okr = static_cast<unsigned>(ri) < static_cast<unsigned>(N);
-      const bool okw = static_cast<unsigned>(wi) < static_cast<unsigned>(N);
-      Mr[k] = okr ? M[static_cast<long>(ri) * d_v] : 0.f;
-      Gr[k] = okr ? G[static_cast<long>(ri) * d_v] : 0.f;
-      Gw[k] = okw ? G[static_cast<long>(wi) * d_v] : 0.f;
-      U[k] = k < W ? a.undo[(tok * W + k) * static_cast<long>(d_v) + ccol] : 0.f;
     }
     // per-lane column partials of the token's sums: [0, 16) dr_i, [16, 32) dw_j
     float part[2 * S];
@@ -268,6 +297,36 @@ __global__ void __launch_bounds__(128) sparse_backward_kernel16(const BackArgs a
         G[static_cast<long>(wi) * d_v] = Gw[j];
         M[static_cast<long>(wi) * d_v] = U[j];
       }
+    }
+    if (t >= 1) {
+      // slots of token t-1 whose row token t just stored: load them again
+      bool hit = false;
+#pragma unroll
+      for (int k = 0; k < 2 * S; ++k) hit |= __shfl_sync(kFull, my_id, k) == n_id;
+      const unsigned stale = __ballot_sync(kFull, hit && static_cast<unsigned>(n_id) < static_cast<unsigned>(N));
+      if (stale) {  // warp-uniform
+#pragma unroll
+        for (int k = 0; k < S; ++k) {
+          const int ri = __shfl_sync(kFull, n_id, k), wi = __shfl_sync(kFull, n_id, 16 + k);
+          if ((stale >> k) & 1u) {
+            nMr[k] = M[static_cast<long>(ri) * d_v];
+            nGr[k] = G[static_cast<long>(ri) * d_v];
+          }
+          if ((stale >> (16 + k)) & 1u) nGw[k] = G[static_cast<long>(wi) * d_v];
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < S; ++k) {
+        Mr[k] = nMr[k];
+        Gr[k] = nGr[k];
+        Gw[k] = nGw[k];
+        U[k] = nU[k];
+      }
+      sc = nsc;
+      my_id = n_id;
+      my_wt = n_wt;
+      n_id = nn_id;
+      n_wt = nn_wt;
     }
   }
   if (__any_sync(kFull, bad) && lane == 0 && a.err) atomicOr(a.err, SDM_DEVERR_INDEX_RANGE);
