@@ -442,9 +442,11 @@ class GpuRun:
         torch.cuda.current_stream().wait_stream(side)
         torch.cuda.synchronize()
         if self.wl.kind == "sdm":
+            # the two addressing calls are independent: parallel branches of the graph
+            fork = torch.cuda.Stream()
             self.g_pre = torch.cuda.CUDAGraph()
             with torch.cuda.graph(self.g_pre):
-                self._run_pre()
+                self._run_pre(fork)
         self.g_main = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.g_main):
             self._run_main()
@@ -462,12 +464,22 @@ class GpuRun:
         else:
             self._run_main()
 
-    def _run_pre(self):
-        """Work before the dominant kernel (addressing)."""
+    def _run_pre(self, fork=None):
+        """Work before the dominant kernel (addressing).  With `fork`, the read
+        addressing runs on that stream beside the write addressing."""
+        import torch
         sh, d = self.wl.shape, self.d
         if self.wl.kind == "sdm":
+            if fork is None:
+                self.sdm.sdm_address(d["s1w"], d["s2w"], sh.k, sh.W, self.iw, self.ww, self.err)
+                self.sdm.sdm_address(d["s1r"], d["s2r"], sh.k, sh.R, self.ir, self.wr, self.err)
+                return
+            cur = torch.cuda.current_stream()
+            fork.wait_stream(cur)
+            with torch.cuda.stream(fork):
+                self.sdm.sdm_address(d["s1r"], d["s2r"], sh.k, sh.R, self.ir, self.wr, self.err)
             self.sdm.sdm_address(d["s1w"], d["s2w"], sh.k, sh.W, self.iw, self.ww, self.err)
-            self.sdm.sdm_address(d["s1r"], d["s2r"], sh.k, sh.R, self.ir, self.wr, self.err)
+            cur.wait_stream(fork)
 
     def _run_main(self):
         """The dominant kernel's call."""
