@@ -578,15 +578,19 @@ class GpuRun:
             state = 2 * sh.B * sh.H * sh.dk * sh.dv * 4
             return tokh * per + state, "GB/s", "hbm", {"bytes_per_token_head": per}
         tokh = sh.B * sh.T * sh.H
+        # Both SSE paths are measured against the FP32-pipe roofline of the recurrence's own arithmetic:
+        # per visited partition and state element a decay mul, a write fma and a read fma (1 + 2 + 2
+        # flop; the delta write adds the prediction fma, 2).  The chunked prefill does that work in
+        # another order (partly on the tensor cores), so for it this is an effective rate; its HBM
+        # I/O (router and key logits, q, v, alpha in; y out; every partition's state read and written
+        # once) is reported beside it.
+        flops = tokh * (sh.topk + 1) * sh.c * sh.d * (7.0 if self.wl.sse_mode else 5.0)
+        info = {"flops_per_token_head": flops / tokh}
         if self.wl.sse_chunked:
-            # chunked prefill: bound by its I/O (router and key logits, q, v, alpha in; y out; every
-            # partition's state read and written once); its MMAs (~3e5 flop per token-head) take less
             per = 4 * sh.N + 4 * sh.c + 2 * sh.c + 2 * sh.d + 4 * sh.c + 4 * sh.d
             state = 2 * sh.B * sh.H * (sh.N + 1) * sh.c * sh.d * 4
-            return tokh * per + state, "GB/s", "hbm", {"bytes_per_token_head": per}
-        # decay mul, write fma, read fma (1 + 2 + 2); the delta write adds the prediction fma (2)
-        flops = tokh * (sh.topk + 1) * sh.c * sh.d * (7.0 if self.wl.sse_mode else 5.0)
-        return flops, "TFLOP/s", "alu", {"flops_per_token_head": flops / tokh}
+            info.update({"io_bytes_per_token_head": per, "io_bytes": tokh * per + state})
+        return flops, "TFLOP/s", "alu", info
 
 
 def run_ours(args, rank, world, local_rank, sampler):
