@@ -37,6 +37,57 @@ __host__ __device__ inline int rec_words(int topk) { return (2 * topk + 2 + 3) &
 // ---------------------------------------------------------------------------
 // Routing prepass.
 // ---------------------------------------------------------------------------
+// Routing with one thread per token-head, for N <= kRouteThreadN without the
+// key-logit statistics (the chunked path): the same selection (order keys,
+// ties to the lower partition) and gates e = softmax over all N logits, the
+// normaliser summed in partition order.
+constexpr int kRouteThreadN = 16;
+
+__global__ void __launch_bounds__(256) sse_route_thread_kernel(const float *__restrict__ route, long tokens, int N,
+                                                               int topk, uint32_t *__restrict__ rec,
+                                                               int32_t *__restrict__ sel_out,
+                                                               int32_t *__restrict__ dev_err) {
+  const long tok = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  bool bad = false;
+  if (tok < tokens) {
+    const float *lg = route + tok * N;
+    uint32_t key[kRouteThreadN];
+    float lv[kRouteThreadN];
+    uint32_t kmax = 0u;
+#pragma unroll
+    for (int j = 0; j < kRouteThreadN; ++j) {
+      lv[j] = j < N ? lg[j] : 0.f;
+      bad |= j < N && !isfinite(lv[j]);
+      key[j] = j < N ? order_key(lv[j]) : 0u;
+      kmax = max(kmax, key[j]);
+    }
+    const float lmax = key_value(kmax);
+    float z = 0.f;
+#pragma unroll
+    for (int j = 0; j < kRouteThreadN; ++j)
+      if (j < N) z += expf(lv[j] - lmax);
+    uint32_t *r = rec + tok * rec_words(topk);
+    uint32_t taken = 0u;
+    for (int s = 0; s < topk; ++s) {
+      uint32_t best = 0u;
+      int bid = -1;
+#pragma unroll
+      for (int j = 0; j < kRouteThreadN; ++j) {  // first (lowest) id wins ties
+        const bool cand = j < N && !((taken >> j) & 1u) && (bid < 0 || key[j] > best);
+        if (cand) {
+          best = key[j];
+          bid = j;
+        }
+      }
+      taken |= 1u << bid;
+      r[s] = static_cast<uint32_t>(bid);
+      r[topk + s] = __float_as_uint(expf(key_value(best) - lmax) / z);
+      if (sel_out) sel_out[tok * topk + s] = bid;
+    }
+  }
+  if (__any_sync(kFull, bad) && (threadIdx.x & 31) == 0 && dev_err) atomicOr(dev_err, SDM_DEVERR_NONFINITE);
+}
+
 __global__ void __launch_bounds__(256) sse_route_kernel(const float *__restrict__ route, const float *__restrict__ klog,
                                                         long tokens, int N, int topk, int c, bool kstats,
                                                         uint32_t *__restrict__ rec, int32_t *__restrict__ sel_out,
@@ -405,8 +456,12 @@ extern "C" int sse_scan(float *state, const float *route_logits, int topk, const
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const long tokens = static_cast<long>(B) * T * H;
   uint32_t *rec = static_cast<uint32_t *>(workspace);
-  sse_route_kernel<<<static_cast<unsigned>((tokens + 7) / 8), 256, 0, st>>>(route_logits, k_logits, tokens, N, topk,
-                                                                           c, !chunk, rec, sel_out, dev_err);
+  if (chunk && N <= kRouteThreadN)
+    sse_route_thread_kernel<<<static_cast<unsigned>((tokens + 255) / 256), 256, 0, st>>>(route_logits, tokens, N, topk,
+                                                                                       rec, sel_out, dev_err);
+  else
+    sse_route_kernel<<<static_cast<unsigned>((tokens + 7) / 8), 256, 0, st>>>(route_logits, k_logits, tokens, N,
+                                                                             topk, c, !chunk, rec, sel_out, dev_err);
   int rc = check_launch("sse_scan: route kernel");
   if (rc != SDM_OK) return rc;
 
