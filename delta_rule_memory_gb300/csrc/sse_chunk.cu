@@ -388,15 +388,32 @@ __global__ void __launch_bounds__(kPThreads, 2) sse_prep_kernel(const PrepArgs a
     // ---- block products; then per channel and block the running products:
     // alpha -> q * F (F = product in the block up to i), kk -> kk * R (R =
     // product in the block after j)
-    {
+    {  // thread (column r, blocks 2hb and 2hb+1) is the only one touching that column of those blocks
       const int r = tid & 127, hb = tid >> 7;
 #pragma unroll
       for (int Jh = 0; Jh < 2; ++Jh) {
         const int J = 2 * hb + Jh;
+        float al[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) al[k] = sal[(16 * J + k) * kLdA + r];
         float P = 1.f;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) P *= sal[(16 * J + k) * kLdA + r];
+        for (int k = 0; k < 16; ++k) P *= al[k];
         sP[J * kCh + r] = P;
+        float F = 1.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const int i = 16 * J + k;
+          F *= al[k];
+          sal[i * kLdA + r] = bf16_to_f32(sq[i * kCh + r]) * F;
+        }
+        float R = 1.f;
+#pragma unroll
+        for (int k = 15; k >= 0; --k) {
+          const int j = 16 * J + k;
+          skk[j * kLdA + r] *= R;
+          R *= al[k];
+        }
       }
     }
     __syncthreads();
@@ -417,23 +434,6 @@ __global__ void __launch_bounds__(kPThreads, 2) sse_prep_kernel(const PrepArgs a
         }
         sPre[J * kCh + r] = pre;
         sSuf[J * kCh + r] = suf;
-        float al[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k) al[k] = sal[(16 * J + k) * kLdA + r];
-        float F = 1.f;
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const int i = 16 * J + k;
-          F *= al[k];
-          sal[i * kLdA + r] = bf16_to_f32(sq[i * kCh + r]) * F;
-        }
-        float R = 1.f;
-#pragma unroll
-        for (int k = 15; k >= 0; --k) {
-          const int j = 16 * J + k;
-          skk[j * kLdA + r] *= R;
-          R *= al[k];
-        }
       }
     }
     __syncthreads();
