@@ -45,9 +45,9 @@ NCU_TRAFFIC = {
     ("sdm_14b_layer", "sdm"): {"bytes": 12.20e9, "digest": "ce4a87fa8968"},
     # both kernels of one full-size gdn_scan call (746.4 MB + 590.5 MB), profiles/gdn_chunk_dense.md
     ("gdn", "gdn"): {"bytes": 1.337e9, "digest": "e2c62e1f689e"},
-    # the five kernels of one full-size sse_scan call on the chunked path (1.072 GB read + 0.799 GB
+    # the five kernels of one full-size sse_scan call on the chunked path (1.073 GB read + 0.799 GB
     # written), profiles/sse_chunk_prefill.md
-    ("sse", "sse"): {"bytes": 1.870e9, "digest": "b07cb43fb7a2"},
+    ("sse", "sse"): {"bytes": 1.872e9, "digest": "4128ebe70bae"},
 }
 
 
