@@ -13,6 +13,7 @@
 // outside it ties the W-th, and selects the top-W; the weights are the
 // softmax of the selected sums.
 #include <climits>
+#include <cstring>
 
 #include "common.cuh"
 
@@ -170,35 +171,58 @@ __device__ __forceinline__ void half_topk(const uint32_t (&key)[E], int n, int k
   }
 }
 
+// The pruned candidate set P = {(x, y) : (x+1)(y+1) <= W} of the k x k grid
+// of sorted half ranks, in column-major order: every slot outside P is
+// dominated by at least W slots of P (the sorted halves make the sum monotone
+// in x and y), so the top-W lies in P unless the W-th sum ties with a sum
+// outside P.  Entry e (e < n, n <= 64) is (x[e], y[e]); corner[x] is the
+// first y outside P in column x (k if none).  Built on the host from (k, W).
+struct Staircase {
+  int8_t x[64], y[64];
+  int8_t corner[32];
+  int n;
+};
+
+Staircase make_staircase(int k, int W) {
+  Staircase st;
+  memset(&st, 0, sizeof(st));
+  int n = 0;
+  for (int x = 0; x < k; ++x) {
+    const int cnt = min(k, W / (x + 1));
+    for (int y = 0; y < cnt; ++y, ++n)
+      if (n < 64) {
+        st.x[n] = static_cast<int8_t>(x);
+        st.y[n] = static_cast<int8_t>(y);
+      }
+    st.corner[x] = static_cast<int8_t>(min(k, W / (x + 1)));
+  }
+  st.n = n;
+  return st;
+}
+
 // One warp per row, persistent over rows.  E1 = score values per lane of a
 // half; E3 = per-lane candidates of the full k*k fallback (8 or 32).
 template <int E1, int E3>
 __global__ void __launch_bounds__(kAddrWarps * 32) address_kernel(const float *__restrict__ s1,
                                                                   const float *__restrict__ s2, long rows,
-                                                                  int sqrtN, int k, int W,
+                                                                  int sqrtN, int k, int W, const Staircase sc,
                                                                   int32_t *__restrict__ idx_out,
                                                                   float *__restrict__ w_out,
                                                                   int32_t *__restrict__ dev_err) {
   __shared__ uint2 cbuf_all[kAddrWarps][64];
   const int lane = threadIdx.x & 31;
   uint2 *cbuf = cbuf_all[threadIdx.x >> 5];
-  // pruned candidate set P = {(x, y) : (x+1)(y+1) <= W}: every slot outside P
-  // is dominated by at least W slots of P (the sorted halves make the sum
-  // monotone in x and y), so the top-W lies in P unless the W-th sum ties with
-  // a sum outside P.  Lane owns P entries lane and lane+32.
-  int px[2], py[2], npr = 0;
-  px[0] = px[1] = py[0] = py[1] = -1;
-  for (int x = 0; x < k; ++x) {
-    const int cnt = min(k, W / (x + 1));
-    for (int o = 0; o < 2; ++o) {
-      const int c = lane + 32 * o - npr;
-      if (c >= 0 && c < cnt) { px[o] = x; py[o] = c; }
-    }
-    npr += cnt;
+  // lane owns entries lane and lane + 32 of the staircase P
+  int px[2], py[2];
+#pragma unroll
+  for (int o = 0; o < 2; ++o) {
+    const int e = lane + 32 * o;
+    px[o] = e < sc.n ? sc.x[e] : -1;
+    py[o] = e < sc.n ? sc.y[e] : -1;
   }
-  const bool pruned_ok = npr <= 64;
-  // corner of the complement of P in column x: (x, floor(W/(x+1))) if inside the k x k grid
-  const int corner_y = lane < k ? W / (lane + 1) : k;
+  const bool pruned_ok = sc.n <= 64;
+  // corner of the complement of P in column x = lane: (x, floor(W/(x+1))) if inside the k x k grid
+  const int corner_y = lane < k ? sc.corner[lane] : k;
 
   const long stride = static_cast<long>(gridDim.x) * kAddrWarps;
   for (long row = static_cast<long>(blockIdx.x) * kAddrWarps + (threadIdx.x >> 5); row < rows; row += stride) {
@@ -324,8 +348,9 @@ extern "C" int sdm_address(const float *s1, const float *s2, int B, int T, int H
   const dim3 grid(static_cast<unsigned>(blocks));
   const dim3 block(kAddrWarps * 32);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const Staircase sc = make_staircase(k, W);
 #define SDM_AK(A, C) \
-  address_kernel<A, C><<<grid, block, 0, st>>>(s1, s2, rows, sqrtN, k, W, idx_out, w_out, dev_err)
+  address_kernel<A, C><<<grid, block, 0, st>>>(s1, s2, rows, sqrtN, k, W, sc, idx_out, w_out, dev_err)
 #define SDM_AK_E3(A)            \
   if (E3 <= 8) SDM_AK(A, 8);    \
   else SDM_AK(A, 32);
