@@ -148,3 +148,19 @@ def test_chunked_sse_local_clock(golden, monkeypatch):
     np.testing.assert_allclose(S[0, 0, N] / S0[0, 0, N], g["dense_retained"][0], atol=5e-4)
     for p in (2, 3):
         assert np.array_equal(S[0, 0, p].view(np.uint32), S0[0, 0, p].view(np.uint32))
+
+
+@pytest.mark.parametrize("N,topk,path", [(12, 6, "chunk"), (16, 3, "chunk"), (40, 5, "chunk"), (12, 6, "recurrent")])
+def test_routing_ties_go_to_the_lower_partition(N, topk, path, monkeypatch):
+    """Router logits on a coarse integer grid, so most tokens have exact ties:
+    the selected partitions must be the oracle's (lower partition first among
+    equal logits) through the per-thread routing of the chunked path (N <= 16),
+    the per-warp routing (N = 40) and the token-by-token path."""
+    monkeypatch.setenv("SDM_SSE_PATH", path)
+    sdm = need_gpu()
+    sh = synth.SSE_PART.with_(B=1, T=96, H=2, N=N, topk=topk)
+    inp = dict(synth.sse_inputs(sh, seed=40 + N))
+    rng = np.random.default_rng(N + topk)
+    inp["route"] = rng.integers(-2, 3, inp["route"].shape).astype(np.float32)
+    S0 = synth.random_state((1, 2, N + 1, 128, 128), seed=41, scale=0.5)
+    _check(sdm, S0, inp, topk)
