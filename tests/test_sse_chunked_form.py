@@ -161,3 +161,70 @@ def test_block_referenced_factors_stay_finite_under_strong_decay():
             if j >= 0:
                 want = g[i] * g[j] * np.sum(q[i] * kk[j]) * 1e-3 ** (i - j)
                 assert A[i, j] == pytest.approx(want, rel=1e-12, abs=1e-300)
+
+
+def offdiag_blocks_by_stacked_product(q, kk, al, g):
+    """The blocks of A below the diagonal (I > J) as products of two
+    block-referenced operands, the form a tensor-core preparation would use:
+        X_I           = rows of block I of  g q F          (F: product in i's block up to i)
+        Z_J^(s)       = rows of block J of  g kk R * prod_{K=J+1}^{J+s-1} P_K
+        A_IJ          = X_I (Z_J^(I-J))^T
+    so all of them come out of one product X [L, c] times the stacked
+    [Z^(1); Z^(2); Z^(3)]^T [c, 3L], with no quotient of decay products."""
+    L, c = q.shape
+    nb = (L + SUB - 1) // SUB
+    F = np.ones((L, c))
+    R = np.ones((L, c))
+    P = np.ones((nb, c))
+    for J in range(nb):
+        s, e = J * SUB, min(L, J * SUB + SUB)
+        run = np.ones(c)
+        for i in range(s, e):
+            run = run * al[i]
+            F[i] = run
+        P[J] = run
+        run = np.ones(c)
+        for j in range(e - 1, s - 1, -1):
+            R[j] = run
+            run = run * al[j]
+    blk = np.arange(L) // SUB
+    X = g[:, None] * q * F
+    Y = g[:, None] * kk * R
+    Zs = []
+    for span in range(1, nb):        # span = I - J
+        mid = np.ones((L, c))
+        for j in range(L):
+            for K in range(blk[j] + 1, min(nb, blk[j] + span)):
+                mid[j] = mid[j] * P[K]
+        Zs.append(Y * mid)
+    G = X @ np.concatenate(Zs, axis=0).T if Zs else np.zeros((L, 0))   # [L, (nb-1) L]
+    A = np.zeros((L, L))
+    for i in range(L):
+        for j in range(L):
+            span = blk[i] - blk[j]
+            if span >= 1:
+                A[i, j] = G[i, (span - 1) * L + j]
+    return A
+
+
+@pytest.mark.parametrize("L,lo", [(64, 0.05), (53, 0.02), (64, 1e-3)])
+def test_offdiagonal_blocks_as_one_stacked_product(L, lo):
+    """The stacked-product form of A's blocks below the diagonal equals the
+    definition, for full and ragged chunks and under decays strong enough
+    that products over the chunk underflow (every factor stays finite)."""
+    rng = np.random.default_rng(int(L + 1000 * lo))
+    c = 16
+    q = rng.standard_normal((L, c))
+    kk = rng.uniform(0.0, 1.0, (L, c))
+    al = rng.uniform(lo, 1.0, (L, c))
+    g = rng.uniform(0.1, 1.0, L)
+    with np.errstate(under="ignore"):
+        _, _, A, _ = chunk_operands(q, kk, al, g)
+        B = offdiag_blocks_by_stacked_product(q, kk, al, g)
+    blk = np.arange(L) // SUB
+    below = blk[:, None] > blk[None, :]
+    assert np.all(np.isfinite(B))
+    # the same products summed in another order: rounding only (entries that
+    # nearly cancel get an absolute bound scaled to the matrix)
+    np.testing.assert_allclose(B[below], A[below], rtol=1e-10, atol=1e-13 * np.abs(A).max())
+    assert not np.any(B[~below])
