@@ -178,6 +178,27 @@ def test_kda_constant_vector_is_gdn():
     np.testing.assert_array_equal(g[1], kd[1])
 
 
+@pytest.mark.parametrize("per_channel", [False, True])
+def test_gdn_value_columns_evolve_independently(per_channel):
+    """The prediction S~^T k and the read S^T q mix the key rows of the state
+    only, never its value columns (Linear Attention Architectures deck, GDN
+    and KDA updates): a scan over any subset of value columns reproduces
+    those columns of the full scan exactly.  A transposed state or operand
+    anywhere in the recurrence breaks this."""
+    T, dk, dv = 12, 6, 7
+    S0 = RNG.standard_normal((1, 1, dk, dv))
+    q, k = RNG.standard_normal((1, T, 1, dk)), RNG.standard_normal((1, T, 1, dk))
+    v = RNG.standard_normal((1, T, 1, dv))
+    a = RNG.uniform(0.5, 1.0, (1, T, 1, dk) if per_channel else (1, T, 1))
+    b = RNG.uniform(0.1, 0.9, (1, T, 1))
+    S, y = oracle.gdn_scan(S0, q, k, v, a, b, per_channel=per_channel)
+    cols = [1, 4, 6]
+    Ss, ys = oracle.gdn_scan(np.ascontiguousarray(S0[..., cols]), q, k, np.ascontiguousarray(v[..., cols]), a, b,
+                             per_channel=per_channel)
+    np.testing.assert_array_equal(Ss, S[..., cols])
+    np.testing.assert_array_equal(ys, y[..., cols])
+
+
 # ---------------------------------------------------------------------------
 # GDN2 (Linear Attention Architectures deck, "GDN2 separates key-side erase and
 # value-side write", Eqs. 21-24): erase gate b on the key side, write gate w on
