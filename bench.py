@@ -207,7 +207,13 @@ def metric_name(wl) -> str:
         return f"{wl.kind} decode tokens/s (one token per sequence per step; ms_per_step is the step latency)"
     if wl.train:
         return "SDM training step tokens/s (addressing, forward with undo log, scan and address backward)"
-    return METRIC if wl.kind == "sdm" else f"{wl.kind} scan tokens/s"
+    if wl.kind == "sdm":
+        if wl.chunked:
+            return "SDM scan tokens/s in chunked form (sdm_scan_chunked, 1.4B layer); achieved HBM GB/s vs peak"
+        if wl.name != "sdm_14b_layer":
+            return f"SDM scan tokens/s ({wl.name}); achieved HBM GB/s vs peak"
+        return METRIC
+    return f"{wl.kind} scan tokens/s"
 
 
 # ---------------------------------------------------------------- workloads
