@@ -37,16 +37,16 @@ if ROOT not in sys.path:
 METRIC = "SDM scan tokens/s (d=1920,H=2,N=57600,W=R=16); achieved HBM GB/s vs peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM traffic of one sparse_scan launch from an ncu capture, valid only while
-# the kernel source hashes to the recorded digest (see profiles/).
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the dominant
+# call of a workload, recorded from an ncu capture.  It is a record, not a
+# measurement of this run, and is reported only while the kernel source still
+# hashes to the digest it was taken at; otherwise the line carries null.
 NCU_TRAFFIC = {
-    # dram__bytes_read.sum + dram__bytes_write.sum of one full-size launch
-    # (8.01 GB + 4.19 GB), profiles/sparse_scan_1.4b_layer.md
+    # one full-size sparse scan launch: 8.01 GB read + 4.19 GB written
     ("sdm_14b_layer", "sdm"): {"bytes": 12.20e9, "digest": "ce4a87fa8968"},
-    # both kernels of one full-size gdn_scan call (746.4 MB + 590.5 MB), profiles/gdn_chunk_dense.md
+    # both kernels of one full-size gdn_scan call: 746.4 MB read + 590.5 MB written
     ("gdn", "gdn"): {"bytes": 1.337e9, "digest": "e2c62e1f689e"},
-    # the five kernels of one full-size sse_scan call on the chunked path (1.073 GB read + 0.799 GB
-    # written), profiles/sse_chunk_prefill.md
+    # the five kernels of one full-size sse_scan call on the chunked path: 1.073 GB read + 0.799 GB written
     ("sse", "sse"): {"bytes": 1.872e9, "digest": "4128ebe70bae"},
 }
 
@@ -180,9 +180,31 @@ def _oracle_sse_seq(args):
     return time.perf_counter() - t0
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (x86: /proc/cpuinfo; Arm: lscpu)."""
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 class OracleSampler:
     """Runs the oracle over whole (b, h) sequences (first t_sample tokens) in a
-    spawn process pool created before any GPU work."""
+    spawn process pool created before any GPU work.
+
+    The GPU's `value` counts tokens (B*T, each with all H heads), so a sample
+    of `nseq` (b, h) sequences of t_sample tokens is nseq*t_sample/H tokens."""
 
     def __init__(self, cores: int):
         self.cores = max(1, cores)
@@ -193,13 +215,22 @@ class OracleSampler:
         self.pool.join()
 
     def run(self, wl: "Workload", inp: dict, t_sample: int, nseq: int):
+        """All-core run: (tokens, wall seconds), one process per sequence."""
         jobs = wl.oracle_jobs(inp, t_sample, nseq)
         fn = {"sdm": _oracle_sdm_seq, "gdn": _oracle_gdn_seq, "kda": _oracle_gdn_seq, "gdn2": _oracle_gdn2_seq,
               "sse": _oracle_sse_seq}[wl.kind]
         t0 = time.perf_counter()
         self.pool.map(fn, jobs, chunksize=1)
         wall = time.perf_counter() - t0
-        return len(jobs) * t_sample, wall
+        return len(jobs) * t_sample / wl.shape.H, wall
+
+    def run_single(self, wl: "Workload", inp: dict, t_sample: int):
+        """One sequence on one core: (tokens, seconds) of the oracle alone."""
+        job = wl.oracle_jobs(inp, t_sample, 1)
+        fn = {"sdm": _oracle_sdm_seq, "gdn": _oracle_gdn_seq, "kda": _oracle_gdn_seq, "gdn2": _oracle_gdn2_seq,
+              "sse": _oracle_sse_seq}[wl.kind]
+        secs = self.pool.map(fn, job, chunksize=1)[0]
+        return t_sample / wl.shape.H, secs
 
 
 def metric_name(wl) -> str:
@@ -207,12 +238,24 @@ def metric_name(wl) -> str:
         return f"{wl.kind} decode tokens/s (one token per sequence per step; ms_per_step is the step latency)"
     if wl.train:
         return "SDM training step tokens/s (addressing, forward with undo log, scan and address backward)"
+    import synth
+    sh = wl.shape
     if wl.kind == "sdm":
         if wl.chunked:
             return "SDM scan tokens/s in chunked form (sdm_scan_chunked, 1.4B layer); achieved HBM GB/s vs peak"
         if wl.name != "sdm_14b_layer":
             return f"SDM scan tokens/s ({wl.name}); achieved HBM GB/s vs peak"
+        ref = synth.SDM_14B_LAYER
+        changed = [f"{k}={getattr(sh, k)}" for k in ("B", "T") if getattr(sh, k) != getattr(ref, k)]
+        if wl.mode != 0:
+            changed.append("perslot")
+        if changed:
+            # a modified run never reports under the 1.4B layer's metric name
+            return f"SDM scan tokens/s (1.4B layer, {', '.join(changed)}); achieved HBM GB/s vs peak"
         return METRIC
+    if sh.B != {"gdn": synth.GDN_DENSE, "kda": synth.GDN_DENSE, "gdn2": synth.GDN_DENSE,
+                "sse": synth.SSE_PART}[wl.kind].B:
+        return f"{wl.kind} scan tokens/s (B={sh.B})"
     return f"{wl.kind} scan tokens/s"
 
 
@@ -611,10 +654,15 @@ def run_ours(args, rank, world, local_rank, sampler):
     cpu = None
     if sampler is not None:
         nseq = min(sampler.cores, wl.shape.B * wl.shape.H)
-        tok, wall = sampler.run(wl, inp, args.cpu_tokens or wl.shape.T, nseq)
-        cpu = {"value": tok / wall, "unit": "tokens/s", "cores": sampler.cores, "kind": "oracle",
-               "sample": f"{nseq} whole (b,h) sequences x first {args.cpu_tokens or wl.shape.T} tokens of the "
-                         f"same workload, fp64 oracle, one process per sequence ({wall:.1f} s wall)"}
+        t_sample = args.cpu_tokens or wl.shape.T
+        tok, wall = sampler.run(wl, inp, t_sample, nseq)
+        tok1, secs1 = sampler.run_single(wl, inp, t_sample)
+        cpu = {"value": tok / wall, "unit": "tokens/s", "cores": nseq, "kind": "oracle",
+               "single_thread": {"value": tok1 / secs1, "unit": "tokens/s", "seconds": secs1},
+               "cpu_model": cpu_model(), "host_cores": os.cpu_count(),
+               "sample": f"{nseq} whole (b,h) sequences x first {t_sample} tokens of the same workload, fp64 "
+                         f"oracle, one process per sequence ({wall:.1f} s wall); tokens = (b,h) token-steps / "
+                         f"H={wl.shape.H}, the unit of the GPU value; single_thread = one sequence on one core"}
     run = GpuRun(wl, inp, device)
     run.overlap = args.overlap_addressing
     del inp
@@ -740,34 +788,20 @@ def run_reference(args, rank, world):
     for _ in range(args.steps):
         tok, wall = sampler.run(wl, inp, t_sample, nseq)
         walls.append(wall)
+    tok1, secs1 = sampler.run_single(wl, inp, t_sample)
     sampler.close()
     ms = 1e3 * statistics.mean(walls)
     value = tok / (ms * 1e-3)
     sample = (f"{nseq} whole (b,h) sequences x first {t_sample} tokens per step, fp64 oracle, one process per "
-              f"sequence")
+              f"sequence; tokens = (b,h) token-steps / H={wl.shape.H}")
     return {"impl": "reference", "metric": metric_name(wl),
             "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded generators; no dataset or weights)", "config": wl.config(),
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": nseq, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": nseq, "kind": "oracle", "sample": sample,
+                             "single_thread": {"value": tok1 / secs1, "unit": "tokens/s", "seconds": secs1},
+                             "cpu_model": cpu_model(), "host_cores": os.cpu_count()},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-
-
-def run_gather_probe():
-    """Compile and run the row-piece gather probe: the DRAM throughput that
-    the sparse scan's access pattern (random 64-byte pieces of 3840-byte rows,
-    two reads per write) allows, next to larger pieces."""
-    import shutil
-    import tempfile
-    src = os.path.join(ROOT, "delta_rule_memory_gb300", "csrc", "probe", "gather_ceiling.cu")
-    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
-    with tempfile.TemporaryDirectory() as tmp:
-        exe = os.path.join(tmp, "gather_ceiling")
-        subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-o", exe, src], check=True)
-        r = subprocess.run([exe], capture_output=True, text=True)
-        sys.stdout.write(r.stdout)
-        if r.returncode != 0:
-            raise SystemExit(f"gather probe failed: {r.stderr.strip()}")
 
 
 def main():
@@ -784,9 +818,6 @@ def main():
     ap.add_argument("--batch", type=int, default=0, help="override B (small cases for profiling only)")
     ap.add_argument("--e2e-chunk", type=int, default=512,
                     help="tokens per pipelined chunk of the end-to-end sparse step (sdm_forward_host chunk_T)")
-    ap.add_argument("--probe", choices=["gather"], default=None,
-                    help="instead of a step, run a measurement probe: 'gather' times random row-piece gathers and "
-                         "scatters on a 3.54 GB table by piece size (csrc/probe/gather_ceiling.cu)")
     ap.add_argument("--overlap-addressing", action="store_true",
                     help="sparse inference step: run step s+1's addressing on a second stream during step s's "
                          "scan (the scan's own time then includes the interference; on the 1.4B layer the "
@@ -797,9 +828,6 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
 
-    if args.probe == "gather":
-        run_gather_probe()
-        return
     if args.impl == "reference":
         if rank != 0:
             return

@@ -19,15 +19,16 @@ import threading
 import torch
 
 __all__ = [
-    "SdmError", "lib", "library_path", "sdm_version", "sdm_address", "sdm_scan", "sdm_scan_workspace_size",
+    "SdmError", "lib", "library_path", "sdm_version", "sdm_check", "sdm_address", "sdm_scan", "sdm_scan_workspace_size",
     "sdm_scan_noalloc", "sdm_forward_host", "sdm_forward_host_workspace_size", "sdm_scan_train",
     "sdm_scan_backward", "sdm_scan_backward_workspace_size", "sdm_address_backward", "sdm_scan_chunked",
     "sdm_scan_chunked_workspace_size",
     "gdn_scan", "gdn_scan_workspace_size", "gdn2_scan", "sse_scan", "sse_scan_workspace_size", "SDM_RESID_SHARED", "SDM_RESID_PERSLOT", "SSE_WRITE_ADDITIVE", "SSE_WRITE_DELTA",
     "SDM_RESID_ADDITIVE", "SDM_DEVERR_INDEX_RANGE", "SDM_DEVERR_INDEX_REPEAT", "SDM_DEVERR_NONFINITE",
+    "SDM_DEVERR_TIMEOUT", "SDM_ERR_DEVICE",
 ]
 
-SDM_OK, SDM_ERR_INVALID_ARG, SDM_ERR_SHAPE, SDM_ERR_ALIGN, SDM_ERR_UNSUPPORTED, SDM_ERR_CUDA = range(6)
+SDM_OK, SDM_ERR_INVALID_ARG, SDM_ERR_SHAPE, SDM_ERR_ALIGN, SDM_ERR_UNSUPPORTED, SDM_ERR_CUDA, SDM_ERR_DEVICE = range(7)
 SDM_DEVERR_INDEX_RANGE, SDM_DEVERR_INDEX_REPEAT, SDM_DEVERR_NONFINITE, SDM_DEVERR_TIMEOUT = 1, 2, 4, 8
 SDM_DTYPE_F32, SDM_DTYPE_BF16 = 0, 1
 SDM_RESID_SHARED, SDM_RESID_PERSLOT, SDM_RESID_ADDITIVE = 0, 1, 2
@@ -42,6 +43,7 @@ _P, _I, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
 _SIGNATURES = {
     "sdm_version": (_I, []),
     "sdm_last_error": (ctypes.c_char_p, []),
+    "sdm_check": (_I, [_P, _P]),
     "sdm_address": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
     "sdm_scan_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "sdm_scan": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P, _P]),
@@ -121,6 +123,15 @@ def _req(t: torch.Tensor, name: str, dtype, shape=None):
 
 def sdm_version() -> int:
     return lib().sdm_version()
+
+
+def sdm_check(dev_err=None, stream=None) -> None:
+    """Synchronise the stream and raise SdmError (status SDM_ERR_DEVICE) if
+    the error word `dev_err` or the library's own timeout record holds a bit.
+    The timeout record is cleared by the check; `dev_err` is not."""
+    if dev_err is not None:
+        _req(dev_err, "dev_err", torch.int32)
+    _check("sdm_check", lib().sdm_check(_ptr(dev_err), _stream(stream)))
 
 
 def sdm_address(s1: torch.Tensor, s2: torch.Tensor, k: int, W: int, idx_out=None, w_out=None, dev_err=None,
@@ -377,9 +388,11 @@ def sdm_forward_host(s1w, s2w, s1r, s2r, v, alpha, beta, k: int, W: int, R: int,
 
 def sdm_scan_noalloc(state, v, alpha, beta, idx_w, w_w, idx_r, w_r, resid_mode=SDM_RESID_SHARED, y=None,
                      dev_err=None, stream=None):
-    """sdm_scan without a workspace argument: the library keeps the scratch
-    in a fixed 8 MiB device array shared by all calls (see sdm.h).  For
-    callers that cannot allocate device memory; concurrent calls race."""
+    """sdm_scan without a workspace argument, for callers that cannot
+    allocate device memory while running.  The library keeps the scratch in
+    one fixed 32 MiB device array per GPU, shared by all calls: B*T*H may be
+    at most 99,864 when W, R <= 16 and 25,890 otherwise (larger calls raise,
+    SDM_ERR_SHAPE); calls that overlap on the GPU race on the array."""
     _req(state, "state", torch.float32)
     if state.dim() != 4:
         raise ValueError("state must be [B,H,N,d_v]")

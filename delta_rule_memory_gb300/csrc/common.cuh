@@ -27,6 +27,32 @@ __device__ __forceinline__ float key_value(uint32_t k) {
   return __uint_as_float(b);
 }
 
+// Timeouts of bounded on-device waits are never dropped: besides the caller's
+// optional error word, every one is OR-ed into this translation unit's own
+// device word, which sdm_check() reads (and clears) through the accessor that
+// SDM_STICKY_ACCESSOR defines in the same file.
+static __device__ int32_t g_sticky_err;
+
+__device__ __forceinline__ void report_timeout(int32_t *err) {
+  if (err) atomicOr(err, SDM_DEVERR_TIMEOUT);
+  atomicOr(&g_sticky_err, SDM_DEVERR_TIMEOUT);
+}
+
+// host side: read this file's sticky word into *bits and clear it
+#define SDM_STICKY_ACCESSOR(name)                                                        \
+  int name(int32_t *bits) {                                                              \
+    int32_t v = 0;                                                                       \
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_sticky_err, sizeof v);                    \
+    if (e != cudaSuccess) return set_error(SDM_ERR_CUDA, "sdm_check: %s", cudaGetErrorString(e)); \
+    if (v) {                                                                             \
+      const int32_t zero = 0;                                                            \
+      e = cudaMemcpyToSymbol(g_sticky_err, &zero, sizeof zero);                          \
+      if (e != cudaSuccess) return set_error(SDM_ERR_CUDA, "sdm_check: %s", cudaGetErrorString(e)); \
+    }                                                                                    \
+    *bits |= v;                                                                          \
+    return SDM_OK;                                                                       \
+  }
+
 __device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_float(uint32_t(h) << 16); }
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {

@@ -374,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, kPrepCtasPerSm) gdn_prep_kernel(cons
     // the chain kernel then reads invalid tiles but ends normally
     if (tid == 0) mma_commit(mbEnd);
     mbar_wait(mbEnd, 0, kWaitLimit);
-    if (tid == 0 && a.err) atomicOr(a.err, SDM_DEVERR_TIMEOUT);
+    if (tid == 0) report_timeout(a.err);
   }
   tc_fence_before();
   __syncthreads();
@@ -660,7 +660,7 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
   }
   tc_fence_before();
   __syncthreads();
-  if (tid == 0 && *abort_flag && a.err) atomicOr(a.err, SDM_DEVERR_TIMEOUT);
+  if (tid == 0 && *abort_flag) report_timeout(a.err);
   if (warp == 0) tmem_dealloc(tmem, kChainTmemCols);
 }
 
@@ -733,5 +733,7 @@ int launch_gdn_chunk(float *state, const uint16_t *q, const uint16_t *k, const u
   gdn_chain_kernel<<<static_cast<unsigned>(static_cast<long>(B) * H), kChainThreads, kChainSmem, st>>>(ca);
   return check_launch("gdn_scan: chunk chain kernel");
 }
+
+SDM_STICKY_ACCESSOR(sticky_gdn_chunk)
 
 }  // namespace sdm

@@ -24,6 +24,7 @@
 // slots with 16-byte loads.
 #include <climits>
 #include <cstdlib>
+#include <cuda.h>
 #include <mutex>
 
 #include "common.cuh"
@@ -623,13 +624,16 @@ extern "C" int sdm_scan_train(float *state, const void *v, int v_dtype, const fl
 // sdm_scan_noalloc: sdm_scan for callers that cannot hand over device scratch
 // memory.  The per-token records live in a fixed, file-scope device array instead
 // of a caller workspace.  Host code cannot use the array's name as a device
-// address, so the address is looked up once per device with
-// cudaGetSymbolAddress (with that device current) and cached; the first call
-// on a device does this lookup, so make that first call before capturing any
-// stream.  Every call shares the one array: calls that can overlap on the GPU
-// (different streams, or several host threads) race on it and must be
-// serialised by the caller.  Every call rewrites all the records it reads, so
-// nothing has to be cleared between calls.
+// address, so the address is looked up with cudaGetSymbolAddress (with the
+// device current) and cached per device together with the id of the CUDA
+// context it was taken in; a call made in another context (the device's
+// primary context destroyed and created again, e.g. after cudaDeviceReset)
+// looks it up again, because the module, and with it the array, may then sit
+// elsewhere.  The first call in a context does this lookup, so make that first
+// call before capturing any stream.  Every call shares the one array: calls
+// that can overlap on the GPU (different streams, or several host threads)
+// race on it and must be serialised by the caller.  Every call rewrites all the
+// records it reads, so nothing has to be cleared between calls.
 // ---------------------------------------------------------------------------
 namespace sdm {
 namespace {
@@ -639,6 +643,31 @@ __device__ __align__(256) unsigned char g_scan_scratch[kStaticScratchBytes];
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 void *g_scratch_addr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};
+
+// id of the current CUDA context (unique for the life of the process), read
+// through the driver entry points the runtime hands out, so that the library
+// does not link the driver library itself
+int current_context_id(unsigned long long *id) {
+  using GetCurrentFn = CUresult (*)(CUcontext *);
+  using GetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  if (!get_current || !get_id) {
+    void *f1 = nullptr, *f2 = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1) != cudaSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) != cudaSuccess ||
+        q1 != cudaDriverEntryPointSuccess || q2 != cudaDriverEntryPointSuccess || !f1 || !f2)
+      return set_error(SDM_ERR_CUDA, "sdm_scan_noalloc: driver entry points cuCtxGetCurrent/cuCtxGetId unavailable");
+    get_current = reinterpret_cast<GetCurrentFn>(f1);
+    get_id = reinterpret_cast<GetIdFn>(f2);
+  }
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, id) != CUDA_SUCCESS)
+    return set_error(SDM_ERR_CUDA, "sdm_scan_noalloc: no current CUDA context");
+  return SDM_OK;
+}
 
 int static_scratch(void **out) {
   int dev = 0;
@@ -646,12 +675,29 @@ int static_scratch(void **out) {
   if (e != cudaSuccess) return set_error(SDM_ERR_CUDA, "sdm_scan_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices) return set_error(SDM_ERR_UNSUPPORTED, "sdm_scan_noalloc: device %d", dev);
   std::lock_guard<std::mutex> lock(g_scratch_mu);
+  unsigned long long ctx_id = 0;
   if (!g_scratch_addr[dev]) {
+    // the first lookup on this device: the runtime makes the primary context
+    // current here if no context is yet
     void *p = nullptr;
     e = cudaGetSymbolAddress(&p, g_scan_scratch);
     if (e != cudaSuccess || !p)
       return set_error(SDM_ERR_CUDA, "sdm_scan_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    const int rc = current_context_id(&ctx_id);
+    if (rc != SDM_OK) return rc;
     g_scratch_addr[dev] = p;
+    g_scratch_ctx[dev] = ctx_id;
+  } else {
+    const int rc = current_context_id(&ctx_id);
+    if (rc != SDM_OK) return rc;
+    if (ctx_id != g_scratch_ctx[dev]) {
+      void *p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_scan_scratch);
+      if (e != cudaSuccess || !p)
+        return set_error(SDM_ERR_CUDA, "sdm_scan_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+      g_scratch_addr[dev] = p;
+      g_scratch_ctx[dev] = ctx_id;
+    }
   }
   *out = g_scratch_addr[dev];
   return SDM_OK;

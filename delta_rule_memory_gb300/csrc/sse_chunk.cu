@@ -800,7 +800,7 @@ __global__ void __maxnreg__(96) sse_chain_kernel(const ChainArgs a) {
   }
   tc_fence_before();
   __syncthreads();
-  if (tid == 0 && *abort_flag && a.err) atomicOr(a.err, SDM_DEVERR_TIMEOUT);
+  if (tid == 0 && *abort_flag) report_timeout(a.err);
   if (warp == 0) tmem_dealloc(tmem, kChainTmemCols);
 }
 
@@ -915,5 +915,7 @@ int launch_sse_chunk(float *state, const uint32_t *rec, int rw, const float *klo
                                                                     reinterpret_cast<float4 *>(y), n4, topk + 1);
   return check_launch("sse_scan: combine kernel");
 }
+
+SDM_STICKY_ACCESSOR(sticky_sse_chunk)
 
 }  // namespace sdm

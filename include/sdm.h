@@ -57,12 +57,20 @@ extern "C" {
 #define SDM_ERR_ALIGN 3        /* pointer not aligned as required */
 #define SDM_ERR_UNSUPPORTED 4  /* unknown dtype or mode */
 #define SDM_ERR_CUDA 5         /* a CUDA launch or copy failed */
+#define SDM_ERR_DEVICE 6       /* sdm_check: a device-side error was recorded */
 
 /* Device-side error bits (OR-ed into *dev_err when dev_err != NULL). */
 #define SDM_DEVERR_INDEX_RANGE 1  /* a slot index outside [0, N) (skipped) */
 #define SDM_DEVERR_INDEX_REPEAT 2 /* a slot repeated within one token's write list */
 #define SDM_DEVERR_NONFINITE 4    /* a NaN or infinite score or logit */
 #define SDM_DEVERR_TIMEOUT 8      /* a bounded on-device wait gave up; outputs invalid */
+
+/*
+ * A timeout (SDM_DEVERR_TIMEOUT) leaves that call's y AND the state it updated
+ * in place undefined; every later call that continues the state builds on the
+ * corrupt values.  So timeouts are never dropped: each one is also recorded in
+ * a library-owned device word, whether or not the call had a dev_err.
+ */
 
 /*
  * Environment variables read at each call (all optional; unset = the library's
@@ -99,6 +107,16 @@ SDM_API int sdm_version(void);
 
 /* Text of the last error raised by a call on this host thread ("" if none). */
 SDM_API const char *sdm_last_error(void);
+
+/*
+ * sdm_check - the device-side status check.  Synchronises `stream`, then reads
+ * the caller's error word `dev_err` (optional; not cleared) and the library's
+ * own timeout record (cleared by this call).  Returns SDM_OK if no bit is set,
+ * SDM_ERR_DEVICE if any is (sdm_last_error() names the bits), SDM_ERR_CUDA if
+ * the synchronisation or a read failed.  Not capturable (it synchronises);
+ * call it after a step, not inside one.
+ */
+SDM_API int sdm_check(const int32_t *dev_err, void *stream);
 
 /*
  * sdm_address - product-key addressing, [SDM] "Product keys select addresses
@@ -221,7 +239,9 @@ SDM_API int sdm_forward_host(const float *s1w, const float *s2w, const float *s1
  * when W, R <= 16 (336 bytes per token-head) and B*T*H <= 25890 when either
  * is larger (1296 bytes); larger calls return SDM_ERR_SHAPE and launch nothing.
  * Set-up: the first call on a device looks up the array's device address
- * (with that device current); make that first call before any stream capture.
+ * (with that device current) and remembers it for the current CUDA context; a
+ * call from a new context on that device (after cudaDeviceReset, say) looks it
+ * up again.  Make the first call in each context before any stream capture.
  * Sharing: all calls in the process share the one array, which keeps the last
  * call's contents (nothing in it needs clearing: every call rewrites what it
  * reads).  Calls that can overlap on the GPU - on different streams, or from

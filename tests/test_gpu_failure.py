@@ -69,3 +69,36 @@ def test_sse_chain_wait_runs_out_and_the_context_stays_usable(monkeypatch):
     assert_y_close(y, yr)
     assert_state_close(S, Sr)
     assert np.all(np.isfinite(S))
+
+
+def test_timeout_without_error_word_is_reported_by_sdm_check(monkeypatch):
+    """A call made without dev_err still cannot lose a timeout: the library
+    records it in its own device word and sdm_check reports it (then clears
+    it, so the next check after a clean call passes)."""
+    import torch
+    sdm = need_gpu()
+    try:  # start from a clean record (the tests above leave timeouts in it)
+        sdm.sdm_check()
+    except sdm.SdmError:
+        pass
+    sdm.sdm_check()
+    monkeypatch.setenv("SDM_GDN_PATH", "chunk")
+    sh = synth.GDN_DENSE.with_(B=1, T=200, H=2)
+    inp = synth.gdn_inputs(sh, seed=94)
+    S0 = synth.random_state((1, 2, 128, 128), seed=95, scale=0.3)
+    monkeypatch.setenv("SDM_TEST_DROP_SIGNAL", "1")
+    sdm.gdn_scan(dev(S0), dev(inp["q"]), dev(inp["k"]), dev(inp["v"]), dev(inp["alpha_gdn"]), dev(inp["beta"]),
+                 False)
+    with pytest.raises(sdm.SdmError) as e:
+        sdm.sdm_check()
+    assert e.value.code == sdm.SDM_ERR_DEVICE
+    assert "wait gave up" in str(e.value)
+    monkeypatch.delenv("SDM_TEST_DROP_SIGNAL")
+    S, y, err = _gdn(sdm, S0, inp)
+    assert err == 0
+    sdm.sdm_check()
+    # the caller's own word is reported too (and left as it is)
+    word = torch.full((1,), SDM_DEVERR_TIMEOUT, dtype=torch.int32, device="cuda")
+    with pytest.raises(sdm.SdmError):
+        sdm.sdm_check(word)
+    assert int(host(word)[0]) == SDM_DEVERR_TIMEOUT
