@@ -416,7 +416,7 @@ class GpuRun:
             self.y = torch.empty((sh.B, sh.T, sh.H, sh.dv), dtype=torch.float32, device=device)
             nws = sdm.gdn_scan_workspace_size(sh.B, sh.T, sh.H, sh.dk, sh.dv, wl.kind == "kda")
             self.ws = torch.empty(max(nws, 1), dtype=torch.uint8, device=device)
-            # chunked GDN: preparation kernel + chain kernel; KDA: one recurrent kernel
+            # chunked GDN / KDA: preparation kernel + chain kernel; token-recurrent: one kernel
             self.launches_per_step = 2 if nws > 0 else 1
         else:
             self.state = torch.zeros((sh.B, sh.H, sh.N + 1, sh.c, sh.d), dtype=torch.float32, device=device)
@@ -725,7 +725,7 @@ def run_ours(args, rank, world, local_rank, sampler):
         # FP32 FMA pipe: 152 SMs x 128 lanes x 2 flop x max SM clock
         peak = 152 * 128 * 2 * float(pk.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
         achieved = algo / (main_ms * 1e-3) / 1e12
-    kernel_file = {"sdm": "sparse_scan.cu", "gdn": "gdn_chunk.cu", "kda": "gdn_scan.cu", "gdn2": "gdn_scan.cu",
+    kernel_file = {"sdm": "sparse_scan.cu", "gdn": "gdn_chunk.cu", "kda": "gdn_chunk.cu", "gdn2": "gdn_scan.cu",
                    "sse": "sse_chunk.cu" if wl.sse_chunked else "sse_scan.cu"}[wl.kind]
     tr = NCU_TRAFFIC.get((wl.name, wl.kind))
     traffic = tr["bytes"] if tr and tr["digest"] == _src_digest(kernel_file) else None
@@ -749,7 +749,8 @@ def run_ours(args, rank, world, local_rank, sampler):
                      "kernel": "sdm_scan_train + sdm_scan_backward + 2 sdm_address_backward" if wl.train else
                      "sdm_scan_chunked (chunk preparation + chain kernels)" if wl.chunked else
                      {"sdm": "sdm_scan (hazard prepass + sparse_scan_kernel)",
-                      "gdn": "gdn_scan (chunk preparation + chain kernels)", "kda": "gdn_scan", "gdn2": "gdn2_scan",
+                      "gdn": "gdn_scan (chunk preparation + chain kernels)",
+                      "kda": "gdn_scan, per-channel decay (KDA chunk preparation + chain kernels)", "gdn2": "gdn2_scan",
                       "sse": "sse_scan (route, group, chunk preparation, chain, combine kernels)"
                       if wl.sse_chunked else "sse_scan (route prepass + sse_scan_kernel)"}[wl.kind],
                      "launch_ms": main_ms, "peak_source": f"{src} ({'hbm_gbs' if bound == 'hbm' else 'FP32 lanes x clock'})",

@@ -95,6 +95,83 @@ constexpr uint32_t kPrepSmem = kPBar + 64;
 constexpr uint32_t kPColGP = 0, kPColW = 64, kPColU = 128, kPrepTmemCols = 256;
 static_assert(2 * (kPrepSmem + 1024) <= 228 * 1024, "two preparation CTAs per SM");
 
+// L^-1 for L = I + A, A strictly lower triangular (fp32, row stride kLd): the
+// 16x16 diagonal blocks by substitution, then the blocks below the diagonal
+// one block distance at a time, X_IJ = -L_II^-1 sum_{K=J}^{I-1} L_IK X_KJ,
+// each thread computing a 1 x 4 strip with 16-byte loads.  Reads only the
+// strictly lower part of sA; writes the lower triangle (diagonal included) of
+// sTf; sZ holds 768 floats of block products.  Called by all kThreads threads
+// (it synchronises the CTA).
+__device__ __forceinline__ void solve_unit_lower(const float *sA, float *sTf, float *sZ, int tid) {
+  if (tid < 64) {
+    const int I = tid >> 4, cc = tid & 15, o = I * 16;
+    float xv[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      float acc = (r == cc) ? 1.f : 0.f;
+#pragma unroll
+      for (int j = 0; j < r; ++j) acc -= sA[(o + r) * kLd + o + j] * xv[j];
+      xv[r] = acc;
+    }
+#pragma unroll
+    for (int r = 0; r < 16; ++r) sTf[(o + r) * kLd + o + cc] = xv[r];
+  }
+  __syncthreads();
+  // ... then the blocks below the diagonal, one block distance at a time:
+  // X_IJ = -L_II^-1 sum_{K=J}^{I-1} L_IK X_KJ.  A thread computes a 1 x 4
+  // strip (pair p, row r, columns c4..c4+3) with 16-byte loads.
+#pragma unroll
+  for (int dist = 1; dist < 4; ++dist) {
+    const bool mine = tid < (4 - dist) * 64;
+    const int p = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
+    const int J = p, I = p + dist;
+    if (mine) {
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int K = 0; K < dist; ++K) {
+        const float *arow = sA + (I * 16 + r) * kLd + (J + K) * 16;
+        const float *xcol = sTf + (J + K) * 16 * kLd + J * 16 + c4;
+#pragma unroll
+        for (int k4 = 0; k4 < 16; k4 += 4) {
+          const float4 av = *reinterpret_cast<const float4 *>(arow + k4);
+          const float aa[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float4 xv = *reinterpret_cast<const float4 *>(xcol + (k4 + e) * kLd);
+            acc[0] = fmaf(aa[e], xv.x, acc[0]);
+            acc[1] = fmaf(aa[e], xv.y, acc[1]);
+            acc[2] = fmaf(aa[e], xv.z, acc[2]);
+            acc[3] = fmaf(aa[e], xv.w, acc[3]);
+          }
+        }
+      }
+      *reinterpret_cast<float4 *>(sZ + p * 256 + r * 16 + c4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    }
+    __syncthreads();
+    if (mine) {
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      const float *xrow = sTf + (I * 16 + r) * kLd + I * 16;
+      const float *zcol = sZ + p * 256 + c4;
+#pragma unroll
+      for (int k4 = 0; k4 < 16; k4 += 4) {
+        const float4 xv = *reinterpret_cast<const float4 *>(xrow + k4);
+        const float xx[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float4 zv = *reinterpret_cast<const float4 *>(zcol + (k4 + e) * 16);
+          acc[0] = fmaf(xx[e], zv.x, acc[0]);
+          acc[1] = fmaf(xx[e], zv.y, acc[1]);
+          acc[2] = fmaf(xx[e], zv.z, acc[2]);
+          acc[3] = fmaf(xx[e], zv.w, acc[3]);
+        }
+      }
+      *reinterpret_cast<float4 *>(sTf + (I * 16 + r) * kLd + J * 16 + c4) =
+          make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
+    }
+    __syncthreads();
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, kPrepCtasPerSm) gdn_prep_kernel(const PrepArgs a) {
   extern __shared__ __align__(1024) unsigned char sm[];
   const int tid = threadIdx.x;
@@ -246,74 +323,8 @@ __global__ void __launch_bounds__(kThreads, kPrepCtasPerSm) gdn_prep_kernel(cons
     }
     __syncthreads();
 
-    // ---- L^-1: 16x16 diagonal blocks by substitution ...
-    if (tid < 64) {
-      const int I = tid >> 4, cc = tid & 15, o = I * 16;
-      float xv[16];
-#pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        float acc = (r == cc) ? 1.f : 0.f;
-#pragma unroll
-        for (int j = 0; j < r; ++j) acc -= sA[(o + r) * kLd + o + j] * xv[j];
-        xv[r] = acc;
-      }
-#pragma unroll
-      for (int r = 0; r < 16; ++r) sTf[(o + r) * kLd + o + cc] = xv[r];
-    }
-    __syncthreads();
-    // ... then the blocks below the diagonal, one block distance at a time:
-    // X_IJ = -L_II^-1 sum_{K=J}^{I-1} L_IK X_KJ.  A thread computes a 1 x 4
-    // strip (pair p, row r, columns c4..c4+3) with 16-byte loads.
-#pragma unroll
-    for (int dist = 1; dist < 4; ++dist) {
-      const bool mine = tid < (4 - dist) * 64;
-      const int p = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
-      const int J = p, I = p + dist;
-      if (mine) {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int K = 0; K < dist; ++K) {
-          const float *arow = sA + (I * 16 + r) * kLd + (J + K) * 16;
-          const float *xcol = sTf + (J + K) * 16 * kLd + J * 16 + c4;
-#pragma unroll
-          for (int k4 = 0; k4 < 16; k4 += 4) {
-            const float4 av = *reinterpret_cast<const float4 *>(arow + k4);
-            const float aa[4] = {av.x, av.y, av.z, av.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float4 xv = *reinterpret_cast<const float4 *>(xcol + (k4 + e) * kLd);
-              acc[0] = fmaf(aa[e], xv.x, acc[0]);
-              acc[1] = fmaf(aa[e], xv.y, acc[1]);
-              acc[2] = fmaf(aa[e], xv.z, acc[2]);
-              acc[3] = fmaf(aa[e], xv.w, acc[3]);
-            }
-          }
-        }
-        *reinterpret_cast<float4 *>(sZ + p * 256 + r * 16 + c4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      }
-      __syncthreads();
-      if (mine) {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        const float *xrow = sTf + (I * 16 + r) * kLd + I * 16;
-        const float *zcol = sZ + p * 256 + c4;
-#pragma unroll
-        for (int k4 = 0; k4 < 16; k4 += 4) {
-          const float4 xv = *reinterpret_cast<const float4 *>(xrow + k4);
-          const float xx[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float4 zv = *reinterpret_cast<const float4 *>(zcol + (k4 + e) * 16);
-            acc[0] = fmaf(xx[e], zv.x, acc[0]);
-            acc[1] = fmaf(xx[e], zv.y, acc[1]);
-            acc[2] = fmaf(xx[e], zv.z, acc[2]);
-            acc[3] = fmaf(xx[e], zv.w, acc[3]);
-          }
-        }
-        *reinterpret_cast<float4 *>(sTf + (I * 16 + r) * kLd + J * 16 + c4) =
-            make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
-      }
-      __syncthreads();
-    }
+    // ---- L^-1 (unit lower triangular inverse of I + A)
+    solve_unit_lower(sA, sTf, sZ, tid);
     // T = L^-1 diag(beta) and T diag(gamma), lower triangles, as B-operand tiles
     {
       const int i = tid >> 2, j0 = (tid & 3) * 16;
@@ -382,6 +393,483 @@ __global__ void __launch_bounds__(kThreads, kPrepCtasPerSm) gdn_prep_kernel(cons
 }
 
 // ===========================================================================
+// Kernel 1 for KDA (a decay per key channel; Linear Attention Architectures
+// deck, "GDN and KDA change the granularity of forgetting", Eqs. 18-20).
+//
+// With lambda_ir = sum_{t<=i} log alpha_tr (per channel r, within the chunk),
+// the chunk form keeps the shape of the GDN one, but every decay sits inside
+// the channel sums:
+//   A_ij  = beta_i sum_r k_ir k_jr e^{lambda_ir - lambda_jr}         (j < i)
+//   Mq_ij = sum_r q_ir k_jr e^{lambda_ir - lambda_jr}                (j <= i)
+//   Qt_i = q_i (.) e^{lambda_i},  Kt_i = k_i (.) e^{lambda_i},
+//   Khat_j = k_j (.) e^{lambda_C - lambda_j},  gamma_C = e^{lambda_C}
+//   T = (I + A)^-1 diag(beta),  W = T Kt,  Ut = T V
+// and the chain runs  U = Ut - W S0,  Y = Qt S0 + Mq U,
+// S_C = diag(gamma_C) S0 + Khat^T U.
+// A and Mq cannot be one K K^T product: each pair needs its own per-channel
+// decay.  Every pair j < i of the chunk is split at the highest bit in which
+// i and j differ (level l = 0..5, half size h = 32 >> l): i lies in the right
+// half and j in the left half of a segment of 2h tokens whose left half ends
+// at token b, so the decay is e^{lambda_i - lambda_b} e^{lambda_b - lambda_j},
+// two factors that are each a decay ratio of at most 1 (no factor is ever an
+// inverse decay).  Levels 0-3 become two tcgen05 products of block-referenced
+// operands (levels 0+1, then 2+3):
+//   rows  [k_i; q_i] (.) e^{lambda_i - lambda_b}  (right-half tokens)
+//   cols  k_j (.) e^{lambda_b - lambda_j}         (left-half tokens)
+// of which only the pairs in the same segment are kept.  Pairs inside a block
+// of 4 tokens (levels 4, 5) and the diagonal of Mq are summed on the CUDA
+// cores with running products of alpha.  One CTA per SM.
+// ===========================================================================
+// ---- one KDA chunk's tiles in the workspace (bytes)
+constexpr uint32_t kVW = 0;        // W hi, lo        [64 i][128 c]   MN-major, as kUW
+constexpr uint32_t kVQ = 32768;    // Qt hi, lo       [64 i][128 c]   K-major
+constexpr uint32_t kVMq = 65536;   // Mq hi, lo       [64 i][64 j]
+constexpr uint32_t kVKh = 81920;   // Khat hi, lo     [64 j][128 c]
+constexpr uint32_t kVG = 114688;   // gamma_C         fp32 [128] (per key channel)
+constexpr uint32_t kVU = 115200;   // Ut = T V        fp32 [64 i][128 d]
+constexpr uint32_t kVUnit = kVU + kC * kDV * 4;
+static_assert(kVUnit % 16 == 0 && kVMq % 16 == 0 && (kVG - kVMq) % 16 == 0 && (kVU - kVG) % 16 == 0,
+              "bulk copies need 16-byte multiples");
+
+struct KdaPrepArgs {
+  const uint16_t *q, *k, *v;
+  const float *alpha, *beta;
+  unsigned char *ws;
+  int T, H, nchunks;
+  long units;  // B * H * nchunks
+  int32_t *err;
+};
+
+constexpr int kLdL = kDK + 4;  // fp32 row stride of lambda (8 consecutive rows hit distinct banks)
+constexpr int kLdS = kC + 1;   // fp32 row stride of the A / Mq staging (a column is conflict-free)
+// shared memory (bytes)
+constexpr uint32_t kKK = 0;                       // K tile bf16 [64][128] K-major          16 KB
+constexpr uint32_t kKQ = 16384;                   // Q tile                                 16 KB
+constexpr uint32_t kKV = 32768;                   // V tile                                 16 KB
+constexpr uint32_t kKLam = 49152;                 // lambda fp32 [64][kLdL]
+constexpr uint32_t kKAl = kKLam + kC * kLdL * 4;  // alpha fp32 [64][128]; then A, Mq staging [64][kLdS]
+constexpr uint32_t kKAlBytes = 2 * kC * kLdS * 4;
+constexpr uint32_t kKOp = kKAl + kKAlBytes;       // level operands: rows hi, lo [128][128], cols hi, lo [64][128]
+constexpr uint32_t kKOpBytes = 98304;
+constexpr uint32_t kKGate = kKOp + kKOpBytes;     // beta [64], block-of-4 sums [16][16]
+constexpr uint32_t kKBar = kKGate + (kC + 256) * 4;
+constexpr uint32_t kKdaSmem = kKBar + 64;
+// inside the operand region once the level products are done
+constexpr uint32_t kOL = 0;                       // L = I + A, fp32 [64][kLd]
+constexpr uint32_t kOTf = kOL + kSolve;           // L^-1
+constexpr uint32_t kOZ = kOTf + kSolve;           // block products of the solve (768 floats)
+constexpr uint32_t kOT = kOZ + 4096;              // T hi, lo [64 i][64 j]
+constexpr uint32_t kOKt = kOT + 16384;            // Kt hi, lo [64][128]
+static_assert(kKAlBytes >= kC * kDK * 4, "alpha fits the staging region");
+static_assert(kOKt + 32768 <= kKOpBytes, "solve and Kt fit the operand region");
+static_assert(kKdaSmem <= 227 * 1024, "one KDA preparation CTA per SM");
+constexpr uint32_t kKColG1 = 0, kKColG2 = 64, kKColW = 128, kKColU = 192, kKdaTmemCols = 256;
+
+// Operands of the level pair (la, lb) into the operand region: rows
+// [k@la; q@la; k@lb; q@lb] of the right-half tokens (32 each) and cols
+// [k@la; k@lb] of the left-half tokens, hi/lo K-major.  A thread takes 8
+// channels of one row; 8 consecutive threads take 8 consecutive rows (one
+// 128-byte core-matrix row group, so stores and lambda loads are conflict-free).
+__device__ __forceinline__ void kda_level_operands(int la, int lb, const unsigned char *sK, const unsigned char *sQ,
+                                                   const float *lam, unsigned char *op, int tid) {
+  for (int id = tid; id < 3072; id += kThreads) {
+    const bool is_row = id < 2048;
+    const int idd = is_row ? id : id - 2048;
+    const int row = ((idd >> 7) << 3) | (idd & 7), g = (idd >> 3) & 15;
+    const int sub = row >> 5, w = row & 31;
+    const int lvl = is_row ? (sub < 2 ? la : lb) : (sub == 0 ? la : lb);
+    const int sh = 5 - lvl, h = 1 << sh, seg = w >> sh;
+    const int b = 2 * h * seg + h - 1;                                 // last token of the left half
+    const int t = is_row ? b + 1 + (w & (h - 1)) : b - h + 1 + (w & (h - 1));
+    const bool from_q = is_row && (sub & 1);
+    const uint4 raw = *reinterpret_cast<const uint4 *>((from_q ? sQ : sK) + kmajor_off(t, 8 * g, kDK));
+    const float4 lt0 = *reinterpret_cast<const float4 *>(lam + t * kLdL + 8 * g);
+    const float4 lt1 = *reinterpret_cast<const float4 *>(lam + t * kLdL + 8 * g + 4);
+    const float4 lb0 = *reinterpret_cast<const float4 *>(lam + b * kLdL + 8 * g);
+    const float4 lb1 = *reinterpret_cast<const float4 *>(lam + b * kLdL + 8 * g + 4);
+    const float dt[8] = {lt0.x - lb0.x, lt0.y - lb0.y, lt0.z - lb0.z, lt0.w - lb0.w,
+                         lt1.x - lb1.x, lt1.y - lb1.y, lt1.z - lb1.z, lt1.w - lb1.w};
+    const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
+    float x[8];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      // right-half row: e^{lambda_t - lambda_b} (t > b); left-half col: e^{lambda_b - lambda_t} (t <= b)
+      x[2 * e] = bf16_to_f32(static_cast<uint16_t>(rw[e] & 0xffff)) * __expf(is_row ? dt[2 * e] : -dt[2 * e]);
+      x[2 * e + 1] = bf16_to_f32(static_cast<uint16_t>(rw[e] >> 16)) * __expf(is_row ? dt[2 * e + 1] : -dt[2 * e + 1]);
+    }
+    if (is_row)
+      store_split8(op, op + 32768, kmajor_off(row, 8 * g, kDK), x);
+    else
+      store_split8(op + 65536, op + 81920, kmajor_off(row, 8 * g, kDK), x);
+  }
+}
+
+// The pairs of the level pair (la, lb) kept from the product in tensor memory
+// (lanes = operand rows, columns = operand cols) into the A / Mq staging.
+// Warp w reads lanes 32*(w%4) (one row kind) and 16 of its level's 32 columns.
+__device__ __forceinline__ void kda_level_extract(int la, int lb, uint32_t tmem_col, float *sAst, float *sMst,
+                                                  const float *be, int warp, int lane) {
+  const int sub = warp & 3, half = warp >> 2;
+  const int lvl = sub < 2 ? la : lb;
+  const int sh = 5 - lvl, h = 1 << sh;
+  float x[16];
+  tmem_ld16(tmem_col + (static_cast<uint32_t>(32 * sub) << 16) + 32 * (sub >> 1) + 16 * half, x);
+  tmem_ld_wait();
+  const int u = lane, seg = u >> sh;
+  const int ti = 2 * h * seg + h + (u & (h - 1));
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    const int v = 16 * half + e;
+    if ((v >> sh) == seg) {
+      const int tj = 2 * h * seg + (v & (h - 1));
+      if (sub & 1)
+        sMst[ti * kLdS + tj] = x[e];
+      else
+        sAst[ti * kLdS + tj] = be[ti] * x[e];
+    }
+  }
+}
+
+__device__ __forceinline__ void kda_issue_level_mma(uint32_t tmem_d, uint32_t op_addr, uint32_t mbar) {
+  const uint64_t dLh = smem_desc(op_addr, 128, kDK * 16), dLl = smem_desc(op_addr + 32768, 128, kDK * 16);
+  const uint64_t dRh = smem_desc(op_addr + 65536, 128, kDK * 16), dRl = smem_desc(op_addr + 81920, 128, kDK * 16);
+  const uint32_t id = idesc_bf16_f32(128, 64);
+#pragma unroll
+  for (int ks = 0; ks < kDK / 16; ++ks) {
+    mma_bf16(tmem_d, dLh + 16u * ks, dRh + 16u * ks, id, ks > 0);
+    mma_bf16(tmem_d, dLh + 16u * ks, dRl + 16u * ks, id, true);
+    mma_bf16(tmem_d, dLl + 16u * ks, dRh + 16u * ks, id, true);
+  }
+  mma_commit(mbar);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs a) {
+  extern __shared__ __align__(1024) unsigned char sm[];
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int row = tid & 127;
+  const int half = tid >> 7;
+  const int lane_base = 32 * (warp & 3);
+  const int T = a.T, H = a.H;
+
+  unsigned char *sK = sm + kKK, *sQ = sm + kKQ, *sV = sm + kKV;
+  float *lam = reinterpret_cast<float *>(sm + kKLam);
+  float *al = reinterpret_cast<float *>(sm + kKAl);
+  float *sAst = reinterpret_cast<float *>(sm + kKAl), *sMst = sAst + kC * kLdS;
+  unsigned char *op = sm + kKOp;
+  float *sL = reinterpret_cast<float *>(op + kOL), *sTf = reinterpret_cast<float *>(op + kOTf);
+  float *sZ = reinterpret_cast<float *>(op + kOZ);
+  unsigned char *sTh = op + kOT, *sTl = op + kOT + 8192, *sKth = op + kOKt, *sKtl = op + kOKt + 16384;
+  float *be = reinterpret_cast<float *>(sm + kKGate);
+  float *w4 = be + kC;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kKBar);
+  uint32_t *holder = reinterpret_cast<uint32_t *>(sm + kKBar + 32);
+  const uint32_t mbG = smem_addr(bars + 0), mbW = smem_addr(bars + 1), mbEnd = smem_addr(bars + 2);
+
+  if (tid == 0) {
+    mbar_init(mbG, 1);
+    mbar_init(mbW, 1);
+    mbar_init(mbEnd, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(smem_addr(holder), kKdaTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *holder;
+  const uint32_t op_addr = smem_addr(op);
+  // W^T = Kt^T T^T and Ut^T = V^T T^T: A operands MN-major (k-step = 16 tokens = 4096 bytes)
+  const uint64_t dKtmn_h = smem_desc(smem_addr(sKth), 2048, 128), dKtmn_l = smem_desc(smem_addr(sKtl), 2048, 128);
+  const uint64_t dVmn = smem_desc(smem_addr(sV), 2048, 128);
+  const uint64_t dTh = smem_desc(smem_addr(sTh), 128, kC * 16), dTl = smem_desc(smem_addr(sTl), 128, kC * 16);
+  const uint32_t idMN = idesc_bf16_f32(128, kC) | (1u << 15);
+
+  bool failed = false;
+  auto wait_ok = [&](uint32_t mb, uint32_t parity) -> bool {
+    const bool ok = mbar_wait(mb, parity, kWaitLimit);
+    tc_fence_before();
+    const bool all = __syncthreads_and(ok) != 0;
+    tc_fence_after();
+    return all;
+  };
+
+  int it = 0;
+  for (long u = blockIdx.x; u < a.units; u += gridDim.x, ++it) {
+    unsigned char *ws = a.ws + u * kVUnit;
+    const long bh = u / a.nchunks;
+    const int t0 = static_cast<int>(u - bh * a.nchunks) * kC;
+    const long tok0 = (bh / H) * T * H + bh % H;
+
+    // ---- inputs: K, Q, V tiles, alpha rows, beta (padding: k = q = v = 0, alpha = 1, beta = 0)
+    for (int id = tid; id < 3 * kC * 16; id += kThreads) {
+      const int m = id >> 10, r = (id >> 4) & 63, k8 = id & 15;
+      const int t = t0 + r;
+      unsigned char *dst = sm + (m == 0 ? kKK : m == 1 ? kKQ : kKV) + kmajor_off(r, k8 * 8, kDK);
+      if (t < T)
+        cp_async<16>(dst, (m == 0 ? a.k : m == 1 ? a.q : a.v) + (tok0 + static_cast<long>(t) * H) * kDK + k8 * 8);
+      else
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+    }
+    for (int id = tid; id < kC * (kDK / 4); id += kThreads) {
+      const int r = id >> 5, c4 = id & 31;
+      const int t = t0 + r;
+      if (t < T)
+        cp_async<16>(al + r * kDK + 4 * c4, a.alpha + (tok0 + static_cast<long>(t) * H) * kDK + 4 * c4);
+      else
+        *reinterpret_cast<float4 *>(al + r * kDK + 4 * c4) = make_float4(1.f, 1.f, 1.f, 1.f);
+    }
+    if (tid < kC) {
+      const int t = t0 + tid;
+      if (t < T)
+        cp_async<4>(be + tid, a.beta + tok0 + static_cast<long>(t) * H);
+      else
+        be[tid] = 0.f;
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
+
+    if (tid < kDK) {
+      // ---- lambda: running sum of log alpha over the chunk, one thread per channel
+      float acc = 0.f;
+#pragma unroll 8
+      for (int t = 0; t < kC; ++t) {
+        acc += __logf(al[t * kDK + tid]);
+        lam[t * kLdL + tid] = acc;
+      }
+    } else {
+      // ---- pairs inside each block of 4 tokens (and the diagonal of Mq) with
+      // running products of alpha: a thread sums 8 channels of one block, then
+      // the 16 threads of a block reduce-scatter their 16 partial sums
+      // (outputs 0-5: A at (1,0),(2,0),(2,1),(3,0),(3,1),(3,2); 6-15: Mq at
+      // (0,0),(1,0),(1,1),(2,0),(2,1),(2,2),(3,0),(3,1),(3,2),(3,3))
+#pragma unroll 1
+      for (int rep = 0; rep < 2; ++rep) {
+        const int item = tid - kDK + kDK * rep;
+        const int blk = item >> 4, cg = item & 15;
+        float kf[4][8], qf[4][8], af[4][8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int t = 4 * blk + i;
+          const uint4 kr = *reinterpret_cast<const uint4 *>(sK + kmajor_off(t, 8 * cg, kDK));
+          const uint4 qr = *reinterpret_cast<const uint4 *>(sQ + kmajor_off(t, 8 * cg, kDK));
+          const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w}, qw[4] = {qr.x, qr.y, qr.z, qr.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            kf[i][2 * e] = bf16_to_f32(static_cast<uint16_t>(kw[e] & 0xffff));
+            kf[i][2 * e + 1] = bf16_to_f32(static_cast<uint16_t>(kw[e] >> 16));
+            qf[i][2 * e] = bf16_to_f32(static_cast<uint16_t>(qw[e] & 0xffff));
+            qf[i][2 * e + 1] = bf16_to_f32(static_cast<uint16_t>(qw[e] >> 16));
+          }
+          const float4 a0 = *reinterpret_cast<const float4 *>(al + t * kDK + 8 * cg);
+          const float4 a1 = *reinterpret_cast<const float4 *>(al + t * kDK + 8 * cg + 4);
+          af[i][0] = a0.x; af[i][1] = a0.y; af[i][2] = a0.z; af[i][3] = a0.w;
+          af[i][4] = a1.x; af[i][5] = a1.y; af[i][6] = a1.z; af[i][7] = a1.w;
+        }
+        float v[16];
+#pragma unroll
+        for (int o = 0; o < 16; ++o) v[o] = 0.f;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const float p10 = af[1][c], p21 = af[2][c], p32 = af[3][c];
+          const float p20 = p21 * p10, p31 = p32 * p21, p30 = p32 * p20;
+          v[0] = fmaf(kf[1][c] * kf[0][c], p10, v[0]);
+          v[1] = fmaf(kf[2][c] * kf[0][c], p20, v[1]);
+          v[2] = fmaf(kf[2][c] * kf[1][c], p21, v[2]);
+          v[3] = fmaf(kf[3][c] * kf[0][c], p30, v[3]);
+          v[4] = fmaf(kf[3][c] * kf[1][c], p31, v[4]);
+          v[5] = fmaf(kf[3][c] * kf[2][c], p32, v[5]);
+          v[6] = fmaf(qf[0][c], kf[0][c], v[6]);
+          v[7] = fmaf(qf[1][c] * kf[0][c], p10, v[7]);
+          v[8] = fmaf(qf[1][c], kf[1][c], v[8]);
+          v[9] = fmaf(qf[2][c] * kf[0][c], p20, v[9]);
+          v[10] = fmaf(qf[2][c] * kf[1][c], p21, v[10]);
+          v[11] = fmaf(qf[2][c], kf[2][c], v[11]);
+          v[12] = fmaf(qf[3][c] * kf[0][c], p30, v[12]);
+          v[13] = fmaf(qf[3][c] * kf[1][c], p31, v[13]);
+          v[14] = fmaf(qf[3][c] * kf[2][c], p32, v[14]);
+          v[15] = fmaf(qf[3][c], kf[3][c], v[15]);
+        }
+        // reduce-scatter over the 16 threads of the block (a half warp): the
+        // thread with index l within its block ends with output l
+        const int l = cg;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const bool up = l & 8;
+          const float send = up ? v[e] : v[e + 8];
+          const float keep = up ? v[e + 8] : v[e];
+          v[e] = keep + __shfl_xor_sync(kFull, send, 8);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const bool up = l & 4;
+          const float send = up ? v[e] : v[e + 4];
+          const float keep = up ? v[e + 4] : v[e];
+          v[e] = keep + __shfl_xor_sync(kFull, send, 4);
+        }
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const bool up = l & 2;
+          const float send = up ? v[e] : v[e + 2];
+          const float keep = up ? v[e + 2] : v[e];
+          v[e] = keep + __shfl_xor_sync(kFull, send, 2);
+        }
+        {
+          const bool up = l & 1;
+          const float send = up ? v[0] : v[1];
+          const float keep = up ? v[1] : v[0];
+          v[0] = keep + __shfl_xor_sync(kFull, send, 1);
+        }
+        w4[item] = v[0];
+      }
+    }
+    __syncthreads();
+
+    // ---- levels 0 and 1 on the tensor cores
+    kda_level_operands(0, 1, sK, sQ, lam, op, tid);
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) kda_issue_level_mma(tmem + kKColG1, op_addr, mbG);
+    // meanwhile: Qt, Khat and gamma_C to the workspace
+    for (int id = tid; id < 2 * kC * 16; id += kThreads) {
+      const int kind = id >> 10, idd = id & 1023;
+      const int t = ((idd >> 7) << 3) | (idd & 7), g = (idd >> 3) & 15;
+      const uint4 raw = *reinterpret_cast<const uint4 *>((kind ? sK : sQ) + kmajor_off(t, 8 * g, kDK));
+      const float *lt = lam + t * kLdL + 8 * g, *le = lam + (kC - 1) * kLdL + 8 * g;
+      const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
+      float x[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        // Qt: e^{lambda_t};  Khat: e^{lambda_C - lambda_t}
+        const float d0 = kind ? le[2 * e] - lt[2 * e] : lt[2 * e];
+        const float d1 = kind ? le[2 * e + 1] - lt[2 * e + 1] : lt[2 * e + 1];
+        x[2 * e] = bf16_to_f32(static_cast<uint16_t>(rw[e] & 0xffff)) * __expf(d0);
+        x[2 * e + 1] = bf16_to_f32(static_cast<uint16_t>(rw[e] >> 16)) * __expf(d1);
+      }
+      unsigned char *dst = ws + (kind ? kVKh : kVQ);
+      store_split8(dst, dst + 16384, kmajor_off(t, 8 * g, kDK), x);
+    }
+    if (tid < kDK) reinterpret_cast<float *>(ws + kVG)[tid] = __expf(lam[(kC - 1) * kLdL + tid]);
+    if (!wait_ok(mbG, 0)) { failed = true; break; }
+    kda_level_extract(0, 1, tmem + kKColG1, sAst, sMst, be, warp, lane);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    // ---- levels 2 and 3
+    kda_level_operands(2, 3, sK, sQ, lam, op, tid);
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) kda_issue_level_mma(tmem + kKColG2, op_addr, mbG);
+    {  // meanwhile: the block-of-4 sums into the staging
+      const int blk = tid >> 4, o = tid & 15;
+      // (i, j) of output o inside the block (4 bits each, output 0 lowest):
+      // i = 1,2,2,3,3,3,0,1,1,2,2,2,3,3,3,3  j = 0,0,1,0,1,2,0,0,1,0,1,2,0,1,2,3
+      const uint64_t oi = 0x3333222110333221ull, oj = 0x3210210100210100ull;
+      const int i = 4 * blk + static_cast<int>((oi >> (4 * o)) & 15);
+      const int j = 4 * blk + static_cast<int>((oj >> (4 * o)) & 15);
+      if (o < 6)
+        sAst[i * kLdS + j] = be[i] * w4[tid];
+      else
+        sMst[i * kLdS + j] = w4[tid];
+    }
+    if (!wait_ok(mbG, 1)) { failed = true; break; }
+    kda_level_extract(2, 3, tmem + kKColG2, sAst, sMst, be, warp, lane);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    // ---- L = I + A (strictly lower part) for the solve; Mq (lower, diagonal
+    // included) to the workspace
+    for (int id = tid; id < kC * kC; id += kThreads) {
+      const int i = id >> 6, j = id & 63;
+      sL[i * kLd + j] = j < i ? sAst[i * kLdS + j] : 0.f;
+    }
+    for (int id = tid; id < kC * 8; id += kThreads) {
+      const int i = id >> 3, j0 = (id & 7) * 8;
+      float x[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = j0 + e <= i ? sMst[i * kLdS + j0 + e] : 0.f;
+      store_split8(ws + kVMq, ws + kVMq + 8192, kmajor_off(i, j0, kC), x);
+    }
+    __syncthreads();
+    solve_unit_lower(sL, sTf, sZ, tid);
+    // T = L^-1 diag(beta) (lower triangle) and Kt = k (.) e^{lambda}, hi/lo operand tiles
+    {
+      const int i = tid >> 2, j0 = (tid & 3) * 16;
+      float x[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int j = j0 + e;
+        x[e] = j <= i ? sTf[i * kLd + j] * be[j] : 0.f;
+      }
+      store_split8(sTh, sTl, kmajor_off(i, j0, kC), x);
+      store_split8(sTh, sTl, kmajor_off(i, j0 + 8, kC), x + 8);
+    }
+    for (int id = tid; id < kC * 16; id += kThreads) {
+      const int t = ((id >> 7) << 3) | (id & 7), g = (id >> 3) & 15;
+      const uint4 raw = *reinterpret_cast<const uint4 *>(sK + kmajor_off(t, 8 * g, kDK));
+      const float *lt = lam + t * kLdL + 8 * g;
+      const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
+      float x[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        x[2 * e] = bf16_to_f32(static_cast<uint16_t>(rw[e] & 0xffff)) * __expf(lt[2 * e]);
+        x[2 * e + 1] = bf16_to_f32(static_cast<uint16_t>(rw[e] >> 16)) * __expf(lt[2 * e + 1]);
+      }
+      store_split8(sKth, sKtl, kmajor_off(t, 8 * g, kDK), x);
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // ---- W^T = Kt^T T^T (three passes) and Ut^T = V^T T^T (V is exact: two)
+    if (tid == 0) {
+#pragma unroll
+      for (int ks = 0; ks < kC / 16; ++ks) {
+        mma_bf16(tmem + kKColW, dKtmn_h + 256u * ks, dTh + 16u * ks, idMN, ks > 0);
+        mma_bf16(tmem + kKColW, dKtmn_h + 256u * ks, dTl + 16u * ks, idMN, true);
+        mma_bf16(tmem + kKColW, dKtmn_l + 256u * ks, dTh + 16u * ks, idMN, true);
+        mma_bf16(tmem + kKColU, dVmn + 256u * ks, dTh + 16u * ks, idMN, ks > 0);
+        mma_bf16(tmem + kKColU, dVmn + 256u * ks, dTl + 16u * ks, idMN, true);
+      }
+      mma_commit(mbW);
+    }
+    if (!wait_ok(mbW, static_cast<uint32_t>(it & 1))) { failed = true; break; }
+    {
+      float *gU = reinterpret_cast<float *>(ws + kVU);
+      for (int i0 = half * 32; i0 < half * 32 + 32; i0 += 16) {
+        float x[16];
+        tmem_ld16(tmem_addr(tmem, lane_base, kKColU + i0), x);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) gU[(i0 + e) * kDV + row] = x[e];
+        tmem_ld16(tmem_addr(tmem, lane_base, kKColW + i0), x);
+        tmem_ld_wait();
+        const uint32_t off = (i0 >> 3) * 2048 + (row >> 3) * 128 + (row & 7) * 16;
+        store_split8(ws + kVW, ws + kVW + 16384, off, x);
+        store_split8(ws + kVW, ws + kVW + 16384, off + 2048, x + 8);
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
+  if (failed) {
+    if (tid == 0) mma_commit(mbEnd);
+    mbar_wait(mbEnd, 0, kWaitLimit);
+    if (tid == 0) report_timeout(a.err);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, kKdaTmemCols);
+}
+
+// ===========================================================================
 // Kernel 2: the chain of chunks of one (batch, head).
 //
 // Warps 0-15 (workers): warp w owns tensor-memory lanes 32*(w%4) .. +31
@@ -415,22 +903,36 @@ constexpr uint32_t kColY1 = 192;  // S0^T Q^T     [128 x 64]
 constexpr uint32_t kColY2 = 256;  // U^T Mq^T     [128 x 64]
 constexpr uint32_t kChainTmemCols = 512;
 
-// shared memory (bytes)
+// shared memory (bytes) and the unit layout the chain reads, GDN or KDA
 constexpr uint32_t kCS = 0;               // S^T hi, lo [128 d][128 c]        2 x 32 KB
 constexpr uint32_t kCU = kCS + 65536;     // U^T hi, lo [128 d][64 j]         2 x 16 KB
-constexpr uint32_t kCW = kCU + 32768;     // W hi, lo, Q (bulk copy)          48 KB
-constexpr uint32_t kCM = kCW + kWBytes;   // Mq hi, lo, Khat hi, lo (bulk)    48 KB
-constexpr uint32_t kCG = kCM + kMBytes;   // gamma_i, two buffers             2 x 256 B
-constexpr uint32_t kCBar = kCG + 2 * kGBytes;
+constexpr uint32_t kCW = kCU + 32768;     // W hi, lo, then Q (GDN) or Qt hi, lo (KDA): one bulk copy
 constexpr int kNBar = 12;
-constexpr uint32_t kChainSmem = kCBar + kNBar * 8 + 16;
+template <bool KDA>
+struct ChainLayout {
+  static constexpr uint32_t unit = KDA ? kVUnit : kUnit;
+  static constexpr uint32_t w_off = KDA ? kVW : kUW;                 // W, Q / Qt
+  static constexpr uint32_t w_bytes = KDA ? kVMq - kVW : kWBytes;
+  static constexpr uint32_t m_off = KDA ? kVMq : kUMq;               // Mq, Khat
+  static constexpr uint32_t m_bytes = KDA ? kVG - kVMq : kMBytes;
+  static constexpr uint32_t g_off = KDA ? kVG : kUG;                 // gamma_C per channel (KDA) / gamma_i (GDN)
+  static constexpr uint32_t g_bytes = KDA ? kVU - kVG : kGBytes;
+  static constexpr uint32_t u_off = KDA ? kVU : kUU;                 // Ut
+  static constexpr uint32_t cm = kCW + w_bytes;                      // Mq hi, lo, Khat hi, lo
+  static constexpr uint32_t cg = cm + m_bytes;                       // gammas, two buffers
+  static constexpr uint32_t cbar = cg + 2 * g_bytes;
+  static constexpr uint32_t smem = cbar + kNBar * 8 + 16;
+  static_assert(smem <= 227 * 1024, "chain shared memory");
+};
 
 // bounded wait that also gives up as soon as another thread has
 __device__ __forceinline__ bool chain_wait(uint32_t mbar, uint32_t parity, volatile int *abort_flag) {
   return mbar_wait_abortable(mbar, parity, kWaitLimit, abort_flag);
 }
 
+template <bool KDA>
 __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
+  using L = ChainLayout<KDA>;
   extern __shared__ __align__(1024) unsigned char sm[];
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -441,12 +943,12 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
 
   unsigned char *sSh = sm + kCS, *sSl = sm + kCS + 32768;
   unsigned char *sUh = sm + kCU, *sUl = sm + kCU + 16384;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kCBar);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::cbar);
   // barriers: 0 W, 1 M, 2-3 gamma buffers, 4 X done, 5 round 1 done, 6 Y2 done,
   // 7 round 2 done, 8-9 S_ready[g], 10 U_ready, 11 drain
   auto bar = [&](int i) { return smem_addr(bars + i); };
-  uint32_t *holder = reinterpret_cast<uint32_t *>(sm + kCBar + kNBar * 8);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + kCBar + kNBar * 8 + 4);
+  uint32_t *holder = reinterpret_cast<uint32_t *>(sm + L::cbar + kNBar * 8);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::cbar + kNBar * 8 + 4);
 
   if (tid == 0) {
     for (int i = 0; i < 8; ++i) mbar_init(bar(i), 1);
@@ -485,7 +987,7 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
     publish_s(1);
     float ut[16];  // Ut[16*qtr + e][row] of the next chunk
     auto load_ut = [&](int c) {
-      const float *src = reinterpret_cast<const float *>(a.ws + (u0 + c) * kUnit + kUU) + row;
+      const float *src = reinterpret_cast<const float *>(a.ws + (u0 + c) * L::unit + L::u_off) + row;
 #pragma unroll
       for (int e = 0; e < 16; ++e) ut[e] = __ldg(src + (16 * qtr + e) * kDV);
     };
@@ -493,7 +995,7 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
     for (int c = 0; c < n; ++c) {
       const uint32_t par = static_cast<uint32_t>(c & 1);
       const bool last = c + 1 == n;
-      const float gc = __ldg(a.gC + u0 + c);
+      const float gc = KDA ? 0.f : __ldg(a.gC + u0 + c);
       // U^T = Ut^T - X for this warp's 16 tokens
       if (!wwait(bar(4), par)) break;
       {
@@ -509,11 +1011,12 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
         mbar_arrive(bar(10));
       }
       if (!last) load_ut(c + 1);
-      // y = gamma_i Y1 + Y2
+      // y = gamma_i Y1 + Y2 (GDN) or Y1 + Y2 (KDA: the decay is inside Qt)
       if (!wwait(bar(6), par)) break;
       if (!wwait(bar(2 + (c & 1)), static_cast<uint32_t>((c >> 1) & 1))) break;
+      const float *gbuf = reinterpret_cast<const float *>(sm + L::cg + (c & 1) * L::g_bytes);
       {
-        const float *gam = reinterpret_cast<const float *>(sm + kCG + (c & 1) * kGBytes) + 16 * qtr;
+        const float *gam = gbuf + 16 * qtr;
         const int t0 = c * kC + 16 * qtr;
         float *yp = a.y + (tok0 + static_cast<long>(t0) * H) * kDV + row;
 #pragma unroll
@@ -524,10 +1027,12 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
           tmem_ld_wait();
 #pragma unroll
           for (int e = 0; e < 8; ++e)
-            if (t0 + h8 + e < T) yp[static_cast<long>(h8 + e) * H * kDV] = fmaf(gam[h8 + e], y1[e], y2[e]);
+            if (t0 + h8 + e < T)
+              yp[static_cast<long>(h8 + e) * H * kDV] = KDA ? y1[e] + y2[e] : fmaf(gam[h8 + e], y1[e], y2[e]);
         }
       }
-      // S^T <- gamma_C S^T + D, published group by group for the next round 1
+      // S^T <- gamma_C S^T + D (KDA: gamma_C per key channel, i.e. per column
+      // of S^T), published group by group for the next round 1
       if (!wwait(bar(7), par)) break;
 #pragma unroll
       for (int g = 0; g < 2; ++g) {
@@ -535,7 +1040,7 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
         tmem_ld16(lanes + kColD + 32 * qtr + 16 * g, x);
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) S[16 * g + e] = fmaf(gc, S[16 * g + e], x[e]);
+        for (int e = 0; e < 16; ++e) S[16 * g + e] = fmaf(KDA ? gbuf[32 * qtr + 16 * g + e] : gc, S[16 * g + e], x[e]);
         if (!last) publish_s(g);
       }
       if (last) {
@@ -547,14 +1052,15 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
     // ------------------------------------------------------------ producer
     const uint32_t sh = smem_addr(sSh), sl = smem_addr(sSl), uh = smem_addr(sUh), ul = smem_addr(sUl);
     const uint32_t wh = smem_addr(sm + kCW), wl = wh + 16384, qa = wh + 32768;
-    const uint32_t mh = smem_addr(sm + kCM), ml = mh + 8192, kh = mh + 16384, kl = mh + 32768;
+    const uint32_t mh = smem_addr(sm + L::cm), ml = mh + 8192, kh = mh + 16384, kl = mh + 32768;
     const uint32_t id64 = idesc_bf16_f32(128, kC), id128 = idesc_bf16_f32(128, kDK);
     // operand descriptors at k-step 0; k-step ks starts 256 bytes further on,
     // i.e. 16 in the descriptor's address field
     const uint64_t dSh = smem_desc(sh, 128, kDK * 16), dSl = smem_desc(sl, 128, kDK * 16);
     // W and Khat^T arrive MN-major (token-contiguous W, column-contiguous Khat)
     const uint64_t dWh = smem_desc(wh, 128, 2048), dWl = smem_desc(wl, 128, 2048);
-    const uint64_t dQ = smem_desc(qa, 128, kDK * 16);
+    const uint64_t dQ = smem_desc(qa, 128, kDK * 16);              // Q (GDN) or Qt hi (KDA)
+    const uint64_t dQl = smem_desc(qa + 16384, 128, kDK * 16);     // Qt lo (KDA)
     const uint64_t dUh = smem_desc(uh, 128, kC * 16), dUl = smem_desc(ul, 128, kC * 16);
     const uint64_t dMh = smem_desc(mh, 128, kC * 16), dMl = smem_desc(ml, 128, kC * 16);
     const uint64_t dKh = smem_desc(kh, 2048, 128), dKl = smem_desc(kl, 2048, 128);
@@ -565,27 +1071,28 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
     };
     int w_issued = 0, w_done = 0, m_issued = 0, m_done = 0, g_issued = 0;
     auto load = [&](int which, int c) {
-      const unsigned char *src = a.ws + (u0 + c) * kUnit;
+      const unsigned char *src = a.ws + (u0 + c) * L::unit;
       fence_async_smem();
       if (which == 0) {
-        mbar_expect_tx(bar(0), kWBytes);
-        bulk_g2s(wh, src + kUW, kWBytes, bar(0));
+        mbar_expect_tx(bar(0), L::w_bytes);
+        bulk_g2s(wh, src + L::w_off, L::w_bytes, bar(0));
         ++w_issued;
       } else {
-        mbar_expect_tx(bar(1), kMBytes);
-        bulk_g2s(mh, src + kUMq, kMBytes, bar(1));
-        mbar_expect_tx(bar(2 + (c & 1)), kGBytes);
-        bulk_g2s(smem_addr(sm + kCG + (c & 1) * kGBytes), src + kUG, kGBytes, bar(2 + (c & 1)));
+        mbar_expect_tx(bar(1), L::m_bytes);
+        bulk_g2s(mh, src + L::m_off, L::m_bytes, bar(1));
+        mbar_expect_tx(bar(2 + (c & 1)), L::g_bytes);
+        bulk_g2s(smem_addr(sm + L::cg + (c & 1) * L::g_bytes), src + L::g_off, L::g_bytes, bar(2 + (c & 1)));
         ++m_issued;
         ++g_issued;
       }
     };
-    // the operands of chunk c into L2 ahead of their copies (three pieces of at most 48 KB)
+    // the operands of chunk c into L2 ahead of their copies (pieces of at most 48 KB)
     auto prefetch = [&](int c) {
-      const unsigned char *pf = a.ws + (u0 + c) * kUnit;
-      prefetch_l2(pf + kUW, kWBytes);
-      prefetch_l2(pf + kUMq, kMBytes + kGBytes);
-      prefetch_l2(pf + kUU, kUnit - kUU);
+      const unsigned char *pf = a.ws + (u0 + c) * L::unit;
+      prefetch_l2(pf + L::w_off, L::w_bytes / 2);
+      prefetch_l2(pf + L::w_off + L::w_bytes / 2, L::w_bytes / 2);
+      prefetch_l2(pf + L::m_off, L::m_bytes + L::g_bytes);
+      prefetch_l2(pf + L::u_off, L::unit - L::u_off);
     };
     if (n > 1) prefetch(1);
     load(0, 0);
@@ -611,6 +1118,7 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
 #pragma unroll
         for (int ks = g; ks < 8; ks += 2) {
           mma(tmem + kColY1, dSh, dQ, ks, id64, ks != 0);
+          if (KDA) mma(tmem + kColY1, dSh, dQl, ks, id64, true);
           mma(tmem + kColY1, dSl, dQ, ks, id64, true);
         }
       }
@@ -727,11 +1235,68 @@ int launch_gdn_chunk(float *state, const uint16_t *q, const uint16_t *k, const u
   ca.nchunks = nchunks;
   ca.err = err;
   ca.drop_signal = test_drop_signal();
-  if (cudaFuncSetAttribute(gdn_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(kChainSmem)) != cudaSuccess)
+  constexpr uint32_t chain_smem = ChainLayout<false>::smem;
+  if (cudaFuncSetAttribute(gdn_chain_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(chain_smem)) != cudaSuccess)
     return check_launch("gdn_scan: set shared memory");
-  gdn_chain_kernel<<<static_cast<unsigned>(static_cast<long>(B) * H), kChainThreads, kChainSmem, st>>>(ca);
+  gdn_chain_kernel<false><<<static_cast<unsigned>(static_cast<long>(B) * H), kChainThreads, chain_smem, st>>>(ca);
   return check_launch("gdn_scan: chunk chain kernel");
+}
+
+// workspace of the chunked KDA path: one unit of tiles per chunk
+size_t kda_chunk_workspace_size(int B, int T, int H) {
+  const long units = static_cast<long>(B) * H * ((T + kC - 1) / kC);
+  const size_t n = static_cast<size_t>(units) * kVUnit;
+  return (n + 255) & ~static_cast<size_t>(255);
+}
+
+// launched by gdn_scan for KDA (a decay per key channel) with d_k = d_v = 128
+int launch_kda_chunk(float *state, const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
+                     const float *beta, int B, int T, int H, float *y, void *workspace, int32_t *err,
+                     cudaStream_t st) {
+  const int nchunks = (T + kC - 1) / kC;
+  const long units = static_cast<long>(B) * H * nchunks;
+  unsigned char *ws = static_cast<unsigned char *>(workspace);
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+
+  KdaPrepArgs pa;
+  pa.q = q;
+  pa.k = k;
+  pa.v = v;
+  pa.alpha = alpha;
+  pa.beta = beta;
+  pa.ws = ws;
+  pa.T = T;
+  pa.H = H;
+  pa.nchunks = nchunks;
+  pa.units = units;
+  pa.err = err;
+  if (cudaFuncSetAttribute(kda_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kKdaSmem)) != cudaSuccess)
+    return check_launch("gdn_scan: set shared memory");
+  const long pgrid = units < sms ? units : sms;
+  kda_prep_kernel<<<static_cast<unsigned>(pgrid), kThreads, kKdaSmem, st>>>(pa);
+  const int rc = check_launch("gdn_scan: KDA chunk preparation kernel");
+  if (rc != SDM_OK) return rc;
+
+  ChainArgs ca;
+  ca.state = state;
+  ca.ws = ws;
+  ca.gC = nullptr;
+  ca.y = y;
+  ca.T = T;
+  ca.H = H;
+  ca.nchunks = nchunks;
+  ca.err = err;
+  ca.drop_signal = test_drop_signal();
+  constexpr uint32_t chain_smem = ChainLayout<true>::smem;
+  if (cudaFuncSetAttribute(gdn_chain_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(chain_smem)) != cudaSuccess)
+    return check_launch("gdn_scan: set shared memory");
+  gdn_chain_kernel<true><<<static_cast<unsigned>(static_cast<long>(B) * H), kChainThreads, chain_smem, st>>>(ca);
+  return check_launch("gdn_scan: KDA chunk chain kernel");
 }
 
 SDM_STICKY_ACCESSOR(sticky_gdn_chunk)

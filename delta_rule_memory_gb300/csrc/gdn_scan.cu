@@ -173,17 +173,26 @@ int launch_recurrent(GdnArgs &args, int B, cudaStream_t st, const char *what) {
 }  // namespace
 
 size_t gdn_chunk_workspace_size(int B, int T, int H);
+size_t kda_chunk_workspace_size(int B, int T, int H);
+int launch_kda_chunk(float *state, const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
+                     const float *beta, int B, int T, int H, float *y, void *workspace, int32_t *err,
+                     cudaStream_t st);
 int launch_gdn_chunk(float *state, const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
                      const float *beta, int B, int T, int H, float *y, void *workspace, int32_t *err,
                      cudaStream_t st);
 
-// dense GDN at d_k = d_v = 128 runs chunkwise on the tensor cores; every other
-// shape (and KDA) runs token by token.  SDM_GDN_PATH=recurrent forces the
+// dense GDN and KDA at d_k = d_v = 128 run chunkwise on the tensor cores;
+// every other shape runs token by token.  SDM_GDN_PATH=recurrent forces the
 // token-by-token kernel (for cross-checks).
 static bool use_chunked(int dk, int dv, int per_channel) {
+  (void)per_channel;
   const char *path = getenv("SDM_GDN_PATH");
   const bool want_recurrent = path && path[0] == 'r';
-  return !per_channel && dk == 128 && dv == 128 && !want_recurrent;
+  return dk == 128 && dv == 128 && !want_recurrent;
+}
+
+static size_t chunk_workspace_size(int B, int T, int H, int per_channel) {
+  return per_channel ? kda_chunk_workspace_size(B, T, H) : gdn_chunk_workspace_size(B, T, H);
 }
 
 }  // namespace sdm
@@ -192,7 +201,7 @@ using namespace sdm;
 
 extern "C" size_t gdn_scan_workspace_size(int B, int T, int H, int dk, int dv, int per_channel) {
   if (B <= 0 || T <= 0 || H <= 0 || !use_chunked(dk, dv, per_channel)) return 0;
-  return gdn_chunk_workspace_size(B, T, H);
+  return chunk_workspace_size(B, T, H, per_channel);
 }
 
 extern "C" int gdn_scan(float *state, const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
@@ -210,10 +219,11 @@ extern "C" int gdn_scan(float *state, const uint16_t *q, const uint16_t *k, cons
   if (dev_err && !aligned(dev_err, 4)) return set_error(SDM_ERR_ALIGN, "gdn_scan: dev_err must be 4-byte aligned");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (use_chunked(dk, dv, per_channel)) {
-    const size_t need = gdn_chunk_workspace_size(B, T, H);
+    const size_t need = chunk_workspace_size(B, T, H, per_channel);
     if (!workspace || workspace_bytes < need)
       return set_error(SDM_ERR_INVALID_ARG, "gdn_scan: workspace of %zu bytes needed", need);
     if (!aligned(workspace, 16)) return set_error(SDM_ERR_ALIGN, "gdn_scan: workspace must be 16-byte aligned");
+    if (per_channel) return launch_kda_chunk(state, q, k, v, alpha, beta, B, T, H, y, workspace, dev_err, st);
     return launch_gdn_chunk(state, q, k, v, alpha, beta, B, T, H, y, workspace, dev_err, st);
   }
   GdnArgs args{};

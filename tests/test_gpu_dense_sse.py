@@ -51,29 +51,52 @@ def test_gdn_full_size_sampled(per_channel):
         assert_state_close(S[b:b + 1, h:h + 1], Sr, what=f"state[{b},{h}]")
 
 
+@pytest.mark.parametrize("per_channel", [False, True], ids=["gdn", "kda"])
 @pytest.mark.parametrize("T", [1, 63, 64, 65, 200, 512, 700])
-def test_gdn_chunked_path_lengths(T, monkeypatch):
-    """Dense GDN at d_k = d_v = 128 runs chunkwise (64 tokens) on the tensor
-    cores: lengths below, at and across a chunk boundary, nonzero state, and
-    longer sequences of 8 and 11 chunks."""
+def test_gdn_chunked_path_lengths(T, per_channel, monkeypatch):
+    """Dense GDN and KDA at d_k = d_v = 128 run chunkwise (64 tokens) on the
+    tensor cores: lengths below, at and across a chunk boundary, nonzero
+    state, and longer sequences of 8 and 11 chunks."""
     sdm = need_gpu()
     monkeypatch.setenv("SDM_GDN_PATH", "chunk")
     import torch
     sh = synth.GDN_DENSE.with_(B=2, T=T, H=2)
     inp = synth.gdn_inputs(sh, seed=40 + T)
     S0 = synth.random_state((2, 2, 128, 128), seed=41, scale=0.3)
-    Sr, yr = oracle.gdn_scan(S0, inp["q"], inp["k"], inp["v"], inp["alpha_gdn"], inp["beta"], False)
+    a = inp["alpha_kda"] if per_channel else inp["alpha_gdn"]
+    Sr, yr = oracle.gdn_scan(S0, inp["q"], inp["k"], inp["v"], a, inp["beta"], per_channel)
     state = dev(S0)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    y = sdm.gdn_scan(state, dev(inp["q"]), dev(inp["k"]), dev(inp["v"]), dev(inp["alpha_gdn"]), dev(inp["beta"]),
-                     False, dev_err=err)
+    y = sdm.gdn_scan(state, dev(inp["q"]), dev(inp["k"]), dev(inp["v"]), dev(a), dev(inp["beta"]),
+                     per_channel, dev_err=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     assert_y_close(host(y), yr)
     assert_state_close(host(state), Sr)
 
 
-def test_gdn_chunked_is_deterministic_and_continues_the_state(monkeypatch):
+@pytest.mark.parametrize("scale", [1.0, 3.0, 6.0])
+def test_kda_chunked_strong_per_channel_decay(scale, monkeypatch):
+    """KDA decays alpha = exp(-scale * softplus(N(0,1))) per key channel: at
+    scale 6 the per-channel log decay over a 64-token chunk spans hundreds of
+    units, so any factor formed as an inverse decay would overflow; every
+    factor here is a decay ratio of at most 1."""
+    sdm = need_gpu()
+    monkeypatch.setenv("SDM_GDN_PATH", "chunk")
+    sh = synth.GDN_DENSE.with_(B=1, T=300, H=2)
+    inp = synth.gdn_inputs(sh, seed=48)
+    a = np.exp(np.log(inp["alpha_kda"].astype(np.float64)) * scale).astype(np.float32)
+    a = np.maximum(a, np.float32(1e-30))
+    inp = dict(inp, alpha_kda=a)
+    S0 = synth.random_state((1, 2, 128, 128), seed=49, scale=0.3)
+    Sr, yr = oracle.gdn_scan(S0, inp["q"], inp["k"], inp["v"], a, inp["beta"], True)
+    S, y = _gdn_gpu(sdm, S0, inp, True)
+    assert_y_close(y, yr)
+    assert_state_close(S, Sr)
+
+
+@pytest.mark.parametrize("per_channel", [False, True], ids=["gdn", "kda"])
+def test_gdn_chunked_is_deterministic_and_continues_the_state(per_channel, monkeypatch):
     """The chunked path (T = 900: 15 chunks) gives the same bits on every
     call, and a sequence cut at a chunk boundary into two calls equals one
     call (the second call continues from the state the first left)."""
@@ -82,49 +105,52 @@ def test_gdn_chunked_is_deterministic_and_continues_the_state(monkeypatch):
     sh = synth.GDN_DENSE.with_(B=2, T=900, H=2)
     inp = synth.gdn_inputs(sh, seed=46)
     S0 = synth.random_state((2, 2, 128, 128), seed=47, scale=0.3)
-    S1, y1 = _gdn_gpu(sdm, S0, inp, False)
-    S2, y2 = _gdn_gpu(sdm, S0, inp, False)
+    S1, y1 = _gdn_gpu(sdm, S0, inp, per_channel)
+    S2, y2 = _gdn_gpu(sdm, S0, inp, per_channel)
     np.testing.assert_array_equal(y1, y2)
     np.testing.assert_array_equal(S1, S2)
     cut = 576
     first = {k: v[:, :cut] for k, v in inp.items() if isinstance(v, np.ndarray) and v.ndim >= 3}
     second = {k: v[:, cut:] for k, v in inp.items() if isinstance(v, np.ndarray) and v.ndim >= 3}
-    Sa, ya = _gdn_gpu(sdm, S0, first, False)
-    Sb, yb = _gdn_gpu(sdm, Sa, second, False)
+    Sa, ya = _gdn_gpu(sdm, S0, first, per_channel)
+    Sb, yb = _gdn_gpu(sdm, Sa, second, per_channel)
     assert_y_close(np.concatenate([ya, yb], axis=1), y1.astype(np.float64))
     assert_state_close(Sb, S1.astype(np.float64))
 
 
-def test_gdn_chunked_matches_token_recurrent(monkeypatch):
+@pytest.mark.parametrize("per_channel", [False, True], ids=["gdn", "kda"])
+def test_gdn_chunked_matches_token_recurrent(per_channel, monkeypatch):
     sdm = need_gpu()
     sh = synth.GDN_DENSE.with_(B=1, T=300, H=3)
     inp = synth.gdn_inputs(sh, seed=44)
     S0 = synth.random_state((1, 3, 128, 128), seed=45, scale=0.3)
     monkeypatch.setenv("SDM_GDN_PATH", "chunk")
-    Sc, yc = _gdn_gpu(sdm, S0, inp, False)
+    Sc, yc = _gdn_gpu(sdm, S0, inp, per_channel)
     monkeypatch.setenv("SDM_GDN_PATH", "recurrent")
-    Sr, yr = _gdn_gpu(sdm, S0, inp, False)
+    Sr, yr = _gdn_gpu(sdm, S0, inp, per_channel)
     assert_y_close(yc, yr)
     assert_state_close(Sc, Sr)
 
 
 def test_kda_with_constant_channel_decay_is_gdn(monkeypatch):
     """KDA with alpha = alpha_t * 1 is GDN (Linear Attention Architectures
-    deck, Eqs. 18-20): bit-exact on the same token-by-token kernel, and within
-    tolerance of the tensor-core GDN path."""
+    deck, Eqs. 18-20): within tolerance between the two tensor-core paths, and
+    bit-exact on the same token-by-token kernel."""
     sdm = need_gpu()
-    sh = synth.GDN_DENSE.with_(B=1, T=64, H=2)
+    sh = synth.GDN_DENSE.with_(B=1, T=200, H=2)
     inp = synth.gdn_inputs(sh, seed=3)
     inp2 = dict(inp)
     inp2["alpha_kda"] = np.repeat(inp["alpha_gdn"][..., None], sh.dk, axis=-1).copy()
     S0 = synth.random_state((1, 2, sh.dk, sh.dv), seed=4, scale=0.2)
-    Sk, yk = _gdn_gpu(sdm, S0, inp2, True)
-    Sc, yc = _gdn_gpu(sdm, S0, inp, False)          # chunked tensor-core path
+    monkeypatch.setenv("SDM_GDN_PATH", "chunk")
+    Sk, yk = _gdn_gpu(sdm, S0, inp2, True)          # chunked KDA
+    Sc, yc = _gdn_gpu(sdm, S0, inp, False)          # chunked GDN
     assert_y_close(yc, yk)
     assert_state_close(Sc, Sk)
     monkeypatch.setenv("SDM_GDN_PATH", "recurrent")
+    Skr, ykr = _gdn_gpu(sdm, S0, inp2, True)
     Sg, yg = _gdn_gpu(sdm, S0, inp, False)
-    assert np.array_equal(yg, yk) and np.array_equal(Sg, Sk)
+    assert np.array_equal(yg, ykr) and np.array_equal(Sg, Skr)
 
 
 def test_sparse_scan_with_every_row_selected_matches_dense():

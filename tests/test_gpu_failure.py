@@ -16,12 +16,13 @@ pytestmark = pytest.mark.gpu
 SDM_DEVERR_TIMEOUT = 8
 
 
-def _gdn(sdm, S0, inp):
+def _gdn(sdm, S0, inp, per_channel=False):
     import torch
     state = dev(S0)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    y = sdm.gdn_scan(state, dev(inp["q"]), dev(inp["k"]), dev(inp["v"]), dev(inp["alpha_gdn"]), dev(inp["beta"]),
-                     False, dev_err=err)
+    a = inp["alpha_kda"] if per_channel else inp["alpha_gdn"]
+    y = sdm.gdn_scan(state, dev(inp["q"]), dev(inp["k"]), dev(inp["v"]), dev(a), dev(inp["beta"]),
+                     per_channel, dev_err=err)
     torch.cuda.synchronize()
     return host(state), host(y), int(host(err)[0])
 
@@ -36,19 +37,21 @@ def _sse(sdm, S0, inp, topk):
     return host(state), host(y), int(host(err)[0])
 
 
-def test_gdn_chain_wait_runs_out_and_the_context_stays_usable(monkeypatch):
+@pytest.mark.parametrize("per_channel", [False, True], ids=["gdn", "kda"])
+def test_gdn_chain_wait_runs_out_and_the_context_stays_usable(per_channel, monkeypatch):
     sdm = need_gpu()
     monkeypatch.setenv("SDM_GDN_PATH", "chunk")
     sh = synth.GDN_DENSE.with_(B=1, T=200, H=2)
     inp = synth.gdn_inputs(sh, seed=90)
     S0 = synth.random_state((1, 2, 128, 128), seed=91, scale=0.3)
     monkeypatch.setenv("SDM_TEST_DROP_SIGNAL", "1")
-    _, _, err = _gdn(sdm, S0, inp)
+    _, _, err = _gdn(sdm, S0, inp, per_channel)
     assert err & SDM_DEVERR_TIMEOUT
     monkeypatch.delenv("SDM_TEST_DROP_SIGNAL")
-    S, y, err = _gdn(sdm, S0, inp)
+    S, y, err = _gdn(sdm, S0, inp, per_channel)
     assert err == 0
-    Sr, yr = oracle.gdn_scan(S0, inp["q"], inp["k"], inp["v"], inp["alpha_gdn"], inp["beta"], False)
+    a = inp["alpha_kda"] if per_channel else inp["alpha_gdn"]
+    Sr, yr = oracle.gdn_scan(S0, inp["q"], inp["k"], inp["v"], a, inp["beta"], per_channel)
     assert_y_close(y, yr)
     assert_state_close(S, Sr)
 
