@@ -43,8 +43,11 @@ constexpr int kThreads = 256;
 constexpr uint32_t kWaitLimit = 1u << 20;  // polls (about 0.1 s) before an mbarrier wait gives up
 
 // ---- one chunk's tiles in the workspace (bytes; K-major no-swizzle bf16 tiles, umma.cuh)
-constexpr uint32_t kUW = 0;       // W hi, lo        [64 i][128 c]   16 KB each, MN-major (8 tokens per 16 B)
-constexpr uint32_t kUQ = 32768;   // Q               [64 i][128 c]   16 KB
+// W hi, then Q, then W lo: [W hi; Q] is one MN-major B operand of N = 128
+// tokens (X and Y1 of the chain in one MMA group)
+constexpr uint32_t kUW = 0;       // W hi            [64 i][128 c]   16 KB, MN-major (8 tokens per 16 B)
+constexpr uint32_t kUQ = 16384;   // Q               [64 i][128 c]   16 KB, MN-major
+constexpr uint32_t kUWl = 32768;  // W lo            [64 i][128 c]   16 KB, MN-major
 constexpr uint32_t kUMq = 49152;  // Mq hi, lo       [64 i][64 j]     8 KB each
 constexpr uint32_t kUKh = 65536;  // Khat hi, lo     [64 j][128 c]   16 KB each, MN-major B of S^T += U^T Khat
 constexpr uint32_t kUG = 98304;   // gamma_i         fp32 [64]
@@ -275,12 +278,23 @@ __global__ void __launch_bounds__(kThreads, kPrepCtasPerSm) gdn_prep_kernel(cons
       tail[tid] = __expf(lam[kC - 1] - lam[tid]);
     }
     __syncthreads();
-    // Q tile to the workspace (read by the chain as is); Khat hi/lo: the K
-    // tile with row j scaled by e^(lambda_C - lambda_j), the MN-major B
-    // operand of the chain's state update
+    // Q tile to the workspace MN-major (8 tokens of one key per 16 bytes,
+    // the layout of W); Khat hi/lo: the K tile with row j scaled by
+    // e^(lambda_C - lambda_j), the MN-major B operand of the chain's state update
+    // (each warp transposes four 8x8 core matrices per ldmatrix: token group
+    // ig, key groups 4m..4m+3; lane t then holds tokens 2(t%4), 2(t%4)+1 of
+    // key 8(4m+j) + t/4 and stores them as 4 bytes of that key's 16-byte piece)
+    for (int o = warp; o < 32; o += kThreads / 32) {
+      const int ig = o >> 2, m = o & 3, lane = tid & 31;
+      uint32_t r[4];
+      ldsm_x4_trans(smem_addr(sQ) + ig * 2048 + (4 * m + (lane >> 3)) * 128 + (lane & 7) * 16, r);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int c = 8 * (4 * m + j) + (lane >> 2);
+        *reinterpret_cast<uint32_t *>(ws + kUQ + ig * 2048 + (c >> 3) * 128 + (c & 7) * 16 + (lane & 3) * 4) = r[j];
+      }
+    }
     for (int o = tid; o < 1024; o += kThreads) {
-      const uint4 qv = reinterpret_cast<const uint4 *>(sQ)[o];
-      reinterpret_cast<uint4 *>(ws + kUQ)[o] = qv;
       const uint4 kv = reinterpret_cast<const uint4 *>(sK)[o];
       const int j = ((o >> 7) << 3) | (o & 7);  // row of the 16-byte piece o (kmajor_off with K = 128)
       const float tj = tail[j];
@@ -372,8 +386,8 @@ __global__ void __launch_bounds__(kThreads, kPrepCtasPerSm) gdn_prep_kernel(cons
         tmem_ld16(tmem_addr(tmem, lane_base, kPColW + i0), x);
         tmem_ld_wait();
         const uint32_t off = (i0 >> 3) * 2048 + (row >> 3) * 128 + (row & 7) * 16;
-        store_split8(ws + kUW, ws + kUW + 16384, off, x);
-        store_split8(ws + kUW, ws + kUW + 16384, off + 2048, x + 8);
+        store_split8(ws + kUW, ws + kUWl, off, x);
+        store_split8(ws + kUW, ws + kUWl, off + 2048, x + 8);
       }
     }
     tc_fence_before();
@@ -421,8 +435,10 @@ __global__ void __launch_bounds__(kThreads, kPrepCtasPerSm) gdn_prep_kernel(cons
 // cores with running products of alpha.  One CTA per SM.
 // ===========================================================================
 // ---- one KDA chunk's tiles in the workspace (bytes)
-constexpr uint32_t kVW = 0;        // W hi, lo        [64 i][128 c]   MN-major, as kUW
-constexpr uint32_t kVQ = 32768;    // Qt hi, lo       [64 i][128 c]   K-major
+constexpr uint32_t kVW = 0;        // W hi            [64 i][128 c]   MN-major, as kUW
+constexpr uint32_t kVQ = 16384;    // Qt hi           [64 i][128 c]   MN-major
+constexpr uint32_t kVWl = 32768;   // W lo
+constexpr uint32_t kVQl = 49152;   // Qt lo
 constexpr uint32_t kVMq = 65536;   // Mq hi, lo       [64 i][64 j]
 constexpr uint32_t kVKh = 81920;   // Khat hi, lo     [64 j][128 c]
 constexpr uint32_t kVG = 114688;   // gamma_C         fp32 [128] (per key channel)
@@ -468,39 +484,52 @@ constexpr uint32_t kKColG1 = 0, kKColG2 = 64, kKColW = 128, kKColU = 192, kKdaTm
 // Operands of the level pair (la, lb) into the operand region: rows
 // [k@la; q@la; k@lb; q@lb] of the right-half tokens (32 each) and cols
 // [k@la; k@lb] of the left-half tokens, hi/lo K-major.  A thread takes 8
-// channels of one row; 8 consecutive threads take 8 consecutive rows (one
-// 128-byte core-matrix row group, so stores and lambda loads are conflict-free).
+// channels of one token of one level (a right-half token gives its k row and
+// its q row from one set of decay factors); 8 consecutive threads take 8
+// consecutive operand rows (one 128-byte core-matrix row group), so the
+// stores are conflict-free.
 __device__ __forceinline__ void kda_level_operands(int la, int lb, const unsigned char *sK, const unsigned char *sQ,
                                                    const float *lam, unsigned char *op, int tid) {
-  for (int id = tid; id < 3072; id += kThreads) {
-    const bool is_row = id < 2048;
-    const int idd = is_row ? id : id - 2048;
-    const int row = ((idd >> 7) << 3) | (idd & 7), g = (idd >> 3) & 15;
-    const int sub = row >> 5, w = row & 31;
-    const int lvl = is_row ? (sub < 2 ? la : lb) : (sub == 0 ? la : lb);
+  for (int id = tid; id < 2048; id += kThreads) {
+    const bool is_row = id < 1024;
+    const int idd = id & 1023;
+    const int lsel = idd >> 9;                                         // 0: level la, 1: level lb
+    const int w = (((idd >> 7) & 3) << 3) | (idd & 7), g = (idd >> 3) & 15;
+    const int lvl = lsel ? lb : la;
     const int sh = 5 - lvl, h = 1 << sh, seg = w >> sh;
     const int b = 2 * h * seg + h - 1;                                 // last token of the left half
     const int t = is_row ? b + 1 + (w & (h - 1)) : b - h + 1 + (w & (h - 1));
-    const bool from_q = is_row && (sub & 1);
-    const uint4 raw = *reinterpret_cast<const uint4 *>((from_q ? sQ : sK) + kmajor_off(t, 8 * g, kDK));
     const float4 lt0 = *reinterpret_cast<const float4 *>(lam + t * kLdL + 8 * g);
     const float4 lt1 = *reinterpret_cast<const float4 *>(lam + t * kLdL + 8 * g + 4);
     const float4 lb0 = *reinterpret_cast<const float4 *>(lam + b * kLdL + 8 * g);
     const float4 lb1 = *reinterpret_cast<const float4 *>(lam + b * kLdL + 8 * g + 4);
     const float dt[8] = {lt0.x - lb0.x, lt0.y - lb0.y, lt0.z - lb0.z, lt0.w - lb0.w,
                          lt1.x - lb1.x, lt1.y - lb1.y, lt1.z - lb1.z, lt1.w - lb1.w};
-    const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
+    // right-half row: e^{lambda_t - lambda_b} (t > b); left-half col: e^{lambda_b - lambda_t} (t <= b)
+    float f[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f[e] = __expf(is_row ? dt[e] : -dt[e]);
+    const uint4 kr = *reinterpret_cast<const uint4 *>(sK + kmajor_off(t, 8 * g, kDK));
+    const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w};
     float x[8];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      // right-half row: e^{lambda_t - lambda_b} (t > b); left-half col: e^{lambda_b - lambda_t} (t <= b)
-      x[2 * e] = bf16_to_f32(static_cast<uint16_t>(rw[e] & 0xffff)) * __expf(is_row ? dt[2 * e] : -dt[2 * e]);
-      x[2 * e + 1] = bf16_to_f32(static_cast<uint16_t>(rw[e] >> 16)) * __expf(is_row ? dt[2 * e + 1] : -dt[2 * e + 1]);
+      x[2 * e] = bf16_to_f32(static_cast<uint16_t>(kw[e] & 0xffff)) * f[2 * e];
+      x[2 * e + 1] = bf16_to_f32(static_cast<uint16_t>(kw[e] >> 16)) * f[2 * e + 1];
     }
-    if (is_row)
-      store_split8(op, op + 32768, kmajor_off(row, 8 * g, kDK), x);
-    else
-      store_split8(op + 65536, op + 81920, kmajor_off(row, 8 * g, kDK), x);
+    if (is_row) {
+      store_split8(op, op + 32768, kmajor_off(64 * lsel + w, 8 * g, kDK), x);
+      const uint4 qr = *reinterpret_cast<const uint4 *>(sQ + kmajor_off(t, 8 * g, kDK));
+      const uint32_t qw[4] = {qr.x, qr.y, qr.z, qr.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        x[2 * e] = bf16_to_f32(static_cast<uint16_t>(qw[e] & 0xffff)) * f[2 * e];
+        x[2 * e + 1] = bf16_to_f32(static_cast<uint16_t>(qw[e] >> 16)) * f[2 * e + 1];
+      }
+      store_split8(op, op + 32768, kmajor_off(64 * lsel + 32 + w, 8 * g, kDK), x);
+    } else {
+      store_split8(op + 65536, op + 81920, kmajor_off(32 * lsel + w, 8 * g, kDK), x);
+    }
   }
 }
 
@@ -732,24 +761,46 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
     __syncthreads();
     tc_fence_after();
     if (tid == 0) kda_issue_level_mma(tmem + kKColG1, op_addr, mbG);
-    // meanwhile: Qt, Khat and gamma_C to the workspace
-    for (int id = tid; id < 2 * kC * 16; id += kThreads) {
-      const int kind = id >> 10, idd = id & 1023;
-      const int t = ((idd >> 7) << 3) | (idd & 7), g = (idd >> 3) & 15;
-      const uint4 raw = *reinterpret_cast<const uint4 *>((kind ? sK : sQ) + kmajor_off(t, 8 * g, kDK));
-      const float *lt = lam + t * kLdL + 8 * g, *le = lam + (kC - 1) * kLdL + 8 * g;
+    // meanwhile: Qt (MN-major: 8 tokens of one key per 16 bytes), Khat and
+    // gamma_C to the workspace
+    // (q transposed by ldmatrix, four 8x8 core matrices per warp and step:
+    // lane t holds tokens 2(t%4), 2(t%4)+1 of key 8(4m+j) + t/4)
+    for (int o = warp; o < 32; o += kThreads / 32) {
+      const int ig = o >> 2, m = o & 3;
+      uint32_t r[4];
+      ldsm_x4_trans(smem_addr(sQ) + ig * 2048 + (4 * m + (lane >> 3)) * 128 + (lane & 7) * 16, r);
+      const int t0 = 8 * ig + 2 * (lane & 3);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int c = 8 * (4 * m + j) + (lane >> 2);
+        const float x0 = bf16_to_f32(static_cast<uint16_t>(r[j] & 0xffff)) * __expf(lam[t0 * kLdL + c]);
+        const float x1 = bf16_to_f32(static_cast<uint16_t>(r[j] >> 16)) * __expf(lam[(t0 + 1) * kLdL + c]);
+        const __nv_bfloat162 hb = __floats2bfloat162_rn(x0, x1);
+        const float2 hf = __bfloat1622float2(hb);
+        const __nv_bfloat162 lb = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+        const uint32_t off = ig * 2048 + (c >> 3) * 128 + (c & 7) * 16 + (lane & 3) * 4;
+        *reinterpret_cast<__nv_bfloat162 *>(ws + kVQ + off) = hb;
+        *reinterpret_cast<__nv_bfloat162 *>(ws + kVQl + off) = lb;
+      }
+    }
+    for (int id = tid; id < kC * 16; id += kThreads) {
+      // Khat = k (.) e^{lambda_C - lambda_t}, K-major
+      const int t = ((id >> 7) << 3) | (id & 7), g = (id >> 3) & 15;
+      const uint4 raw = *reinterpret_cast<const uint4 *>(sK + kmajor_off(t, 8 * g, kDK));
+      const float4 t0v = *reinterpret_cast<const float4 *>(lam + t * kLdL + 8 * g);
+      const float4 t1v = *reinterpret_cast<const float4 *>(lam + t * kLdL + 8 * g + 4);
+      const float4 e0v = *reinterpret_cast<const float4 *>(lam + (kC - 1) * kLdL + 8 * g);
+      const float4 e1v = *reinterpret_cast<const float4 *>(lam + (kC - 1) * kLdL + 8 * g + 4);
+      const float d[8] = {e0v.x - t0v.x, e0v.y - t0v.y, e0v.z - t0v.z, e0v.w - t0v.w,
+                          e1v.x - t1v.x, e1v.y - t1v.y, e1v.z - t1v.z, e1v.w - t1v.w};
       const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
       float x[8];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        // Qt: e^{lambda_t};  Khat: e^{lambda_C - lambda_t}
-        const float d0 = kind ? le[2 * e] - lt[2 * e] : lt[2 * e];
-        const float d1 = kind ? le[2 * e + 1] - lt[2 * e + 1] : lt[2 * e + 1];
-        x[2 * e] = bf16_to_f32(static_cast<uint16_t>(rw[e] & 0xffff)) * __expf(d0);
-        x[2 * e + 1] = bf16_to_f32(static_cast<uint16_t>(rw[e] >> 16)) * __expf(d1);
+        x[2 * e] = bf16_to_f32(static_cast<uint16_t>(rw[e] & 0xffff)) * __expf(d[2 * e]);
+        x[2 * e + 1] = bf16_to_f32(static_cast<uint16_t>(rw[e] >> 16)) * __expf(d[2 * e + 1]);
       }
-      unsigned char *dst = ws + (kind ? kVKh : kVQ);
-      store_split8(dst, dst + 16384, kmajor_off(t, 8 * g, kDK), x);
+      store_split8(ws + kVKh, ws + kVKh + 16384, kmajor_off(t, 8 * g, kDK), x);
     }
     if (tid < kDK) reinterpret_cast<float *>(ws + kVG)[tid] = __expf(lam[(kC - 1) * kLdL + tid]);
     if (!wait_ok(mbG, 0)) { failed = true; break; }
@@ -813,7 +864,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
     for (int id = tid; id < kC * 16; id += kThreads) {
       const int t = ((id >> 7) << 3) | (id & 7), g = (id >> 3) & 15;
       const uint4 raw = *reinterpret_cast<const uint4 *>(sK + kmajor_off(t, 8 * g, kDK));
-      const float *lt = lam + t * kLdL + 8 * g;
+      const float4 t0v = *reinterpret_cast<const float4 *>(lam + t * kLdL + 8 * g);
+      const float4 t1v = *reinterpret_cast<const float4 *>(lam + t * kLdL + 8 * g + 4);
+      const float lt[8] = {t0v.x, t0v.y, t0v.z, t0v.w, t1v.x, t1v.y, t1v.z, t1v.w};
       const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
       float x[8];
 #pragma unroll
@@ -851,8 +904,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
         tmem_ld16(tmem_addr(tmem, lane_base, kKColW + i0), x);
         tmem_ld_wait();
         const uint32_t off = (i0 >> 3) * 2048 + (row >> 3) * 128 + (row & 7) * 16;
-        store_split8(ws + kVW, ws + kVW + 16384, off, x);
-        store_split8(ws + kVW, ws + kVW + 16384, off + 2048, x + 8);
+        store_split8(ws + kVW, ws + kVWl, off, x);
+        store_split8(ws + kVW, ws + kVWl, off + 2048, x + 8);
       }
     }
     tc_fence_before();
@@ -875,13 +928,16 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
 // Warps 0-15 (workers): warp w owns tensor-memory lanes 32*(w%4) .. +31
 // (value rows d) and quarter w/4 of each tile's columns; it keeps its 32
 // columns of S^T in registers.  Warp 16 (producer, one lane) issues the bulk
-// copies and the MMAs.  Per chunk:
-//   round 1  X = S0^T W^T (then Y1 = S0^T Q^T), issued in two column groups as
-//            the workers publish the bf16 split of S0 (S_ready[g]);
+// copies and the MMAs.  Per chunk, the state's own chain first and the output
+// behind it (the tensor pipe runs one thread's MMAs in order):
+//   round 1  [X | Y1] = S0^T [W^T | Q^T] as one MMA group of N = 128,
+//            issued in two column groups as the workers publish the bf16
+//            split of S0 (S_ready[g]); the next chunk's W and Q load as soon
+//            as it is done;
 //   workers  U^T = Ut^T - X, split, published (U_ready);
-//   round 2  Y2 = U^T Mq^T, then D = U^T Khat;
-//   workers  y = gamma_i Y1 + Y2; S^T <- gamma_C S^T + D, split for the next
-//            round 1.
+//   round 2  D = U^T Khat; then Y2 = U^T Mq^T;
+//   workers  S^T <- gamma_C S^T + D, split for the next round 1; then
+//            y = gamma_i Y1 + Y2 (GDN) or Y1 + Y2 (KDA).
 // ===========================================================================
 struct ChainArgs {
   float *state;
@@ -898,9 +954,10 @@ constexpr int kChainThreads = kWorkers + 32;
 
 // tensor-memory columns (fp32)
 constexpr uint32_t kColD = 0;     // U^T Khat     [128 d x 128 c]
-constexpr uint32_t kColX = 128;   // S0^T W^T     [128 x 64]
-constexpr uint32_t kColY1 = 192;  // S0^T Q^T     [128 x 64]
-constexpr uint32_t kColY2 = 256;  // U^T Mq^T     [128 x 64]
+constexpr uint32_t kColXY = 128;  // [S0^T W^T | S0^T Q^T]  [128 x (64 + 64)], one MMA group of N = 128;
+                                  // two buffers by chunk parity (chunk c+1's group may be issued
+                                  // while the workers still read chunk c's Y1)
+constexpr uint32_t kColY2 = 384;  // U^T Mq^T     [128 x 64]
 constexpr uint32_t kChainTmemCols = 512;
 
 // shared memory (bytes) and the unit layout the chain reads, GDN or KDA
@@ -925,9 +982,10 @@ struct ChainLayout {
   static_assert(smem <= 227 * 1024, "chain shared memory");
 };
 
-// bounded wait that also gives up as soon as another thread has
+// bounded wait (about 0.13 s) that also gives up as soon as another thread has
+constexpr uint32_t kHintedWaitLimit = 1u << 17;
 __device__ __forceinline__ bool chain_wait(uint32_t mbar, uint32_t parity, volatile int *abort_flag) {
-  return mbar_wait_abortable(mbar, parity, kWaitLimit, abort_flag);
+  return mbar_wait_hinted(mbar, parity, kHintedWaitLimit, abort_flag);
 }
 
 template <bool KDA>
@@ -944,15 +1002,15 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
   unsigned char *sSh = sm + kCS, *sSl = sm + kCS + 32768;
   unsigned char *sUh = sm + kCU, *sUl = sm + kCU + 16384;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::cbar);
-  // barriers: 0 W, 1 M, 2-3 gamma buffers, 4 X done, 5 round 1 done, 6 Y2 done,
-  // 7 round 2 done, 8-9 S_ready[g], 10 U_ready, 11 drain
+  // barriers: 0 W, 1 M, 2-3 gamma buffers, 4 round 1 ([X | Y1]) done, 5 unused,
+  // 6 Y2 done (the chunk's last MMA), 7 D done, 8-9 S_ready[g], 10 U_ready, 11 drain
   auto bar = [&](int i) { return smem_addr(bars + i); };
   uint32_t *holder = reinterpret_cast<uint32_t *>(sm + L::cbar + kNBar * 8);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::cbar + kNBar * 8 + 4);
 
   if (tid == 0) {
     for (int i = 0; i < 8; ++i) mbar_init(bar(i), 1);
-    for (int i = 8; i < 11; ++i) mbar_init(bar(i), kWorkers);
+    for (int i = 8; i < 11; ++i) mbar_init(bar(i), kWorkers / 32);  // one arrival per worker warp
     mbar_init(bar(11), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -976,12 +1034,15 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
 #pragma unroll
     for (int j = 0; j < 32; ++j) S[j] = gS[static_cast<long>(32 * qtr + j) * kDV + row];
     // publish the bf16 split of columns [32*qtr + 16g, +16) of S^T
+    // a warp's stores are fenced towards the tensor core by every lane, then
+    // ordered within the warp, then released by one arrival
     auto publish_s = [&](int g) {
       store_split8(sSh, sSl, kmajor_off(row, 32 * qtr + 16 * g, kDK), S + 16 * g);
       store_split8(sSh, sSl, kmajor_off(row, 32 * qtr + 16 * g + 8, kDK), S + 16 * g + 8);
       fence_async_smem();
       tc_fence_before();
-      mbar_arrive(bar(8 + g));
+      __syncwarp();
+      if ((tid & 31) == 0) mbar_arrive(bar(8 + g));
     };
     publish_s(0);
     publish_s(1);
@@ -1000,7 +1061,7 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
       if (!wwait(bar(4), par)) break;
       {
         float x[16];
-        tmem_ld16(lanes + kColX + 16 * qtr, x);
+        tmem_ld16(lanes + kColXY + 128 * (c & 1) + 16 * qtr, x);
         tmem_ld_wait();
 #pragma unroll
         for (int e = 0; e < 16; ++e) x[e] = ut[e] - x[e];
@@ -1008,32 +1069,17 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
         store_split8(sUh, sUl, kmajor_off(row, 16 * qtr + 8, kC), x + 8);
         fence_async_smem();
         tc_fence_before();
-        mbar_arrive(bar(10));
+        __syncwarp();
+        if ((tid & 31) == 0) mbar_arrive(bar(10));
       }
       if (!last) load_ut(c + 1);
-      // y = gamma_i Y1 + Y2 (GDN) or Y1 + Y2 (KDA: the decay is inside Qt)
-      if (!wwait(bar(6), par)) break;
+      // this chunk's gammas (loaded long before; checked while D runs)
       if (!wwait(bar(2 + (c & 1)), static_cast<uint32_t>((c >> 1) & 1))) break;
-      const float *gbuf = reinterpret_cast<const float *>(sm + L::cg + (c & 1) * L::g_bytes);
-      {
-        const float *gam = gbuf + 16 * qtr;
-        const int t0 = c * kC + 16 * qtr;
-        float *yp = a.y + (tok0 + static_cast<long>(t0) * H) * kDV + row;
-#pragma unroll
-        for (int h8 = 0; h8 < 16; h8 += 8) {
-          float y1[8], y2[8];
-          tmem_ld8(lanes + kColY1 + 16 * qtr + h8, y1);
-          tmem_ld8(lanes + kColY2 + 16 * qtr + h8, y2);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            if (t0 + h8 + e < T)
-              yp[static_cast<long>(h8 + e) * H * kDV] = KDA ? y1[e] + y2[e] : fmaf(gam[h8 + e], y1[e], y2[e]);
-        }
-      }
       // S^T <- gamma_C S^T + D (KDA: gamma_C per key channel, i.e. per column
-      // of S^T), published group by group for the next round 1
+      // of S^T), published group by group for the next round 1.  D completing
+      // also means Y1 (issued before it) no longer reads the published S.
       if (!wwait(bar(7), par)) break;
+      const float *gbuf = reinterpret_cast<const float *>(sm + L::cg + (c & 1) * L::g_bytes);
 #pragma unroll
       for (int g = 0; g < 2; ++g) {
         float x[16];
@@ -1047,24 +1093,43 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) gS[static_cast<long>(32 * qtr + j) * kDV + row] = S[j];
       }
+      // y = gamma_i Y1 + Y2 (GDN) or Y1 + Y2 (KDA: the decay is inside Qt),
+      // off the state's critical path
+      if (!wwait(bar(6), par)) break;
+      {
+        const float *gam = gbuf + 16 * qtr;
+        const int t0 = c * kC + 16 * qtr;
+        float *yp = a.y + (tok0 + static_cast<long>(t0) * H) * kDV + row;
+#pragma unroll
+        for (int h8 = 0; h8 < 16; h8 += 8) {
+          float y1[8], y2[8];
+          tmem_ld8(lanes + kColXY + 128 * (c & 1) + 64 + 16 * qtr + h8, y1);
+          tmem_ld8(lanes + kColY2 + 16 * qtr + h8, y2);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            if (t0 + h8 + e < T)
+              yp[static_cast<long>(h8 + e) * H * kDV] = KDA ? y1[e] + y2[e] : fmaf(gam[h8 + e], y1[e], y2[e]);
+        }
+      }
     }
   } else if (tid == kWorkers) {
     // ------------------------------------------------------------ producer
     const uint32_t sh = smem_addr(sSh), sl = smem_addr(sSl), uh = smem_addr(sUh), ul = smem_addr(sUl);
-    const uint32_t wh = smem_addr(sm + kCW), wl = wh + 16384, qa = wh + 32768;
+    // W region: W hi, Q / Qt hi, W lo, (KDA) Qt lo, all MN-major with 8-token
+    // groups 2048 bytes apart, so [W hi; Q hi] and [W lo; Qt lo] are B
+    // operands of N = 128 tokens
+    const uint32_t wh = smem_addr(sm + kCW), wl = wh + 32768;
     const uint32_t mh = smem_addr(sm + L::cm), ml = mh + 8192, kh = mh + 16384, kl = mh + 32768;
     const uint32_t id64 = idesc_bf16_f32(128, kC), id128 = idesc_bf16_f32(128, kDK);
     // operand descriptors at k-step 0; k-step ks starts 256 bytes further on,
     // i.e. 16 in the descriptor's address field
-    const uint64_t dSh = smem_desc(sh, 128, kDK * 16), dSl = smem_desc(sl, 128, kDK * 16);
-    // W and Khat^T arrive MN-major (token-contiguous W, column-contiguous Khat)
-    const uint64_t dWh = smem_desc(wh, 128, 2048), dWl = smem_desc(wl, 128, 2048);
-    const uint64_t dQ = smem_desc(qa, 128, kDK * 16);              // Q (GDN) or Qt hi (KDA)
-    const uint64_t dQl = smem_desc(qa + 16384, 128, kDK * 16);     // Qt lo (KDA)
-    const uint64_t dUh = smem_desc(uh, 128, kC * 16), dUl = smem_desc(ul, 128, kC * 16);
+    const uint64_t dSh = smem_desc(smem_addr(sSh), 128, kDK * 16), dSl = smem_desc(smem_addr(sSl), 128, kDK * 16);
+    const uint64_t dWQh = smem_desc(wh, 128, 2048), dWQl = smem_desc(wl, 128, 2048);
+    const uint64_t dUh = smem_desc(smem_addr(sUh), 128, kC * 16), dUl = smem_desc(smem_addr(sUl), 128, kC * 16);
     const uint64_t dMh = smem_desc(mh, 128, kC * 16), dMl = smem_desc(ml, 128, kC * 16);
     const uint64_t dKh = smem_desc(kh, 2048, 128), dKl = smem_desc(kl, 2048, 128);
-    const uint32_t id64w = id64 | (1u << 16), id128k = id128 | (1u << 16);  // B MN-major
+    const uint32_t id64w = id64 | (1u << 16), id128w = id128 | (1u << 16), id128k = id128 | (1u << 16);  // B MN-major
     // k-step ks: A advances 256 bytes (16 in the descriptor); B by bstep
     auto mma = [&](uint32_t d, uint64_t A, uint64_t Bm, int ks, uint32_t idesc, bool acc, uint32_t bstep = 16u) {
       mma_bf16(d, A + 16u * ks, Bm + bstep * ks, idesc, acc);
@@ -1101,7 +1166,11 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
     for (int c = 0; c < n && ok; ++c) {
       const uint32_t par = static_cast<uint32_t>(c & 1);
       if (c + 2 < n) prefetch(c + 2);  // chunk c + 2 into L2 while this one runs
-      // round 1, column group g = k-steps g, g + 2, g + 4, g + 6 of S^T
+      // round 1: [X | Y1] = S0^T [W^T | Q^T] as each column group g (k-steps
+      // g, g + 2, g + 4, g + 6) of S^T is published: S hi x [W hi; Q], S hi x
+      // W lo (GDN, N = 64: Q is exact) or S hi x [W lo; Qt lo] (KDA), S lo x
+      // [W hi; Q]
+      const uint32_t xy = tmem + kColXY + 128 * (c & 1);
       ok = chain_wait(bar(0), par, abort_flag);
       if (ok) ++w_done;
 #pragma unroll
@@ -1110,32 +1179,25 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
         if (!ok) break;
 #pragma unroll
         for (int ks = g; ks < 8; ks += 2) {
-          mma(tmem + kColX, dSh, dWh, ks, id64w, ks != 0);
-          mma(tmem + kColX, dSh, dWl, ks, id64w, true);
-          mma(tmem + kColX, dSl, dWh, ks, id64w, true);
-        }
-        if (g == 1 && !(a.drop_signal && c == 0)) mma_commit(bar(4));
-#pragma unroll
-        for (int ks = g; ks < 8; ks += 2) {
-          mma(tmem + kColY1, dSh, dQ, ks, id64, ks != 0);
-          if (KDA) mma(tmem + kColY1, dSh, dQl, ks, id64, true);
-          mma(tmem + kColY1, dSl, dQ, ks, id64, true);
+          mma(xy, dSh, dWQh, ks, id128w, ks != 0);
+          mma(xy, dSh, dWQl, ks, KDA ? id128w : id64w, true);
+          mma(xy, dSl, dWQh, ks, id128w, true);
         }
       }
       if (!ok) break;
-      mma_commit(bar(5));
-      // round 2
+      if (!(a.drop_signal && c == 0)) mma_commit(bar(4));
+      // the W region is free once the group is done: the next chunk's W and Q
+      if (c + 1 < n) {
+        ok = chain_wait(bar(4), par, abort_flag);
+        if (!ok) break;
+        load(0, c + 1);
+      }
+      // round 2: D = U^T Khat first (the state update waits for it), then
+      // Y2 = U^T Mq^T
       ok = chain_wait(bar(1), par, abort_flag);
       if (ok) ++m_done;
       if (ok) ok = chain_wait(bar(10), par, abort_flag);
       if (!ok) break;
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        mma(tmem + kColY2, dUh, dMh, ks, id64, ks != 0);
-        mma(tmem + kColY2, dUh, dMl, ks, id64, true);
-        mma(tmem + kColY2, dUl, dMh, ks, id64, true);
-      }
-      mma_commit(bar(6));
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
         mma(tmem + kColD, dUh, dKh, ks, id128k, ks != 0, 256u);
@@ -1143,11 +1205,17 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
         mma(tmem + kColD, dUl, dKh, ks, id128k, true, 256u);
       }
       mma_commit(bar(7));
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        mma(tmem + kColY2, dUh, dMh, ks, id64, ks != 0);
+        mma(tmem + kColY2, dUh, dMl, ks, id64, true);
+        mma(tmem + kColY2, dUl, dMh, ks, id64, true);
+      }
+      mma_commit(bar(6));
       if (c + 1 < n) {
-        // the next chunk's operands, each as soon as its buffer is free
-        ok = chain_wait(bar(5), par, abort_flag);
-        if (ok) load(0, c + 1);
-        if (ok) ok = chain_wait(bar(7), par, abort_flag);
+        // the next chunk's Mq, Khat and gammas once Y2 (the chunk's last MMA,
+        // which reads Mq) is done
+        ok = chain_wait(bar(6), par, abort_flag);
         if (ok) load(1, c + 1);
       }
     }

@@ -199,6 +199,32 @@ __device__ __forceinline__ bool mbar_wait_abortable(uint32_t mbar, uint32_t pari
   return false;
 }
 
+// Wait as mbar_wait_abortable does, but each poll lets the hardware suspend
+// the thread for up to 1 us until the phase completes (try_wait with a
+// suspend-time hint), so a completion is seen as soon as it happens without
+// busy polling.  At most `limit` polls (about limit microseconds); a wait
+// that runs out sets the abort flag.
+__device__ __forceinline__ bool mbar_wait_hinted(uint32_t mbar, uint32_t parity, uint32_t limit,
+                                                 volatile int *abort_flag) {
+  for (uint32_t i = 0; i < limit; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(done)
+        : "r"(mbar), "r"(parity), "n"(1000)
+        : "memory");
+    if (done) {
+      asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+      return true;
+    }
+    if (*abort_flag) return false;
+  }
+  *abort_flag = 1;
+  return false;
+}
+
 // 8 consecutive fp32 -> one 16-byte chunk of bf16 hi and one of bf16 lo
 // (hi = bf16(x), lo = bf16(x - hi), converted two at a time)
 __device__ __forceinline__ void store_split8(unsigned char *hi, unsigned char *lo, uint32_t off, const float *x) {
@@ -213,6 +239,16 @@ __device__ __forceinline__ void store_split8(unsigned char *hi, unsigned char *l
   }
   *reinterpret_cast<uint4 *>(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
   *reinterpret_cast<uint4 *>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// Four 8x8 b16 matrices from shared memory, transposed: lane l gives the
+// address of row l%8 of matrix l/8 (16 contiguous bytes); afterwards r[j] of
+// lane t holds column t/4 of matrix j, rows 2(t%4) (low half) and 2(t%4)+1.
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t saddr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(saddr)
+               : "memory");
 }
 
 // split x into bf16 hi + bf16 lo with hi + lo = x to ~2^-16 relative
