@@ -410,7 +410,10 @@ class GpuRun:
         elif wl.kind == "gdn2":
             self.state = torch.zeros((sh.B, sh.H, sh.dk, sh.dv), dtype=torch.float32, device=device)
             self.y = torch.empty((sh.B, sh.T, sh.H, sh.dv), dtype=torch.float32, device=device)
-            self.launches_per_step = 1
+            nws = sdm.gdn2_scan_workspace_size(sh.B, sh.T, sh.H, sh.dk, sh.dv)
+            self.ws = torch.empty(max(nws, 1), dtype=torch.uint8, device=device)
+            # chunked: preparation kernel + chain kernel; token-recurrent: one kernel
+            self.launches_per_step = 2 if nws > 0 else 1
         elif wl.kind in ("gdn", "kda"):
             self.state = torch.zeros((sh.B, sh.H, sh.dk, sh.dv), dtype=torch.float32, device=device)
             self.y = torch.empty((sh.B, sh.T, sh.H, sh.dv), dtype=torch.float32, device=device)
@@ -548,7 +551,8 @@ class GpuRun:
             self.sdm.sdm_scan(self.state, d["v"], d["alpha"], d["beta"], self.iw, self.ww, self.ir, self.wr,
                               self.wl.mode, self.y, self.ws, self.err)
         elif self.wl.kind == "gdn2":
-            self.sdm.gdn2_scan(self.state, d["q"], d["k"], d["v"], d["alpha_kda"], d["b_erase"], d["w_write"], self.y)
+            self.sdm.gdn2_scan(self.state, d["q"], d["k"], d["v"], d["alpha_kda"], d["b_erase"], d["w_write"], self.y,
+                               workspace=self.ws, dev_err=self.err)
         elif self.wl.kind in ("gdn", "kda"):
             a = d["alpha_kda" if self.wl.kind == "kda" else "alpha_gdn"]
             self.sdm.gdn_scan(self.state, d["q"], d["k"], d["v"], a, d["beta"], self.wl.kind == "kda", self.y,
@@ -725,7 +729,7 @@ def run_ours(args, rank, world, local_rank, sampler):
         # FP32 FMA pipe: 152 SMs x 128 lanes x 2 flop x max SM clock
         peak = 152 * 128 * 2 * float(pk.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
         achieved = algo / (main_ms * 1e-3) / 1e12
-    kernel_file = {"sdm": "sparse_scan.cu", "gdn": "gdn_chunk.cu", "kda": "gdn_chunk.cu", "gdn2": "gdn_scan.cu",
+    kernel_file = {"sdm": "sparse_scan.cu", "gdn": "gdn_chunk.cu", "kda": "gdn_chunk.cu", "gdn2": "gdn_chunk.cu",
                    "sse": "sse_chunk.cu" if wl.sse_chunked else "sse_scan.cu"}[wl.kind]
     tr = NCU_TRAFFIC.get((wl.name, wl.kind))
     traffic = tr["bytes"] if tr and tr["digest"] == _src_digest(kernel_file) else None
@@ -750,7 +754,8 @@ def run_ours(args, rank, world, local_rank, sampler):
                      "sdm_scan_chunked (chunk preparation + chain kernels)" if wl.chunked else
                      {"sdm": "sdm_scan (hazard prepass + sparse_scan_kernel)",
                       "gdn": "gdn_scan (chunk preparation + chain kernels)",
-                      "kda": "gdn_scan, per-channel decay (KDA chunk preparation + chain kernels)", "gdn2": "gdn2_scan",
+                      "kda": "gdn_scan, per-channel decay (KDA chunk preparation + chain kernels)",
+                      "gdn2": "gdn2_scan (GDN2 chunk preparation + chain kernels)",
                       "sse": "sse_scan (route, group, chunk preparation, chain, combine kernels)"
                       if wl.sse_chunked else "sse_scan (route prepass + sse_scan_kernel)"}[wl.kind],
                      "launch_ms": main_ms, "peak_source": f"{src} ({'hbm_gbs' if bound == 'hbm' else 'FP32 lanes x clock'})",

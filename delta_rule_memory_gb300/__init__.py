@@ -23,7 +23,7 @@ __all__ = [
     "sdm_scan_noalloc", "sdm_forward_host", "sdm_forward_host_workspace_size", "sdm_scan_train",
     "sdm_scan_backward", "sdm_scan_backward_workspace_size", "sdm_address_backward", "sdm_scan_chunked",
     "sdm_scan_chunked_workspace_size",
-    "gdn_scan", "gdn_scan_workspace_size", "gdn2_scan", "sse_scan", "sse_scan_workspace_size", "SDM_RESID_SHARED", "SDM_RESID_PERSLOT", "SSE_WRITE_ADDITIVE", "SSE_WRITE_DELTA",
+    "gdn_scan", "gdn_scan_workspace_size", "gdn2_scan", "gdn2_scan_workspace_size", "sse_scan", "sse_scan_workspace_size", "SDM_RESID_SHARED", "SDM_RESID_PERSLOT", "SSE_WRITE_ADDITIVE", "SSE_WRITE_DELTA",
     "SDM_RESID_ADDITIVE", "SDM_DEVERR_INDEX_RANGE", "SDM_DEVERR_INDEX_REPEAT", "SDM_DEVERR_NONFINITE",
     "SDM_DEVERR_TIMEOUT", "SDM_ERR_DEVICE",
 ]
@@ -62,7 +62,8 @@ _SIGNATURES = {
                               _SZ, _P, _P]),
     "gdn_scan_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "gdn_scan": (_I, [_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _SZ, _P, _P]),
-    "gdn2_scan": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "gdn2_scan_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "gdn2_scan": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _SZ, _P, _P]),
     "sse_scan_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I, _I]),
     "sse_scan": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _SZ, _P, _P]),
 }
@@ -458,7 +459,11 @@ def gdn_scan(state, q, k, v, alpha, beta, per_channel: bool, y=None, workspace=N
     return y
 
 
-def gdn2_scan(state, q, k, v, alpha, b_erase, w_write, y=None, dev_err=None, stream=None):
+def gdn2_scan_workspace_size(B: int, T: int, H: int, dk: int, dv: int) -> int:
+    return int(lib().gdn2_scan_workspace_size(B, T, H, dk, dv))
+
+
+def gdn2_scan(state, q, k, v, alpha, b_erase, w_write, y=None, workspace=None, dev_err=None, stream=None):
     """GDN2 scan; updates `state` [B,H,dk,dv] in place and returns y fp32
     [B,T,H,dv].  q, k bf16 [B,T,H,dk]; v bf16 [B,T,H,dv]; alpha and b_erase
     fp32 [B,T,H,dk]; w_write fp32 [B,T,H,dv]."""
@@ -477,11 +482,16 @@ def gdn2_scan(state, q, k, v, alpha, b_erase, w_write, y=None, dev_err=None, str
     if y is None:
         y = torch.empty((B, T, H, dv), dtype=torch.float32, device=state.device)
     _req(y, "y", torch.float32, (B, T, H, dv))
+    need = gdn2_scan_workspace_size(B, T, H, dk, dv)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=state.device)
+    if workspace is not None:
+        _req(workspace, "workspace", torch.uint8)
     if dev_err is not None:
         _req(dev_err, "dev_err", torch.int32)
     rc = lib().gdn2_scan(state.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), alpha.data_ptr(),
-                         b_erase.data_ptr(), w_write.data_ptr(), B, T, H, dk, dv, y.data_ptr(), _ptr(dev_err),
-                         _stream(stream))
+                         b_erase.data_ptr(), w_write.data_ptr(), B, T, H, dk, dv, y.data_ptr(), _ptr(workspace),
+                         0 if workspace is None else workspace.numel(), _ptr(dev_err), _stream(stream))
     _check("gdn2_scan", rc)
     return y
 

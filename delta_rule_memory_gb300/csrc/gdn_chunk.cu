@@ -450,6 +450,7 @@ static_assert(kVUnit % 16 == 0 && kVMq % 16 == 0 && (kVG - kVMq) % 16 == 0 && (k
 struct KdaPrepArgs {
   const uint16_t *q, *k, *v;
   const float *alpha, *beta;
+  const float *b_erase, *w_write;  // GDN2 only: erase gate [B,T,H,dk], write gate [B,T,H,dv]
   unsigned char *ws;
   int T, H, nchunks;
   long units;  // B * H * nchunks
@@ -478,6 +479,7 @@ constexpr uint32_t kOT = kOZ + 4096;              // T hi, lo [64 i][64 j]
 constexpr uint32_t kOKt = kOT + 16384;            // Kt hi, lo [64][128]
 static_assert(kKAlBytes >= kC * kDK * 4, "alpha fits the staging region");
 static_assert(kOKt + 32768 <= kKOpBytes, "solve and Kt fit the operand region");
+static_assert(kOL + 32768 <= kOZ, "GDN2's Z hi/lo fits the solve buffers (L, L^-1) it replaces");
 static_assert(kKdaSmem <= 227 * 1024, "one KDA preparation CTA per SM");
 constexpr uint32_t kKColG1 = 0, kKColG2 = 64, kKColW = 128, kKColU = 192, kKdaTmemCols = 256;
 
@@ -488,8 +490,12 @@ constexpr uint32_t kKColG1 = 0, kKColG2 = 64, kKColW = 128, kKColU = 192, kKdaTm
 // its q row from one set of decay factors); 8 consecutive threads take 8
 // consecutive operand rows (one 128-byte core-matrix row group), so the
 // stores are conflict-free.
+// GDN2: the k rows of A are e_t = b_t (.) k_t (the erase gate times the key),
+// read as gb[t * gstride + c] for the chunk's valid tokens t < nvalid.
+template <bool G2>
 __device__ __forceinline__ void kda_level_operands(int la, int lb, const unsigned char *sK, const unsigned char *sQ,
-                                                   const float *lam, unsigned char *op, int tid) {
+                                                   const float *lam, unsigned char *op, int tid, const float *gb,
+                                                   long gstride, int nvalid) {
   for (int id = tid; id < 2048; id += kThreads) {
     const bool is_row = id < 1024;
     const int idd = id & 1023;
@@ -517,6 +523,16 @@ __device__ __forceinline__ void kda_level_operands(int la, int lb, const unsigne
       x[2 * e] = bf16_to_f32(static_cast<uint16_t>(kw[e] & 0xffff)) * f[2 * e];
       x[2 * e + 1] = bf16_to_f32(static_cast<uint16_t>(kw[e] >> 16)) * f[2 * e + 1];
     }
+    if (G2 && is_row) {
+      float bv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (t < nvalid) {
+        const float4 b0 = __ldg(reinterpret_cast<const float4 *>(gb + t * gstride + 8 * g));
+        const float4 b1 = __ldg(reinterpret_cast<const float4 *>(gb + t * gstride + 8 * g + 4));
+        bv[0] = b0.x; bv[1] = b0.y; bv[2] = b0.z; bv[3] = b0.w; bv[4] = b1.x; bv[5] = b1.y; bv[6] = b1.z; bv[7] = b1.w;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] *= bv[e];
+    }
     if (is_row) {
       store_split8(op, op + 32768, kmajor_off(64 * lsel + w, 8 * g, kDK), x);
       const uint4 qr = *reinterpret_cast<const uint4 *>(sQ + kmajor_off(t, 8 * g, kDK));
@@ -536,6 +552,7 @@ __device__ __forceinline__ void kda_level_operands(int la, int lb, const unsigne
 // The pairs of the level pair (la, lb) kept from the product in tensor memory
 // (lanes = operand rows, columns = operand cols) into the A / Mq staging.
 // Warp w reads lanes 32*(w%4) (one row kind) and 16 of its level's 32 columns.
+template <bool G2>
 __device__ __forceinline__ void kda_level_extract(int la, int lb, uint32_t tmem_col, float *sAst, float *sMst,
                                                   const float *be, int warp, int lane) {
   const int sub = warp & 3, half = warp >> 2;
@@ -554,7 +571,7 @@ __device__ __forceinline__ void kda_level_extract(int la, int lb, uint32_t tmem_
       if (sub & 1)
         sMst[ti * kLdS + tj] = x[e];
       else
-        sAst[ti * kLdS + tj] = be[ti] * x[e];
+        sAst[ti * kLdS + tj] = G2 ? x[e] : be[ti] * x[e];
     }
   }
 }
@@ -572,6 +589,7 @@ __device__ __forceinline__ void kda_issue_level_mma(uint32_t tmem_d, uint32_t op
   mma_commit(mbar);
 }
 
+template <bool G2>
 __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs a) {
   extern __shared__ __align__(1024) unsigned char sm[];
   const int tid = threadIdx.x;
@@ -610,6 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
   // W^T = Kt^T T^T and Ut^T = V^T T^T: A operands MN-major (k-step = 16 tokens = 4096 bytes)
   const uint64_t dKtmn_h = smem_desc(smem_addr(sKth), 2048, 128), dKtmn_l = smem_desc(smem_addr(sKtl), 2048, 128);
   const uint64_t dVmn = smem_desc(smem_addr(sV), 2048, 128);
+  const uint64_t dZmn_h = smem_desc(smem_addr(op + kOL), 2048, 128), dZmn_l = smem_desc(smem_addr(op + kOL + 16384), 2048, 128);
   const uint64_t dTh = smem_desc(smem_addr(sTh), 128, kC * 16), dTl = smem_desc(smem_addr(sTl), 128, kC * 16);
   const uint32_t idMN = idesc_bf16_f32(128, kC) | (1u << 15);
 
@@ -628,6 +647,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
     const long bh = u / a.nchunks;
     const int t0 = static_cast<int>(u - bh * a.nchunks) * kC;
     const long tok0 = (bh / H) * T * H + bh % H;
+    // GDN2 gates of the chunk's tokens: row t at gb[t * gstride], valid for t < nvalid
+    const long gstride = static_cast<long>(H) * kDK;
+    const int nvalid = T - t0 < kC ? T - t0 : kC;
+    const float *gb = G2 ? a.b_erase + (tok0 + static_cast<long>(t0) * H) * kDK : nullptr;
+    const float *gw = G2 ? a.w_write + (tok0 + static_cast<long>(t0) * H) * kDV : nullptr;
 
     // ---- inputs: K, Q, V tiles, alpha rows, beta (padding: k = q = v = 0, alpha = 1, beta = 0)
     for (int id = tid; id < 3 * kC * 16; id += kThreads) {
@@ -647,7 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
       else
         *reinterpret_cast<float4 *>(al + r * kDK + 4 * c4) = make_float4(1.f, 1.f, 1.f, 1.f);
     }
-    if (tid < kC) {
+    if (tid < kC && !G2) {
       const int t = t0 + tid;
       if (t < T)
         cp_async<4>(be + tid, a.beta + tok0 + static_cast<long>(t) * H);
@@ -695,6 +719,25 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
           af[i][0] = a0.x; af[i][1] = a0.y; af[i][2] = a0.z; af[i][3] = a0.w;
           af[i][4] = a1.x; af[i][5] = a1.y; af[i][6] = a1.z; af[i][7] = a1.w;
         }
+        // left factors of A: k (KDA, beta applied later) or e = b (.) k (GDN2)
+        float ef[4][8];
+#pragma unroll
+        for (int i = 1; i < 4; ++i) {
+          const int t = 4 * blk + i;
+          float bv[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
+          if (G2) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) bv[e] = 0.f;
+            if (t < nvalid) {
+              const float4 b0 = __ldg(reinterpret_cast<const float4 *>(gb + t * gstride + 8 * cg));
+              const float4 b1 = __ldg(reinterpret_cast<const float4 *>(gb + t * gstride + 8 * cg + 4));
+              bv[0] = b0.x; bv[1] = b0.y; bv[2] = b0.z; bv[3] = b0.w;
+              bv[4] = b1.x; bv[5] = b1.y; bv[6] = b1.z; bv[7] = b1.w;
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) ef[i][e] = bv[e] * kf[i][e];
+        }
         float v[16];
 #pragma unroll
         for (int o = 0; o < 16; ++o) v[o] = 0.f;
@@ -702,12 +745,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
         for (int c = 0; c < 8; ++c) {
           const float p10 = af[1][c], p21 = af[2][c], p32 = af[3][c];
           const float p20 = p21 * p10, p31 = p32 * p21, p30 = p32 * p20;
-          v[0] = fmaf(kf[1][c] * kf[0][c], p10, v[0]);
-          v[1] = fmaf(kf[2][c] * kf[0][c], p20, v[1]);
-          v[2] = fmaf(kf[2][c] * kf[1][c], p21, v[2]);
-          v[3] = fmaf(kf[3][c] * kf[0][c], p30, v[3]);
-          v[4] = fmaf(kf[3][c] * kf[1][c], p31, v[4]);
-          v[5] = fmaf(kf[3][c] * kf[2][c], p32, v[5]);
+          v[0] = fmaf(ef[1][c] * kf[0][c], p10, v[0]);
+          v[1] = fmaf(ef[2][c] * kf[0][c], p20, v[1]);
+          v[2] = fmaf(ef[2][c] * kf[1][c], p21, v[2]);
+          v[3] = fmaf(ef[3][c] * kf[0][c], p30, v[3]);
+          v[4] = fmaf(ef[3][c] * kf[1][c], p31, v[4]);
+          v[5] = fmaf(ef[3][c] * kf[2][c], p32, v[5]);
           v[6] = fmaf(qf[0][c], kf[0][c], v[6]);
           v[7] = fmaf(qf[1][c] * kf[0][c], p10, v[7]);
           v[8] = fmaf(qf[1][c], kf[1][c], v[8]);
@@ -755,7 +798,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
     __syncthreads();
 
     // ---- levels 0 and 1 on the tensor cores
-    kda_level_operands(0, 1, sK, sQ, lam, op, tid);
+    kda_level_operands<G2>(0, 1, sK, sQ, lam, op, tid, gb, gstride, nvalid);
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -804,13 +847,13 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
     }
     if (tid < kDK) reinterpret_cast<float *>(ws + kVG)[tid] = __expf(lam[(kC - 1) * kLdL + tid]);
     if (!wait_ok(mbG, 0)) { failed = true; break; }
-    kda_level_extract(0, 1, tmem + kKColG1, sAst, sMst, be, warp, lane);
+    kda_level_extract<G2>(0, 1, tmem + kKColG1, sAst, sMst, be, warp, lane);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
 
     // ---- levels 2 and 3
-    kda_level_operands(2, 3, sK, sQ, lam, op, tid);
+    kda_level_operands<G2>(2, 3, sK, sQ, lam, op, tid, gb, gstride, nvalid);
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -824,12 +867,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
       const int i = 4 * blk + static_cast<int>((oi >> (4 * o)) & 15);
       const int j = 4 * blk + static_cast<int>((oj >> (4 * o)) & 15);
       if (o < 6)
-        sAst[i * kLdS + j] = be[i] * w4[tid];
+        sAst[i * kLdS + j] = G2 ? w4[tid] : be[i] * w4[tid];
       else
         sMst[i * kLdS + j] = w4[tid];
     }
     if (!wait_ok(mbG, 1)) { failed = true; break; }
-    kda_level_extract(2, 3, tmem + kKColG2, sAst, sMst, be, warp, lane);
+    kda_level_extract<G2>(2, 3, tmem + kKColG2, sAst, sMst, be, warp, lane);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -849,17 +892,41 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
     }
     __syncthreads();
     solve_unit_lower(sL, sTf, sZ, tid);
-    // T = L^-1 diag(beta) (lower triangle) and Kt = k (.) e^{lambda}, hi/lo operand tiles
+    // T = L^-1 diag(beta) (KDA) or L^-1 (GDN2), lower triangle, and Kt = k (.)
+    // e^{lambda} (KDA) or Et = b (.) k (.) e^{lambda} (GDN2), hi/lo operand tiles
     {
       const int i = tid >> 2, j0 = (tid & 3) * 16;
       float x[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         const int j = j0 + e;
-        x[e] = j <= i ? sTf[i * kLd + j] * be[j] : 0.f;
+        x[e] = j <= i ? (G2 ? sTf[i * kLd + j] : sTf[i * kLd + j] * be[j]) : 0.f;
       }
       store_split8(sTh, sTl, kmajor_off(i, j0, kC), x);
       store_split8(sTh, sTl, kmajor_off(i, j0 + 8, kC), x + 8);
+    }
+    if (G2) {
+      // Z = w (.) v, hi/lo K-major [64 t][128 d] into the solve buffers (free
+      // once T is written): the MN-major A operand of Ut^T = Z^T T^T
+      __syncthreads();
+      for (int id = tid; id < kC * 16; id += kThreads) {
+        const int t = ((id >> 7) << 3) | (id & 7), g = (id >> 3) & 15;
+        const uint4 raw = *reinterpret_cast<const uint4 *>(sV + kmajor_off(t, 8 * g, kDV));
+        const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
+        float wv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (t < nvalid) {
+          const float4 w0 = __ldg(reinterpret_cast<const float4 *>(gw + t * static_cast<long>(H) * kDV + 8 * g));
+          const float4 w1 = __ldg(reinterpret_cast<const float4 *>(gw + t * static_cast<long>(H) * kDV + 8 * g + 4));
+          wv[0] = w0.x; wv[1] = w0.y; wv[2] = w0.z; wv[3] = w0.w; wv[4] = w1.x; wv[5] = w1.y; wv[6] = w1.z; wv[7] = w1.w;
+        }
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          x[2 * e] = bf16_to_f32(static_cast<uint16_t>(rw[e] & 0xffff)) * wv[2 * e];
+          x[2 * e + 1] = bf16_to_f32(static_cast<uint16_t>(rw[e] >> 16)) * wv[2 * e + 1];
+        }
+        store_split8(op + kOL, op + kOL + 16384, kmajor_off(t, 8 * g, kDV), x);
+      }
     }
     for (int id = tid; id < kC * 16; id += kThreads) {
       const int t = ((id >> 7) << 3) | (id & 7), g = (id >> 3) & 15;
@@ -868,11 +935,21 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
       const float4 t1v = *reinterpret_cast<const float4 *>(lam + t * kLdL + 8 * g + 4);
       const float lt[8] = {t0v.x, t0v.y, t0v.z, t0v.w, t1v.x, t1v.y, t1v.z, t1v.w};
       const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
+      float bv[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
+      if (G2) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) bv[e] = 0.f;
+        if (t < nvalid) {
+          const float4 b0 = __ldg(reinterpret_cast<const float4 *>(gb + t * gstride + 8 * g));
+          const float4 b1 = __ldg(reinterpret_cast<const float4 *>(gb + t * gstride + 8 * g + 4));
+          bv[0] = b0.x; bv[1] = b0.y; bv[2] = b0.z; bv[3] = b0.w; bv[4] = b1.x; bv[5] = b1.y; bv[6] = b1.z; bv[7] = b1.w;
+        }
+      }
       float x[8];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        x[2 * e] = bf16_to_f32(static_cast<uint16_t>(rw[e] & 0xffff)) * __expf(lt[2 * e]);
-        x[2 * e + 1] = bf16_to_f32(static_cast<uint16_t>(rw[e] >> 16)) * __expf(lt[2 * e + 1]);
+        x[2 * e] = bf16_to_f32(static_cast<uint16_t>(rw[e] & 0xffff)) * bv[2 * e] * __expf(lt[2 * e]);
+        x[2 * e + 1] = bf16_to_f32(static_cast<uint16_t>(rw[e] >> 16)) * bv[2 * e + 1] * __expf(lt[2 * e + 1]);
       }
       store_split8(sKth, sKtl, kmajor_off(t, 8 * g, kDK), x);
     }
@@ -887,8 +964,14 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
         mma_bf16(tmem + kKColW, dKtmn_h + 256u * ks, dTh + 16u * ks, idMN, ks > 0);
         mma_bf16(tmem + kKColW, dKtmn_h + 256u * ks, dTl + 16u * ks, idMN, true);
         mma_bf16(tmem + kKColW, dKtmn_l + 256u * ks, dTh + 16u * ks, idMN, true);
-        mma_bf16(tmem + kKColU, dVmn + 256u * ks, dTh + 16u * ks, idMN, ks > 0);
-        mma_bf16(tmem + kKColU, dVmn + 256u * ks, dTl + 16u * ks, idMN, true);
+        if (G2) {
+          mma_bf16(tmem + kKColU, dZmn_h + 256u * ks, dTh + 16u * ks, idMN, ks > 0);
+          mma_bf16(tmem + kKColU, dZmn_h + 256u * ks, dTl + 16u * ks, idMN, true);
+          mma_bf16(tmem + kKColU, dZmn_l + 256u * ks, dTh + 16u * ks, idMN, true);
+        } else {
+          mma_bf16(tmem + kKColU, dVmn + 256u * ks, dTh + 16u * ks, idMN, ks > 0);
+          mma_bf16(tmem + kKColU, dVmn + 256u * ks, dTl + 16u * ks, idMN, true);
+        }
       }
       mma_commit(mbW);
     }
@@ -1318,16 +1401,18 @@ size_t kda_chunk_workspace_size(int B, int T, int H) {
   return (n + 255) & ~static_cast<size_t>(255);
 }
 
-// launched by gdn_scan for KDA (a decay per key channel) with d_k = d_v = 128
+// launched by gdn_scan for KDA (a decay per key channel) and by gdn2_scan for
+// GDN2 (b_erase, w_write non-null), both with d_k = d_v = 128
 int launch_kda_chunk(float *state, const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
-                     const float *beta, int B, int T, int H, float *y, void *workspace, int32_t *err,
-                     cudaStream_t st) {
+                     const float *beta, const float *b_erase, const float *w_write, int B, int T, int H, float *y,
+                     void *workspace, int32_t *err, cudaStream_t st) {
   const int nchunks = (T + kC - 1) / kC;
   const long units = static_cast<long>(B) * H * nchunks;
   unsigned char *ws = static_cast<unsigned char *>(workspace);
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const bool g2 = b_erase != nullptr;
 
   KdaPrepArgs pa;
   pa.q = q;
@@ -1335,18 +1420,27 @@ int launch_kda_chunk(float *state, const uint16_t *q, const uint16_t *k, const u
   pa.v = v;
   pa.alpha = alpha;
   pa.beta = beta;
+  pa.b_erase = b_erase;
+  pa.w_write = w_write;
   pa.ws = ws;
   pa.T = T;
   pa.H = H;
   pa.nchunks = nchunks;
   pa.units = units;
   pa.err = err;
-  if (cudaFuncSetAttribute(kda_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(kKdaSmem)) != cudaSuccess)
-    return check_launch("gdn_scan: set shared memory");
   const long pgrid = units < sms ? units : sms;
-  kda_prep_kernel<<<static_cast<unsigned>(pgrid), kThreads, kKdaSmem, st>>>(pa);
-  const int rc = check_launch("gdn_scan: KDA chunk preparation kernel");
+  if (g2) {
+    if (cudaFuncSetAttribute(kda_prep_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kKdaSmem)) != cudaSuccess)
+      return check_launch("gdn2_scan: set shared memory");
+    kda_prep_kernel<true><<<static_cast<unsigned>(pgrid), kThreads, kKdaSmem, st>>>(pa);
+  } else {
+    if (cudaFuncSetAttribute(kda_prep_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kKdaSmem)) != cudaSuccess)
+      return check_launch("gdn_scan: set shared memory");
+    kda_prep_kernel<false><<<static_cast<unsigned>(pgrid), kThreads, kKdaSmem, st>>>(pa);
+  }
+  const int rc = check_launch(g2 ? "gdn2_scan: chunk preparation kernel" : "gdn_scan: KDA chunk preparation kernel");
   if (rc != SDM_OK) return rc;
 
   ChainArgs ca;
@@ -1364,7 +1458,7 @@ int launch_kda_chunk(float *state, const uint16_t *q, const uint16_t *k, const u
                            static_cast<int>(chain_smem)) != cudaSuccess)
     return check_launch("gdn_scan: set shared memory");
   gdn_chain_kernel<true><<<static_cast<unsigned>(static_cast<long>(B) * H), kChainThreads, chain_smem, st>>>(ca);
-  return check_launch("gdn_scan: KDA chunk chain kernel");
+  return check_launch(g2 ? "gdn2_scan: chunk chain kernel" : "gdn_scan: KDA chunk chain kernel");
 }
 
 SDM_STICKY_ACCESSOR(sticky_gdn_chunk)

@@ -175,8 +175,8 @@ int launch_recurrent(GdnArgs &args, int B, cudaStream_t st, const char *what) {
 size_t gdn_chunk_workspace_size(int B, int T, int H);
 size_t kda_chunk_workspace_size(int B, int T, int H);
 int launch_kda_chunk(float *state, const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
-                     const float *beta, int B, int T, int H, float *y, void *workspace, int32_t *err,
-                     cudaStream_t st);
+                     const float *beta, const float *b_erase, const float *w_write, int B, int T, int H, float *y,
+                     void *workspace, int32_t *err, cudaStream_t st);
 int launch_gdn_chunk(float *state, const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
                      const float *beta, int B, int T, int H, float *y, void *workspace, int32_t *err,
                      cudaStream_t st);
@@ -223,7 +223,8 @@ extern "C" int gdn_scan(float *state, const uint16_t *q, const uint16_t *k, cons
     if (!workspace || workspace_bytes < need)
       return set_error(SDM_ERR_INVALID_ARG, "gdn_scan: workspace of %zu bytes needed", need);
     if (!aligned(workspace, 16)) return set_error(SDM_ERR_ALIGN, "gdn_scan: workspace must be 16-byte aligned");
-    if (per_channel) return launch_kda_chunk(state, q, k, v, alpha, beta, B, T, H, y, workspace, dev_err, st);
+    if (per_channel)
+      return launch_kda_chunk(state, q, k, v, alpha, beta, nullptr, nullptr, B, T, H, y, workspace, dev_err, st);
     return launch_gdn_chunk(state, q, k, v, alpha, beta, B, T, H, y, workspace, dev_err, st);
   }
   GdnArgs args{};
@@ -242,10 +243,14 @@ extern "C" int gdn_scan(float *state, const uint16_t *q, const uint16_t *k, cons
   return launch_recurrent(args, B, st, "gdn_scan");
 }
 
+extern "C" size_t gdn2_scan_workspace_size(int B, int T, int H, int dk, int dv) {
+  if (B <= 0 || T <= 0 || H <= 0 || !use_chunked(dk, dv, 1)) return 0;
+  return kda_chunk_workspace_size(B, T, H);
+}
+
 extern "C" int gdn2_scan(float *state, const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
                          const float *b_erase, const float *w_write, int B, int T, int H, int dk, int dv, float *y,
-                         int32_t *dev_err, void *stream) {
-  (void)dev_err;
+                         void *workspace, size_t workspace_bytes, int32_t *dev_err, void *stream) {
   if (!state || !q || !k || !v || !alpha || !b_erase || !w_write || !y)
     return set_error(SDM_ERR_INVALID_ARG, "gdn2_scan: null pointer");
   if (B < 0 || T < 0 || H < 0) return set_error(SDM_ERR_INVALID_ARG, "gdn2_scan: negative size");
@@ -255,6 +260,15 @@ extern "C" int gdn2_scan(float *state, const uint16_t *q, const uint16_t *k, con
       !aligned(alpha, 16) || !aligned(b_erase, 16) || !aligned(w_write, 16))
     return set_error(SDM_ERR_ALIGN, "gdn2_scan: every tensor needs 16-byte alignment");
   if (B == 0 || T == 0 || H == 0) return SDM_OK;
+  if (dev_err && !aligned(dev_err, 4)) return set_error(SDM_ERR_ALIGN, "gdn2_scan: dev_err must be 4-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (use_chunked(dk, dv, 1)) {
+    const size_t need = kda_chunk_workspace_size(B, T, H);
+    if (!workspace || workspace_bytes < need)
+      return set_error(SDM_ERR_INVALID_ARG, "gdn2_scan: workspace of %zu bytes needed", need);
+    if (!aligned(workspace, 16)) return set_error(SDM_ERR_ALIGN, "gdn2_scan: workspace must be 16-byte aligned");
+    return launch_kda_chunk(state, q, k, v, alpha, nullptr, b_erase, w_write, B, T, H, y, workspace, dev_err, st);
+  }
   GdnArgs args{};
   args.state = state;
   args.q = q;
@@ -270,5 +284,5 @@ extern "C" int gdn2_scan(float *state, const uint16_t *q, const uint16_t *k, con
   args.dv = dv;
   args.per_channel = 1;
   args.gdn2 = 1;
-  return launch_recurrent(args, B, static_cast<cudaStream_t>(stream), "gdn2_scan");
+  return launch_recurrent(args, B, st, "gdn2_scan");
 }

@@ -356,11 +356,11 @@ SDM_API int sdm_scan_backward(float *state, float *dstate, const void *v, int v_
                               int32_t *dev_err, void *stream);
 
 /*
- * Scratch bytes gdn_scan needs.  Dense GDN at dk = dv = 128 (the chunked
- * tensor-core path) needs one tile set per chunk of 64 tokens (operands of
- * the state-dependent products: 114,944 bytes) plus 4 bytes per chunk,
- * rounded up to 256: about 1.8 KB per token-head.  Every other shape, KDA, and
- * SDM_GDN_PATH=recurrent need none (0).
+ * Scratch bytes gdn_scan needs.  At dk = dv = 128 (the chunked tensor-core
+ * path) one tile set per chunk of 64 tokens (the operands of the
+ * state-dependent products): GDN 131,328 bytes plus 4, KDA 147,968 bytes,
+ * rounded up to 256 (about 2.1 / 2.3 KB per token-head).  Every other shape
+ * and SDM_GDN_PATH=recurrent need none (0).
  */
 SDM_API size_t gdn_scan_workspace_size(int B, int T, int H, int dk, int dv, int per_channel);
 
@@ -384,12 +384,15 @@ SDM_API size_t gdn_scan_workspace_size(int B, int T, int H, int dk, int dv, int 
  *           its contents on return are undefined.  Too small: SDM_ERR_INVALID_ARG.
  * dev_err : optional; SDM_DEVERR_TIMEOUT if a bounded wait of the tensor-core
  *           kernels gave up (outputs then invalid).
- * Kernels: dense GDN with dk = dv = 128 runs chunkwise (64 tokens) on the
+ * Kernels: GDN and KDA with dk = dv = 128 run chunkwise (64 tokens) on the
  *          tensor cores ([SDM] App. A.1-A.2, Eq. 7, dense case): a kernel
  *          parallel over all chunks prepares each chunk's state-independent
  *          operands in the workspace, then one CTA per (batch, head) runs the
- *          chunks in order with the state in tensor memory.  KDA and other
- *          widths run token by token in fp32.
+ *          chunks in order with the state in registers.  KDA's per-channel
+ *          decays sit inside the chunk's pair sums; each pair's decay is
+ *          formed as a product of two decay ratios of at most 1 about a
+ *          segment boundary, never with an inverse decay.  alpha must lie in
+ *          (0, 1].  Other widths run token by token in fp32.
  * Limits: dk in {16, 32, 64, 128}; dv % 32 == 0, dv <= 256.  state and y
  *         16-byte aligned; q, k, v 16-byte aligned (dk, dv multiples of 8).
  */
@@ -406,18 +409,27 @@ SDM_API int gdn_scan(float *state, const uint16_t *q, const uint16_t *k, const u
  *   y_t  = S^T q_t
  * b = w = beta 1 is KDA.
  *
+ * Chunk form (dk = dv = 128): the KDA chunk form of gdn_scan with the erase
+ * rows e_i in place of beta_i k_i (A_ij = sum_r e_ir k_jr e^{lambda_ir -
+ * lambda_jr}, W = (I + A)^-1 (e (.) e^{lambda})) and Ut = (I + A)^-1 z, on
+ * the same two tensor-core kernels; other widths run token by token.
+ *
  * state   : fp32 [B,H,dk,dv] in place.
  * q, k    : bf16 [B,T,H,dk];  v : bf16 [B,T,H,dv].
- * alpha   : fp32 [B,T,H,dk].  b_erase : fp32 [B,T,H,dk].  w_write : fp32 [B,T,H,dv].
+ * alpha   : fp32 [B,T,H,dk] in (0, 1].  b_erase : fp32 [B,T,H,dk].  w_write : fp32 [B,T,H,dv].
  * y       : fp32 [B,T,H,dv].
- * dev_err : unused (kept for a uniform call shape); may be NULL.
- * Kernel: token by token in fp32, one CTA per (batch, head, 32 value columns).
+ * workspace : device scratch of gdn2_scan_workspace_size() bytes, 16-byte
+ *           aligned (NULL allowed when that size is 0); contents undefined on
+ *           return.  Too small: SDM_ERR_INVALID_ARG.
+ * dev_err : optional; SDM_DEVERR_TIMEOUT if a bounded wait of the tensor-core
+ *           kernels gave up (outputs then invalid).
  * Limits: dk in {16, 32, 64, 128}; dv % 32 == 0, dv <= 256; every tensor
- *         16-byte aligned.  No workspace.
+ *         16-byte aligned.
  */
+SDM_API size_t gdn2_scan_workspace_size(int B, int T, int H, int dk, int dv);
 SDM_API int gdn2_scan(float *state, const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
                       const float *b_erase, const float *w_write, int B, int T, int H, int dk, int dv, float *y,
-                      int32_t *dev_err, void *stream);
+                      void *workspace, size_t workspace_bytes, int32_t *dev_err, void *stream);
 
 /*
  * Scratch bytes sse_scan needs for these sizes and write mode: one routing

@@ -225,6 +225,51 @@ def test_gdn2_full_size_sampled():
         assert_state_close(S[b:b + 1, h:h + 1], Sr, what=f"state[{b},{h}]")
 
 
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 200, 700])
+def test_gdn2_chunked_path_lengths(T, monkeypatch):
+    """GDN2 at d_k = d_v = 128 runs in chunk form on the tensor cores (the KDA
+    chunk form with erase rows e = b (.) k and Ut = (I + A)^-1 (w (.) v)):
+    lengths around chunk edges from a nonzero state."""
+    sdm = need_gpu()
+    monkeypatch.setenv("SDM_GDN_PATH", "chunk")
+    sh = synth.GDN_DENSE.with_(B=2, T=T, H=2)
+    inp = synth.gdn_inputs(sh, seed=70 + T)
+    S0 = synth.random_state((2, 2, 128, 128), seed=71, scale=0.3)
+    Sr, yr = oracle.gdn2_scan(S0, inp["q"], inp["k"], inp["v"], inp["alpha_kda"], inp["b_erase"], inp["w_write"])
+    S, y = _gdn2_gpu(sdm, S0, inp)
+    assert_y_close(y, yr)
+    assert_state_close(S, Sr)
+
+
+def test_gdn2_chunked_matches_token_recurrent(monkeypatch):
+    sdm = need_gpu()
+    sh = synth.GDN_DENSE.with_(B=1, T=300, H=3)
+    inp = synth.gdn_inputs(sh, seed=72)
+    S0 = synth.random_state((1, 3, 128, 128), seed=73, scale=0.3)
+    monkeypatch.setenv("SDM_GDN_PATH", "chunk")
+    Sc, yc = _gdn2_gpu(sdm, S0, inp)
+    monkeypatch.setenv("SDM_GDN_PATH", "recurrent")
+    Sr, yr = _gdn2_gpu(sdm, S0, inp)
+    assert_y_close(yc, yr.astype(np.float64))
+    assert_state_close(Sc, Sr.astype(np.float64))
+
+
+def test_gdn2_chunked_gates_equal_to_beta_match_kda(monkeypatch):
+    """b = w = beta 1 makes GDN2 KDA: the two chunked tensor-core paths agree
+    within tolerance (they differ in where beta enters the products)."""
+    sdm = need_gpu()
+    monkeypatch.setenv("SDM_GDN_PATH", "chunk")
+    sh = synth.GDN_DENSE.with_(B=1, T=200, H=2)
+    inp = dict(synth.gdn_inputs(sh, seed=74))
+    inp["b_erase"] = np.repeat(inp["beta"][..., None], 128, axis=-1).astype(np.float32)
+    inp["w_write"] = np.repeat(inp["beta"][..., None], 128, axis=-1).astype(np.float32)
+    S0 = synth.random_state((1, 2, 128, 128), seed=75, scale=0.3)
+    S2, y2 = _gdn2_gpu(sdm, S0, inp)
+    Sk, yk = _gdn_gpu(sdm, S0, inp, True)
+    assert_y_close(y2, yk.astype(np.float64))
+    assert_state_close(S2, Sk.astype(np.float64))
+
+
 def test_gdn2_gates_equal_to_beta_match_the_kda_kernel():
     """b = w = beta 1 on the GPU gives the KDA kernel's result (within fp32
     rounding of the differently ordered products)."""
