@@ -73,6 +73,25 @@ def shard_seed(rank: int) -> int:
     return rank
 
 
+def global_batch(B: int, world: int) -> int:
+    """Under N ranks the job is one global workload of B * N sequences per
+    head: rank r owns the batch elements rank_shard(r) and draws them with
+    seed shard_seed(r), so the global input is the per-rank draws
+    concatenated along the batch axis."""
+    return B * world
+
+
+def rank_shard(B: int, world: int, rank: int) -> slice:
+    """The batch elements of the global workload (global_batch(B, world)
+    sequences per head) that rank `rank` runs: a contiguous block of B.
+    Every (batch, head) sequence of the scan is independent, so the ranks
+    exchange nothing and their outputs, concatenated in rank order along the
+    batch axis, are the global workload's outputs."""
+    if not 0 <= rank < world:
+        raise ValueError("rank out of range")
+    return slice(rank * B, (rank + 1) * B)
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -734,6 +753,12 @@ def run_ours(args, rank, world, local_rank, sampler):
     tr = NCU_TRAFFIC.get((wl.name, wl.kind))
     traffic = tr["bytes"] if tr and tr["digest"] == _src_digest(kernel_file) else None
     tokens = wl.tokens * world
+    cfg = wl.config()
+    if world > 1:
+        sl = rank_shard(wl.shape.B, world, rank)
+        cfg["parallelism"] = (f"dp{world}: one global batch of {global_batch(wl.shape.B, world)} sequences per head, "
+                              f"rank r runs batch elements [r*{wl.shape.B}, (r+1)*{wl.shape.B}) drawn with seed r "
+                              f"(rank 0: {sl.start}..{sl.stop - 1}); no exchange on the data path")
     out = {
         "metric": metric_name(wl),
         "value": tokens / (ms_per_step * 1e-3),
@@ -747,7 +772,7 @@ def run_ours(args, rank, world, local_rank, sampler):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic (seeded generators; no dataset or weights)",
-        "config": wl.config(),
+        "config": cfg,
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": algo_unit,
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": "sdm_scan_train + sdm_scan_backward + 2 sdm_address_backward" if wl.train else

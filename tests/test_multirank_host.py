@@ -50,6 +50,61 @@ def test_two_gloo_ranks_take_max_time_and_distinct_shards():
     assert out[0][1] == [True, False]              # rank 1 drew a different batch
 
 
+def _split_worker(rank, world, port, out):
+    """Rank r runs the oracle on its own shard of the global tiny SDM workload
+    (its batch elements, drawn with its seed) and the shards are gathered."""
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import numpy as np
+    import bench
+    import oracle
+    import synth
+    sh = synth.SDM_TINY.with_(B=2, H=2, T=48)
+    inp = synth.sdm_inputs(sh, seed=bench.shard_seed(rank))
+    ref = oracle.sdm_forward(inp, sh.k, sh.W, sh.R)
+    ys = [torch.zeros(ref["y"].size, dtype=torch.float64) for _ in range(world)]
+    ms = [torch.zeros(ref["state"].size, dtype=torch.float64) for _ in range(world)]
+    dist.all_gather(ys, torch.from_numpy(np.ascontiguousarray(ref["y"]).ravel()))
+    dist.all_gather(ms, torch.from_numpy(np.ascontiguousarray(ref["state"]).ravel()))
+    if rank == 0:
+        out["y"] = np.concatenate([g.numpy().reshape(ref["y"].shape) for g in ys], axis=0)
+        out["state"] = np.concatenate([g.numpy().reshape(ref["state"].shape) for g in ms], axis=0)
+    dist.destroy_process_group()
+
+
+def test_bh_split_over_two_ranks_reassembles_the_single_process_result():
+    """The multi-GPU split: one global workload of 2 x 2 batch elements, rank r
+    taking rank_shard(r) (drawn with shard_seed(r)); the shards' oracle
+    outputs, concatenated in rank order, equal the single-process oracle on the
+    global input bit for bit (the sequences are independent: no exchange)."""
+    import numpy as np
+    import bench
+    import oracle
+    import synth
+    ctx = tmp.get_context("spawn")
+    mgr = ctx.Manager()
+    out = mgr.dict()
+    port = _free_port()
+    world = 2
+    procs = [ctx.Process(target=_split_worker, args=(r, world, port, out)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=180)
+        assert p.exitcode == 0
+    sh = synth.SDM_TINY.with_(B=2, H=2, T=48)
+    parts = [synth.sdm_inputs(sh, seed=bench.shard_seed(r)) for r in range(world)]
+    glob = {k: (np.concatenate([p[k] for p in parts], axis=0) if isinstance(parts[0][k], np.ndarray) else parts[0][k])
+            for k in parts[0]}
+    assert glob["s1w"].shape[0] == bench.global_batch(sh.B, world)
+    for r in range(world):
+        sl = bench.rank_shard(sh.B, world, r)
+        assert np.array_equal(glob["v"][sl], parts[r]["v"])
+    ref = oracle.sdm_forward(glob, sh.k, sh.W, sh.R)
+    assert np.array_equal(out["y"], ref["y"])
+    assert np.array_equal(out["state"], ref["state"])
+
+
 def test_single_rank_is_identity():
     import bench
     assert bench.max_over_ranks(3.5, 1) == 3.5
