@@ -5,9 +5,12 @@
 // warp-level top-k over (key descending, id ascending), where key is the
 // order-preserving uint32 image of an fp32 score: candidates sit in lane
 // registers, and per output rank one redux.sync max finds the best key, one
-// redux.sync min the lowest id holding it, and the owning lane pops it.
-// Stage 1 and 2 select the top-k of each score half (ids = positions), first
-// filtering by a provable lower bound of the k-th score; stage 3 forms the
+// redux.sync min the lowest id holding it, and the lane holding that id (ids
+// are unique) pops it.  Stage 1 and 2 select the top-k of each score half
+// (ids = positions), first filtering by a provable lower bound of the k-th
+// score (the k-th largest lane maximum, from a bitonic sort of the warp); the
+// two halves' selections run interleaved, so each redux chain hides the
+// other's latency.  Stage 3 forms the
 // fp32 sums s1[a] + s2[b] (ids = a*sqrtN + b) of only the candidates that can
 // reach the top-W (a staircase of the two sorted halves), checks that no sum
 // outside it ties the W-th, and selects the top-W; the weights are the
@@ -101,6 +104,119 @@ __device__ __forceinline__ void warp_topk2(uint32_t k0, int i0, uint32_t k1, int
   }
 }
 
+// Exact top-`count` (count <= 32) of up to 64 (key, id) pairs held two per
+// lane, where the ids of real entries are unique and at least `count` entries
+// are real.  Per output rank one redux.sync max finds the best key, one
+// redux.sync min the lowest id holding it, and the lane holding that id (ids
+// are unique) pops it; lane 0 records the rank in `rbuf` (32 entries of the
+// warp's own scratch).  On return lane r holds rank r (r < count).
+__device__ __forceinline__ void warp_topk2_fast(uint32_t k0, int i0, uint32_t k1, int i1, int count, uint2 *rbuf,
+                                                uint32_t &okey, int &oid) {
+  const int lane = threadIdx.x & 31;
+  if (k1 > k0 || (k1 == k0 && i1 < i0)) {
+    const uint32_t tk = k0; k0 = k1; k1 = tk;
+    const int ti = i0; i0 = i1; i1 = ti;
+  }
+#pragma unroll 4
+  for (int r = 0; r < count; ++r) {
+    const uint32_t m = __reduce_max_sync(kFull, k0);
+    const int wid = __reduce_min_sync(kFull, k0 == m ? i0 : INT_MAX);
+    const bool pop = i0 == wid;
+    k0 = pop ? k1 : k0;
+    i0 = pop ? i1 : i0;
+    k1 = pop ? 0u : k1;
+    i1 = pop ? INT_MAX : i1;
+    if (lane == 0) rbuf[r] = make_uint2(m, static_cast<unsigned>(wid));
+  }
+  __syncwarp();
+  const uint2 e = lane < count ? rbuf[lane] : make_uint2(0u, static_cast<unsigned>(INT_MAX));
+  __syncwarp();
+  okey = e.x;
+  oid = static_cast<int>(e.y);
+}
+
+// warp_topk2_fast on two independent candidate sets at once (the two score
+// halves of a row): their redux chains interleave, so each hides the other's
+// latency.  Results go through rbufA / rbufB (32 entries each).
+__device__ __forceinline__ void warp_topk2_fast_x2(uint2 ca0, uint2 ca1, uint2 cb0, uint2 cb1, int count,
+                                                   uint2 *rbufA, uint2 *rbufB, uint2 &outA, uint2 &outB) {
+  const int lane = threadIdx.x & 31;
+  uint32_t ka0 = ca0.x, ka1 = ca1.x, kb0 = cb0.x, kb1 = cb1.x;
+  int ia0 = static_cast<int>(ca0.y), ia1 = static_cast<int>(ca1.y);
+  int ib0 = static_cast<int>(cb0.y), ib1 = static_cast<int>(cb1.y);
+  if (ka1 > ka0 || (ka1 == ka0 && ia1 < ia0)) {
+    const uint32_t tk = ka0; ka0 = ka1; ka1 = tk;
+    const int ti = ia0; ia0 = ia1; ia1 = ti;
+  }
+  if (kb1 > kb0 || (kb1 == kb0 && ib1 < ib0)) {
+    const uint32_t tk = kb0; kb0 = kb1; kb1 = tk;
+    const int ti = ib0; ib0 = ib1; ib1 = ti;
+  }
+#pragma unroll 2
+  for (int r = 0; r < count; ++r) {
+    const uint32_t ma = __reduce_max_sync(kFull, ka0);
+    const uint32_t mb = __reduce_max_sync(kFull, kb0);
+    const int wa = __reduce_min_sync(kFull, ka0 == ma ? ia0 : INT_MAX);
+    const int wb = __reduce_min_sync(kFull, kb0 == mb ? ib0 : INT_MAX);
+    const bool pa = ia0 == wa, pb = ib0 == wb;
+    ka0 = pa ? ka1 : ka0;
+    ia0 = pa ? ia1 : ia0;
+    ka1 = pa ? 0u : ka1;
+    ia1 = pa ? INT_MAX : ia1;
+    kb0 = pb ? kb1 : kb0;
+    ib0 = pb ? ib1 : ib0;
+    kb1 = pb ? 0u : kb1;
+    ib1 = pb ? INT_MAX : ib1;
+    if (lane == 0) {
+      rbufA[r] = make_uint2(ma, static_cast<unsigned>(wa));
+      rbufB[r] = make_uint2(mb, static_cast<unsigned>(wb));
+    }
+  }
+  __syncwarp();
+  const uint2 pad = make_uint2(0u, static_cast<unsigned>(INT_MAX));
+  outA = lane < count ? rbufA[lane] : pad;
+  outB = lane < count ? rbufB[lane] : pad;
+  __syncwarp();
+}
+
+// Candidates of one score half for the fast path: the entries with key >= tau
+// compacted into cbuf in ballot order (count `cnt`, at most 64), read back two
+// per lane.
+template <int E>
+__device__ __forceinline__ void compact_half(const uint32_t (&key)[E], int n, uint32_t tau, uint2 *cbuf, int cnt,
+                                             uint2 &c0, uint2 &c1) {
+  const int lane = threadIdx.x & 31;
+  int basepos = 0;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const bool in = key[e] >= tau && lane + 32 * e < n;
+    const unsigned bal = __ballot_sync(kFull, in);
+    if (in) cbuf[basepos + __popc(bal & ((1u << lane) - 1))] = make_uint2(key[e], lane + 32 * e);
+    basepos += __popc(bal);
+  }
+  __syncwarp();
+  const uint2 pad = make_uint2(0u, static_cast<unsigned>(INT_MAX));
+  c0 = lane < cnt ? cbuf[lane] : pad;
+  c1 = lane + 32 < cnt ? cbuf[lane + 32] : pad;
+  __syncwarp();
+}
+
+// The k-th largest (k <= 32) of the 32 lanes' values: a bitonic sort of the
+// warp, descending, then lane k-1's value.
+__device__ __forceinline__ uint32_t warp_kth_largest(uint32_t v, int k) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int blk = 2; blk <= 32; blk <<= 1) {
+#pragma unroll
+    for (int j = blk >> 1; j > 0; j >>= 1) {
+      const uint32_t o = __shfl_xor_sync(kFull, v, j);
+      const bool desc = (lane & blk) == 0, lower = (lane & j) == 0;
+      v = (lower == desc) ? max(v, o) : min(v, o);
+    }
+  }
+  return __shfl_sync(kFull, v, k - 1);
+}
+
 // Top-k of one score half (positions 0..n-1, E values per lane at lane+32e).
 // Fast path: tau = the k-th largest of the 32 lane maxima is a lower bound of
 // the k-th largest score, so every top-k element has key >= tau; when at most
@@ -116,14 +232,8 @@ __device__ __forceinline__ void half_topk(const uint32_t (&key)[E], int n, int k
   int cnt = 0;
   uint32_t tau = 0;
   if (E > 2) {
-    // k-th largest lane maximum: remove the largest k-1 lane maxima
-    uint32_t v = lm;
-    for (int r = 0; r < k - 1; ++r) {
-      const uint32_t m = __reduce_max_sync(kFull, v);
-      const unsigned who = __ballot_sync(kFull, v == m);
-      if (lane == __ffs(who) - 1) v = 0;
-    }
-    tau = __reduce_max_sync(kFull, v);
+    // k-th largest lane maximum
+    tau = warp_kth_largest(lm, k);
 #pragma unroll
     for (int e = 0; e < E; ++e) cnt += __popc(__ballot_sync(kFull, key[e] >= tau && lane + 32 * e < n));
   }
@@ -140,11 +250,8 @@ __device__ __forceinline__ void half_topk(const uint32_t (&key)[E], int n, int k
     const uint2 c0 = lane < cnt ? cbuf[lane] : make_uint2(0u, static_cast<unsigned>(INT_MAX));
     const uint2 c1 = lane + 32 < cnt ? cbuf[lane + 32] : make_uint2(0u, static_cast<unsigned>(INT_MAX));
     __syncwarp();
-    uint32_t ok[2];
-    int oi[2];
-    warp_topk2(c0.x, static_cast<int>(c0.y), c1.x, static_cast<int>(c1.y), k, ok, oi);
-    okey = ok[0];
-    oid = oi[0];
+    // cnt >= k real candidates with unique positions
+    warp_topk2_fast(c0.x, static_cast<int>(c0.y), c1.x, static_cast<int>(c1.y), k, cbuf, okey, oid);
   } else if (E <= 2) {
     uint32_t k0 = key[0], k1 = E > 1 ? key[E - 1] : 0u;
     int i0 = lane < n ? lane : INT_MAX, i1 = (E > 1 && lane + 32 < n) ? lane + 32 : INT_MAX;
@@ -209,7 +316,7 @@ __global__ void __launch_bounds__(kAddrWarps * 32) address_kernel(const float *_
                                                                   int32_t *__restrict__ idx_out,
                                                                   float *__restrict__ w_out,
                                                                   int32_t *__restrict__ dev_err) {
-  __shared__ uint2 cbuf_all[kAddrWarps][64];
+  __shared__ uint2 cbuf_all[kAddrWarps][128];
   const int lane = threadIdx.x & 31;
   uint2 *cbuf = cbuf_all[threadIdx.x >> 5];
   // lane owns entries lane and lane + 32 of the staircase P
@@ -230,22 +337,57 @@ __global__ void __launch_bounds__(kAddrWarps * 32) address_kernel(const float *_
     float hv[2];
     int hid[2];
     bool bad = false;
+    uint32_t key1[E1], key2[E1];
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const float *src = (half == 0 ? s1 : s2) + row * sqrtN;
-      uint32_t key[E1];
+    for (int e = 0; e < E1; ++e) {
+      const int j = lane + 32 * e;
+      const float x1 = j < sqrtN ? s1[row * sqrtN + j] : 0.f;
+      const float x2 = j < sqrtN ? s2[row * sqrtN + j] : 0.f;
+      bad |= j < sqrtN && (!isfinite(x1) || !isfinite(x2));
+      key1[e] = j < sqrtN ? order_key(x1) : 0u;
+      key2[e] = j < sqrtN ? order_key(x2) : 0u;
+    }
+    bool both_fast = false;
+    if (E1 > 2) {
+      // both halves at once: tau of each (the k-th largest lane maximum, a
+      // lower bound of the k-th largest score), the candidates >= tau, and
+      // when both sets hold at most 64 the two exact selections interleaved
+      uint32_t lm1 = 0, lm2 = 0;
 #pragma unroll
       for (int e = 0; e < E1; ++e) {
-        const int j = lane + 32 * e;
-        const float x = j < sqrtN ? src[j] : 0.f;
-        bad |= j < sqrtN && !isfinite(x);
-        key[e] = j < sqrtN ? order_key(x) : 0u;
+        lm1 = max(lm1, key1[e]);
+        lm2 = max(lm2, key2[e]);
       }
-      uint32_t ok;
-      int oi;
-      half_topk<E1>(key, sqrtN, k, cbuf, ok, oi);
-      hv[half] = key_value(ok);
-      hid[half] = oi;
+      const uint32_t tau1 = warp_kth_largest(lm1, k), tau2 = warp_kth_largest(lm2, k);
+      int cnt1 = 0, cnt2 = 0;
+#pragma unroll
+      for (int e = 0; e < E1; ++e) {
+        const bool v = lane + 32 * e < sqrtN;
+        cnt1 += __popc(__ballot_sync(kFull, key1[e] >= tau1 && v));
+        cnt2 += __popc(__ballot_sync(kFull, key2[e] >= tau2 && v));
+      }
+      if (cnt1 <= 64 && cnt2 <= 64) {
+        uint2 a0, a1, b0, b1;
+        compact_half<E1>(key1, sqrtN, tau1, cbuf, cnt1, a0, a1);
+        compact_half<E1>(key2, sqrtN, tau2, cbuf + 64, cnt2, b0, b1);
+        uint2 oa, ob;
+        warp_topk2_fast_x2(a0, a1, b0, b1, k, cbuf, cbuf + 64, oa, ob);
+        hv[0] = key_value(oa.x);
+        hid[0] = static_cast<int>(oa.y);
+        hv[1] = key_value(ob.x);
+        hid[1] = static_cast<int>(ob.y);
+        both_fast = true;
+      }
+    }
+    if (!both_fast) {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t ok;
+        int oi;
+        half_topk<E1>(half == 0 ? key1 : key2, sqrtN, k, cbuf, ok, oi);
+        hv[half] = key_value(ok);
+        hid[half] = oi;
+      }
     }
     if (__any_sync(kFull, bad) && lane == 0 && dev_err) atomicOr(dev_err, SDM_DEVERR_NONFINITE);
 
@@ -266,7 +408,13 @@ __global__ void __launch_bounds__(kAddrWarps * 32) address_kernel(const float *_
         ck[o] = px[o] >= 0 ? order_key(__fadd_rn(av, bv)) : 0u;
         ci[o] = px[o] >= 0 ? ai * sqrtN + bi : INT_MAX;
       }
-      warp_topk2(ck[0], ci[0], ck[1], ci[1], W, ok, oi);
+      if (W <= 32) {  // the staircase holds at least W candidates with unique slot ids
+        warp_topk2_fast(ck[0], ci[0], ck[1], ci[1], W, cbuf, ok[0], oi[0]);
+        ok[1] = 0u;
+        oi[1] = INT_MAX;
+      } else {
+        warp_topk2(ck[0], ci[0], ck[1], ci[1], W, ok, oi);
+      }
       // exactness: the best sum outside P sits on one of its corners
       const uint32_t kw = __shfl_sync(kFull, (W - 1) < 32 ? ok[0] : ok[1], (W - 1) & 31);
       const float bcorner = __shfl_sync(kFull, hv[1], corner_y < k ? corner_y : 0);
