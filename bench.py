@@ -43,9 +43,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # hashes to the digest it was taken at; otherwise the line carries null.
 NCU_TRAFFIC = {
     # one full-size sparse scan launch: 8.01 GB read + 4.19 GB written
-    ("sdm_14b_layer", "sdm"): {"bytes": 12.20e9, "digest": "ce4a87fa8968"},
-    # both kernels of one full-size gdn_scan call: 746.4 MB read + 590.5 MB written
-    ("gdn", "gdn"): {"bytes": 1.337e9, "digest": "e2c62e1f689e"},
+    ("sdm_14b_layer", "sdm"): {"bytes": 12.20e9, "digest": "8821957384b6"},
+    # both kernels of one full-size gdn_scan call: 746.2 MB read + 592.5 MB written
+    ("gdn", "gdn"): {"bytes": 1.338e9, "digest": "6a9be503d782"},
     # the five kernels of one full-size sse_scan call on the chunked path: 1.073 GB read + 0.799 GB written
     ("sse", "sse"): {"bytes": 1.872e9, "digest": "4128ebe70bae"},
 }
