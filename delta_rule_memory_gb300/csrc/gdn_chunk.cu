@@ -464,22 +464,23 @@ constexpr uint32_t kKK = 0;                       // K tile bf16 [64][128] K-maj
 constexpr uint32_t kKQ = 16384;                   // Q tile                                 16 KB
 constexpr uint32_t kKV = 32768;                   // V tile                                 16 KB
 constexpr uint32_t kKLam = 49152;                 // lambda fp32 [64][kLdL]
-constexpr uint32_t kKAl = kKLam + kC * kLdL * 4;  // alpha fp32 [64][128]; then A, Mq staging [64][kLdS]
-constexpr uint32_t kKAlBytes = 2 * kC * kLdS * 4;
+constexpr uint32_t kKAl = kKLam + kC * kLdL * 4;  // alpha fp32 [64][128]; then L = I + A fp32 [64][kLd]
+                                                  // (the solve's input) and the Mq staging [64][kLdS]
+constexpr uint32_t kKAlBytes = kC * kLd * 4 + kC * kLdS * 4;
 constexpr uint32_t kKOp = kKAl + kKAlBytes;       // level operands: rows hi, lo [128][128], cols hi, lo [64][128]
 constexpr uint32_t kKOpBytes = 98304;
 constexpr uint32_t kKGate = kKOp + kKOpBytes;     // beta [64], block-of-4 sums [16][16]
 constexpr uint32_t kKBar = kKGate + (kC + 256) * 4;
 constexpr uint32_t kKdaSmem = kKBar + 64;
 // inside the operand region once the level products are done
-constexpr uint32_t kOL = 0;                       // L = I + A, fp32 [64][kLd]
+constexpr uint32_t kOL = 0;                       // GDN2's Z hi/lo (32 KB) once T is written
 constexpr uint32_t kOTf = kOL + kSolve;           // L^-1
 constexpr uint32_t kOZ = kOTf + kSolve;           // block products of the solve (768 floats)
 constexpr uint32_t kOT = kOZ + 4096;              // T hi, lo [64 i][64 j]
 constexpr uint32_t kOKt = kOT + 16384;            // Kt hi, lo [64][128]
 static_assert(kKAlBytes >= kC * kDK * 4, "alpha fits the staging region");
 static_assert(kOKt + 32768 <= kKOpBytes, "solve and Kt fit the operand region");
-static_assert(kOL + 32768 <= kOZ, "GDN2's Z hi/lo fits the solve buffers (L, L^-1) it replaces");
+static_assert(kOL + 32768 <= kOZ, "GDN2's Z hi/lo fits below the solve's block products");
 static_assert(kKdaSmem <= 227 * 1024, "one KDA preparation CTA per SM");
 constexpr uint32_t kKColG1 = 0, kKColG2 = 64, kKColW = 128, kKColU = 192, kKdaTmemCols = 256;
 
@@ -496,6 +497,7 @@ template <bool G2>
 __device__ __forceinline__ void kda_level_operands(int la, int lb, const unsigned char *sK, const unsigned char *sQ,
                                                    const float *lam, unsigned char *op, int tid, const float *gb,
                                                    long gstride, int nvalid) {
+#pragma unroll 2
   for (int id = tid; id < 2048; id += kThreads) {
     const bool is_row = id < 1024;
     const int idd = id & 1023;
@@ -552,8 +554,10 @@ __device__ __forceinline__ void kda_level_operands(int la, int lb, const unsigne
 // The pairs of the level pair (la, lb) kept from the product in tensor memory
 // (lanes = operand rows, columns = operand cols) into the A / Mq staging.
 // Warp w reads lanes 32*(w%4) (one row kind) and 16 of its level's 32 columns.
+// A entries (beta applied; none for GDN2) go straight into L = I + A (row
+// stride kLd), of which the solve reads only the strictly lower part.
 template <bool G2>
-__device__ __forceinline__ void kda_level_extract(int la, int lb, uint32_t tmem_col, float *sAst, float *sMst,
+__device__ __forceinline__ void kda_level_extract(int la, int lb, uint32_t tmem_col, float *sL, float *sMst,
                                                   const float *be, int warp, int lane) {
   const int sub = warp & 3, half = warp >> 2;
   const int lvl = sub < 2 ? la : lb;
@@ -571,7 +575,7 @@ __device__ __forceinline__ void kda_level_extract(int la, int lb, uint32_t tmem_
       if (sub & 1)
         sMst[ti * kLdS + tj] = x[e];
       else
-        sAst[ti * kLdS + tj] = G2 ? x[e] : be[ti] * x[e];
+        sL[ti * kLd + tj] = G2 ? x[e] : be[ti] * x[e];
     }
   }
 }
@@ -602,9 +606,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
   unsigned char *sK = sm + kKK, *sQ = sm + kKQ, *sV = sm + kKV;
   float *lam = reinterpret_cast<float *>(sm + kKLam);
   float *al = reinterpret_cast<float *>(sm + kKAl);
-  float *sAst = reinterpret_cast<float *>(sm + kKAl), *sMst = sAst + kC * kLdS;
+  float *sL = reinterpret_cast<float *>(sm + kKAl), *sMst = sL + kC * kLd;
   unsigned char *op = sm + kKOp;
-  float *sL = reinterpret_cast<float *>(op + kOL), *sTf = reinterpret_cast<float *>(op + kOTf);
+  float *sTf = reinterpret_cast<float *>(op + kOTf);
   float *sZ = reinterpret_cast<float *>(op + kOZ);
   unsigned char *sTh = op + kOT, *sTl = op + kOT + 8192, *sKth = op + kOKt, *sKtl = op + kOKt + 16384;
   float *be = reinterpret_cast<float *>(sm + kKGate);
@@ -653,6 +657,29 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
     const float *gb = G2 ? a.b_erase + (tok0 + static_cast<long>(t0) * H) * kDK : nullptr;
     const float *gw = G2 ? a.w_write + (tok0 + static_cast<long>(t0) * H) * kDV : nullptr;
 
+    // the next unit's input rows into L2 while this one is prepared
+    {
+      const long un = u + gridDim.x;
+      if (un < a.units) {
+        const long bhn = un / a.nchunks;
+        const int t0n = static_cast<int>(un - bhn * a.nchunks) * kC;
+        const long tokn = (bhn / H) * T * H + bhn % H;
+        // 64 rows: k, q, v (two 128-byte lines each) and alpha (four): ten lines a row
+        for (int id = tid; id < kC * 10; id += kThreads) {
+          const int r = id / 10, w = id - 10 * r;
+          if (t0n + r < T) {
+            const long row = tokn + static_cast<long>(t0n + r) * H;
+            const void *p = w < 6 ? static_cast<const void *>((w < 2 ? a.k : w < 4 ? a.q : a.v) + row * kDK + 64 * (w & 1))
+                                  : static_cast<const void *>(a.alpha + row * kDK + 32 * (w - 6));
+            prefetch_line_l2(p);
+            if (G2 && w >= 6) {
+              prefetch_line_l2(a.b_erase + row * kDK + 32 * (w - 6));
+              prefetch_line_l2(a.w_write + row * kDV + 32 * (w - 6));
+            }
+          }
+        }
+      }
+    }
     // ---- inputs: K, Q, V tiles, alpha rows, beta (padding: k = q = v = 0, alpha = 1, beta = 0)
     for (int id = tid; id < 3 * kC * 16; id += kThreads) {
       const int m = id >> 10, r = (id >> 4) & 63, k8 = id & 15;
@@ -682,23 +709,13 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
     cp_async_wait<0>();
     __syncthreads();
 
-    if (tid < kDK) {
-      // ---- lambda: running sum of log alpha over the chunk, one thread per channel
-      float acc = 0.f;
-#pragma unroll 8
-      for (int t = 0; t < kC; ++t) {
-        acc += __logf(al[t * kDK + tid]);
-        lam[t * kLdL + tid] = acc;
-      }
-    } else {
-      // ---- pairs inside each block of 4 tokens (and the diagonal of Mq) with
-      // running products of alpha: a thread sums 8 channels of one block, then
-      // the 16 threads of a block reduce-scatter their 16 partial sums
-      // (outputs 0-5: A at (1,0),(2,0),(2,1),(3,0),(3,1),(3,2); 6-15: Mq at
-      // (0,0),(1,0),(1,1),(2,0),(2,1),(2,2),(3,0),(3,1),(3,2),(3,3))
-#pragma unroll 1
-      for (int rep = 0; rep < 2; ++rep) {
-        const int item = tid - kDK + kDK * rep;
+    // ---- pairs inside each block of 4 tokens (and the diagonal of Mq) with
+    // running products of alpha: a thread sums 8 channels of one block, then
+    // the 16 threads of a block (a half warp) reduce-scatter their 16 partial
+    // sums (outputs 0-5: A at (1,0),(2,0),(2,1),(3,0),(3,1),(3,2); 6-15: Mq at
+    // (0,0),(1,0),(1,1),(2,0),(2,1),(2,2),(3,0),(3,1),(3,2),(3,3))
+    {
+        const int item = tid;
         const int blk = item >> 4, cg = item & 15;
         float kf[4][8], qf[4][8], af[4][8];
 #pragma unroll
@@ -793,6 +810,25 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
           v[0] = keep + __shfl_xor_sync(kFull, send, 1);
         }
         w4[item] = v[0];
+    }
+    // ---- lambda: running sum of log alpha over the chunk, two threads per
+    // channel (tokens 0-31 and 32-63), then the second half adds the first's total
+    {
+      const int r = tid & (kDK - 1), hf = tid >> 7;
+      float la[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) la[e] = al[(32 * hf + e) * kDK + r];
+      float acc = 0.f;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        acc += __logf(la[e]);
+        lam[(32 * hf + e) * kLdL + r] = acc;
+      }
+      __syncthreads();
+      if (hf) {
+        const float base = lam[31 * kLdL + r];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) lam[(32 + e) * kLdL + r] += base;
       }
     }
     __syncthreads();
@@ -847,7 +883,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
     }
     if (tid < kDK) reinterpret_cast<float *>(ws + kVG)[tid] = __expf(lam[(kC - 1) * kLdL + tid]);
     if (!wait_ok(mbG, 0)) { failed = true; break; }
-    kda_level_extract<G2>(0, 1, tmem + kKColG1, sAst, sMst, be, warp, lane);
+    kda_level_extract<G2>(0, 1, tmem + kKColG1, sL, sMst, be, warp, lane);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -867,24 +903,20 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
       const int i = 4 * blk + static_cast<int>((oi >> (4 * o)) & 15);
       const int j = 4 * blk + static_cast<int>((oj >> (4 * o)) & 15);
       if (o < 6)
-        sAst[i * kLdS + j] = G2 ? w4[tid] : be[i] * w4[tid];
+        sL[i * kLd + j] = G2 ? w4[tid] : be[i] * w4[tid];
       else
         sMst[i * kLdS + j] = w4[tid];
     }
     if (!wait_ok(mbG, 1)) { failed = true; break; }
-    kda_level_extract<G2>(2, 3, tmem + kKColG2, sAst, sMst, be, warp, lane);
+    kda_level_extract<G2>(2, 3, tmem + kKColG2, sL, sMst, be, warp, lane);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
 
-    // ---- L = I + A (strictly lower part) for the solve; Mq (lower, diagonal
-    // included) to the workspace
-    for (int id = tid; id < kC * kC; id += kThreads) {
-      const int i = id >> 6, j = id & 63;
-      sL[i * kLd + j] = j < i ? sAst[i * kLdS + j] : 0.f;
-    }
+    // ---- Mq (lower, diagonal included) to the workspace (8 consecutive
+    // threads take 8 consecutive rows: one contiguous 128-byte piece)
     for (int id = tid; id < kC * 8; id += kThreads) {
-      const int i = id >> 3, j0 = (id & 7) * 8;
+      const int i = ((id >> 6) << 3) | (id & 7), j0 = ((id >> 3) & 7) * 8;
       float x[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) x[e] = j0 + e <= i ? sMst[i * kLdS + j0 + e] : 0.f;
