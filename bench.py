@@ -749,7 +749,7 @@ def run_ours(args, rank, world, local_rank, sampler):
         peak = 152 * 128 * 2 * float(pk.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
         achieved = algo / (main_ms * 1e-3) / 1e12
     kernel_file = {"sdm": "sparse_scan.cu", "gdn": "gdn_chunk.cu", "kda": "gdn_chunk.cu", "gdn2": "gdn_chunk.cu",
-                   "sse": "sse_chunk.cu" if wl.sse_chunked else "sse_scan.cu"}[wl.kind]
+                   "sse": ("gdn_chunk.cu" if wl.sse_mode else "sse_chunk.cu") if wl.sse_chunked else "sse_scan.cu"}[wl.kind]
     tr = NCU_TRAFFIC.get((wl.name, wl.kind))
     traffic = tr["bytes"] if tr and tr["digest"] == _src_digest(kernel_file) else None
     tokens = wl.tokens * world
@@ -781,7 +781,9 @@ def run_ours(args, rank, world, local_rank, sampler):
                       "gdn": "gdn_scan (chunk preparation + chain kernels)",
                       "kda": "gdn_scan, per-channel decay (KDA chunk preparation + chain kernels)",
                       "gdn2": "gdn2_scan (GDN2 chunk preparation + chain kernels)",
-                      "sse": "sse_scan (route, group, chunk preparation, chain, combine kernels)"
+                      "sse": ("sse_scan, delta write (route, group, KDA-form chunk preparation, chain, combine "
+                              "kernels)" if wl.sse_mode else
+                              "sse_scan (route, group, chunk preparation, chain, combine kernels)")
                       if wl.sse_chunked else "sse_scan (route prepass + sse_scan_kernel)"}[wl.kind],
                      "launch_ms": main_ms, "peak_source": f"{src} ({'hbm_gbs' if bound == 'hbm' else 'FP32 lanes x clock'})",
                      **algo_info},

@@ -29,6 +29,7 @@
 #include <cstdlib>
 
 #include "common.cuh"
+#include "sse_group.cuh"
 #include "umma.cuh"
 
 namespace sdm {
@@ -447,10 +448,25 @@ constexpr uint32_t kVUnit = kVU + kC * kDV * 4;
 static_assert(kVUnit % 16 == 0 && kVMq % 16 == 0 && (kVG - kVMq) % 16 == 0 && (kVU - kVG) % 16 == 0,
               "bulk copies need 16-byte multiples");
 
+// the three instances of the per-channel-decay preparation
+constexpr int kModeKda = 0;   // KDA: k, q, v, alpha, beta per token
+constexpr int kModeGdn2 = 1;  // GDN2: erase rows e = b (.) k, T = (I + A)^-1, Ut = T (w (.) v)
+constexpr int kModeSse = 2;   // SSE delta write: the visits of one partition (keys kk = softmax of the
+                              // key logits, beta = the gate, reads scaled by the gate)
+// the SSE delta unit: the KDA unit with each visit's staging row after gamma_C
+constexpr uint32_t kSRows = kVG + 512;  // int32 [64], -1 for padding visits
+constexpr uint32_t kSU = kVU + 256;     // Ut
+constexpr uint32_t kSUnit = kVUnit + 256;
+
 struct KdaPrepArgs {
   const uint16_t *q, *k, *v;
   const float *alpha, *beta;
   const float *b_erase, *w_write;  // GDN2 only: erase gate [B,T,H,dk], write gate [B,T,H,dv]
+  // SSE delta only: key logits [B,T,H,c], routing records, group tables
+  const float *klog;
+  const uint32_t *rec, *grp;
+  int N, topk, rw, umax;
+  long gwords;
   unsigned char *ws;
   int T, H, nchunks;
   long units;  // B * H * nchunks
@@ -469,8 +485,9 @@ constexpr uint32_t kKAl = kKLam + kC * kLdL * 4;  // alpha fp32 [64][128]; then 
 constexpr uint32_t kKAlBytes = kC * kLd * 4 + kC * kLdS * 4;
 constexpr uint32_t kKOp = kKAl + kKAlBytes;       // level operands: rows hi, lo [128][128], cols hi, lo [64][128]
 constexpr uint32_t kKOpBytes = 98304;
-constexpr uint32_t kKGate = kKOp + kKOpBytes;     // beta [64], block-of-4 sums [16][16]
-constexpr uint32_t kKBar = kKGate + (kC + 256) * 4;
+constexpr uint32_t kKGate = kKOp + kKOpBytes;     // beta [64], block-of-4 sums [16][16]; SSE: visit
+                                                  // token-heads [64], staging rows [64], unit info [4]
+constexpr uint32_t kKBar = kKGate + (kC + 256 + 2 * kC + 4) * 4;
 constexpr uint32_t kKdaSmem = kKBar + 64;
 // inside the operand region once the level products are done
 constexpr uint32_t kOL = 0;                       // GDN2's Z hi/lo (32 KB) once T is written
@@ -484,6 +501,29 @@ static_assert(kOL + 32768 <= kOZ, "GDN2's Z hi/lo fits below the solve's block p
 static_assert(kKdaSmem <= 227 * 1024, "one KDA preparation CTA per SM");
 constexpr uint32_t kKColG1 = 0, kKColG2 = 64, kKColW = 128, kKColU = 192, kKdaTmemCols = 256;
 
+// 8 key channels c0..c0+7 of token t as fp32: the bf16 K tile, plus (SSE
+// delta: the keys are fp32 row weights kept as bf16 hi + lo) the lo tile
+template <int MODE>
+__device__ __forceinline__ void load_k8(const unsigned char *sK, const unsigned char *sKlo, int t, int c0,
+                                        float (&x)[8]) {
+  const uint4 hr = *reinterpret_cast<const uint4 *>(sK + kmajor_off(t, c0, kDK));
+  const uint32_t hw[4] = {hr.x, hr.y, hr.z, hr.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    x[2 * e] = bf16_to_f32(static_cast<uint16_t>(hw[e] & 0xffff));
+    x[2 * e + 1] = bf16_to_f32(static_cast<uint16_t>(hw[e] >> 16));
+  }
+  if (MODE == kModeSse) {
+    const uint4 lr = *reinterpret_cast<const uint4 *>(sKlo + kmajor_off(t, c0, kDK));
+    const uint32_t lw[4] = {lr.x, lr.y, lr.z, lr.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      x[2 * e] += bf16_to_f32(static_cast<uint16_t>(lw[e] & 0xffff));
+      x[2 * e + 1] += bf16_to_f32(static_cast<uint16_t>(lw[e] >> 16));
+    }
+  }
+}
+
 // Operands of the level pair (la, lb) into the operand region: rows
 // [k@la; q@la; k@lb; q@lb] of the right-half tokens (32 each) and cols
 // [k@la; k@lb] of the left-half tokens, hi/lo K-major.  A thread takes 8
@@ -493,10 +533,11 @@ constexpr uint32_t kKColG1 = 0, kKColG2 = 64, kKColW = 128, kKColU = 192, kKdaTm
 // stores are conflict-free.
 // GDN2: the k rows of A are e_t = b_t (.) k_t (the erase gate times the key),
 // read as gb[t * gstride + c] for the chunk's valid tokens t < nvalid.
-template <bool G2>
-__device__ __forceinline__ void kda_level_operands(int la, int lb, const unsigned char *sK, const unsigned char *sQ,
-                                                   const float *lam, unsigned char *op, int tid, const float *gb,
-                                                   long gstride, int nvalid) {
+template <int MODE>
+__device__ __forceinline__ void kda_level_operands(int la, int lb, const unsigned char *sK, const unsigned char *sKlo,
+                                                   const unsigned char *sQ, const float *lam, unsigned char *op,
+                                                   int tid, const float *gb, long gstride, int nvalid) {
+  constexpr bool G2 = MODE == kModeGdn2;
 #pragma unroll 2
   for (int id = tid; id < 2048; id += kThreads) {
     const bool is_row = id < 1024;
@@ -517,14 +558,10 @@ __device__ __forceinline__ void kda_level_operands(int la, int lb, const unsigne
     float f[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) f[e] = __expf(is_row ? dt[e] : -dt[e]);
-    const uint4 kr = *reinterpret_cast<const uint4 *>(sK + kmajor_off(t, 8 * g, kDK));
-    const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w};
     float x[8];
+    load_k8<MODE>(sK, sKlo, t, 8 * g, x);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      x[2 * e] = bf16_to_f32(static_cast<uint16_t>(kw[e] & 0xffff)) * f[2 * e];
-      x[2 * e + 1] = bf16_to_f32(static_cast<uint16_t>(kw[e] >> 16)) * f[2 * e + 1];
-    }
+    for (int e = 0; e < 8; ++e) x[e] *= f[e];
     if (G2 && is_row) {
       float bv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       if (t < nvalid) {
@@ -556,9 +593,10 @@ __device__ __forceinline__ void kda_level_operands(int la, int lb, const unsigne
 // Warp w reads lanes 32*(w%4) (one row kind) and 16 of its level's 32 columns.
 // A entries (beta applied; none for GDN2) go straight into L = I + A (row
 // stride kLd), of which the solve reads only the strictly lower part.
-template <bool G2>
+template <int MODE>
 __device__ __forceinline__ void kda_level_extract(int la, int lb, uint32_t tmem_col, float *sL, float *sMst,
                                                   const float *be, int warp, int lane) {
+  constexpr bool G2 = MODE == kModeGdn2;
   const int sub = warp & 3, half = warp >> 2;
   const int lvl = sub < 2 ? la : lb;
   const int sh = 5 - lvl, h = 1 << sh;
@@ -593,8 +631,9 @@ __device__ __forceinline__ void kda_issue_level_mma(uint32_t tmem_d, uint32_t op
   mma_commit(mbar);
 }
 
-template <bool G2>
+template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs a) {
+  constexpr bool G2 = MODE == kModeGdn2, SSE = MODE == kModeSse;
   extern __shared__ __align__(1024) unsigned char sm[];
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -603,7 +642,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
   const int lane_base = 32 * (warp & 3);
   const int T = a.T, H = a.H;
 
-  unsigned char *sK = sm + kKK, *sQ = sm + kKQ, *sV = sm + kKV;
+  // SSE: the V tile's slot holds the keys' lo tile, and V arrives late in the
+  // operand region (free once the level products are done)
+  unsigned char *sK = sm + kKK, *sQ = sm + kKQ, *sKlo = sm + kKV;
+  unsigned char *sV = SSE ? sm + kKOp : sm + kKV;
   float *lam = reinterpret_cast<float *>(sm + kKLam);
   float *al = reinterpret_cast<float *>(sm + kKAl);
   float *sL = reinterpret_cast<float *>(sm + kKAl), *sMst = sL + kC * kLd;
@@ -613,6 +655,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
   unsigned char *sTh = op + kOT, *sTl = op + kOT + 8192, *sKth = op + kOKt, *sKtl = op + kOKt + 16384;
   float *be = reinterpret_cast<float *>(sm + kKGate);
   float *w4 = be + kC;
+  int *rtok = reinterpret_cast<int *>(w4 + 256);    // SSE: token-head of each visit (-1: padding)
+  int *rrow = rtok + kC;                            // SSE: staging row of each visit
+  int *info = rrow + kC;                            // SSE: partition, first position, visits, list offset
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kKBar);
   uint32_t *holder = reinterpret_cast<uint32_t *>(sm + kKBar + 32);
   const uint32_t mbG = smem_addr(bars + 0), mbW = smem_addr(bars + 1), mbEnd = smem_addr(bars + 2);
@@ -645,12 +690,59 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
     return all;
   };
 
-  int it = 0;
-  for (long u = blockIdx.x; u < a.units; u += gridDim.x, ++it) {
-    unsigned char *ws = a.ws + u * kVUnit;
-    const long bh = u / a.nchunks;
-    const int t0 = static_cast<int>(u - bh * a.nchunks) * kC;
+  int it = 0;  // units done by this CTA (the parity of the W/U barrier)
+  for (long u = blockIdx.x; u < a.units; u += gridDim.x) {
+    unsigned char *ws = a.ws + u * (SSE ? kSUnit : kVUnit);
+    const long bh = SSE ? u / a.umax : u / a.nchunks;
+    const int t0 = SSE ? 0 : static_cast<int>(u - bh * a.nchunks) * kC;
     const long tok0 = (bh / H) * T * H + bh % H;
+    if (SSE) {
+      // the unit: a chunk of 64 visits of one partition of this (batch, head)
+      // (sse_group.cuh); units past the (batch, head)'s own count are skipped
+      const int uu = static_cast<int>(u - bh * a.umax);
+      const uint32_t *g = a.grp + bh * a.gwords;
+      const int N = a.N;
+      if (uu >= static_cast<int>(g[ssegrp::kGFirst + N])) continue;  // uniform over the CTA
+      if (warp == 0) {
+        const int nS = (T + kC - 1) / kC;
+        int p = N, pos0 = uu * kC, cnt = T, off = 0;
+        if (uu >= nS) {  // routed: the last partition whose first unit is <= uu
+          const bool c0 = lane < N && static_cast<int>(g[ssegrp::kGFirst + lane]) <= uu;
+          const bool c1 = lane + 32 < N && static_cast<int>(g[ssegrp::kGFirst + lane + 32]) <= uu;
+          p = __popc(__ballot_sync(kFull, c0)) + __popc(__ballot_sync(kFull, c1)) - 1;
+          pos0 = (uu - static_cast<int>(g[ssegrp::kGFirst + p])) * kC;
+          cnt = static_cast<int>(g[ssegrp::kGCnt + p]);
+          off = static_cast<int>(g[ssegrp::kGOff + p]);
+        }
+        if (lane == 0) {
+          info[0] = p;
+          info[1] = pos0;
+          info[2] = cnt;
+          info[3] = off;
+        }
+      }
+      __syncthreads();
+      if (tid < kC) {
+        const int p = info[0], pos = info[1] + tid, topk = a.topk;
+        int tl = -1, srow = -1;
+        float gate = 0.f;
+        if (pos < info[2]) {
+          int t = pos, r = topk;  // the shared partition: every token, slot topk, gate 1
+          if (p < N) {
+            const uint32_t e = g[ssegrp::kGHdr + info[3] + pos];
+            t = static_cast<int>(e >> 4);
+            r = static_cast<int>(e & 15u);
+          }
+          tl = static_cast<int>((bh / H * T + t) * H + bh % H);
+          gate = r < topk ? __uint_as_float(a.rec[static_cast<long>(tl) * a.rw + topk + r]) : 1.f;
+          srow = tl * (topk + 1) + r;
+        }
+        rtok[tid] = tl;
+        rrow[tid] = srow;
+        be[tid] = gate;  // the write strength of the delta rule
+      }
+      __syncthreads();
+    }
     // GDN2 gates of the chunk's tokens: row t at gb[t * gstride], valid for t < nvalid
     const long gstride = static_cast<long>(H) * kDK;
     const int nvalid = T - t0 < kC ? T - t0 : kC;
@@ -658,7 +750,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
     const float *gw = G2 ? a.w_write + (tok0 + static_cast<long>(t0) * H) * kDV : nullptr;
 
     // the next unit's input rows into L2 while this one is prepared
-    {
+    if (!SSE) {
       const long un = u + gridDim.x;
       if (un < a.units) {
         const long bhn = un / a.nchunks;
@@ -680,25 +772,47 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
         }
       }
     }
-    // ---- inputs: K, Q, V tiles, alpha rows, beta (padding: k = q = v = 0, alpha = 1, beta = 0)
-    for (int id = tid; id < 3 * kC * 16; id += kThreads) {
-      const int m = id >> 10, r = (id >> 4) & 63, k8 = id & 15;
-      const int t = t0 + r;
-      unsigned char *dst = sm + (m == 0 ? kKK : m == 1 ? kKQ : kKV) + kmajor_off(r, k8 * 8, kDK);
-      if (t < T)
-        cp_async<16>(dst, (m == 0 ? a.k : m == 1 ? a.q : a.v) + (tok0 + static_cast<long>(t) * H) * kDK + k8 * 8);
-      else
-        *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+    // ---- inputs: K, Q, V tiles, alpha rows, beta (padding: k = q = v = 0, alpha = 1, beta = 0).
+    // SSE: q rows and the key logits (into the lambda buffer) of the gathered
+    // visits; V comes later
+    if (SSE) {
+      for (int id = tid; id < kC * 16; id += kThreads) {
+        const int r = id >> 4, k8 = id & 15;
+        unsigned char *dst = sQ + kmajor_off(r, k8 * 8, kDK);
+        if (rtok[r] >= 0)
+          cp_async<16>(dst, a.q + static_cast<long>(rtok[r]) * kDK + k8 * 8);
+        else
+          *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+      }
+      for (int id = tid; id < kC * (kDK / 4); id += kThreads) {
+        const int r = id >> 5, c4 = id & 31;
+        if (rtok[r] >= 0)
+          cp_async<16>(lam + r * kLdL + 4 * c4, a.klog + static_cast<long>(rtok[r]) * kDK + 4 * c4);
+        else
+          *reinterpret_cast<float4 *>(lam + r * kLdL + 4 * c4) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    } else {
+      for (int id = tid; id < 3 * kC * 16; id += kThreads) {
+        const int m = id >> 10, r = (id >> 4) & 63, k8 = id & 15;
+        const int t = t0 + r;
+        unsigned char *dst = sm + (m == 0 ? kKK : m == 1 ? kKQ : kKV) + kmajor_off(r, k8 * 8, kDK);
+        if (t < T)
+          cp_async<16>(dst, (m == 0 ? a.k : m == 1 ? a.q : a.v) + (tok0 + static_cast<long>(t) * H) * kDK + k8 * 8);
+        else
+          *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+      }
     }
     for (int id = tid; id < kC * (kDK / 4); id += kThreads) {
       const int r = id >> 5, c4 = id & 31;
       const int t = t0 + r;
-      if (t < T)
-        cp_async<16>(al + r * kDK + 4 * c4, a.alpha + (tok0 + static_cast<long>(t) * H) * kDK + 4 * c4);
+      const bool valid = SSE ? rtok[r] >= 0 : t < T;
+      const long src = SSE ? static_cast<long>(rtok[r]) : tok0 + static_cast<long>(t) * H;
+      if (valid)
+        cp_async<16>(al + r * kDK + 4 * c4, a.alpha + src * kDK + 4 * c4);
       else
         *reinterpret_cast<float4 *>(al + r * kDK + 4 * c4) = make_float4(1.f, 1.f, 1.f, 1.f);
     }
-    if (tid < kC && !G2) {
+    if (tid < kC && !G2 && !SSE) {
       const int t = t0 + tid;
       if (t < T)
         cp_async<4>(be + tid, a.beta + tok0 + static_cast<long>(t) * H);
@@ -708,6 +822,45 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
     cp_async_commit();
     cp_async_wait<0>();
     __syncthreads();
+    if (SSE) {
+      // kk = softmax of each visit's key logits, in place (a warp takes 8 rows,
+      // a lane 4 channels); padding visits get kk = 0
+#pragma unroll 2
+      for (int e = 0; e < kC / 8; ++e) {
+        const int i = (kC / 8) * warp + e;
+        float4 *x = reinterpret_cast<float4 *>(lam + i * kLdL) + lane;
+        float4 v = *x;
+        if (rtok[i] >= 0) {  // warp-uniform
+          const bool bad = !(isfinite(v.x) && isfinite(v.y) && isfinite(v.z) && isfinite(v.w));
+          if (__any_sync(kFull, bad) && lane == 0 && a.err) atomicOr(a.err, SDM_DEVERR_NONFINITE);
+          float m = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+          v.x = __expf(v.x - m);
+          v.y = __expf(v.y - m);
+          v.z = __expf(v.z - m);
+          v.w = __expf(v.w - m);
+          float z = (v.x + v.y) + (v.z + v.w);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(kFull, z, o);
+          const float zi = 1.0f / z;
+          v = make_float4(v.x * zi, v.y * zi, v.z * zi, v.w * zi);
+        } else {
+          v = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        *x = v;
+      }
+      __syncthreads();
+      // kk as bf16 hi + lo K-major tiles (8 consecutive threads: 8 consecutive rows)
+      for (int id = tid; id < kC * 16; id += kThreads) {
+        const int t = ((id >> 7) << 3) | (id & 7), g = (id >> 3) & 15;
+        const float4 k0 = *reinterpret_cast<const float4 *>(lam + t * kLdL + 8 * g);
+        const float4 k1 = *reinterpret_cast<const float4 *>(lam + t * kLdL + 8 * g + 4);
+        const float x[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+        store_split8(sK, sKlo, kmajor_off(t, 8 * g, kDK), x);
+      }
+      __syncthreads();
+    }
 
     // ---- pairs inside each block of 4 tokens (and the diagonal of Mq) with
     // running products of alpha: a thread sums 8 channels of one block, then
@@ -721,13 +874,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int t = 4 * blk + i;
-          const uint4 kr = *reinterpret_cast<const uint4 *>(sK + kmajor_off(t, 8 * cg, kDK));
+          load_k8<MODE>(sK, sKlo, t, 8 * cg, kf[i]);
           const uint4 qr = *reinterpret_cast<const uint4 *>(sQ + kmajor_off(t, 8 * cg, kDK));
-          const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w}, qw[4] = {qr.x, qr.y, qr.z, qr.w};
+          const uint32_t qw[4] = {qr.x, qr.y, qr.z, qr.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            kf[i][2 * e] = bf16_to_f32(static_cast<uint16_t>(kw[e] & 0xffff));
-            kf[i][2 * e + 1] = bf16_to_f32(static_cast<uint16_t>(kw[e] >> 16));
             qf[i][2 * e] = bf16_to_f32(static_cast<uint16_t>(qw[e] & 0xffff));
             qf[i][2 * e + 1] = bf16_to_f32(static_cast<uint16_t>(qw[e] >> 16));
           }
@@ -834,7 +985,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
     __syncthreads();
 
     // ---- levels 0 and 1 on the tensor cores
-    kda_level_operands<G2>(0, 1, sK, sQ, lam, op, tid, gb, gstride, nvalid);
+    kda_level_operands<MODE>(0, 1, sK, sKlo, sQ, lam, op, tid, gb, gstride, nvalid);
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -852,8 +1003,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int c = 8 * (4 * m + j) + (lane >> 2);
-        const float x0 = bf16_to_f32(static_cast<uint16_t>(r[j] & 0xffff)) * __expf(lam[t0 * kLdL + c]);
-        const float x1 = bf16_to_f32(static_cast<uint16_t>(r[j] >> 16)) * __expf(lam[(t0 + 1) * kLdL + c]);
+        // (SSE: the read of the visit is scaled by its gate)
+        const float g0 = SSE ? be[t0] : 1.f, g1 = SSE ? be[t0 + 1] : 1.f;
+        const float x0 = g0 * bf16_to_f32(static_cast<uint16_t>(r[j] & 0xffff)) * __expf(lam[t0 * kLdL + c]);
+        const float x1 = g1 * bf16_to_f32(static_cast<uint16_t>(r[j] >> 16)) * __expf(lam[(t0 + 1) * kLdL + c]);
         const __nv_bfloat162 hb = __floats2bfloat162_rn(x0, x1);
         const float2 hf = __bfloat1622float2(hb);
         const __nv_bfloat162 lb = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
@@ -865,31 +1018,27 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
     for (int id = tid; id < kC * 16; id += kThreads) {
       // Khat = k (.) e^{lambda_C - lambda_t}, K-major
       const int t = ((id >> 7) << 3) | (id & 7), g = (id >> 3) & 15;
-      const uint4 raw = *reinterpret_cast<const uint4 *>(sK + kmajor_off(t, 8 * g, kDK));
       const float4 t0v = *reinterpret_cast<const float4 *>(lam + t * kLdL + 8 * g);
       const float4 t1v = *reinterpret_cast<const float4 *>(lam + t * kLdL + 8 * g + 4);
       const float4 e0v = *reinterpret_cast<const float4 *>(lam + (kC - 1) * kLdL + 8 * g);
       const float4 e1v = *reinterpret_cast<const float4 *>(lam + (kC - 1) * kLdL + 8 * g + 4);
       const float d[8] = {e0v.x - t0v.x, e0v.y - t0v.y, e0v.z - t0v.z, e0v.w - t0v.w,
                           e1v.x - t1v.x, e1v.y - t1v.y, e1v.z - t1v.z, e1v.w - t1v.w};
-      const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
       float x[8];
+      load_k8<MODE>(sK, sKlo, t, 8 * g, x);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        x[2 * e] = bf16_to_f32(static_cast<uint16_t>(rw[e] & 0xffff)) * __expf(d[2 * e]);
-        x[2 * e + 1] = bf16_to_f32(static_cast<uint16_t>(rw[e] >> 16)) * __expf(d[2 * e + 1]);
-      }
+      for (int e = 0; e < 8; ++e) x[e] *= __expf(d[e]);
       store_split8(ws + kVKh, ws + kVKh + 16384, kmajor_off(t, 8 * g, kDK), x);
     }
     if (tid < kDK) reinterpret_cast<float *>(ws + kVG)[tid] = __expf(lam[(kC - 1) * kLdL + tid]);
     if (!wait_ok(mbG, 0)) { failed = true; break; }
-    kda_level_extract<G2>(0, 1, tmem + kKColG1, sL, sMst, be, warp, lane);
+    kda_level_extract<MODE>(0, 1, tmem + kKColG1, sL, sMst, be, warp, lane);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
 
     // ---- levels 2 and 3
-    kda_level_operands<G2>(2, 3, sK, sQ, lam, op, tid, gb, gstride, nvalid);
+    kda_level_operands<MODE>(2, 3, sK, sKlo, sQ, lam, op, tid, gb, gstride, nvalid);
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -908,18 +1057,32 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
         sMst[i * kLdS + j] = w4[tid];
     }
     if (!wait_ok(mbG, 1)) { failed = true; break; }
-    kda_level_extract<G2>(2, 3, tmem + kKColG2, sL, sMst, be, warp, lane);
+    kda_level_extract<MODE>(2, 3, tmem + kKColG2, sL, sMst, be, warp, lane);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (SSE) {
+      // V rows of the visits into the operand region, free now: they land
+      // while the solve runs
+      for (int id = tid; id < kC * 16; id += kThreads) {
+        const int r = id >> 4, k8 = id & 15;
+        unsigned char *dst = sV + kmajor_off(r, k8 * 8, kDV);
+        if (rtok[r] >= 0)
+          cp_async<16>(dst, a.v + static_cast<long>(rtok[r]) * kDV + k8 * 8);
+        else
+          *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+      }
+      cp_async_commit();
+    }
 
     // ---- Mq (lower, diagonal included) to the workspace (8 consecutive
     // threads take 8 consecutive rows: one contiguous 128-byte piece)
     for (int id = tid; id < kC * 8; id += kThreads) {
       const int i = ((id >> 6) << 3) | (id & 7), j0 = ((id >> 3) & 7) * 8;
       float x[8];
+      const float gi = SSE ? be[i] : 1.f;  // SSE: the read of visit i is scaled by its gate
 #pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = j0 + e <= i ? sMst[i * kLdS + j0 + e] : 0.f;
+      for (int e = 0; e < 8; ++e) x[e] = j0 + e <= i ? gi * sMst[i * kLdS + j0 + e] : 0.f;
       store_split8(ws + kVMq, ws + kVMq + 8192, kmajor_off(i, j0, kC), x);
     }
     __syncthreads();
@@ -962,11 +1125,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
     }
     for (int id = tid; id < kC * 16; id += kThreads) {
       const int t = ((id >> 7) << 3) | (id & 7), g = (id >> 3) & 15;
-      const uint4 raw = *reinterpret_cast<const uint4 *>(sK + kmajor_off(t, 8 * g, kDK));
       const float4 t0v = *reinterpret_cast<const float4 *>(lam + t * kLdL + 8 * g);
       const float4 t1v = *reinterpret_cast<const float4 *>(lam + t * kLdL + 8 * g + 4);
       const float lt[8] = {t0v.x, t0v.y, t0v.z, t0v.w, t1v.x, t1v.y, t1v.z, t1v.w};
-      const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
+      float kx[8];
+      load_k8<MODE>(sK, sKlo, t, 8 * g, kx);
       float bv[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
       if (G2) {
 #pragma unroll
@@ -979,12 +1142,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
       }
       float x[8];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        x[2 * e] = bf16_to_f32(static_cast<uint16_t>(rw[e] & 0xffff)) * bv[2 * e] * __expf(lt[2 * e]);
-        x[2 * e + 1] = bf16_to_f32(static_cast<uint16_t>(rw[e] >> 16)) * bv[2 * e + 1] * __expf(lt[2 * e + 1]);
-      }
+      for (int e = 0; e < 8; ++e) x[e] = kx[e] * bv[e] * __expf(lt[e]);
       store_split8(sKth, sKtl, kmajor_off(t, 8 * g, kDK), x);
     }
+    if (SSE) cp_async_wait<0>();
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -1008,8 +1169,9 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
       mma_commit(mbW);
     }
     if (!wait_ok(mbW, static_cast<uint32_t>(it & 1))) { failed = true; break; }
+    if (SSE && tid < kC) reinterpret_cast<int *>(ws + kSRows)[tid] = rrow[tid];
     {
-      float *gU = reinterpret_cast<float *>(ws + kVU);
+      float *gU = reinterpret_cast<float *>(ws + (SSE ? kSU : kVU));
       for (int i0 = half * 32; i0 < half * 32 + 32; i0 += 16) {
         float x[16];
         tmem_ld16(tmem_addr(tmem, lane_base, kKColU + i0), x);
@@ -1026,6 +1188,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    ++it;
   }
   if (failed) {
     if (tid == 0) mma_commit(mbEnd);
@@ -1060,6 +1223,12 @@ struct ChainArgs {
   const float *gC;
   float *y;
   int T, H, nchunks;
+  // SSE delta only: the group tables, units per (batch, head), routed
+  // partitions, (batch, head) count, the visits' staging rows
+  const uint32_t *grp;
+  long gwords, bhn;
+  int umax, N;
+  float *stage;
   int drop_signal;  // test hook: the first X-done signal is never sent, so the workers' bounded wait runs out
   int32_t *err;
 };
@@ -1080,16 +1249,19 @@ constexpr uint32_t kCS = 0;               // S^T hi, lo [128 d][128 c]        2 
 constexpr uint32_t kCU = kCS + 65536;     // U^T hi, lo [128 d][64 j]         2 x 16 KB
 constexpr uint32_t kCW = kCU + 32768;     // W hi, lo, then Q (GDN) or Qt hi, lo (KDA): one bulk copy
 constexpr int kNBar = 12;
-template <bool KDA>
+// CM: 0 GDN, 1 KDA / GDN2, 2 SSE delta (the KDA layout plus each visit's
+// staging row after gamma_C)
+template <int CM>
 struct ChainLayout {
-  static constexpr uint32_t unit = KDA ? kVUnit : kUnit;
+  static constexpr bool KDA = CM >= 1;
+  static constexpr uint32_t unit = CM == 2 ? kSUnit : KDA ? kVUnit : kUnit;
   static constexpr uint32_t w_off = KDA ? kVW : kUW;                 // W, Q / Qt
   static constexpr uint32_t w_bytes = KDA ? kVMq - kVW : kWBytes;
   static constexpr uint32_t m_off = KDA ? kVMq : kUMq;               // Mq, Khat
   static constexpr uint32_t m_bytes = KDA ? kVG - kVMq : kMBytes;
   static constexpr uint32_t g_off = KDA ? kVG : kUG;                 // gamma_C per channel (KDA) / gamma_i (GDN)
-  static constexpr uint32_t g_bytes = KDA ? kVU - kVG : kGBytes;
-  static constexpr uint32_t u_off = KDA ? kVU : kUU;                 // Ut
+  static constexpr uint32_t g_bytes = CM == 2 ? kSU - kVG : KDA ? kVU - kVG : kGBytes;
+  static constexpr uint32_t u_off = CM == 2 ? kSU : KDA ? kVU : kUU;  // Ut
   static constexpr uint32_t cm = kCW + w_bytes;                      // Mq hi, lo, Khat hi, lo
   static constexpr uint32_t cg = cm + m_bytes;                       // gammas, two buffers
   static constexpr uint32_t cbar = cg + 2 * g_bytes;
@@ -1103,16 +1275,43 @@ __device__ __forceinline__ bool chain_wait(uint32_t mbar, uint32_t parity, volat
   return mbar_wait_hinted(mbar, parity, kHintedWaitLimit, abort_flag);
 }
 
-template <bool KDA>
+template <int CM>
 __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
-  using L = ChainLayout<KDA>;
+  using L = ChainLayout<CM>;
+  constexpr bool KDA = CM >= 1, SSE = CM == 2;
   extern __shared__ __align__(1024) unsigned char sm[];
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
-  const long bh = blockIdx.x;
-  const int T = a.T, H = a.H, n = a.nchunks;
-  const long tok0 = (bh / H) * T * H + bh % H;  // token t -> tok0 + t*H
-  const long u0 = bh * n;
+  const int T = a.T, H = a.H;
+  long bh = blockIdx.x, u0;
+  int n;
+  float *gS;
+  if (SSE) {
+    // one (batch, head, partition), the shared partitions first (the longest
+    // chains); its units are consecutive in the (batch, head)'s unit space
+    int p;
+    if (static_cast<long>(blockIdx.x) < a.bhn) {
+      p = a.N;
+    } else {
+      bh = (blockIdx.x - a.bhn) / a.N;
+      p = static_cast<int>((blockIdx.x - a.bhn) % a.N);
+    }
+    const uint32_t *g = a.grp + bh * a.gwords;
+    int first = 0, count = (T + kC - 1) / kC;
+    if (p < a.N) {
+      first = static_cast<int>(g[ssegrp::kGFirst + p]);
+      count = static_cast<int>(g[ssegrp::kGFirst + p + 1]) - first;
+    }
+    if (count == 0) return;  // a partition nobody visited keeps its state (the whole CTA leaves)
+    u0 = bh * a.umax + first;
+    n = count;
+    gS = a.state + (bh * (a.N + 1) + p) * static_cast<long>(kDK * kDV);
+  } else {
+    n = a.nchunks;
+    u0 = bh * n;
+    gS = a.state + bh * kDK * kDV;
+  }
+  const long tok0 = (bh / H) * T * H + bh % H;  // token t -> tok0 + t*H (GDN / KDA)
 
   unsigned char *sSh = sm + kCS, *sSl = sm + kCS + 32768;
   unsigned char *sUh = sm + kCU, *sUl = sm + kCU + 16384;
@@ -1144,7 +1343,6 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
     auto wwait = [&](uint32_t mb, uint32_t parity) -> bool {
       return __all_sync(kFull, chain_wait(mb, parity, abort_flag)) != 0;
     };
-    float *gS = a.state + bh * kDK * kDV;
     float S[32];  // S^T[row][32*qtr + j]
 #pragma unroll
     for (int j = 0; j < 32; ++j) S[j] = gS[static_cast<long>(32 * qtr + j) * kDV + row];
@@ -1213,8 +1411,9 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
       if (!wwait(bar(6), par)) break;
       {
         const float *gam = gbuf + 16 * qtr;
+        const int *srow = reinterpret_cast<const int *>(gbuf + kDK) + 16 * qtr;  // SSE: the visits' staging rows
         const int t0 = c * kC + 16 * qtr;
-        float *yp = a.y + (tok0 + static_cast<long>(t0) * H) * kDV + row;
+        float *yp = SSE ? nullptr : a.y + (tok0 + static_cast<long>(t0) * H) * kDV + row;
 #pragma unroll
         for (int h8 = 0; h8 < 16; h8 += 8) {
           float y1[8], y2[8];
@@ -1222,9 +1421,14 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
           tmem_ld8(lanes + kColY2 + 16 * qtr + h8, y2);
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            if (t0 + h8 + e < T)
+          for (int e = 0; e < 8; ++e) {
+            if (SSE) {
+              const int r = srow[h8 + e];
+              if (r >= 0) a.stage[static_cast<long>(r) * kDV + row] = y1[e] + y2[e];
+            } else if (t0 + h8 + e < T) {
               yp[static_cast<long>(h8 + e) * H * kDV] = KDA ? y1[e] + y2[e] : fmaf(gam[h8 + e], y1[e], y2[e]);
+            }
+          }
         }
       }
     }
@@ -1386,7 +1590,7 @@ int launch_gdn_chunk(float *state, const uint16_t *q, const uint16_t *k, const u
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
 
-  PrepArgs pa;
+  PrepArgs pa{};
   pa.q = q;
   pa.k = k;
   pa.v = v;
@@ -1408,7 +1612,7 @@ int launch_gdn_chunk(float *state, const uint16_t *q, const uint16_t *k, const u
   const int rc = check_launch("gdn_scan: chunk preparation kernel");
   if (rc != SDM_OK) return rc;
 
-  ChainArgs ca;
+  ChainArgs ca{};
   ca.state = state;
   ca.ws = ws;
   ca.gC = gC;
@@ -1418,11 +1622,11 @@ int launch_gdn_chunk(float *state, const uint16_t *q, const uint16_t *k, const u
   ca.nchunks = nchunks;
   ca.err = err;
   ca.drop_signal = test_drop_signal();
-  constexpr uint32_t chain_smem = ChainLayout<false>::smem;
-  if (cudaFuncSetAttribute(gdn_chain_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  constexpr uint32_t chain_smem = ChainLayout<0>::smem;
+  if (cudaFuncSetAttribute(gdn_chain_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(chain_smem)) != cudaSuccess)
     return check_launch("gdn_scan: set shared memory");
-  gdn_chain_kernel<false><<<static_cast<unsigned>(static_cast<long>(B) * H), kChainThreads, chain_smem, st>>>(ca);
+  gdn_chain_kernel<0><<<static_cast<unsigned>(static_cast<long>(B) * H), kChainThreads, chain_smem, st>>>(ca);
   return check_launch("gdn_scan: chunk chain kernel");
 }
 
@@ -1446,7 +1650,7 @@ int launch_kda_chunk(float *state, const uint16_t *q, const uint16_t *k, const u
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const bool g2 = b_erase != nullptr;
 
-  KdaPrepArgs pa;
+  KdaPrepArgs pa{};
   pa.q = q;
   pa.k = k;
   pa.v = v;
@@ -1462,20 +1666,20 @@ int launch_kda_chunk(float *state, const uint16_t *q, const uint16_t *k, const u
   pa.err = err;
   const long pgrid = units < sms ? units : sms;
   if (g2) {
-    if (cudaFuncSetAttribute(kda_prep_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(kda_prep_kernel<kModeGdn2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kKdaSmem)) != cudaSuccess)
       return check_launch("gdn2_scan: set shared memory");
-    kda_prep_kernel<true><<<static_cast<unsigned>(pgrid), kThreads, kKdaSmem, st>>>(pa);
+    kda_prep_kernel<kModeGdn2><<<static_cast<unsigned>(pgrid), kThreads, kKdaSmem, st>>>(pa);
   } else {
-    if (cudaFuncSetAttribute(kda_prep_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(kda_prep_kernel<kModeKda>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kKdaSmem)) != cudaSuccess)
       return check_launch("gdn_scan: set shared memory");
-    kda_prep_kernel<false><<<static_cast<unsigned>(pgrid), kThreads, kKdaSmem, st>>>(pa);
+    kda_prep_kernel<kModeKda><<<static_cast<unsigned>(pgrid), kThreads, kKdaSmem, st>>>(pa);
   }
   const int rc = check_launch(g2 ? "gdn2_scan: chunk preparation kernel" : "gdn_scan: KDA chunk preparation kernel");
   if (rc != SDM_OK) return rc;
 
-  ChainArgs ca;
+  ChainArgs ca{};
   ca.state = state;
   ca.ws = ws;
   ca.gC = nullptr;
@@ -1485,12 +1689,75 @@ int launch_kda_chunk(float *state, const uint16_t *q, const uint16_t *k, const u
   ca.nchunks = nchunks;
   ca.err = err;
   ca.drop_signal = test_drop_signal();
-  constexpr uint32_t chain_smem = ChainLayout<true>::smem;
-  if (cudaFuncSetAttribute(gdn_chain_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  constexpr uint32_t chain_smem = ChainLayout<1>::smem;
+  if (cudaFuncSetAttribute(gdn_chain_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(chain_smem)) != cudaSuccess)
     return check_launch("gdn_scan: set shared memory");
-  gdn_chain_kernel<true><<<static_cast<unsigned>(static_cast<long>(B) * H), kChainThreads, chain_smem, st>>>(ca);
+  gdn_chain_kernel<1><<<static_cast<unsigned>(static_cast<long>(B) * H), kChainThreads, chain_smem, st>>>(ca);
   return check_launch(g2 ? "gdn2_scan: chunk chain kernel" : "gdn_scan: KDA chunk chain kernel");
+}
+
+// bytes of one unit of the SSE delta prefill (sse_chunk.cu sizes the workspace)
+size_t sse_delta_unit_bytes() { return kSUnit; }
+
+// launched by sse_scan's chunked path for the delta write, after the routing
+// and group kernels: the chunk preparation of every unit (its visits gathered
+// from the group table), then one chain CTA per (batch, head, partition)
+// writing each visit's gated read to its staging row
+int launch_sse_delta_chunk(float *state, const uint32_t *rec, int rw, const uint32_t *grp, long gwords, int umax,
+                           const float *klog, const uint16_t *q, const uint16_t *v, const float *alpha, int B, int T,
+                           int H, int N, int topk, unsigned char *units, float *stage, int32_t *err, cudaStream_t st) {
+  const long bhn = static_cast<long>(B) * H;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+
+  KdaPrepArgs pa{};
+  pa.q = q;
+  pa.v = v;
+  pa.alpha = alpha;
+  pa.klog = klog;
+  pa.rec = rec;
+  pa.grp = grp;
+  pa.N = N;
+  pa.topk = topk;
+  pa.rw = rw;
+  pa.umax = umax;
+  pa.gwords = gwords;
+  pa.ws = units;
+  pa.T = T;
+  pa.H = H;
+  pa.nchunks = umax;
+  pa.units = bhn * umax;
+  pa.err = err;
+  if (cudaFuncSetAttribute(kda_prep_kernel<kModeSse>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kKdaSmem)) != cudaSuccess)
+    return check_launch("sse_scan: set shared memory");
+  const long pgrid = pa.units < sms ? pa.units : sms;
+  kda_prep_kernel<kModeSse><<<static_cast<unsigned>(pgrid), kThreads, kKdaSmem, st>>>(pa);
+  int rc = check_launch("sse_scan: delta chunk preparation kernel");
+  if (rc != SDM_OK) return rc;
+
+  ChainArgs ca{};
+  ca.state = state;
+  ca.ws = units;
+  ca.T = T;
+  ca.H = H;
+  ca.nchunks = umax;
+  ca.grp = grp;
+  ca.gwords = gwords;
+  ca.bhn = bhn;
+  ca.umax = umax;
+  ca.N = N;
+  ca.stage = stage;
+  ca.err = err;
+  ca.drop_signal = test_drop_signal();
+  constexpr uint32_t chain_smem = ChainLayout<2>::smem;
+  if (cudaFuncSetAttribute(gdn_chain_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(chain_smem)) != cudaSuccess)
+    return check_launch("sse_scan: set shared memory");
+  gdn_chain_kernel<2><<<static_cast<unsigned>(bhn * (N + 1)), kChainThreads, chain_smem, st>>>(ca);
+  return check_launch("sse_scan: delta chunk chain kernel");
 }
 
 SDM_STICKY_ACCESSOR(sticky_gdn_chunk)

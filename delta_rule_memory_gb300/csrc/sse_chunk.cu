@@ -39,6 +39,7 @@
 #include <climits>
 
 #include "common.cuh"
+#include "sse_group.cuh"
 #include "umma.cuh"
 
 namespace sdm {
@@ -49,8 +50,8 @@ using namespace umma;
 constexpr int kC = 64;      // visits per chunk
 constexpr int kCh = 128;    // c: rows of a partition (key width)
 constexpr int kD = 128;     // d: value width (the MMA M)
-constexpr int kMaxTopk = 8;
-constexpr int kMaxN = 64;
+constexpr int kMaxTopk = ssegrp::kMaxTopk;
+constexpr int kMaxN = ssegrp::kMaxN;
 constexpr uint32_t kWaitLimit = 1u << 20;  // polls (about 0.1 s) before an mbarrier wait gives up
 
 // ---- one unit in the workspace (bytes)
@@ -66,19 +67,13 @@ constexpr uint32_t kXYBytes = kXG - kXA;    // A, V, Kh (one bulk copy)
 constexpr uint32_t kXZBytes = kXUnit - kXG; // gamma and rows (one bulk copy, double-buffered)
 static_assert(kXUnit % 16 == 0 && kXYBytes % 16 == 0 && kXZBytes % 16 == 0, "bulk copies need 16-byte multiples");
 
-// ---- group table of one (batch, head), in 32-bit words
-constexpr int kGFirst = 0;   // first unit of routed partition p (p = 0..N-1); [N] = units in total
-constexpr int kGCnt = 72;    // visits of routed partition p
-constexpr int kGOff = 136;   // offset of p's visit list among the entries
-constexpr int kGHdr = 200;   // then the entries: (token << 4) | rank, partition by partition, time order
-
-__host__ __device__ inline int units_max(int T, int N, int topk) {
-  // shared: ceil(T/C); routed: sum_p ceil(n_p/C) <= floor((topk*T + (C-1)*N)/C)
-  return (T + kC - 1) / kC + static_cast<int>((static_cast<long>(topk) * T + static_cast<long>(kC - 1) * N) / kC);
-}
-__host__ __device__ inline long group_words(int T, int topk) {
-  return kGHdr + ((static_cast<long>(topk) * T + 3) & ~3L);
-}
+// ---- group table of one (batch, head): sse_group.cuh
+using ssegrp::group_words;
+using ssegrp::kGCnt;
+using ssegrp::kGFirst;
+using ssegrp::kGHdr;
+using ssegrp::kGOff;
+using ssegrp::units_max;
 
 // ===========================================================================
 // group: per (batch, head), the visits sorted by partition, time order kept.
@@ -831,40 +826,37 @@ inline size_t round256(size_t n) { return (n + 255) & ~static_cast<size_t>(255);
 
 }  // namespace
 
+size_t sse_delta_unit_bytes();  // gdn_chunk.cu
+int launch_sse_delta_chunk(float *state, const uint32_t *rec, int rw, const uint32_t *grp, long gwords, int umax,
+                           const float *klog, const uint16_t *q, const uint16_t *v, const float *alpha, int B, int T,
+                           int H, int N, int topk, unsigned char *units, float *stage, int32_t *err, cudaStream_t st);
+
 // Workspace bytes of the chunked path beyond the routing records: group
-// tables, the units, the staging rows.
-size_t sse_chunk_workspace_size(int B, int T, int H, int N, int topk) {
+// tables, the units (the additive write's or, for the delta write, the KDA
+// chunk form's), the staging rows.
+size_t sse_chunk_workspace_size(int B, int T, int H, int N, int topk, int write_mode) {
   const size_t bh = static_cast<size_t>(B) * H;
-  return round256(bh * group_words(T, topk) * 4) + bh * units_max(T, N, topk) * static_cast<size_t>(kXUnit) +
+  const size_t unit = write_mode == SSE_WRITE_DELTA ? sse_delta_unit_bytes() : static_cast<size_t>(kXUnit);
+  return round256(bh * group_words(T, topk) * 4) + round256(bh * units_max(T, N, topk) * unit) +
          round256(bh * T * static_cast<size_t>(topk + 1) * kD * 4);
 }
 
-// Shapes the chunked path takes: the additive write with c = d = 128.
+// Shapes the chunked path takes: c = d = 128, either write.
 bool sse_chunk_supported(int write_mode, int N, int topk, int c, int d) {
-  return write_mode == SSE_WRITE_ADDITIVE && c == kCh && d == kD && N <= kMaxN && topk <= kMaxTopk;
+  return (write_mode == SSE_WRITE_ADDITIVE || write_mode == SSE_WRITE_DELTA) && c == kCh && d == kD && N <= kMaxN &&
+         topk <= kMaxTopk;
 }
 
 int test_drop_signal();  // gdn_chunk.cu: the SDM_TEST_DROP_SIGNAL test hook
 
-// launched by sse_scan after the routing prepass (rec: the routing records;
-// chunk_ws: sse_chunk_workspace_size bytes, 256-byte aligned)
-int launch_sse_chunk(float *state, const uint32_t *rec, int rw, const float *klog, const uint16_t *q,
-                     const uint16_t *v, const float *alpha, int B, int T, int H, int N, int topk, float *y,
-                     unsigned char *chunk_ws, int32_t *err, cudaStream_t st) {
-  const long bhn = static_cast<long>(B) * H;
-  const long gwords = group_words(T, topk);
-  const int umax = units_max(T, N, topk);
-  uint32_t *grp = reinterpret_cast<uint32_t *>(chunk_ws);
-  unsigned char *units = chunk_ws + round256(static_cast<size_t>(bhn) * gwords * 4);
-  float *stage = reinterpret_cast<float *>(units + static_cast<size_t>(bhn) * umax * kXUnit);
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+namespace {
 
-  sse_group_kernel<<<static_cast<unsigned>(bhn), kGroupThreads, 0, st>>>(rec, T, H, N, topk, rw, grp, gwords);
-  int rc = check_launch("sse_scan: group kernel");
-  if (rc != SDM_OK) return rc;
-
+// the additive write's preparation and chain (the units and staging rows of
+// the chunked path)
+int launch_sse_additive_chunk(float *state, const uint32_t *rec, int rw, const uint32_t *grp, long gwords, int umax,
+                              const float *klog, const uint16_t *q, const uint16_t *v, const float *alpha, long bhn,
+                              int T, int H, int N, int topk, unsigned char *units, float *stage, int32_t *err,
+                              int sms, cudaStream_t st) {
   PrepArgs pa;
   pa.q = q;
   pa.v = v;
@@ -887,7 +879,7 @@ int launch_sse_chunk(float *state, const uint32_t *rec, int rw, const float *klo
     return check_launch("sse_scan: set shared memory");
   const long pmax = static_cast<long>(sms) * 2;
   sse_prep_kernel<<<static_cast<unsigned>(pa.total < pmax ? pa.total : pmax), kPThreads, kPrepSmem, st>>>(pa);
-  rc = check_launch("sse_scan: chunk preparation kernel");
+  const int rc = check_launch("sse_scan: chunk preparation kernel");
   if (rc != SDM_OK) return rc;
 
   ChainArgs ca;
@@ -906,7 +898,36 @@ int launch_sse_chunk(float *state, const uint32_t *rec, int rw, const float *klo
                            static_cast<int>(kChainSmem)) != cudaSuccess)
     return check_launch("sse_scan: set shared memory");
   sse_chain_kernel<<<static_cast<unsigned>(bhn * (N + 1)), kChainThreads, kChainSmem, st>>>(ca);
-  rc = check_launch("sse_scan: chunk chain kernel");
+  return check_launch("sse_scan: chunk chain kernel");
+}
+
+}  // namespace
+
+// launched by sse_scan after the routing prepass (rec: the routing records;
+// chunk_ws: sse_chunk_workspace_size bytes, 256-byte aligned)
+int launch_sse_chunk(float *state, const uint32_t *rec, int rw, const float *klog, const uint16_t *q,
+                     const uint16_t *v, const float *alpha, int write_mode, int B, int T, int H, int N, int topk,
+                     float *y, unsigned char *chunk_ws, int32_t *err, cudaStream_t st) {
+  const long bhn = static_cast<long>(B) * H;
+  const long gwords = group_words(T, topk);
+  const int umax = units_max(T, N, topk);
+  const size_t unit = write_mode == SSE_WRITE_DELTA ? sse_delta_unit_bytes() : static_cast<size_t>(kXUnit);
+  uint32_t *grp = reinterpret_cast<uint32_t *>(chunk_ws);
+  unsigned char *units = chunk_ws + round256(static_cast<size_t>(bhn) * gwords * 4);
+  float *stage = reinterpret_cast<float *>(units + round256(static_cast<size_t>(bhn) * umax * unit));
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+
+  sse_group_kernel<<<static_cast<unsigned>(bhn), kGroupThreads, 0, st>>>(rec, T, H, N, topk, rw, grp, gwords);
+  int rc = check_launch("sse_scan: group kernel");
+  if (rc != SDM_OK) return rc;
+  if (write_mode == SSE_WRITE_DELTA)
+    rc = launch_sse_delta_chunk(state, rec, rw, grp, gwords, umax, klog, q, v, alpha, B, T, H, N, topk, units, stage,
+                                err, st);
+  else
+    rc = launch_sse_additive_chunk(state, rec, rw, grp, gwords, umax, klog, q, v, alpha, bhn, T, H, N, topk, units,
+                                   stage, err, sms, st);
   if (rc != SDM_OK) return rc;
 
   const long n4 = bhn * T * (kD / 4);

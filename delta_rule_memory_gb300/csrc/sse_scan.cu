@@ -23,6 +23,7 @@
 #include <cstring>
 
 #include "common.cuh"
+#include "sse_group.cuh"
 
 namespace sdm {
 namespace {
@@ -32,7 +33,7 @@ constexpr int kSseThreads = 256;  // 16 columns x 16 row groups
 constexpr int kSseP = 4;          // tokens prefetched ahead
 constexpr int kSseMaxTopk = 8;
 
-__host__ __device__ inline int rec_words(int topk) { return (2 * topk + 2 + 3) & ~3; }
+using ssegrp::rec_words;
 
 // ---------------------------------------------------------------------------
 // Routing prepass.
@@ -386,16 +387,17 @@ size_t sse_smem_bytes(int N, int c, int topk, int mode) {
 using namespace sdm;
 
 namespace sdm {
-size_t sse_chunk_workspace_size(int B, int T, int H, int N, int topk);
+size_t sse_chunk_workspace_size(int B, int T, int H, int N, int topk, int write_mode);
 bool sse_chunk_supported(int write_mode, int N, int topk, int c, int d);
 int launch_sse_chunk(float *state, const uint32_t *rec, int rw, const float *klog, const uint16_t *q,
-                     const uint16_t *v, const float *alpha, int B, int T, int H, int N, int topk, float *y,
-                     unsigned char *chunk_ws, int32_t *err, cudaStream_t st);
+                     const uint16_t *v, const float *alpha, int write_mode, int B, int T, int H, int N, int topk,
+                     float *y, unsigned char *chunk_ws, int32_t *err, cudaStream_t st);
 }  // namespace sdm
 
-// The additive write with c = d = 128 runs as a chunked prefill by partition
-// (sse_chunk.cu) once T reaches one chunk; other shapes, the delta write and
-// short sequences run token by token.  SDM_SSE_PATH=recurrent forces the
+// Both writes with c = d = 128 run as a chunked prefill by partition once T
+// reaches one chunk (the additive write in sse_chunk.cu's GLA chunk form, the
+// delta write in the KDA chunk form of gdn_chunk.cu); other shapes and short
+// sequences run token by token.  SDM_SSE_PATH=recurrent forces the
 // token-by-token kernel, SDM_SSE_PATH=chunk the chunked path for any T.
 static bool use_sse_chunk(int write_mode, int T, int N, int topk, int c, int d) {
   if (!sse_chunk_supported(write_mode, N, topk, c, d)) return false;
@@ -413,7 +415,7 @@ static size_t rec_bytes(int B, int T, int H, int topk) {
 extern "C" size_t sse_scan_workspace_size(int B, int T, int H, int N, int topk, int c, int d, int write_mode) {
   if (B <= 0 || T <= 0 || H <= 0 || N <= 0 || topk <= 0) return 0;
   size_t n = rec_bytes(B, T, H, topk);
-  if (use_sse_chunk(write_mode, T, N, topk, c, d)) n += sse_chunk_workspace_size(B, T, H, N, topk);
+  if (use_sse_chunk(write_mode, T, N, topk, c, d)) n += sse_chunk_workspace_size(B, T, H, N, topk, write_mode);
   return n;
 }
 
@@ -466,7 +468,7 @@ extern "C" int sse_scan(float *state, const float *route_logits, int topk, const
   if (rc != SDM_OK) return rc;
 
   if (chunk)
-    return launch_sse_chunk(state, rec, rec_words(topk), k_logits, q, v, alpha, B, T, H, N, topk, y,
+    return launch_sse_chunk(state, rec, rec_words(topk), k_logits, q, v, alpha, write_mode, B, T, H, N, topk, y,
                             static_cast<unsigned char *>(workspace) + rec_bytes(B, T, H, topk), dev_err, st);
 
   SseArgs args;

@@ -52,17 +52,20 @@ def test_version_and_workspace(sdm):
 def test_sse_workspace_sizes(sdm, monkeypatch):
     """Routing records only on the token-by-token path; on the chunked
     prefill path also the group tables (200 header words + topk*T entries per
-    (batch, head)), ceil(T/64) + floor((topk*T + 63*N)/64) units of 99,072
-    bytes per (batch, head), and (topk+1) staging rows of d fp32 per token."""
+    (batch, head)), ceil(T/64) + floor((topk*T + 63*N)/64) units per (batch,
+    head) of 99,072 bytes (additive write) or 148,224 bytes (delta write), and
+    (topk+1) staging rows of d fp32 per token."""
     monkeypatch.delenv("SDM_SSE_PATH", raising=False)
     B, T, H, N, k = 4, 4096, 8, 8, 2
     rec = B * T * H * 8 * 4                       # 2k + 2 words, rounded up to 4
     assert sdm.sse_scan_workspace_size(B, T, H, N, k, 64, 128, 0) == rec
-    assert sdm.sse_scan_workspace_size(B, T, H, N, k, 128, 128, 1) == rec     # delta write: token by token
     r256 = lambda n: (n + 255) // 256 * 256
     units = (T + 63) // 64 + (k * T + 63 * N) // 64
-    chunk = r256(B * H * (200 + k * T) * 4) + B * H * units * 99072 + r256(B * T * H * (k + 1) * 128 * 4)
-    assert sdm.sse_scan_workspace_size(B, T, H, N, k, 128, 128, 0) == rec + chunk
+    chunk = lambda unit: (r256(B * H * (200 + k * T) * 4) + B * H * units * unit +
+                          r256(B * T * H * (k + 1) * 128 * 4))
+    assert sdm.sse_scan_workspace_size(B, T, H, N, k, 128, 128, 0) == rec + chunk(99072)
+    assert sdm.sse_scan_workspace_size(B, T, H, N, k, 128, 128, 1) == rec + chunk(148224)
+    assert sdm.sse_scan_workspace_size(B, T, H, N, k, 64, 128, 1) == rec     # c != 128: token by token
     assert sdm.sse_scan_workspace_size(1, 63, 1, N, k, 128, 128, 0) == r256(63 * 8 * 4)   # below one chunk
     monkeypatch.setenv("SDM_SSE_PATH", "chunk")
     assert sdm.sse_scan_workspace_size(1, 63, 1, N, k, 128, 128, 0) > r256(63 * 8 * 4)

@@ -27,12 +27,12 @@ def _gdn(sdm, S0, inp, per_channel=False):
     return host(state), host(y), int(host(err)[0])
 
 
-def _sse(sdm, S0, inp, topk):
+def _sse(sdm, S0, inp, topk, mode):
     import torch
     state = dev(S0)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     y = sdm.sse_scan(state, dev(inp["route"]), topk, dev(inp["klog"]), dev(inp["q"]), dev(inp["v"]),
-                     dev(inp["alpha"]), dev_err=err)
+                     dev(inp["alpha"]), dev_err=err, write_mode=mode)
     torch.cuda.synchronize()
     return host(state), host(y), int(host(err)[0])
 
@@ -56,19 +56,20 @@ def test_gdn_chain_wait_runs_out_and_the_context_stays_usable(per_channel, monke
     assert_state_close(S, Sr)
 
 
-def test_sse_chain_wait_runs_out_and_the_context_stays_usable(monkeypatch):
+@pytest.mark.parametrize("mode", [oracle.SSE_WRITE_ADDITIVE, oracle.SSE_WRITE_DELTA], ids=["additive", "delta"])
+def test_sse_chain_wait_runs_out_and_the_context_stays_usable(mode, monkeypatch):
     sdm = need_gpu()
     monkeypatch.setenv("SDM_SSE_PATH", "chunk")
     sh = synth.SSE_PART.with_(B=1, T=200, H=2)
     inp = synth.sse_inputs(sh, seed=92)
     S0 = synth.random_state((1, 2, sh.N + 1, 128, 128), seed=93, scale=0.5)
     monkeypatch.setenv("SDM_TEST_DROP_SIGNAL", "1")
-    _, _, err = _sse(sdm, S0, inp, sh.topk)
+    _, _, err = _sse(sdm, S0, inp, sh.topk, mode)
     assert err & SDM_DEVERR_TIMEOUT
     monkeypatch.delenv("SDM_TEST_DROP_SIGNAL")
-    S, y, err = _sse(sdm, S0, inp, sh.topk)
+    S, y, err = _sse(sdm, S0, inp, sh.topk, mode)
     assert err == 0
-    Sr, yr, _ = oracle.sse_scan(S0, inp["route"], sh.topk, inp["klog"], inp["q"], inp["v"], inp["alpha"])
+    Sr, yr, _ = oracle.sse_scan(S0, inp["route"], sh.topk, inp["klog"], inp["q"], inp["v"], inp["alpha"], mode)
     assert_y_close(y, yr)
     assert_state_close(S, Sr)
     assert np.all(np.isfinite(S))

@@ -2,8 +2,11 @@
 groups tokens while preserving causal order"; "One gate controls both writes
 and reads", Eqs. 9-14) through the C ABI, against the fp64 oracle.
 
-sse_scan takes this path for the additive write with c = d = 128 once T
-reaches one chunk of 64 visits; SDM_SSE_PATH=chunk forces it for any T and
+sse_scan takes this path for both writes with c = d = 128 once T reaches
+one chunk of 64 visits: the additive write (Eq. 11) through its own prep and
+chain kernels, the delta write (Eq. 12) through the per-channel-decay delta
+chunk form of the dense KDA scan, run per partition on its visit
+subsequence.  SDM_SSE_PATH=chunk forces the path for any T and
 SDM_SSE_PATH=recurrent forces the token-by-token kernel."""
 import numpy as np
 import pytest
@@ -14,24 +17,27 @@ from helpers import assert_state_close, assert_y_close, dev, host, need_gpu
 
 pytestmark = pytest.mark.gpu
 
+WRITES = pytest.mark.parametrize("mode", [oracle.SSE_WRITE_ADDITIVE, oracle.SSE_WRITE_DELTA],
+                                 ids=["additive", "delta"])
 
-def _run(sdm, S0, inp, topk, ws_extra=0):
+
+def _run(sdm, S0, inp, topk, ws_extra=0, mode=0):
     import torch
     B, T, H, N = inp["route"].shape
     state = dev(S0)
     sel = torch.zeros((B, T, H, topk), dtype=torch.int32, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     c, d = S0.shape[3], S0.shape[4]
-    ws = torch.empty(sdm.sse_scan_workspace_size(B, T, H, N, topk, c, d, 0) + ws_extra, dtype=torch.uint8,
+    ws = torch.empty(sdm.sse_scan_workspace_size(B, T, H, N, topk, c, d, mode) + ws_extra, dtype=torch.uint8,
                      device="cuda")
     y = sdm.sse_scan(state, dev(inp["route"]), topk, dev(inp["klog"]), dev(inp["q"]), dev(inp["v"]),
-                     dev(inp["alpha"]), sel_out=sel, workspace=ws, dev_err=err)
+                     dev(inp["alpha"]), sel_out=sel, workspace=ws, dev_err=err, write_mode=mode)
     return host(state), host(y), host(sel), int(host(err)[0])
 
 
-def _check(sdm, S0, inp, topk):
-    Sr, yr, selr = oracle.sse_scan(S0, inp["route"], topk, inp["klog"], inp["q"], inp["v"], inp["alpha"])
-    S, y, sel, err = _run(sdm, S0, inp, topk)
+def _check(sdm, S0, inp, topk, mode=0):
+    Sr, yr, selr = oracle.sse_scan(S0, inp["route"], topk, inp["klog"], inp["q"], inp["v"], inp["alpha"], mode)
+    S, y, sel, err = _run(sdm, S0, inp, topk, mode=mode)
     assert err == 0
     np.testing.assert_array_equal(sel, selr)
     assert_y_close(y, yr)
@@ -51,27 +57,30 @@ def _check(sdm, S0, inp, topk):
     (2, 300, 1, 16, 1),    # partitions with few visits (some with none)
     (1, 160, 1, 64, 8),    # the largest N and top-k
 ])
-def test_chunked_sse_matches_the_oracle(B, T, H, N, topk, monkeypatch):
+@WRITES
+def test_chunked_sse_matches_the_oracle(B, T, H, N, topk, mode, monkeypatch):
     monkeypatch.setenv("SDM_SSE_PATH", "chunk")
     sdm = need_gpu()
     sh = synth.SSE_PART.with_(B=B, T=T, H=H, N=N, topk=topk)
     inp = synth.sse_inputs(sh, seed=T + N)
     S0 = synth.random_state((B, H, N + 1, 128, 128), seed=N, scale=0.5)
-    _check(sdm, S0, inp, topk)
+    _check(sdm, S0, inp, topk, mode)
 
 
 @pytest.mark.parametrize("T", [1, 5, 63, 65])
-def test_chunked_sse_short_sequences(T, monkeypatch):
+@WRITES
+def test_chunked_sse_short_sequences(T, mode, monkeypatch):
     """One ragged chunk (or one full chunk and a one-visit tail)."""
     monkeypatch.setenv("SDM_SSE_PATH", "chunk")
     sdm = need_gpu()
     sh = synth.SSE_PART.with_(B=2, T=T, H=2)
     inp = synth.sse_inputs(sh, seed=3 * T)
     S0 = synth.random_state((2, 2, sh.N + 1, 128, 128), seed=T, scale=0.5)
-    _check(sdm, S0, inp, sh.topk)
+    _check(sdm, S0, inp, sh.topk, mode)
 
 
-def test_chunked_sse_strong_decay_stays_accurate(monkeypatch):
+@WRITES
+def test_chunked_sse_strong_decay_stays_accurate(mode, monkeypatch):
     """alpha down to 0.01: products over a whole chunk underflow, which a
     quotient form would turn into 0/0; the block-referenced factors keep every
     pair exact."""
@@ -82,19 +91,20 @@ def test_chunked_sse_strong_decay_stays_accurate(monkeypatch):
     rng = np.random.default_rng(5)
     inp["alpha"] = rng.uniform(0.01, 1.0, inp["alpha"].shape).astype(np.float32)
     S0 = synth.random_state((1, 2, sh.N + 1, 128, 128), seed=12, scale=0.5)
-    _check(sdm, S0, inp, sh.topk)
+    _check(sdm, S0, inp, sh.topk, mode)
 
 
-def test_chunked_and_recurrent_paths_agree_and_are_deterministic(monkeypatch):
+@WRITES
+def test_chunked_and_recurrent_paths_agree_and_are_deterministic(mode, monkeypatch):
     sdm = need_gpu()
     sh = synth.SSE_PART.with_(B=2, T=256, H=2)
     inp = synth.sse_inputs(sh, seed=21)
     S0 = synth.random_state((2, 2, sh.N + 1, 128, 128), seed=22, scale=0.5)
     monkeypatch.setenv("SDM_SSE_PATH", "chunk")
-    Sc, yc, selc, e1 = _run(sdm, S0, inp, sh.topk)
-    Sc2, yc2, _, e2 = _run(sdm, S0, inp, sh.topk)
+    Sc, yc, selc, e1 = _run(sdm, S0, inp, sh.topk, mode=mode)
+    Sc2, yc2, _, e2 = _run(sdm, S0, inp, sh.topk, mode=mode)
     monkeypatch.setenv("SDM_SSE_PATH", "recurrent")
-    Sr, yr, selr, e3 = _run(sdm, S0, inp, sh.topk)
+    Sr, yr, selr, e3 = _run(sdm, S0, inp, sh.topk, mode=mode)
     assert e1 == e2 == e3 == 0
     np.testing.assert_array_equal(selc, selr)
     np.testing.assert_array_equal(yc, yc2)      # fixed summation order: bit-reproducible
@@ -104,25 +114,27 @@ def test_chunked_and_recurrent_paths_agree_and_are_deterministic(monkeypatch):
 
 
 def test_chunked_sse_is_the_default_for_the_prefill_shape(monkeypatch):
-    """Without SDM_SSE_PATH, c = d = 128, additive and T >= 64 takes the
-    chunked path (its workspace holds the units), other shapes do not."""
+    """Without SDM_SSE_PATH, c = d = 128 and T >= 64 takes the chunked path
+    for either write (its workspace holds the units), other shapes do not."""
     monkeypatch.delenv("SDM_SSE_PATH", raising=False)
     sdm = need_gpu()
     rec_only = sdm.sse_scan_workspace_size(4, 4096, 8, 8, 2, 64, 128, 0)
     assert sdm.sse_scan_workspace_size(4, 4096, 8, 8, 2, 128, 128, 0) > rec_only + 4096 * 32 * 99072 // 64
-    assert sdm.sse_scan_workspace_size(4, 4096, 8, 8, 2, 128, 128, 1) == rec_only
+    assert sdm.sse_scan_workspace_size(4, 4096, 8, 8, 2, 128, 128, 1) > rec_only + 4096 * 32 * 148224 // 64
+    assert sdm.sse_scan_workspace_size(4, 4096, 8, 8, 2, 64, 128, 1) == rec_only
     assert sdm.sse_scan_workspace_size(4, 32, 8, 8, 2, 128, 128, 0) == sdm.sse_scan_workspace_size(
         4, 32, 8, 8, 2, 64, 128, 0)
 
 
-def test_chunked_sse_rejects_a_short_workspace(monkeypatch):
+@WRITES
+def test_chunked_sse_rejects_a_short_workspace(mode, monkeypatch):
     monkeypatch.setenv("SDM_SSE_PATH", "chunk")
     sdm = need_gpu()
     sh = synth.SSE_PART.with_(B=1, T=70, H=1)
     inp = synth.sse_inputs(sh, seed=2)
     S0 = np.zeros((1, 1, sh.N + 1, 128, 128), np.float32)
     with pytest.raises(RuntimeError):
-        _run(sdm, S0, inp, sh.topk, ws_extra=-256)
+        _run(sdm, S0, inp, sh.topk, ws_extra=-256, mode=mode)
 
 
 def test_chunked_sse_local_clock(golden, monkeypatch):
@@ -151,7 +163,8 @@ def test_chunked_sse_local_clock(golden, monkeypatch):
 
 
 @pytest.mark.parametrize("N,topk,path", [(12, 6, "chunk"), (16, 3, "chunk"), (40, 5, "chunk"), (12, 6, "recurrent")])
-def test_routing_ties_go_to_the_lower_partition(N, topk, path, monkeypatch):
+@WRITES
+def test_routing_ties_go_to_the_lower_partition(N, topk, path, mode, monkeypatch):
     """Router logits on a coarse integer grid, so most tokens have exact ties:
     the selected partitions must be the oracle's (lower partition first among
     equal logits) through the per-thread routing of the chunked path (N <= 16),
@@ -163,4 +176,4 @@ def test_routing_ties_go_to_the_lower_partition(N, topk, path, monkeypatch):
     rng = np.random.default_rng(N + topk)
     inp["route"] = rng.integers(-2, 3, inp["route"].shape).astype(np.float32)
     S0 = synth.random_state((1, 2, N + 1, 128, 128), seed=41, scale=0.5)
-    _check(sdm, S0, inp, topk)
+    _check(sdm, S0, inp, topk, mode)
