@@ -83,8 +83,8 @@ extern "C" {
  *       chunked tensor-core path (shape rules permitting).
  *   SDM_SSE_PATH=recurrent|chunk    sse_scan: force the token-by-token or the
  *       chunked prefill path (shape rules permitting).
- *   SDM_TEST_DROP_SIGNAL=1          test hook: the chunked GDN and SSE chain
- *       kernels skip one internal signal, so a bounded on-device wait runs out
+ *   SDM_TEST_DROP_SIGNAL=1          test hook: the chunked GDN, KDA, GDN2 and
+ *       SSE chain kernels skip one internal signal, so a bounded on-device wait runs out
  *       and the call reports SDM_DEVERR_TIMEOUT (its outputs are invalid; the
  *       CUDA context stays usable).  Never set in normal use.
  */
@@ -436,10 +436,11 @@ SDM_API int gdn2_scan(float *state, const uint16_t *q, const uint16_t *k, const 
  * record per token (selected partitions, their gates, and the max and
  * inverse normaliser of the row softmax), rounded up to 256 bytes; when the
  * call takes the chunked prefill path (below) also, per (batch, head), the
- * visit lists grouped by partition, one operand unit of 99,072 bytes per
- * chunk of 64 visits (at most ceil(T/64) + floor((topk*T + 63*N)/64) units),
- * and one staging row of d fp32 per visit.  Read SDM_SSE_PATH at the call,
- * so query it under the same environment as sse_scan.
+ * visit lists grouped by partition, one operand unit per chunk of 64 visits
+ * (at most ceil(T/64) + floor((topk*T + 63*N)/64) units; 99,072 bytes each
+ * for the additive write, 148,224 for the delta write), and one staging row
+ * of d fp32 per visit.  Read SDM_SSE_PATH at the call, so query it under the
+ * same environment as sse_scan.
  */
 SDM_API size_t sse_scan_workspace_size(int B, int T, int H, int N, int topk, int c, int d, int write_mode);
 
@@ -459,13 +460,16 @@ SDM_API size_t sse_scan_workspace_size(int B, int T, int H, int N, int topk, int
  *   unvisited partitions keep their bits (their decay clock stops)
  *   y_t  = sum_p g_p sum_j q_t[j] S^p[j,:]                 (after the write)
  *
- * Paths.  The additive write with c = d = 128 and T >= 64 runs as a prefill
- * by varlen grouping ([SSE] "Varlen groups tokens while preserving causal
+ * Paths.  Either write with c = d = 128 and T >= 64 runs as a prefill by
+ * varlen grouping ([SSE] "Varlen groups tokens while preserving causal
  * order"): the visits of each partition gathered in time order, each group
- * run in chunks of 64 visits on the tensor cores (chunkwise GLA form), and
- * every token's visit outputs summed in a fixed order (routed ranks, then the
- * shared partition), so results are deterministic.  Everything else runs
- * token by token with the partitions resident in shared memory.  The
+ * run in chunks of 64 visits on the tensor cores, and every token's visit
+ * outputs summed in a fixed order (routed ranks, then the shared partition),
+ * so results are deterministic.  The additive write takes the chunkwise GLA
+ * form; the delta write is the gated delta rule with a decay per key row, so
+ * it takes the chunk form of the per-channel-decay (KDA) scan with keys kk,
+ * write strength g and every read scaled by g.  Everything else runs token
+ * by token with the partitions resident in shared memory.  The
  * environment variable SDM_SSE_PATH=recurrent forces the token-by-token
  * kernel; SDM_SSE_PATH=chunk the chunked path for any T (same shape rules).
  *
