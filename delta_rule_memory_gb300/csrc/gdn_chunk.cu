@@ -104,7 +104,7 @@ static_assert(2 * (kPrepSmem + 1024) <= 228 * 1024, "two preparation CTAs per SM
 // one block distance at a time, X_IJ = -L_II^-1 sum_{K=J}^{I-1} L_IK X_KJ,
 // each thread computing a 1 x 4 strip with 16-byte loads.  Reads only the
 // strictly lower part of sA; writes the lower triangle (diagonal included) of
-// sTf; sZ holds 768 floats of block products.  Called by all kThreads threads
+// sTf; sZ holds 768 floats of block products.  Called by every thread of the CTA (at least 192)
 // (it synchronises the CTA).
 __device__ __forceinline__ void solve_unit_lower(const float *sA, float *sTf, float *sZ, int tid) {
   if (tid < 64) {
@@ -499,6 +499,7 @@ static_assert(kKAlBytes >= kC * kDK * 4, "alpha fits the staging region");
 static_assert(kOKt + 32768 <= kKOpBytes, "solve and Kt fit the operand region");
 static_assert(kOL + 32768 <= kOZ, "GDN2's Z hi/lo fits below the solve's block products");
 static_assert(kKdaSmem <= 227 * 1024, "one KDA preparation CTA per SM");
+constexpr int kKThreads = 512;  // 16 warps (at most 128 registers a thread)
 constexpr uint32_t kKColG1 = 0, kKColG2 = 64, kKColW = 128, kKColU = 192, kKdaTmemCols = 256;
 
 // 8 key channels c0..c0+7 of token t as fp32: the bf16 K tile, plus (SSE
@@ -539,7 +540,7 @@ __device__ __forceinline__ void kda_level_operands(int la, int lb, const unsigne
                                                    int tid, const float *gb, long gstride, int nvalid) {
   constexpr bool G2 = MODE == kModeGdn2;
 #pragma unroll 2
-  for (int id = tid; id < 2048; id += kThreads) {
+  for (int id = tid; id < 2048; id += kKThreads) {
     const bool is_row = id < 1024;
     const int idd = id & 1023;
     const int lsel = idd >> 9;                                         // 0: level la, 1: level lb
@@ -590,24 +591,24 @@ __device__ __forceinline__ void kda_level_operands(int la, int lb, const unsigne
 
 // The pairs of the level pair (la, lb) kept from the product in tensor memory
 // (lanes = operand rows, columns = operand cols) into the A / Mq staging.
-// Warp w reads lanes 32*(w%4) (one row kind) and 16 of its level's 32 columns.
+// Warp w reads lanes 32*(w%4) (one row kind) and 8 of its level's 32 columns.
 // A entries (beta applied; none for GDN2) go straight into L = I + A (row
 // stride kLd), of which the solve reads only the strictly lower part.
 template <int MODE>
 __device__ __forceinline__ void kda_level_extract(int la, int lb, uint32_t tmem_col, float *sL, float *sMst,
                                                   const float *be, int warp, int lane) {
   constexpr bool G2 = MODE == kModeGdn2;
-  const int sub = warp & 3, half = warp >> 2;
+  const int sub = warp & 3, qtr = warp >> 2;
   const int lvl = sub < 2 ? la : lb;
   const int sh = 5 - lvl, h = 1 << sh;
-  float x[16];
-  tmem_ld16(tmem_col + (static_cast<uint32_t>(32 * sub) << 16) + 32 * (sub >> 1) + 16 * half, x);
+  float x[8];
+  tmem_ld8(tmem_col + (static_cast<uint32_t>(32 * sub) << 16) + 32 * (sub >> 1) + 8 * qtr, x);
   tmem_ld_wait();
   const int u = lane, seg = u >> sh;
   const int ti = 2 * h * seg + h + (u & (h - 1));
 #pragma unroll
-  for (int e = 0; e < 16; ++e) {
-    const int v = 16 * half + e;
+  for (int e = 0; e < 8; ++e) {
+    const int v = 8 * qtr + e;
     if ((v >> sh) == seg) {
       const int tj = 2 * h * seg + (v & (h - 1));
       if (sub & 1)
@@ -632,13 +633,12 @@ __device__ __forceinline__ void kda_issue_level_mma(uint32_t tmem_d, uint32_t op
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs a) {
+__global__ void __launch_bounds__(kKThreads, 1) kda_prep_kernel(const KdaPrepArgs a) {
   constexpr bool G2 = MODE == kModeGdn2, SSE = MODE == kModeSse;
   extern __shared__ __align__(1024) unsigned char sm[];
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int row = tid & 127;
-  const int half = tid >> 7;
   const int lane_base = 32 * (warp & 3);
   const int T = a.T, H = a.H;
 
@@ -757,7 +757,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
         const int t0n = static_cast<int>(un - bhn * a.nchunks) * kC;
         const long tokn = (bhn / H) * T * H + bhn % H;
         // 64 rows: k, q, v (two 128-byte lines each) and alpha (four): ten lines a row
-        for (int id = tid; id < kC * 10; id += kThreads) {
+        for (int id = tid; id < kC * 10; id += kKThreads) {
           const int r = id / 10, w = id - 10 * r;
           if (t0n + r < T) {
             const long row = tokn + static_cast<long>(t0n + r) * H;
@@ -776,7 +776,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
     // SSE: q rows and the key logits (into the lambda buffer) of the gathered
     // visits; V comes later
     if (SSE) {
-      for (int id = tid; id < kC * 16; id += kThreads) {
+      for (int id = tid; id < kC * 16; id += kKThreads) {
         const int r = id >> 4, k8 = id & 15;
         unsigned char *dst = sQ + kmajor_off(r, k8 * 8, kDK);
         if (rtok[r] >= 0)
@@ -784,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
         else
           *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
       }
-      for (int id = tid; id < kC * (kDK / 4); id += kThreads) {
+      for (int id = tid; id < kC * (kDK / 4); id += kKThreads) {
         const int r = id >> 5, c4 = id & 31;
         if (rtok[r] >= 0)
           cp_async<16>(lam + r * kLdL + 4 * c4, a.klog + static_cast<long>(rtok[r]) * kDK + 4 * c4);
@@ -792,7 +792,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
           *reinterpret_cast<float4 *>(lam + r * kLdL + 4 * c4) = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     } else {
-      for (int id = tid; id < 3 * kC * 16; id += kThreads) {
+      for (int id = tid; id < 3 * kC * 16; id += kKThreads) {
         const int m = id >> 10, r = (id >> 4) & 63, k8 = id & 15;
         const int t = t0 + r;
         unsigned char *dst = sm + (m == 0 ? kKK : m == 1 ? kKQ : kKV) + kmajor_off(r, k8 * 8, kDK);
@@ -802,7 +802,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
           *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
       }
     }
-    for (int id = tid; id < kC * (kDK / 4); id += kThreads) {
+    for (int id = tid; id < kC * (kDK / 4); id += kKThreads) {
       const int r = id >> 5, c4 = id & 31;
       const int t = t0 + r;
       const bool valid = SSE ? rtok[r] >= 0 : t < T;
@@ -823,11 +823,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
     cp_async_wait<0>();
     __syncthreads();
     if (SSE) {
-      // kk = softmax of each visit's key logits, in place (a warp takes 8 rows,
+      // kk = softmax of each visit's key logits, in place (a warp takes 4 rows,
       // a lane 4 channels); padding visits get kk = 0
+      constexpr int kRowsPerWarp = kC / (kKThreads / 32);
 #pragma unroll 2
-      for (int e = 0; e < kC / 8; ++e) {
-        const int i = (kC / 8) * warp + e;
+      for (int e = 0; e < kRowsPerWarp; ++e) {
+        const int i = kRowsPerWarp * warp + e;
         float4 *x = reinterpret_cast<float4 *>(lam + i * kLdL) + lane;
         float4 v = *x;
         if (rtok[i] >= 0) {  // warp-uniform
@@ -852,7 +853,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
       }
       __syncthreads();
       // kk as bf16 hi + lo K-major tiles (8 consecutive threads: 8 consecutive rows)
-      for (int id = tid; id < kC * 16; id += kThreads) {
+      for (int id = tid; id < kC * 16; id += kKThreads) {
         const int t = ((id >> 7) << 3) | (id & 7), g = (id >> 3) & 15;
         const float4 k0 = *reinterpret_cast<const float4 *>(lam + t * kLdL + 8 * g);
         const float4 k1 = *reinterpret_cast<const float4 *>(lam + t * kLdL + 8 * g + 4);
@@ -862,55 +863,70 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
       __syncthreads();
     }
 
-    // ---- pairs inside each block of 4 tokens (and the diagonal of Mq) with
-    // running products of alpha: a thread sums 8 channels of one block, then
-    // the 16 threads of a block (a half warp) reduce-scatter their 16 partial
-    // sums (outputs 0-5: A at (1,0),(2,0),(2,1),(3,0),(3,1),(3,2); 6-15: Mq at
-    // (0,0),(1,0),(1,1),(2,0),(2,1),(2,2),(3,0),(3,1),(3,2),(3,3))
-    {
-        const int item = tid;
-        const int blk = item >> 4, cg = item & 15;
-        float kf[4][8], qf[4][8], af[4][8];
+    // ---- two groups of 8 warps at once:
+    // warps 0-7: pairs inside each block of 4 tokens (and the diagonal of Mq)
+    // with running products of alpha.  A thread sums 8 channels of one block
+    // (two halves of 4), then the 16 threads of the block reduce-scatter their
+    // 16 partial sums (outputs 0-5: A at (1,0),(2,0),(2,1),(3,0),(3,1),(3,2);
+    // 6-15: Mq at (0,0),(1,0),(1,1),(2,0),(2,1),(2,2),(3,0),(3,1),(3,2),(3,3)).
+    // The lanes of a warp alternate between its two blocks, so a quarter-warp's
+    // 16-byte row loads fall on two bank groups, not one.
+    // warps 8-15: lambda, the running sum of log alpha over the chunk, two
+    // threads per channel (tokens 0-31 and 32-63); the second half then adds
+    // the first's total.
+    if (tid < 256) {
+      const int blk = 2 * warp + (lane & 1), cg = lane >> 1;
+      uint4 kraw[4], klraw[4], qraw[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int t = 4 * blk + i;
+        kraw[i] = *reinterpret_cast<const uint4 *>(sK + kmajor_off(t, 8 * cg, kDK));
+        if (SSE) klraw[i] = *reinterpret_cast<const uint4 *>(sKlo + kmajor_off(t, 8 * cg, kDK));
+        qraw[i] = *reinterpret_cast<const uint4 *>(sQ + kmajor_off(t, 8 * cg, kDK));
+      }
+      float v[16];
+#pragma unroll
+      for (int o = 0; o < 16; ++o) v[o] = 0.f;
+#pragma unroll
+      for (int hc = 0; hc < 2; ++hc) {
+        // channels 8 cg + 4 hc .. + 3: words 2 hc, 2 hc + 1 of each raw row
+        float kf[4][4], qf[4][4], af[4][4], ef[4][4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int t = 4 * blk + i;
-          load_k8<MODE>(sK, sKlo, t, 8 * cg, kf[i]);
-          const uint4 qr = *reinterpret_cast<const uint4 *>(sQ + kmajor_off(t, 8 * cg, kDK));
-          const uint32_t qw[4] = {qr.x, qr.y, qr.z, qr.w};
+          const uint32_t kw[2] = {hc ? kraw[i].z : kraw[i].x, hc ? kraw[i].w : kraw[i].y};
+          const uint32_t qw[2] = {hc ? qraw[i].z : qraw[i].x, hc ? qraw[i].w : qraw[i].y};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
+          for (int e = 0; e < 2; ++e) {
+            kf[i][2 * e] = bf16_to_f32(static_cast<uint16_t>(kw[e] & 0xffff));
+            kf[i][2 * e + 1] = bf16_to_f32(static_cast<uint16_t>(kw[e] >> 16));
             qf[i][2 * e] = bf16_to_f32(static_cast<uint16_t>(qw[e] & 0xffff));
             qf[i][2 * e + 1] = bf16_to_f32(static_cast<uint16_t>(qw[e] >> 16));
           }
-          const float4 a0 = *reinterpret_cast<const float4 *>(al + t * kDK + 8 * cg);
-          const float4 a1 = *reinterpret_cast<const float4 *>(al + t * kDK + 8 * cg + 4);
-          af[i][0] = a0.x; af[i][1] = a0.y; af[i][2] = a0.z; af[i][3] = a0.w;
-          af[i][4] = a1.x; af[i][5] = a1.y; af[i][6] = a1.z; af[i][7] = a1.w;
-        }
-        // left factors of A: k (KDA, beta applied later) or e = b (.) k (GDN2)
-        float ef[4][8];
+          if (SSE) {
+            const uint32_t lw[2] = {hc ? klraw[i].z : klraw[i].x, hc ? klraw[i].w : klraw[i].y};
 #pragma unroll
-        for (int i = 1; i < 4; ++i) {
-          const int t = 4 * blk + i;
-          float bv[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
+            for (int e = 0; e < 2; ++e) {
+              kf[i][2 * e] += bf16_to_f32(static_cast<uint16_t>(lw[e] & 0xffff));
+              kf[i][2 * e + 1] += bf16_to_f32(static_cast<uint16_t>(lw[e] >> 16));
+            }
+          }
+          const float4 a4 = *reinterpret_cast<const float4 *>(al + t * kDK + 8 * cg + 4 * hc);
+          af[i][0] = a4.x; af[i][1] = a4.y; af[i][2] = a4.z; af[i][3] = a4.w;
+          // left factors of A: k (beta applied later) or e = b (.) k (GDN2)
+          float bv[4] = {1.f, 1.f, 1.f, 1.f};
           if (G2) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) bv[e] = 0.f;
+            bv[0] = bv[1] = bv[2] = bv[3] = 0.f;
             if (t < nvalid) {
-              const float4 b0 = __ldg(reinterpret_cast<const float4 *>(gb + t * gstride + 8 * cg));
-              const float4 b1 = __ldg(reinterpret_cast<const float4 *>(gb + t * gstride + 8 * cg + 4));
-              bv[0] = b0.x; bv[1] = b0.y; bv[2] = b0.z; bv[3] = b0.w;
-              bv[4] = b1.x; bv[5] = b1.y; bv[6] = b1.z; bv[7] = b1.w;
+              const float4 b4 = __ldg(reinterpret_cast<const float4 *>(gb + t * gstride + 8 * cg + 4 * hc));
+              bv[0] = b4.x; bv[1] = b4.y; bv[2] = b4.z; bv[3] = b4.w;
             }
           }
 #pragma unroll
-          for (int e = 0; e < 8; ++e) ef[i][e] = bv[e] * kf[i][e];
+          for (int e = 0; e < 4; ++e) ef[i][e] = bv[e] * kf[i][e];
         }
-        float v[16];
 #pragma unroll
-        for (int o = 0; o < 16; ++o) v[o] = 0.f;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < 4; ++c) {
           const float p10 = af[1][c], p21 = af[2][c], p32 = af[3][c];
           const float p20 = p21 * p10, p31 = p32 * p21, p30 = p32 * p20;
           v[0] = fmaf(ef[1][c] * kf[0][c], p10, v[0]);
@@ -930,42 +946,40 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
           v[14] = fmaf(qf[3][c] * kf[2][c], p32, v[14]);
           v[15] = fmaf(qf[3][c], kf[3][c], v[15]);
         }
-        // reduce-scatter over the 16 threads of the block (a half warp): the
-        // thread with index l within its block ends with output l
-        const int l = cg;
+      }
+      // reduce-scatter over the block's 16 threads (lanes of one parity): the
+      // thread with channel group l ends with output l
+      const int l = cg;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const bool up = l & 8;
-          const float send = up ? v[e] : v[e + 8];
-          const float keep = up ? v[e + 8] : v[e];
-          v[e] = keep + __shfl_xor_sync(kFull, send, 8);
-        }
+      for (int e = 0; e < 8; ++e) {
+        const bool up = l & 8;
+        const float send = up ? v[e] : v[e + 8];
+        const float keep = up ? v[e + 8] : v[e];
+        v[e] = keep + __shfl_xor_sync(kFull, send, 16);
+      }
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const bool up = l & 4;
-          const float send = up ? v[e] : v[e + 4];
-          const float keep = up ? v[e + 4] : v[e];
-          v[e] = keep + __shfl_xor_sync(kFull, send, 4);
-        }
+      for (int e = 0; e < 4; ++e) {
+        const bool up = l & 4;
+        const float send = up ? v[e] : v[e + 4];
+        const float keep = up ? v[e + 4] : v[e];
+        v[e] = keep + __shfl_xor_sync(kFull, send, 8);
+      }
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const bool up = l & 2;
-          const float send = up ? v[e] : v[e + 2];
-          const float keep = up ? v[e + 2] : v[e];
-          v[e] = keep + __shfl_xor_sync(kFull, send, 2);
-        }
-        {
-          const bool up = l & 1;
-          const float send = up ? v[0] : v[1];
-          const float keep = up ? v[1] : v[0];
-          v[0] = keep + __shfl_xor_sync(kFull, send, 1);
-        }
-        w4[item] = v[0];
-    }
-    // ---- lambda: running sum of log alpha over the chunk, two threads per
-    // channel (tokens 0-31 and 32-63), then the second half adds the first's total
-    {
-      const int r = tid & (kDK - 1), hf = tid >> 7;
+      for (int e = 0; e < 2; ++e) {
+        const bool up = l & 2;
+        const float send = up ? v[e] : v[e + 2];
+        const float keep = up ? v[e + 2] : v[e];
+        v[e] = keep + __shfl_xor_sync(kFull, send, 4);
+      }
+      {
+        const bool up = l & 1;
+        const float send = up ? v[0] : v[1];
+        const float keep = up ? v[1] : v[0];
+        v[0] = keep + __shfl_xor_sync(kFull, send, 2);
+      }
+      w4[16 * blk + l] = v[0];
+    } else {
+      const int r = tid & (kDK - 1), hf = (tid >> 7) & 1;
       float la[32];
 #pragma unroll
       for (int e = 0; e < 32; ++e) la[e] = al[(32 * hf + e) * kDK + r];
@@ -975,12 +989,13 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
         acc += __logf(la[e]);
         lam[(32 * hf + e) * kLdL + r] = acc;
       }
-      __syncthreads();
-      if (hf) {
-        const float base = lam[31 * kLdL + r];
+    }
+    __syncthreads();
+    if (tid >= 384) {
+      const int r = tid & (kDK - 1);
+      const float base = lam[31 * kLdL + r];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) lam[(32 + e) * kLdL + r] += base;
-      }
+      for (int e = 0; e < 32; ++e) lam[(32 + e) * kLdL + r] += base;
     }
     __syncthreads();
 
@@ -995,7 +1010,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
     // gamma_C to the workspace
     // (q transposed by ldmatrix, four 8x8 core matrices per warp and step:
     // lane t holds tokens 2(t%4), 2(t%4)+1 of key 8(4m+j) + t/4)
-    for (int o = warp; o < 32; o += kThreads / 32) {
+    for (int o = warp; o < 32; o += kKThreads / 32) {
       const int ig = o >> 2, m = o & 3;
       uint32_t r[4];
       ldsm_x4_trans(smem_addr(sQ) + ig * 2048 + (4 * m + (lane >> 3)) * 128 + (lane & 7) * 16, r);
@@ -1015,7 +1030,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
         *reinterpret_cast<__nv_bfloat162 *>(ws + kVQl + off) = lb;
       }
     }
-    for (int id = tid; id < kC * 16; id += kThreads) {
+    for (int id = tid; id < kC * 16; id += kKThreads) {
       // Khat = k (.) e^{lambda_C - lambda_t}, K-major
       const int t = ((id >> 7) << 3) | (id & 7), g = (id >> 3) & 15;
       const float4 t0v = *reinterpret_cast<const float4 *>(lam + t * kLdL + 8 * g);
@@ -1044,7 +1059,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
     __syncthreads();
     tc_fence_after();
     if (tid == 0) kda_issue_level_mma(tmem + kKColG2, op_addr, mbG);
-    {  // meanwhile: the block-of-4 sums into the staging
+    if (tid < 256) {  // meanwhile: the block-of-4 sums into the staging
       const int blk = tid >> 4, o = tid & 15;
       // (i, j) of output o inside the block (4 bits each, output 0 lowest):
       // i = 1,2,2,3,3,3,0,1,1,2,2,2,3,3,3,3  j = 0,0,1,0,1,2,0,0,1,0,1,2,0,1,2,3
@@ -1064,7 +1079,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
     if (SSE) {
       // V rows of the visits into the operand region, free now: they land
       // while the solve runs
-      for (int id = tid; id < kC * 16; id += kThreads) {
+      for (int id = tid; id < kC * 16; id += kKThreads) {
         const int r = id >> 4, k8 = id & 15;
         unsigned char *dst = sV + kmajor_off(r, k8 * 8, kDV);
         if (rtok[r] >= 0)
@@ -1077,7 +1092,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
 
     // ---- Mq (lower, diagonal included) to the workspace (8 consecutive
     // threads take 8 consecutive rows: one contiguous 128-byte piece)
-    for (int id = tid; id < kC * 8; id += kThreads) {
+    for (int id = tid; id < kC * 8; id += kKThreads) {
       const int i = ((id >> 6) << 3) | (id & 7), j0 = ((id >> 3) & 7) * 8;
       float x[8];
       const float gi = SSE ? be[i] : 1.f;  // SSE: the read of visit i is scaled by its gate
@@ -1090,21 +1105,20 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
     // T = L^-1 diag(beta) (KDA) or L^-1 (GDN2), lower triangle, and Kt = k (.)
     // e^{lambda} (KDA) or Et = b (.) k (.) e^{lambda} (GDN2), hi/lo operand tiles
     {
-      const int i = tid >> 2, j0 = (tid & 3) * 16;
-      float x[16];
+      const int i = tid >> 3, j0 = (tid & 7) * 8;
+      float x[8];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
+      for (int e = 0; e < 8; ++e) {
         const int j = j0 + e;
         x[e] = j <= i ? (G2 ? sTf[i * kLd + j] : sTf[i * kLd + j] * be[j]) : 0.f;
       }
       store_split8(sTh, sTl, kmajor_off(i, j0, kC), x);
-      store_split8(sTh, sTl, kmajor_off(i, j0 + 8, kC), x + 8);
     }
     if (G2) {
       // Z = w (.) v, hi/lo K-major [64 t][128 d] into the solve buffers (free
       // once T is written): the MN-major A operand of Ut^T = Z^T T^T
       __syncthreads();
-      for (int id = tid; id < kC * 16; id += kThreads) {
+      for (int id = tid; id < kC * 16; id += kKThreads) {
         const int t = ((id >> 7) << 3) | (id & 7), g = (id >> 3) & 15;
         const uint4 raw = *reinterpret_cast<const uint4 *>(sV + kmajor_off(t, 8 * g, kDV));
         const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
@@ -1123,7 +1137,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
         store_split8(op + kOL, op + kOL + 16384, kmajor_off(t, 8 * g, kDV), x);
       }
     }
-    for (int id = tid; id < kC * 16; id += kThreads) {
+    for (int id = tid; id < kC * 16; id += kKThreads) {
       const int t = ((id >> 7) << 3) | (id & 7), g = (id >> 3) & 15;
       const float4 t0v = *reinterpret_cast<const float4 *>(lam + t * kLdL + 8 * g);
       const float4 t1v = *reinterpret_cast<const float4 *>(lam + t * kLdL + 8 * g + 4);
@@ -1172,7 +1186,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_prep_kernel(const KdaPrepArgs
     if (SSE && tid < kC) reinterpret_cast<int *>(ws + kSRows)[tid] = rrow[tid];
     {
       float *gU = reinterpret_cast<float *>(ws + (SSE ? kSU : kVU));
-      for (int i0 = half * 32; i0 < half * 32 + 32; i0 += 16) {
+      {
+        const int i0 = 16 * (tid >> 7);  // a quarter of the tokens per group of 4 warps
         float x[16];
         tmem_ld16(tmem_addr(tmem, lane_base, kKColU + i0), x);
         tmem_ld_wait();
@@ -1669,12 +1684,12 @@ int launch_kda_chunk(float *state, const uint16_t *q, const uint16_t *k, const u
     if (cudaFuncSetAttribute(kda_prep_kernel<kModeGdn2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kKdaSmem)) != cudaSuccess)
       return check_launch("gdn2_scan: set shared memory");
-    kda_prep_kernel<kModeGdn2><<<static_cast<unsigned>(pgrid), kThreads, kKdaSmem, st>>>(pa);
+    kda_prep_kernel<kModeGdn2><<<static_cast<unsigned>(pgrid), kKThreads, kKdaSmem, st>>>(pa);
   } else {
     if (cudaFuncSetAttribute(kda_prep_kernel<kModeKda>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kKdaSmem)) != cudaSuccess)
       return check_launch("gdn_scan: set shared memory");
-    kda_prep_kernel<kModeKda><<<static_cast<unsigned>(pgrid), kThreads, kKdaSmem, st>>>(pa);
+    kda_prep_kernel<kModeKda><<<static_cast<unsigned>(pgrid), kKThreads, kKdaSmem, st>>>(pa);
   }
   const int rc = check_launch(g2 ? "gdn2_scan: chunk preparation kernel" : "gdn_scan: KDA chunk preparation kernel");
   if (rc != SDM_OK) return rc;
@@ -1734,7 +1749,7 @@ int launch_sse_delta_chunk(float *state, const uint32_t *rec, int rw, const uint
                            static_cast<int>(kKdaSmem)) != cudaSuccess)
     return check_launch("sse_scan: set shared memory");
   const long pgrid = pa.units < sms ? pa.units : sms;
-  kda_prep_kernel<kModeSse><<<static_cast<unsigned>(pgrid), kThreads, kKdaSmem, st>>>(pa);
+  kda_prep_kernel<kModeSse><<<static_cast<unsigned>(pgrid), kKThreads, kKdaSmem, st>>>(pa);
   int rc = check_launch("sse_scan: delta chunk preparation kernel");
   if (rc != SDM_OK) return rc;
 
