@@ -485,9 +485,10 @@ constexpr uint32_t kKAl = kKLam + kC * kLdL * 4;  // alpha fp32 [64][128]; then 
 constexpr uint32_t kKAlBytes = kC * kLd * 4 + kC * kLdS * 4;
 constexpr uint32_t kKOp = kKAl + kKAlBytes;       // level operands: rows hi, lo [128][128], cols hi, lo [64][128]
 constexpr uint32_t kKOpBytes = 98304;
-constexpr uint32_t kKGate = kKOp + kKOpBytes;     // beta [64], block-of-4 sums [16][16]; SSE: visit
-                                                  // token-heads [64], staging rows [64], unit info [4]
-constexpr uint32_t kKBar = kKGate + (kC + 256 + 2 * kC + 4) * 4;
+constexpr uint32_t kKGate = kKOp + kKOpBytes;     // beta [2][64], block-of-4 sums [16][16]; SSE: visit
+                                                  // token-heads [2][64], staging rows [2][64], unit
+                                                  // info [2][4] (two buffers: this unit, the next)
+constexpr uint32_t kKBar = kKGate + (2 * kC + 256 + 4 * kC + 8) * 4;
 constexpr uint32_t kKdaSmem = kKBar + 64;
 // inside the operand region once the level products are done
 constexpr uint32_t kOL = 0;                       // GDN2's Z hi/lo (32 KB) once T is written
@@ -653,11 +654,15 @@ __global__ void __launch_bounds__(kKThreads, 1) kda_prep_kernel(const KdaPrepArg
   float *sTf = reinterpret_cast<float *>(op + kOTf);
   float *sZ = reinterpret_cast<float *>(op + kOZ);
   unsigned char *sTh = op + kOT, *sTl = op + kOT + 8192, *sKth = op + kOKt, *sKtl = op + kOKt + 16384;
-  float *be = reinterpret_cast<float *>(sm + kKGate);
-  float *w4 = be + kC;
-  int *rtok = reinterpret_cast<int *>(w4 + 256);    // SSE: token-head of each visit (-1: padding)
-  int *rrow = rtok + kC;                            // SSE: staging row of each visit
-  int *info = rrow + kC;                            // SSE: partition, first position, visits, list offset
+  // per unit, two buffers (this unit's and the next one's, whose inputs load
+  // while this one finishes): beta (SSE: the visits' gates) and, SSE only, the
+  // token-head (-1: padding) and staging row of each visit and the unit's
+  // partition, first position, visit count and list offset
+  float *be_all = reinterpret_cast<float *>(sm + kKGate);
+  float *w4 = be_all + 2 * kC;
+  int *rtok_all = reinterpret_cast<int *>(w4 + 256);
+  int *rrow_all = rtok_all + 2 * kC;
+  int *info_all = rrow_all + 2 * kC;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kKBar);
   uint32_t *holder = reinterpret_cast<uint32_t *>(sm + kKBar + 32);
   const uint32_t mbG = smem_addr(bars + 0), mbW = smem_addr(bars + 1), mbEnd = smem_addr(bars + 2);
@@ -690,136 +695,169 @@ __global__ void __launch_bounds__(kKThreads, 1) kda_prep_kernel(const KdaPrepArg
     return all;
   };
 
-  int it = 0;  // units done by this CTA (the parity of the W/U barrier)
-  for (long u = blockIdx.x; u < a.units; u += gridDim.x) {
-    unsigned char *ws = a.ws + u * (SSE ? kSUnit : kVUnit);
-    const long bh = SSE ? u / a.umax : u / a.nchunks;
+  // SSE: units past the (batch, head)'s own count are skipped (uniform over the CTA)
+  auto unit_valid = [&](long u) -> bool {
+    if (!SSE) return true;
+    const long bh = u / a.umax;
+    return static_cast<int>(u - bh * a.umax) < static_cast<int>(a.grp[bh * a.gwords + ssegrp::kGFirst + a.N]);
+  };
+  auto next_unit = [&](long u) -> long {
+    for (u += gridDim.x; u < a.units && !unit_valid(u); u += gridDim.x) {
+    }
+    return u;
+  };
+  // SSE: the visits of unit u (a chunk of 64 visits of one partition of its
+  // (batch, head), sse_group.cuh) into buffer b: token-heads, staging rows,
+  // gates (the write strength of the delta rule).  Synchronises the CTA.
+  auto sse_setup = [&](long u, int b) {
+    const long bh = u / a.umax;
+    const int uu = static_cast<int>(u - bh * a.umax);
+    const uint32_t *g = a.grp + bh * a.gwords;
+    const int N = a.N;
+    int *info = info_all + 4 * b;
+    if (warp == 0) {
+      const int nS = (T + kC - 1) / kC;
+      int p = N, pos0 = uu * kC, cnt = T, off = 0;
+      if (uu >= nS) {  // routed: the last partition whose first unit is <= uu
+        const bool c0 = lane < N && static_cast<int>(g[ssegrp::kGFirst + lane]) <= uu;
+        const bool c1 = lane + 32 < N && static_cast<int>(g[ssegrp::kGFirst + lane + 32]) <= uu;
+        p = __popc(__ballot_sync(kFull, c0)) + __popc(__ballot_sync(kFull, c1)) - 1;
+        pos0 = (uu - static_cast<int>(g[ssegrp::kGFirst + p])) * kC;
+        cnt = static_cast<int>(g[ssegrp::kGCnt + p]);
+        off = static_cast<int>(g[ssegrp::kGOff + p]);
+      }
+      if (lane == 0) {
+        info[0] = p;
+        info[1] = pos0;
+        info[2] = cnt;
+        info[3] = off;
+      }
+    }
+    __syncthreads();
+    if (tid < kC) {
+      const int p = info[0], pos = info[1] + tid, topk = a.topk;
+      int tl = -1, srow = -1;
+      float gate = 0.f;
+      if (pos < info[2]) {
+        int t = pos, r = topk;  // the shared partition: every token, slot topk, gate 1
+        if (p < N) {
+          const uint32_t e = g[ssegrp::kGHdr + info[3] + pos];
+          t = static_cast<int>(e >> 4);
+          r = static_cast<int>(e & 15u);
+        }
+        tl = static_cast<int>((bh / H * T + t) * H + bh % H);
+        gate = r < topk ? __uint_as_float(a.rec[static_cast<long>(tl) * a.rw + topk + r]) : 1.f;
+        srow = tl * (topk + 1) + r;
+      }
+      rtok_all[b * kC + tid] = tl;
+      rrow_all[b * kC + tid] = srow;
+      be_all[b * kC + tid] = gate;
+    }
+    __syncthreads();
+  };
+  // ---- inputs of unit u into buffer b, in three groups issued as their
+  // destinations free up (padding: k = q = v = 0, alpha = 1, beta = 0):
+  // Q (SSE: the visits' q rows) ...
+  auto load_q = [&](long u, int b) {
+    const int *rt = rtok_all + b * kC;
+    const long bh = SSE ? 0 : u / a.nchunks;
+    const int t0 = SSE ? 0 : static_cast<int>(u - bh * a.nchunks) * kC;
+    const long tok0 = (bh / H) * T * H + bh % H;
+    for (int id = tid; id < kC * 16; id += kKThreads) {
+      const int r = id >> 4, k8 = id & 15;
+      unsigned char *dst = sQ + kmajor_off(r, k8 * 8, kDK);
+      const bool valid = SSE ? rt[r] >= 0 : t0 + r < T;
+      const long src = SSE ? static_cast<long>(rt[r]) : tok0 + static_cast<long>(t0 + r) * H;
+      if (valid)
+        cp_async<16>(dst, a.q + src * kDK + k8 * 8);
+      else
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+    }
+    cp_async_commit();
+  };
+  // ... alpha, beta and K (SSE: the key logits, into the lambda buffer) ...
+  auto load_kal = [&](long u, int b) {
+    const int *rt = rtok_all + b * kC;
+    const long bh = SSE ? 0 : u / a.nchunks;
     const int t0 = SSE ? 0 : static_cast<int>(u - bh * a.nchunks) * kC;
     const long tok0 = (bh / H) * T * H + bh % H;
     if (SSE) {
-      // the unit: a chunk of 64 visits of one partition of this (batch, head)
-      // (sse_group.cuh); units past the (batch, head)'s own count are skipped
-      const int uu = static_cast<int>(u - bh * a.umax);
-      const uint32_t *g = a.grp + bh * a.gwords;
-      const int N = a.N;
-      if (uu >= static_cast<int>(g[ssegrp::kGFirst + N])) continue;  // uniform over the CTA
-      if (warp == 0) {
-        const int nS = (T + kC - 1) / kC;
-        int p = N, pos0 = uu * kC, cnt = T, off = 0;
-        if (uu >= nS) {  // routed: the last partition whose first unit is <= uu
-          const bool c0 = lane < N && static_cast<int>(g[ssegrp::kGFirst + lane]) <= uu;
-          const bool c1 = lane + 32 < N && static_cast<int>(g[ssegrp::kGFirst + lane + 32]) <= uu;
-          p = __popc(__ballot_sync(kFull, c0)) + __popc(__ballot_sync(kFull, c1)) - 1;
-          pos0 = (uu - static_cast<int>(g[ssegrp::kGFirst + p])) * kC;
-          cnt = static_cast<int>(g[ssegrp::kGCnt + p]);
-          off = static_cast<int>(g[ssegrp::kGOff + p]);
-        }
-        if (lane == 0) {
-          info[0] = p;
-          info[1] = pos0;
-          info[2] = cnt;
-          info[3] = off;
-        }
-      }
-      __syncthreads();
-      if (tid < kC) {
-        const int p = info[0], pos = info[1] + tid, topk = a.topk;
-        int tl = -1, srow = -1;
-        float gate = 0.f;
-        if (pos < info[2]) {
-          int t = pos, r = topk;  // the shared partition: every token, slot topk, gate 1
-          if (p < N) {
-            const uint32_t e = g[ssegrp::kGHdr + info[3] + pos];
-            t = static_cast<int>(e >> 4);
-            r = static_cast<int>(e & 15u);
-          }
-          tl = static_cast<int>((bh / H * T + t) * H + bh % H);
-          gate = r < topk ? __uint_as_float(a.rec[static_cast<long>(tl) * a.rw + topk + r]) : 1.f;
-          srow = tl * (topk + 1) + r;
-        }
-        rtok[tid] = tl;
-        rrow[tid] = srow;
-        be[tid] = gate;  // the write strength of the delta rule
-      }
-      __syncthreads();
-    }
-    // GDN2 gates of the chunk's tokens: row t at gb[t * gstride], valid for t < nvalid
-    const long gstride = static_cast<long>(H) * kDK;
-    const int nvalid = T - t0 < kC ? T - t0 : kC;
-    const float *gb = G2 ? a.b_erase + (tok0 + static_cast<long>(t0) * H) * kDK : nullptr;
-    const float *gw = G2 ? a.w_write + (tok0 + static_cast<long>(t0) * H) * kDV : nullptr;
-
-    // the next unit's input rows into L2 while this one is prepared
-    if (!SSE) {
-      const long un = u + gridDim.x;
-      if (un < a.units) {
-        const long bhn = un / a.nchunks;
-        const int t0n = static_cast<int>(un - bhn * a.nchunks) * kC;
-        const long tokn = (bhn / H) * T * H + bhn % H;
-        // 64 rows: k, q, v (two 128-byte lines each) and alpha (four): ten lines a row
-        for (int id = tid; id < kC * 10; id += kKThreads) {
-          const int r = id / 10, w = id - 10 * r;
-          if (t0n + r < T) {
-            const long row = tokn + static_cast<long>(t0n + r) * H;
-            const void *p = w < 6 ? static_cast<const void *>((w < 2 ? a.k : w < 4 ? a.q : a.v) + row * kDK + 64 * (w & 1))
-                                  : static_cast<const void *>(a.alpha + row * kDK + 32 * (w - 6));
-            prefetch_line_l2(p);
-            if (G2 && w >= 6) {
-              prefetch_line_l2(a.b_erase + row * kDK + 32 * (w - 6));
-              prefetch_line_l2(a.w_write + row * kDV + 32 * (w - 6));
-            }
-          }
-        }
-      }
-    }
-    // ---- inputs: K, Q, V tiles, alpha rows, beta (padding: k = q = v = 0, alpha = 1, beta = 0).
-    // SSE: q rows and the key logits (into the lambda buffer) of the gathered
-    // visits; V comes later
-    if (SSE) {
-      for (int id = tid; id < kC * 16; id += kKThreads) {
-        const int r = id >> 4, k8 = id & 15;
-        unsigned char *dst = sQ + kmajor_off(r, k8 * 8, kDK);
-        if (rtok[r] >= 0)
-          cp_async<16>(dst, a.q + static_cast<long>(rtok[r]) * kDK + k8 * 8);
-        else
-          *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
-      }
       for (int id = tid; id < kC * (kDK / 4); id += kKThreads) {
         const int r = id >> 5, c4 = id & 31;
-        if (rtok[r] >= 0)
-          cp_async<16>(lam + r * kLdL + 4 * c4, a.klog + static_cast<long>(rtok[r]) * kDK + 4 * c4);
+        if (rt[r] >= 0)
+          cp_async<16>(lam + r * kLdL + 4 * c4, a.klog + static_cast<long>(rt[r]) * kDK + 4 * c4);
         else
           *reinterpret_cast<float4 *>(lam + r * kLdL + 4 * c4) = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     } else {
-      for (int id = tid; id < 3 * kC * 16; id += kKThreads) {
-        const int m = id >> 10, r = (id >> 4) & 63, k8 = id & 15;
-        const int t = t0 + r;
-        unsigned char *dst = sm + (m == 0 ? kKK : m == 1 ? kKQ : kKV) + kmajor_off(r, k8 * 8, kDK);
-        if (t < T)
-          cp_async<16>(dst, (m == 0 ? a.k : m == 1 ? a.q : a.v) + (tok0 + static_cast<long>(t) * H) * kDK + k8 * 8);
+      for (int id = tid; id < kC * 16; id += kKThreads) {
+        const int r = id >> 4, k8 = id & 15;
+        unsigned char *dst = sK + kmajor_off(r, k8 * 8, kDK);
+        if (t0 + r < T)
+          cp_async<16>(dst, a.k + (tok0 + static_cast<long>(t0 + r) * H) * kDK + k8 * 8);
         else
           *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
       }
     }
     for (int id = tid; id < kC * (kDK / 4); id += kKThreads) {
       const int r = id >> 5, c4 = id & 31;
-      const int t = t0 + r;
-      const bool valid = SSE ? rtok[r] >= 0 : t < T;
-      const long src = SSE ? static_cast<long>(rtok[r]) : tok0 + static_cast<long>(t) * H;
+      const bool valid = SSE ? rt[r] >= 0 : t0 + r < T;
+      const long src = SSE ? static_cast<long>(rt[r]) : tok0 + static_cast<long>(t0 + r) * H;
       if (valid)
         cp_async<16>(al + r * kDK + 4 * c4, a.alpha + src * kDK + 4 * c4);
       else
         *reinterpret_cast<float4 *>(al + r * kDK + 4 * c4) = make_float4(1.f, 1.f, 1.f, 1.f);
     }
     if (tid < kC && !G2 && !SSE) {
-      const int t = t0 + tid;
-      if (t < T)
-        cp_async<4>(be + tid, a.beta + tok0 + static_cast<long>(t) * H);
+      float *bb = be_all + b * kC;
+      if (t0 + tid < T)
+        cp_async<4>(bb + tid, a.beta + tok0 + static_cast<long>(t0 + tid) * H);
       else
-        be[tid] = 0.f;
+        bb[tid] = 0.f;
     }
     cp_async_commit();
+  };
+  // ... and V (SSE: loaded inside the unit, below)
+  auto load_v = [&](long u) {
+    const long bh = u / a.nchunks;
+    const int t0 = static_cast<int>(u - bh * a.nchunks) * kC;
+    const long tok0 = (bh / H) * T * H + bh % H;
+    for (int id = tid; id < kC * 16; id += kKThreads) {
+      const int r = id >> 4, k8 = id & 15;
+      unsigned char *dst = sV + kmajor_off(r, k8 * 8, kDV);
+      if (t0 + r < T)
+        cp_async<16>(dst, a.v + (tok0 + static_cast<long>(t0 + r) * H) * kDV + k8 * 8);
+      else
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+    }
+    cp_async_commit();
+  };
+
+  int it = 0;  // units done by this CTA (the parity of the W/U barrier)
+  int buf = 0;
+  long u = next_unit(static_cast<long>(blockIdx.x) - static_cast<long>(gridDim.x));
+  if (u < a.units) {
+    if (SSE) sse_setup(u, 0);
+    load_q(u, 0);
+    load_kal(u, 0);
+    if (!SSE) load_v(u);
+  }
+  for (; u < a.units; buf ^= 1) {
+    const long un = next_unit(u);
+    const bool has_next = un < a.units;
+    if (SSE && has_next) sse_setup(un, buf ^ 1);
+    float *be = be_all + buf * kC;
+    const int *rtok = rtok_all + buf * kC;
+    const int *rrow = rrow_all + buf * kC;
+    unsigned char *ws = a.ws + u * (SSE ? kSUnit : kVUnit);
+    const long bh = SSE ? u / a.umax : u / a.nchunks;
+    const int t0 = SSE ? 0 : static_cast<int>(u - bh * a.nchunks) * kC;
+    const long tok0 = (bh / H) * T * H + bh % H;
+    // GDN2 gates of the chunk's tokens: row t at gb[t * gstride], valid for t < nvalid
+    const long gstride = static_cast<long>(H) * kDK;
+    const int nvalid = T - t0 < kC ? T - t0 : kC;
+    const float *gb = G2 ? a.b_erase + (tok0 + static_cast<long>(t0) * H) * kDK : nullptr;
+    const float *gw = G2 ? a.w_write + (tok0 + static_cast<long>(t0) * H) * kDV : nullptr;
     cp_async_wait<0>();
     __syncthreads();
     if (SSE) {
@@ -1006,11 +1044,11 @@ __global__ void __launch_bounds__(kKThreads, 1) kda_prep_kernel(const KdaPrepArg
     __syncthreads();
     tc_fence_after();
     if (tid == 0) kda_issue_level_mma(tmem + kKColG1, op_addr, mbG);
-    // meanwhile: Qt (MN-major: 8 tokens of one key per 16 bytes), Khat and
-    // gamma_C to the workspace
-    // (q transposed by ldmatrix, four 8x8 core matrices per warp and step:
-    // lane t holds tokens 2(t%4), 2(t%4)+1 of key 8(4m+j) + t/4)
-    for (int o = warp; o < 32; o += kKThreads / 32) {
+    // meanwhile (warps 1-15; warp 0's issuing thread waits on the tensor core):
+    // Qt (MN-major: 8 tokens of one key per 16 bytes), Khat and gamma_C to the
+    // workspace (q transposed by ldmatrix, four 8x8 core matrices per warp and
+    // step: lane t holds tokens 2(t%4), 2(t%4)+1 of key 8(4m+j) + t/4)
+    for (int o = warp - 1; warp > 0 && o < 32; o += kKThreads / 32 - 1) {
       const int ig = o >> 2, m = o & 3;
       uint32_t r[4];
       ldsm_x4_trans(smem_addr(sQ) + ig * 2048 + (4 * m + (lane >> 3)) * 128 + (lane & 7) * 16, r);
@@ -1030,7 +1068,7 @@ __global__ void __launch_bounds__(kKThreads, 1) kda_prep_kernel(const KdaPrepArg
         *reinterpret_cast<__nv_bfloat162 *>(ws + kVQl + off) = lb;
       }
     }
-    for (int id = tid; id < kC * 16; id += kKThreads) {
+    for (int id = tid - 32; tid >= 32 && id < kC * 16; id += kKThreads - 32) {
       // Khat = k (.) e^{lambda_C - lambda_t}, K-major
       const int t = ((id >> 7) << 3) | (id & 7), g = (id >> 3) & 15;
       const float4 t0v = *reinterpret_cast<const float4 *>(lam + t * kLdL + 8 * g);
@@ -1045,7 +1083,8 @@ __global__ void __launch_bounds__(kKThreads, 1) kda_prep_kernel(const KdaPrepArg
       for (int e = 0; e < 8; ++e) x[e] *= __expf(d[e]);
       store_split8(ws + kVKh, ws + kVKh + 16384, kmajor_off(t, 8 * g, kDK), x);
     }
-    if (tid < kDK) reinterpret_cast<float *>(ws + kVG)[tid] = __expf(lam[(kC - 1) * kLdL + tid]);
+    if (tid >= 32 && tid < 32 + kDK)
+      reinterpret_cast<float *>(ws + kVG)[tid - 32] = __expf(lam[(kC - 1) * kLdL + tid - 32]);
     if (!wait_ok(mbG, 0)) { failed = true; break; }
     kda_level_extract<MODE>(0, 1, tmem + kKColG1, sL, sMst, be, warp, lane);
     tc_fence_before();
@@ -1059,17 +1098,19 @@ __global__ void __launch_bounds__(kKThreads, 1) kda_prep_kernel(const KdaPrepArg
     __syncthreads();
     tc_fence_after();
     if (tid == 0) kda_issue_level_mma(tmem + kKColG2, op_addr, mbG);
-    if (tid < 256) {  // meanwhile: the block-of-4 sums into the staging
-      const int blk = tid >> 4, o = tid & 15;
+    // the Q tile is free: the next unit's q rows
+    if (has_next) load_q(un, buf ^ 1);
+    if (tid >= 32 && tid < 288) {  // meanwhile: the block-of-4 sums into the staging
+      const int blk = (tid - 32) >> 4, o = (tid - 32) & 15;
       // (i, j) of output o inside the block (4 bits each, output 0 lowest):
       // i = 1,2,2,3,3,3,0,1,1,2,2,2,3,3,3,3  j = 0,0,1,0,1,2,0,0,1,0,1,2,0,1,2,3
       const uint64_t oi = 0x3333222110333221ull, oj = 0x3210210100210100ull;
       const int i = 4 * blk + static_cast<int>((oi >> (4 * o)) & 15);
       const int j = 4 * blk + static_cast<int>((oj >> (4 * o)) & 15);
       if (o < 6)
-        sL[i * kLd + j] = G2 ? w4[tid] : be[i] * w4[tid];
+        sL[i * kLd + j] = G2 ? w4[tid - 32] : be[i] * w4[tid - 32];
       else
-        sMst[i * kLdS + j] = w4[tid];
+        sMst[i * kLdS + j] = w4[tid - 32];
     }
     if (!wait_ok(mbG, 1)) { failed = true; break; }
     kda_level_extract<MODE>(2, 3, tmem + kKColG2, sL, sMst, be, warp, lane);
@@ -1164,6 +1205,8 @@ __global__ void __launch_bounds__(kKThreads, 1) kda_prep_kernel(const KdaPrepArg
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // K, alpha, beta and lambda are free: the next unit's
+    if (has_next) load_kal(un, buf ^ 1);
     // ---- W^T = Kt^T T^T (three passes) and Ut^T = V^T T^T (V is exact: two)
     if (tid == 0) {
 #pragma unroll
@@ -1183,6 +1226,8 @@ __global__ void __launch_bounds__(kKThreads, 1) kda_prep_kernel(const KdaPrepArg
       mma_commit(mbW);
     }
     if (!wait_ok(mbW, static_cast<uint32_t>(it & 1))) { failed = true; break; }
+    // the V tile is free: the next unit's
+    if (has_next && !SSE) load_v(un);
     if (SSE && tid < kC) reinterpret_cast<int *>(ws + kSRows)[tid] = rrow[tid];
     {
       float *gU = reinterpret_cast<float *>(ws + (SSE ? kSU : kVU));
@@ -1204,7 +1249,9 @@ __global__ void __launch_bounds__(kKThreads, 1) kda_prep_kernel(const KdaPrepArg
     __syncthreads();
     tc_fence_after();
     ++it;
+    u = un;
   }
+  cp_async_wait<0>();  // (a wait that ran out may leave the next unit's loads in flight)
   if (failed) {
     if (tid == 0) mma_commit(mbEnd);
     mbar_wait(mbEnd, 0, kWaitLimit);

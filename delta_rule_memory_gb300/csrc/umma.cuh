@@ -97,11 +97,6 @@ __device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
 }
 
-// one 128-byte line of global memory into L2 (an ordinary load-unit prefetch)
-__device__ __forceinline__ void prefetch_line_l2(const void *p) {
-  asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p));
-}
-
 // Wait for the phase with the given parity to complete; gives up after
 // `limit` polls (backing off with nanosleep) and returns false (the caller
 // records an error and stops).
