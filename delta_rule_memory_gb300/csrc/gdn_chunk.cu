@@ -104,8 +104,17 @@ static_assert(2 * (kPrepSmem + 1024) <= 228 * 1024, "two preparation CTAs per SM
 // one block distance at a time, X_IJ = -L_II^-1 sum_{K=J}^{I-1} L_IK X_KJ,
 // each thread computing a 1 x 4 strip with 16-byte loads.  Reads only the
 // strictly lower part of sA; writes the lower triangle (diagonal included) of
-// sTf; sZ holds 768 floats of block products.  Called by every thread of the CTA (at least 192)
-// (it synchronises the CTA).
+// sTf; sZ holds 768 floats of block products.  kNamed = 0: called by every
+// thread of the CTA (at least 192), synchronising the CTA; else by threads
+// 0 .. kNamed-1 only (kNamed >= 192), synchronising them on named barrier 1.
+template <int kNamed = 0>
+__device__ __forceinline__ void solve_sync() {
+  if (kNamed == 0)
+    __syncthreads();
+  else
+    asm volatile("bar.sync 1, %0;\n" ::"n"(kNamed) : "memory");
+}
+template <int kNamed = 0>
 __device__ __forceinline__ void solve_unit_lower(const float *sA, float *sTf, float *sZ, int tid) {
   if (tid < 64) {
     const int I = tid >> 4, cc = tid & 15, o = I * 16;
@@ -120,7 +129,7 @@ __device__ __forceinline__ void solve_unit_lower(const float *sA, float *sTf, fl
 #pragma unroll
     for (int r = 0; r < 16; ++r) sTf[(o + r) * kLd + o + cc] = xv[r];
   }
-  __syncthreads();
+  solve_sync<kNamed>();
   // ... then the blocks below the diagonal, one block distance at a time:
   // X_IJ = -L_II^-1 sum_{K=J}^{I-1} L_IK X_KJ.  A thread computes a 1 x 4
   // strip (pair p, row r, columns c4..c4+3) with 16-byte loads.
@@ -151,7 +160,7 @@ __device__ __forceinline__ void solve_unit_lower(const float *sA, float *sTf, fl
       }
       *reinterpret_cast<float4 *>(sZ + p * 256 + r * 16 + c4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
     }
-    __syncthreads();
+    solve_sync<kNamed>();
     if (mine) {
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
       const float *xrow = sTf + (I * 16 + r) * kLd + I * 16;
@@ -172,7 +181,7 @@ __device__ __forceinline__ void solve_unit_lower(const float *sA, float *sTf, fl
       *reinterpret_cast<float4 *>(sTf + (I * 16 + r) * kLd + J * 16 + c4) =
           make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
     }
-    __syncthreads();
+    solve_sync<kNamed>();
   }
 }
 
@@ -535,18 +544,21 @@ __device__ __forceinline__ void load_k8(const unsigned char *sK, const unsigned 
 // stores are conflict-free.
 // GDN2: the k rows of A are e_t = b_t (.) k_t (the erase gate times the key),
 // read as gb[t * gstride + c] for the chunk's valid tokens t < nvalid.
-template <int MODE>
-__device__ __forceinline__ void kda_level_operands(int la, int lb, const unsigned char *sK, const unsigned char *sKlo,
+// lam holds lambda in log2 units, so each factor is one 2^x.
+// Item k of a thread (k = 0..3): rows for k < 2, level LA for even k; the
+// operand row w and channel group g are the thread's own for every k.
+template <int MODE, int LA, int LB>
+__device__ __forceinline__ void kda_level_operands(const unsigned char *sK, const unsigned char *sKlo,
                                                    const unsigned char *sQ, const float *lam, unsigned char *op,
                                                    int tid, const float *gb, long gstride, int nvalid) {
   constexpr bool G2 = MODE == kModeGdn2;
+  static_assert(kKThreads == 512, "four items per thread");
+  const int w = (((tid >> 7) & 3) << 3) | (tid & 7), g = (tid >> 3) & 15;
 #pragma unroll 2
-  for (int id = tid; id < 2048; id += kKThreads) {
-    const bool is_row = id < 1024;
-    const int idd = id & 1023;
-    const int lsel = idd >> 9;                                         // 0: level la, 1: level lb
-    const int w = (((idd >> 7) & 3) << 3) | (idd & 7), g = (idd >> 3) & 15;
-    const int lvl = lsel ? lb : la;
+  for (int k = 0; k < 4; ++k) {
+    const bool is_row = k < 2;
+    const int lsel = k & 1;                                            // 0: level LA, 1: level LB
+    const int lvl = lsel ? LB : LA;
     const int sh = 5 - lvl, h = 1 << sh, seg = w >> sh;
     const int b = 2 * h * seg + h - 1;                                 // last token of the left half
     const int t = is_row ? b + 1 + (w & (h - 1)) : b - h + 1 + (w & (h - 1));
@@ -559,7 +571,7 @@ __device__ __forceinline__ void kda_level_operands(int la, int lb, const unsigne
     // right-half row: e^{lambda_t - lambda_b} (t > b); left-half col: e^{lambda_b - lambda_t} (t <= b)
     float f[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) f[e] = __expf(is_row ? dt[e] : -dt[e]);
+    for (int e = 0; e < 8; ++e) f[e] = ex2_approx(is_row ? dt[e] : -dt[e]);
     float x[8];
     load_k8<MODE>(sK, sKlo, t, 8 * g, x);
 #pragma unroll
@@ -909,9 +921,9 @@ __global__ void __launch_bounds__(kKThreads, 1) kda_prep_kernel(const KdaPrepArg
     // 6-15: Mq at (0,0),(1,0),(1,1),(2,0),(2,1),(2,2),(3,0),(3,1),(3,2),(3,3)).
     // The lanes of a warp alternate between its two blocks, so a quarter-warp's
     // 16-byte row loads fall on two bank groups, not one.
-    // warps 8-15: lambda, the running sum of log alpha over the chunk, two
-    // threads per channel (tokens 0-31 and 32-63); the second half then adds
-    // the first's total.
+    // warps 8-15: lambda, the running sum of log alpha over the chunk (kept in
+    // log2 units: every decay factor below is a 2^x), two threads per channel
+    // (tokens 0-31 and 32-63); the second half then adds the first's total.
     if (tid < 256) {
       const int blk = 2 * warp + (lane & 1), cg = lane >> 1;
       uint4 kraw[4], klraw[4], qraw[4];
@@ -1024,7 +1036,7 @@ __global__ void __launch_bounds__(kKThreads, 1) kda_prep_kernel(const KdaPrepArg
       float acc = 0.f;
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
-        acc += __logf(la[e]);
+        acc += lg2_approx(la[e]);
         lam[(32 * hf + e) * kLdL + r] = acc;
       }
     }
@@ -1038,7 +1050,7 @@ __global__ void __launch_bounds__(kKThreads, 1) kda_prep_kernel(const KdaPrepArg
     __syncthreads();
 
     // ---- levels 0 and 1 on the tensor cores
-    kda_level_operands<MODE>(0, 1, sK, sKlo, sQ, lam, op, tid, gb, gstride, nvalid);
+    kda_level_operands<MODE, 0, 1>(sK, sKlo, sQ, lam, op, tid, gb, gstride, nvalid);
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -1058,8 +1070,8 @@ __global__ void __launch_bounds__(kKThreads, 1) kda_prep_kernel(const KdaPrepArg
         const int c = 8 * (4 * m + j) + (lane >> 2);
         // (SSE: the read of the visit is scaled by its gate)
         const float g0 = SSE ? be[t0] : 1.f, g1 = SSE ? be[t0 + 1] : 1.f;
-        const float x0 = g0 * bf16_to_f32(static_cast<uint16_t>(r[j] & 0xffff)) * __expf(lam[t0 * kLdL + c]);
-        const float x1 = g1 * bf16_to_f32(static_cast<uint16_t>(r[j] >> 16)) * __expf(lam[(t0 + 1) * kLdL + c]);
+        const float x0 = g0 * bf16_to_f32(static_cast<uint16_t>(r[j] & 0xffff)) * ex2_approx(lam[t0 * kLdL + c]);
+        const float x1 = g1 * bf16_to_f32(static_cast<uint16_t>(r[j] >> 16)) * ex2_approx(lam[(t0 + 1) * kLdL + c]);
         const __nv_bfloat162 hb = __floats2bfloat162_rn(x0, x1);
         const float2 hf = __bfloat1622float2(hb);
         const __nv_bfloat162 lb = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
@@ -1080,11 +1092,11 @@ __global__ void __launch_bounds__(kKThreads, 1) kda_prep_kernel(const KdaPrepArg
       float x[8];
       load_k8<MODE>(sK, sKlo, t, 8 * g, x);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] *= __expf(d[e]);
+      for (int e = 0; e < 8; ++e) x[e] *= ex2_approx(d[e]);
       store_split8(ws + kVKh, ws + kVKh + 16384, kmajor_off(t, 8 * g, kDK), x);
     }
     if (tid >= 32 && tid < 32 + kDK)
-      reinterpret_cast<float *>(ws + kVG)[tid - 32] = __expf(lam[(kC - 1) * kLdL + tid - 32]);
+      reinterpret_cast<float *>(ws + kVG)[tid - 32] = ex2_approx(lam[(kC - 1) * kLdL + tid - 32]);
     if (!wait_ok(mbG, 0)) { failed = true; break; }
     kda_level_extract<MODE>(0, 1, tmem + kKColG1, sL, sMst, be, warp, lane);
     tc_fence_before();
@@ -1092,7 +1104,7 @@ __global__ void __launch_bounds__(kKThreads, 1) kda_prep_kernel(const KdaPrepArg
     tc_fence_after();
 
     // ---- levels 2 and 3
-    kda_level_operands<MODE>(2, 3, sK, sKlo, sQ, lam, op, tid, gb, gstride, nvalid);
+    kda_level_operands<MODE, 2, 3>(sK, sKlo, sQ, lam, op, tid, gb, gstride, nvalid);
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -1142,9 +1154,36 @@ __global__ void __launch_bounds__(kKThreads, 1) kda_prep_kernel(const KdaPrepArg
       store_split8(ws + kVMq, ws + kVMq + 8192, kmajor_off(i, j0, kC), x);
     }
     __syncthreads();
-    solve_unit_lower(sL, sTf, sZ, tid);
-    // T = L^-1 diag(beta) (KDA) or L^-1 (GDN2), lower triangle, and Kt = k (.)
-    // e^{lambda} (KDA) or Et = b (.) k (.) e^{lambda} (GDN2), hi/lo operand tiles
+    if (tid < 256) {
+      solve_unit_lower<256>(sL, sTf, sZ, tid);
+    } else {
+      // meanwhile (warps 8-15): Kt = k (.) e^{lambda} (KDA) or Et = b (.) k (.)
+      // e^{lambda} (GDN2), hi/lo operand tiles
+      for (int id = tid - 256; id < kC * 16; id += kKThreads - 256) {
+        const int t = ((id >> 7) << 3) | (id & 7), g = (id >> 3) & 15;
+        const float4 t0v = *reinterpret_cast<const float4 *>(lam + t * kLdL + 8 * g);
+        const float4 t1v = *reinterpret_cast<const float4 *>(lam + t * kLdL + 8 * g + 4);
+        const float lt[8] = {t0v.x, t0v.y, t0v.z, t0v.w, t1v.x, t1v.y, t1v.z, t1v.w};
+        float kx[8];
+        load_k8<MODE>(sK, sKlo, t, 8 * g, kx);
+        float bv[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
+        if (G2) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) bv[e] = 0.f;
+          if (t < nvalid) {
+            const float4 b0 = __ldg(reinterpret_cast<const float4 *>(gb + t * gstride + 8 * g));
+            const float4 b1 = __ldg(reinterpret_cast<const float4 *>(gb + t * gstride + 8 * g + 4));
+            bv[0] = b0.x; bv[1] = b0.y; bv[2] = b0.z; bv[3] = b0.w; bv[4] = b1.x; bv[5] = b1.y; bv[6] = b1.z; bv[7] = b1.w;
+          }
+        }
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = kx[e] * bv[e] * ex2_approx(lt[e]);
+        store_split8(sKth, sKtl, kmajor_off(t, 8 * g, kDK), x);
+      }
+    }
+    __syncthreads();
+    // T = L^-1 diag(beta) (KDA) or L^-1 (GDN2), lower triangle, hi/lo
     {
       const int i = tid >> 3, j0 = (tid & 7) * 8;
       float x[8];
@@ -1178,35 +1217,11 @@ __global__ void __launch_bounds__(kKThreads, 1) kda_prep_kernel(const KdaPrepArg
         store_split8(op + kOL, op + kOL + 16384, kmajor_off(t, 8 * g, kDV), x);
       }
     }
-    for (int id = tid; id < kC * 16; id += kKThreads) {
-      const int t = ((id >> 7) << 3) | (id & 7), g = (id >> 3) & 15;
-      const float4 t0v = *reinterpret_cast<const float4 *>(lam + t * kLdL + 8 * g);
-      const float4 t1v = *reinterpret_cast<const float4 *>(lam + t * kLdL + 8 * g + 4);
-      const float lt[8] = {t0v.x, t0v.y, t0v.z, t0v.w, t1v.x, t1v.y, t1v.z, t1v.w};
-      float kx[8];
-      load_k8<MODE>(sK, sKlo, t, 8 * g, kx);
-      float bv[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
-      if (G2) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) bv[e] = 0.f;
-        if (t < nvalid) {
-          const float4 b0 = __ldg(reinterpret_cast<const float4 *>(gb + t * gstride + 8 * g));
-          const float4 b1 = __ldg(reinterpret_cast<const float4 *>(gb + t * gstride + 8 * g + 4));
-          bv[0] = b0.x; bv[1] = b0.y; bv[2] = b0.z; bv[3] = b0.w; bv[4] = b1.x; bv[5] = b1.y; bv[6] = b1.z; bv[7] = b1.w;
-        }
-      }
-      float x[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = kx[e] * bv[e] * __expf(lt[e]);
-      store_split8(sKth, sKtl, kmajor_off(t, 8 * g, kDK), x);
-    }
     if (SSE) cp_async_wait<0>();
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // K, alpha, beta and lambda are free: the next unit's
-    if (has_next) load_kal(un, buf ^ 1);
     // ---- W^T = Kt^T T^T (three passes) and Ut^T = V^T T^T (V is exact: two)
     if (tid == 0) {
 #pragma unroll
@@ -1225,9 +1240,9 @@ __global__ void __launch_bounds__(kKThreads, 1) kda_prep_kernel(const KdaPrepArg
       }
       mma_commit(mbW);
     }
+    // K, alpha, beta and lambda are free: the next unit's, while the products run
+    if (has_next) load_kal(un, buf ^ 1);
     if (!wait_ok(mbW, static_cast<uint32_t>(it & 1))) { failed = true; break; }
-    // the V tile is free: the next unit's
-    if (has_next && !SSE) load_v(un);
     if (SSE && tid < kC) reinterpret_cast<int *>(ws + kSRows)[tid] = rrow[tid];
     {
       float *gU = reinterpret_cast<float *>(ws + (SSE ? kSU : kVU));
@@ -1245,6 +1260,8 @@ __global__ void __launch_bounds__(kKThreads, 1) kda_prep_kernel(const KdaPrepArg
         store_split8(ws + kVW, ws + kVWl, off + 2048, x + 8);
       }
     }
+    // the V tile is free: the next unit's
+    if (has_next && !SSE) load_v(un);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();

@@ -97,6 +97,19 @@ __device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// 2^x and log2(x) on the special-function unit (PTX ex2.approx.ftz.f32 and
+// lg2.approx.ftz.f32; subnormal inputs and results flush to zero)
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Wait for the phase with the given parity to complete; gives up after
 // `limit` polls (backing off with nanosleep) and returns false (the caller
 // records an error and stops).
