@@ -1143,22 +1143,22 @@ __global__ void __launch_bounds__(kKThreads, 1) kda_prep_kernel(const KdaPrepArg
       cp_async_commit();
     }
 
-    // ---- Mq (lower, diagonal included) to the workspace (8 consecutive
-    // threads take 8 consecutive rows: one contiguous 128-byte piece)
-    for (int id = tid; id < kC * 8; id += kKThreads) {
-      const int i = ((id >> 6) << 3) | (id & 7), j0 = ((id >> 3) & 7) * 8;
-      float x[8];
-      const float gi = SSE ? be[i] : 1.f;  // SSE: the read of visit i is scaled by its gate
-#pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = j0 + e <= i ? gi * sMst[i * kLdS + j0 + e] : 0.f;
-      store_split8(ws + kVMq, ws + kVMq + 8192, kmajor_off(i, j0, kC), x);
-    }
-    __syncthreads();
     if (tid < 256) {
       solve_unit_lower<256>(sL, sTf, sZ, tid);
     } else {
-      // meanwhile (warps 8-15): Kt = k (.) e^{lambda} (KDA) or Et = b (.) k (.)
-      // e^{lambda} (GDN2), hi/lo operand tiles
+      // meanwhile (warps 8-15): Mq (lower, diagonal included) to the workspace
+      // (8 consecutive threads take 8 consecutive rows: one contiguous
+      // 128-byte piece) ...
+      for (int id = tid - 256; id < kC * 8; id += kKThreads - 256) {
+        const int i = ((id >> 6) << 3) | (id & 7), j0 = ((id >> 3) & 7) * 8;
+        float x[8];
+        const float gi = SSE ? be[i] : 1.f;  // SSE: the read of visit i is scaled by its gate
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = j0 + e <= i ? gi * sMst[i * kLdS + j0 + e] : 0.f;
+        store_split8(ws + kVMq, ws + kVMq + 8192, kmajor_off(i, j0, kC), x);
+      }
+      // ... and Kt = k (.) e^{lambda} (KDA) or Et = b (.) k (.) e^{lambda}
+      // (GDN2), hi/lo operand tiles
       for (int id = tid - 256; id < kC * 16; id += kKThreads - 256) {
         const int t = ((id >> 7) << 3) | (id & 7), g = (id >> 3) & 15;
         const float4 t0v = *reinterpret_cast<const float4 *>(lam + t * kLdL + 8 * g);
@@ -1183,9 +1183,10 @@ __global__ void __launch_bounds__(kKThreads, 1) kda_prep_kernel(const KdaPrepArg
       }
     }
     __syncthreads();
-    // T = L^-1 diag(beta) (KDA) or L^-1 (GDN2), lower triangle, hi/lo
+    // T = L^-1 diag(beta) (KDA) or L^-1 (GDN2), lower triangle, hi/lo (8
+    // consecutive threads take 8 consecutive rows: conflict-free stores)
     {
-      const int i = tid >> 3, j0 = (tid & 7) * 8;
+      const int i = ((tid >> 6) << 3) | (tid & 7), j0 = ((tid >> 3) & 7) * 8;
       float x[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
