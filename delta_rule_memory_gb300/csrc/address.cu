@@ -179,26 +179,45 @@ __device__ __forceinline__ void warp_topk2_fast_x2(uint2 ca0, uint2 ca1, uint2 c
   __syncwarp();
 }
 
-// Candidates of one score half for the fast path: the entries with key >= tau
-// compacted into cbuf in ballot order (count `cnt`, at most 64), read back two
-// per lane.
+// Both halves' lower bounds at once: v packs two 16-bit keys (the top half of
+// each score half's lane maximum); a bitonic sort of the warp, descending in
+// each 16-bit half independently (max.u16x2 / min.u16x2), then lane k-1's
+// pair.  Truncation is monotone, so the result is the truncated k-th largest
+// lane maximum of each half: still a lower bound of that half's k-th score.
+__device__ __forceinline__ uint32_t warp_kth_largest_x2(uint32_t v, int k) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int blk = 2; blk <= 32; blk <<= 1) {
+#pragma unroll
+    for (int j = blk >> 1; j > 0; j >>= 1) {
+      const uint32_t o = __shfl_xor_sync(kFull, v, j);
+      const bool desc = (lane & blk) == 0, lower = (lane & j) == 0;
+      uint32_t r;
+      if (lower == desc)
+        asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(o));
+      else
+        asm("min.u16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(o));
+      v = r;
+    }
+  }
+  return __shfl_sync(kFull, v, k - 1);
+}
+
+// Candidates of one score half: the entries with key >= tau compacted into
+// cbuf in ballot order (at most 64 stored); returns how many qualified.
 template <int E>
-__device__ __forceinline__ void compact_half(const uint32_t (&key)[E], int n, uint32_t tau, uint2 *cbuf, int cnt,
-                                             uint2 &c0, uint2 &c1) {
+__device__ __forceinline__ int count_compact(const uint32_t (&key)[E], int n, uint32_t tau, uint2 *cbuf) {
   const int lane = threadIdx.x & 31;
   int basepos = 0;
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     const bool in = key[e] >= tau && lane + 32 * e < n;
     const unsigned bal = __ballot_sync(kFull, in);
-    if (in) cbuf[basepos + __popc(bal & ((1u << lane) - 1))] = make_uint2(key[e], lane + 32 * e);
+    const int pos = basepos + __popc(bal & ((1u << lane) - 1));
+    if (in && pos < 64) cbuf[pos] = make_uint2(key[e], lane + 32 * e);
     basepos += __popc(bal);
   }
-  __syncwarp();
-  const uint2 pad = make_uint2(0u, static_cast<unsigned>(INT_MAX));
-  c0 = lane < cnt ? cbuf[lane] : pad;
-  c1 = lane + 32 < cnt ? cbuf[lane + 32] : pad;
-  __syncwarp();
+  return basepos;
 }
 
 // The k-th largest (k <= 32) of the 32 lanes' values: a bitonic sort of the
@@ -358,18 +377,16 @@ __global__ void __launch_bounds__(kAddrWarps * 32) address_kernel(const float *_
         lm1 = max(lm1, key1[e]);
         lm2 = max(lm2, key2[e]);
       }
-      const uint32_t tau1 = warp_kth_largest(lm1, k), tau2 = warp_kth_largest(lm2, k);
-      int cnt1 = 0, cnt2 = 0;
-#pragma unroll
-      for (int e = 0; e < E1; ++e) {
-        const bool v = lane + 32 * e < sqrtN;
-        cnt1 += __popc(__ballot_sync(kFull, key1[e] >= tau1 && v));
-        cnt2 += __popc(__ballot_sync(kFull, key2[e] >= tau2 && v));
-      }
+      const uint32_t tp = warp_kth_largest_x2((lm1 & 0xffff0000u) | (lm2 >> 16), k);
+      const uint32_t tau1 = tp & 0xffff0000u, tau2 = tp << 16;
+      const int cnt1 = count_compact<E1>(key1, sqrtN, tau1, cbuf);
+      const int cnt2 = count_compact<E1>(key2, sqrtN, tau2, cbuf + 64);
       if (cnt1 <= 64 && cnt2 <= 64) {
-        uint2 a0, a1, b0, b1;
-        compact_half<E1>(key1, sqrtN, tau1, cbuf, cnt1, a0, a1);
-        compact_half<E1>(key2, sqrtN, tau2, cbuf + 64, cnt2, b0, b1);
+        __syncwarp();
+        const uint2 pad = make_uint2(0u, static_cast<unsigned>(INT_MAX));
+        const uint2 a0 = lane < cnt1 ? cbuf[lane] : pad, a1 = lane + 32 < cnt1 ? cbuf[lane + 32] : pad;
+        const uint2 b0 = lane < cnt2 ? cbuf[64 + lane] : pad, b1 = lane + 32 < cnt2 ? cbuf[64 + lane + 32] : pad;
+        __syncwarp();
         uint2 oa, ob;
         warp_topk2_fast_x2(a0, a1, b0, b1, k, cbuf, cbuf + 64, oa, ob);
         hv[0] = key_value(oa.x);
