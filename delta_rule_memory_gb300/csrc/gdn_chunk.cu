@@ -442,7 +442,9 @@ __global__ void __launch_bounds__(kThreads, kPrepCtasPerSm) gdn_prep_kernel(cons
 //   cols  k_j (.) e^{lambda_b - lambda_j}         (left-half tokens)
 // of which only the pairs in the same segment are kept.  Pairs inside a block
 // of 4 tokens (levels 4, 5) and the diagonal of Mq are summed on the CUDA
-// cores with running products of alpha.  One CTA per SM.
+// cores with running products of alpha.  One CTA of 16 warps per SM,
+// persistent over units; independent phases run on separate warp groups at
+// once, and the next unit's inputs load as this unit's buffers free up.
 // ===========================================================================
 // ---- one KDA chunk's tiles in the workspace (bytes)
 constexpr uint32_t kVW = 0;        // W hi            [64 i][128 c]   MN-major, as kUW
