@@ -350,8 +350,9 @@ __global__ void __launch_bounds__(kThreads, kPrepCtasPerSm) gdn_prep_kernel(cons
     // ---- L^-1 (unit lower triangular inverse of I + A)
     solve_unit_lower(sA, sTf, sZ, tid);
     // T = L^-1 diag(beta) and T diag(gamma), lower triangles, as B-operand tiles
+    // (8 consecutive threads take 8 consecutive rows: conflict-free stores)
     {
-      const int i = tid >> 2, j0 = (tid & 3) * 16;
+      const int i = ((tid >> 5) << 3) | (tid & 7), j0 = ((tid >> 3) & 3) * 16;
       float x[16], xg[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
