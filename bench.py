@@ -44,10 +44,16 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 NCU_TRAFFIC = {
     # one full-size sparse scan launch: 8.01 GB read + 4.19 GB written
     ("sdm_14b_layer", "sdm"): {"bytes": 12.20e9, "digest": "8821957384b6"},
-    # both kernels of one full-size gdn_scan call: 746.2 MB read + 592.5 MB written
-    ("gdn", "gdn"): {"bytes": 1.338e9, "digest": "6a9be503d782"},
-    # the five kernels of one full-size sse_scan call on the chunked path: 1.073 GB read + 0.799 GB written
-    ("sse", "sse"): {"bytes": 1.872e9, "digest": "4128ebe70bae"},
+    # both kernels of one full-size gdn_scan call: 746.2 MB read + 592.2 MB written
+    ("gdn", "gdn"): {"bytes": 1.338e9, "digest": "317af5b32f35"},
+    # both kernels of one full-size KDA gdn_scan call: 947.1 MB read + 664.1 MB written
+    ("kda", "kda"): {"bytes": 1.611e9, "digest": "317af5b32f35"},
+    # both kernels of one full-size gdn2_scan call: 1214.7 MB read + 675.0 MB written
+    ("gdn2", "gdn2"): {"bytes": 1.890e9, "digest": "317af5b32f35"},
+    # the five kernels of one full-size sse_scan call on the chunked path: 1.071 GB read + 0.807 GB written
+    ("sse", "sse"): {"bytes": 1.878e9, "digest": "e8641d4f8400"},
+    # the five kernels of one full-size delta-write sse_scan call: 1.451 GB read + 1.115 GB written
+    ("sse_delta", "sse"): {"bytes": 2.565e9, "digest": "317af5b32f35"},
 }
 
 
@@ -750,7 +756,7 @@ def run_ours(args, rank, world, local_rank, sampler):
         achieved = algo / (main_ms * 1e-3) / 1e12
     kernel_file = {"sdm": "sparse_scan.cu", "gdn": "gdn_chunk.cu", "kda": "gdn_chunk.cu", "gdn2": "gdn_chunk.cu",
                    "sse": ("gdn_chunk.cu" if wl.sse_mode else "sse_chunk.cu") if wl.sse_chunked else "sse_scan.cu"}[wl.kind]
-    tr = NCU_TRAFFIC.get((wl.name, wl.kind))
+    tr = NCU_TRAFFIC.get((wl.name, wl.kind)) if not args.batch else None  # recorded at the configured sizes only
     traffic = tr["bytes"] if tr and tr["digest"] == _src_digest(kernel_file) else None
     tokens = wl.tokens * world
     cfg = wl.config()
