@@ -1357,6 +1357,11 @@ constexpr uint32_t kHintedWaitLimit = 1u << 17;
 __device__ __forceinline__ bool chain_wait(uint32_t mbar, uint32_t parity, volatile int *abort_flag) {
   return mbar_wait_hinted(mbar, parity, kHintedWaitLimit, abort_flag);
 }
+// the producer's waits: a busy wait (one thread), so it issues the moment an operand is ready
+constexpr uint32_t kSpinWaitLimit = 1u << 24;
+__device__ __forceinline__ bool producer_wait(uint32_t mbar, uint32_t parity, volatile int *abort_flag) {
+  return mbar_wait_spin(mbar, parity, kSpinWaitLimit, abort_flag);
+}
 
 template <int CM>
 __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
@@ -1573,11 +1578,11 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
       // W lo (GDN, N = 64: Q is exact) or S hi x [W lo; Qt lo] (KDA), S lo x
       // [W hi; Q]
       const uint32_t xy = tmem + kColXY + 128 * (c & 1);
-      ok = chain_wait(bar(0), par, abort_flag);
+      ok = producer_wait(bar(0), par, abort_flag);
       if (ok) ++w_done;
 #pragma unroll
       for (int g = 0; g < 2; ++g) {
-        if (ok) ok = chain_wait(bar(8 + g), par, abort_flag);
+        if (ok) ok = producer_wait(bar(8 + g), par, abort_flag);
         if (!ok) break;
 #pragma unroll
         for (int ks = g; ks < 8; ks += 2) {
@@ -1590,15 +1595,15 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
       if (!(a.drop_signal && c == 0)) mma_commit(bar(4));
       // the W region is free once the group is done: the next chunk's W and Q
       if (c + 1 < n) {
-        ok = chain_wait(bar(4), par, abort_flag);
+        ok = producer_wait(bar(4), par, abort_flag);
         if (!ok) break;
         load(0, c + 1);
       }
       // round 2: D = U^T Khat first (the state update waits for it), then
       // Y2 = U^T Mq^T
-      ok = chain_wait(bar(1), par, abort_flag);
+      ok = producer_wait(bar(1), par, abort_flag);
       if (ok) ++m_done;
-      if (ok) ok = chain_wait(bar(10), par, abort_flag);
+      if (ok) ok = producer_wait(bar(10), par, abort_flag);
       if (!ok) break;
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
@@ -1617,7 +1622,7 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
       if (c + 1 < n) {
         // the next chunk's Mq, Khat and gammas once Y2 (the chunk's last MMA,
         // which reads Mq) is done
-        ok = chain_wait(bar(6), par, abort_flag);
+        ok = producer_wait(bar(6), par, abort_flag);
         if (ok) load(1, c + 1);
       }
     }

@@ -53,6 +53,8 @@ constexpr int kD = 128;     // d: value width (the MMA M)
 constexpr int kMaxTopk = ssegrp::kMaxTopk;
 constexpr int kMaxN = ssegrp::kMaxN;
 constexpr uint32_t kWaitLimit = 1u << 20;  // polls (about 0.1 s) before an mbarrier wait gives up
+constexpr uint32_t kHintedWaitLimit = 1u << 17;  // polls of up to 1 us each (the workers' suspending waits)
+constexpr uint32_t kSpinWaitLimit = 1u << 24;    // non-blocking polls (the producer's busy waits)
 
 // ---- one unit in the workspace (bytes)
 constexpr uint32_t kXQ = 0;       // Qt hi, lo   [64 i][128 r] K-major, 16 KB each
@@ -648,7 +650,7 @@ __global__ void __maxnreg__(96) sse_chain_kernel(const ChainArgs a) {
     const int row = 32 * (warp & 3) + (tid & 31), qtr = warp >> 2;
     const uint32_t lanes = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
     auto wwait = [&](uint32_t mb, uint32_t parity) -> bool {
-      return __all_sync(kFull, mbar_wait_abortable(mb, parity, kWaitLimit, abort_flag)) != 0;
+      return __all_sync(kFull, mbar_wait_hinted(mb, parity, kHintedWaitLimit, abort_flag)) != 0;
     };
     float S[32];  // S^T[row][32*qtr + j] = S[32*qtr + j][row]
 #pragma unroll
@@ -726,7 +728,8 @@ __global__ void __maxnreg__(96) sse_chain_kernel(const ChainArgs a) {
       prefetch_l2(pf, kXV);
       prefetch_l2(pf + kXV, kXUnit - kXV);
     };
-    auto wait = [&](int i, uint32_t parity) { return mbar_wait_abortable(bar(i), parity, kWaitLimit, abort_flag); };
+    // a busy wait (one thread), so the producer issues the moment an operand is ready
+    auto wait = [&](int i, uint32_t parity) { return mbar_wait_spin(bar(i), parity, kSpinWaitLimit, abort_flag); };
     if (n > 1) prefetch(1);
     load_x(0);
     load_yz(0);

@@ -212,6 +212,30 @@ __device__ __forceinline__ bool mbar_wait_abortable(uint32_t mbar, uint32_t pari
   return false;
 }
 
+// Wait as mbar_wait_abortable does, polling with the non-blocking test_wait
+// (a busy wait for one thread that must see the completion at once); checks
+// the abort flag every 256 polls; at most `limit` polls.
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t mbar, uint32_t parity, uint32_t limit,
+                                               volatile int *abort_flag) {
+  for (uint32_t i = 0; i < limit; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(done)
+        : "r"(mbar), "r"(parity)
+        : "memory");
+    if (done) {
+      asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+      return true;
+    }
+    if ((i & 255) == 255 && *abort_flag) return false;
+  }
+  *abort_flag = 1;
+  return false;
+}
+
 // Wait as mbar_wait_abortable does, but each poll lets the hardware suspend
 // the thread for up to 1 us until the phase completes (try_wait with a
 // suspend-time hint), so a completion is seen as soon as it happens without
