@@ -260,9 +260,10 @@ __global__ void __launch_bounds__(kThreads, kPrepCtasPerSm) gdn_prep_kernel(cons
     }
     cp_async_commit();
     cp_async_wait<0>();
-    // lambda = inclusive prefix sum of log alpha (two warps of 32 tokens)
+    // lambda = inclusive prefix sum of log2 alpha (two warps of 32 tokens; log2
+    // units, so every decay factor below is one ex2)
     if (warp < 2) {
-      float x = __logf(al[tid]);
+      float x = lg2_approx(al[tid]);
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const float y = __shfl_up_sync(kFull, x, o);
@@ -284,8 +285,8 @@ __global__ void __launch_bounds__(kThreads, kPrepCtasPerSm) gdn_prep_kernel(cons
     if (warp == 1) lam[tid] += lam[31];
     __syncthreads();
     if (tid < kC) {
-      gam[tid] = __expf(lam[tid]);
-      tail[tid] = __expf(lam[kC - 1] - lam[tid]);
+      gam[tid] = ex2_approx(lam[tid]);
+      tail[tid] = ex2_approx(lam[kC - 1] - lam[tid]);
     }
     __syncthreads();
     // Q tile to the workspace MN-major (8 tokens of one key per 16 bytes,
@@ -325,20 +326,26 @@ __global__ void __launch_bounds__(kThreads, kPrepCtasPerSm) gdn_prep_kernel(cons
       const float li = lam[i];
       const float bi = be[i];
       for (int j0 = half * 32; j0 < half * 32 + 32; j0 += 16) {
+        // a block of 16 columns above every row of the warp is skipped (warp-uniform)
+        const bool any = __any_sync(kFull, j0 <= i);
         float x[16];
-        tmem_ld16(tmem_addr(tmem, lane_base, kPColGP + j0), x);
-        tmem_ld_wait();
-        if (row < 64) {  // strictly lower part of L = I + A (the unit diagonal is implicit)
+        if (any) {
+          tmem_ld16(tmem_addr(tmem, lane_base, kPColGP + j0), x);
+          tmem_ld_wait();
+        }
+        if (row < 64) {  // strictly lower part of L = I + A (the solve reads no other entry)
+          if (any) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int j = j0 + e;
-            sA[i * kLd + j] = j < i ? bi * __expf(li - lam[j]) * x[e] : 0.f;
+            for (int e = 0; e < 16; ++e) {
+              const int j = j0 + e;
+              if (j < i) sA[i * kLd + j] = bi * ex2_approx(li - lam[j]) * x[e];
+            }
           }
         } else {  // Mq, lower part including the diagonal, to the workspace
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int j = j0 + e;
-            x[e] = j <= i ? __expf(li - lam[j]) * x[e] : 0.f;
+            x[e] = (any && j <= i) ? ex2_approx(li - lam[j]) * x[e] : 0.f;
           }
           store_split8(ws + kUMq, ws + kUMq + 8192, kmajor_off(i, j0, kC), x);
           store_split8(ws + kUMq, ws + kUMq + 8192, kmajor_off(i, j0 + 8, kC), x + 8);
