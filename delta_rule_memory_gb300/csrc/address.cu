@@ -329,7 +329,7 @@ Staircase make_staircase(int k, int W) {
 // One warp per row, persistent over rows.  E1 = score values per lane of a
 // half; E3 = per-lane candidates of the full k*k fallback (8 or 32).
 template <int E1, int E3>
-__global__ void __launch_bounds__(kAddrWarps * 32) address_kernel(const float *__restrict__ s1,
+__global__ void __launch_bounds__(kAddrWarps * 32, (E1 <= 8 && E3 <= 8) ? 4 : 1) address_kernel(const float *__restrict__ s1,
                                                                   const float *__restrict__ s2, long rows,
                                                                   int sqrtN, int k, int W, const Staircase sc,
                                                                   int32_t *__restrict__ idx_out,
@@ -464,17 +464,18 @@ __global__ void __launch_bounds__(kAddrWarps * 32) address_kernel(const float *_
 #pragma unroll
     for (int o = 0; o < 2; ++o) {
       const int r = lane + 32 * o;
-      ex[o] = (r < W) ? expf(key_value(ok[o]) - smax) : 0.f;
+      ex[o] = (r < W) ? __expf(key_value(ok[o]) - smax) : 0.f;
       part += ex[o];
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(kFull, part, off);
+    const float inv = 1.0f / part;
 #pragma unroll
     for (int o = 0; o < 2; ++o) {
       const int r = lane + 32 * o;
       if (r < W) {
         idx_out[row * W + r] = oi[o];
-        w_out[row * W + r] = ex[o] / part;
+        w_out[row * W + r] = ex[o] * inv;
       }
     }
   }
