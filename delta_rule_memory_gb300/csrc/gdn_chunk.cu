@@ -54,8 +54,8 @@ constexpr uint32_t kUKh = 65536;  // Khat hi, lo     [64 j][128 c]   16 KB each,
 constexpr uint32_t kUG = 98304;   // gamma_i         fp32 [64]
 constexpr uint32_t kUU = 98560;   // Ut = T V        fp32 [64 i][128 d]
 constexpr uint32_t kUnit = kUU + kC * kDV * 4;
-constexpr uint32_t kWBytes = kUMq - kUW;  // W and Q: one bulk copy (round 1 operands)
-constexpr uint32_t kMBytes = kUG - kUMq;  // Mq and Khat: one bulk copy (round 2 operands)
+constexpr uint32_t kWBytes = kUMq - kUW;  // W and Q: one bulk copy (phase 1 operands)
+constexpr uint32_t kMBytes = kUG - kUMq;  // Mq and Khat: one bulk copy (phase 2 operands)
 constexpr uint32_t kGBytes = kUU - kUG;   // gamma
 static_assert(kUnit % 16 == 0 && kWBytes % 16 == 0 && kMBytes % 16 == 0, "bulk copies need 16-byte multiples");
 
@@ -1298,13 +1298,13 @@ __global__ void __launch_bounds__(kKThreads, 1) kda_prep_kernel(const KdaPrepArg
 // columns of S^T in registers.  Warp 16 (producer, one lane) issues the bulk
 // copies and the MMAs.  Per chunk, the state's own chain first and the output
 // behind it (the tensor pipe runs one thread's MMAs in order):
-//   round 1  [X | Y1] = S0^T [W^T | Q^T] as one MMA group of N = 128,
+//   phase 1  [X | Y1] = S0^T [W^T | Q^T] as one MMA group of N = 128,
 //            issued in two column groups as the workers publish the bf16
 //            split of S0 (S_ready[g]); the next chunk's W and Q load as soon
 //            as it is done;
 //   workers  U^T = Ut^T - X, split, published (U_ready);
-//   round 2  D = U^T Khat; then Y2 = U^T Mq^T;
-//   workers  S^T <- gamma_C S^T + D, split for the next round 1; then
+//   phase 2  D = U^T Khat; then Y2 = U^T Mq^T;
+//   workers  S^T <- gamma_C S^T + D, split for the next phase 1; then
 //            y = gamma_i Y1 + Y2 (GDN) or Y1 + Y2 (KDA).
 // ===========================================================================
 struct ChainArgs {
@@ -1411,7 +1411,7 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
   unsigned char *sSh = sm + kCS, *sSl = sm + kCS + 32768;
   unsigned char *sUh = sm + kCU, *sUl = sm + kCU + 16384;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::cbar);
-  // barriers: 0 W, 1 M, 2-3 gamma buffers, 4 round 1 ([X | Y1]) done, 5 unused,
+  // barriers: 0 W, 1 M, 2-3 gamma buffers, 4 phase 1 ([X | Y1]) done, 5 unused,
   // 6 Y2 done (the chunk's last MMA), 7 D done, 8-9 S_ready[g], 10 U_ready, 11 drain
   auto bar = [&](int i) { return smem_addr(bars + i); };
   uint32_t *holder = reinterpret_cast<uint32_t *>(sm + L::cbar + kNBar * 8);
@@ -1484,7 +1484,7 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
       // this chunk's gammas (loaded long before; checked while D runs)
       if (!wwait(bar(2 + (c & 1)), static_cast<uint32_t>((c >> 1) & 1))) break;
       // S^T <- gamma_C S^T + D (KDA: gamma_C per key channel, i.e. per column
-      // of S^T), published group by group for the next round 1.  D completing
+      // of S^T), published group by group for the next phase 1.  D completing
       // also means Y1 (issued before it) no longer reads the published S.
       if (!wwait(bar(7), par)) break;
       const float *gbuf = reinterpret_cast<const float *>(sm + L::cg + (c & 1) * L::g_bytes);
@@ -1595,7 +1595,7 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
     for (int c = 0; c < n && ok; ++c) {
       const uint32_t par = static_cast<uint32_t>(c & 1);
       if (c + 2 < n) prefetch(c + 2);  // chunk c + 2 into L2 while this one runs
-      // round 1: [X | Y1] = S0^T [W^T | Q^T] as each column group g (k-steps
+      // phase 1: [X | Y1] = S0^T [W^T | Q^T] as each column group g (k-steps
       // g, g + 2, g + 4, g + 6) of S^T is published: S hi x [W hi; Q], S hi x
       // W lo (GDN, N = 64: Q is exact) or S hi x [W lo; Qt lo] (KDA), S lo x
       // [W hi; Q]
@@ -1621,7 +1621,7 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
         if (!ok) break;
         load(0, c + 1);
       }
-      // round 2: D = U^T Khat first (the state update waits for it), then
+      // phase 2: D = U^T Khat first (the state update waits for it), then
       // Y2 = U^T Mq^T
       ok = producer_wait(bar(1), par, abort_flag);
       if (ok) ++m_done;
