@@ -1,5 +1,6 @@
-"""The per-channel-decay chunk form that the tensor-core preparation and chain
-kernels implement (KDA: Linear Attention Architectures deck, "GDN and KDA
+"""The chunk forms that the tensor-core preparation and chain
+kernels implement (dense GDN, and the per-channel-decay form of KDA: Linear
+Attention Architectures deck, "GDN and KDA
 change the granularity of forgetting", Eqs. 18-20; GDN2: "GDN2 separates
 key-side erase and value-side write", Eqs. 21-24; the SSE delta write on each
 partition's visit subsequence), written out in numpy and checked against the
@@ -191,5 +192,45 @@ def test_sse_delta_chunk_form_matches_the_oracle(T, N, topk):
         Y[ts] += Yp
     Sr, Yr, _ = oracle.sse_scan(S0[None, None], route[None, :, None], topk, klog[None, :, None], q[None, :, None],
                                 v[None, :, None], al[None, :, None], oracle.SSE_WRITE_DELTA)
+    close(Y, Yr[0, :, 0])
+    close(S, Sr[0, 0])
+
+
+def gdn_chunk_step(S0, q, k, v, al, beta):
+    """The dense GDN chunk (a scalar decay per token; SDM deck App. A.1-A.2,
+    Eq. 7, dense case) as the GDN preparation and chain form it: with
+    gamma_i = e^{lambda_i}, A_ij = beta_i e^{lambda_i - lambda_j} k_i . k_j
+    (j < i), T = (I + A)^-1 diag(beta), W = T diag(gamma) K, Ut = T V,
+    U = Ut - W S0, Y = diag(gamma) Q S0 + Mq U (Mq_ij = e^{lambda_i -
+    lambda_j} q_i . k_j, j <= i), S_C = gamma_C S0 + Khat^T U (Khat_j =
+    e^{lambda_C - lambda_j} k_j)."""
+    lam = np.cumsum(np.log(al))
+    dec = np.exp(lam[:, None] - lam[None, :])
+    A = np.tril(beta[:, None] * dec * (k @ k.T), -1)
+    Mq = np.tril(dec * (q @ k.T))
+    T = np.linalg.inv(np.eye(C) + A) * beta[None, :]
+    gam = np.exp(lam)
+    W = T @ (gam[:, None] * k)
+    U = T @ v - W @ S0
+    Y = gam[:, None] * (q @ S0) + Mq @ U
+    S = gam[-1] * S0 + (np.exp(lam[-1] - lam)[:, None] * k).T @ U
+    return S, Y
+
+
+@pytest.mark.parametrize("T", [1, 64, 150])
+def test_gdn_chunk_form_matches_the_oracle(T):
+    dk, dv = 16, 12
+    S0, q, k, v, al, beta = inputs(T, dk, dv, seed=90 + T)
+    a = al[:, 0]  # one decay per token
+    S = np.array(S0)
+    Y = np.zeros((T, dv))
+    for t0 in range(0, T, C):
+        L = min(C, T - t0)
+        sl = slice(t0, t0 + L)
+        S, Yc = gdn_chunk_step(S, pad(q[sl], L, 0), pad(k[sl], L, 0), pad(v[sl], L, 0), pad(a[sl], L, 1),
+                               pad(beta[sl], L, 0))
+        Y[sl] = Yc[:L]
+    Sr, Yr = oracle.gdn_scan(S0[None, None], q[None, :, None], k[None, :, None], v[None, :, None],
+                             a[None, :, None], beta[None, :, None], False)
     close(Y, Yr[0, :, 0])
     close(S, Sr[0, 0])
