@@ -564,6 +564,21 @@ __device__ __forceinline__ void kda_level_operands(const unsigned char *sK, cons
   constexpr bool G2 = MODE == kModeGdn2;
   static_assert(kKThreads == 512, "four items per thread");
   const int w = (((tid >> 7) & 3) << 3) | (tid & 7), g = (tid >> 3) & 15;
+  // GDN2: the erase gates of this thread's two row items, loaded from global
+  // memory before any of the work that needs them
+  float4 gbr[2][2];
+  if (G2) {
+#pragma unroll
+    for (int ls = 0; ls < 2; ++ls) {
+      const int sh = 5 - (ls ? LB : LA), h = 1 << sh;
+      const int t = 2 * h * (w >> sh) + h + (w & (h - 1));
+      gbr[ls][0] = gbr[ls][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (t < nvalid) {
+        gbr[ls][0] = __ldg(reinterpret_cast<const float4 *>(gb + t * gstride + 8 * g));
+        gbr[ls][1] = __ldg(reinterpret_cast<const float4 *>(gb + t * gstride + 8 * g + 4));
+      }
+    }
+  }
 #pragma unroll 2
   for (int k = 0; k < 4; ++k) {
     const bool is_row = k < 2;
@@ -587,12 +602,8 @@ __device__ __forceinline__ void kda_level_operands(const unsigned char *sK, cons
 #pragma unroll
     for (int e = 0; e < 8; ++e) x[e] *= f[e];
     if (G2 && is_row) {
-      float bv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      if (t < nvalid) {
-        const float4 b0 = __ldg(reinterpret_cast<const float4 *>(gb + t * gstride + 8 * g));
-        const float4 b1 = __ldg(reinterpret_cast<const float4 *>(gb + t * gstride + 8 * g + 4));
-        bv[0] = b0.x; bv[1] = b0.y; bv[2] = b0.z; bv[3] = b0.w; bv[4] = b1.x; bv[5] = b1.y; bv[6] = b1.z; bv[7] = b1.w;
-      }
+      const float4 b0 = lsel ? gbr[1][0] : gbr[0][0], b1 = lsel ? gbr[1][1] : gbr[0][1];
+      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
       for (int e = 0; e < 8; ++e) x[e] *= bv[e];
     }
