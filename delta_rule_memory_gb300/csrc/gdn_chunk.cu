@@ -1169,7 +1169,21 @@ __global__ void __launch_bounds__(kKThreads, 1) kda_prep_kernel(const KdaPrepArg
     } else {
       // meanwhile (warps 8-15): Mq (lower, diagonal included) to the workspace
       // (8 consecutive threads take 8 consecutive rows: one contiguous
-      // 128-byte piece) ...
+      // 128-byte piece) ...  (GDN2: the erase gates of the thread's Et items
+      // are loaded first, so their latency passes under the Mq store)
+      float4 eb[4][2];
+      if (G2) {
+#pragma unroll
+        for (int s4 = 0; s4 < 4; ++s4) {
+          const int id = tid - 256 + s4 * (kKThreads - 256);
+          const int t = ((id >> 7) << 3) | (id & 7), g = (id >> 3) & 15;
+          eb[s4][0] = eb[s4][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (t < nvalid) {
+            eb[s4][0] = __ldg(reinterpret_cast<const float4 *>(gb + t * gstride + 8 * g));
+            eb[s4][1] = __ldg(reinterpret_cast<const float4 *>(gb + t * gstride + 8 * g + 4));
+          }
+        }
+      }
       for (int id = tid - 256; id < kC * 8; id += kKThreads - 256) {
         const int i = ((id >> 6) << 3) | (id & 7), j0 = ((id >> 3) & 7) * 8;
         float x[8];
@@ -1180,7 +1194,9 @@ __global__ void __launch_bounds__(kKThreads, 1) kda_prep_kernel(const KdaPrepArg
       }
       // ... and Kt = k (.) e^{lambda} (KDA) or Et = b (.) k (.) e^{lambda}
       // (GDN2), hi/lo operand tiles
-      for (int id = tid - 256; id < kC * 16; id += kKThreads - 256) {
+#pragma unroll
+      for (int s4 = 0; s4 < 4; ++s4) {
+        const int id = tid - 256 + s4 * (kKThreads - 256);
         const int t = ((id >> 7) << 3) | (id & 7), g = (id >> 3) & 15;
         const float4 t0v = *reinterpret_cast<const float4 *>(lam + t * kLdL + 8 * g);
         const float4 t1v = *reinterpret_cast<const float4 *>(lam + t * kLdL + 8 * g + 4);
@@ -1189,13 +1205,8 @@ __global__ void __launch_bounds__(kKThreads, 1) kda_prep_kernel(const KdaPrepArg
         load_k8<MODE>(sK, sKlo, t, 8 * g, kx);
         float bv[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
         if (G2) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) bv[e] = 0.f;
-          if (t < nvalid) {
-            const float4 b0 = __ldg(reinterpret_cast<const float4 *>(gb + t * gstride + 8 * g));
-            const float4 b1 = __ldg(reinterpret_cast<const float4 *>(gb + t * gstride + 8 * g + 4));
-            bv[0] = b0.x; bv[1] = b0.y; bv[2] = b0.z; bv[3] = b0.w; bv[4] = b1.x; bv[5] = b1.y; bv[6] = b1.z; bv[7] = b1.w;
-          }
+          bv[0] = eb[s4][0].x; bv[1] = eb[s4][0].y; bv[2] = eb[s4][0].z; bv[3] = eb[s4][0].w;
+          bv[4] = eb[s4][1].x; bv[5] = eb[s4][1].y; bv[6] = eb[s4][1].z; bv[7] = eb[s4][1].w;
         }
         float x[8];
 #pragma unroll
@@ -1204,6 +1215,20 @@ __global__ void __launch_bounds__(kKThreads, 1) kda_prep_kernel(const KdaPrepArg
       }
     }
     __syncthreads();
+    // GDN2: the write gates of the thread's two Z items, loaded before T is built
+    float4 zw[2][2];
+    if (G2) {
+#pragma unroll
+      for (int s2 = 0; s2 < 2; ++s2) {
+        const int id = tid + s2 * kKThreads;
+        const int t = ((id >> 7) << 3) | (id & 7), g = (id >> 3) & 15;
+        zw[s2][0] = zw[s2][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (t < nvalid) {
+          zw[s2][0] = __ldg(reinterpret_cast<const float4 *>(gw + t * static_cast<long>(H) * kDV + 8 * g));
+          zw[s2][1] = __ldg(reinterpret_cast<const float4 *>(gw + t * static_cast<long>(H) * kDV + 8 * g + 4));
+        }
+      }
+    }
     // T = L^-1 diag(beta) (KDA) or L^-1 (GDN2), lower triangle, hi/lo (8
     // consecutive threads take 8 consecutive rows: conflict-free stores)
     {
@@ -1220,16 +1245,14 @@ __global__ void __launch_bounds__(kKThreads, 1) kda_prep_kernel(const KdaPrepArg
       // Z = w (.) v, hi/lo K-major [64 t][128 d] into the solve buffers (free
       // once T is written): the MN-major A operand of Ut^T = Z^T T^T
       __syncthreads();
-      for (int id = tid; id < kC * 16; id += kKThreads) {
+#pragma unroll
+      for (int s2 = 0; s2 < 2; ++s2) {
+        const int id = tid + s2 * kKThreads;
         const int t = ((id >> 7) << 3) | (id & 7), g = (id >> 3) & 15;
         const uint4 raw = *reinterpret_cast<const uint4 *>(sV + kmajor_off(t, 8 * g, kDV));
         const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
-        float wv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        if (t < nvalid) {
-          const float4 w0 = __ldg(reinterpret_cast<const float4 *>(gw + t * static_cast<long>(H) * kDV + 8 * g));
-          const float4 w1 = __ldg(reinterpret_cast<const float4 *>(gw + t * static_cast<long>(H) * kDV + 8 * g + 4));
-          wv[0] = w0.x; wv[1] = w0.y; wv[2] = w0.z; wv[3] = w0.w; wv[4] = w1.x; wv[5] = w1.y; wv[6] = w1.z; wv[7] = w1.w;
-        }
+        const float wv[8] = {zw[s2][0].x, zw[s2][0].y, zw[s2][0].z, zw[s2][0].w,
+                             zw[s2][1].x, zw[s2][1].y, zw[s2][1].z, zw[s2][1].w};
         float x[8];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
