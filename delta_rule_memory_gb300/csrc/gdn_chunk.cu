@@ -579,7 +579,7 @@ __device__ __forceinline__ void kda_level_operands(const unsigned char *sK, cons
       }
     }
   }
-#pragma unroll 2
+#pragma unroll
   for (int k = 0; k < 4; ++k) {
     const bool is_row = k < 2;
     const int lsel = k & 1;                                            // 0: level LA, 1: level LB
