@@ -897,7 +897,7 @@ __global__ void __launch_bounds__(kKThreads, 1) kda_prep_kernel(const KdaPrepArg
       // kk = softmax of each visit's key logits, in place (a warp takes 4 rows,
       // a lane 4 channels); padding visits get kk = 0
       constexpr int kRowsPerWarp = kC / (kKThreads / 32);
-#pragma unroll 2
+#pragma unroll
       for (int e = 0; e < kRowsPerWarp; ++e) {
         const int i = kRowsPerWarp * warp + e;
         float4 *x = reinterpret_cast<float4 *>(lam + i * kLdL) + lane;

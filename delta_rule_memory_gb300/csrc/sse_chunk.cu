@@ -460,7 +460,7 @@ __global__ void __launch_bounds__(kPThreads, 2) sse_prep_kernel(const PrepArgs a
       for (int e = 0; e < 4; ++e)
 #pragma unroll
         for (int f = 0; f < 4; ++f) acc[e][f] = 0.f;
-#pragma unroll 2
+#pragma unroll
       for (int m = 0; m < 4; ++m) {
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
