@@ -590,7 +590,7 @@ class GpuRun:
         self.pre()
         self.main()
 
-    def e2e_step(self, chunk_T: int = 512):
+    def e2e_step(self, chunk_T: int = 384):
         """One step through the public API from host buffers: for the sparse
         workloads the native pipelined entry point sdm_forward_host (inputs
         copied in and y copied out per chunk, overlapped with compute); for the
@@ -855,7 +855,7 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=0, help="tokens per sampled sequence for the oracle")
     ap.add_argument("--cpu-cores", type=int, default=0)
     ap.add_argument("--batch", type=int, default=0, help="override B (small cases for profiling only)")
-    ap.add_argument("--e2e-chunk", type=int, default=512,
+    ap.add_argument("--e2e-chunk", type=int, default=384,
                     help="tokens per pipelined chunk of the end-to-end sparse step (sdm_forward_host chunk_T)")
     ap.add_argument("--overlap-addressing", action="store_true",
                     help="sparse inference step: run step s+1's addressing on a second stream during step s's "
