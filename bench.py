@@ -44,16 +44,16 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 NCU_TRAFFIC = {
     # one full-size sparse scan launch: 8.01 GB read + 4.19 GB written
     ("sdm_14b_layer", "sdm"): {"bytes": 12.20e9, "digest": "8821957384b6"},
-    # both kernels of one full-size gdn_scan call: 746.0 MB read + 592.3 MB written
-    ("gdn", "gdn"): {"bytes": 1.338e9, "digest": "ac9e67db8d6f"},
-    # both kernels of one full-size KDA gdn_scan call: 947.3 MB read + 664.0 MB written
-    ("kda", "kda"): {"bytes": 1.611e9, "digest": "ac9e67db8d6f"},
-    # both kernels of one full-size gdn2_scan call: 1214.8 MB read + 675.2 MB written
-    ("gdn2", "gdn2"): {"bytes": 1.890e9, "digest": "ac9e67db8d6f"},
+    # both kernels of one full-size gdn_scan call: 746.1 MB read + 591.4 MB written
+    ("gdn", "gdn"): {"bytes": 1.338e9, "digest": "d778d873446b"},
+    # both kernels of one full-size KDA gdn_scan call: 947.1 MB read + 663.3 MB written
+    ("kda", "kda"): {"bytes": 1.610e9, "digest": "d778d873446b"},
+    # both kernels of one full-size gdn2_scan call: 1214.7 MB read + 674.1 MB written
+    ("gdn2", "gdn2"): {"bytes": 1.889e9, "digest": "d778d873446b"},
     # the five kernels of one full-size sse_scan call on the chunked path: 1.073 GB read + 0.808 GB written
     ("sse", "sse"): {"bytes": 1.881e9, "digest": "b0880e3053d9"},
-    # the five kernels of one full-size delta-write sse_scan call: 1.452 GB read + 1.116 GB written
-    ("sse_delta", "sse"): {"bytes": 2.568e9, "digest": "ac9e67db8d6f"},
+    # the five kernels of one full-size delta-write sse_scan call: 1.449 GB read + 1.114 GB written
+    ("sse_delta", "sse"): {"bytes": 2.563e9, "digest": "d778d873446b"},
 }
 
 

@@ -15,18 +15,24 @@
 //                      triangular inverse, T, then W and Ut by MMA, Mq and
 //                      Khat, written to the workspace as ready-made operand
 //                      tiles of the second kernel.
-//   gdn_chain_kernel - one CTA per (batch, head), chunk after chunk: two
-//                      rounds of MMAs on the state (S^T, d_v x d_k, fp32,
-//                      held in the registers of the worker warps), fed by a
-//                      producer warp; the next chunk's tiles stream in with
-//                      bulk asynchronous copies meanwhile.
-// Every state contraction is written transposed so that its M is d_v = 128.
+//   gdn_chain_pair_kernel - two CTAs per (batch, head), each owning 64 of
+//                      the value columns, chunk after chunk: two rounds of
+//                      MMAs on the state (fp32, held in the registers of the
+//                      worker warps), fed by a producer warp; the next
+//                      chunk's tiles stream in with bulk asynchronous copies
+//                      meanwhile.  Every contraction has M = 128 (tokens of
+//                      [W; Q], or key channels) and N = 64 (the columns).
+//   gdn_chain_kernel - the same chain on one CTA per (batch, head), taken
+//                      when the pairs would not all be resident at once;
+//                      there every state contraction is written transposed
+//                      so that its M is d_v = 128.
 // Operands that are not exact in bf16 (state, U, T, W, Mq, Khat) are split
 // into bf16 hi + lo and multiplied as hi*hi + hi*lo + lo*hi, which keeps
 // fp32-level accuracy.  Decay ratios are always formed as exp(l_i - l_j) with
 // j <= i.
 #include <climits>
 #include <cstdlib>
+#include <cstring>
 
 #include "common.cuh"
 #include "sse_group.cuh"
@@ -77,7 +83,6 @@ struct PrepArgs {
   const uint16_t *q, *k, *v;
   const float *alpha, *beta;
   unsigned char *ws;
-  float *gC;  // gamma_C of every chunk
   int T, H, nchunks;
   long units;  // B * H * nchunks
   int32_t *err;
@@ -388,7 +393,6 @@ __global__ void __launch_bounds__(kThreads, kPrepCtasPerSm) gdn_prep_kernel(cons
       mma_commit(mbW);
     }
     if (tid < kC) reinterpret_cast<float *>(ws + kUG)[tid] = gam[tid];
-    if (tid == 0) a.gC[u] = gam[kC - 1];
     if (!wait_ok(mbW, par)) { failed = true; break; }
     // Ut[i][d] to the workspace (thread d: coalesced over d); W (lane c,
     // tokens i) as the MN-major B operand of the chain: 8 consecutive i of
@@ -1344,7 +1348,6 @@ __global__ void __launch_bounds__(kKThreads, 1) kda_prep_kernel(const KdaPrepArg
 struct ChainArgs {
   float *state;
   const unsigned char *ws;
-  const float *gC;
   float *y;
   int T, H, nchunks;
   // SSE delta only: the group tables, units per (batch, head), routed
@@ -1498,7 +1501,6 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
     for (int c = 0; c < n; ++c) {
       const uint32_t par = static_cast<uint32_t>(c & 1);
       const bool last = c + 1 == n;
-      const float gc = KDA ? 0.f : __ldg(a.gC + u0 + c);
       // U^T = Ut^T - X for this warp's 16 tokens
       if (!wwait(bar(4), par)) break;
       {
@@ -1529,7 +1531,8 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
           tmem_ld16(lanes + kColD + 32 * qtr + 16 * g, x);
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 16; ++e) S[16 * g + e] = fmaf(KDA ? gbuf[32 * qtr + 16 * g + e] : gc, S[16 * g + e], x[e]);
+          for (int e = 0; e < 16; ++e)
+            S[16 * g + e] = fmaf(gbuf[KDA ? 32 * qtr + 16 * g + e : kC - 1], S[16 * g + e], x[e]);
           if (!last) publish_s(g);
         }
       } else {
@@ -1703,13 +1706,337 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
   if (warp == 0) tmem_dealloc(tmem, kChainTmemCols);
 }
 
+
+// ===========================================================================
+// Kernel 2, split by value columns: the chain of one (batch, head) on a pair
+// of CTAs, CTA h of the pair owning value columns [64h, 64h + 64).  Each
+// value column evolves independently, so the two CTAs never communicate.
+// The products are turned so that every MMA has M = 128 and N = 64 (the
+// CTA's columns):
+//   phase 1  [X; Y1] = [W; Q] S0      A = [W; Q] (128 tokens, MN-major from the
+//                                      unit), B = S0 (d_k x 64, MN-major);
+//   workers  U = Ut - X (token rows, warps of lanes 0-63), split, published;
+//   phase 2  D = Khat^T U              A = Khat^T (MN-major from the unit);
+//            Y2 = [0; Mq] U            A = Mq below 64 zero rows, so Y2 lands
+//                                      in the lanes of Y1;
+//   workers  S <- gamma_C S + D (all 16 warps, lane = key channel), split for
+//            the next phase 1; y = gamma_i Y1 + Y2 (GDN) or Y1 + Y2 (KDA) on
+//            the warps of lanes 64-127.
+// Against one CTA per (b, h) this halves the state update per thread and
+// gives the output to the warps that have no U to form.
+// ===========================================================================
+constexpr uint32_t kQS = 0;              // S hi, lo [128 c][64 d] MN-major      2 x 16 KB
+constexpr uint32_t kQU = kQS + 32768;    // U hi, lo [64 i][64 d] MN-major       2 x 8 KB
+constexpr uint32_t kQW = kQU + 16384;    // W hi | Q (Qt) hi | W lo | Qt lo (KDA) or zeros (GDN)   64 KB
+constexpr uint32_t kQM = kQW + 65536;    // zeros | Mq hi | zeros | Mq lo | Khat hi | Khat lo        64 KB
+constexpr uint32_t kQG = kQM + 65536;    // gammas, two buffers
+constexpr uint32_t kQColXY = 0;          // [X; Y1] [128 x 64], two buffers by chunk parity
+constexpr uint32_t kQColD = 128;         // D       [128 c x 64 d]
+constexpr uint32_t kQColY2 = 192;        // Y2      [128 x 64] (rows 64-127), two buffers
+constexpr uint32_t kQTmemCols = 512;
+template <int CM>
+struct PairLayout {
+  static constexpr bool KDA = CM == 1;
+  static constexpr uint32_t unit = KDA ? kVUnit : kUnit;
+  static constexpr uint32_t w_off = KDA ? kVW : kUW;
+  static constexpr uint32_t w_bytes = KDA ? kVMq - kVW : kWBytes;    // 64 KB (KDA) or 48 KB (GDN)
+  static constexpr uint32_t m_off = KDA ? kVMq : kUMq;               // Mq hi, Mq lo, Khat hi, Khat lo
+  static constexpr uint32_t m_bytes = KDA ? kVG - kVMq : kMBytes;    // 48 KB
+  static constexpr uint32_t g_off = KDA ? kVG : kUG;
+  static constexpr uint32_t g_bytes = KDA ? kVU - kVG : kGBytes;
+  static constexpr uint32_t u_off = KDA ? kVU : kUU;
+  static constexpr uint32_t cbar = kQG + 2 * g_bytes;
+  static constexpr uint32_t smem = cbar + kNBar * 8 + 16;
+  static_assert(m_bytes == 49152 && w_bytes <= 65536, "unit regions");
+  static_assert(smem <= 227 * 1024 && smem > 114 * 1024, "one pair CTA per SM (its 512 tensor-memory columns)");
+};
+// MN-major tile of 64 columns (S: rows = key channels, U: rows = tokens):
+// 8 consecutive columns per 16 bytes, 8-row groups 1024 bytes apart
+__device__ __forceinline__ uint32_t mn64_off(int r, int d) {
+  return static_cast<uint32_t>((r >> 3) * 1024 + (d >> 3) * 128 + (r & 7) * 16 + (d & 7) * 2);
+}
+
+template <int CM>
+__global__ void __maxnreg__(96) gdn_chain_pair_kernel(const ChainArgs a) {
+  using L = PairLayout<CM>;
+  constexpr bool KDA = CM == 1;
+  extern __shared__ __align__(1024) unsigned char sm[];
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int T = a.T, H = a.H;
+  const long bh = blockIdx.x >> 1;
+  const int d0 = 64 * static_cast<int>(blockIdx.x & 1);  // this CTA's value columns
+  const int n = a.nchunks;
+  const long u0 = bh * n;
+  float *gS = a.state + bh * kDK * kDV;
+  const long tok0 = (bh / H) * T * H + bh % H;
+
+  unsigned char *sSh = sm + kQS, *sSl = sm + kQS + 16384;
+  unsigned char *sUh = sm + kQU, *sUl = sm + kQU + 8192;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::cbar);
+  // barriers: 0 W, 1 M, 2-3 gamma buffers, 4 phase 1 done, 6 Y2 done (the
+  // chunk's last MMA), 7 D done, 8-9 S_ready[g] (key channels 64g..64g+63),
+  // 10 U_ready, 11 drain
+  auto bar = [&](int i) { return smem_addr(bars + i); };
+  uint32_t *holder = reinterpret_cast<uint32_t *>(sm + L::cbar + kNBar * 8);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::cbar + kNBar * 8 + 4);
+
+  if (tid == 0) {
+    for (int i = 0; i < 8; ++i) mbar_init(bar(i), 1);
+    for (int i = 8; i < 11; ++i) mbar_init(bar(i), kWorkers / 64);  // one arrival per worker warp of the half
+    mbar_init(bar(11), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(smem_addr(holder), kQTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *holder;
+
+  if (warp < kWorkers / 32) {
+    // ------------------------------------------------------------ workers
+    // warp w: tensor-memory lanes 32 q .. 32 q + 31 (q = w % 4), value columns
+    // 16 qtr .. 16 qtr + 15 of the CTA's 64 (qtr = w / 4)
+    const int q = warp & 3, qtr = warp >> 2;
+    const int row = 32 * q + lane;  // key channel (state), token (q < 2: X) or token + 64 (q >= 2: Y)
+    const int dc = 16 * qtr;        // first of this thread's 16 columns
+    const uint32_t lanes = tmem + (static_cast<uint32_t>(32 * q) << 16);
+    auto wwait = [&](uint32_t mb, uint32_t parity) -> bool {
+      return __all_sync(kFull, chain_wait(mb, parity, abort_flag)) != 0;
+    };
+    // zero rows of the operand regions that no copy writes: above Mq hi and
+    // Mq lo (Y2's A), and (GDN) the Q lo slot of phase 1's lo pass
+    {
+      uint4 *z0 = reinterpret_cast<uint4 *>(sm + kQM), *z1 = reinterpret_cast<uint4 *>(sm + kQM + 16384);
+      for (int i = tid; i < 512; i += kWorkers) z0[i] = z1[i] = make_uint4(0u, 0u, 0u, 0u);
+      if (!KDA) {
+        uint4 *z2 = reinterpret_cast<uint4 *>(sm + kQW + 49152);
+        for (int i = tid; i < 1024; i += kWorkers) z2[i] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    float S[16];  // S[row][d0 + dc + e]
+    {
+      const float4 *src = reinterpret_cast<const float4 *>(gS + static_cast<long>(row) * kDV + d0 + dc);
+#pragma unroll
+      for (int e4 = 0; e4 < 4; ++e4) {
+        const float4 x = src[e4];
+        S[4 * e4] = x.x;
+        S[4 * e4 + 1] = x.y;
+        S[4 * e4 + 2] = x.z;
+        S[4 * e4 + 3] = x.w;
+      }
+    }
+    // the bf16 split of this thread's 16 state columns, released by one
+    // arrival per warp on S_ready[q / 2]
+    auto publish_s = [&]() {
+      store_split8(sSh, sSl, mn64_off(row, dc), S);
+      store_split8(sSh, sSl, mn64_off(row, dc + 8), S + 8);
+      fence_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(8 + (q >> 1)));
+    };
+    publish_s();
+    float ut[16];  // Ut[row][d0 + dc + e] of the next chunk (q < 2)
+    auto load_ut = [&](int c) {
+      const float4 *src = reinterpret_cast<const float4 *>(
+          reinterpret_cast<const float *>(a.ws + (u0 + c) * L::unit + L::u_off) + static_cast<long>(row) * kDV + d0 + dc);
+#pragma unroll
+      for (int e4 = 0; e4 < 4; ++e4) {
+        const float4 x = __ldg(src + e4);
+        ut[4 * e4] = x.x;
+        ut[4 * e4 + 1] = x.y;
+        ut[4 * e4 + 2] = x.z;
+        ut[4 * e4 + 3] = x.w;
+      }
+    };
+    if (q < 2) load_ut(0);
+    for (int c = 0; c < n; ++c) {
+      const uint32_t par = static_cast<uint32_t>(c & 1);
+      const bool last = c + 1 == n;
+      if (q < 2) {
+        // U = Ut - X for token `row`
+        if (!wwait(bar(4), par)) break;
+        float x[16];
+        tmem_ld16(lanes + kQColXY + 64 * (c & 1) + dc, x);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) x[e] = ut[e] - x[e];
+        store_split8(sUh, sUl, mn64_off(row, dc), x);
+        store_split8(sUh, sUl, mn64_off(row, dc + 8), x + 8);
+        fence_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(10));
+        if (!last) load_ut(c + 1);
+      }
+      // this chunk's gammas (loaded long before)
+      if (!wwait(bar(2 + (c & 1)), static_cast<uint32_t>((c >> 1) & 1))) break;
+      const float *gbuf = reinterpret_cast<const float *>(sm + kQG + (c & 1) * L::g_bytes);
+      // GDN's gamma_i of this thread's output token, read before the state is
+      // published (the buffer is refilled two chunks on)
+      const float gi = (!KDA && q >= 2) ? gbuf[row - 64] : 1.f;
+      // S <- gamma_C S + D; D completing also means phase 1 no longer reads S
+      if (!wwait(bar(7), par)) break;
+      {
+        float x[16];
+        tmem_ld16(lanes + kQColD + dc, x);
+        tmem_ld_wait();
+        const float g = gbuf[KDA ? row : kC - 1];  // KDA: gamma_C per key channel; GDN: gamma of the chunk's last token
+#pragma unroll
+        for (int e = 0; e < 16; ++e) S[e] = fmaf(g, S[e], x[e]);
+      }
+      if (!last) {
+        publish_s();
+      } else {
+        float4 *dst = reinterpret_cast<float4 *>(gS + static_cast<long>(row) * kDV + d0 + dc);
+#pragma unroll
+        for (int e4 = 0; e4 < 4; ++e4) dst[e4] = make_float4(S[4 * e4], S[4 * e4 + 1], S[4 * e4 + 2], S[4 * e4 + 3]);
+      }
+      if (q >= 2) {
+        // y = gamma_i Y1 + Y2 (GDN) or Y1 + Y2 (KDA: the decay is inside Qt)
+        if (!wwait(bar(6), par)) break;
+        float y1[16], y2[16];
+        tmem_ld16(lanes + kQColXY + 64 * (c & 1) + dc, y1);
+        tmem_ld16(lanes + kQColY2 + 64 * (c & 1) + dc, y2);
+        tmem_ld_wait();
+        const int t = c * kC + row - 64;
+        if (t < T) {
+          float4 *yp = reinterpret_cast<float4 *>(a.y + (tok0 + static_cast<long>(t) * H) * kDV + d0 + dc);
+#pragma unroll
+          for (int e4 = 0; e4 < 4; ++e4) {
+            float o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[e] = KDA ? y1[4 * e4 + e] + y2[4 * e4 + e] : fmaf(gi, y1[4 * e4 + e], y2[4 * e4 + e]);
+            yp[e4] = make_float4(o[0], o[1], o[2], o[3]);
+          }
+        }
+      }
+    }
+  } else if (tid == kWorkers) {
+    // ------------------------------------------------------------ producer
+    const uint32_t wh = smem_addr(sm + kQW), wl = wh + 32768;  // [W hi; Q hi], [W lo; Qt lo or zeros]
+    const uint32_t mz = smem_addr(sm + kQM);                    // zeros | Mq hi | zeros | Mq lo | Khat hi | Khat lo
+    const uint32_t kh = mz + 32768, kl = mz + 49152;
+    // phase 1: A [W; Q] MN-major (LBO 128 along key channels, SBO 2048 along
+    // tokens), B = S MN-major (LBO 1024 along key channels, SBO 128 along
+    // value columns); a k-step of 16 key channels advances A 256 bytes, B 2048
+    const uint64_t dAh = smem_desc(wh, 128, 2048), dAl = smem_desc(wl, 128, 2048);
+    const uint64_t dSh = smem_desc(smem_addr(sSh), 1024, 128), dSl = smem_desc(smem_addr(sSl), 1024, 128);
+    // phase 2: A = Khat^T MN-major (LBO 2048 along tokens, SBO 128 along key
+    // channels; a k-step of 16 tokens advances 4096 bytes); A = [0; Mq]
+    // K-major (LBO 128, SBO 1024; 256 bytes a k-step), starting 64 zero rows
+    // (8 KB) above Mq; B = U MN-major (LBO 1024, SBO 128; 2048 bytes a k-step)
+    const uint64_t dKh = smem_desc(kh, 2048, 128), dKl = smem_desc(kl, 2048, 128);
+    const uint64_t dMh = smem_desc(mz, 128, 1024), dMl = smem_desc(mz + 16384, 128, 1024);
+    const uint64_t dUh = smem_desc(smem_addr(sUh), 1024, 128), dUl = smem_desc(smem_addr(sUl), 1024, 128);
+    const uint32_t idMM = idesc_bf16_f32(128, 64) | (1u << 15) | (1u << 16);  // A and B MN-major
+    const uint32_t idKM = idesc_bf16_f32(128, 64) | (1u << 16);                // A K-major, B MN-major
+    int w_issued = 0, w_done = 0, m_issued = 0, m_done = 0, g_issued = 0;
+    auto load = [&](int which, int c) {
+      const unsigned char *src = a.ws + (u0 + c) * L::unit;
+      fence_async_smem();
+      if (which == 0) {
+        mbar_expect_tx(bar(0), L::w_bytes);
+        bulk_g2s(wh, src + L::w_off, L::w_bytes, bar(0));
+        ++w_issued;
+      } else {
+        // Mq hi below its zero rows; Mq lo, Khat hi and Khat lo (contiguous in
+        // the unit) below the second zero rows
+        mbar_expect_tx(bar(1), L::m_bytes);
+        bulk_g2s(mz + 8192, src + L::m_off, 8192, bar(1));
+        bulk_g2s(mz + 24576, src + L::m_off + 8192, L::m_bytes - 8192, bar(1));
+        mbar_expect_tx(bar(2 + (c & 1)), L::g_bytes);
+        bulk_g2s(smem_addr(sm + kQG + (c & 1) * L::g_bytes), src + L::g_off, L::g_bytes, bar(2 + (c & 1)));
+        ++m_issued;
+        ++g_issued;
+      }
+    };
+    auto prefetch = [&](int c) {
+      const unsigned char *pf = a.ws + (u0 + c) * L::unit;
+      prefetch_l2(pf + L::w_off, L::w_bytes / 2);
+      prefetch_l2(pf + L::w_off + L::w_bytes / 2, L::w_bytes / 2);
+      prefetch_l2(pf + L::m_off, L::m_bytes + L::g_bytes);
+      prefetch_l2(pf + L::u_off, L::unit - L::u_off);
+    };
+    if (n > 1) prefetch(1);
+    load(0, 0);
+    load(1, 0);
+    bool ok = true;
+    for (int c = 0; c < n && ok; ++c) {
+      const uint32_t par = static_cast<uint32_t>(c & 1);
+      if (c + 2 < n) prefetch(c + 2);
+      // phase 1, key channels 64 g .. 64 g + 63 (k-steps 4 g .. 4 g + 3) as
+      // their half of S is published: A hi x S hi, A lo x S hi, A hi x S lo
+      const uint32_t xy = tmem + kQColXY + 64 * (c & 1);
+      ok = producer_wait(bar(0), par, abort_flag);
+      if (ok) ++w_done;
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        if (ok) ok = producer_wait(bar(8 + g), par, abort_flag);
+        if (!ok) break;
+#pragma unroll
+        for (int ks = 4 * g; ks < 4 * g + 4; ++ks) {
+          mma_bf16(xy, dAh + 16u * ks, dSh + 128u * ks, idMM, ks != 0);
+          mma_bf16(xy, dAl + 16u * ks, dSh + 128u * ks, idMM, true);
+          mma_bf16(xy, dAh + 16u * ks, dSl + 128u * ks, idMM, true);
+        }
+      }
+      if (!ok) break;
+      if (!(a.drop_signal && c == 0)) mma_commit(bar(4));
+      if (c + 1 < n) {
+        ok = producer_wait(bar(4), par, abort_flag);
+        if (!ok) break;
+        load(0, c + 1);
+      }
+      // phase 2: D = Khat^T U (the state update waits for it), then Y2
+      ok = producer_wait(bar(1), par, abort_flag);
+      if (ok) ++m_done;
+      if (ok) ok = producer_wait(bar(10), par, abort_flag);
+      if (!ok) break;
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        mma_bf16(tmem + kQColD, dKh + 256u * ks, dUh + 128u * ks, idMM, ks != 0);
+        mma_bf16(tmem + kQColD, dKl + 256u * ks, dUh + 128u * ks, idMM, true);
+        mma_bf16(tmem + kQColD, dKh + 256u * ks, dUl + 128u * ks, idMM, true);
+      }
+      mma_commit(bar(7));
+      const uint32_t y2 = tmem + kQColY2 + 64 * (c & 1);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        mma_bf16(y2, dMh + 16u * ks, dUh + 128u * ks, idKM, ks != 0);
+        mma_bf16(y2, dMl + 16u * ks, dUh + 128u * ks, idKM, true);
+        mma_bf16(y2, dMh + 16u * ks, dUl + 128u * ks, idKM, true);
+      }
+      mma_commit(bar(6));
+      if (c + 1 < n) {
+        ok = producer_wait(bar(6), par, abort_flag);
+        if (ok) load(1, c + 1);
+      }
+    }
+    mma_commit(bar(11));
+    mbar_wait(bar(11), 0, kWaitLimit);
+    if (w_done < w_issued) mbar_wait(bar(0), static_cast<uint32_t>((w_issued - 1) & 1), kWaitLimit);
+    if (m_done < m_issued) mbar_wait(bar(1), static_cast<uint32_t>((m_issued - 1) & 1), kWaitLimit);
+    for (int gb = 0; gb < 2; ++gb) {
+      const int loads = (g_issued + 1 - gb) / 2;
+      if (loads > 0) mbar_wait(bar(2 + gb), static_cast<uint32_t>((loads - 1) & 1), kWaitLimit);
+    }
+    if (!ok) *abort_flag = 1;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0 && *abort_flag) report_timeout(a.err);
+  if (warp == 0) tmem_dealloc(tmem, kQTmemCols);
+}
+
 }  // namespace
 
-// workspace of the chunked GDN path: one unit of tiles per chunk, then gamma_C
-// of every chunk
+// workspace of the chunked GDN path: one unit of tiles per chunk
 size_t gdn_chunk_workspace_size(int B, int T, int H) {
   const long units = static_cast<long>(B) * H * ((T + kC - 1) / kC);
-  const size_t n = static_cast<size_t>(units) * (kUnit + sizeof(float));
+  const size_t n = static_cast<size_t>(units) * kUnit;
   return (n + 255) & ~static_cast<size_t>(255);
 }
 
@@ -1722,6 +2049,16 @@ int test_drop_signal() {
   return (s && s[0] == '1') ? 1 : 0;
 }
 
+// The chain's form: a CTA pair per (b, h) (value columns split) when every
+// pair is resident at once, else one CTA per (b, h).  SDM_GDN_CHAIN=single or
+// =pair forces one form (read per call).
+bool chain_in_pairs(long bh, int sms) {
+  const char *s = getenv("SDM_GDN_CHAIN");
+  if (s && strcmp(s, "single") == 0) return false;
+  if (s && strcmp(s, "pair") == 0) return true;
+  return 2 * bh <= sms;
+}
+
 // launched by gdn_scan for dense GDN with d_k = d_v = 128
 int launch_gdn_chunk(float *state, const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
                      const float *beta, int B, int T, int H, float *y, void *workspace, int32_t *err,
@@ -1729,7 +2066,6 @@ int launch_gdn_chunk(float *state, const uint16_t *q, const uint16_t *k, const u
   const int nchunks = (T + kC - 1) / kC;
   const long units = static_cast<long>(B) * H * nchunks;
   unsigned char *ws = static_cast<unsigned char *>(workspace);
-  float *gC = reinterpret_cast<float *>(ws + static_cast<size_t>(units) * kUnit);
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -1741,7 +2077,6 @@ int launch_gdn_chunk(float *state, const uint16_t *q, const uint16_t *k, const u
   pa.alpha = alpha;
   pa.beta = beta;
   pa.ws = ws;
-  pa.gC = gC;
   pa.T = T;
   pa.H = H;
   pa.nchunks = nchunks;
@@ -1759,18 +2094,26 @@ int launch_gdn_chunk(float *state, const uint16_t *q, const uint16_t *k, const u
   ChainArgs ca{};
   ca.state = state;
   ca.ws = ws;
-  ca.gC = gC;
   ca.y = y;
   ca.T = T;
   ca.H = H;
   ca.nchunks = nchunks;
   ca.err = err;
   ca.drop_signal = test_drop_signal();
+  const long bh = static_cast<long>(B) * H;
+  if (chain_in_pairs(bh, sms)) {
+    constexpr uint32_t pair_smem = PairLayout<0>::smem;
+    if (cudaFuncSetAttribute(gdn_chain_pair_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(pair_smem)) != cudaSuccess)
+      return check_launch("gdn_scan: set shared memory");
+    gdn_chain_pair_kernel<0><<<static_cast<unsigned>(2 * bh), kChainThreads, pair_smem, st>>>(ca);
+    return check_launch("gdn_scan: chunk chain kernel");
+  }
   constexpr uint32_t chain_smem = ChainLayout<0>::smem;
   if (cudaFuncSetAttribute(gdn_chain_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(chain_smem)) != cudaSuccess)
     return check_launch("gdn_scan: set shared memory");
-  gdn_chain_kernel<0><<<static_cast<unsigned>(static_cast<long>(B) * H), kChainThreads, chain_smem, st>>>(ca);
+  gdn_chain_kernel<0><<<static_cast<unsigned>(bh), kChainThreads, chain_smem, st>>>(ca);
   return check_launch("gdn_scan: chunk chain kernel");
 }
 
@@ -1826,18 +2169,26 @@ int launch_kda_chunk(float *state, const uint16_t *q, const uint16_t *k, const u
   ChainArgs ca{};
   ca.state = state;
   ca.ws = ws;
-  ca.gC = nullptr;
   ca.y = y;
   ca.T = T;
   ca.H = H;
   ca.nchunks = nchunks;
   ca.err = err;
   ca.drop_signal = test_drop_signal();
+  const long bh = static_cast<long>(B) * H;
+  if (chain_in_pairs(bh, sms)) {
+    constexpr uint32_t pair_smem = PairLayout<1>::smem;
+    if (cudaFuncSetAttribute(gdn_chain_pair_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(pair_smem)) != cudaSuccess)
+      return check_launch("gdn_scan: set shared memory");
+    gdn_chain_pair_kernel<1><<<static_cast<unsigned>(2 * bh), kChainThreads, pair_smem, st>>>(ca);
+    return check_launch(g2 ? "gdn2_scan: chunk chain kernel" : "gdn_scan: KDA chunk chain kernel");
+  }
   constexpr uint32_t chain_smem = ChainLayout<1>::smem;
   if (cudaFuncSetAttribute(gdn_chain_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(chain_smem)) != cudaSuccess)
     return check_launch("gdn_scan: set shared memory");
-  gdn_chain_kernel<1><<<static_cast<unsigned>(static_cast<long>(B) * H), kChainThreads, chain_smem, st>>>(ca);
+  gdn_chain_kernel<1><<<static_cast<unsigned>(bh), kChainThreads, chain_smem, st>>>(ca);
   return check_launch(g2 ? "gdn2_scan: chunk chain kernel" : "gdn_scan: KDA chunk chain kernel");
 }
 

@@ -358,7 +358,7 @@ SDM_API int sdm_scan_backward(float *state, float *dstate, const void *v, int v_
 /*
  * Scratch bytes gdn_scan needs.  At dk = dv = 128 (the chunked tensor-core
  * path) one tile set per chunk of 64 tokens (the operands of the
- * state-dependent products): GDN 131,328 bytes plus 4, KDA 147,968 bytes,
+ * state-dependent products): GDN 131,328 bytes, KDA 147,968 bytes,
  * rounded up to 256 (about 2.1 / 2.3 KB per token-head).  Every other shape
  * and SDM_GDN_PATH=recurrent need none (0).
  */
@@ -387,8 +387,10 @@ SDM_API size_t gdn_scan_workspace_size(int B, int T, int H, int dk, int dv, int 
  * Kernels: GDN and KDA with dk = dv = 128 run chunkwise (64 tokens) on the
  *          tensor cores ([SDM] App. A.1-A.2, Eq. 7, dense case): a kernel
  *          parallel over all chunks prepares each chunk's state-independent
- *          operands in the workspace, then one CTA per (batch, head) runs the
- *          chunks in order with the state in registers.  KDA's per-channel
+ *          operands in the workspace, then two CTAs per (batch, head), each
+ *          owning half of the value columns, run the chunks in order with the
+ *          state in registers (one CTA per (batch, head) when 2*B*H exceeds
+ *          the SM count; SDM_GDN_CHAIN=pair|single forces one form).  KDA's per-channel
  *          decays sit inside the chunk's pair sums; each pair's decay is
  *          formed as a product of two decay ratios of at most 1 about a
  *          segment boundary, never with an inverse decay.  alpha must lie in

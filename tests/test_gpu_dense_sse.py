@@ -51,14 +51,17 @@ def test_gdn_full_size_sampled(per_channel):
         assert_state_close(S[b:b + 1, h:h + 1], Sr, what=f"state[{b},{h}]")
 
 
+@pytest.mark.parametrize("chain", ["pair", "single"])
 @pytest.mark.parametrize("per_channel", [False, True], ids=["gdn", "kda"])
 @pytest.mark.parametrize("T", [1, 63, 64, 65, 200, 512, 700])
-def test_gdn_chunked_path_lengths(T, per_channel, monkeypatch):
+def test_gdn_chunked_path_lengths(T, per_channel, chain, monkeypatch):
     """Dense GDN and KDA at d_k = d_v = 128 run chunkwise (64 tokens) on the
     tensor cores: lengths below, at and across a chunk boundary, nonzero
-    state, and longer sequences of 8 and 11 chunks."""
+    state, and longer sequences of 8 and 11 chunks; the chain on a CTA pair
+    per (b, h) (value columns split) and on one CTA per (b, h)."""
     sdm = need_gpu()
     monkeypatch.setenv("SDM_GDN_PATH", "chunk")
+    monkeypatch.setenv("SDM_GDN_CHAIN", chain)
     import torch
     sh = synth.GDN_DENSE.with_(B=2, T=T, H=2)
     inp = synth.gdn_inputs(sh, seed=40 + T)
@@ -75,14 +78,16 @@ def test_gdn_chunked_path_lengths(T, per_channel, monkeypatch):
     assert_state_close(host(state), Sr)
 
 
+@pytest.mark.parametrize("chain", ["pair", "single"])
 @pytest.mark.parametrize("scale", [1.0, 3.0, 6.0])
-def test_kda_chunked_strong_per_channel_decay(scale, monkeypatch):
+def test_kda_chunked_strong_per_channel_decay(scale, chain, monkeypatch):
     """KDA decays alpha = exp(-scale * softplus(N(0,1))) per key channel: at
     scale 6 the per-channel log decay over a 64-token chunk spans hundreds of
     units, so any factor formed as an inverse decay would overflow; every
     factor here is a decay ratio of at most 1."""
     sdm = need_gpu()
     monkeypatch.setenv("SDM_GDN_PATH", "chunk")
+    monkeypatch.setenv("SDM_GDN_CHAIN", chain)
     sh = synth.GDN_DENSE.with_(B=1, T=300, H=2)
     inp = synth.gdn_inputs(sh, seed=48)
     a = np.exp(np.log(inp["alpha_kda"].astype(np.float64)) * scale).astype(np.float32)
@@ -95,13 +100,15 @@ def test_kda_chunked_strong_per_channel_decay(scale, monkeypatch):
     assert_state_close(S, Sr)
 
 
+@pytest.mark.parametrize("chain", ["pair", "single"])
 @pytest.mark.parametrize("per_channel", [False, True], ids=["gdn", "kda"])
-def test_gdn_chunked_is_deterministic_and_continues_the_state(per_channel, monkeypatch):
+def test_gdn_chunked_is_deterministic_and_continues_the_state(per_channel, chain, monkeypatch):
     """The chunked path (T = 900: 15 chunks) gives the same bits on every
     call, and a sequence cut at a chunk boundary into two calls equals one
     call (the second call continues from the state the first left)."""
     sdm = need_gpu()
     monkeypatch.setenv("SDM_GDN_PATH", "chunk")
+    monkeypatch.setenv("SDM_GDN_CHAIN", chain)
     sh = synth.GDN_DENSE.with_(B=2, T=900, H=2)
     inp = synth.gdn_inputs(sh, seed=46)
     S0 = synth.random_state((2, 2, 128, 128), seed=47, scale=0.3)
@@ -225,13 +232,15 @@ def test_gdn2_full_size_sampled():
         assert_state_close(S[b:b + 1, h:h + 1], Sr, what=f"state[{b},{h}]")
 
 
+@pytest.mark.parametrize("chain", ["pair", "single"])
 @pytest.mark.parametrize("T", [1, 63, 64, 65, 200, 700])
-def test_gdn2_chunked_path_lengths(T, monkeypatch):
+def test_gdn2_chunked_path_lengths(T, chain, monkeypatch):
     """GDN2 at d_k = d_v = 128 runs in chunk form on the tensor cores (the KDA
     chunk form with erase rows e = b (.) k and Ut = (I + A)^-1 (w (.) v)):
-    lengths around chunk edges from a nonzero state."""
+    lengths around chunk edges from a nonzero state, on both chain forms."""
     sdm = need_gpu()
     monkeypatch.setenv("SDM_GDN_PATH", "chunk")
+    monkeypatch.setenv("SDM_GDN_CHAIN", chain)
     sh = synth.GDN_DENSE.with_(B=2, T=T, H=2)
     inp = synth.gdn_inputs(sh, seed=70 + T)
     S0 = synth.random_state((2, 2, 128, 128), seed=71, scale=0.3)

@@ -37,10 +37,12 @@ def _sse(sdm, S0, inp, topk, mode):
     return host(state), host(y), int(host(err)[0])
 
 
+@pytest.mark.parametrize("chain", ["pair", "single"])
 @pytest.mark.parametrize("per_channel", [False, True], ids=["gdn", "kda"])
-def test_gdn_chain_wait_runs_out_and_the_context_stays_usable(per_channel, monkeypatch):
+def test_gdn_chain_wait_runs_out_and_the_context_stays_usable(per_channel, chain, monkeypatch):
     sdm = need_gpu()
     monkeypatch.setenv("SDM_GDN_PATH", "chunk")
+    monkeypatch.setenv("SDM_GDN_CHAIN", chain)
     sh = synth.GDN_DENSE.with_(B=1, T=200, H=2)
     inp = synth.gdn_inputs(sh, seed=90)
     S0 = synth.random_state((1, 2, 128, 128), seed=91, scale=0.3)
