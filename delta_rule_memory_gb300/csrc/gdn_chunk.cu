@@ -1407,26 +1407,28 @@ __device__ __forceinline__ bool producer_wait(uint32_t mbar, uint32_t parity, vo
   return mbar_wait_spin(mbar, parity, kSpinWaitLimit, abort_flag);
 }
 
+// the chain of one (batch, head) (SSE: one (batch, head, partition)) on the
+// CTA `cta` of the launch
 template <int CM>
-__global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
+__device__ __forceinline__ void chain_single(const ChainArgs &a, long cta) {
   using L = ChainLayout<CM>;
   constexpr bool KDA = CM >= 1, SSE = CM == 2;
   extern __shared__ __align__(1024) unsigned char sm[];
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int T = a.T, H = a.H;
-  long bh = blockIdx.x, u0;
+  long bh = cta, u0;
   int n;
   float *gS;
   if (SSE) {
     // one (batch, head, partition), the shared partitions first (the longest
     // chains); its units are consecutive in the (batch, head)'s unit space
     int p;
-    if (static_cast<long>(blockIdx.x) < a.bhn) {
+    if (cta < a.bhn) {
       p = a.N;
     } else {
-      bh = (blockIdx.x - a.bhn) / a.N;
-      p = static_cast<int>((blockIdx.x - a.bhn) % a.N);
+      bh = (cta - a.bhn) / a.N;
+      p = static_cast<int>((cta - a.bhn) % a.N);
     }
     const uint32_t *g = a.grp + bh * a.gwords;
     int first = 0, count = (T + kC - 1) / kC;
@@ -1706,6 +1708,11 @@ __global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
   if (warp == 0) tmem_dealloc(tmem, kChainTmemCols);
 }
 
+template <int CM>
+__global__ void __maxnreg__(96) gdn_chain_kernel(const ChainArgs a) {
+  chain_single<CM>(a, blockIdx.x);
+}
+
 
 // ===========================================================================
 // Kernel 2, split by value columns: the chain of one (batch, head) on a pair
@@ -1734,17 +1741,19 @@ constexpr uint32_t kQColXY = 0;          // [X; Y1] [128 x 64], two buffers by c
 constexpr uint32_t kQColD = 128;         // D       [128 c x 64 d]
 constexpr uint32_t kQColY2 = 192;        // Y2      [128 x 64] (rows 64-127), two buffers
 constexpr uint32_t kQTmemCols = 512;
+// CM as the single form's: 0 GDN, 1 KDA / GDN2, 2 SSE delta (the KDA layout
+// plus each visit's staging row after gamma_C)
 template <int CM>
 struct PairLayout {
-  static constexpr bool KDA = CM == 1;
-  static constexpr uint32_t unit = KDA ? kVUnit : kUnit;
+  static constexpr bool KDA = CM >= 1;
+  static constexpr uint32_t unit = CM == 2 ? kSUnit : KDA ? kVUnit : kUnit;
   static constexpr uint32_t w_off = KDA ? kVW : kUW;
   static constexpr uint32_t w_bytes = KDA ? kVMq - kVW : kWBytes;    // 64 KB (KDA) or 48 KB (GDN)
   static constexpr uint32_t m_off = KDA ? kVMq : kUMq;               // Mq hi, Mq lo, Khat hi, Khat lo
   static constexpr uint32_t m_bytes = KDA ? kVG - kVMq : kMBytes;    // 48 KB
   static constexpr uint32_t g_off = KDA ? kVG : kUG;
-  static constexpr uint32_t g_bytes = KDA ? kVU - kVG : kGBytes;
-  static constexpr uint32_t u_off = KDA ? kVU : kUU;
+  static constexpr uint32_t g_bytes = CM == 2 ? kSU - kVG : KDA ? kVU - kVG : kGBytes;
+  static constexpr uint32_t u_off = CM == 2 ? kSU : KDA ? kVU : kUU;
   static constexpr uint32_t cbar = kQG + 2 * g_bytes;
   static constexpr uint32_t smem = cbar + kNBar * 8 + 16;
   static_assert(m_bytes == 49152 && w_bytes <= 65536, "unit regions");
@@ -1756,19 +1765,22 @@ __device__ __forceinline__ uint32_t mn64_off(int r, int d) {
   return static_cast<uint32_t>((r >> 3) * 1024 + (d >> 3) * 128 + (r & 7) * 16 + (d & 7) * 2);
 }
 
+// the chain of one (batch, head) on CTA `cta` of a pair (cta / 2 is the pair);
+// SSE delta: the chain of the (batch, head)'s shared partition, which every
+// token visits (its units are the first ceil(T / 64) of the (batch, head))
 template <int CM>
-__global__ void __maxnreg__(96) gdn_chain_pair_kernel(const ChainArgs a) {
+__device__ __forceinline__ void chain_pair(const ChainArgs &a, long cta) {
   using L = PairLayout<CM>;
-  constexpr bool KDA = CM == 1;
+  constexpr bool KDA = CM >= 1, SSE = CM == 2;
   extern __shared__ __align__(1024) unsigned char sm[];
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int T = a.T, H = a.H;
-  const long bh = blockIdx.x >> 1;
-  const int d0 = 64 * static_cast<int>(blockIdx.x & 1);  // this CTA's value columns
-  const int n = a.nchunks;
-  const long u0 = bh * n;
-  float *gS = a.state + bh * kDK * kDV;
+  const long bh = cta >> 1;
+  const int d0 = 64 * static_cast<int>(cta & 1);  // this CTA's value columns
+  const int n = SSE ? (T + kC - 1) / kC : a.nchunks;
+  const long u0 = SSE ? bh * a.umax : bh * n;
+  float *gS = a.state + (SSE ? bh * (a.N + 1) + a.N : bh) * static_cast<long>(kDK * kDV);
   const long tok0 = (bh / H) * T * H + bh % H;
 
   unsigned char *sSh = sm + kQS, *sSl = sm + kQS + 16384;
@@ -1877,6 +1889,8 @@ __global__ void __maxnreg__(96) gdn_chain_pair_kernel(const ChainArgs a) {
       // GDN's gamma_i of this thread's output token, read before the state is
       // published (the buffer is refilled two chunks on)
       const float gi = (!KDA && q >= 2) ? gbuf[row - 64] : 1.f;
+      // SSE: the staging row of this thread's visit (-1 for padding)
+      const int sr = (SSE && q >= 2) ? reinterpret_cast<const int *>(gbuf + kDK)[row - 64] : -1;
       // S <- gamma_C S + D; D completing also means phase 1 no longer reads S
       if (!wwait(bar(7), par)) break;
       {
@@ -1902,8 +1916,9 @@ __global__ void __maxnreg__(96) gdn_chain_pair_kernel(const ChainArgs a) {
         tmem_ld16(lanes + kQColY2 + 64 * (c & 1) + dc, y2);
         tmem_ld_wait();
         const int t = c * kC + row - 64;
-        if (t < T) {
-          float4 *yp = reinterpret_cast<float4 *>(a.y + (tok0 + static_cast<long>(t) * H) * kDV + d0 + dc);
+        if (SSE ? sr >= 0 : t < T) {
+          float4 *yp = reinterpret_cast<float4 *>(
+              SSE ? a.stage + static_cast<long>(sr) * kDV + d0 + dc : a.y + (tok0 + static_cast<long>(t) * H) * kDV + d0 + dc);
 #pragma unroll
           for (int e4 = 0; e4 < 4; ++e4) {
             float o[4];
@@ -2029,6 +2044,21 @@ __global__ void __maxnreg__(96) gdn_chain_pair_kernel(const ChainArgs a) {
   __syncthreads();
   if (tid == 0 && *abort_flag) report_timeout(a.err);
   if (warp == 0) tmem_dealloc(tmem, kQTmemCols);
+}
+
+template <int CM>
+__global__ void __maxnreg__(96) gdn_chain_pair_kernel(const ChainArgs a) {
+  chain_pair<CM>(a, blockIdx.x);
+}
+
+// SSE delta write: the shared partitions' chains (the longest: every token
+// visits them) on CTA pairs, first, then the routed partitions' chains on one
+// CTA each, in one launch
+__global__ void __maxnreg__(96) gdn_chain_sse_kernel(const ChainArgs a) {
+  if (static_cast<long>(blockIdx.x) < 2 * a.bhn)
+    chain_pair<2>(a, blockIdx.x);
+  else
+    chain_single<2>(a, static_cast<long>(blockIdx.x) - a.bhn);
 }
 
 }  // namespace
@@ -2247,6 +2277,15 @@ int launch_sse_delta_chunk(float *state, const uint32_t *rec, int rw, const uint
   ca.stage = stage;
   ca.err = err;
   ca.drop_signal = test_drop_signal();
+  if (chain_in_pairs(bhn, sms)) {
+    constexpr uint32_t sse_smem =
+        PairLayout<2>::smem > ChainLayout<2>::smem ? PairLayout<2>::smem : ChainLayout<2>::smem;
+    if (cudaFuncSetAttribute(gdn_chain_sse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sse_smem)) != cudaSuccess)
+      return check_launch("sse_scan: set shared memory");
+    gdn_chain_sse_kernel<<<static_cast<unsigned>(bhn * (N + 2)), kChainThreads, sse_smem, st>>>(ca);
+    return check_launch("sse_scan: delta chunk chain kernel");
+  }
   constexpr uint32_t chain_smem = ChainLayout<2>::smem;
   if (cudaFuncSetAttribute(gdn_chain_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(chain_smem)) != cudaSuccess)

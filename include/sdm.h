@@ -470,7 +470,9 @@ SDM_API size_t sse_scan_workspace_size(int B, int T, int H, int N, int topk, int
  * so results are deterministic.  The additive write takes the chunkwise GLA
  * form; the delta write is the gated delta rule with a decay per key row, so
  * it takes the chunk form of the per-channel-decay (KDA) scan with keys kk,
- * write strength g and every read scaled by g.  Everything else runs token
+ * write strength g and every read scaled by g (the shared partitions'
+ * chains, the longest, on CTA pairs as gdn_scan's; SDM_GDN_CHAIN=single puts
+ * every chain on one CTA).  Everything else runs token
  * by token with the partitions resident in shared memory.  The
  * environment variable SDM_SSE_PATH=recurrent forces the token-by-token
  * kernel; SDM_SSE_PATH=chunk the chunked path for any T (same shape rules).

@@ -58,10 +58,12 @@ def test_gdn_chain_wait_runs_out_and_the_context_stays_usable(per_channel, chain
     assert_state_close(S, Sr)
 
 
-@pytest.mark.parametrize("mode", [oracle.SSE_WRITE_ADDITIVE, oracle.SSE_WRITE_DELTA], ids=["additive", "delta"])
-def test_sse_chain_wait_runs_out_and_the_context_stays_usable(mode, monkeypatch):
+@pytest.mark.parametrize("mode,chain", [(oracle.SSE_WRITE_ADDITIVE, "pair"), (oracle.SSE_WRITE_DELTA, "pair"),
+                                        (oracle.SSE_WRITE_DELTA, "single")], ids=["additive", "delta", "delta-single"])
+def test_sse_chain_wait_runs_out_and_the_context_stays_usable(mode, chain, monkeypatch):
     sdm = need_gpu()
     monkeypatch.setenv("SDM_SSE_PATH", "chunk")
+    monkeypatch.setenv("SDM_GDN_CHAIN", chain)
     sh = synth.SSE_PART.with_(B=1, T=200, H=2)
     inp = synth.sse_inputs(sh, seed=92)
     S0 = synth.random_state((1, 2, sh.N + 1, 128, 128), seed=93, scale=0.5)

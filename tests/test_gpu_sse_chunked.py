@@ -67,6 +67,21 @@ def test_chunked_sse_matches_the_oracle(B, T, H, N, topk, mode, monkeypatch):
     _check(sdm, S0, inp, topk, mode)
 
 
+@pytest.mark.parametrize("chain", ["pair", "single"])
+@pytest.mark.parametrize("B,T,H,N,topk", [(2, 200, 2, 8, 2), (1, 64, 2, 5, 3), (1, 160, 1, 64, 8)])
+def test_chunked_sse_delta_on_both_chain_forms(B, T, H, N, topk, chain, monkeypatch):
+    """The delta write's chains: the shared partitions on CTA pairs (value
+    columns split) beside the routed partitions on one CTA each, in one
+    launch, and every chain on one CTA."""
+    monkeypatch.setenv("SDM_SSE_PATH", "chunk")
+    monkeypatch.setenv("SDM_GDN_CHAIN", chain)
+    sdm = need_gpu()
+    sh = synth.SSE_PART.with_(B=B, T=T, H=H, N=N, topk=topk)
+    inp = synth.sse_inputs(sh, seed=3 * T + N)
+    S0 = synth.random_state((B, H, N + 1, 128, 128), seed=N + 1, scale=0.5)
+    _check(sdm, S0, inp, topk, oracle.SSE_WRITE_DELTA)
+
+
 @pytest.mark.parametrize("T", [1, 5, 63, 65])
 @WRITES
 def test_chunked_sse_short_sequences(T, mode, monkeypatch):
