@@ -569,14 +569,18 @@ __global__ void __launch_bounds__(kPThreads, 2) sse_prep_kernel(const PrepArgs a
 // Warps 0-15 (workers): warp w owns tensor-memory lanes 32*(w%4) .. +31
 // (value columns d) and quarter w/4 of the rows r (S) and of the unit's
 // visits (O).  Warp 16 (producer, one lane) issues the bulk copies and the
-// MMAs.  Per unit c (buffers b = c % 2 for A/V/Kh, gamma/rows, D and O):
-//   producer  D[b] = V^T Kh and O[b]^T = V^T A^T (state-independent; issued
-//             as soon as unit c's tiles are in and unit c-2's D/O were read),
-//             then, once the workers have published S0: O[b]^T += S0^T Qt^T;
-//             then the copies of unit c+1
-//   workers   S^T <- gamma S^T + D[b], published as bf16 hi/lo for unit c+1;
-//             O[b]^T staged per visit
-// so unit c+1's state-independent MMAs run while the workers fold unit c.
+// MMAs.  Per unit c (buffers b = c % 2 for Qt, gamma/rows, D and O; one
+// buffer for A/V/Kh):
+//   producer  D[b] = V^T Kh and O[b]^T = V^T A^T (state-independent), then,
+//             once the workers have published S0: O[b]^T += S0^T Qt^T; then
+//             the copies: A/V/Kh of unit c+1 as soon as D[b] and V^T A^T are
+//             done, Qt of unit c+2 once this unit's MMAs are
+//   workers   S^T <- gamma S^T + D[b] as soon as D[b] is done, published as
+//             bf16 hi/lo for unit c+1 once this unit's MMAs no longer read
+//             S0; O[b]^T staged per visit
+// Qt is double-buffered so that the next unit's copy is long done when its
+// state-dependent MMAs can start: the per-unit cycle is the tensor pipe's
+// work plus the state's publish, not a copy's latency.
 // ===========================================================================
 struct ChainArgs {
   float *state;
@@ -595,11 +599,11 @@ constexpr int kChainThreads = kWorkers + 32;
 constexpr uint32_t kColD = 0, kColO = 256, kChainTmemCols = 512;
 // shared memory (bytes)
 constexpr uint32_t kSS = 0;                      // S^T hi, lo [128 d][128 r]   2 x 32 KB
-constexpr uint32_t kSX = 65536;                  // Qt hi, lo                   32 KB
-constexpr uint32_t kSY = kSX + kXQBytes;         // A hi, lo, V, Kh hi, lo      2 x 64 KB
-constexpr uint32_t kSZ = kSY + 2 * kXYBytes;     // gamma + rows                2 x 768 B
+constexpr uint32_t kSX = 65536;                  // Qt hi, lo                   2 x 32 KB (two units)
+constexpr uint32_t kSY = kSX + 2 * kXQBytes;     // A hi, lo, V, Kh hi, lo      64 KB
+constexpr uint32_t kSZ = kSY + kXYBytes;         // gamma + rows                2 x 768 B
 constexpr uint32_t kSBar = kSZ + 2 * kXZBytes;
-constexpr int kNBar = 10;
+constexpr int kNBar = 13;
 constexpr uint32_t kChainSmem = kSBar + kNBar * 8 + 16;
 static_assert(kChainSmem <= 227 * 1024, "chain shared memory");
 
@@ -626,9 +630,11 @@ __global__ void __maxnreg__(96) sse_chain_kernel(const ChainArgs a) {
 
   unsigned char *sSh = sm + kSS, *sSl = sm + kSS + 32768;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kSBar);
-  // barriers: 0 Qt loaded, 1-2 A/V/Kh loaded [b], 3-4 gamma/rows loaded [b], 5 MMAs of the unit done,
-  // 6 S published (workers), 7-8 D[b] and O[b] read (workers), 9 drain
-  enum { kBarX = 0, kBarY = 1, kBarZ = 3, kBarMma = 5, kBarS = 6, kBarFree = 7, kBarDrain = 9 };
+  // barriers: 0-1 Qt loaded [b], 2 A/V/Kh loaded, 3-4 gamma/rows loaded [b], 5 MMAs of the unit done,
+  // 6 S published (workers), 7-8 D[b] and O[b] read (workers), 9 drain, 10-11 D[b] done,
+  // 12 A/V/Kh read (D and V^T A^T done)
+  enum { kBarX = 0, kBarY = 2, kBarZ = 3, kBarMma = 5, kBarS = 6, kBarFree = 7, kBarDrain = 9, kBarD = 10,
+         kBarYFree = 12 };
   auto bar = [&](int i) { return smem_addr(bars + i); };
   uint32_t *holder = reinterpret_cast<uint32_t *>(sm + kSBar + kNBar * 8);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + kSBar + kNBar * 8 + 4);
@@ -666,8 +672,8 @@ __global__ void __maxnreg__(96) sse_chain_kernel(const ChainArgs a) {
     for (int c = 0; c < n; ++c) {
       const int b = c & 1;
       const bool last = c + 1 == n;
-      if (!wwait(bar(kBarMma), static_cast<uint32_t>(c & 1))) break;
       if (!wwait(bar(kBarZ + b), static_cast<uint32_t>((c >> 1) & 1))) break;
+      if (!wwait(bar(kBarD + b), static_cast<uint32_t>((c >> 1) & 1))) break;
       const unsigned char *z = sm + kSZ + b * kXZBytes;
       const float *gam = reinterpret_cast<const float *>(z) + 32 * qtr;
 #pragma unroll
@@ -678,6 +684,8 @@ __global__ void __maxnreg__(96) sse_chain_kernel(const ChainArgs a) {
 #pragma unroll
         for (int e = 0; e < 16; ++e) S[16 * hh + e] = fmaf(gam[16 * hh + e], S[16 * hh + e], x[e]);
       }
+      // the unit's MMAs done: the published S0 is no longer read and O[b] is complete
+      if (!wwait(bar(kBarMma), static_cast<uint32_t>(c & 1))) break;
       if (!last) publish();
       {
         const int *rows = reinterpret_cast<const int *>(z + (kXR - kXG)) + 16 * qtr;
@@ -702,25 +710,27 @@ __global__ void __maxnreg__(96) sse_chain_kernel(const ChainArgs a) {
     const uint32_t sh = smem_addr(sSh), sl = smem_addr(sSl);
     const uint32_t xq = smem_addr(sm + kSX);
     const uint64_t dSh = smem_desc(sh, 128, kCh * 16), dSl = smem_desc(sl, 128, kCh * 16);
-    const uint64_t dQh = smem_desc(xq, 128, kCh * 16), dQl = smem_desc(xq + 16384, 128, kCh * 16);
     const uint32_t idO = idesc_bf16_f32(128, kC), idOv = idO | (1u << 15);
     const uint32_t idD = idesc_bf16_f32(128, kCh) | (1u << 15) | (1u << 16);
-    int x_issued = 0, x_done = 0, y_issued[2] = {0, 0}, y_done[2] = {0, 0}, z_issued[2] = {0, 0};
-    auto load_x = [&](int c) {
-      fence_async_smem();
-      mbar_expect_tx(bar(kBarX), kXQBytes);
-      bulk_g2s(xq, ub + static_cast<long>(c) * kXUnit + kXQ, kXQBytes, bar(kBarX));
-      ++x_issued;
-    };
-    auto load_yz = [&](int c) {
-      const unsigned char *src = ub + static_cast<long>(c) * kXUnit;
+    int x_issued[2] = {0, 0}, x_done[2] = {0, 0}, y_issued = 0, y_done = 0, z_issued[2] = {0, 0};
+    auto load_x = [&](int c) {  // Qt of unit c into buffer c % 2
       const int b = c & 1;
       fence_async_smem();
-      mbar_expect_tx(bar(kBarY + b), kXYBytes);
-      bulk_g2s(smem_addr(sm + kSY + b * kXYBytes), src + kXA, kXYBytes, bar(kBarY + b));
-      ++y_issued[b];
+      mbar_expect_tx(bar(kBarX + b), kXQBytes);
+      bulk_g2s(xq + b * kXQBytes, ub + static_cast<long>(c) * kXUnit + kXQ, kXQBytes, bar(kBarX + b));
+      ++x_issued[b];
+    };
+    auto load_y = [&](int c) {  // A, V, Kh of unit c
+      fence_async_smem();
+      mbar_expect_tx(bar(kBarY), kXYBytes);
+      bulk_g2s(smem_addr(sm + kSY), ub + static_cast<long>(c) * kXUnit + kXA, kXYBytes, bar(kBarY));
+      ++y_issued;
+    };
+    auto load_z = [&](int c) {  // gamma and rows of unit c into buffer c % 2
+      const int b = c & 1;
+      fence_async_smem();
       mbar_expect_tx(bar(kBarZ + b), kXZBytes);
-      bulk_g2s(smem_addr(sm + kSZ + b * kXZBytes), src + kXG, kXZBytes, bar(kBarZ + b));
+      bulk_g2s(smem_addr(sm + kSZ + b * kXZBytes), ub + static_cast<long>(c) * kXUnit + kXG, kXZBytes, bar(kBarZ + b));
       ++z_issued[b];
     };
     auto prefetch = [&](int c) {
@@ -732,40 +742,46 @@ __global__ void __maxnreg__(96) sse_chain_kernel(const ChainArgs a) {
     auto wait = [&](int i, uint32_t parity) { return mbar_wait_spin(bar(i), parity, kSpinWaitLimit, abort_flag); };
     if (n > 1) prefetch(1);
     load_x(0);
-    load_yz(0);
+    if (n > 1) load_x(1);
+    load_y(0);
+    load_z(0);
+    const uint32_t ya = smem_addr(sm + kSY);
+    const uint32_t yv = ya + (kXV - kXA), yk = ya + (kXK - kXA);
+    const uint64_t dAh = smem_desc(ya, 128, kC * 16), dAl = smem_desc(ya + 8192, 128, kC * 16);
+    // V^T (A operand) and Kh (B operand) are MN-major: 8 consecutive d (or
+    // r) per 16 bytes, 8-visit groups 2048 bytes apart; a k-step of 16
+    // visits is 4096 bytes (256 in the descriptor)
+    const uint64_t dV = smem_desc(yv, 2048, 128);
+    const uint64_t dKh = smem_desc(yk, 2048, 128), dKl = smem_desc(yk + 16384, 2048, 128);
     bool ok = true;
     for (int c = 0; c < n && ok; ++c) {
       const int b = c & 1;
       if (c + 2 < n) prefetch(c + 2);
       // state-independent MMAs of unit c
-      ok = wait(kBarY + b, static_cast<uint32_t>((c >> 1) & 1));
-      if (ok) ++y_done[b];
+      ok = wait(kBarY, static_cast<uint32_t>(c & 1));
+      if (ok) ++y_done;
       if (ok && c >= 2) ok = wait(kBarFree + b, static_cast<uint32_t>(((c - 2) >> 1) & 1));  // D[b], O[b] read
       if (!ok) break;
-      const uint32_t ya = smem_addr(sm + kSY + b * kXYBytes);
-      const uint32_t yv = ya + (kXV - kXA), yk = ya + (kXK - kXA);
-      const uint64_t dAh = smem_desc(ya, 128, kC * 16), dAl = smem_desc(ya + 8192, 128, kC * 16);
-      // V^T (A operand) and Kh (B operand) are MN-major: 8 consecutive d (or
-      // r) per 16 bytes, 8-visit groups 2048 bytes apart; a k-step of 16
-      // visits is 4096 bytes (256 in the descriptor)
-      const uint64_t dV = smem_desc(yv, 2048, 128);
-      const uint64_t dKh = smem_desc(yk, 2048, 128), dKl = smem_desc(yk + 16384, 2048, 128);
       const uint32_t tD = tmem + kColD + 128 * b, tO = tmem + kColO + 64 * b;
 #pragma unroll
       for (int ks = 0; ks < kC / 16; ++ks) {
         mma_bf16(tD, dV + 256u * ks, dKh + 256u * ks, idD, ks > 0);
         mma_bf16(tD, dV + 256u * ks, dKl + 256u * ks, idD, true);
       }
+      mma_commit(bar(kBarD + b));
 #pragma unroll
       for (int ks = 0; ks < kC / 16; ++ks) {
         mma_bf16(tO, dV + 256u * ks, dAh + 16u * ks, idOv, ks > 0);
         mma_bf16(tO, dV + 256u * ks, dAl + 16u * ks, idOv, true);
       }
+      mma_commit(bar(kBarYFree));
       // the state-dependent part
-      ok = wait(kBarX, static_cast<uint32_t>(c & 1));
-      if (ok) ++x_done;
+      ok = wait(kBarX + b, static_cast<uint32_t>((c >> 1) & 1));
+      if (ok) ++x_done[b];
       if (ok) ok = wait(kBarS, static_cast<uint32_t>(c & 1));  // S0 of unit c published
       if (!ok) break;
+      const uint32_t xb = xq + b * kXQBytes;
+      const uint64_t dQh = smem_desc(xb, 128, kCh * 16), dQl = smem_desc(xb + 16384, 128, kCh * 16);
 #pragma unroll
       for (int ks = 0; ks < kCh / 16; ++ks) {
         mma_bf16(tO, dSh + 16u * ks, dQh + 16u * ks, idO, true);
@@ -774,12 +790,17 @@ __global__ void __maxnreg__(96) sse_chain_kernel(const ChainArgs a) {
       }
       if (!(a.drop_signal && c == 0)) mma_commit(bar(kBarMma));
       if (c + 1 < n) {
-        // unit c+1's tiles into the other buffers once the workers are done with unit c-1
-        if (c >= 1) ok = wait(kBarFree + (b ^ 1), static_cast<uint32_t>(((c - 1) >> 1) & 1));
-        if (ok) load_yz(c + 1);
-        // its Qt once this unit's MMAs have read theirs
-        if (ok) ok = wait(kBarMma, static_cast<uint32_t>(c & 1));
-        if (ok) load_x(c + 1);
+        // unit c+1's A/V/Kh once unit c's state-independent MMAs have read
+        // theirs; its gamma/rows once the workers are done with unit c-1's
+        ok = wait(kBarYFree, static_cast<uint32_t>(c & 1));
+        if (ok) load_y(c + 1);
+        if (ok && c >= 1) ok = wait(kBarFree + (b ^ 1), static_cast<uint32_t>(((c - 1) >> 1) & 1));
+        if (ok) load_z(c + 1);
+        // unit c+2's Qt into this buffer once this unit's MMAs have read it
+        if (ok && c + 2 < n) {
+          ok = wait(kBarMma, static_cast<uint32_t>(c & 1));
+          if (ok) load_x(c + 2);
+        }
       }
     }
     // every MMA issued has completed before tensor memory is freed (also when
@@ -788,10 +809,10 @@ __global__ void __maxnreg__(96) sse_chain_kernel(const ChainArgs a) {
     mbar_wait(bar(kBarDrain), 0, kWaitLimit);
     // and every bulk copy has landed before the CTA exits (bounded waits; in
     // the normal path they have all been seen complete already)
-    if (x_done < x_issued) mbar_wait(bar(kBarX), static_cast<uint32_t>((x_issued - 1) & 1), kWaitLimit);
+    if (y_done < y_issued) mbar_wait(bar(kBarY), static_cast<uint32_t>((y_issued - 1) & 1), kWaitLimit);
     for (int bb = 0; bb < 2; ++bb) {
-      if (y_done[bb] < y_issued[bb])
-        mbar_wait(bar(kBarY + bb), static_cast<uint32_t>((y_issued[bb] - 1) & 1), kWaitLimit);
+      if (x_done[bb] < x_issued[bb])
+        mbar_wait(bar(kBarX + bb), static_cast<uint32_t>((x_issued[bb] - 1) & 1), kWaitLimit);
       if (z_issued[bb] > 0) mbar_wait(bar(kBarZ + bb), static_cast<uint32_t>((z_issued[bb] - 1) & 1), kWaitLimit);
     }
     if (!ok) *abort_flag = 1;
