@@ -78,6 +78,24 @@ def test_gdn_chunked_path_lengths(T, per_channel, chain, monkeypatch):
     assert_state_close(host(state), Sr)
 
 
+@pytest.mark.parametrize("per_channel", [False, True], ids=["gdn", "kda"])
+def test_gdn_chunked_many_heads_default_chain_form(per_channel, monkeypatch):
+    """B*H = 96 chains: more CTA pairs than a GB300 holds at once, so the
+    default form there is one CTA per (b, h); whichever form the device
+    size selects must match the oracle."""
+    sdm = need_gpu()
+    monkeypatch.setenv("SDM_GDN_PATH", "chunk")
+    monkeypatch.delenv("SDM_GDN_CHAIN", raising=False)
+    sh = synth.GDN_DENSE.with_(B=6, T=130, H=16)
+    inp = synth.gdn_inputs(sh, seed=52)
+    S0 = synth.random_state((6, 16, 128, 128), seed=53, scale=0.3)
+    a = inp["alpha_kda"] if per_channel else inp["alpha_gdn"]
+    Sr, yr = oracle.gdn_scan(S0, inp["q"], inp["k"], inp["v"], a, inp["beta"], per_channel)
+    S, y = _gdn_gpu(sdm, S0, inp, per_channel)
+    assert_y_close(y, yr)
+    assert_state_close(S, Sr)
+
+
 @pytest.mark.parametrize("chain", ["pair", "single"])
 @pytest.mark.parametrize("scale", [1.0, 3.0, 6.0])
 def test_kda_chunked_strong_per_channel_decay(scale, chain, monkeypatch):

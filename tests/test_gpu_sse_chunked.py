@@ -82,6 +82,19 @@ def test_chunked_sse_delta_on_both_chain_forms(B, T, H, N, topk, chain, monkeypa
     _check(sdm, S0, inp, topk, oracle.SSE_WRITE_DELTA)
 
 
+def test_chunked_sse_delta_many_heads_default_chain_form(monkeypatch):
+    """B*H = 96: more shared-partition CTA pairs than a GB300 holds at once,
+    so the default there puts every chain on one CTA; the result must match
+    the oracle whichever form the device size selects."""
+    monkeypatch.setenv("SDM_SSE_PATH", "chunk")
+    monkeypatch.delenv("SDM_GDN_CHAIN", raising=False)
+    sdm = need_gpu()
+    sh = synth.SSE_PART.with_(B=6, T=100, H=16, N=4, topk=2)
+    inp = synth.sse_inputs(sh, seed=77)
+    S0 = synth.random_state((6, 16, 5, 128, 128), seed=78, scale=0.5)
+    _check(sdm, S0, inp, 2, oracle.SSE_WRITE_DELTA)
+
+
 @pytest.mark.parametrize("T", [1, 5, 63, 65])
 @WRITES
 def test_chunked_sse_short_sequences(T, mode, monkeypatch):
