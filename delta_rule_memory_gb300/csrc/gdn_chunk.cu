@@ -1289,9 +1289,14 @@ __global__ void __launch_bounds__(kKThreads, 1) kda_prep_kernel(const KdaPrepArg
       }
       mma_commit(mbW);
     }
-    // K, alpha, beta and lambda are free: the next unit's, while the products run
+    // K, alpha, beta and lambda are free: the next unit's, while the products
+    // run; GDN2's V too (its Ut takes z = w (.) v, built before the products)
     if (has_next) load_kal(un, buf ^ 1);
+    if (has_next && G2) load_v(un);
     if (!wait_ok(mbW, static_cast<uint32_t>(it & 1))) { failed = true; break; }
+    // KDA's V tile is free once the products that read it are done: the next
+    // unit's, so it lands under the stores below
+    if (has_next && !SSE && !G2) load_v(un);
     if (SSE && tid < kC) reinterpret_cast<int *>(ws + kSRows)[tid] = rrow[tid];
     {
       float *gU = reinterpret_cast<float *>(ws + (SSE ? kSU : kVU));
@@ -1309,8 +1314,6 @@ __global__ void __launch_bounds__(kKThreads, 1) kda_prep_kernel(const KdaPrepArg
         store_split8(ws + kVW, ws + kVWl, off + 2048, x + 8);
       }
     }
-    // the V tile is free: the next unit's
-    if (has_next && !SSE) load_v(un);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
