@@ -703,11 +703,13 @@ __global__ void __launch_bounds__(kKThreads, 1) kda_prep_kernel(const KdaPrepArg
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + kKBar);
   uint32_t *holder = reinterpret_cast<uint32_t *>(sm + kKBar + 32);
   const uint32_t mbG = smem_addr(bars + 0), mbW = smem_addr(bars + 1), mbEnd = smem_addr(bars + 2);
+  const uint32_t mbU = smem_addr(bars + 3);  // Ut^T = V^T T^T done (V free), KDA and SSE
 
   if (tid == 0) {
     mbar_init(mbG, 1);
     mbar_init(mbW, 1);
     mbar_init(mbEnd, 1);
+    mbar_init(mbU, 1);
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(smem_addr(holder), kKdaTmemCols);
@@ -1271,8 +1273,17 @@ __global__ void __launch_bounds__(kKThreads, 1) kda_prep_kernel(const KdaPrepArg
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // ---- W^T = Kt^T T^T (three passes) and Ut^T = V^T T^T (V is exact: two)
+    // ---- Ut^T = V^T T^T (V is exact: two passes; KDA and SSE: first, on its
+    // own commit, so the V tile frees early) and W^T = Kt^T T^T (three)
     if (tid == 0) {
+      if (!G2) {
+#pragma unroll
+        for (int ks = 0; ks < kC / 16; ++ks) {
+          mma_bf16(tmem + kKColU, dVmn + 256u * ks, dTh + 16u * ks, idMN, ks > 0);
+          mma_bf16(tmem + kKColU, dVmn + 256u * ks, dTl + 16u * ks, idMN, true);
+        }
+        mma_commit(mbU);
+      }
 #pragma unroll
       for (int ks = 0; ks < kC / 16; ++ks) {
         mma_bf16(tmem + kKColW, dKtmn_h + 256u * ks, dTh + 16u * ks, idMN, ks > 0);
@@ -1282,21 +1293,20 @@ __global__ void __launch_bounds__(kKThreads, 1) kda_prep_kernel(const KdaPrepArg
           mma_bf16(tmem + kKColU, dZmn_h + 256u * ks, dTh + 16u * ks, idMN, ks > 0);
           mma_bf16(tmem + kKColU, dZmn_h + 256u * ks, dTl + 16u * ks, idMN, true);
           mma_bf16(tmem + kKColU, dZmn_l + 256u * ks, dTh + 16u * ks, idMN, true);
-        } else {
-          mma_bf16(tmem + kKColU, dVmn + 256u * ks, dTh + 16u * ks, idMN, ks > 0);
-          mma_bf16(tmem + kKColU, dVmn + 256u * ks, dTl + 16u * ks, idMN, true);
         }
       }
       mma_commit(mbW);
     }
     // K, alpha, beta and lambda are free: the next unit's, while the products
-    // run; GDN2's V too (its Ut takes z = w (.) v, built before the products)
+    // run; V too as soon as no product reads it (GDN2's Ut takes z = w (.) v,
+    // built before the products; KDA's reads V and completes first)
     if (has_next) load_kal(un, buf ^ 1);
     if (has_next && G2) load_v(un);
+    if (has_next && !SSE && !G2) {
+      if (!wait_ok(mbU, static_cast<uint32_t>(it & 1))) { failed = true; break; }
+      load_v(un);
+    }
     if (!wait_ok(mbW, static_cast<uint32_t>(it & 1))) { failed = true; break; }
-    // KDA's V tile is free once the products that read it are done: the next
-    // unit's, so it lands under the stores below
-    if (has_next && !SSE && !G2) load_v(un);
     if (SSE && tid < kC) reinterpret_cast<int *>(ws + kSRows)[tid] = rrow[tid];
     {
       float *gU = reinterpret_cast<float *>(ws + (SSE ? kSU : kVU));
