@@ -44,16 +44,16 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 NCU_TRAFFIC = {
     # one full-size sparse scan launch: 8.01 GB read + 4.19 GB written
     ("sdm_14b_layer", "sdm"): {"bytes": 12.20e9, "digest": "8821957384b6"},
-    # both kernels of one full-size gdn_scan call: 746.1 MB read + 591.6 MB written
-    ("gdn", "gdn"): {"bytes": 1.338e9, "digest": "212ce400a39e"},
-    # both kernels of one full-size KDA gdn_scan call: 947.2 MB read + 663.7 MB written
-    ("kda", "kda"): {"bytes": 1.611e9, "digest": "212ce400a39e"},
-    # both kernels of one full-size gdn2_scan call: 1214.5 MB read + 674.3 MB written
-    ("gdn2", "gdn2"): {"bytes": 1.889e9, "digest": "212ce400a39e"},
-    # the five kernels of one full-size sse_scan call on the chunked path: 1.063 GB read + 0.808 GB written
-    ("sse", "sse"): {"bytes": 1.871e9, "digest": "106dd028442b"},
-    # the five kernels of one full-size delta-write sse_scan call: 1.385 GB read + 1.110 GB written
-    ("sse_delta", "sse"): {"bytes": 2.495e9, "digest": "212ce400a39e"},
+    # both kernels of one full-size gdn_scan call: 746.1 MB read + 591.0 MB written
+    ("gdn", "gdn"): {"bytes": 1.337e9, "digest": "c77c8abaf750"},
+    # both kernels of one full-size KDA gdn_scan call: 947.1 MB read + 663.2 MB written
+    ("kda", "kda"): {"bytes": 1.610e9, "digest": "c77c8abaf750"},
+    # both kernels of one full-size gdn2_scan call: 1214.6 MB read + 673.5 MB written
+    ("gdn2", "gdn2"): {"bytes": 1.888e9, "digest": "c77c8abaf750"},
+    # the five kernels of one full-size sse_scan call on the chunked path: 1.063 GB read + 0.807 GB written
+    ("sse", "sse"): {"bytes": 1.869e9, "digest": "106dd028442b"},
+    # the five kernels of one full-size delta-write sse_scan call: 1.387 GB read + 1.110 GB written
+    ("sse_delta", "sse"): {"bytes": 2.497e9, "digest": "c77c8abaf750"},
 }
 
 
