@@ -284,18 +284,20 @@ __global__ void __launch_bounds__(128) sparse_backward_kernel16(const BackArgs a
       pt[R + W] = dalpha;
       pt[R + W + 1] = dbeta;
     }
-    // stores: read rows, then written rows (gradient and the undone table row)
+    // stores: read rows, then written rows (gradient and the undone table row),
+    // with the streaming hint (evict first) so that L2 stays with the gathers
+    // of the tokens still to come (measured: training step 19.77 -> 19.54 ms)
 #pragma unroll
     for (int i = 0; i < S; ++i) {
       const int ri = __shfl_sync(kFull, my_id, i);
-      if (active && static_cast<unsigned>(ri) < static_cast<unsigned>(N)) G[static_cast<long>(ri) * d_v] = Gr[i];
+      if (active && static_cast<unsigned>(ri) < static_cast<unsigned>(N)) __stcs(&G[static_cast<long>(ri) * d_v], Gr[i]);
     }
 #pragma unroll
     for (int j = 0; j < S; ++j) {
       const int wi = __shfl_sync(kFull, my_id, 16 + j);
       if (active && static_cast<unsigned>(wi) < static_cast<unsigned>(N)) {
-        G[static_cast<long>(wi) * d_v] = Gw[j];
-        M[static_cast<long>(wi) * d_v] = U[j];
+        __stcs(&G[static_cast<long>(wi) * d_v], Gw[j]);
+        __stcs(&M[static_cast<long>(wi) * d_v], U[j]);
       }
     }
     if (t >= 1) {
